@@ -1,0 +1,195 @@
+/*
+ * repro.h -- C ABI of the bitwise-reproducible int8 quantisation-aware linear
+ * layer (forward and backward) and of the fixed-order gradient reduction that
+ * follows it, for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages about the preprint "OPEN-1B: A Fully Auditable Training
+ * Run", Gensyn):
+ *   [abstract]  arxivdaily.com/papers/2609.17380, English abstract: a definite
+ *               order is imposed on GPU kernel reductions, batch ordering and
+ *               collectives so any step replays bit for bit on one device.
+ *   [works]     Open-1B review, onedev.kr/papers/92, section "How it works"
+ *               (어떻게 동작하나): fixed reduction order on every backend,
+ *               explicit unfused multiply-add, subnormals flushed to zero.
+ *   [use]       same page, section "How to use" (어떻게 쓰나): every attention
+ *               and feed-forward linear is int8 QAT (LSQ-based) with 8-bit
+ *               weights and activations; the weight scale is re-pinned every
+ *               optimiser step to 2*mean(|w|)/sqrt(q_max).
+ *   [limits]    same page, section "Premises and limits" (전제와 한계): the
+ *               audit replays a three-level reduction on one device --
+ *               micro-batch accumulation, intra-node reduce-scatter, and the
+ *               replica all-reduce as a TreeFold in recursive-doubling pairing
+ *               order; stochastic rounding is rejected.
+ *
+ * Numerics, for every call (the library's fixing of what the pages leave open):
+ *   - binary32, round-to-nearest-even, never a fused multiply-add;
+ *   - subnormal operands are read as signed zero, subnormal results (after
+ *     IEEE rounding) are written as signed zero;
+ *   - "canonical sum" of L terms: chunks of 64 consecutive terms summed left
+ *     to right seeded with the chunk's first term, then the chunk partials
+ *     combined by the stride-doubling pairwise tree (t_j += t_{j+s}, j a
+ *     multiple of 2s, j+s < C, s = 1, 2, 4, ...).  L = 0 gives +0.
+ *   - q_max = 127; int8 codes lie in [-127, 127].
+ * Results are bit-identical across runs, streams and launch configurations.
+ *
+ * Conventions:
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; tensors are
+ *     dense row-major.  Scales are single floats in DEVICE memory, so a whole
+ *     step can run without host synchronisation.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call only enqueues work on it and returns; nothing is synchronous
+ *     except repro_device_check().
+ *   - Errors are returned as negative repro_status codes; nothing is launched
+ *     when the arguments are invalid.  Device pointers must be 16-byte aligned.
+ *   - The library allocates no device memory: calls that need scratch space
+ *     take a caller-provided workspace and report its size through *_ws_bytes.
+ *   - The library keeps no state between calls except a per-device
+ *     architecture check, the launch-configuration override and the device
+ *     error word read by repro_device_check().
+ */
+#ifndef REPRO_H
+#define REPRO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define REPRO_VERSION 1
+#define REPRO_QMAX 127
+#define REPRO_CHUNK 64
+#define REPRO_MAX_REPLICAS 64
+
+typedef enum {
+    REPRO_OK = 0,
+    REPRO_ERR_ARG = -1,       /* NULL pointer, unknown mode/flag, q_max != 127, R out of range */
+    REPRO_ERR_SHAPE = -2,     /* negative size, empty tensor where a value is required, K too large */
+    REPRO_ERR_ALIGN = -3,     /* a device pointer is not 16-byte aligned */
+    REPRO_ERR_ARCH = -4,      /* the current device is not compute capability 10.3 (GB300) */
+    REPRO_ERR_LAUNCH = -5,    /* the CUDA runtime reported an error while enqueueing */
+    REPRO_ERR_TIMEOUT = -6,   /* a bounded device-side wait gave up (repro_device_check) */
+    REPRO_ERR_WORKSPACE = -7, /* workspace NULL or smaller than *_ws_bytes() */
+    REPRO_ERR_ALIAS = -8      /* two buffers that must not overlap do */
+} repro_status;
+
+typedef enum {
+    REPRO_SCALE_WEIGHT_MEANABS = 0, /* s = (2 (x) (canon_sum|x| (/) n)) (/) sqrt(q_max) */
+    REPRO_SCALE_ACT_AMAX = 1        /* s = max|x| (/) q_max                             */
+} repro_scale_mode;
+
+/* ------------------------------------------------------------------------
+ * Scale ([use]; [limits]: the learned LSQ step size diverged in int8
+ * pre-training and is instead recomputed from the weights every step).
+ *   mode WEIGHT_MEANABS: S = canonical sum of |x_i| over the flat tensor,
+ *     mean = S (/) float(n), s = (2 (x) mean) (/) sqrt(float(q_max)).
+ *   mode ACT_AMAX: s = (max_i |x_i|) (/) float(q_max) (max is exact, so its
+ *     evaluation order is free).
+ * x: n floats; scale_out: 1 float (device).  ws: workspace of at least
+ * repro_wscale_ws_bytes(n) bytes (contents on entry are ignored).
+ * Errors: n <= 0 -> REPRO_ERR_SHAPE; unknown mode or q_max != 127 ->
+ * REPRO_ERR_ARG; small ws -> REPRO_ERR_WORKSPACE.
+ * ------------------------------------------------------------------------ */
+int repro_wscale(const float* x, int64_t n, int mode, int qmax, float* scale_out,
+                 void* ws, size_t ws_bytes, void* stream);
+size_t repro_wscale_ws_bytes(int64_t n);
+
+/* ------------------------------------------------------------------------
+ * Quantise ([use]: 8-bit weights and activations; [limits]: deterministic
+ * rounding).  q_i = clamp(round_half_even(x_i (/) s), -127, 127), where the
+ * quotient is the correctly rounded binary32 division (rounding the quotient
+ * and then the integer is the defined double rounding).  s <= subnormal gives
+ * q = 0 everywhere; a NaN quotient gives 0; +-Inf clamps.
+ * x: n floats; scale: 1 float (device); q_out: n int8.  n == 0 is a no-op.
+ * ------------------------------------------------------------------------ */
+int repro_quant_i8(const float* x, int64_t n, const float* scale, int qmax,
+                   int8_t* q_out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Forward ([use]; [abstract]).  acc[m,n] = sum_k Xq[m,k]*Wq[n,k] computed
+ * exactly as an integer (so its order cannot matter), then
+ * Y[m,n] = (float(acc) (x) s_x) (x) s_w -- two unfused multiplies, left to
+ * right.  xq: M x K int8, wq: N x K int8 (nn.Linear layout), y: M x N float.
+ * Requires K <= 133144 so that |acc| <= 127*127*K fits in int32
+ * (REPRO_ERR_SHAPE otherwise).  M, N or K may be 0 (K == 0 writes +0 times
+ * the scales).
+ * ------------------------------------------------------------------------ */
+int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x,
+                     const float* s_w, float* y, int64_t M, int64_t N, int64_t K,
+                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * Backward ([works]: fixed order, unfused multiply then add).  Operands are
+ * dequantised from int8 on the fly, identically every time:
+ *   W^[n,k] = float(Wq[n,k]) (x) s_w,   X^[m,k] = float(Xq[m,k]) (x) s_x
+ *   dX[m,k] = canonical sum over n = 0..N-1 of ( dY[m,n] (x) W^[n,k] )
+ *   dW[n,k] = canonical sum over m = 0..M-1 of ( dY[m,n] (x) X^[m,k] )
+ * (straight-through estimator; no clipping mask.)
+ * dy: M x N float; xq: M x K int8; wq: N x K int8; dx: M x K float or NULL
+ * (skip); dw: N x K float or NULL (skip).  xq/s_x may be NULL when dw is NULL;
+ * wq/s_w may be NULL when dx is NULL.
+ * flags: REPRO_BWD_DW_ACCUMULATE -- instead of storing dW, update
+ *   dw[n,k] <- dw[n,k] (+) dW[n,k] (one add of the fully formed dW; the same
+ *   bits as repro_grad_accum on a stored dW).
+ * ws: at least repro_linear_bwd_ws_bytes(M, N, K) bytes (may be 0).
+ * dx and dw must not overlap dy, xq or wq (REPRO_ERR_ALIAS).
+ * ------------------------------------------------------------------------ */
+#define REPRO_BWD_DW_ACCUMULATE 1
+int repro_linear_bwd(const float* dy, const int8_t* xq, const int8_t* wq,
+                     const float* s_x, const float* s_w, float* dx, float* dw,
+                     int64_t M, int64_t N, int64_t K, int flags,
+                     void* ws, size_t ws_bytes, void* stream);
+size_t repro_linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K);
+
+/* ------------------------------------------------------------------------
+ * Micro-batch accumulation ([limits], level 1 of the replayed reduction):
+ * acc[i] <- acc[i] (+) g[i].  Called once per micro-batch after the first, in
+ * micro-batch order (the first micro-batch's gradient is the accumulator's
+ * initial value).  acc and g must not overlap (REPRO_ERR_ALIAS).
+ * ------------------------------------------------------------------------ */
+int repro_grad_accum(float* acc, const float* g, int64_t n, void* stream);
+
+/* ------------------------------------------------------------------------
+ * TreeFold ([limits], level 3: the replica all-reduce replayed on one device,
+ * pairing partials in the order of a recursive-doubling all-reduce).  With
+ * p' = largest power of two <= R and r = R - p': survivors are
+ * [P0(+)P1, ..., P_{2r-2}(+)P_{2r-1}, P_{2r}, ..., P_{R-1}]; then for
+ * d = 1, 2, ..., p'/2 survivor j is combined with survivor j XOR d; the
+ * result is survivor 0 (equal on every rank).  For R = 2^k this is the
+ * adjacent-pair tree.
+ * parts: HOST array of R device pointers, each to n floats (any memory
+ * placement; only the logical order of the array matters); out: n floats and
+ * may alias parts[0] exactly (no other overlap).  1 <= R <= 64.
+ * ------------------------------------------------------------------------ */
+int repro_treefold(const float* const* parts, int R, int64_t n, float* out,
+                   void* stream);
+
+/* ------------------------------------------------------------------------
+ * Housekeeping.
+ * repro_status_str: static description of a status code.
+ * repro_version: REPRO_VERSION.
+ * repro_device_check: synchronises `stream`, then reads and clears the
+ *   device error word set by bounded device-side waits; returns REPRO_OK or
+ *   REPRO_ERR_TIMEOUT (or REPRO_ERR_LAUNCH if the stream reported an error).
+ * repro_set_launch_cfg: test hook that changes how work is split across
+ *   thread blocks (never the arithmetic); NULL restores the defaults.  Used
+ *   to show that results do not depend on the launch configuration.  Not
+ *   thread-safe; affects subsequent calls in this process.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int bwd_segment_log2;   /* -1: default; else 2^k chunks per backward reduction segment (0..8) */
+    int reduce_block_log2;  /* -1: default; else 2^k chunk partials per block in repro_wscale (0..10) */
+    int fwd_path;           /* -1: default; 0: CUDA-core exact path; 1: tensor-core path */
+    int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
+} repro_launch_cfg;
+
+const char* repro_status_str(int status);
+int repro_version(void);
+int repro_device_check(void* stream);
+int repro_set_launch_cfg(const repro_launch_cfg* cfg);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* REPRO_H */

@@ -1,0 +1,278 @@
+"""CPU oracle of the bitwise-reproducible int8 QAT linear layer.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg (``bench.py``) may import this package.  The CUDA
+library and its Python binding never import it; there is no CPU fallback.
+
+The arithmetic lives in ``oracle.c`` (plain C11, contraction off, subnormals
+flushed in software); this module only compiles it and marshals numpy arrays
+through ctypes.  See ``oracle.h`` for the definitions and their sources.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+CFLAGS = [
+    "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+    "-fexcess-precision=standard", "-fPIC", "-shared",
+]
+
+
+def build(force: bool = False, openmp: bool = True) -> str:
+    """Compile oracle.c into liboracle.so next to it; return the path."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                   os.path.getmtime(os.path.join(_HERE, "oracle.h")))):
+        return _LIB_PATH
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        raise RuntimeError("no C compiler found to build the oracle")
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    flags = CFLAGS + (["-fopenmp"] if openmp else [])
+    cmd = [cc, *flags, _SRC, "-o", tmp, "-lm"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0 and openmp:
+        os.unlink(tmp)
+        return build(force=True, openmp=False)
+    if r.returncode != 0:
+        os.unlink(tmp)
+        raise RuntimeError("oracle build failed:\n" + r.stderr)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_lib = None
+
+_f32p = ctypes.POINTER(ctypes.c_float)
+_i8p = ctypes.POINTER(ctypes.c_int8)
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i64 = ctypes.c_int64
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        path = build()
+        L = ctypes.CDLL(path)
+        sig = {
+            "oracle_flush": (ctypes.c_float, [ctypes.c_float]),
+            "oracle_add": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+            "oracle_mul": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+            "oracle_div": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+            "oracle_sqrt": (ctypes.c_float, [ctypes.c_float]),
+            "oracle_i2f": (ctypes.c_float, [_i64]),
+            "oracle_quant_one": (ctypes.c_int, [ctypes.c_float, ctypes.c_float, ctypes.c_int]),
+            "oracle_canon_sum": (ctypes.c_float, [_f32p, _i64]),
+            "oracle_wscale": (ctypes.c_float, [_f32p, _i64, ctypes.c_int, ctypes.c_int]),
+            "oracle_quant_i8": (None, [_f32p, _i64, ctypes.c_float, ctypes.c_int, _i8p]),
+            "oracle_linear_fwd": (None, [_i8p, _i8p, ctypes.c_float, ctypes.c_float, _f32p,
+                                         _i64, _i64, _i64]),
+            "oracle_linear_fwd_at": (None, [_i8p, _i8p, ctypes.c_float, ctypes.c_float,
+                                            _i64, _i64, _i64, _i64p, _i64p, _i64, _f32p]),
+            "oracle_int_dot": (ctypes.c_int64, [_i8p, _i8p, _i64, _i64, _i64]),
+            "oracle_linear_bwd_dx": (None, [_f32p, _i8p, ctypes.c_float, _f32p, _i64, _i64, _i64]),
+            "oracle_linear_bwd_dw": (None, [_f32p, _i8p, ctypes.c_float, _f32p, _i64, _i64, _i64]),
+            "oracle_linear_bwd_dx_at": (None, [_f32p, _i8p, ctypes.c_float, _i64, _i64, _i64,
+                                               _i64p, _i64p, _i64, _f32p]),
+            "oracle_linear_bwd_dw_at": (None, [_f32p, _i8p, ctypes.c_float, _i64, _i64, _i64,
+                                               _i64p, _i64p, _i64, _f32p]),
+            "oracle_grad_accum": (None, [_f32p, _f32p, _i64]),
+            "oracle_treefold_one": (ctypes.c_float, [_f32p, ctypes.c_int]),
+            "oracle_treefold": (None, [ctypes.POINTER(_f32p), ctypes.c_int, _i64, _f32p]),
+            "oracle_treefold_all_ranks": (None, [_f32p, ctypes.c_int, _f32p]),
+            "oracle_threads": (ctypes.c_int, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------- helpers
+
+def _f32(a) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    return a
+
+
+def _i8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int8)
+
+
+def _p(a: np.ndarray, t):
+    return a.ctypes.data_as(t)
+
+
+def f32_bits(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float32).view(np.uint32)
+
+
+# ---------------------------------------------------------------- elementary ops
+
+def flush(a: float) -> float:
+    return lib().oracle_flush(a)
+
+
+def add(a: float, b: float) -> float:
+    return lib().oracle_add(a, b)
+
+
+def mul(a: float, b: float) -> float:
+    return lib().oracle_mul(a, b)
+
+
+def div(a: float, b: float) -> float:
+    return lib().oracle_div(a, b)
+
+
+def sqrt(a: float) -> float:
+    return lib().oracle_sqrt(a)
+
+
+def i2f(v: int) -> float:
+    return lib().oracle_i2f(int(v))
+
+
+def quant_one(x: float, s: float, qmax: int = 127) -> int:
+    return lib().oracle_quant_one(x, s, qmax)
+
+
+# ---------------------------------------------------------------- the path
+
+def canon_sum(p) -> np.float32:
+    p = _f32(p).ravel()
+    return np.float32(lib().oracle_canon_sum(_p(p, _f32p), p.size))
+
+
+def wscale(x, mode: int, qmax: int = 127) -> np.float32:
+    x = _f32(x).ravel()
+    return np.float32(lib().oracle_wscale(_p(x, _f32p), x.size, int(mode), int(qmax)))
+
+
+def quant_i8(x, s: float, qmax: int = 127) -> np.ndarray:
+    x = _f32(x)
+    q = np.empty(x.shape, dtype=np.int8)
+    lib().oracle_quant_i8(_p(x, _f32p), x.size, float(s), int(qmax), _p(q, _i8p))
+    return q
+
+
+def linear_fwd(xq, wq, s_x: float, s_w: float) -> np.ndarray:
+    xq, wq = _i8(xq), _i8(wq)
+    M, K = xq.shape
+    N, K2 = wq.shape
+    assert K == K2
+    y = np.empty((M, N), dtype=np.float32)
+    lib().oracle_linear_fwd(_p(xq, _i8p), _p(wq, _i8p), float(s_x), float(s_w),
+                            _p(y, _f32p), M, N, K)
+    return y
+
+
+def linear_fwd_at(xq, wq, s_x, s_w, idx_m, idx_n) -> np.ndarray:
+    xq, wq = _i8(xq), _i8(wq)
+    M, K = xq.shape
+    N = wq.shape[0]
+    im = np.ascontiguousarray(idx_m, dtype=np.int64)
+    jn = np.ascontiguousarray(idx_n, dtype=np.int64)
+    out = np.empty(im.size, dtype=np.float32)
+    lib().oracle_linear_fwd_at(_p(xq, _i8p), _p(wq, _i8p), float(s_x), float(s_w), M, N, K,
+                               _p(im, _i64p), _p(jn, _i64p), im.size, _p(out, _f32p))
+    return out
+
+
+def int_dot(xq, wq, m: int, n: int) -> int:
+    xq, wq = _i8(xq), _i8(wq)
+    return int(lib().oracle_int_dot(_p(xq, _i8p), _p(wq, _i8p), m, n, xq.shape[1]))
+
+
+def linear_bwd_dx(dy, wq, s_w: float) -> np.ndarray:
+    dy, wq = _f32(dy), _i8(wq)
+    M, N = dy.shape
+    N2, K = wq.shape
+    assert N == N2
+    dx = np.empty((M, K), dtype=np.float32)
+    lib().oracle_linear_bwd_dx(_p(dy, _f32p), _p(wq, _i8p), float(s_w), _p(dx, _f32p), M, N, K)
+    return dx
+
+
+def linear_bwd_dw(dy, xq, s_x: float) -> np.ndarray:
+    dy, xq = _f32(dy), _i8(xq)
+    M, N = dy.shape
+    M2, K = xq.shape
+    assert M == M2
+    dw = np.empty((N, K), dtype=np.float32)
+    lib().oracle_linear_bwd_dw(_p(dy, _f32p), _p(xq, _i8p), float(s_x), _p(dw, _f32p), M, N, K)
+    return dw
+
+
+def linear_bwd_dx_at(dy, wq, s_w, idx_m, idx_k) -> np.ndarray:
+    dy, wq = _f32(dy), _i8(wq)
+    M, N = dy.shape
+    K = wq.shape[1]
+    im = np.ascontiguousarray(idx_m, dtype=np.int64)
+    ik = np.ascontiguousarray(idx_k, dtype=np.int64)
+    out = np.empty(im.size, dtype=np.float32)
+    lib().oracle_linear_bwd_dx_at(_p(dy, _f32p), _p(wq, _i8p), float(s_w), M, N, K,
+                                  _p(im, _i64p), _p(ik, _i64p), im.size, _p(out, _f32p))
+    return out
+
+
+def linear_bwd_dw_at(dy, xq, s_x, idx_n, idx_k) -> np.ndarray:
+    dy, xq = _f32(dy), _i8(xq)
+    M, N = dy.shape
+    K = xq.shape[1]
+    i_n = np.ascontiguousarray(idx_n, dtype=np.int64)
+    ik = np.ascontiguousarray(idx_k, dtype=np.int64)
+    out = np.empty(i_n.size, dtype=np.float32)
+    lib().oracle_linear_bwd_dw_at(_p(dy, _f32p), _p(xq, _i8p), float(s_x), M, N, K,
+                                  _p(i_n, _i64p), _p(ik, _i64p), i_n.size, _p(out, _f32p))
+    return out
+
+
+def grad_accum(acc, g) -> np.ndarray:
+    """Returns acc (+) g as a new array (inputs untouched)."""
+    out = _f32(acc).copy()
+    g = _f32(g)
+    assert out.size == g.size
+    lib().oracle_grad_accum(_p(out, _f32p), _p(g, _f32p), out.size)
+    return out
+
+
+def treefold_one(vals) -> np.float32:
+    v = _f32(vals).ravel()
+    return np.float32(lib().oracle_treefold_one(_p(v, _f32p), v.size))
+
+
+def treefold_all_ranks(vals) -> np.ndarray:
+    v = _f32(vals).ravel()
+    out = np.empty(v.size, dtype=np.float32)
+    lib().oracle_treefold_all_ranks(_p(v, _f32p), v.size, _p(out, _f32p))
+    return out
+
+
+def treefold(parts) -> np.ndarray:
+    """parts: a sequence of R equal-length float32 arrays (any memory layout)."""
+    arrs = [_f32(p).ravel() for p in parts]
+    R = len(arrs)
+    n = arrs[0].size
+    assert all(a.size == n for a in arrs)
+    ptrs = (_f32p * R)(*[_p(a, _f32p) for a in arrs])
+    out = np.empty(n, dtype=np.float32)
+    lib().oracle_treefold(ptrs, R, n, _p(out, _f32p))
+    return out
+
+
+def threads() -> int:
+    return int(lib().oracle_threads())

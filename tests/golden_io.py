@@ -1,0 +1,59 @@
+"""Readers for the hand-worked fixtures under tests/golden/ (see each file's
+header for the passage it follows)."""
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for raw in f:
+            line = raw.split("#", 1)[0].strip()
+            if line:
+                yield line
+
+
+def bits_to_f32(b: int) -> np.float32:
+    return np.array([b], dtype=np.uint32).view(np.float32)[0]
+
+
+def f32_to_bits(x) -> int:
+    return int(np.array([x], dtype=np.float32).view(np.uint32)[0])
+
+
+def quant_cases():
+    for line in _lines("quant_rne.txt"):
+        xb, sb, q = line.split()
+        yield int(xb, 16), int(sb, 16), int(q)
+
+
+def ftz_cases():
+    for line in _lines("ftz_cases.txt"):
+        op, a, b, e = line.split()
+        yield op, int(a, 16), int(b, 16), int(e, 16)
+
+
+def canon_cases():
+    """Yields (terms float32 array, expected bits)."""
+    for line in _lines("canon_discriminators.txt"):
+        lhs, rhs = line.split("->")
+        toks = lhs.split()
+        L = int(toks[0])
+        fill = float(toks[1])
+        p = np.full(L, fill, dtype=np.float32)
+        for t in toks[2:]:
+            i, v = t.split(":")
+            p[int(i)] = np.float32(float(v))
+        yield p, int(rhs.split()[0], 16)
+
+
+def treefold_cases():
+    for line in _lines("treefold_cases.txt"):
+        lhs, rhs = line.split("->")
+        toks = lhs.split()
+        R = int(toks[0])
+        vals = np.array([float(v) for v in toks[1:]], dtype=np.float32)
+        assert vals.size == R
+        yield vals, int(rhs.split()[0], 16)
