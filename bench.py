@@ -1,0 +1,441 @@
+"""Benchmark of the bit-exact int8-QAT linear hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of the workload
+(default: one GQA decoder block's four linears, 4 micro-batches of 16,384
+tokens, TreeFold over R = 6 replicas): weight scales and int8 weights, then per
+micro-batch and linear the activation scale, int8 activations, exact int8
+forward, canonical-order fp32 dX and dW with dW accumulated in micro-batch
+order, and finally TreeFold.  Inputs are seeded synthetic tensors resident in
+HBM (about 8 GB, far larger than L2) when the timed region starts.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload block|attn_out|gate_up|down_accum|tiny]
+
+Prints one JSON line (rank 0).  N > 1 runs one independent replica per GPU
+("replicas only": the step has no collective on its data path); `value` is the
+tokens of all ranks divided by the slowest rank's time.  `--impl reference`
+times the CPU oracle on a bounded slice of the same workload's step.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bitwise_reproducible_int8_gb300 import inputs  # noqa: E402
+
+METRIC = "tokens/s bit-exact int8-QAT linear fwd+bwd (1 GB300); % of int8/FP32/HBM roofline"
+UNIT = "tokens/s"
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- oracle leg
+
+def oracle_sample_step(wl, host, frac_log2: int) -> tuple:
+    """The oracle, as it stands, over a uniform 2^-k slice of one step's work:
+    scales and int8 codes in full (they are O(n)); the forward and dX for the
+    first M/2^k tokens of every micro-batch; dW for the first N/2^k rows of
+    every weight, reduced over all M tokens; accumulation and TreeFold over
+    that slice of the gradient.  Returns (seconds, tokens credited)."""
+    import oracle as orc
+    L, J, M = len(wl.linears), wl.microbatches, wl.tokens
+    f = 1 << frac_log2
+    m_s = max(1, M // f)
+    n_s = [max(1, -(-l.n_out // f)) for l in wl.linears]
+    dY_cols = [[np.ascontiguousarray(host.dY[i][j][:, :n_s[i]]) for j in range(J)]
+               for i in range(L)]
+    noise = []
+    if wl.replicas > 1:
+        offs = np.cumsum([0] + [l.n_out * l.k_in for l in wl.linears])
+        idx = np.concatenate([offs[i] + np.arange(n_s[i] * l.k_in)
+                              for i, l in enumerate(wl.linears)])
+        noise = [host.noise[r][idx] for r in range(1, wl.replicas)]
+    t0 = time.perf_counter()
+    s_w = [orc.wscale(host.W[i], 0) for i in range(L)]
+    wq = [orc.quant_i8(host.W[i], s_w[i]) for i in range(L)]
+    G = [None] * L
+    for j in range(J):
+        for i in range(L):
+            X, dY = host.X[i][j], host.dY[i][j]
+            s_x = orc.wscale(X, 1)
+            xq = orc.quant_i8(X, s_x)
+            orc.linear_fwd(xq[:m_s], wq[i], s_x, s_w[i])
+            orc.linear_bwd_dx(dY[:m_s], wq[i], s_w[i])
+            dw = orc.linear_bwd_dw(dY_cols[i][j], xq, s_x)
+            G[i] = dw if G[i] is None else orc.grad_accum(G[i], dw)
+    sec = time.perf_counter() - t0
+    if wl.replicas > 1:
+        g = np.concatenate([x.ravel() for x in G])
+        parts = [g] + [orc.grad_accum(g, nz) for nz in noise]   # replica set-up, untimed
+        t1 = time.perf_counter()
+        orc.treefold(parts)
+        sec += time.perf_counter() - t1
+    # credit tokens in proportion to the MACs done: forward, dX and dW each
+    # cost M * sum(N K) per micro-batch in the full step
+    rho_dw = sum(n * l.k_in for n, l in zip(n_s, wl.linears)) / \
+        sum(l.n_out * l.k_in for l in wl.linears)
+    frac = (2.0 * m_s / M + rho_dw) / 3.0
+    return sec, wl.tokens * J * frac
+
+
+def _sample_text(wl, frac_log2, toks):
+    return (f"{wl.name}: about 1/{1 << frac_log2} of one step's work -- forward and dX for the "
+            f"first {max(1, wl.tokens >> frac_log2)} tokens of each of {wl.microbatches} "
+            f"micro-batches, dW for the first ceil(N/{1 << frac_log2}) rows of every weight "
+            f"over all tokens, scales and int8 codes in full, TreeFold over that slice; "
+            f"credited {toks:.1f} tokens (in proportion to the MACs done)")
+
+
+def cpu_baseline(wl, host, frac_log2: int) -> dict:
+    import oracle as orc
+    orc.build()
+    sec, toks = oracle_sample_step(wl, host, frac_log2)
+    return {"value": toks / sec, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
+            "sample": _sample_text(wl, frac_log2, toks) + f"; {sec:.2f} s"}
+
+
+def run_reference(args, wl):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle as orc
+    from bitwise_reproducible_int8_gb300 import step as S
+    orc.build()
+    host = S.generate_host_inputs(wl)
+    for _ in range(args.warmup):
+        oracle_sample_step(wl, host, args.ref_frac_log2)
+    runs = [oracle_sample_step(wl, host, args.ref_frac_log2) for _ in range(args.steps)]
+    total = sum(r[0] for r in runs)
+    toks = sum(r[1] for r in runs)
+    value = toks / total
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8/f32",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": wl.name, "tokens_per_step": wl.tokens * wl.microbatches,
+                   "sample_fraction": 1.0 / (1 << args.ref_frac_log2),
+                   "parallelism": "replicas only"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
+                         "sample": _sample_text(wl, args.ref_frac_log2, toks / args.steps)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our leg
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    from bitwise_reproducible_int8_gb300 import build_lib
+    from bitwise_reproducible_int8_gb300 import repro as R
+    from bitwise_reproducible_int8_gb300 import step as S
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    if world > 1:
+        dist.barrier()
+    # replicas only: rank r owns its own micro-batches (windows m mod R = r)
+    wl_r = dataclasses.replace(wl, x_seed_base=wl.x_seed_base + rank * wl.microbatches)
+    host = S.generate_host_inputs(wl_r)
+    hp = S.HotPathStep(wl_r, host, fused_accum=not args.unfused_accum)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        if wl_r.replicas > 1:
+            tf, hp.TF = hp.TF, None
+            hp.run(stream)
+            hp.prepare_replicas(stream)
+            hp.TF = tf
+        for _ in range(args.warmup):
+            hp.run(stream)
+    stream.synchronize()
+    if R.repro_device_check(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- device-timed region: K steps, inputs resident in HBM
+    timers = {}
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = R.repro_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(args.steps):
+            hp.run(stream, timers=timers)
+        t_end.record(stream)
+    stream.synchronize()
+    launches = R.repro_launch_count() - launches0
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end)
+    if R.repro_device_check(stream) != 0:
+        raise RuntimeError("device error during the timed steps")
+    per_class = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in timers.items()}
+    launch_counts = {k: len(v) for k, v in timers.items()}
+
+    t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    tokens_all = hp.tokens() * args.steps * world
+    value = tokens_all / (ms_max / 1000.0)
+
+    # ---- end to end: host inputs copied in, result copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(hp, host, args.steps, stream, world)
+
+    if rank == 0:
+        peaks = load_peaks()
+        sms = torch.cuda.get_device_properties(local).multi_processor_count
+        fl = hp.flops()
+        bwd_ms = per_class.get("bwd_dx", 0.0) + per_class.get("bwd_dw", 0.0)
+        bwd_ops = (fl["bwd_dx_fp32_ops"] + fl["bwd_dw_fp32_ops"]) * args.steps
+        fp32_peak = sms * 128 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        achieved = bwd_ops / (bwd_ms / 1000.0) / 1e12 if bwd_ms > 0 else 0.0
+        nb = launch_counts.get("bwd_dx", 0) + launch_counts.get("bwd_dw", 0)
+        roofline = {
+            "bound": "alu", "kernel": "k_bwd (dX and dW, canonical-order fp32)",
+            "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
+            "frac": achieved / fp32_peak if fp32_peak else None,
+            "peak_note": f"FP32 pipe: {sms} SMs x 128 lanes x {peaks.get('sm_max_mhz', 2070.0):.0f} MHz,"
+                         " one FMUL or FADD per lane per clock (no FMA may be used)",
+            "traffic": None, "launches": nb,
+            "flops_per_launch": bwd_ops / nb if nb else None,
+            "avg_launch_ms": bwd_ms / nb if nb else None,
+        }
+        other = {}
+        fwd_ms = per_class.get("fwd", 0.0)
+        if fwd_ms > 0:
+            other["fwd_int8"] = {"achieved_tops": fl["fwd_int_ops"] * args.steps / (fwd_ms / 1e3) / 1e12,
+                                 "ms_per_step": fwd_ms / args.steps}
+        gbytes = hbm_bytes(hp)
+        for cls, nbytes in gbytes.items():
+            c_ms = per_class.get(cls, 0.0)
+            if c_ms > 0:
+                gbs = nbytes * args.steps / (c_ms / 1e3) / 1e9
+                other[cls] = {"achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+                              "ms_per_step": c_ms / args.steps}
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(wl_r, host, args.cpu_frac_log2)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "i8/f32", "data": "synthetic",
+            "config": {"workload": wl.name, "tokens_per_step": hp.tokens(),
+                       "micro_batches": wl.microbatches, "micro_batch_tokens": wl.tokens,
+                       "linears": [f"{l.name} {l.n_out}x{l.k_in}" for l in wl.linears],
+                       "replicas": wl.replicas, "parallelism": "replicas only",
+                       "accumulation": "unfused repro_grad_accum" if args.unfused_accum
+                       else "fused into the dW epilogue",
+                       "l2": f"inputs larger than L2: {resident_gb(hp):.1f} GB resident, "
+                             "streamed once per step"},
+            "roofline": roofline, "other_kernels": other,
+            "ms_per_step_by_call": {k: v / args.steps for k, v in per_class.items()},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk, "peaks_source": peaks["source"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def resident_gb(hp) -> float:
+    tot = sum(x.numel() * 4 for i in range(len(hp.X)) for x in hp.X[i])
+    tot += sum(x.numel() * 4 for i in range(len(hp.dY)) for x in hp.dY[i])
+    return tot / 1e9
+
+
+def hbm_bytes(hp) -> dict:
+    """Algorithmic HBM bytes per step of the streaming call classes."""
+    wl = hp.wl
+    J = wl.microbatches
+    nw = sum(w.numel() for w in hp.W)
+    nx = sum(x.numel() for i in range(len(hp.X)) for x in hp.X[i])
+    out = {"wscale_w": 4 * nw, "quant_w": 5 * nw, "wscale_x": 4 * nx, "quant_x": 5 * nx}
+    if hp.TF is not None:
+        out["treefold"] = 4 * (wl.replicas + 1) * hp.n_grad
+    if hp.dW_tmp is not None:
+        out["accum"] = 12 * nw * (J - 1)
+    return out
+
+
+def measure_e2e(hp, host, steps, stream, world):
+    """Same steps through the public API with host buffers: every step copies
+    its inputs from pinned host memory (weights, then each micro-batch's X and
+    dY on a copy stream overlapped with compute) and reads the result back."""
+    import torch
+    L, J = len(hp.wl.linears), hp.wl.microbatches
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    hW = [pin(host.W[i]) for i in range(L)]
+    hX = [[pin(host.X[i][j]) for j in range(J)] for i in range(L)]
+    hdY = [[pin(host.dY[i][j]) for j in range(J)] for i in range(L)]
+    res = hp.result()
+    out_host = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
+    h2d = sum(t.numel() * 4 for t in hW) + sum(t.numel() * 4 for r in hX for t in r) + \
+        sum(t.numel() * 4 for r in hdY for t in r)
+    d2h = res.numel() * 4
+    copy = torch.cuda.Stream()
+
+    def one_step():
+        evs = []
+        copy.wait_stream(stream)
+        with torch.cuda.stream(copy):
+            for i in range(L):
+                hp.W[i].copy_(hW[i], non_blocking=True)
+            for j in range(J):
+                for i in range(L):
+                    hp.X[i][j].copy_(hX[i][j], non_blocking=True)
+                    hp.dY[i][j].copy_(hdY[i][j], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(copy)
+                evs.append(e)
+        hp.run(stream, wait_events=evs)
+        with torch.cuda.stream(stream):
+            out_host.copy_(res, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        one_step()
+    stream.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        one_step()
+    b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b)
+    t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    return {"value": hp.tokens() * steps * world / (ms / 1000.0), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": ms / steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="block", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--unfused-accum", action="store_true",
+                    help="accumulate dW with repro_grad_accum instead of the fused epilogue")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-frac-log2", type=int, default=10,
+                    help="the oracle's timed sample is 2^-k of one step's work")
+    ap.add_argument("--ref-frac-log2", type=int, default=12,
+                    help="each reference-arm step is 2^-k of one step's work")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,363 @@
+// api.cu -- the C ABI declared in include/repro.h: argument validation,
+// architecture check, workspace sizing and dispatch to the kernels.  No call
+// allocates device memory; every call enqueues on the caller's stream.
+#include <stdint.h>
+#include <string.h>
+
+#include "internal.h"
+#include "repro.h"
+
+namespace repro {
+
+namespace {
+
+LaunchCfg g_cfg = {-1, -1, -1, 0};
+
+constexpr int kMaxDevices = 64;
+int g_arch_ok[kMaxDevices];   // 0 unknown, 1 GB300, -1 other
+int g_sms[kMaxDevices];
+
+__device__ int g_device_error;   // set by bounded device-side waits
+
+unsigned long long g_launches;    // kernels enqueued by this library
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return -1;
+    return dev;
+}
+
+} // namespace
+
+const LaunchCfg& launch_cfg() { return g_cfg; }
+
+int num_sms()
+{
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices)
+        return 152;
+    if (g_sms[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 152;
+        g_sms[dev] = v;
+    }
+    return g_sms[dev];
+}
+
+void count_launches(int k) { __atomic_fetch_add(&g_launches, (unsigned long long)k, __ATOMIC_RELAXED); }
+
+int* device_error_word()
+{
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess)
+        return nullptr;
+    return static_cast<int*>(p);
+}
+
+} // namespace repro
+
+using namespace repro;
+
+namespace {
+
+int check_arch()
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return REPRO_ERR_LAUNCH;
+    if (dev >= kMaxDevices)
+        return REPRO_ERR_ARCH;
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return REPRO_ERR_LAUNCH;
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_arch_ok[dev] == 1 ? REPRO_OK : REPRO_ERR_ARCH;
+}
+
+// output rows are tiled 64 per CTA along grid.y (at most 65535 tiles)
+constexpr int64_t kMaxRows = 65535LL * 64;
+
+inline bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline bool al4(const void* p) { return ((uintptr_t)p & 3u) == 0; }
+
+inline bool overlap(const void* a, size_t na, const void* b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0)
+        return false;
+    const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+    return x < y + nb && y < x + na;
+}
+
+inline int status_of(cudaError_t e) { return e == cudaSuccess ? REPRO_OK : REPRO_ERR_LAUNCH; }
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int stream_grid(int64_t work_items)
+{
+    const int cfg = g_cfg.elementwise_blocks;
+    if (cfg > 0)
+        return cfg;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    const int64_t want = (work_items + 255) / 256;
+    return (int)(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+int seg_log2() { return g_cfg.bwd_segment_log2 < 0 ? 8 : g_cfg.bwd_segment_log2; }
+
+} // namespace
+
+extern "C" {
+
+const char* repro_status_str(int s)
+{
+    switch (s) {
+    case REPRO_OK: return "ok";
+    case REPRO_ERR_ARG: return "invalid argument (null pointer, mode, flag, q_max or R)";
+    case REPRO_ERR_SHAPE: return "invalid shape";
+    case REPRO_ERR_ALIGN: return "device pointer not aligned (16 bytes for tensors, 4 for scales)";
+    case REPRO_ERR_ARCH: return "current device is not a GB300 (compute capability 10.3)";
+    case REPRO_ERR_LAUNCH: return "CUDA runtime error while enqueueing";
+    case REPRO_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    case REPRO_ERR_WORKSPACE: return "workspace missing or too small";
+    case REPRO_ERR_ALIAS: return "buffers that must not overlap do";
+    default: return "unknown status";
+    }
+}
+
+int repro_version(void) { return REPRO_VERSION; }
+
+uint64_t repro_launch_count(void) { return (uint64_t)__atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+int repro_set_launch_cfg(const repro_launch_cfg* cfg)
+{
+    if (!cfg) {
+        g_cfg = LaunchCfg{-1, -1, -1, 0};
+        return REPRO_OK;
+    }
+    if (cfg->bwd_segment_log2 < -1 || cfg->bwd_segment_log2 > 8)
+        return REPRO_ERR_ARG;
+    if (cfg->reduce_block_log2 < -1 || cfg->reduce_block_log2 > 10)
+        return REPRO_ERR_ARG;
+    if (cfg->fwd_path < -1 || cfg->fwd_path > 1)
+        return REPRO_ERR_ARG;
+    if (cfg->elementwise_blocks < -1 || cfg->elementwise_blocks > (1 << 20))
+        return REPRO_ERR_ARG;
+    g_cfg.bwd_segment_log2 = cfg->bwd_segment_log2;
+    g_cfg.reduce_block_log2 = cfg->reduce_block_log2;
+    g_cfg.fwd_path = cfg->fwd_path;
+    g_cfg.elementwise_blocks = cfg->elementwise_blocks < 0 ? 0 : cfg->elementwise_blocks;
+    return REPRO_OK;
+}
+
+int repro_device_check(void* stream)
+{
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess)
+        return REPRO_ERR_LAUNCH;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess)
+        return REPRO_ERR_LAUNCH;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
+            return REPRO_ERR_LAUNCH;
+        return REPRO_ERR_TIMEOUT;
+    }
+    return REPRO_OK;
+}
+
+size_t repro_wscale_ws_bytes(int64_t n)
+{
+    if (n <= 0)
+        return 0;
+    return wscale_ws_bytes(n, 0);   // the largest over every launch configuration
+}
+
+int repro_wscale(const float* x, int64_t n, int mode, int qmax, float* scale_out, void* ws,
+                 size_t ws_bytes, void* stream)
+{
+    if (!x || !scale_out)
+        return REPRO_ERR_ARG;
+    if (mode != REPRO_SCALE_WEIGHT_MEANABS && mode != REPRO_SCALE_ACT_AMAX)
+        return REPRO_ERR_ARG;
+    if (qmax != REPRO_QMAX)
+        return REPRO_ERR_ARG;
+    if (n <= 0)
+        return REPRO_ERR_SHAPE;
+    if (!al16(x) || !al4(scale_out))
+        return REPRO_ERR_ALIGN;
+    if (!ws || ws_bytes < repro_wscale_ws_bytes(n))
+        return REPRO_ERR_WORKSPACE;
+    if (!al16(ws))
+        return REPRO_ERR_ALIGN;
+    if (overlap(ws, ws_bytes, x, (size_t)n * 4) || overlap(ws, ws_bytes, scale_out, 4))
+        return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    if (mode == REPRO_SCALE_WEIGHT_MEANABS)
+        return status_of(launch_wscale_meanabs(x, n, qmax, scale_out, ws, g_cfg.reduce_block_log2,
+                                               as_stream(stream)));
+    return status_of(launch_wscale_amax(x, n, qmax, scale_out, ws, amax_grid(n), as_stream(stream)));
+}
+
+int repro_quant_i8(const float* x, int64_t n, const float* scale, int qmax, int8_t* q_out,
+                   void* stream)
+{
+    if (qmax != REPRO_QMAX)
+        return REPRO_ERR_ARG;
+    if (n < 0)
+        return REPRO_ERR_SHAPE;
+    if (n == 0)
+        return REPRO_OK;
+    if (!x || !scale || !q_out)
+        return REPRO_ERR_ARG;
+    if (!al16(x) || !al16(q_out) || !al4(scale))
+        return REPRO_ERR_ALIGN;
+    if (overlap(q_out, (size_t)n, x, (size_t)n * 4) || overlap(q_out, (size_t)n, scale, 4))
+        return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_quant(x, n, scale, qmax, q_out, stream_grid(n / 16), as_stream(stream)));
+}
+
+int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x, const float* s_w,
+                     float* y, int64_t M, int64_t N, int64_t K, void* stream)
+{
+    if (M < 0 || N < 0 || K < 0 || K > 133144 || M > kMaxRows || N > kMaxRows)
+        return REPRO_ERR_SHAPE;
+    if (M == 0 || N == 0)
+        return REPRO_OK;
+    if (!y || !s_x || !s_w || (K > 0 && (!xq || !wq)))
+        return REPRO_ERR_ARG;
+    if (!al16(y) || (xq && !al16(xq)) || (wq && !al16(wq)) || !al4(s_x) || !al4(s_w))
+        return REPRO_ERR_ALIGN;
+    const size_t ybytes = (size_t)(M * N) * 4;
+    if (overlap(y, ybytes, xq, (size_t)(M * K)) || overlap(y, ybytes, wq, (size_t)(N * K)) ||
+        overlap(y, ybytes, s_x, 4) || overlap(y, ybytes, s_w, 4))
+        return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_fwd_cuda_core(xq, wq, s_x, s_w, y, M, N, K, as_stream(stream)));
+}
+
+size_t repro_linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (M <= 0 || N <= 0 || K <= 0)
+        return 0;
+    return bwd_ws_bytes(M, N, K, seg_log2());
+}
+
+int repro_linear_bwd(const float* dy, const int8_t* xq, const int8_t* wq, const float* s_x,
+                     const float* s_w, float* dx, float* dw, int64_t M, int64_t N, int64_t K,
+                     int flags, void* ws, size_t ws_bytes, void* stream)
+{
+    if (flags & ~REPRO_BWD_DW_ACCUMULATE)
+        return REPRO_ERR_ARG;
+    if (M < 0 || N < 0 || K < 0 || M > kMaxRows || N > kMaxRows || K > kMaxRows * 64)
+        return REPRO_ERR_SHAPE;
+    if (!dx && !dw)
+        return REPRO_ERR_ARG;
+    const bool want_dx = dx && M > 0 && K > 0;
+    const bool want_dw = dw && N > 0 && K > 0;
+    if (!want_dx && !want_dw)
+        return REPRO_OK;
+    if ((want_dx && N > 0 && (!dy || !wq || !s_w)) || (want_dw && M > 0 && (!dy || !xq || !s_x)))
+        return REPRO_ERR_ARG;
+    if ((dy && !al16(dy)) || (xq && !al16(xq)) || (wq && !al16(wq)) || (dx && !al16(dx)) ||
+        (dw && !al16(dw)) || (s_x && !al4(s_x)) || (s_w && !al4(s_w)))
+        return REPRO_ERR_ALIGN;
+    const size_t dyb = (size_t)(M * N) * 4, xqb = (size_t)(M * K), wqb = (size_t)(N * K);
+    const size_t dxb = want_dx ? (size_t)(M * K) * 4 : 0, dwb = want_dw ? (size_t)(N * K) * 4 : 0;
+    if (overlap(dx, dxb, dy, dyb) || overlap(dx, dxb, xq, xqb) || overlap(dx, dxb, wq, wqb) ||
+        overlap(dw, dwb, dy, dyb) || overlap(dw, dwb, xq, xqb) || overlap(dw, dwb, wq, wqb) ||
+        overlap(dx, dxb, dw, dwb) || overlap(dx, dxb, s_x, 4) || overlap(dx, dxb, s_w, 4) ||
+        overlap(dw, dwb, s_x, 4) || overlap(dw, dwb, s_w, 4))
+        return REPRO_ERR_ALIAS;
+    const int sl = seg_log2();
+    const size_t need = bwd_ws_bytes(M, N, K, sl);
+    if (need > 0) {
+        if (!ws || ws_bytes < need)
+            return REPRO_ERR_WORKSPACE;
+        if (!al16(ws))
+            return REPRO_ERR_ALIGN;
+        if (overlap(ws, ws_bytes, dx, dxb) || overlap(ws, ws_bytes, dw, dwb) ||
+            overlap(ws, ws_bytes, dy, dyb))
+            return REPRO_ERR_ALIAS;
+    }
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    cudaStream_t s = as_stream(stream);
+    if (want_dx) {
+        cudaError_t e = launch_bwd_dx(dy, wq, s_w, dx, M, N, K, sl, static_cast<float*>(ws), s);
+        if (e != cudaSuccess)
+            return REPRO_ERR_LAUNCH;
+    }
+    if (want_dw) {
+        cudaError_t e = launch_bwd_dw(dy, xq, s_x, dw, M, N, K, sl,
+                                      (flags & REPRO_BWD_DW_ACCUMULATE) != 0,
+                                      static_cast<float*>(ws), s);
+        if (e != cudaSuccess)
+            return REPRO_ERR_LAUNCH;
+    }
+    return REPRO_OK;
+}
+
+int repro_grad_accum(float* acc, const float* g, int64_t n, void* stream)
+{
+    if (n < 0)
+        return REPRO_ERR_SHAPE;
+    if (n == 0)
+        return REPRO_OK;
+    if (!acc || !g)
+        return REPRO_ERR_ARG;
+    if (!al16(acc) || !al16(g))
+        return REPRO_ERR_ALIGN;
+    if (overlap(acc, (size_t)n * 4, g, (size_t)n * 4))
+        return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_grad_accum(acc, g, n, stream_grid(n / 4), as_stream(stream)));
+}
+
+int repro_treefold(const float* const* parts, int R, int64_t n, float* out, void* stream)
+{
+    if (!parts || R < 1 || R > REPRO_MAX_REPLICAS)
+        return REPRO_ERR_ARG;
+    if (n < 0)
+        return REPRO_ERR_SHAPE;
+    if (!out)
+        return REPRO_ERR_ARG;
+    for (int r = 0; r < R; ++r) {
+        if (!parts[r])
+            return REPRO_ERR_ARG;
+        if (!al16(parts[r]))
+            return REPRO_ERR_ALIGN;
+    }
+    if (!al16(out))
+        return REPRO_ERR_ALIGN;
+    if (n == 0)
+        return REPRO_OK;
+    const size_t nb = (size_t)n * 4;
+    for (int r = 0; r < R; ++r) {
+        if (r == 0 && parts[0] == out)
+            continue;
+        if (overlap(out, nb, parts[r], nb))
+            return REPRO_ERR_ALIAS;
+    }
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_treefold(parts, R, n, out, stream_grid(n / 4), as_stream(stream)));
+}
+
+} // extern "C"

@@ -1,0 +1,91 @@
+// common.cuh -- device arithmetic of the reproducible path and small helpers.
+//
+// Arithmetic model (Open-1B review, onedev.kr/papers/92, section "How it
+// works": fixed order, explicit unfused multiply and add, subnormals flushed on
+// every backend):
+//   * a product is `mul.rn.f32` -- IEEE round-to-nearest-even with gradual
+//     underflow, no flush.  Every product is consumed by an `add.rn.ftz.f32`
+//     (which reads a subnormal operand as a signed zero) or passed through
+//     flush() before it is stored, so the flush happens exactly once, after
+//     IEEE rounding, as the oracle defines it.  This keeps the result
+//     independent of how a hardware flush treats results that round up to the
+//     smallest normal.
+//   * a sum is `add.rn.ftz.f32`: operands flushed, IEEE sum, subnormal result
+//     flushed.  A sum of two values on the 2^-149 grid is exact whenever it is
+//     subnormal, so this flush is unambiguous.
+//   * flush(x) = x (+) -0 with the same instruction: the identity on every
+//     normal value and on both zeros, and the signed zero for a subnormal.
+// All inline asm is non-volatile: the operations are pure, the compiler may
+// schedule them, and explicit rounding modifiers forbid any contraction.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace repro {
+
+__device__ __forceinline__ float fmul_rn(float a, float b)
+{
+    float r;
+    asm("mul.rn.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float fadd_ftz(float a, float b)
+{
+    float r;
+    asm("add.rn.ftz.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float flush(float x)
+{
+    return fadd_ftz(x, -0.0f);
+}
+
+// product stored or reused as an operand: round, then flush
+__device__ __forceinline__ float fmul_flush(float a, float b)
+{
+    return flush(fmul_rn(a, b));
+}
+
+// Packed pairs (sm_100 family): two independent lanes per instruction, same
+// rounding as the scalar forms.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(unsigned long long v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ unsigned long long fmul2_rn(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+__device__ __forceinline__ unsigned long long fadd2_ftz(unsigned long long a, unsigned long long b)
+{
+    unsigned long long r;
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// dequantised operand: float(q) (x) s, flushed (q is an exact small integer)
+__device__ __forceinline__ float dequant(int q, float s)
+{
+    return fmul_flush(__int2float_rn(q), s);
+}
+
+__device__ __forceinline__ float4 flush4(float4 v)
+{
+    return make_float4(flush(v.x), flush(v.y), flush(v.z), flush(v.w));
+}
+
+} // namespace repro

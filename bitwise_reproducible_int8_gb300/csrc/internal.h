@@ -1,0 +1,56 @@
+// internal.h -- launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Arguments are already validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#define REPRO_MAX_PARTS_INTERNAL 64
+
+namespace repro {
+
+struct LaunchCfg {
+    int bwd_segment_log2;   // chunks per backward reduction segment = 2^k (0..8)
+    int reduce_block_log2;  // chunk partials per block in the scale reduction (0..10)
+    int fwd_path;           // 0: CUDA-core exact path, 1: tensor-core path
+    int elementwise_blocks; // 0: default grid for streaming kernels
+};
+
+const LaunchCfg& launch_cfg();
+int num_sms();
+int* device_error_word();   // device address of the bounded-wait error flag
+void count_launches(int k); // adds k to the process-wide launch counter
+
+// ---- scale (k_scale.cu)
+size_t wscale_ws_bytes(int64_t n, int block_log2);
+cudaError_t launch_wscale_meanabs(const float* x, int64_t n, int qmax, float* scale_out,
+                                  void* ws, int block_log2, cudaStream_t st);
+cudaError_t launch_wscale_amax(const float* x, int64_t n, int qmax, float* scale_out,
+                               void* ws, int grid, cudaStream_t st);
+int amax_grid(int64_t n);
+
+// ---- quantiser (k_quant.cu)
+cudaError_t launch_quant(const float* x, int64_t n, const float* scale, int qmax, int8_t* q,
+                         int grid, cudaStream_t st);
+
+// ---- forward (k_fwd.cu)
+cudaError_t launch_fwd_cuda_core(const int8_t* xq, const int8_t* wq, const float* s_x,
+                                 const float* s_w, float* y, int64_t M, int64_t N, int64_t K,
+                                 cudaStream_t st);
+
+// ---- backward (k_bwd.cu)
+size_t bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int seg_log2);
+cudaError_t launch_bwd_dx(const float* dy, const int8_t* wq, const float* s_w, float* dx,
+                          int64_t M, int64_t N, int64_t K, int seg_log2, float* ws,
+                          cudaStream_t st);
+cudaError_t launch_bwd_dw(const float* dy, const int8_t* xq, const float* s_x, float* dw,
+                          int64_t M, int64_t N, int64_t K, int seg_log2, bool accumulate,
+                          float* ws, cudaStream_t st);
+
+// ---- reductions (k_reduce.cu)
+cudaError_t launch_grad_accum(float* acc, const float* g, int64_t n, int grid, cudaStream_t st);
+cudaError_t launch_treefold(const float* const* parts, int R, int64_t n, float* out, int grid,
+                            cudaStream_t st);
+
+} // namespace repro

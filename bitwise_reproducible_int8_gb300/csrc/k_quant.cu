@@ -1,0 +1,82 @@
+// k_quant.cu -- int8 quantiser.
+//
+// q = clamp(round_half_even(x (/) s), -127, 127): int8 weights and activations
+// for every attention/FFN linear (Open-1B review, onedev.kr/papers/92, section
+// "How to use"), deterministic rounding since stochastic rounding breaks
+// bitwise reproducibility (section "Premises and limits").  The quotient is
+// the correctly rounded binary32 division; it is then rounded to an integer
+// with ties to even (cvt.rni), which saturates out-of-range values and maps
+// NaN to 0 before the clamp.  A zero (or subnormal) scale gives q = 0.
+//
+// Streaming kernel: each thread converts 16 elements per step with four
+// 16-byte loads and one 16-byte store; the grid is a multiple of the SM count.
+#include "common.cuh"
+#include "internal.h"
+
+namespace repro {
+namespace {
+
+__device__ __forceinline__ int quant_one(float x, float s, int qmax)
+{
+    const float v = __fdiv_rn(flush(x), s);
+    int q = __float2int_rn(v);
+    q = q > qmax ? qmax : q;
+    q = q < -qmax ? -qmax : q;
+    return q;
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
+{
+    return (uint32_t)(a & 0xff) | ((uint32_t)(b & 0xff) << 8) | ((uint32_t)(c & 0xff) << 16) |
+           ((uint32_t)(d & 0xff) << 24);
+}
+
+__global__ void __launch_bounds__(256)
+k_quant(const float* __restrict__ x, int64_t n, const float* __restrict__ scale, int qmax,
+        int8_t* __restrict__ q)
+{
+    const float s = flush(*scale);
+    const int64_t nv = n >> 4;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    uint4* q16 = reinterpret_cast<uint4*>(q);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    if (s == 0.f) {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride)
+            q16[i] = make_uint4(0, 0, 0, 0);
+    } else {
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+            const float4 a = __ldg(x4 + 4 * i + 0);
+            const float4 b = __ldg(x4 + 4 * i + 1);
+            const float4 c = __ldg(x4 + 4 * i + 2);
+            const float4 d = __ldg(x4 + 4 * i + 3);
+            uint4 o;
+            o.x = pack4(quant_one(a.x, s, qmax), quant_one(a.y, s, qmax), quant_one(a.z, s, qmax),
+                        quant_one(a.w, s, qmax));
+            o.y = pack4(quant_one(b.x, s, qmax), quant_one(b.y, s, qmax), quant_one(b.z, s, qmax),
+                        quant_one(b.w, s, qmax));
+            o.z = pack4(quant_one(c.x, s, qmax), quant_one(c.y, s, qmax), quant_one(c.z, s, qmax),
+                        quant_one(c.w, s, qmax));
+            o.w = pack4(quant_one(d.x, s, qmax), quant_one(d.y, s, qmax), quant_one(d.z, s, qmax),
+                        quant_one(d.w, s, qmax));
+            q16[i] = o;
+        }
+    }
+    // tail (< 16 elements)
+    if (blockIdx.x == 0) {
+        const int64_t i = (nv << 4) + threadIdx.x;
+        if (threadIdx.x < 16 && i < n)
+            q[i] = (int8_t)(s == 0.f ? 0 : quant_one(x[i], s, qmax));
+    }
+}
+
+} // namespace
+
+cudaError_t launch_quant(const float* x, int64_t n, const float* scale, int qmax, int8_t* q,
+                         int grid, cudaStream_t st)
+{
+    k_quant<<<grid, 256, 0, st>>>(x, n, scale, qmax, q);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+} // namespace repro

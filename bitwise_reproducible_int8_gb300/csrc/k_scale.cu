@@ -1,0 +1,264 @@
+// k_scale.cu -- per-tensor scales.
+//
+// Weight scale (Open-1B review, onedev.kr/papers/92, sections "How to use" and
+// "Premises and limits": the step size is re-pinned from the weights every
+// optimiser step as 2*mean(|w|)/sqrt(q_max)).  The sum of |w| follows the
+// canonical order: chunks of 64 summed left to right, then the stride-doubling
+// pairwise tree over chunk partials.  The tree over any aligned block of 2^b
+// chunk partials is itself the canonical tree of that block, and the tree over
+// the block results (ragged last block included) completes the canonical tree,
+// so the reduction runs as one pass over HBM (phase 1: one CTA per aligned
+// block of chunks) plus tiny tree passes over the block partials.
+//
+// Activation scale: max|x| / q_max; the maximum is exact, so any order works.
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace repro {
+namespace {
+
+constexpr int P1_CHUNKS = 128;   // chunks (and threads) per phase-1 CTA
+constexpr int P2_MAX = 1024;     // partials (and threads) per tree-pass CTA
+
+// Phase 1: CTA b sums chunks [b*2^k, (b+1)*2^k) (k <= 7) and reduces their
+// partials with the stride-doubling tree.  The CTA's slice of x is staged in
+// shared memory with coalesced 16-byte loads; chunk j's 16 float4 are stored
+// XOR-swizzled (slot p ^ (j & 15)) so both the fill and the per-thread reads
+// are free of bank conflicts.
+__global__ void __launch_bounds__(P1_CHUNKS)
+k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __restrict__ part)
+{
+    __shared__ float4 S[P1_CHUNKS * 16];
+    __shared__ float T[P1_CHUNKS];
+    const int nb = 1 << blk_log2;
+    const int64_t C = (n + 63) >> 6;
+    const int64_t c0 = (int64_t)blockIdx.x * nb;
+    const int cnt = (int)min((int64_t)nb, C - c0);
+    const int64_t e0 = c0 * 64;
+
+    for (int g = threadIdx.x; g < cnt * 16; g += blockDim.x) {
+        const int ch = g >> 4, p = g & 15;
+        const int64_t e = e0 + (int64_t)g * 4;
+        float4 v;
+        if (e + 4 <= n) {
+            v = __ldg(reinterpret_cast<const float4*>(x + e));
+        } else {
+            v.x = (e + 0 < n) ? x[e + 0] : 0.f;
+            v.y = (e + 1 < n) ? x[e + 1] : 0.f;
+            v.z = (e + 2 < n) ? x[e + 2] : 0.f;
+            v.w = (e + 3 < n) ? x[e + 3] : 0.f;
+        }
+        S[ch * 16 + (p ^ (ch & 15))] = v;
+    }
+    __syncthreads();
+
+    for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
+        const int64_t lo = e0 + (int64_t)j * 64;
+        const int len = (int)min((int64_t)64, n - lo);
+        float a;
+        if (len == 64) {
+            float4 v = S[j * 16 + (0 ^ (j & 15))];
+            a = fabsf(v.x);
+            a = fadd_ftz(a, fabsf(v.y));
+            a = fadd_ftz(a, fabsf(v.z));
+            a = fadd_ftz(a, fabsf(v.w));
+#pragma unroll
+            for (int p = 1; p < 16; ++p) {
+                v = S[j * 16 + (p ^ (j & 15))];
+                a = fadd_ftz(a, fabsf(v.x));
+                a = fadd_ftz(a, fabsf(v.y));
+                a = fadd_ftz(a, fabsf(v.z));
+                a = fadd_ftz(a, fabsf(v.w));
+            }
+        } else {
+            a = 0.f;
+            for (int i = 0; i < len; ++i) {
+                const float4 v = S[j * 16 + ((i >> 2) ^ (j & 15))];
+                const int u = i & 3;
+                const float t = fabsf(u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w);
+                a = (i == 0) ? t : fadd_ftz(a, t);
+            }
+        }
+        T[j] = a;
+    }
+    __syncthreads();
+
+    for (int s = 1; s < cnt; s <<= 1) {
+        const int j = threadIdx.x * 2 * s;
+        if (j + s < cnt)
+            T[j] = fadd_ftz(T[j], T[j + s]);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        part[blockIdx.x] = T[0];
+}
+
+// s_w = (2 (x) (S (/) float(n))) (/) sqrt(float(q_max)); every operand and
+// result flushed
+__device__ float weight_scale_from_sum(float S, int64_t n, int qmax)
+{
+    const float mean = flush(__fdiv_rn(flush(S), __ll2float_rn(n)));
+    const float twice = fmul_flush(2.0f, mean);
+    const float root = flush(__fsqrt_rn(__int2float_rn(qmax)));
+    return flush(__fdiv_rn(twice, root));
+}
+
+// Tree pass: CTA b reduces partials [b*2^k, (b+1)*2^k) of `in` with the
+// stride-doubling tree.  With one CTA left it finishes the weight scale.
+__global__ void __launch_bounds__(P2_MAX)
+k_tree_pass(const float* __restrict__ in, int64_t cnt_total, int blk_log2,
+            float* __restrict__ out, int final_pass, int64_t n, int qmax,
+            float* __restrict__ scale_out)
+{
+    __shared__ float T[P2_MAX];
+    const int nb = 1 << blk_log2;
+    const int64_t b0 = (int64_t)blockIdx.x * nb;
+    const int cnt = (int)min((int64_t)nb, cnt_total - b0);
+    for (int j = threadIdx.x; j < cnt; j += blockDim.x)
+        T[j] = in[b0 + j];
+    __syncthreads();
+    for (int s = 1; s < cnt; s <<= 1) {
+        for (int j = threadIdx.x * 2 * s; j + s < cnt; j += blockDim.x * 2 * s)
+            T[j] = fadd_ftz(T[j], T[j + s]);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        if (final_pass)
+            scale_out[0] = weight_scale_from_sum(T[0], n, qmax);
+        else
+            out[blockIdx.x] = T[0];
+    }
+}
+
+// ---------------------------------------------------------------- amax
+
+__device__ __forceinline__ float absflush(float v)
+{
+    v = fabsf(v);
+    return v < FLT_MIN ? 0.f : v;
+}
+
+__global__ void __launch_bounds__(256)
+k_amax_partial(const float* __restrict__ x, int64_t n, float* __restrict__ part)
+{
+    float m = 0.f;
+    const int64_t nv = n >> 2;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 v = __ldg(x4 + i);
+        m = fmaxf(m, fmaxf(fmaxf(absflush(v.x), absflush(v.y)), fmaxf(absflush(v.z), absflush(v.w))));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 3))
+        m = fmaxf(m, absflush(x[(nv << 2) + threadIdx.x]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float W[8];
+    if ((threadIdx.x & 31) == 0)
+        W[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+            m = fmaxf(m, W[w]);
+        part[blockIdx.x] = m;
+    }
+}
+
+__global__ void __launch_bounds__(1024)
+k_amax_final(const float* __restrict__ part, int cnt, int qmax, float* __restrict__ scale_out)
+{
+    float m = 0.f;
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x)
+        m = fmaxf(m, part[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float W[32];
+    if ((threadIdx.x & 31) == 0)
+        W[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+            m = fmaxf(m, W[w]);
+        scale_out[0] = flush(__fdiv_rn(m, __int2float_rn(qmax)));
+    }
+}
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+} // namespace
+
+// Phase-1 block of 2^min(k,7) chunks, tree passes of 2^max(k,1) partials
+// (capped at 1024).  Workspace: phase-1 partials, then the first tree pass's
+// output; later passes ping-pong between the two regions (they only shrink).
+static void split_blocks(int block_log2, int& p1_log2, int& p2_log2)
+{
+    if (block_log2 < 0) {   // default: 128-chunk CTAs, 1024-partial tree passes
+        p1_log2 = 7;
+        p2_log2 = 10;
+        return;
+    }
+    p1_log2 = block_log2 < 7 ? block_log2 : 7;
+    p2_log2 = block_log2 < 1 ? 1 : (block_log2 > 10 ? 10 : block_log2);
+}
+
+size_t wscale_ws_bytes(int64_t n, int block_log2)
+{
+    int p1, p2;
+    split_blocks(block_log2, p1, p2);
+    const int64_t C = cdiv(n, 64);
+    const int64_t c1 = cdiv(C, (int64_t)1 << p1);
+    const int64_t c2 = cdiv(c1, (int64_t)1 << p2);
+    return (size_t)(c1 + c2 + 64) * sizeof(float);
+}
+
+cudaError_t launch_wscale_meanabs(const float* x, int64_t n, int qmax, float* scale_out,
+                                  void* ws, int block_log2, cudaStream_t st)
+{
+    int p1, p2;
+    split_blocks(block_log2, p1, p2);
+    const int64_t C = cdiv(n, 64);
+    int64_t cnt = cdiv(C, (int64_t)1 << p1);
+    float* regA = static_cast<float*>(ws);
+    float* regB = regA + cnt + 32;
+    k_absum_chunks<<<(unsigned)cnt, P1_CHUNKS, 0, st>>>(x, n, p1, regA);
+    count_launches(1);
+    float* src = regA;
+    float* dst = regB;
+    for (;;) {
+        const int64_t grid = cdiv(cnt, (int64_t)1 << p2);
+        const int final_pass = grid == 1;
+        k_tree_pass<<<(unsigned)grid, P2_MAX, 0, st>>>(src, cnt, p2, dst, final_pass, n, qmax,
+                                                       scale_out);
+        count_launches(1);
+        if (final_pass)
+            break;
+        cnt = grid;
+        float* t = src;
+        src = dst;
+        dst = t;
+    }
+    return cudaGetLastError();
+}
+
+int amax_grid(int64_t n)
+{
+    const int64_t want = cdiv(n, 256 * 4 * 4);
+    const int64_t cap = (int64_t)num_sms() * 4;
+    return (int)(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+cudaError_t launch_wscale_amax(const float* x, int64_t n, int qmax, float* scale_out, void* ws,
+                               int grid, cudaStream_t st)
+{
+    float* part = static_cast<float*>(ws);
+    k_amax_partial<<<grid, 256, 0, st>>>(x, n, part);
+    k_amax_final<<<1, 1024, 0, st>>>(part, grid, qmax, scale_out);
+    count_launches(2);
+    return cudaGetLastError();
+}
+
+} // namespace repro

@@ -38,9 +38,13 @@ def _threads() -> int:
         return max(1, min(32, os.cpu_count() or 1))
 
 
-def normal(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
-    """float32 N(0, std^2) samples, reproducible for (seed, stream, shape)."""
+def normal(seed: int, stream: int, shape, std: float = 1.0, rows: int | None = None) -> np.ndarray:
+    """float32 N(0, std^2) samples, reproducible for (seed, stream, shape).
+    With `rows`, only the first `rows` rows are drawn: the same bytes as the
+    leading rows of the full tensor."""
     shape = tuple(int(s) for s in shape)
+    if rows is not None:
+        shape = (min(int(rows), shape[0]),) + shape[1:]
     n = int(np.prod(shape)) if shape else 1
     out = np.empty(n, dtype=np.float32)
     nblk = (n + BLOCK - 1) // BLOCK
@@ -61,10 +65,10 @@ def normal(seed: int, stream: int, shape, std: float = 1.0) -> np.ndarray:
     return out.reshape(shape)
 
 
-def silu_times_normal(seed: int, shape) -> np.ndarray:
+def silu_times_normal(seed: int, shape, rows: int | None = None) -> np.ndarray:
     """SiLU(a) * b with a, b ~ N(0, 1), in fp32 (the down projection's input)."""
-    a = normal(seed, S_A, shape)
-    b = normal(seed, S_B, shape)
+    a = normal(seed, S_A, shape, rows=rows)
+    b = normal(seed, S_B, shape, rows=rows)
     # SiLU(a) = a / (1 + exp(-a)), evaluated in fp32 on the host
     with np.errstate(over="ignore"):
         s = a / (np.float32(1.0) + np.exp(-a))
@@ -123,18 +127,18 @@ def weight(wl: Workload, i: int) -> np.ndarray:
     return normal(wl.w_seed_base + i, S_W, (lin.n_out, lin.k_in), 0.02)
 
 
-def activation(wl: Workload, i: int, mb: int) -> np.ndarray:
+def activation(wl: Workload, i: int, mb: int, rows: int | None = None) -> np.ndarray:
     lin = wl.linears[i]
     seed = wl.x_seed_base + mb
     if lin.silu_input:
-        return silu_times_normal(seed * 16 + i, (wl.tokens, lin.k_in))
-    return normal(seed * 16 + i, S_X, (wl.tokens, lin.k_in), 1.0)
+        return silu_times_normal(seed * 16 + i, (wl.tokens, lin.k_in), rows=rows)
+    return normal(seed * 16 + i, S_X, (wl.tokens, lin.k_in), 1.0, rows=rows)
 
 
-def upstream_grad(wl: Workload, i: int, mb: int) -> np.ndarray:
+def upstream_grad(wl: Workload, i: int, mb: int, rows: int | None = None) -> np.ndarray:
     lin = wl.linears[i]
     seed = wl.x_seed_base + mb
-    return normal(seed * 16 + i, S_DY, (wl.tokens, lin.n_out), 1e-3)
+    return normal(seed * 16 + i, S_DY, (wl.tokens, lin.n_out), 1e-3, rows=rows)
 
 
 def replica_noise(wl: Workload, r: int, n: int) -> np.ndarray:

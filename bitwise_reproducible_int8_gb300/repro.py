@@ -1,0 +1,229 @@
+"""Thin Python binding of librepro.so (include/repro.h): argument marshalling
+only.  Every step of the path runs in the library's CUDA kernels; torch is used
+for device memory and streams.  There is no fallback: if the library is not
+built, or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "librepro.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "repro.h")
+
+REPRO_OK = 0
+STATUS_NAMES = {
+    0: "REPRO_OK", -1: "REPRO_ERR_ARG", -2: "REPRO_ERR_SHAPE", -3: "REPRO_ERR_ALIGN",
+    -4: "REPRO_ERR_ARCH", -5: "REPRO_ERR_LAUNCH", -6: "REPRO_ERR_TIMEOUT",
+    -7: "REPRO_ERR_WORKSPACE", -8: "REPRO_ERR_ALIAS",
+}
+REPRO_SCALE_WEIGHT_MEANABS = 0
+REPRO_SCALE_ACT_AMAX = 1
+REPRO_BWD_DW_ACCUMULATE = 1
+REPRO_QMAX = 127
+REPRO_MAX_REPLICAS = 64
+
+
+class ReproError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS_NAMES.get(status, status)} "
+                         f"({lib().repro_status_str(status).decode()})")
+
+
+class LaunchCfg(ctypes.Structure):
+    _fields_ = [("bwd_segment_log2", ctypes.c_int), ("reduce_block_log2", ctypes.c_int),
+                ("fwd_path", ctypes.c_int), ("elementwise_blocks", ctypes.c_int)]
+
+
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "repro_wscale": (_int, [_vp, _i64, _int, _int, _vp, _vp, _sz, _vp]),
+    "repro_wscale_ws_bytes": (_sz, [_i64]),
+    "repro_quant_i8": (_int, [_vp, _i64, _vp, _int, _vp, _vp]),
+    "repro_linear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "repro_linear_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int,
+                                _vp, _sz, _vp]),
+    "repro_linear_bwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
+    "repro_grad_accum": (_int, [_vp, _vp, _i64, _vp]),
+    "repro_treefold": (_int, [ctypes.POINTER(_vp), _int, _i64, _vp, _vp]),
+    "repro_status_str": (ctypes.c_char_p, [_int]),
+    "repro_version": (_int, []),
+    "repro_device_check": (_int, [_vp]),
+    "repro_launch_count": (ctypes.c_uint64, []),
+    "repro_set_launch_cfg": (_int, [ctypes.POINTER(LaunchCfg)]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "bitwise_reproducible_int8_gb300.build_lib.build() (there is no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def declared_functions() -> list:
+    """Names of the functions declared in include/repro.h."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int|size_t|uint64_t)\s+(repro_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != REPRO_OK:
+        raise ReproError(fn, status)
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ the calls
+
+def repro_wscale_ws_bytes(n: int) -> int:
+    return int(lib().repro_wscale_ws_bytes(int(n)))
+
+
+def repro_wscale(x: torch.Tensor, mode: int, scale_out: torch.Tensor, ws=None,
+                 qmax: int = REPRO_QMAX, stream=None) -> None:
+    """scale_out[0] <- weight (mode 0) or activation (mode 1) scale of x."""
+    n = x.numel()
+    if ws is None:
+        ws = _workspace(repro_wscale_ws_bytes(n), x.device)
+    _check("repro_wscale", lib().repro_wscale(
+        _ptr(x, torch.float32, "x"), n, int(mode), int(qmax),
+        _ptr(scale_out, torch.float32, "scale_out"), _ptr(ws, None, "ws"),
+        ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 1 << 62,
+        _stream(stream)))
+
+
+def repro_quant_i8(x: torch.Tensor, scale: torch.Tensor, q_out: torch.Tensor,
+                   qmax: int = REPRO_QMAX, stream=None) -> None:
+    if q_out.numel() != x.numel():
+        raise ValueError("q_out must have as many elements as x")
+    _check("repro_quant_i8", lib().repro_quant_i8(
+        _ptr(x, torch.float32, "x"), x.numel(), _ptr(scale, torch.float32, "scale"), int(qmax),
+        _ptr(q_out, torch.int8, "q_out"), _stream(stream)))
+
+
+def repro_linear_fwd(xq: torch.Tensor, wq: torch.Tensor, s_x: torch.Tensor, s_w: torch.Tensor,
+                     y: torch.Tensor, stream=None) -> None:
+    M, K = xq.shape
+    N, K2 = wq.shape
+    if K != K2 or tuple(y.shape) != (M, N):
+        raise ValueError("shape mismatch: xq [M,K], wq [N,K], y [M,N]")
+    _check("repro_linear_fwd", lib().repro_linear_fwd(
+        _ptr(xq, torch.int8, "xq"), _ptr(wq, torch.int8, "wq"), _ptr(s_x, torch.float32, "s_x"),
+        _ptr(s_w, torch.float32, "s_w"), _ptr(y, torch.float32, "y"), M, N, K, _stream(stream)))
+
+
+def repro_linear_bwd_ws_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().repro_linear_bwd_ws_bytes(int(M), int(N), int(K)))
+
+
+def repro_linear_bwd(dy: torch.Tensor, xq, wq, s_x, s_w, dx=None, dw=None,
+                     accumulate: bool = False, ws=None, stream=None) -> None:
+    M, N = dy.shape
+    K = (xq if xq is not None else wq).shape[1]
+    if dx is not None and tuple(dx.shape) != (M, K):
+        raise ValueError("dx must be [M,K]")
+    if dw is not None and tuple(dw.shape) != (N, K):
+        raise ValueError("dw must be [N,K]")
+    if ws is None:
+        need = repro_linear_bwd_ws_bytes(M, N, K)
+        ws = _workspace(need, dy.device) if need > 0 else None
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check("repro_linear_bwd", lib().repro_linear_bwd(
+        _ptr(dy, torch.float32, "dy"), _ptr(xq, torch.int8, "xq"), _ptr(wq, torch.int8, "wq"),
+        _ptr(s_x, torch.float32, "s_x"), _ptr(s_w, torch.float32, "s_w"),
+        _ptr(dx, torch.float32, "dx"), _ptr(dw, torch.float32, "dw"), M, N, K,
+        REPRO_BWD_DW_ACCUMULATE if accumulate else 0, _ptr(ws, None, "ws"), ws_bytes,
+        _stream(stream)))
+
+
+def repro_grad_accum(acc: torch.Tensor, g: torch.Tensor, stream=None) -> None:
+    if acc.numel() != g.numel():
+        raise ValueError("acc and g must have the same number of elements")
+    _check("repro_grad_accum", lib().repro_grad_accum(
+        _ptr(acc, torch.float32, "acc"), _ptr(g, torch.float32, "g"), acc.numel(),
+        _stream(stream)))
+
+
+def repro_treefold(parts, out: torch.Tensor, stream=None) -> None:
+    R = len(parts)
+    n = out.numel()
+    if any(p.numel() != n for p in parts):
+        raise ValueError("every partial must have out.numel() elements")
+    arr = (_vp * max(R, 1))(*[_ptr(p, torch.float32, "part") for p in parts])
+    _check("repro_treefold", lib().repro_treefold(arr, R, n, _ptr(out, torch.float32, "out"),
+                                                  _stream(stream)))
+
+
+def repro_status_str(status: int) -> str:
+    return lib().repro_status_str(int(status)).decode()
+
+
+def repro_version() -> int:
+    return int(lib().repro_version())
+
+
+def repro_launch_count() -> int:
+    return int(lib().repro_launch_count())
+
+
+def repro_device_check(stream=None) -> int:
+    return int(lib().repro_device_check(_stream(stream)))
+
+
+def repro_set_launch_cfg(bwd_segment_log2: int = -1, reduce_block_log2: int = -1,
+                         fwd_path: int = -1, elementwise_blocks: int = -1, reset: bool = False):
+    if reset:
+        _check("repro_set_launch_cfg", lib().repro_set_launch_cfg(None))
+        return
+    cfg = LaunchCfg(bwd_segment_log2, reduce_block_log2, fwd_path, elementwise_blocks)
+    _check("repro_set_launch_cfg", lib().repro_set_launch_cfg(ctypes.byref(cfg)))

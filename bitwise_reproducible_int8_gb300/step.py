@@ -1,0 +1,197 @@
+"""One step of the hot path over a workload, through the C ABI.
+
+A step is, for every linear of the workload:
+  re-pin the weight scale and quantise the weights (once per step);
+then for every micro-batch j and linear i:
+  activation scale -> quantise X -> int8 forward -> dX -> dW, with dW
+  accumulated into the linear's gradient in micro-batch order (level 1 of the
+  replayed reduction);
+and finally, when the workload has R > 1 replicas, TreeFold of the flat
+gradient buffer with the R - 1 other replicas' partials (level 3).
+
+The other replicas' partials are built once, outside any timed region, as
+P_r = G (+) noise_r from this replica's accumulated gradient G -- the same
+construction as the small single-linear case -- so that every step folds six
+real-sized, gradient-like buffers.  All arithmetic happens in librepro.so; this
+module only allocates device memory (torch) and enqueues calls.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import inputs
+from . import repro as R
+
+
+@dataclass
+class HostInputs:
+    W: list          # [i] -> np.float32 [N_i, K_i]
+    X: list          # [i][j] -> np.float32 [M, K_i]
+    dY: list         # [i][j] -> np.float32 [M, N_i]
+    noise: list      # [r] -> np.float32 [sum N_i K_i]  (r = 1..R-1; index 0 unused)
+
+
+def generate_host_inputs(wl: inputs.Workload) -> HostInputs:
+    L = len(wl.linears)
+    W = [inputs.weight(wl, i) for i in range(L)]
+    X = [[inputs.activation(wl, i, j) for j in range(wl.microbatches)] for i in range(L)]
+    dY = [[inputs.upstream_grad(wl, i, j) for j in range(wl.microbatches)] for i in range(L)]
+    n_grad = sum(l.n_out * l.k_in for l in wl.linears)
+    noise = [None] + [inputs.replica_noise(wl, r, n_grad) for r in range(1, max(wl.replicas, 1))]
+    return HostInputs(W, X, dY, noise)
+
+
+def grad_offsets(wl: inputs.Workload):
+    offs, o = [], 0
+    for l in wl.linears:
+        offs.append(o)
+        o += l.n_out * l.k_in
+    return offs, o
+
+
+class HotPathStep:
+    """Device buffers for one workload and the calls of one step."""
+
+    CLASSES = ("wscale_w", "quant_w", "wscale_x", "quant_x", "fwd", "bwd_dx", "bwd_dw",
+               "accum", "treefold")
+
+    def __init__(self, wl: inputs.Workload, host: HostInputs | None = None,
+                 fused_accum: bool = True, device: str = "cuda"):
+        self.wl = wl
+        self.fused_accum = fused_accum
+        self.host = host if host is not None else generate_host_inputs(wl)
+        dev = torch.device(device)
+        self.dev = dev
+        L, J, M = len(wl.linears), wl.microbatches, wl.tokens
+        h = self.host
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        self.W = [t(h.W[i]) for i in range(L)]
+        self.X = [[t(h.X[i][j]) for j in range(J)] for i in range(L)]
+        self.dY = [[t(h.dY[i][j]) for j in range(J)] for i in range(L)]
+        self.Wq = [torch.empty(w.shape, dtype=torch.int8, device=dev) for w in self.W]
+        self.Xq = [torch.empty((M, l.k_in), dtype=torch.int8, device=dev) for l in wl.linears]
+        self.s_w = torch.zeros(L, dtype=torch.float32, device=dev)
+        self.s_x = torch.zeros(L, dtype=torch.float32, device=dev)
+        self.Y = [torch.empty((M, l.n_out), dtype=torch.float32, device=dev) for l in wl.linears]
+        self.dX = [torch.empty((M, l.k_in), dtype=torch.float32, device=dev) for l in wl.linears]
+        offs, n_grad = grad_offsets(wl)
+        self.n_grad = n_grad
+        self.G = torch.empty(n_grad, dtype=torch.float32, device=dev)
+        self.Gv = [self.G[o:o + l.n_out * l.k_in].view(l.n_out, l.k_in)
+                   for o, l in zip(offs, wl.linears)]
+        self.dW_tmp = None
+        if not fused_accum and J > 1:
+            self.dW_tmp = [torch.empty((l.n_out, l.k_in), dtype=torch.float32, device=dev)
+                           for l in wl.linears]
+        n_max = max(max(w.numel() for w in self.W), max(x.numel() for x in self.X[0]))
+        n_max = max(n_max, *(x.numel() for i in range(L) for x in self.X[i]))
+        self.ws_scale = torch.empty(max(R.repro_wscale_ws_bytes(n_max), 16), dtype=torch.uint8,
+                                    device=dev)
+        need = max(R.repro_linear_bwd_ws_bytes(M, l.n_out, l.k_in) for l in wl.linears)
+        self.ws_bwd = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+        self.parts = None
+        self.TF = None
+        if wl.replicas > 1:
+            self.TF = torch.empty(n_grad, dtype=torch.float32, device=dev)
+
+    # ------------------------------------------------------------------ step
+
+    def _ev(self, timers, cls, stream):
+        if timers is None:
+            return None
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        timers.setdefault(cls, []).append([e, None])
+        return e
+
+    def _end(self, timers, cls, stream):
+        if timers is None:
+            return
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        timers[cls][-1][1] = e
+
+    def run(self, stream: torch.cuda.Stream, timers: dict | None = None,
+            wait_events: list | None = None) -> None:
+        """Enqueue one step on `stream`.  With `timers`, records a CUDA event
+        pair around every call, grouped by call class.  `wait_events[j]`, if
+        given, is waited on before micro-batch j's first use of its inputs."""
+        wl, s = self.wl, stream
+        L, J = len(wl.linears), wl.microbatches
+        sw = lambda i: self.s_w[i:i + 1]  # noqa: E731
+        sx = lambda i: self.s_x[i:i + 1]  # noqa: E731
+        if wait_events is not None and wait_events[0] is not None:
+            s.wait_event(wait_events[0])
+        for i in range(L):
+            self._ev(timers, "wscale_w", s)
+            R.repro_wscale(self.W[i], R.REPRO_SCALE_WEIGHT_MEANABS, sw(i), ws=self.ws_scale,
+                           stream=s)
+            self._end(timers, "wscale_w", s)
+            self._ev(timers, "quant_w", s)
+            R.repro_quant_i8(self.W[i], sw(i), self.Wq[i], stream=s)
+            self._end(timers, "quant_w", s)
+        for j in range(J):
+            if wait_events is not None and j > 0 and wait_events[j] is not None:
+                s.wait_event(wait_events[j])
+            for i in range(L):
+                X, dY = self.X[i][j], self.dY[i][j]
+                self._ev(timers, "wscale_x", s)
+                R.repro_wscale(X, R.REPRO_SCALE_ACT_AMAX, sx(i), ws=self.ws_scale, stream=s)
+                self._end(timers, "wscale_x", s)
+                self._ev(timers, "quant_x", s)
+                R.repro_quant_i8(X, sx(i), self.Xq[i], stream=s)
+                self._end(timers, "quant_x", s)
+                self._ev(timers, "fwd", s)
+                R.repro_linear_fwd(self.Xq[i], self.Wq[i], sx(i), sw(i), self.Y[i], stream=s)
+                self._end(timers, "fwd", s)
+                self._ev(timers, "bwd_dx", s)
+                R.repro_linear_bwd(dY, None, self.Wq[i], None, sw(i), dx=self.dX[i], dw=None,
+                                   ws=self.ws_bwd, stream=s)
+                self._end(timers, "bwd_dx", s)
+                if j == 0 or self.fused_accum:
+                    self._ev(timers, "bwd_dw", s)
+                    R.repro_linear_bwd(dY, self.Xq[i], None, sx(i), None, dx=None,
+                                       dw=self.Gv[i], accumulate=j > 0, ws=self.ws_bwd, stream=s)
+                    self._end(timers, "bwd_dw", s)
+                else:
+                    self._ev(timers, "bwd_dw", s)
+                    R.repro_linear_bwd(dY, self.Xq[i], None, sx(i), None, dx=None,
+                                       dw=self.dW_tmp[i], ws=self.ws_bwd, stream=s)
+                    self._end(timers, "bwd_dw", s)
+                    self._ev(timers, "accum", s)
+                    R.repro_grad_accum(self.Gv[i], self.dW_tmp[i], stream=s)
+                    self._end(timers, "accum", s)
+        if self.TF is not None:
+            if self.parts is None:
+                raise RuntimeError("prepare_replicas() must run before a step with TreeFold")
+            self._ev(timers, "treefold", s)
+            R.repro_treefold([self.G] + self.parts, self.TF, stream=s)
+            self._end(timers, "treefold", s)
+
+    def prepare_replicas(self, stream: torch.cuda.Stream) -> None:
+        """P_r = G (+) noise_r for r = 1..R-1, from the current G (untimed)."""
+        if self.wl.replicas <= 1:
+            return
+        self.parts = []
+        for r in range(1, self.wl.replicas):
+            p = self.G.clone()
+            R.repro_grad_accum(p, torch.from_numpy(self.host.noise[r]).to(self.dev), stream=stream)
+            self.parts.append(p)
+
+    def result(self) -> torch.Tensor:
+        """The step's result: the folded gradient (or G without TreeFold)."""
+        return self.TF if self.TF is not None else self.G
+
+    def flops(self):
+        """Algorithmic work of one step: int8 MACs (forward) and fp32
+        multiplies+adds (backward), per call class."""
+        wl = self.wl
+        M, J = wl.tokens, wl.microbatches
+        mac = sum(M * l.n_out * l.k_in for l in wl.linears) * J
+        return {"fwd_int_ops": 2 * mac, "bwd_dx_fp32_ops": 2 * mac, "bwd_dw_fp32_ops": 2 * mac}
+
+    def tokens(self) -> int:
+        return self.wl.tokens * self.wl.microbatches

@@ -111,9 +111,9 @@ int repro_quant_i8(const float* x, int64_t n, const float* scale, int qmax,
  * exactly as an integer (so its order cannot matter), then
  * Y[m,n] = (float(acc) (x) s_x) (x) s_w -- two unfused multiplies, left to
  * right.  xq: M x K int8, wq: N x K int8 (nn.Linear layout), y: M x N float.
- * Requires K <= 133144 so that |acc| <= 127*127*K fits in int32
- * (REPRO_ERR_SHAPE otherwise).  M, N or K may be 0 (K == 0 writes +0 times
- * the scales).
+ * Requires K <= 133144 so that |acc| <= 127*127*K fits in int32, and
+ * M, N <= 4194240 (REPRO_ERR_SHAPE otherwise).  M, N or K may be 0 (K == 0
+ * writes +0 times the scales).
  * ------------------------------------------------------------------------ */
 int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x,
                      const float* s_w, float* y, int64_t M, int64_t N, int64_t K,
@@ -132,7 +132,9 @@ int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x,
  * flags: REPRO_BWD_DW_ACCUMULATE -- instead of storing dW, update
  *   dw[n,k] <- dw[n,k] (+) dW[n,k] (one add of the fully formed dW; the same
  *   bits as repro_grad_accum on a stored dW).
- * ws: at least repro_linear_bwd_ws_bytes(M, N, K) bytes (may be 0).
+ * ws: at least repro_linear_bwd_ws_bytes(M, N, K) bytes for the current
+ * launch configuration (0 by default whenever M and N are <= 16384).
+ * M, N <= 4194240 (REPRO_ERR_SHAPE otherwise).
  * dx and dw must not overlap dy, xq or wq (REPRO_ERR_ALIAS).
  * ------------------------------------------------------------------------ */
 #define REPRO_BWD_DW_ACCUMULATE 1
@@ -172,6 +174,8 @@ int repro_treefold(const float* const* parts, int R, int64_t n, float* out,
  * repro_device_check: synchronises `stream`, then reads and clears the
  *   device error word set by bounded device-side waits; returns REPRO_OK or
  *   REPRO_ERR_TIMEOUT (or REPRO_ERR_LAUNCH if the stream reported an error).
+ * repro_launch_count: number of kernels this library has enqueued in this
+ *   process (all devices, all streams); a diagnostic for counting launches.
  * repro_set_launch_cfg: test hook that changes how work is split across
  *   thread blocks (never the arithmetic); NULL restores the defaults.  Used
  *   to show that results do not depend on the launch configuration.  Not
@@ -187,6 +191,7 @@ typedef struct {
 const char* repro_status_str(int status);
 int repro_version(void);
 int repro_device_check(void* stream);
+uint64_t repro_launch_count(void);
 int repro_set_launch_cfg(const repro_launch_cfg* cfg);
 
 #ifdef __cplusplus

@@ -1,0 +1,140 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads and exports
+every function include/repro.h declares; invalid arguments are rejected with
+the documented status codes before anything is launched; workspace sizes and
+the launch-configuration hook behave as documented."""
+import ctypes
+
+import pytest
+
+from bitwise_reproducible_int8_gb300 import build_lib, repro
+
+
+@pytest.fixture(scope="module")
+def L():
+    build_lib.build()
+    return repro.lib()
+
+
+A = 0x10000  # a fake, 16-byte aligned device address (never dereferenced)
+
+
+def test_exports_every_declared_symbol(L):
+    names = repro.declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    for n in ["repro_wscale", "repro_quant_i8", "repro_linear_fwd", "repro_linear_bwd",
+              "repro_grad_accum", "repro_treefold"]:
+        assert n in names
+
+
+def test_status_strings_and_version(L):
+    assert repro.repro_version() == 1
+    for code in range(-8, 1):
+        assert repro.repro_status_str(code) != "unknown status"
+    assert repro.repro_status_str(-99) == "unknown status"
+
+
+def test_wscale_argument_checks(L):
+    f = L.repro_wscale
+    ws = A * 4
+    assert f(None, 10, 0, 127, A, ws, 1 << 20, None) == -1           # null x
+    assert f(A, 10, 2, 127, A + 64, ws, 1 << 20, None) == -1         # bad mode
+    assert f(A, 10, 0, 100, A + 64, ws, 1 << 20, None) == -1         # q_max
+    assert f(A, 0, 0, 127, A + 64, ws, 1 << 20, None) == -2          # empty
+    assert f(A + 4, 10, 0, 127, A + 64, ws, 1 << 20, None) == -3     # misaligned x
+    assert f(A, 10, 0, 127, A + 64, None, 0, None) == -7             # no workspace
+    assert f(A, 1 << 20, 0, 127, A + 64, ws, 16, None) == -7         # small workspace
+    assert f(A, 100, 0, 127, A + 64, A, 1 << 20, None) == -8         # ws overlaps x
+
+
+def test_wscale_ws_bytes_covers_all_blocks(L):
+    for n in [1, 64, 65, 10 ** 6, 23068672]:
+        C = (n + 63) // 64
+        assert repro.repro_wscale_ws_bytes(n) >= 4 * (C + (C + 1) // 2)
+    assert repro.repro_wscale_ws_bytes(0) == 0
+
+
+def test_quant_argument_checks(L):
+    f = L.repro_quant_i8
+    assert f(A, 10, A + 4096, 126, A * 2, None) == -1
+    assert f(A, -1, A + 4096, 127, A * 2, None) == -2
+    assert f(None, 0, None, 127, None, None) == 0                     # empty is a no-op
+    assert f(None, 10, A + 4096, 127, A * 2, None) == -1
+    assert f(A, 10, A + 4096, 127, A * 2 + 8, None) == -3             # misaligned q
+    assert f(A, 10, A + 4096, 127, A + 8, None) == -3
+    assert f(A, 100, A + 4096, 127, A + 16, None) == -8               # q inside x
+
+
+def test_linear_fwd_argument_checks(L):
+    f = L.repro_linear_fwd
+    assert f(A, A * 2, A * 3, A * 3 + 4, A * 4, 8, 8, 133145, None) == -2   # K too large
+    assert f(A, A * 2, A * 3, A * 3 + 4, A * 4, -1, 8, 8, None) == -2
+    assert f(None, None, None, None, None, 0, 8, 8, None) == 0              # M == 0
+    assert f(A, A * 2, None, A * 3, A * 4, 8, 8, 8, None) == -1             # null scale
+    assert f(A + 1, A * 2, A * 3, A * 3 + 4, A * 4, 8, 8, 8, None) == -3
+    assert f(A, A * 2, A * 3, A * 3 + 4, A, 8, 8, 8, None) == -8            # y overlaps xq
+
+
+def test_linear_bwd_argument_checks(L):
+    f = L.repro_linear_bwd
+    M = N = K = 8
+    args = lambda **k: [k.get("dy", A), k.get("xq", A * 2), k.get("wq", A * 3),  # noqa: E731
+                        k.get("sx", A * 4), k.get("sw", A * 4 + 4), k.get("dx", A * 5),
+                        k.get("dw", A * 6), M, N, K, k.get("flags", 0), None, 0, None]
+    assert f(*args(flags=2)) == -1
+    assert f(*args(dx=None, dw=None)) == -1
+    assert f(*args(wq=None)) == -1                       # dx wanted, wq missing
+    assert f(*args(xq=None)) == -1                       # dw wanted, xq missing
+    assert f(*args(dy=A + 8)) == -3
+    assert f(*args(dx=A)) == -8                          # dx overlaps dy
+    assert f(*args(dw=A * 5)) == -8                      # dx and dw overlap
+
+
+def test_bwd_workspace_follows_segments(L):
+    try:
+        assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 0
+        repro.repro_set_launch_cfg(bwd_segment_log2=4)
+        # dW: 256 chunks / 16 = 16 segments of N x K partials
+        assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 16 * 2048 * 2048 * 4
+        f = L.repro_linear_bwd
+        B = 1 << 32   # widely spaced fake addresses: nothing overlaps
+        assert f(B, B * 2, B * 3, B * 4, B * 4 + 4, B * 5, B * 6, 16384, 8, 8, 0, None, 0,
+                 None) == -7
+    finally:
+        repro.repro_set_launch_cfg(reset=True)
+
+
+def test_grad_accum_and_treefold_checks(L):
+    assert L.repro_grad_accum(A, A, 10, None) == -8
+    assert L.repro_grad_accum(A, A + 16, 10, None) == -8
+    assert L.repro_grad_accum(A + 4, A * 2, 10, None) == -3
+    assert L.repro_grad_accum(None, None, 0, None) == 0
+    P = ctypes.c_void_p
+    parts = (P * 3)(A, A * 2, A * 3)
+    assert L.repro_treefold(parts, 0, 10, A * 4, None) == -1
+    assert L.repro_treefold(parts, 65, 10, A * 4, None) == -1
+    assert L.repro_treefold(None, 3, 10, A * 4, None) == -1
+    assert L.repro_treefold(parts, 3, 10, A * 2, None) == -8          # out overlaps parts[1]
+    bad = (P * 3)(A, A * 2 + 4, A * 3)
+    assert L.repro_treefold(bad, 3, 10, A * 4, None) == -3
+    null = (P * 3)(A, None, A * 3)
+    assert L.repro_treefold(null, 3, 10, A * 4, None) == -1
+
+
+def test_launch_cfg_validation(L):
+    try:
+        with pytest.raises(repro.ReproError):
+            repro.repro_set_launch_cfg(bwd_segment_log2=9)
+        with pytest.raises(repro.ReproError):
+            repro.repro_set_launch_cfg(reduce_block_log2=11)
+        with pytest.raises(repro.ReproError):
+            repro.repro_set_launch_cfg(fwd_path=2)
+        repro.repro_set_launch_cfg(bwd_segment_log2=0, reduce_block_log2=0, fwd_path=0,
+                                   elementwise_blocks=152)
+    finally:
+        repro.repro_set_launch_cfg(reset=True)
+
+
+def test_launch_counter_readable(L):
+    assert repro.repro_launch_count() >= 0
