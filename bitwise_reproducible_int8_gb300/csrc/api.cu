@@ -11,7 +11,7 @@ namespace repro {
 
 namespace {
 
-LaunchCfg g_cfg = {-1, -1, -1, 0};
+LaunchCfg g_cfg = {-1, -1, -1, 0, 1};
 
 constexpr int kMaxDevices = 64;
 int g_arch_ok[kMaxDevices];   // 0 unknown, 1 GB300, -1 other
@@ -110,6 +110,12 @@ int stream_grid(int64_t work_items)
 
 int seg_log2() { return g_cfg.bwd_segment_log2 < 0 ? 8 : g_cfg.bwd_segment_log2; }
 
+// tensor-core forward only when the launch configuration selects it
+bool use_tc(int64_t M, int64_t N, int64_t K)
+{
+    return g_cfg.fwd_path == 1 && fwd_tc_supported(M, N, K);
+}
+
 } // namespace
 
 extern "C" {
@@ -137,7 +143,7 @@ uint64_t repro_launch_count(void) { return (uint64_t)__atomic_load_n(&g_launches
 int repro_set_launch_cfg(const repro_launch_cfg* cfg)
 {
     if (!cfg) {
-        g_cfg = LaunchCfg{-1, -1, -1, 0};
+        g_cfg = LaunchCfg{-1, -1, -1, 0, 1};
         return REPRO_OK;
     }
     if (cfg->bwd_segment_log2 < -1 || cfg->bwd_segment_log2 > 8)
@@ -148,10 +154,13 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
         return REPRO_ERR_ARG;
     if (cfg->elementwise_blocks < -1 || cfg->elementwise_blocks > (1 << 20))
         return REPRO_ERR_ARG;
+    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 1)
+        return REPRO_ERR_ARG;
     g_cfg.bwd_segment_log2 = cfg->bwd_segment_log2;
     g_cfg.reduce_block_log2 = cfg->reduce_block_log2;
     g_cfg.fwd_path = cfg->fwd_path;
     g_cfg.elementwise_blocks = cfg->elementwise_blocks < 0 ? 0 : cfg->elementwise_blocks;
+    g_cfg.bwd_kernel = cfg->bwd_kernel < 0 ? 1 : cfg->bwd_kernel;
     return REPRO_OK;
 }
 
@@ -227,8 +236,16 @@ int repro_quant_i8(const float* x, int64_t n, const float* scale, int qmax, int8
     return status_of(launch_quant(x, n, scale, qmax, q_out, stream_grid(n / 16), as_stream(stream)));
 }
 
+size_t repro_linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K)
+{
+    if (!use_tc(M, N, K))
+        return 0;
+    return fwd_tc_ws_bytes(M, N, K);
+}
+
 int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x, const float* s_w,
-                     float* y, int64_t M, int64_t N, int64_t K, void* stream)
+                     float* y, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                     void* stream)
 {
     if (M < 0 || N < 0 || K < 0 || K > 133144 || M > kMaxRows || N > kMaxRows)
         return REPRO_ERR_SHAPE;
@@ -242,9 +259,23 @@ int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x, const
     if (overlap(y, ybytes, xq, (size_t)(M * K)) || overlap(y, ybytes, wq, (size_t)(N * K)) ||
         overlap(y, ybytes, s_x, 4) || overlap(y, ybytes, s_w, 4))
         return REPRO_ERR_ALIAS;
+    const bool tc = use_tc(M, N, K);
+    if (tc) {
+        const size_t need = fwd_tc_ws_bytes(M, N, K);
+        if (!ws || ws_bytes < need)
+            return REPRO_ERR_WORKSPACE;
+        if (!al16(ws))
+            return REPRO_ERR_ALIGN;
+        if (overlap(ws, ws_bytes, y, ybytes) || overlap(ws, ws_bytes, xq, (size_t)(M * K)) ||
+            overlap(ws, ws_bytes, wq, (size_t)(N * K)) || overlap(ws, ws_bytes, s_x, 4) ||
+            overlap(ws, ws_bytes, s_w, 4))
+            return REPRO_ERR_ALIAS;
+    }
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    if (tc)
+        return status_of(launch_fwd_tc(xq, wq, s_x, s_w, y, M, N, K, ws, as_stream(stream)));
     return status_of(launch_fwd_cuda_core(xq, wq, s_x, s_w, y, M, N, K, as_stream(stream)));
 }
 

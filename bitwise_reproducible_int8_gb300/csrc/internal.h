@@ -15,6 +15,7 @@ struct LaunchCfg {
     int reduce_block_log2;  // chunk partials per block in the scale reduction (0..10)
     int fwd_path;           // 0: CUDA-core exact path, 1: tensor-core path
     int elementwise_blocks; // 0: default grid for streaming kernels
+    int bwd_kernel;         // 0: plain backward kernel, 1: pipelined packed kernel
 };
 
 const LaunchCfg& launch_cfg();
@@ -38,6 +39,12 @@ cudaError_t launch_quant(const float* x, int64_t n, const float* scale, int qmax
 cudaError_t launch_fwd_cuda_core(const int8_t* xq, const int8_t* wq, const float* s_x,
                                  const float* s_w, float* y, int64_t M, int64_t N, int64_t K,
                                  cudaStream_t st);
+
+// ---- forward on tensor cores (k_fwd_tc.cu)
+bool fwd_tc_supported(int64_t M, int64_t N, int64_t K);
+size_t fwd_tc_ws_bytes(int64_t M, int64_t N, int64_t K);
+cudaError_t launch_fwd_tc(const int8_t* xq, const int8_t* wq, const float* s_x, const float* s_w,
+                          float* y, int64_t M, int64_t N, int64_t K, void* ws, cudaStream_t st);
 
 // ---- backward (k_bwd.cu)
 size_t bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int seg_log2);

@@ -37,7 +37,8 @@ class ReproError(RuntimeError):
 
 class LaunchCfg(ctypes.Structure):
     _fields_ = [("bwd_segment_log2", ctypes.c_int), ("reduce_block_log2", ctypes.c_int),
-                ("fwd_path", ctypes.c_int), ("elementwise_blocks", ctypes.c_int)]
+                ("fwd_path", ctypes.c_int), ("elementwise_blocks", ctypes.c_int),
+                ("bwd_kernel", ctypes.c_int)]
 
 
 _vp = ctypes.c_void_p
@@ -49,7 +50,8 @@ _SIGNATURES = {
     "repro_wscale": (_int, [_vp, _i64, _int, _int, _vp, _vp, _sz, _vp]),
     "repro_wscale_ws_bytes": (_sz, [_i64]),
     "repro_quant_i8": (_int, [_vp, _i64, _vp, _int, _vp, _vp]),
-    "repro_linear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "repro_linear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "repro_linear_fwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
     "repro_linear_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int,
                                 _vp, _sz, _vp]),
     "repro_linear_bwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
@@ -151,15 +153,24 @@ def repro_quant_i8(x: torch.Tensor, scale: torch.Tensor, q_out: torch.Tensor,
         _ptr(q_out, torch.int8, "q_out"), _stream(stream)))
 
 
+def repro_linear_fwd_ws_bytes(M: int, N: int, K: int) -> int:
+    return int(lib().repro_linear_fwd_ws_bytes(int(M), int(N), int(K)))
+
+
 def repro_linear_fwd(xq: torch.Tensor, wq: torch.Tensor, s_x: torch.Tensor, s_w: torch.Tensor,
-                     y: torch.Tensor, stream=None) -> None:
+                     y: torch.Tensor, ws=None, stream=None) -> None:
     M, K = xq.shape
     N, K2 = wq.shape
     if K != K2 or tuple(y.shape) != (M, N):
         raise ValueError("shape mismatch: xq [M,K], wq [N,K], y [M,N]")
+    if ws is None:
+        need = repro_linear_fwd_ws_bytes(M, N, K)
+        ws = _workspace(need, y.device) if need > 0 else None
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check("repro_linear_fwd", lib().repro_linear_fwd(
         _ptr(xq, torch.int8, "xq"), _ptr(wq, torch.int8, "wq"), _ptr(s_x, torch.float32, "s_x"),
-        _ptr(s_w, torch.float32, "s_w"), _ptr(y, torch.float32, "y"), M, N, K, _stream(stream)))
+        _ptr(s_w, torch.float32, "s_w"), _ptr(y, torch.float32, "y"), M, N, K,
+        _ptr(ws, None, "ws"), ws_bytes, _stream(stream)))
 
 
 def repro_linear_bwd_ws_bytes(M: int, N: int, K: int) -> int:
@@ -221,9 +232,10 @@ def repro_device_check(stream=None) -> int:
 
 
 def repro_set_launch_cfg(bwd_segment_log2: int = -1, reduce_block_log2: int = -1,
-                         fwd_path: int = -1, elementwise_blocks: int = -1, reset: bool = False):
+                         fwd_path: int = -1, elementwise_blocks: int = -1, bwd_kernel: int = -1,
+                         reset: bool = False):
     if reset:
         _check("repro_set_launch_cfg", lib().repro_set_launch_cfg(None))
         return
-    cfg = LaunchCfg(bwd_segment_log2, reduce_block_log2, fwd_path, elementwise_blocks)
+    cfg = LaunchCfg(bwd_segment_log2, reduce_block_log2, fwd_path, elementwise_blocks, bwd_kernel)
     _check("repro_set_launch_cfg", lib().repro_set_launch_cfg(ctypes.byref(cfg)))

@@ -92,6 +92,8 @@ class HotPathStep:
                                     device=dev)
         need = max(R.repro_linear_bwd_ws_bytes(M, l.n_out, l.k_in) for l in wl.linears)
         self.ws_bwd = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+        need = max(R.repro_linear_fwd_ws_bytes(M, l.n_out, l.k_in) for l in wl.linears)
+        self.ws_fwd = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
         self.parts = None
         self.TF = None
         if wl.replicas > 1:
@@ -145,7 +147,8 @@ class HotPathStep:
                 R.repro_quant_i8(X, sx(i), self.Xq[i], stream=s)
                 self._end(timers, "quant_x", s)
                 self._ev(timers, "fwd", s)
-                R.repro_linear_fwd(self.Xq[i], self.Wq[i], sx(i), sw(i), self.Y[i], stream=s)
+                R.repro_linear_fwd(self.Xq[i], self.Wq[i], sx(i), sw(i), self.Y[i],
+                                   ws=self.ws_fwd, stream=s)
                 self._end(timers, "fwd", s)
                 self._ev(timers, "bwd_dx", s)
                 R.repro_linear_bwd(dY, None, self.Wq[i], None, sw(i), dx=self.dX[i], dw=None,

@@ -114,10 +114,15 @@ int repro_quant_i8(const float* x, int64_t n, const float* scale, int qmax,
  * Requires K <= 133144 so that |acc| <= 127*127*K fits in int32, and
  * M, N <= 4194240 (REPRO_ERR_SHAPE otherwise).  M, N or K may be 0 (K == 0
  * writes +0 times the scales).
+ * When K is a multiple of 8 the product runs on the tensor cores from bf16
+ * copies of the codes, which the call writes into `ws` (at least
+ * repro_linear_fwd_ws_bytes(M, N, K) bytes; 0 for shapes that use the exact
+ * CUDA-core path).  Too small a workspace -> REPRO_ERR_WORKSPACE.
  * ------------------------------------------------------------------------ */
 int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x,
                      const float* s_w, float* y, int64_t M, int64_t N, int64_t K,
-                     void* stream);
+                     void* ws, size_t ws_bytes, void* stream);
+size_t repro_linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K);
 
 /* ------------------------------------------------------------------------
  * Backward ([works]: fixed order, unfused multiply then add).  Operands are
@@ -186,6 +191,7 @@ typedef struct {
     int reduce_block_log2;  /* -1: default; else 2^k chunk partials per block in repro_wscale (0..10) */
     int fwd_path;           /* -1: default; 0: CUDA-core exact path; 1: tensor-core path */
     int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
+    int bwd_kernel;         /* -1: default (1); 0: plain backward kernel; 1: pipelined kernel */
 } repro_launch_cfg;
 
 const char* repro_status_str(int status);

@@ -67,13 +67,33 @@ def test_quant_argument_checks(L):
 
 
 def test_linear_fwd_argument_checks(L):
-    f = L.repro_linear_fwd
-    assert f(A, A * 2, A * 3, A * 3 + 4, A * 4, 8, 8, 133145, None) == -2   # K too large
-    assert f(A, A * 2, A * 3, A * 3 + 4, A * 4, -1, 8, 8, None) == -2
-    assert f(None, None, None, None, None, 0, 8, 8, None) == 0              # M == 0
-    assert f(A, A * 2, None, A * 3, A * 4, 8, 8, 8, None) == -1             # null scale
-    assert f(A + 1, A * 2, A * 3, A * 3 + 4, A * 4, 8, 8, 8, None) == -3
-    assert f(A, A * 2, A * 3, A * 3 + 4, A, 8, 8, 8, None) == -8            # y overlaps xq
+    def f(*a):
+        return L.repro_linear_fwd(*a[:8], None, 0, None)
+    assert f(A, A * 2, A * 3, A * 3 + 4, A * 4, 8, 8, 133145) == -2   # K too large
+    assert f(A, A * 2, A * 3, A * 3 + 4, A * 4, -1, 8, 8) == -2
+    assert f(None, None, None, None, None, 0, 8, 8) == 0              # M == 0
+    assert f(A, A * 2, None, A * 3, A * 4, 8, 8, 8) == -1             # null scale
+    assert f(A + 1, A * 2, A * 3, A * 3 + 4, A * 4, 8, 8, 8) == -3
+    assert f(A, A * 2, A * 3, A * 3 + 4, A, 8, 8, 8) == -8            # y overlaps xq
+
+
+def test_linear_fwd_workspace(L):
+    try:
+        repro.repro_set_launch_cfg(fwd_path=0)
+        assert repro.repro_linear_fwd_ws_bytes(16384, 2048, 2048) == 0
+        repro.repro_set_launch_cfg(fwd_path=1)
+        need = repro.repro_linear_fwd_ws_bytes(16384, 2048, 2048)
+        assert need >= 2 * (16384 + 2048) * 2048
+        assert repro.repro_linear_fwd_ws_bytes(16, 16, 12) == 0     # K % 8 != 0: CUDA cores
+        B = 1 << 32
+        assert L.repro_linear_fwd(B, B * 2, B * 3, B * 3 + 4, B * 4, 16384, 2048, 2048,
+                                  None, 0, None) == -7
+        assert L.repro_linear_fwd(B, B * 2, B * 3, B * 3 + 4, B * 4, 16384, 2048, 2048,
+                                  B * 8, need - 1, None) == -7
+        assert L.repro_linear_fwd(B, B * 2, B * 3, B * 3 + 4, B * 4, 16384, 2048, 2048,
+                                  B, need, None) == -8              # ws overlaps xq
+    finally:
+        repro.repro_set_launch_cfg(reset=True)
 
 
 def test_linear_bwd_argument_checks(L):

@@ -124,8 +124,10 @@ BWD_SHAPES = [(1, 1, 1), (3, 1, 5), (64, 128, 256), (200, 130, 70), (257, 64, 65
               (130, 257, 96), (64, 64, 64), (1000, 300, 17), (96, 4100, 20)]
 
 
+@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("M,N,K", BWD_SHAPES)
-def test_backward(orc, M, N, K):
+def test_backward(orc, M, N, K, kernel):
+    R.repro_set_launch_cfg(bwd_kernel=kernel)
     rng = np.random.default_rng(M * 7 + N * 3 + K)
     dy = (rng.standard_normal((M, N)) * 1e-3).astype(np.float32)
     xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
@@ -136,15 +138,16 @@ def test_backward(orc, M, N, K):
     G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, s_x), f"dw {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("seg", [0, 1, 2, 3, 4, 8])
-def test_backward_launch_invariance(orc, seg):
-    # long reductions split into aligned segments of 2^seg chunks
+def test_backward_launch_invariance(orc, seg, kernel):
+    # long reductions split into aligned segments of 2^seg chunks, by either kernel
     rng = np.random.default_rng(seg)
     M, N, K = 1100, 900, 40
     dy = (rng.standard_normal((M, N)) * 1e-3).astype(np.float32)
     xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
     wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
-    R.repro_set_launch_cfg(bwd_segment_log2=seg)
+    R.repro_set_launch_cfg(bwd_segment_log2=seg, bwd_kernel=kernel)
     dx, dw = G.gpu_bwd(dy, xq, wq, np.float32(0.03), np.float32(0.003))
     G.assert_bits_equal(dx, orc.linear_bwd_dx(dy, wq, np.float32(0.003)), f"dx seg {seg}")
     G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, np.float32(0.03)), f"dw seg {seg}")
