@@ -109,6 +109,30 @@ def dist_env():
     return ws, rank, local
 
 
+def replica_workload(wl, rank: int):
+    """Replicas only: rank r processes its own micro-batches (the pages' data
+    ownership: window m belongs to rank m mod R), so its seeds are offset by
+    r times the micro-batch count; weights are shared."""
+    return dataclasses.replace(wl, x_seed_base=wl.x_seed_base + rank * wl.microbatches)
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """Slowest rank's time (all_reduce MAX; a no-op for one rank)."""
+    if world <= 1:
+        return float(ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank_step: int, steps: int, world: int,
+                           ms_max: float) -> float:
+    """Tokens of all ranks over the slowest rank's time."""
+    return tokens_per_rank_step * steps * world / (ms_max / 1000.0)
+
+
 # ---------------------------------------------------------------- oracle leg
 
 def oracle_sample_step(wl, host, frac_log2: int) -> tuple:
@@ -222,8 +246,7 @@ def run_ours(args, wl):
         build_lib.build()
     if world > 1:
         dist.barrier()
-    # replicas only: rank r owns its own micro-batches (windows m mod R = r)
-    wl_r = dataclasses.replace(wl, x_seed_base=wl.x_seed_base + rank * wl.microbatches)
+    wl_r = replica_workload(wl, rank)
     host = S.generate_host_inputs(wl_r)
     hp = S.HotPathStep(wl_r, host, fused_accum=not args.unfused_accum)
     stream = torch.cuda.Stream()
@@ -267,12 +290,8 @@ def run_ours(args, wl):
     per_class = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in timers.items()}
     launch_counts = {k: len(v) for k, v in timers.items()}
 
-    t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    tokens_all = hp.tokens() * args.steps * world
-    value = tokens_all / (ms_max / 1000.0)
+    ms_max = max_over_ranks(ms, world, "cuda")
+    value = whole_job_tokens_per_s(hp.tokens(), args.steps, world, ms_max)
 
     # ---- end to end: host inputs copied in, result copied out, every step
     e2e = None
@@ -402,13 +421,8 @@ def measure_e2e(hp, host, steps, stream, world):
         one_step()
     b.record(stream)
     stream.synchronize()
-    ms = a.elapsed_time(b)
-    t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
-    return {"value": hp.tokens() * steps * world / (ms / 1000.0), "unit": UNIT,
+    ms = max_over_ranks(a.elapsed_time(b), world, "cuda")
+    return {"value": whole_job_tokens_per_s(hp.tokens(), steps, world, ms), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": ms / steps}
 

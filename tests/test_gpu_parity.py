@@ -237,7 +237,7 @@ def test_treefold_golden():
 
 def test_treefold_in_place_and_layout(orc):
     rng = np.random.default_rng(8)
-    Rn, n = 6, 10_001
+    Rn, n = 6, 10_004          # rows of the block stay 16-byte aligned
     block = (rng.standard_normal((Rn, n)) * 1e-3).astype(np.float32)
     ref = orc.treefold([block[r] for r in range(Rn)])
     tb = G.dev(block)
