@@ -284,7 +284,7 @@ def test_tiny_workload_end_to_end(orc):
     dx, dw = orc.linear_bwd_dx(dY, wq, s_w), orc.linear_bwd_dw(dY, xq, s_x)
     noise = [inputs.replica_noise(wl, r, dw.size).reshape(dw.shape) for r in range(wl.replicas)]
     reps = [orc.grad_accum(dw, nz) for nz in noise]
-    tf = orc.treefold(reps)
+    tf = orc.treefold(reps).reshape(dw.shape)
     # GPU side, same host inputs
     Wt, Xt, dYt = G.dev(W), G.dev(X), G.dev(dY)
     sw_t, sx_t = torch.empty(1, device="cuda"), torch.empty(1, device="cuda")
