@@ -118,6 +118,10 @@ bool use_tc(int64_t M, int64_t N, int64_t K)
 
 } // namespace
 
+namespace repro {
+int arch_status() { return check_arch(); }
+} // namespace repro
+
 extern "C" {
 
 const char* repro_status_str(int s)

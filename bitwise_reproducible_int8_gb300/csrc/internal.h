@@ -21,6 +21,7 @@ struct LaunchCfg {
 const LaunchCfg& launch_cfg();
 int num_sms();
 int* device_error_word();   // device address of the bounded-wait error flag
+int arch_status();          // REPRO_OK when the current device is a GB300
 void count_launches(int k); // adds k to the process-wide launch counter
 
 // ---- scale (k_scale.cu)

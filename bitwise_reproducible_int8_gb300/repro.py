@@ -49,6 +49,7 @@ _sz = ctypes.c_size_t
 _SIGNATURES = {
     "repro_wscale": (_int, [_vp, _i64, _int, _int, _vp, _vp, _sz, _vp]),
     "repro_wscale_ws_bytes": (_sz, [_i64]),
+    "repro_wscale_noalloc": (_int, [_vp, _i64, _int, _int, _vp, _vp]),
     "repro_quant_i8": (_int, [_vp, _i64, _vp, _int, _vp, _vp]),
     "repro_linear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "repro_linear_fwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
@@ -142,6 +143,15 @@ def repro_wscale(x: torch.Tensor, mode: int, scale_out: torch.Tensor, ws=None,
         _ptr(scale_out, torch.float32, "scale_out"), _ptr(ws, None, "ws"),
         ws.numel() * ws.element_size() if isinstance(ws, torch.Tensor) else 1 << 62,
         _stream(stream)))
+
+
+def repro_wscale_noalloc(x: torch.Tensor, mode: int, scale_out: torch.Tensor,
+                         qmax: int = REPRO_QMAX, stream=None) -> None:
+    """repro_wscale without a workspace, for callers that cannot allocate
+    device memory; scratch comes from a fixed array inside the library."""
+    _check("repro_wscale_noalloc", lib().repro_wscale_noalloc(
+        _ptr(x, torch.float32, "x"), x.numel(), int(mode), int(qmax),
+        _ptr(scale_out, torch.float32, "scale_out"), _stream(stream)))
 
 
 def repro_quant_i8(x: torch.Tensor, scale: torch.Tensor, q_out: torch.Tensor,

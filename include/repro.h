@@ -194,6 +194,28 @@ typedef struct {
     int bwd_kernel;         /* -1: default (1); 0: plain backward kernel; 1: pipelined kernel */
 } repro_launch_cfg;
 
+/* ------------------------------------------------------------------------
+ * Allocation-free scale, for callers that cannot hand the library any device
+ * memory: code whose device allocations all belong to another owner (a host
+ * application's private pool, a plugin without allocator hooks), or a loop
+ * that must never call cudaMalloc because that would synchronise the device.
+ * The pages have no counterpart: this is an interface convenience only, with
+ * the same arithmetic and the same bits as repro_wscale.
+ * Same arguments and results as repro_wscale, minus the workspace: the
+ * scratch is a fixed array of REPRO_NOALLOC_SCRATCH_FLOATS floats (256 KB)
+ * inside the library, held by every GPU that loads the library until the
+ * process exits.  n may be at most REPRO_NOALLOC_MAX_N (REPRO_ERR_SHAPE
+ * otherwise); the block split is always the default one.  The first call on a
+ * device, made with that device current, looks up the array's device address
+ * (make it before any stream capture).  Calls share the array and race if
+ * their work overlaps on the GPU; nothing in it needs clearing.  Allocates
+ * nothing.
+ * ------------------------------------------------------------------------ */
+#define REPRO_NOALLOC_SCRATCH_FLOATS 65536
+#define REPRO_NOALLOC_MAX_N 535822336LL   /* 65408 blocks of 8192 elements */
+int repro_wscale_noalloc(const float* x, int64_t n, int mode, int qmax, float* scale_out,
+                         void* stream);
+
 const char* repro_status_str(int status);
 int repro_version(void);
 int repro_device_check(void* stream);
