@@ -601,6 +601,287 @@ __global__ void __launch_bounds__(256, 1) k_bwd2(const BwdArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Staged variant (default for aligned shapes: rows of dY and of the int8
+// operand start on 16-byte boundaries).  Same tile, per-output order, packed
+// arithmetic and tree as k_bwd2; the data movement changes:
+//   * the next chunk's raw bytes are copied global -> shared with cp.async
+//     (16-byte pieces, zero-filled outside the tensor) while the current chunk
+//     is computed, so no registers wait on global memory;
+//   * after a barrier, a transform pass turns the raw chunk into the compute
+//     layout: dY flushed (and transposed for dX, through a raw layout padded
+//     to 68 floats per row so the transposing reads are conflict-free), the
+//     int8 operand dequantised into the duplicated pair layout;
+//   * stack levels 0-3 stay in registers, levels 4-7 (merged at most once per
+//     16 chunks) live in a per-thread slice of shared memory, which frees 64
+//     registers for a one-step-ahead prefetch of the shared-memory fragments.
+// ---------------------------------------------------------------------------
+
+constexpr int RAW_A_LD = 68;                                   // floats per raw A row
+constexpr int RAW_A_BYTES = CH * RAW_A_LD * 4;                 // 17408
+constexpr int RAW_B_BYTES = CH * BT;                           // 4096 int8
+constexpr int COMP_BYTES = 3 * CH * BT * 4;                    // 49152
+constexpr int REG_LVL = 4;                                     // levels kept in registers
+constexpr int EXT_BYTES = (MAXLVL - REG_LVL) * 8 * 256 * 8;    // 65536
+constexpr size_t BWD3_SMEM = (size_t)RAW_A_BYTES + RAW_B_BYTES + COMP_BYTES + EXT_BYTES;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// raw copy of chunk r0: A as 64 rows x 64 floats (DW: rows = reduction index,
+// columns = i; DX: rows = i, columns = reduction index), B as 64 rows x 64 int8
+template <bool DW>
+__device__ __forceinline__ void issue_raw(float* __restrict__ rawA, int8_t* __restrict__ rawB,
+                                          const BwdArgs& a, int64_t i0, int64_t j0, int64_t r0,
+                                          int valid, int tid)
+{
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int p = tid + it * 256;
+        const int row = p >> 4, f = p & 15;
+        const float* src;
+        bool ok;
+        if (DW) {
+            src = a.dy + (r0 + row) * a.ldy + i0 + 4 * f;
+            ok = row < valid && i0 + 4 * f < a.I;
+        } else {
+            src = a.dy + (i0 + row) * a.ldy + r0 + 4 * f;
+            ok = i0 + row < a.I && 4 * f < valid;
+        }
+        cp_async16(rawA + row * RAW_A_LD + 4 * f, ok ? src : a.dy, ok ? 16u : 0u);
+    }
+    {
+        const int row = tid >> 2, part = tid & 3;
+        const bool ok = row < valid && j0 + 16 * part < a.J;
+        const int8_t* src = ok ? a.q + (r0 + row) * a.J + j0 + 16 * part : a.q;
+        cp_async16(rawB + row * BT + 16 * part, src, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+}
+
+template <bool DW>
+__device__ __forceinline__ void transform(float* __restrict__ As, float* __restrict__ B0,
+                                          float* __restrict__ B1, const float* __restrict__ rawA,
+                                          const int8_t* __restrict__ rawB, float s, int tid)
+{
+    if (DW) {
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int e = tid + it * 256;
+            const int r = e >> 4, f = e & 15;
+            const float4 v = *reinterpret_cast<const float4*>(rawA + r * RAW_A_LD + 4 * f);
+            *reinterpret_cast<float4*>(&As[r * BT + 4 * f]) = flush4(v);
+        }
+    } else {
+        const int i = tid & 63;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int f = (tid >> 6) + 4 * it;
+            const float4 v = *reinterpret_cast<const float4*>(rawA + i * RAW_A_LD + 4 * f);
+            As[(4 * f + 0) * BT + i] = flush(v.x);
+            As[(4 * f + 1) * BT + i] = flush(v.y);
+            As[(4 * f + 2) * BT + i] = flush(v.z);
+            As[(4 * f + 3) * BT + i] = flush(v.w);
+        }
+    }
+    const int4 w = *reinterpret_cast<const int4*>(rawB + (tid >> 2) * BT + 16 * (tid & 3));
+    store_b(B0, B1, w, s, tid);
+}
+
+template <bool DW>
+__global__ void __launch_bounds__(256, 1) k_bwd3(const BwdArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem3[];
+    float* rawA = reinterpret_cast<float*>(smem3);
+    int8_t* rawB = reinterpret_cast<int8_t*>(smem3 + RAW_A_BYTES);
+    float* As = reinterpret_cast<float*>(smem3 + RAW_A_BYTES + RAW_B_BYTES);
+    float* B0 = As + CH * BT;
+    float* B1 = As + 2 * CH * BT;
+    u64* ext = reinterpret_cast<u64*>(smem3 + RAW_A_BYTES + RAW_B_BYTES + COMP_BYTES);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ty = (warp >> 1) * 4 + (lane >> 3);
+    const int tx = (warp & 1) * 8 + (lane & 7);
+    const int64_t i0 = (int64_t)blockIdx.y * BT, j0 = (int64_t)blockIdx.x * BT;
+    const float s = flush(*a.scale);
+
+    const int64_t C = (a.R + CH - 1) / CH;
+    const int64_t cbeg = (int64_t)blockIdx.z << a.seg_log2;
+    const int64_t cend = min(C, cbeg + ((int64_t)1 << a.seg_log2));
+
+    // level l >= REG_LVL, pair e of this thread
+    auto X = [&](int l, int e) -> u64& { return ext[((l - REG_LVL) * 8 + e) * 256 + tid]; };
+
+    u64 S[REG_LVL][8];
+    u64 acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        acc[e] = 0ull;
+#pragma unroll
+    for (int l = 0; l < REG_LVL; ++l)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            S[l][e] = 0ull;
+
+    issue_raw<DW>(rawA, rawB, a, i0, j0, cbeg * CH, (int)min((int64_t)CH, a.R - cbeg * CH), tid);
+    cp_async_wait_all();
+    __syncthreads();
+    transform<DW>(As, B0, B1, rawA, rawB, s, tid);
+    __syncthreads();
+
+    const float* Ar = As + 4 * ty;
+    const float* B0r = B0 + 4 * tx;
+    const float* B1r = B1 + 4 * tx;
+
+    for (int64_t c = cbeg; c < cend; ++c) {
+        const int64_t r0 = c * CH;
+        const int valid = (int)min((int64_t)CH, a.R - r0);
+        const bool more = c + 1 < cend;
+        if (more)
+            issue_raw<DW>(rawA, rawB, a, i0, j0, r0 + CH, (int)min((int64_t)CH, a.R - r0 - CH),
+                          tid);
+
+        // the chunk, with the next step's fragments loaded one step ahead
+        ulonglong2 av = *reinterpret_cast<const ulonglong2*>(Ar);
+        ulonglong2 b01 = *reinterpret_cast<const ulonglong2*>(B0r);
+        ulonglong2 b23 = *reinterpret_cast<const ulonglong2*>(B1r);
+        {
+            const u64 A_[2] = {av.x, av.y};
+            const u64 B_[4] = {b01.x, b01.y, b23.x, b23.y};
+            if (valid > 1) {
+                av = *reinterpret_cast<const ulonglong2*>(Ar + BT);
+                b01 = *reinterpret_cast<const ulonglong2*>(B0r + BT);
+                b23 = *reinterpret_cast<const ulonglong2*>(B1r + BT);
+            }
+#pragma unroll
+            for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    acc[ip * 4 + j] = fmul2_rn(A_[ip], B_[j]);
+        }
+        if (valid == CH) {
+#pragma unroll 7
+            for (int r = 1; r < CH; ++r) {
+                const u64 A_[2] = {av.x, av.y};
+                const u64 B_[4] = {b01.x, b01.y, b23.x, b23.y};
+                const int rn = r + 1 < CH ? r + 1 : r;
+                av = *reinterpret_cast<const ulonglong2*>(Ar + rn * BT);
+                b01 = *reinterpret_cast<const ulonglong2*>(B0r + rn * BT);
+                b23 = *reinterpret_cast<const ulonglong2*>(B1r + rn * BT);
+#pragma unroll
+                for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        acc[ip * 4 + j] = fadd2_ftz(acc[ip * 4 + j], fmul2_rn(A_[ip], B_[j]));
+            }
+        } else {
+            for (int r = 1; r < valid; ++r) {
+                const u64 A_[2] = {av.x, av.y};
+                const u64 B_[4] = {b01.x, b01.y, b23.x, b23.y};
+                const int rn = r + 1 < valid ? r + 1 : r;
+                av = *reinterpret_cast<const ulonglong2*>(Ar + rn * BT);
+                b01 = *reinterpret_cast<const ulonglong2*>(B0r + rn * BT);
+                b23 = *reinterpret_cast<const ulonglong2*>(B1r + rn * BT);
+#pragma unroll
+                for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        acc[ip * 4 + j] = fadd2_ftz(acc[ip * 4 + j], fmul2_rn(A_[ip], B_[j]));
+            }
+        }
+
+        // tree: push (merge the levels named by the trailing ones of cs) or,
+        // after the segment's last chunk, fold every occupied level
+        const int cs = (int)(c - cbeg);
+        if (more) {
+            const int tz = __ffs(~cs) - 1;
+#pragma unroll
+            for (int t = 0; t < MAXLVL; ++t) {
+                if (tz == t) {
+#pragma unroll
+                    for (int l = 0; l < t; ++l)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            acc[e] = fadd2_ftz(l < REG_LVL ? S[l < REG_LVL ? l : 0][e] : X(l, e), acc[e]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (t < REG_LVL)
+                            S[t < REG_LVL ? t : 0][e] = acc[e];
+                        else
+                            X(t, e) = acc[e];
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int l = 0; l < MAXLVL; ++l) {
+                if ((cs >> l) & 1) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        acc[e] = fadd2_ftz(l < REG_LVL ? S[l < REG_LVL ? l : 0][e] : X(l, e), acc[e]);
+                }
+            }
+        }
+
+        if (more) {
+            cp_async_wait_all();
+            __syncthreads();            // comp reads done, raw chunk visible
+            transform<DW>(As, B0, B1, rawA, rawB, s, tid);
+            __syncthreads();            // comp ready
+        }
+    }
+
+    float o[4][4];
+#pragma unroll
+    for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float lo, hi;
+            unpack2(acc[ip * 4 + j], lo, hi);
+            o[2 * ip][j] = lo;
+            o[2 * ip + 1][j] = hi;
+        }
+    if (a.nseg == 1) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t row = i0 + 4 * ty + i;
+            if (row >= a.I)
+                continue;
+            const int64_t col = j0 + 4 * tx;
+            if (col >= a.J)
+                continue;
+            float* dst = a.out + row * a.J + col;     // J % 16 == 0: whole float4 inside
+            float v0 = flush(o[i][0]), v1 = flush(o[i][1]), v2 = flush(o[i][2]), v3 = flush(o[i][3]);
+            if (a.accumulate) {
+                const float4 old = *reinterpret_cast<const float4*>(dst);
+                v0 = fadd_ftz(old.x, v0);
+                v1 = fadd_ftz(old.y, v1);
+                v2 = fadd_ftz(old.z, v2);
+                v3 = fadd_ftz(old.w, v3);
+            }
+            *reinterpret_cast<float4*>(dst) = make_float4(v0, v1, v2, v3);
+        }
+    } else {
+        float* base = a.ws + (int64_t)blockIdx.z * a.I * a.J;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t row = i0 + 4 * ty + i;
+            const int64_t col = j0 + 4 * tx;
+            if (row < a.I && col < a.J)
+                *reinterpret_cast<float4*>(base + row * a.J + col) =
+                    make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+        }
+    }
+}
+
 // one level of the tree over segment partials: ws[j] <- ws[j] (+) ws[j + s]
 // for every j that is a multiple of 2s with j + s < nseg
 __global__ void k_seg_level(float* __restrict__ ws, int nseg, int s, int64_t count)
@@ -669,8 +950,18 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
     a.nseg = (int)nseg_for(R, seg_log2);
     a.accumulate = accumulate ? 1 : 0;
     dim3 grid((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BT), (unsigned)a.nseg);
-    if (launch_cfg().bwd_kernel == 0) {
+    // the staged kernel needs 16-byte-aligned rows: dY rows (N % 4) and int8
+    // rows (J % 16); other shapes take the register-prefetch kernel
+    const bool aligned = (ldy % 4) == 0 && (J % 16) == 0;
+    const int kernel = launch_cfg().bwd_kernel;
+    if (kernel == 0) {
         k_bwd<DW><<<grid, 256, 0, st>>>(a);
+    } else if (kernel == 2 && aligned) {
+        cudaError_t e = cudaFuncSetAttribute(k_bwd3<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)BWD3_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        k_bwd3<DW><<<grid, 256, BWD3_SMEM, st>>>(a);
     } else {
         // opt in to 96 KB of dynamic shared memory (on the current device)
         cudaError_t e = cudaFuncSetAttribute(k_bwd2<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,

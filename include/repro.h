@@ -189,9 +189,9 @@ int repro_treefold(const float* const* parts, int R, int64_t n, float* out,
 typedef struct {
     int bwd_segment_log2;   /* -1: default; else 2^k chunks per backward reduction segment (0..8) */
     int reduce_block_log2;  /* -1: default; else 2^k chunk partials per block in repro_wscale (0..10) */
-    int fwd_path;           /* -1: default; 0: CUDA-core exact path; 1: tensor-core path */
+    int fwd_path;           /* -1: default (tensor cores when K % 8 == 0); 0: CUDA cores; 1: tensor cores */
     int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
-    int bwd_kernel;         /* -1: default (1); 0: plain backward kernel; 1: pipelined kernel */
+    int bwd_kernel;         /* -1: default (2); 0: plain; 1: register prefetch; 2: staged (aligned shapes, else 1) */
 } repro_launch_cfg;
 
 /* ------------------------------------------------------------------------

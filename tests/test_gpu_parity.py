@@ -89,11 +89,13 @@ def test_quant_half_integers(orc):
 # ----------------------------------------------------------------- forward
 
 FWD_SHAPES = [(1, 1, 1), (3, 5, 7), (64, 128, 256), (130, 70, 200), (65, 129, 1040),
-              (200, 96, 2048), (17, 300, 33)]
+              (200, 96, 2048), (17, 300, 33), (257, 129, 5632), (128, 128, 8), (300, 260, 520)]
 
 
+@pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("M,N,K", FWD_SHAPES)
-def test_forward(orc, M, N, K):
+def test_forward(orc, M, N, K, path):
+    R.repro_set_launch_cfg(fwd_path=path)
     rng = np.random.default_rng(M + N + K)
     xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
     wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
@@ -102,8 +104,10 @@ def test_forward(orc, M, N, K):
                         f"fwd {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("K", [1024, 1040, 2048, 5632])
-def test_forward_adversarial(orc, K):
+def test_forward_adversarial(orc, K, path):
+    R.repro_set_launch_cfg(fwd_path=path)
     # all codes at the clamp: |acc| = 16129 K, above 2^24 for K > 1040
     M, N = 4, 4
     xq = np.full((M, K), 127, np.int8)
@@ -121,10 +125,11 @@ def test_forward_adversarial(orc, K):
 # ----------------------------------------------------------------- backward
 
 BWD_SHAPES = [(1, 1, 1), (3, 1, 5), (64, 128, 256), (200, 130, 70), (257, 64, 65),
-              (130, 257, 96), (64, 64, 64), (1000, 300, 17), (96, 4100, 20)]
+              (130, 257, 96), (64, 64, 64), (1000, 300, 17), (96, 4100, 20),
+              (257, 68, 96), (100, 4100, 32), (1000, 300, 16), (70, 132, 48)]
 
 
-@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("kernel", [0, 1, 2])
 @pytest.mark.parametrize("M,N,K", BWD_SHAPES)
 def test_backward(orc, M, N, K, kernel):
     R.repro_set_launch_cfg(bwd_kernel=kernel)
@@ -138,12 +143,12 @@ def test_backward(orc, M, N, K, kernel):
     G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, s_x), f"dw {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("kernel", [0, 1, 2])
 @pytest.mark.parametrize("seg", [0, 1, 2, 3, 4, 8])
 def test_backward_launch_invariance(orc, seg, kernel):
     # long reductions split into aligned segments of 2^seg chunks, by either kernel
     rng = np.random.default_rng(seg)
-    M, N, K = 1100, 900, 40
+    M, N, K = 1100, 900, 48
     dy = (rng.standard_normal((M, N)) * 1e-3).astype(np.float32)
     xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
     wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
