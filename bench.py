@@ -240,6 +240,8 @@ def run_ours(args, wl):
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
+    if args.bwd_kernel >= 0:
+        R.repro_set_launch_cfg(bwd_kernel=args.bwd_kernel)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     if rank == 0 or not os.path.exists(build_lib.LIB):
@@ -437,6 +439,8 @@ def main(argv=None):
     ap.add_argument("--unfused-accum", action="store_true",
                     help="accumulate dW with repro_grad_accum instead of the fused epilogue")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--bwd-kernel", type=int, default=-1,
+                    help="backward kernel variant (launch-configuration hook; -1: default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-frac-log2", type=int, default=10,
                     help="the oracle's timed sample is 2^-k of one step's work")

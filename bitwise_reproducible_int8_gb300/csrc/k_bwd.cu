@@ -882,6 +882,274 @@ __global__ void __launch_bounds__(256, 1) k_bwd3(const BwdArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Wide-tile variant (default for aligned shapes).  Shared-memory bandwidth
+// bounds the 4 x 4 thread tile: every 16-byte shared load costs one wavefront
+// per quarter-warp however many lanes share its address, so the cost is one
+// wavefront per warp per float a thread loads.  A thread of this kernel owns
+// 8 x 4 outputs (0.375 loaded floats per output instead of 0.75), and builds
+// the packed (b, b) pairs with a register move instead of a duplicated
+// shared-memory copy.  CTA tile 128 (i) x 64 (j), 256 threads; cp.async
+// staging and transform pass as in k_bwd3; tree levels 0-3 in registers,
+// 4-7 in 128 KB of per-thread shared memory.  Same per-output arithmetic.
+// ---------------------------------------------------------------------------
+
+constexpr int BI4 = 128;                                      // tile rows (i)
+constexpr int RAW4_A_BYTES = 128 * 68 * 4;                    // 34816 (DX; DW needs 64 x 132)
+constexpr int RAW4_B_BYTES = CH * BT;                         // 4096
+constexpr int COMP4_A_BYTES = CH * BI4 * 4;                   // 32768
+constexpr int COMP4_B_BYTES = CH * BT * 4;                    // 16384
+constexpr int EXT4_BYTES = (MAXLVL - REG_LVL) * 16 * 256 * 8; // 131072
+constexpr size_t BWD4_SMEM =
+    (size_t)RAW4_A_BYTES + RAW4_B_BYTES + COMP4_A_BYTES + COMP4_B_BYTES + EXT4_BYTES;
+
+template <bool DW>
+__device__ __forceinline__ void issue_raw4(float* __restrict__ rawA, int8_t* __restrict__ rawB,
+                                           const BwdArgs& a, int64_t i0, int64_t j0, int64_t r0,
+                                           int valid, int tid)
+{
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int p = tid + it * 256;
+        const float* src;
+        float* dst;
+        bool ok;
+        if (DW) {   // 64 rows (reduction) x 128 floats (i), row pitch 132
+            const int row = p >> 5, f = p & 31;
+            src = a.dy + (r0 + row) * a.ldy + i0 + 4 * f;
+            ok = row < valid && i0 + 4 * f < a.I;
+            dst = rawA + row * 132 + 4 * f;
+        } else {    // 128 rows (i) x 64 floats (reduction), row pitch 68
+            const int row = p >> 4, f = p & 15;
+            src = a.dy + (i0 + row) * a.ldy + r0 + 4 * f;
+            ok = i0 + row < a.I && 4 * f < valid;
+            dst = rawA + row * 68 + 4 * f;
+        }
+        cp_async16(dst, ok ? src : a.dy, ok ? 16u : 0u);
+    }
+    {
+        const int row = tid >> 2, part = tid & 3;
+        const bool ok = row < valid && j0 + 16 * part < a.J;
+        const int8_t* src = ok ? a.q + (r0 + row) * a.J + j0 + 16 * part : a.q;
+        cp_async16(rawB + row * BT + 16 * part, src, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+}
+
+template <bool DW>
+__device__ __forceinline__ void transform4(float* __restrict__ As, float* __restrict__ Bs,
+                                           const float* __restrict__ rawA,
+                                           const int8_t* __restrict__ rawB, float s, int tid)
+{
+    if (DW) {
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int e = tid + it * 256;
+            const int r = e >> 5, f = e & 31;
+            const float4 v = *reinterpret_cast<const float4*>(rawA + r * 132 + 4 * f);
+            *reinterpret_cast<float4*>(&As[r * BI4 + 4 * f]) = flush4(v);
+        }
+    } else {
+        const int i = tid & 127;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int f = (tid >> 7) + 2 * it;
+            const float4 v = *reinterpret_cast<const float4*>(rawA + i * 68 + 4 * f);
+            As[(4 * f + 0) * BI4 + i] = flush(v.x);
+            As[(4 * f + 1) * BI4 + i] = flush(v.y);
+            As[(4 * f + 2) * BI4 + i] = flush(v.z);
+            As[(4 * f + 3) * BI4 + i] = flush(v.w);
+        }
+    }
+    const int row = tid >> 2, part = tid & 3;
+    const int4 w = *reinterpret_cast<const int4*>(rawB + row * BT + 16 * part);
+    const int words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<float4*>(&Bs[row * BT + 16 * part + 4 * u]) =
+            make_float4(dequant((int)(int8_t)(words[u]), s), dequant((int)(int8_t)(words[u] >> 8), s),
+                        dequant((int)(int8_t)(words[u] >> 16), s),
+                        dequant((int)(int8_t)(words[u] >> 24), s));
+}
+
+// one reduction step: rows 8ty..8ty+7 as 4 pairs, columns 4tx..4tx+3
+template <bool FIRST>
+__device__ __forceinline__ void step4(u64 (&acc)[16], const ulonglong2& a03, const ulonglong2& a47,
+                                      const float4& b)
+{
+    const u64 P[4] = {a03.x, a03.y, a47.x, a47.y};
+    const u64 D[4] = {pack2(b.x, b.x), pack2(b.y, b.y), pack2(b.z, b.z), pack2(b.w, b.w)};
+#pragma unroll
+    for (int ip = 0; ip < 4; ++ip)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const u64 p = fmul2_rn(P[ip], D[j]);
+            acc[ip * 4 + j] = FIRST ? p : fadd2_ftz(acc[ip * 4 + j], p);
+        }
+}
+
+template <bool DW>
+__global__ void __launch_bounds__(256, 1) k_bwd4(const BwdArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem4[];
+    float* rawA = reinterpret_cast<float*>(smem4);
+    int8_t* rawB = reinterpret_cast<int8_t*>(smem4 + RAW4_A_BYTES);
+    float* As = reinterpret_cast<float*>(smem4 + RAW4_A_BYTES + RAW4_B_BYTES);
+    float* Bs = reinterpret_cast<float*>(smem4 + RAW4_A_BYTES + RAW4_B_BYTES + COMP4_A_BYTES);
+    u64* ext = reinterpret_cast<u64*>(smem4 + RAW4_A_BYTES + RAW4_B_BYTES + COMP4_A_BYTES +
+                                      COMP4_B_BYTES);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ty = (warp >> 1) * 4 + (lane >> 3);   // rows 8ty .. 8ty+7
+    const int tx = (warp & 1) * 8 + (lane & 7);     // cols 4tx .. 4tx+3
+    const int64_t i0 = (int64_t)blockIdx.y * BI4, j0 = (int64_t)blockIdx.x * BT;
+    const float s = flush(*a.scale);
+
+    const int64_t C = (a.R + CH - 1) / CH;
+    const int64_t cbeg = (int64_t)blockIdx.z << a.seg_log2;
+    const int64_t cend = min(C, cbeg + ((int64_t)1 << a.seg_log2));
+
+    auto X = [&](int l, int e) -> u64& { return ext[((l - REG_LVL) * 16 + e) * 256 + tid]; };
+
+    u64 S[REG_LVL][16];
+    u64 acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        acc[e] = 0ull;
+#pragma unroll
+    for (int l = 0; l < REG_LVL; ++l)
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            S[l][e] = 0ull;
+
+    issue_raw4<DW>(rawA, rawB, a, i0, j0, cbeg * CH, (int)min((int64_t)CH, a.R - cbeg * CH), tid);
+    cp_async_wait_all();
+    __syncthreads();
+    transform4<DW>(As, Bs, rawA, rawB, s, tid);
+    __syncthreads();
+
+    const float* Ar = As + 8 * ty;
+    const float* Br = Bs + 4 * tx;
+
+    for (int64_t c = cbeg; c < cend; ++c) {
+        const int64_t r0 = c * CH;
+        const int valid = (int)min((int64_t)CH, a.R - r0);
+        const bool more = c + 1 < cend;
+        if (more)
+            issue_raw4<DW>(rawA, rawB, a, i0, j0, r0 + CH,
+                           (int)min((int64_t)CH, a.R - r0 - CH), tid);
+
+        ulonglong2 a03 = *reinterpret_cast<const ulonglong2*>(Ar);
+        ulonglong2 a47 = *reinterpret_cast<const ulonglong2*>(Ar + 4);
+        float4 b = *reinterpret_cast<const float4*>(Br);
+        {
+            const ulonglong2 c03 = a03, c47 = a47;
+            const float4 cb = b;
+            if (valid > 1) {
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + BI4);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + BI4 + 4);
+                b = *reinterpret_cast<const float4*>(Br + BT);
+            }
+            step4<true>(acc, c03, c47, cb);
+        }
+        if (valid == CH) {
+#pragma unroll 7
+            for (int r = 1; r < CH; ++r) {
+                const ulonglong2 c03 = a03, c47 = a47;
+                const float4 cb = b;
+                const int rn = r + 1 < CH ? r + 1 : r;
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4 + 4);
+                b = *reinterpret_cast<const float4*>(Br + rn * BT);
+                step4<false>(acc, c03, c47, cb);
+            }
+        } else {
+            for (int r = 1; r < valid; ++r) {
+                const ulonglong2 c03 = a03, c47 = a47;
+                const float4 cb = b;
+                const int rn = r + 1 < valid ? r + 1 : r;
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4 + 4);
+                b = *reinterpret_cast<const float4*>(Br + rn * BT);
+                step4<false>(acc, c03, c47, cb);
+            }
+        }
+
+        const int cs = (int)(c - cbeg);
+        if (more) {
+            const int tz = __ffs(~cs) - 1;
+#pragma unroll
+            for (int t = 0; t < MAXLVL; ++t) {
+                if (tz == t) {
+#pragma unroll
+                    for (int l = 0; l < t; ++l)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            acc[e] = fadd2_ftz(l < REG_LVL ? S[l < REG_LVL ? l : 0][e] : X(l, e), acc[e]);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        if (t < REG_LVL)
+                            S[t < REG_LVL ? t : 0][e] = acc[e];
+                        else
+                            X(t, e) = acc[e];
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int l = 0; l < MAXLVL; ++l) {
+                if ((cs >> l) & 1) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        acc[e] = fadd2_ftz(l < REG_LVL ? S[l < REG_LVL ? l : 0][e] : X(l, e), acc[e]);
+                }
+            }
+        }
+
+        if (more) {
+            cp_async_wait_all();
+            __syncthreads();
+            transform4<DW>(As, Bs, rawA, rawB, s, tid);
+            __syncthreads();
+        }
+    }
+
+    // row 8ty + 2ip + h, column 4tx + j is lane h of acc[ip*4 + j]
+    const int64_t col = j0 + 4 * tx;
+#pragma unroll
+    for (int ip = 0; ip < 4; ++ip) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t row = i0 + 8 * ty + 2 * ip + h;
+            float o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo, hi;
+                unpack2(acc[ip * 4 + j], lo, hi);
+                o[j] = h ? hi : lo;
+            }
+            if (row >= a.I || col >= a.J)
+                continue;
+            if (a.nseg == 1) {
+                float* dst = a.out + row * a.J + col;    // J % 16 == 0: whole float4 inside
+                float v0 = flush(o[0]), v1 = flush(o[1]), v2 = flush(o[2]), v3 = flush(o[3]);
+                if (a.accumulate) {
+                    const float4 old = *reinterpret_cast<const float4*>(dst);
+                    v0 = fadd_ftz(old.x, v0);
+                    v1 = fadd_ftz(old.y, v1);
+                    v2 = fadd_ftz(old.z, v2);
+                    v3 = fadd_ftz(old.w, v3);
+                }
+                *reinterpret_cast<float4*>(dst) = make_float4(v0, v1, v2, v3);
+            } else {
+                float* base = a.ws + (int64_t)blockIdx.z * a.I * a.J;
+                *reinterpret_cast<float4*>(base + row * a.J + col) = make_float4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+}
+
 // one level of the tree over segment partials: ws[j] <- ws[j] (+) ws[j + s]
 // for every j that is a multiple of 2s with j + s < nseg
 __global__ void k_seg_level(float* __restrict__ ws, int nseg, int s, int64_t count)
@@ -956,7 +1224,14 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
     const int kernel = launch_cfg().bwd_kernel;
     if (kernel == 0) {
         k_bwd<DW><<<grid, 256, 0, st>>>(a);
-    } else if (kernel == 2 && aligned) {
+    } else if (kernel == 3 && aligned) {
+        cudaError_t e = cudaFuncSetAttribute(k_bwd4<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)BWD4_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        dim3 g4((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BI4), (unsigned)a.nseg);
+        k_bwd4<DW><<<g4, 256, BWD4_SMEM, st>>>(a);
+    } else if (kernel >= 2 && aligned) {
         cudaError_t e = cudaFuncSetAttribute(k_bwd3<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)BWD3_SMEM);
         if (e != cudaSuccess)

@@ -191,7 +191,8 @@ typedef struct {
     int reduce_block_log2;  /* -1: default; else 2^k chunk partials per block in repro_wscale (0..10) */
     int fwd_path;           /* -1: default (tensor cores when K % 8 == 0); 0: CUDA cores; 1: tensor cores */
     int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
-    int bwd_kernel;         /* -1: default (2); 0: plain; 1: register prefetch; 2: staged (aligned shapes, else 1) */
+    int bwd_kernel;         /* -1: default (2); 0: plain; 1: register prefetch; 2: staged;
+                               3: staged wide tile (2 and 3 need aligned rows, else 1) */
 } repro_launch_cfg;
 
 /* ------------------------------------------------------------------------
