@@ -11,7 +11,7 @@ namespace repro {
 
 namespace {
 
-LaunchCfg g_cfg = {-1, -1, -1, 0, 2};
+LaunchCfg g_cfg = {-1, -1, -1, 0, 4};
 
 constexpr int kMaxDevices = 64;
 int g_arch_ok[kMaxDevices];   // 0 unknown, 1 GB300, -1 other
@@ -108,7 +108,8 @@ int stream_grid(int64_t work_items)
     return (int)(want < 1 ? 1 : (want > cap ? cap : want));
 }
 
-int seg_log2() { return g_cfg.bwd_segment_log2 < 0 ? 8 : g_cfg.bwd_segment_log2; }
+// -1: chosen per shape by the backward launcher
+int seg_log2() { return g_cfg.bwd_segment_log2; }
 
 // tensor-core forward for every supported shape unless the launch
 // configuration asks for the CUDA-core path
@@ -148,7 +149,7 @@ uint64_t repro_launch_count(void) { return (uint64_t)__atomic_load_n(&g_launches
 int repro_set_launch_cfg(const repro_launch_cfg* cfg)
 {
     if (!cfg) {
-        g_cfg = LaunchCfg{-1, -1, -1, 0, 2};
+        g_cfg = LaunchCfg{-1, -1, -1, 0, 4};
         return REPRO_OK;
     }
     if (cfg->bwd_segment_log2 < -1 || cfg->bwd_segment_log2 > 8)
@@ -159,13 +160,13 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
         return REPRO_ERR_ARG;
     if (cfg->elementwise_blocks < -1 || cfg->elementwise_blocks > (1 << 20))
         return REPRO_ERR_ARG;
-    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 3)
+    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 4)
         return REPRO_ERR_ARG;
     g_cfg.bwd_segment_log2 = cfg->bwd_segment_log2;
     g_cfg.reduce_block_log2 = cfg->reduce_block_log2;
     g_cfg.fwd_path = cfg->fwd_path;
     g_cfg.elementwise_blocks = cfg->elementwise_blocks < 0 ? 0 : cfg->elementwise_blocks;
-    g_cfg.bwd_kernel = cfg->bwd_kernel < 0 ? 2 : cfg->bwd_kernel;
+    g_cfg.bwd_kernel = cfg->bwd_kernel < 0 ? 4 : cfg->bwd_kernel;
     return REPRO_OK;
 }
 

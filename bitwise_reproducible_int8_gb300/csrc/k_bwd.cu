@@ -1150,6 +1150,289 @@ __global__ void __launch_bounds__(256, 1) k_bwd4(const BwdArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-memory variant.  k_bwd4's tile and arithmetic, with the resources the
+// backward leaves idle put to work:
+//   * tree levels 2-7 live in tensor memory (unused by this kernel): each
+//     thread owns one TMEM lane (32*(warp%4) + lane) and a 256-column slice
+//     ((warp/4)*256), one 32-column block per level, written and read with
+//     tcgen05.st / tcgen05.ld 32x32b.x32 at chunk boundaries only;
+//   * the shared memory this frees double-buffers both the raw (cp.async) and
+//     the compute stages, so each chunk needs one barrier: after it, a thread
+//     transforms chunk c+1 into the other compute buffer and then computes
+//     chunk c, overlapping other warps' transforms with its arithmetic;
+//   * the registers it frees let each reduction step issue its 16 products
+//     before its 16 additions.
+// The CTA allocates all 512 TMEM columns (one CTA per SM) and frees them
+// before it exits.
+// ---------------------------------------------------------------------------
+
+constexpr int RAW5_STAGE = RAW4_A_BYTES + RAW4_B_BYTES;          // 38912
+constexpr int COMP5_STAGE = COMP4_A_BYTES + COMP4_B_BYTES;       // 49152
+constexpr size_t BWD5_SMEM = 2 * (size_t)RAW5_STAGE + 2 * (size_t)COMP5_STAGE + 16;
+constexpr int REG5 = 2;                                          // levels in registers
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const u64 (&v)[16])
+{
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        w[2 * e] = (uint32_t)(v[e] & 0xffffffffull);
+        w[2 * e + 1] = (uint32_t)(v[e] >> 32);
+    }
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
+        "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
+        "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32_u64(uint32_t taddr, u64 (&v)[16])
+{
+    uint32_t w[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+          "=r"(w[7]), "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]),
+          "=r"(w[14]), "=r"(w[15]), "=r"(w[16]), "=r"(w[17]), "=r"(w[18]), "=r"(w[19]),
+          "=r"(w[20]), "=r"(w[21]), "=r"(w[22]), "=r"(w[23]), "=r"(w[24]), "=r"(w[25]),
+          "=r"(w[26]), "=r"(w[27]), "=r"(w[28]), "=r"(w[29]), "=r"(w[30]), "=r"(w[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        v[e] = (u64)w[2 * e] | ((u64)w[2 * e + 1] << 32);
+}
+
+template <bool FIRST>
+__device__ __forceinline__ void step5(u64 (&acc)[16], const ulonglong2& a03, const ulonglong2& a47,
+                                      const float4& b)
+{
+    const u64 P[4] = {a03.x, a03.y, a47.x, a47.y};
+    const u64 D[4] = {pack2(b.x, b.x), pack2(b.y, b.y), pack2(b.z, b.z), pack2(b.w, b.w)};
+    u64 prod[16];
+#pragma unroll
+    for (int ip = 0; ip < 4; ++ip)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            prod[ip * 4 + j] = fmul2_rn(P[ip], D[j]);
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        acc[e] = FIRST ? prod[e] : fadd2_ftz(acc[e], prod[e]);
+}
+
+template <bool DW>
+__global__ void __launch_bounds__(256, 1) k_bwd5(const BwdArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem5[];
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem5 + 2 * RAW5_STAGE + 2 * COMP5_STAGE);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ty = (warp >> 1) * 4 + (lane >> 3);
+    const int tx = (warp & 1) * 8 + (lane & 7);
+    const int64_t i0 = (int64_t)blockIdx.y * BI4, j0 = (int64_t)blockIdx.x * BT;
+    const float s = flush(*a.scale);
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // this thread's slice: lane 32*(warp%4)+lane, columns (warp/4)*256 + 32*(level-2)
+    const uint32_t tbase = *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 256);
+
+    const int64_t C = (a.R + CH - 1) / CH;
+    const int64_t cbeg = (int64_t)blockIdx.z << a.seg_log2;
+    const int64_t cend = min(C, cbeg + ((int64_t)1 << a.seg_log2));
+
+    auto rawA = [&](int b) { return reinterpret_cast<float*>(smem5 + b * RAW5_STAGE); };
+    auto rawB = [&](int b) { return reinterpret_cast<int8_t*>(smem5 + b * RAW5_STAGE + RAW4_A_BYTES); };
+    auto compA = [&](int b) { return reinterpret_cast<float*>(smem5 + 2 * RAW5_STAGE + b * COMP5_STAGE); };
+    auto compB = [&](int b) {
+        return reinterpret_cast<float*>(smem5 + 2 * RAW5_STAGE + b * COMP5_STAGE + COMP4_A_BYTES);
+    };
+    auto valid_of = [&](int64_t c) { return (int)min((int64_t)CH, a.R - c * CH); };
+
+    u64 S[REG5][16];
+    u64 acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        acc[e] = 0ull;
+#pragma unroll
+    for (int l = 0; l < REG5; ++l)
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            S[l][e] = 0ull;
+
+    // prologue: chunk cbeg transformed into compute buffer 0; chunk cbeg+1's
+    // raw copy in flight into raw buffer 1
+    issue_raw4<DW>(rawA(0), rawB(0), a, i0, j0, cbeg * CH, valid_of(cbeg), tid);
+    if (cbeg + 1 < cend)
+        issue_raw4<DW>(rawA(1), rawB(1), a, i0, j0, (cbeg + 1) * CH, valid_of(cbeg + 1), tid);
+    if (cbeg + 1 < cend)
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else
+        cp_async_wait_all();
+    __syncthreads();
+    transform4<DW>(compA(0), compB(0), rawA(0), rawB(0), s, tid);
+
+    for (int64_t c = cbeg; c < cend; ++c) {
+        const int cs = (int)(c - cbeg);
+        const int buf = cs & 1;
+        const bool more = c + 1 < cend;
+        // raw(c+1) has landed (this thread's pieces); after the barrier every
+        // thread's pieces are visible, compute buffer `buf` is complete, and
+        // every thread is done with raw buffer `buf` and compute buffer buf^1
+        cp_async_wait_all();
+        __syncthreads();
+        if (c + 2 < cend)
+            issue_raw4<DW>(rawA(buf), rawB(buf), a, i0, j0, (c + 2) * CH, valid_of(c + 2), tid);
+        if (more)
+            transform4<DW>(compA(buf ^ 1), compB(buf ^ 1), rawA(buf ^ 1), rawB(buf ^ 1), s, tid);
+
+        const int valid = valid_of(c);
+        const float* Ar = compA(buf) + 8 * ty;
+        const float* Br = compB(buf) + 4 * tx;
+        ulonglong2 a03 = *reinterpret_cast<const ulonglong2*>(Ar);
+        ulonglong2 a47 = *reinterpret_cast<const ulonglong2*>(Ar + 4);
+        float4 b = *reinterpret_cast<const float4*>(Br);
+        {
+            const ulonglong2 c03 = a03, c47 = a47;
+            const float4 cb = b;
+            if (valid > 1) {
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + BI4);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + BI4 + 4);
+                b = *reinterpret_cast<const float4*>(Br + BT);
+            }
+            step5<true>(acc, c03, c47, cb);
+        }
+        if (valid == CH) {
+#pragma unroll 7
+            for (int r = 1; r < CH; ++r) {
+                const ulonglong2 c03 = a03, c47 = a47;
+                const float4 cb = b;
+                const int rn = r + 1 < CH ? r + 1 : r;
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4 + 4);
+                b = *reinterpret_cast<const float4*>(Br + rn * BT);
+                step5<false>(acc, c03, c47, cb);
+            }
+        } else {
+            for (int r = 1; r < valid; ++r) {
+                const ulonglong2 c03 = a03, c47 = a47;
+                const float4 cb = b;
+                const int rn = r + 1 < valid ? r + 1 : r;
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4 + 4);
+                b = *reinterpret_cast<const float4*>(Br + rn * BT);
+                step5<false>(acc, c03, c47, cb);
+            }
+        }
+
+        // tree over chunk partials; levels >= REG5 go through tensor memory
+        if (more) {
+            const int tz = __ffs(~cs) - 1;
+#pragma unroll
+            for (int t = 0; t < MAXLVL; ++t) {
+                if (tz == t) {
+#pragma unroll
+                    for (int l = 0; l < t; ++l) {
+                        if (l < REG5) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                acc[e] = fadd2_ftz(S[l < REG5 ? l : 0][e], acc[e]);
+                        } else {
+                            u64 v[16];
+                            tmem_ld32_u64(tbase + (uint32_t)(32 * (l - REG5)), v);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                acc[e] = fadd2_ftz(v[e], acc[e]);
+                        }
+                    }
+                    if (t < REG5) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            S[t < REG5 ? t : 0][e] = acc[e];
+                    } else {
+                        tmem_st32(tbase + (uint32_t)(32 * (t - REG5)), acc);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int l = 0; l < MAXLVL; ++l) {
+                if ((cs >> l) & 1) {
+                    if (l < REG5) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            acc[e] = fadd2_ftz(S[l < REG5 ? l : 0][e], acc[e]);
+                    } else {
+                        u64 v[16];
+                        tmem_ld32_u64(tbase + (uint32_t)(32 * (l - REG5)), v);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            acc[e] = fadd2_ftz(v[e], acc[e]);
+                    }
+                }
+            }
+        }
+    }
+
+    const int64_t col = j0 + 4 * tx;
+#pragma unroll
+    for (int ip = 0; ip < 4; ++ip) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t row = i0 + 8 * ty + 2 * ip + h;
+            float o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo, hi;
+                unpack2(acc[ip * 4 + j], lo, hi);
+                o[j] = h ? hi : lo;
+            }
+            if (row >= a.I || col >= a.J)
+                continue;
+            if (a.nseg == 1) {
+                float* dst = a.out + row * a.J + col;
+                float v0 = flush(o[0]), v1 = flush(o[1]), v2 = flush(o[2]), v3 = flush(o[3]);
+                if (a.accumulate) {
+                    const float4 old = *reinterpret_cast<const float4*>(dst);
+                    v0 = fadd_ftz(old.x, v0);
+                    v1 = fadd_ftz(old.y, v1);
+                    v2 = fadd_ftz(old.z, v2);
+                    v3 = fadd_ftz(old.w, v3);
+                }
+                *reinterpret_cast<float4*>(dst) = make_float4(v0, v1, v2, v3);
+            } else {
+                float* base = a.ws + (int64_t)blockIdx.z * a.I * a.J;
+                *reinterpret_cast<float4*>(base + row * a.J + col) = make_float4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(*tmem_slot)
+                     : "memory");
+    }
+}
+
 // one level of the tree over segment partials: ws[j] <- ws[j] (+) ws[j + s]
 // for every j that is a multiple of 2s with j + s < nseg
 __global__ void k_seg_level(float* __restrict__ ws, int nseg, int s, int64_t count)
@@ -1190,6 +1473,57 @@ int64_t nseg_for(int64_t R, int seg_log2)
     return cdiv(cdiv(R, CH), (int64_t)1 << seg_log2);
 }
 
+// kernel variant actually launched for a shape (the staged kernels need
+// 16-byte-aligned rows) and its tile height
+int kernel_for(int64_t ldy, int64_t J)
+{
+    const int k = launch_cfg().bwd_kernel;
+    const bool aligned = (ldy % 4) == 0 && (J % 16) == 0;
+    if (k >= 2 && !aligned)
+        return 1;
+    return k;
+}
+
+int tile_rows(int kernel) { return kernel >= 3 ? BI4 : BT; }
+
+// Segment size when the launch configuration leaves it open.  One CTA runs
+// per SM, so a grid of tiles that is not close to a whole number of waves
+// wastes SMs in its last wave; splitting the reduction into aligned segments
+// multiplies the CTA count (the segment partials are then folded by the
+// pairwise passes, same bits).  Picks the fewest segments (at most 8) that
+// reach 95 % wave efficiency, else the most efficient split.
+int auto_seg_log2(int64_t I, int64_t J, int64_t R, int kernel)
+{
+    const int64_t C = cdiv(R, CH);
+    int kmax = 0;
+    while (((int64_t)1 << kmax) < C)
+        ++kmax;
+    if (kmax > MAXLVL)
+        kmax = MAXLVL;
+    const int64_t tiles = cdiv(J, BT) * cdiv(I, tile_rows(kernel));
+    const int64_t sms = num_sms();
+    int best = kmax;
+    double best_eff = -1.0;
+    for (int k = kmax; k >= 0 && k >= kmax - 3; --k) {
+        const int64_t ctas = tiles * nseg_for(R, k);
+        const double eff = (double)ctas / (double)(cdiv(ctas, sms) * sms);
+        if (eff >= 0.95)
+            return k;
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = k;
+        }
+    }
+    return best;
+}
+
+int resolve_seg(int seg_log2, int64_t I, int64_t J, int64_t R, int64_t ldy)
+{
+    if (seg_log2 >= 0)
+        return seg_log2;
+    return auto_seg_log2(I, J, R, kernel_for(ldy, J));
+}
+
 template <bool DW>
 cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out, int64_t I,
                 int64_t J, int64_t R, int64_t ldy, int seg_log2, bool accumulate, float* ws,
@@ -1204,6 +1538,7 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
         count_launches(1);
         return cudaGetLastError();
     }
+    seg_log2 = resolve_seg(seg_log2, I, J, R, ldy);
     BwdArgs a;
     a.dy = dy;
     a.q = q;
@@ -1218,13 +1553,20 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
     a.nseg = (int)nseg_for(R, seg_log2);
     a.accumulate = accumulate ? 1 : 0;
     dim3 grid((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BT), (unsigned)a.nseg);
-    // the staged kernel needs 16-byte-aligned rows: dY rows (N % 4) and int8
+    // the staged kernels need 16-byte-aligned rows: dY rows (N % 4) and int8
     // rows (J % 16); other shapes take the register-prefetch kernel
-    const bool aligned = (ldy % 4) == 0 && (J % 16) == 0;
-    const int kernel = launch_cfg().bwd_kernel;
+    const int kernel = kernel_for(ldy, J);
+    const bool aligned = kernel >= 2;
     if (kernel == 0) {
         k_bwd<DW><<<grid, 256, 0, st>>>(a);
-    } else if (kernel == 3 && aligned) {
+    } else if (kernel == 4 && aligned) {
+        cudaError_t e = cudaFuncSetAttribute(k_bwd5<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)BWD5_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        dim3 g5((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BI4), (unsigned)a.nseg);
+        k_bwd5<DW><<<g5, 256, BWD5_SMEM, st>>>(a);
+    } else if (kernel >= 3 && aligned) {
         cudaError_t e = cudaFuncSetAttribute(k_bwd4<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)BWD4_SMEM);
         if (e != cudaSuccess)
@@ -1262,7 +1604,9 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
 
 size_t bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int seg_log2)
 {
-    const int64_t sx = nseg_for(N, seg_log2), sw = nseg_for(M, seg_log2);
+    // dX: I = M, J = K, R = N, dY rows of N; dW: I = N, J = K, R = M
+    const int64_t sx = nseg_for(N, resolve_seg(seg_log2, M, K, N, N));
+    const int64_t sw = nseg_for(M, resolve_seg(seg_log2, N, K, M, N));
     const int64_t bx = sx > 1 ? sx * M * K : 0;
     const int64_t bw = sw > 1 ? sw * N * K : 0;
     return (size_t)((bx > bw ? bx : bw) * (int64_t)sizeof(float));

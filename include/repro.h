@@ -138,7 +138,8 @@ size_t repro_linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K);
  *   dw[n,k] <- dw[n,k] (+) dW[n,k] (one add of the fully formed dW; the same
  *   bits as repro_grad_accum on a stored dW).
  * ws: at least repro_linear_bwd_ws_bytes(M, N, K) bytes for the current
- * launch configuration (0 by default whenever M and N are <= 16384).
+ * launch configuration.  Long reductions, and grids too small to fill whole
+ * waves of SMs, are split into aligned segments whose partials live there.
  * M, N <= 4194240 (REPRO_ERR_SHAPE otherwise).
  * dx and dw must not overlap dy, xq or wq (REPRO_ERR_ALIAS).
  * ------------------------------------------------------------------------ */
@@ -187,12 +188,14 @@ int repro_treefold(const float* const* parts, int R, int64_t n, float* out,
  *   thread-safe; affects subsequent calls in this process.
  * ------------------------------------------------------------------------ */
 typedef struct {
-    int bwd_segment_log2;   /* -1: default; else 2^k chunks per backward reduction segment (0..8) */
+    int bwd_segment_log2;   /* -1: chosen per shape (whole-wave CTA counts); else 2^k chunks
+                               per backward reduction segment (0..8) */
     int reduce_block_log2;  /* -1: default; else 2^k chunk partials per block in repro_wscale (0..10) */
     int fwd_path;           /* -1: default (tensor cores when K % 8 == 0); 0: CUDA cores; 1: tensor cores */
     int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
-    int bwd_kernel;         /* -1: default (2); 0: plain; 1: register prefetch; 2: staged;
-                               3: staged wide tile (2 and 3 need aligned rows, else 1) */
+    int bwd_kernel;         /* -1: default; 0: plain; 1: register prefetch; 2: staged;
+                               3: staged wide tile; 4: wide tile with the tree in tensor
+                               memory (2-4 need 16-byte-aligned rows, else 1) */
 } repro_launch_cfg;
 
 /* ------------------------------------------------------------------------

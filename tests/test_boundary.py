@@ -113,6 +113,7 @@ def test_linear_bwd_argument_checks(L):
 
 def test_bwd_workspace_follows_segments(L):
     try:
+        repro.repro_set_launch_cfg(bwd_segment_log2=8)
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 0
         repro.repro_set_launch_cfg(bwd_segment_log2=4)
         # dW: 256 chunks / 16 = 16 segments of N x K partials
