@@ -160,7 +160,7 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
         return REPRO_ERR_ARG;
     if (cfg->elementwise_blocks < -1 || cfg->elementwise_blocks > (1 << 20))
         return REPRO_ERR_ARG;
-    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 4)
+    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 5)
         return REPRO_ERR_ARG;
     g_cfg.bwd_segment_log2 = cfg->bwd_segment_log2;
     g_cfg.reduce_block_log2 = cfg->reduce_block_log2;

@@ -1212,6 +1212,42 @@ __device__ __forceinline__ void tmem_ld32_u64(uint32_t taddr, u64 (&v)[16])
         v[e] = (u64)w[2 * e] | ((u64)w[2 * e + 1] << 32);
 }
 
+// 16-column halves (8 pairs) of a level, to keep the transient register peak low
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const u64* v)
+{
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        w[2 * e] = (uint32_t)(v[e] & 0xffffffffull);
+        w[2 * e + 1] = (uint32_t)(v[e] >> 32);
+    }
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// acc[e] <- level[e] (+) acc[e] for the 8 pairs of one half
+__device__ __forceinline__ void tmem_fold16(uint32_t taddr, u64* acc)
+{
+    uint32_t w[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+          "=r"(w[7]), "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]),
+          "=r"(w[14]), "=r"(w[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        acc[e] = fadd2_ftz((u64)w[2 * e] | ((u64)w[2 * e + 1] << 32), acc[e]);
+}
+
 template <bool FIRST>
 __device__ __forceinline__ void step5(u64 (&acc)[16], const ulonglong2& a03, const ulonglong2& a47,
                                       const float4& b)
@@ -1433,6 +1469,297 @@ __global__ void __launch_bounds__(256, 1) k_bwd5(const BwdArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Twelve-warp variant: k_bwd4's 8 x 4 thread tile on 384 threads (CTA tile
+// 192 x 64) so that three warps per SM sub-partition hide each other's
+// fixed-latency waits.  To fit 170 registers per thread, tree levels 0-1 stay
+// in registers, levels 2-6 live in tensor memory (warp w: lanes 32*(w%4)..,
+// a 160-column slice at (w/4)*160) and level 7 in shared memory.  Staging as
+// in k_bwd4 (cp.async raw copy, transform pass, two barriers per chunk).
+// ---------------------------------------------------------------------------
+
+constexpr int NT6 = 384;
+constexpr int BI6 = 192;
+constexpr int RAW6_A_BYTES = BI6 * 68 * 4;                     // 52224 (DX; DW: 64 x 196)
+constexpr int RAW6_B_BYTES = CH * BT;                          // 4096
+constexpr int COMP6_A_BYTES = CH * BI6 * 4;                    // 49152
+constexpr int COMP6_B_BYTES = CH * BT * 4;                     // 16384
+constexpr int EXT6_BYTES = 16 * NT6 * 8;                       // 49152: level 7
+constexpr size_t BWD6_SMEM = (size_t)RAW6_A_BYTES + RAW6_B_BYTES + COMP6_A_BYTES +
+                             COMP6_B_BYTES + EXT6_BYTES + 16;
+
+template <bool DW>
+__device__ __forceinline__ void issue_raw6(float* __restrict__ rawA, int8_t* __restrict__ rawB,
+                                           const BwdArgs& a, int64_t i0, int64_t j0, int64_t r0,
+                                           int valid, int tid)
+{
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int p = tid + it * NT6;
+        const float* src;
+        float* dst;
+        bool ok;
+        if (DW) {   // 64 rows (reduction) x 192 floats (i), pitch 196
+            const int row = p / 48, f = p % 48;
+            src = a.dy + (r0 + row) * a.ldy + i0 + 4 * f;
+            ok = row < valid && i0 + 4 * f < a.I;
+            dst = rawA + row * 196 + 4 * f;
+        } else {    // 192 rows (i) x 64 floats (reduction), pitch 68
+            const int row = p >> 4, f = p & 15;
+            src = a.dy + (i0 + row) * a.ldy + r0 + 4 * f;
+            ok = i0 + row < a.I && 4 * f < valid;
+            dst = rawA + row * 68 + 4 * f;
+        }
+        cp_async16(dst, ok ? src : a.dy, ok ? 16u : 0u);
+    }
+    if (tid < 256) {
+        const int row = tid >> 2, part = tid & 3;
+        const bool ok = row < valid && j0 + 16 * part < a.J;
+        const int8_t* src = ok ? a.q + (r0 + row) * a.J + j0 + 16 * part : a.q;
+        cp_async16(rawB + row * BT + 16 * part, src, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+}
+
+template <bool DW>
+__device__ __forceinline__ void transform6(float* __restrict__ As, float* __restrict__ Bs,
+                                           const float* __restrict__ rawA,
+                                           const int8_t* __restrict__ rawB, float s, int tid)
+{
+    if (DW) {
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int e = tid + it * NT6;
+            const int r = e / 48, f = e % 48;
+            const float4 v = *reinterpret_cast<const float4*>(rawA + r * 196 + 4 * f);
+            *reinterpret_cast<float4*>(&As[r * BI6 + 4 * f]) = flush4(v);
+        }
+    } else {
+        const int i = tid % BI6, fg = tid / BI6;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int f = fg + 2 * it;
+            const float4 v = *reinterpret_cast<const float4*>(rawA + i * 68 + 4 * f);
+            As[(4 * f + 0) * BI6 + i] = flush(v.x);
+            As[(4 * f + 1) * BI6 + i] = flush(v.y);
+            As[(4 * f + 2) * BI6 + i] = flush(v.z);
+            As[(4 * f + 3) * BI6 + i] = flush(v.w);
+        }
+    }
+    if (tid < 256) {
+        const int row = tid >> 2, part = tid & 3;
+        const int4 w = *reinterpret_cast<const int4*>(rawB + row * BT + 16 * part);
+        const int words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<float4*>(&Bs[row * BT + 16 * part + 4 * u]) = make_float4(
+                dequant((int)(int8_t)(words[u]), s), dequant((int)(int8_t)(words[u] >> 8), s),
+                dequant((int)(int8_t)(words[u] >> 16), s), dequant((int)(int8_t)(words[u] >> 24), s));
+    }
+}
+
+template <bool DW>
+__global__ void __launch_bounds__(NT6, 1) k_bwd6(const BwdArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem6[];
+    float* rawA = reinterpret_cast<float*>(smem6);
+    int8_t* rawB = reinterpret_cast<int8_t*>(smem6 + RAW6_A_BYTES);
+    float* As = reinterpret_cast<float*>(smem6 + RAW6_A_BYTES + RAW6_B_BYTES);
+    float* Bs = reinterpret_cast<float*>(smem6 + RAW6_A_BYTES + RAW6_B_BYTES + COMP6_A_BYTES);
+    u64* ext7 = reinterpret_cast<u64*>(smem6 + RAW6_A_BYTES + RAW6_B_BYTES + COMP6_A_BYTES +
+                                       COMP6_B_BYTES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem6 + RAW6_A_BYTES + RAW6_B_BYTES +
+                                                      COMP6_A_BYTES + COMP6_B_BYTES + EXT6_BYTES);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int ty = (warp >> 1) * 4 + (lane >> 3);   // rows 8ty .. 8ty+7 (ty < 24)
+    const int tx = (warp & 1) * 8 + (lane & 7);     // cols 4tx .. 4tx+3
+    const int64_t i0 = (int64_t)blockIdx.y * BI6, j0 = (int64_t)blockIdx.x * BT;
+    const float s = flush(*a.scale);
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tbase = *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) +
+                           (uint32_t)((warp >> 2) * 160);
+
+    const int64_t C = (a.R + CH - 1) / CH;
+    const int64_t cbeg = (int64_t)blockIdx.z << a.seg_log2;
+    const int64_t cend = min(C, cbeg + ((int64_t)1 << a.seg_log2));
+
+    u64 S[2][16];
+    u64 acc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        acc[e] = 0ull;
+#pragma unroll
+    for (int l = 0; l < 2; ++l)
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            S[l][e] = 0ull;
+
+    issue_raw6<DW>(rawA, rawB, a, i0, j0, cbeg * CH, (int)min((int64_t)CH, a.R - cbeg * CH), tid);
+    cp_async_wait_all();
+    __syncthreads();
+    transform6<DW>(As, Bs, rawA, rawB, s, tid);
+    __syncthreads();
+
+    const float* Ar = As + 8 * ty;
+    const float* Br = Bs + 4 * tx;
+
+    for (int64_t c = cbeg; c < cend; ++c) {
+        const int64_t r0 = c * CH;
+        const int valid = (int)min((int64_t)CH, a.R - r0);
+        const bool more = c + 1 < cend;
+        if (more)
+            issue_raw6<DW>(rawA, rawB, a, i0, j0, r0 + CH, (int)min((int64_t)CH, a.R - r0 - CH),
+                           tid);
+
+        ulonglong2 a03 = *reinterpret_cast<const ulonglong2*>(Ar);
+        ulonglong2 a47 = *reinterpret_cast<const ulonglong2*>(Ar + 4);
+        float4 b = *reinterpret_cast<const float4*>(Br);
+        {
+            const ulonglong2 c03 = a03, c47 = a47;
+            const float4 cb = b;
+            if (valid > 1) {
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + BI6);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + BI6 + 4);
+                b = *reinterpret_cast<const float4*>(Br + BT);
+            }
+            step4<true>(acc, c03, c47, cb);
+        }
+        if (valid == CH) {
+#pragma unroll 7
+            for (int r = 1; r < CH; ++r) {
+                const ulonglong2 c03 = a03, c47 = a47;
+                const float4 cb = b;
+                const int rn = r + 1 < CH ? r + 1 : r;
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI6);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI6 + 4);
+                b = *reinterpret_cast<const float4*>(Br + rn * BT);
+                step4<false>(acc, c03, c47, cb);
+            }
+        } else {
+            for (int r = 1; r < valid; ++r) {
+                const ulonglong2 c03 = a03, c47 = a47;
+                const float4 cb = b;
+                const int rn = r + 1 < valid ? r + 1 : r;
+                a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI6);
+                a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI6 + 4);
+                b = *reinterpret_cast<const float4*>(Br + rn * BT);
+                step4<false>(acc, c03, c47, cb);
+            }
+        }
+
+        // tree: levels 0-1 registers, 2-6 tensor memory, 7 shared memory
+        const int cs = (int)(c - cbeg);
+        if (more) {
+            const int tz = __ffs(~cs) - 1;
+#pragma unroll
+            for (int t = 0; t < MAXLVL; ++t) {
+                if (tz == t) {
+#pragma unroll
+                    for (int l = 0; l < t; ++l) {
+                        if (l < 2) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                acc[e] = fadd2_ftz(S[l < 2 ? l : 0][e], acc[e]);
+                        } else {
+                            tmem_fold16(tbase + (uint32_t)(32 * (l - 2)), acc);
+                            tmem_fold16(tbase + (uint32_t)(32 * (l - 2) + 16), acc + 8);
+                        }
+                    }
+                    if (t < 2) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            S[t < 2 ? t : 0][e] = acc[e];
+                    } else if (t < 7) {
+                        tmem_st16(tbase + (uint32_t)(32 * (t - 2)), acc);
+                        tmem_st16(tbase + (uint32_t)(32 * (t - 2) + 16), acc + 8);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            ext7[e * NT6 + tid] = acc[e];
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int l = 0; l < MAXLVL; ++l) {
+                if ((cs >> l) & 1) {
+                    if (l < 2) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            acc[e] = fadd2_ftz(S[l < 2 ? l : 0][e], acc[e]);
+                    } else if (l < 7) {
+                        tmem_fold16(tbase + (uint32_t)(32 * (l - 2)), acc);
+                        tmem_fold16(tbase + (uint32_t)(32 * (l - 2) + 16), acc + 8);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            acc[e] = fadd2_ftz(ext7[e * NT6 + tid], acc[e]);
+                    }
+                }
+            }
+        }
+
+        if (more) {
+            cp_async_wait_all();
+            __syncthreads();
+            transform6<DW>(As, Bs, rawA, rawB, s, tid);
+            __syncthreads();
+        }
+    }
+
+    const int64_t col = j0 + 4 * tx;
+#pragma unroll
+    for (int ip = 0; ip < 4; ++ip) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t row = i0 + 8 * ty + 2 * ip + h;
+            float o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float lo, hi;
+                unpack2(acc[ip * 4 + j], lo, hi);
+                o[j] = h ? hi : lo;
+            }
+            if (row >= a.I || col >= a.J)
+                continue;
+            if (a.nseg == 1) {
+                float* dst = a.out + row * a.J + col;
+                float v0 = flush(o[0]), v1 = flush(o[1]), v2 = flush(o[2]), v3 = flush(o[3]);
+                if (a.accumulate) {
+                    const float4 old = *reinterpret_cast<const float4*>(dst);
+                    v0 = fadd_ftz(old.x, v0);
+                    v1 = fadd_ftz(old.y, v1);
+                    v2 = fadd_ftz(old.z, v2);
+                    v3 = fadd_ftz(old.w, v3);
+                }
+                *reinterpret_cast<float4*>(dst) = make_float4(v0, v1, v2, v3);
+            } else {
+                float* base = a.ws + (int64_t)blockIdx.z * a.I * a.J;
+                *reinterpret_cast<float4*>(base + row * a.J + col) = make_float4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(*tmem_slot)
+                     : "memory");
+    }
+}
+
 // one level of the tree over segment partials: ws[j] <- ws[j] (+) ws[j + s]
 // for every j that is a multiple of 2s with j + s < nseg
 __global__ void k_seg_level(float* __restrict__ ws, int nseg, int s, int64_t count)
@@ -1484,7 +1811,7 @@ int kernel_for(int64_t ldy, int64_t J)
     return k;
 }
 
-int tile_rows(int kernel) { return kernel >= 3 ? BI4 : BT; }
+int tile_rows(int kernel) { return kernel == 5 ? BI6 : (kernel >= 3 ? BI4 : BT); }
 
 // Segment size when the launch configuration leaves it open.  One CTA runs
 // per SM, so a grid of tiles that is not close to a whole number of waves
@@ -1559,6 +1886,13 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
     const bool aligned = kernel >= 2;
     if (kernel == 0) {
         k_bwd<DW><<<grid, 256, 0, st>>>(a);
+    } else if (kernel == 5 && aligned) {
+        cudaError_t e = cudaFuncSetAttribute(k_bwd6<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)BWD6_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        dim3 g6((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BI6), (unsigned)a.nseg);
+        k_bwd6<DW><<<g6, NT6, BWD6_SMEM, st>>>(a);
     } else if (kernel == 4 && aligned) {
         cudaError_t e = cudaFuncSetAttribute(k_bwd5<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)BWD5_SMEM);

@@ -195,7 +195,8 @@ typedef struct {
     int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
     int bwd_kernel;         /* -1: default (3); 0: plain; 1: register prefetch; 2: staged;
                                3: staged wide tile; 4: wide tile with the tree in tensor
-                               memory (2-4 need 16-byte-aligned rows, else 1) */
+                               memory; 5: twelve-warp wide tile (2-5 need 16-byte-aligned
+                               rows, else 1) */
 } repro_launch_cfg;
 
 /* ------------------------------------------------------------------------
