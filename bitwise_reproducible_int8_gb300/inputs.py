@@ -119,6 +119,9 @@ WORKLOADS = {
                            "down projection, 4 micro-batches, dW accumulated in order"),
     "block": Workload("block", TOKENS_PER_MICROBATCH, (QKV, O_PROJ, GATE_UP, DOWN), 4, 6, 100, 0,
                       "one GQA decoder block's linears, 4 micro-batches, TreeFold over R=6"),
+    # profiling case: a few GB on the device, TreeFold inputs (6 x 92 MB) larger than L2
+    "gate_up_r6": Workload("gate_up_r6", TOKENS_PER_MICROBATCH, (GATE_UP,), 1, 6, 0, 0,
+                           "gate+up projection, one micro-batch, TreeFold over R=6"),
 }
 
 
