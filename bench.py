@@ -35,6 +35,12 @@ sys.path.insert(0, ROOT)
 from bitwise_reproducible_int8_gb300 import inputs  # noqa: E402
 
 METRIC = "tokens/s bit-exact int8-QAT linear fwd+bwd (1 GB300); % of int8/FP32/HBM roofline"
+
+# DRAM bytes (read + write) per backward launch of the default kernel, averaged over
+# the 160 backward launches of one block step, from one ncu capture of
+# dram__bytes_read.sum + dram__bytes_write.sum (single pass) on a GB300.  Valid only
+# for that kernel and workload; anything else reports null.
+BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd4"): 544.7e6}
 UNIT = "tokens/s"
 
 
@@ -309,13 +315,15 @@ def run_ours(args, wl):
         fp32_peak = sms * 128 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         achieved = bwd_ops / (bwd_ms / 1000.0) / 1e12 if bwd_ms > 0 else 0.0
         nb = launch_counts.get("bwd_dx", 0) + launch_counts.get("bwd_dw", 0)
+        kname = {0: "k_bwd", 1: "k_bwd2", 2: "k_bwd3", 3: "k_bwd4", 4: "k_bwd5",
+                 5: "k_bwd6"}[args.bwd_kernel if args.bwd_kernel >= 0 else 3]
         roofline = {
-            "bound": "alu", "kernel": "k_bwd (dX and dW, canonical-order fp32)",
+            "bound": "alu", "kernel": f"{kname} (dX and dW, canonical-order fp32)",
             "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
             "frac": achieved / fp32_peak if fp32_peak else None,
             "peak_note": f"FP32 pipe: {sms} SMs x 128 lanes x {peaks.get('sm_max_mhz', 2070.0):.0f} MHz,"
                          " one FMUL or FADD per lane per clock (no FMA may be used)",
-            "traffic": None, "launches": nb,
+            "traffic": BWD_TRAFFIC_PER_LAUNCH.get((wl.name, kname)), "launches": nb,
             "flops_per_launch": bwd_ops / nb if nb else None,
             "avg_launch_ms": bwd_ms / nb if nb else None,
         }
