@@ -259,11 +259,8 @@ def run_ours(args, wl):
     hp = S.HotPathStep(wl_r, host, fused_accum=not args.unfused_accum)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        if wl_r.replicas > 1:
-            tf, hp.TF = hp.TF, None
-            hp.run(stream)
-            hp.prepare_replicas(stream)
-            hp.TF = tf
+        if wl_r.replicas > 1 or wl_r.shards > 1:
+            hp.prepare(stream)
         for _ in range(args.warmup):
             hp.run(stream)
     stream.synchronize()
@@ -349,7 +346,8 @@ def run_ours(args, wl):
             "config": {"workload": wl.name, "tokens_per_step": hp.tokens(),
                        "micro_batches": wl.microbatches, "micro_batch_tokens": wl.tokens,
                        "linears": [f"{l.name} {l.n_out}x{l.k_in}" for l in wl.linears],
-                       "replicas": wl.replicas, "parallelism": "replicas only",
+                       "replicas": wl.replicas, "shards": wl.shards,
+                       "parallelism": "replicas only",
                        "accumulation": "unfused repro_grad_accum" if args.unfused_accum
                        else "fused into the dW epilogue",
                        "l2": f"inputs larger than L2: {resident_gb(hp):.1f} GB resident, "
@@ -381,6 +379,11 @@ def hbm_bytes(hp) -> dict:
     out = {"wscale_w": 4 * nw, "quant_w": 5 * nw, "wscale_x": 4 * nx, "quant_x": 5 * nx}
     if hp.TF is not None:
         out["treefold"] = 4 * (wl.replicas + 1) * hp.n_grad
+    if hp.G2 is not None:
+        out["running_sum"] = 4 * (wl.shards + 1) * hp.n_grad
+    if hp.use_optimizer:
+        out["sumsq"] = 4 * hp.n_grad
+        out["adamw"] = 28 * hp.n_grad
     if hp.dW_tmp is not None:
         out["accum"] = 12 * nw * (J - 1)
     return out

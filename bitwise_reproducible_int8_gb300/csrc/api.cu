@@ -366,6 +366,96 @@ int repro_grad_accum(float* acc, const float* g, int64_t n, void* stream)
     return status_of(launch_grad_accum(acc, g, n, stream_grid(n / 4), as_stream(stream)));
 }
 
+size_t repro_sumsq_ws_bytes(int64_t n)
+{
+    if (n <= 0)
+        return 0;
+    return wscale_ws_bytes(n, 0);
+}
+
+int repro_sumsq(const float* g, int64_t n, float* out, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!g || !out)
+        return REPRO_ERR_ARG;
+    if (n <= 0)
+        return REPRO_ERR_SHAPE;
+    if (!al16(g) || !al4(out))
+        return REPRO_ERR_ALIGN;
+    if (!ws || ws_bytes < repro_sumsq_ws_bytes(n))
+        return REPRO_ERR_WORKSPACE;
+    if (!al16(ws))
+        return REPRO_ERR_ALIGN;
+    if (overlap(ws, ws_bytes, g, (size_t)n * 4) || overlap(ws, ws_bytes, out, 4))
+        return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_sumsq(g, n, out, ws, g_cfg.reduce_block_log2, as_stream(stream)));
+}
+
+int repro_adamw_step(float* p, float* m, float* v, const float* g, int64_t n, const float* sumsq,
+                     const repro_adamw_hparams* hp, int64_t t, void* stream)
+{
+    if (!hp || t < 1)
+        return REPRO_ERR_ARG;
+    if (n < 0)
+        return REPRO_ERR_SHAPE;
+    if (n == 0)
+        return REPRO_OK;
+    if (!p || !m || !v || !g || !sumsq)
+        return REPRO_ERR_ARG;
+    if (!al16(p) || !al16(m) || !al16(v) || !al16(g) || !al4(sumsq))
+        return REPRO_ERR_ALIGN;
+    const size_t nb = (size_t)n * 4;
+    if (overlap(p, nb, m, nb) || overlap(p, nb, v, nb) || overlap(m, nb, v, nb) ||
+        overlap(g, nb, p, nb) || overlap(g, nb, m, nb) || overlap(g, nb, v, nb) ||
+        overlap(sumsq, 4, p, nb) || overlap(sumsq, 4, m, nb) || overlap(sumsq, 4, v, nb))
+        return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    AdamWArgs h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_norm};
+    return status_of(launch_adamw(p, m, v, g, n, sumsq, h, t, stream_grid(n / 4), as_stream(stream)));
+}
+
+// shared checks of the multi-input folds (running sum, TreeFold)
+static int check_parts(const float* const* parts, int count, int64_t n, const float* out)
+{
+    if (!parts || count < 1 || count > REPRO_MAX_REPLICAS)
+        return REPRO_ERR_ARG;
+    if (n < 0)
+        return REPRO_ERR_SHAPE;
+    if (!out)
+        return REPRO_ERR_ARG;
+    for (int r = 0; r < count; ++r) {
+        if (!parts[r])
+            return REPRO_ERR_ARG;
+        if (!al16(parts[r]))
+            return REPRO_ERR_ALIGN;
+    }
+    if (!al16(out))
+        return REPRO_ERR_ALIGN;
+    const size_t nb = (size_t)n * 4;
+    for (int r = 0; r < count; ++r) {
+        if (r == 0 && parts[0] == out)
+            continue;
+        if (overlap(out, nb, parts[r], nb))
+            return REPRO_ERR_ALIAS;
+    }
+    return REPRO_OK;
+}
+
+int repro_running_sum(const float* const* parts, int S, int64_t n, float* out, void* stream)
+{
+    int st = check_parts(parts, S, n, out);
+    if (st != REPRO_OK || n == 0)
+        return st;
+    st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_running_sum(parts, S, n, out, stream_grid(n / 4), as_stream(stream)));
+}
+
 int repro_treefold(const float* const* parts, int R, int64_t n, float* out, void* stream)
 {
     if (!parts || R < 1 || R > REPRO_MAX_REPLICAS)

@@ -32,6 +32,17 @@ cudaError_t launch_wscale_amax(const float* x, int64_t n, int qmax, float* scale
                                void* ws, int grid, cudaStream_t st);
 int amax_grid(int64_t n);
 
+cudaError_t launch_sumsq(const float* x, int64_t n, float* out, void* ws, int block_log2,
+                         cudaStream_t st);
+
+// ---- optimiser (k_optim.cu)
+struct AdamWArgs {
+    float lr, beta1, beta2, eps, weight_decay, max_norm;
+};
+cudaError_t launch_adamw(float* p, float* m, float* v, const float* g, int64_t n,
+                         const float* sumsq, const AdamWArgs& h, int64_t t, int grid,
+                         cudaStream_t st);
+
 // ---- quantiser (k_quant.cu)
 cudaError_t launch_quant(const float* x, int64_t n, const float* scale, int qmax, int8_t* q,
                          int grid, cudaStream_t st);
@@ -58,6 +69,8 @@ cudaError_t launch_bwd_dw(const float* dy, const int8_t* xq, const float* s_x, f
 
 // ---- reductions (k_reduce.cu)
 cudaError_t launch_grad_accum(float* acc, const float* g, int64_t n, int grid, cudaStream_t st);
+cudaError_t launch_running_sum(const float* const* parts, int S, int64_t n, float* out, int grid,
+                               cudaStream_t st);
 cudaError_t launch_treefold(const float* const* parts, int R, int64_t n, float* out, int grid,
                             cudaStream_t st);
 

@@ -120,7 +120,69 @@ k_treefold_generic(const Parts parts, int R, int64_t n, float* out)
     }
 }
 
+// level 2: left fold of S shard partials in mesh order (first taken as it is)
+template <int S>
+__global__ void __launch_bounds__(256)
+k_running_sum(const Parts parts, int64_t n, float* out)
+{
+    const int64_t nv = n >> 2;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float4 a = __ldg(reinterpret_cast<const float4*>(parts.p[0]) + i);
+#pragma unroll
+        for (int s = 1; s < S; ++s) {
+            const float4 b = __ldg(reinterpret_cast<const float4*>(parts.p[s]) + i);
+            a.x = fadd_ftz(a.x, b.x);
+            a.y = fadd_ftz(a.y, b.y);
+            a.z = fadd_ftz(a.z, b.z);
+            a.w = fadd_ftz(a.w, b.w);
+        }
+        reinterpret_cast<float4*>(out)[i] = a;
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 3)) {
+        const int64_t i = (nv << 2) + threadIdx.x;
+        float a = parts.p[0][i];
+#pragma unroll
+        for (int s = 1; s < S; ++s)
+            a = fadd_ftz(a, parts.p[s][i]);
+        out[i] = a;
+    }
+}
+
+__global__ void __launch_bounds__(256)
+k_running_sum_generic(const Parts parts, int S, int64_t n, float* out)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        float a = parts.p[0][i];
+        for (int s = 1; s < S; ++s)
+            a = fadd_ftz(a, parts.p[s][i]);
+        out[i] = a;
+    }
+}
+
 } // namespace
+
+cudaError_t launch_running_sum(const float* const* parts, int S, int64_t n, float* out, int grid,
+                               cudaStream_t st)
+{
+    Parts P;
+    for (int r = 0; r < REPRO_MAX_PARTS_INTERNAL; ++r)
+        P.p[r] = r < S ? parts[r] : nullptr;
+    switch (S) {
+    case 1: k_running_sum<1><<<grid, 256, 0, st>>>(P, n, out); break;
+    case 2: k_running_sum<2><<<grid, 256, 0, st>>>(P, n, out); break;
+    case 3: k_running_sum<3><<<grid, 256, 0, st>>>(P, n, out); break;
+    case 4: k_running_sum<4><<<grid, 256, 0, st>>>(P, n, out); break;
+    case 5: k_running_sum<5><<<grid, 256, 0, st>>>(P, n, out); break;
+    case 6: k_running_sum<6><<<grid, 256, 0, st>>>(P, n, out); break;
+    case 7: k_running_sum<7><<<grid, 256, 0, st>>>(P, n, out); break;
+    case 8: k_running_sum<8><<<grid, 256, 0, st>>>(P, n, out); break;
+    default: k_running_sum_generic<<<grid, 256, 0, st>>>(P, S, n, out); break;
+    }
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_grad_accum(float* acc, const float* g, int64_t n, int grid, cudaStream_t st)
 {

@@ -27,6 +27,15 @@ constexpr int P2_MAX = 1024;     // partials (and threads) per tree-pass CTA
 // shared memory with coalesced 16-byte loads; chunk j's 16 float4 are stored
 // XOR-swizzled (slot p ^ (j & 15)) so both the fill and the per-thread reads
 // are free of bank conflicts.
+// term of the canonical sum: |x| (weight scale) or x (x) x (squared norm); a
+// subnormal x gives a term the first add reads as zero either way
+template <int SQUARE>
+__device__ __forceinline__ float term(float x)
+{
+    return SQUARE ? fmul_rn(x, x) : fabsf(x);
+}
+
+template <int SQUARE>
 __global__ void __launch_bounds__(P1_CHUNKS)
 k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __restrict__ part)
 {
@@ -60,24 +69,24 @@ k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __re
         float a;
         if (len == 64) {
             float4 v = S[j * 16 + (0 ^ (j & 15))];
-            a = fabsf(v.x);
-            a = fadd_ftz(a, fabsf(v.y));
-            a = fadd_ftz(a, fabsf(v.z));
-            a = fadd_ftz(a, fabsf(v.w));
+            a = term<SQUARE>(v.x);
+            a = fadd_ftz(a, term<SQUARE>(v.y));
+            a = fadd_ftz(a, term<SQUARE>(v.z));
+            a = fadd_ftz(a, term<SQUARE>(v.w));
 #pragma unroll
             for (int p = 1; p < 16; ++p) {
                 v = S[j * 16 + (p ^ (j & 15))];
-                a = fadd_ftz(a, fabsf(v.x));
-                a = fadd_ftz(a, fabsf(v.y));
-                a = fadd_ftz(a, fabsf(v.z));
-                a = fadd_ftz(a, fabsf(v.w));
+                a = fadd_ftz(a, term<SQUARE>(v.x));
+                a = fadd_ftz(a, term<SQUARE>(v.y));
+                a = fadd_ftz(a, term<SQUARE>(v.z));
+                a = fadd_ftz(a, term<SQUARE>(v.w));
             }
         } else {
             a = 0.f;
             for (int i = 0; i < len; ++i) {
                 const float4 v = S[j * 16 + ((i >> 2) ^ (j & 15))];
                 const int u = i & 3;
-                const float t = fabsf(u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w);
+                const float t = term<SQUARE>(u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w);
                 a = (i == 0) ? t : fadd_ftz(a, t);
             }
         }
@@ -125,8 +134,10 @@ k_tree_pass(const float* __restrict__ in, int64_t cnt_total, int blk_log2,
         __syncthreads();
     }
     if (threadIdx.x == 0) {
-        if (final_pass)
+        if (final_pass == 1)
             scale_out[0] = weight_scale_from_sum(T[0], n, qmax);
+        else if (final_pass == 2)
+            scale_out[0] = flush(T[0]);      // the canonical sum itself
         else
             out[blockIdx.x] = T[0];
     }
@@ -215,8 +226,11 @@ size_t wscale_ws_bytes(int64_t n, int block_log2)
     return (size_t)(c1 + c2 + 64) * sizeof(float);
 }
 
-cudaError_t launch_wscale_meanabs(const float* x, int64_t n, int qmax, float* scale_out,
-                                  void* ws, int block_log2, cudaStream_t st)
+// canonical sum of |x_i| (square = 0) or x_i (x) x_i (square = 1); with
+// square = 0 the last pass turns the sum into the weight scale, with
+// square = 1 it stores the sum
+static cudaError_t canonical_sum(const float* x, int64_t n, int square, int qmax, float* out,
+                                 void* ws, int block_log2, cudaStream_t st)
 {
     int p1, p2;
     split_blocks(block_log2, p1, p2);
@@ -224,13 +238,17 @@ cudaError_t launch_wscale_meanabs(const float* x, int64_t n, int qmax, float* sc
     int64_t cnt = cdiv(C, (int64_t)1 << p1);
     float* regA = static_cast<float*>(ws);
     float* regB = regA + cnt + 32;
-    k_absum_chunks<<<(unsigned)cnt, P1_CHUNKS, 0, st>>>(x, n, p1, regA);
+    float* scale_out = out;
+    if (square)
+        k_absum_chunks<1><<<(unsigned)cnt, P1_CHUNKS, 0, st>>>(x, n, p1, regA);
+    else
+        k_absum_chunks<0><<<(unsigned)cnt, P1_CHUNKS, 0, st>>>(x, n, p1, regA);
     count_launches(1);
     float* src = regA;
     float* dst = regB;
     for (;;) {
         const int64_t grid = cdiv(cnt, (int64_t)1 << p2);
-        const int final_pass = grid == 1;
+        const int final_pass = grid == 1 ? (square ? 2 : 1) : 0;
         k_tree_pass<<<(unsigned)grid, P2_MAX, 0, st>>>(src, cnt, p2, dst, final_pass, n, qmax,
                                                        scale_out);
         count_launches(1);
@@ -242,6 +260,18 @@ cudaError_t launch_wscale_meanabs(const float* x, int64_t n, int qmax, float* sc
         dst = t;
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_wscale_meanabs(const float* x, int64_t n, int qmax, float* scale_out,
+                                  void* ws, int block_log2, cudaStream_t st)
+{
+    return canonical_sum(x, n, 0, qmax, scale_out, ws, block_log2, st);
+}
+
+cudaError_t launch_sumsq(const float* x, int64_t n, float* out, void* ws, int block_log2,
+                         cudaStream_t st)
+{
+    return canonical_sum(x, n, 1, 0, out, ws, block_log2, st);
 }
 
 int amax_grid(int64_t n)

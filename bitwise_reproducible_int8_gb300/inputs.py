@@ -106,6 +106,8 @@ class Workload:
     w_seed_base: int = 0        # weight i uses seed w_seed_base + i
     x_seed_base: int = 0        # micro-batch j uses seed x_seed_base + j
     description: str = field(default="", compare=False)
+    shards: int = 1             # S for the level-2 running sum (1: none)
+    optimizer: bool = False     # clip + AdamW on the folded gradient after TreeFold
 
 
 WORKLOADS = {
@@ -119,6 +121,11 @@ WORKLOADS = {
                            "down projection, 4 micro-batches, dW accumulated in order"),
     "block": Workload("block", TOKENS_PER_MICROBATCH, (QKV, O_PROJ, GATE_UP, DOWN), 4, 6, 100, 0,
                       "one GQA decoder block's linears, 4 micro-batches, TreeFold over R=6"),
+    # the audit's full three-level replay: micro-batch accumulation, running sum
+    # over S = 8 shard partials of this replica (mesh order), TreeFold over R = 6
+    "block_audit": Workload("block_audit", TOKENS_PER_MICROBATCH, (QKV, O_PROJ, GATE_UP, DOWN), 4, 6,
+                            100, 0, "block linears, 4 micro-batches, 8 shards, 6 replicas, "
+                            "then clip + AdamW", 8, True),
     # profiling case: a few GB on the device, TreeFold inputs (6 x 92 MB) larger than L2
     "gate_up_r6": Workload("gate_up_r6", TOKENS_PER_MICROBATCH, (GATE_UP,), 1, 6, 0, 0,
                            "gate+up projection, one micro-batch, TreeFold over R=6"),
@@ -146,6 +153,10 @@ def upstream_grad(wl: Workload, i: int, mb: int, rows: int | None = None) -> np.
 
 def replica_noise(wl: Workload, r: int, n: int) -> np.ndarray:
     return normal(1000 + r, S_NOISE, (n,), 1e-5)
+
+
+def shard_noise(wl: Workload, s: int, n: int) -> np.ndarray:
+    return normal(2000 + s, S_NOISE, (n,), 1e-5)
 
 
 def small_case(seed: int, M: int, N: int, K: int, x_std=1.0, w_std=0.02, dy_std=1e-3):

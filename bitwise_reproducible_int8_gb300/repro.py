@@ -35,6 +35,11 @@ class ReproError(RuntimeError):
                          f"({lib().repro_status_str(status).decode()})")
 
 
+class AdamWHparams(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_float) for k in
+                ("lr", "beta1", "beta2", "eps", "weight_decay", "max_norm")]
+
+
 class LaunchCfg(ctypes.Structure):
     _fields_ = [("bwd_segment_log2", ctypes.c_int), ("reduce_block_log2", ctypes.c_int),
                 ("fwd_path", ctypes.c_int), ("elementwise_blocks", ctypes.c_int),
@@ -58,6 +63,11 @@ _SIGNATURES = {
     "repro_linear_bwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
     "repro_grad_accum": (_int, [_vp, _vp, _i64, _vp]),
     "repro_treefold": (_int, [ctypes.POINTER(_vp), _int, _i64, _vp, _vp]),
+    "repro_running_sum": (_int, [ctypes.POINTER(_vp), _int, _i64, _vp, _vp]),
+    "repro_sumsq": (_int, [_vp, _i64, _vp, _vp, _sz, _vp]),
+    "repro_sumsq_ws_bytes": (_sz, [_i64]),
+    "repro_adamw_step": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, ctypes.POINTER(AdamWHparams),
+                                _i64, _vp]),
     "repro_status_str": (ctypes.c_char_p, [_int]),
     "repro_version": (_int, []),
     "repro_device_check": (_int, [_vp]),
@@ -215,6 +225,17 @@ def repro_grad_accum(acc: torch.Tensor, g: torch.Tensor, stream=None) -> None:
         _stream(stream)))
 
 
+def repro_running_sum(parts, out: torch.Tensor, stream=None) -> None:
+    """out <- left fold of the partials in the given (mesh) order."""
+    S = len(parts)
+    n = out.numel()
+    if any(p.numel() != n for p in parts):
+        raise ValueError("every partial must have out.numel() elements")
+    arr = (_vp * max(S, 1))(*[_ptr(p, torch.float32, "part") for p in parts])
+    _check("repro_running_sum", lib().repro_running_sum(arr, S, n, _ptr(out, torch.float32, "out"),
+                                                        _stream(stream)))
+
+
 def repro_treefold(parts, out: torch.Tensor, stream=None) -> None:
     R = len(parts)
     n = out.numel()
@@ -223,6 +244,35 @@ def repro_treefold(parts, out: torch.Tensor, stream=None) -> None:
     arr = (_vp * max(R, 1))(*[_ptr(p, torch.float32, "part") for p in parts])
     _check("repro_treefold", lib().repro_treefold(arr, R, n, _ptr(out, torch.float32, "out"),
                                                   _stream(stream)))
+
+
+def repro_sumsq_ws_bytes(n: int) -> int:
+    return int(lib().repro_sumsq_ws_bytes(int(n)))
+
+
+def repro_sumsq(g: torch.Tensor, out: torch.Tensor, ws=None, stream=None) -> None:
+    """out[0] <- canonical sum of g_i (x) g_i."""
+    n = g.numel()
+    if ws is None:
+        ws = _workspace(repro_sumsq_ws_bytes(n), g.device)
+    _check("repro_sumsq", lib().repro_sumsq(
+        _ptr(g, torch.float32, "g"), n, _ptr(out, torch.float32, "out"), _ptr(ws, None, "ws"),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def repro_adamw_step(p: torch.Tensor, m: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                     sumsq: torch.Tensor, t: int, lr: float = 4.5e-4, beta1: float = 0.9,
+                     beta2: float = 0.95, eps: float = 1e-8, weight_decay: float = 0.1,
+                     max_norm: float = 1.0, stream=None) -> None:
+    """Clip to the global norm sqrt(sumsq) and apply AdamW step t in place."""
+    n = p.numel()
+    if not (m.numel() == v.numel() == g.numel() == n):
+        raise ValueError("p, m, v and g must have the same number of elements")
+    hp = AdamWHparams(lr, beta1, beta2, eps, weight_decay, max_norm)
+    _check("repro_adamw_step", lib().repro_adamw_step(
+        _ptr(p, torch.float32, "p"), _ptr(m, torch.float32, "m"), _ptr(v, torch.float32, "v"),
+        _ptr(g, torch.float32, "g"), n, _ptr(sumsq, torch.float32, "sumsq"), ctypes.byref(hp),
+        int(t), _stream(stream)))
 
 
 def repro_status_str(status: int) -> str:

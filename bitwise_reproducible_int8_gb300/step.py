@@ -7,12 +7,18 @@ then for every micro-batch j and linear i:
   accumulated into the linear's gradient in micro-batch order (level 1 of the
   replayed reduction);
 and finally, when the workload has R > 1 replicas, TreeFold of the flat
-gradient buffer with the R - 1 other replicas' partials (level 3).
+gradient buffer with the R - 1 other replicas' partials (level 3), and, for
+workloads with an optimiser, the global gradient norm and a clipped AdamW
+update of the (flat) weights, which the next step re-pins and quantises.
 
-The other replicas' partials are built once, outside any timed region, as
-P_r = G (+) noise_r from this replica's accumulated gradient G -- the same
-construction as the small single-linear case -- so that every step folds six
-real-sized, gradient-like buffers.  All arithmetic happens in librepro.so; this
+With S > 1 shards (the audit's full three-level replay), level 2 folds this
+virtual rank's G with the S - 1 other shards' partials of the same replica as a
+running sum in mesh order, before TreeFold.
+
+The other shards' and replicas' partials are built once, outside any timed
+region, as Q_s = G (+) noise_s and P_r = G_2 (+) noise_r (G_2 the level-2 sum,
+or G without shards) -- the same construction as the small single-linear case
+-- so that every step folds real-sized, gradient-like buffers.  All arithmetic happens in librepro.so; this
 module only allocates device memory (torch) and enqueues calls.
 """
 from __future__ import annotations
@@ -32,6 +38,7 @@ class HostInputs:
     X: list          # [i][j] -> np.float32 [M, K_i]
     dY: list         # [i][j] -> np.float32 [M, N_i]
     noise: list      # [r] -> np.float32 [sum N_i K_i]  (r = 1..R-1; index 0 unused)
+    shard_noise: list = None   # [s] -> np.float32 [sum N_i K_i] (s = 1..S-1; index 0 unused)
 
 
 def generate_host_inputs(wl: inputs.Workload) -> HostInputs:
@@ -41,7 +48,8 @@ def generate_host_inputs(wl: inputs.Workload) -> HostInputs:
     dY = [[inputs.upstream_grad(wl, i, j) for j in range(wl.microbatches)] for i in range(L)]
     n_grad = sum(l.n_out * l.k_in for l in wl.linears)
     noise = [None] + [inputs.replica_noise(wl, r, n_grad) for r in range(1, max(wl.replicas, 1))]
-    return HostInputs(W, X, dY, noise)
+    snoise = [None] + [inputs.shard_noise(wl, s, n_grad) for s in range(1, max(wl.shards, 1))]
+    return HostInputs(W, X, dY, noise, snoise)
 
 
 def grad_offsets(wl: inputs.Workload):
@@ -68,7 +76,11 @@ class HotPathStep:
         L, J, M = len(wl.linears), wl.microbatches, wl.tokens
         h = self.host
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
-        self.W = [t(h.W[i]) for i in range(L)]
+        offs, n_grad = grad_offsets(wl)
+        # weights as views of one flat buffer laid out like the flat gradient
+        self.Wflat = torch.cat([t(h.W[i]).reshape(-1) for i in range(L)])
+        self.W = [self.Wflat[o:o + l.n_out * l.k_in].view(l.n_out, l.k_in)
+                  for o, l in zip(offs, wl.linears)]
         self.X = [[t(h.X[i][j]) for j in range(J)] for i in range(L)]
         self.dY = [[t(h.dY[i][j]) for j in range(J)] for i in range(L)]
         self.Wq = [torch.empty(w.shape, dtype=torch.int8, device=dev) for w in self.W]
@@ -77,7 +89,6 @@ class HotPathStep:
         self.s_x = torch.zeros(L, dtype=torch.float32, device=dev)
         self.Y = [torch.empty((M, l.n_out), dtype=torch.float32, device=dev) for l in wl.linears]
         self.dX = [torch.empty((M, l.k_in), dtype=torch.float32, device=dev) for l in wl.linears]
-        offs, n_grad = grad_offsets(wl)
         self.n_grad = n_grad
         self.G = torch.empty(n_grad, dtype=torch.float32, device=dev)
         self.Gv = [self.G[o:o + l.n_out * l.k_in].view(l.n_out, l.k_in)
@@ -98,6 +109,18 @@ class HotPathStep:
         self.TF = None
         if wl.replicas > 1:
             self.TF = torch.empty(n_grad, dtype=torch.float32, device=dev)
+        self.shard_parts = None
+        self.G2 = None
+        if wl.shards > 1:
+            self.G2 = torch.empty(n_grad, dtype=torch.float32, device=dev)
+        self.use_optimizer = wl.optimizer
+        self.step_t = 0
+        if wl.optimizer:
+            self.m = torch.zeros(n_grad, dtype=torch.float32, device=dev)
+            self.v = torch.zeros(n_grad, dtype=torch.float32, device=dev)
+            self.sumsq = torch.zeros(1, dtype=torch.float32, device=dev)
+            self.ws_sumsq = torch.empty(max(R.repro_sumsq_ws_bytes(n_grad), 16),
+                                        dtype=torch.uint8, device=dev)
 
     # ------------------------------------------------------------------ step
 
@@ -167,26 +190,63 @@ class HotPathStep:
                     self._ev(timers, "accum", s)
                     R.repro_grad_accum(self.Gv[i], self.dW_tmp[i], stream=s)
                     self._end(timers, "accum", s)
-        if self.TF is not None:
+        level2 = self.G
+        if self.G2 is not None and self.shard_parts is not None:
+            self._ev(timers, "running_sum", s)
+            R.repro_running_sum([self.G] + self.shard_parts, self.G2, stream=s)
+            self._end(timers, "running_sum", s)
+            level2 = self.G2
+        if self.TF is not None and not getattr(self, "skip_treefold", False):
             if self.parts is None:
                 raise RuntimeError("prepare_replicas() must run before a step with TreeFold")
             self._ev(timers, "treefold", s)
-            R.repro_treefold([self.G] + self.parts, self.TF, stream=s)
+            R.repro_treefold([level2] + self.parts, self.TF, stream=s)
             self._end(timers, "treefold", s)
+        if self.use_optimizer and not getattr(self, "skip_treefold", False):
+            grad = self.result()
+            self.step_t += 1
+            self._ev(timers, "sumsq", s)
+            R.repro_sumsq(grad, self.sumsq, ws=self.ws_sumsq, stream=s)
+            self._end(timers, "sumsq", s)
+            self._ev(timers, "adamw", s)
+            R.repro_adamw_step(self.Wflat, self.m, self.v, grad, self.sumsq, self.step_t, stream=s)
+            self._end(timers, "adamw", s)
 
     def prepare_replicas(self, stream: torch.cuda.Stream) -> None:
-        """P_r = G (+) noise_r for r = 1..R-1, from the current G (untimed)."""
+        """Q_s = G (+) shard_noise_s (s = 1..S-1), then G_2 = running sum, then
+        P_r = G_2 (+) noise_r (r = 1..R-1), from the current G (untimed)."""
+        base = self.G
+        if self.G2 is not None:
+            self.shard_parts = []
+            for sh in range(1, self.wl.shards):
+                q = self.G.clone()
+                R.repro_grad_accum(q, torch.from_numpy(self.host.shard_noise[sh]).to(self.dev),
+                                   stream=stream)
+                self.shard_parts.append(q)
+            R.repro_running_sum([self.G] + self.shard_parts, self.G2, stream=stream)
+            base = self.G2
         if self.wl.replicas <= 1:
             return
         self.parts = []
         for r in range(1, self.wl.replicas):
-            p = self.G.clone()
+            p = base.clone()
             R.repro_grad_accum(p, torch.from_numpy(self.host.noise[r]).to(self.dev), stream=stream)
             self.parts.append(p)
 
     def result(self) -> torch.Tensor:
-        """The step's result: the folded gradient (or G without TreeFold)."""
-        return self.TF if self.TF is not None else self.G
+        """The step's result: the folded gradient (or the level-2 sum, or G)."""
+        if self.TF is not None:
+            return self.TF
+        return self.G2 if self.G2 is not None else self.G
+
+    def prepare(self, stream: torch.cuda.Stream) -> None:
+        """One step without the folds that need the other ranks' partials, then
+        build those partials (everything untimed)."""
+        self.skip_treefold, shards = True, self.shard_parts
+        self.shard_parts = None
+        self.run(stream)
+        self.skip_treefold, self.shard_parts = False, shards
+        self.prepare_replicas(stream)
 
     def flops(self):
         """Algorithmic work of one step: int8 MACs (forward) and fp32

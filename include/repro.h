@@ -159,6 +159,20 @@ size_t repro_linear_bwd_ws_bytes(int64_t M, int64_t N, int64_t K);
 int repro_grad_accum(float* acc, const float* g, int64_t n, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Reduce-scatter replay ([limits], level 2: the intra-node reduce-scatter is
+ * replayed as a running sum in one loop over virtual ranks in mesh order,
+ * replica-major and shard-minor, with one partial resident at a time):
+ * out = (...((P0 (+) P1) (+) P2) ...) (+) P_{S-1}, shard index increasing.
+ * The same bits as starting an accumulator from P0 and calling
+ * repro_grad_accum with P1 .. P_{S-1} in order, which is the streaming form
+ * that keeps one partial resident; this call folds resident partials in one
+ * pass.  parts: HOST array of S device pointers (1 <= S <= 64); out may alias
+ * parts[0] exactly (no other overlap).
+ * ------------------------------------------------------------------------ */
+int repro_running_sum(const float* const* parts, int S, int64_t n, float* out,
+                      void* stream);
+
+/* ------------------------------------------------------------------------
  * TreeFold ([limits], level 3: the replica all-reduce replayed on one device,
  * pairing partials in the order of a recursive-doubling all-reduce).  With
  * p' = largest power of two <= R and r = R - p': survivors are
@@ -172,6 +186,33 @@ int repro_grad_accum(float* acc, const float* g, int64_t n, void* stream);
  * ------------------------------------------------------------------------ */
 int repro_treefold(const float* const* parts, int R, int64_t n, float* out,
                    void* stream);
+
+/* ------------------------------------------------------------------------
+ * Optimiser step after TreeFold ([limits]: AdamW, beta1 0.9, beta2 0.95,
+ * eps 1e-8, decoupled weight decay 0.1, global L2-norm clipping at 1.0).
+ * The pages fix no operation order; the library's is (binary32, rounded and
+ * flushed, never fused):
+ *   repro_sumsq: out = canonical sum of g_i (x) g_i over the flat gradient.
+ *   repro_adamw_step, per element, with norm = sqrt(*sumsq):
+ *     coef = min(max_norm (/) (norm (+) 1e-6), 1);  g' = g (x) coef
+ *     m = (b1 (x) m) (+) ((1 (-) b1) (x) g')
+ *     v = (b2 (x) v) (+) ((1 (-) b2) (x) (g' (x) g'))
+ *     p = (p (x) (1 (-) lr (x) wd)) (-) lr (x) ((m (/) (1 (-) b1^t)) (/)
+ *                                             (sqrt(v (/) (1 (-) b2^t)) (+) eps))
+ *   where b^t is computed by right-to-left binary exponentiation with rounded
+ *   multiplies and t >= 1 is the step number.  p, m, v are updated in place;
+ *   all are n floats (device), sumsq 1 float (device), hp a HOST struct.
+ *   The learning rate schedule belongs to the caller (lr per call).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay, max_norm;
+} repro_adamw_hparams;
+int repro_sumsq(const float* g, int64_t n, float* out, void* ws, size_t ws_bytes,
+                void* stream);
+size_t repro_sumsq_ws_bytes(int64_t n);
+int repro_adamw_step(float* p, float* m, float* v, const float* g, int64_t n,
+                     const float* sumsq, const repro_adamw_hparams* hp, int64_t t,
+                     void* stream);
 
 /* ------------------------------------------------------------------------
  * Housekeeping.

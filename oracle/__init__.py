@@ -54,6 +54,12 @@ def build(force: bool = False, openmp: bool = True) -> str:
 
 _lib = None
 
+
+class AdamWHparams(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_float) for k in
+                ("lr", "beta1", "beta2", "eps", "weight_decay", "max_norm")]
+
+
 _f32p = ctypes.POINTER(ctypes.c_float)
 _i8p = ctypes.POINTER(ctypes.c_int8)
 _i64p = ctypes.POINTER(ctypes.c_int64)
@@ -88,10 +94,16 @@ def lib() -> ctypes.CDLL:
             "oracle_linear_bwd_dw_at": (None, [_f32p, _i8p, ctypes.c_float, _i64, _i64, _i64,
                                                _i64p, _i64p, _i64, _f32p]),
             "oracle_grad_accum": (None, [_f32p, _f32p, _i64]),
+            "oracle_running_sum": (None, [ctypes.POINTER(_f32p), ctypes.c_int, _i64, _f32p]),
             "oracle_treefold_one": (ctypes.c_float, [_f32p, ctypes.c_int]),
             "oracle_treefold": (None, [ctypes.POINTER(_f32p), ctypes.c_int, _i64, _f32p]),
             "oracle_treefold_all_ranks": (None, [_f32p, ctypes.c_int, _f32p]),
             "oracle_threads": (ctypes.c_int, []),
+            "oracle_sumsq": (ctypes.c_float, [_f32p, _i64]),
+            "oracle_pow_t": (ctypes.c_float, [ctypes.c_float, _i64]),
+            "oracle_clip_coef": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+            "oracle_adamw_step": (None, [_f32p, _f32p, _f32p, _f32p, _i64, ctypes.c_float,
+                                         ctypes.POINTER(AdamWHparams), _i64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -250,6 +262,18 @@ def grad_accum(acc, g) -> np.ndarray:
     return out
 
 
+def running_sum(parts) -> np.ndarray:
+    """Left fold of equal-length float32 arrays in the given order."""
+    arrs = [_f32(p).ravel() for p in parts]
+    S = len(arrs)
+    n = arrs[0].size
+    assert all(a.size == n for a in arrs)
+    ptrs = (_f32p * S)(*[_p(a, _f32p) for a in arrs])
+    out = np.empty(n, dtype=np.float32)
+    lib().oracle_running_sum(ptrs, S, n, _p(out, _f32p))
+    return out
+
+
 def treefold_one(vals) -> np.float32:
     v = _f32(vals).ravel()
     return np.float32(lib().oracle_treefold_one(_p(v, _f32p), v.size))
@@ -272,6 +296,30 @@ def treefold(parts) -> np.ndarray:
     out = np.empty(n, dtype=np.float32)
     lib().oracle_treefold(ptrs, R, n, _p(out, _f32p))
     return out
+
+
+def sumsq(g) -> np.float32:
+    g = _f32(g).ravel()
+    return np.float32(lib().oracle_sumsq(_p(g, _f32p), g.size))
+
+
+def pow_t(b: float, t: int) -> np.float32:
+    return np.float32(lib().oracle_pow_t(float(b), int(t)))
+
+
+def clip_coef(s: float, max_norm: float) -> np.float32:
+    return np.float32(lib().oracle_clip_coef(float(s), float(max_norm)))
+
+
+def adamw_step(p, m, v, g, s: float, t: int, lr=4.5e-4, beta1=0.9, beta2=0.95, eps=1e-8,
+               weight_decay=0.1, max_norm=1.0):
+    """Returns new (p, m, v) as float32 arrays (inputs untouched)."""
+    p, m, v = _f32(p).copy(), _f32(m).copy(), _f32(v).copy()
+    g = _f32(g)
+    hp = AdamWHparams(lr, beta1, beta2, eps, weight_decay, max_norm)
+    lib().oracle_adamw_step(_p(p, _f32p), _p(m, _f32p), _p(v, _f32p), _p(g, _f32p), p.size,
+                            float(s), ctypes.byref(hp), int(t))
+    return p, m, v
 
 
 def threads() -> int:

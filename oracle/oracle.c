@@ -294,6 +294,26 @@ void oracle_grad_accum(float* acc, const float* g, int64_t n)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Level 2: the intra-node reduce-scatter is replayed as a running sum in one */
+/* loop over virtual ranks in mesh order, so only one partial is resident     */
+/* ([P4] "Premises and limits"): a left fold in shard order, first partial    */
+/* taken as it is.                                                            */
+/* ------------------------------------------------------------------------ */
+
+void oracle_running_sum(const float* const* parts, int S, int64_t n, float* out)
+{
+    if (S < 1)
+        return;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float a = parts[0][i];
+        for (int s = 1; s < S; ++s)
+            a = oracle_add(a, parts[s][i]);
+        out[i] = a;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* A10: TreeFold ([P4] "Premises and limits": the replica all-reduce is      */
 /* replayed by folding partials in the pairing order of the cluster's        */
 /* recursive-doubling all-reduce).  For R not a power of two the pre-step of */
@@ -365,6 +385,64 @@ void oracle_treefold(const float* const* parts, int R, int64_t n, float* out)
         for (int r = 0; r < R; ++r)
             vals[r] = parts[r][i];
         out[i] = oracle_treefold_one(vals, R);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Optimiser step (see oracle.h for the fixed operation order).               */
+/* ------------------------------------------------------------------------ */
+
+float oracle_sumsq(const float* g, int64_t n)
+{
+    float* t = (float*)malloc((size_t)(n > 0 ? n : 1) * sizeof(float));
+    for (int64_t i = 0; i < n; ++i)
+        t[i] = oracle_mul(g[i], g[i]);
+    float S = oracle_canon_sum(t, n);
+    free(t);
+    return oracle_flush(S);
+}
+
+float oracle_pow_t(float b, int64_t t)
+{
+    float r = 1.0f, base = b;
+    while (t > 0) {
+        if (t & 1)
+            r = oracle_mul(r, base);
+        base = oracle_mul(base, base);
+        t >>= 1;
+    }
+    return r;
+}
+
+float oracle_clip_coef(float sumsq, float max_norm)
+{
+    float norm = oracle_sqrt(sumsq);
+    float coef = oracle_div(max_norm, oracle_add(norm, 1e-6f));
+    return coef < 1.0f ? coef : 1.0f;
+}
+
+void oracle_adamw_step(float* p, float* m, float* v, const float* g, int64_t n, float sumsq,
+                       const oracle_adamw_hparams* hp, int64_t t)
+{
+    const float coef = oracle_clip_coef(sumsq, hp->max_norm);
+    const float one_b1 = oracle_add(1.0f, -hp->beta1);
+    const float one_b2 = oracle_add(1.0f, -hp->beta2);
+    const float bc1 = oracle_add(1.0f, -oracle_pow_t(hp->beta1, t));
+    const float bc2 = oracle_add(1.0f, -oracle_pow_t(hp->beta2, t));
+    const float decay = oracle_add(1.0f, -oracle_mul(hp->lr, hp->weight_decay));
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        const float gc = oracle_mul(g[i], coef);
+        const float mi = oracle_add(oracle_mul(hp->beta1, m[i]), oracle_mul(one_b1, gc));
+        const float vi = oracle_add(oracle_mul(hp->beta2, v[i]),
+                                    oracle_mul(one_b2, oracle_mul(gc, gc)));
+        const float mh = oracle_div(mi, bc1);
+        const float vh = oracle_div(vi, bc2);
+        const float den = oracle_add(oracle_sqrt(vh), hp->eps);
+        const float upd = oracle_mul(hp->lr, oracle_div(mh, den));
+        p[i] = oracle_add(oracle_mul(p[i], decay), -upd);
+        m[i] = mi;
+        v[i] = vi;
     }
 }
 

@@ -99,12 +99,36 @@ void oracle_linear_bwd_dw_at(const float* dy, const int8_t* xq, float s_x,
 /* ---- A9: acc[i] <- acc[i] (+) g[i] ---- */
 void oracle_grad_accum(float* acc, const float* g, int64_t n);
 
+/* ---- level 2 of the replayed reduction: running sum over S shard partials in
+ * mesh order, out = (...((P0 (+) P1) (+) P2) ...) (+) P_{S-1} ---- */
+void oracle_running_sum(const float* const* parts, int S, int64_t n, float* out);
+
 /* ---- A10: TreeFold over R replica partials, recursive-doubling pairing ---- */
 float oracle_treefold_one(const float* vals, int R);
 void  oracle_treefold(const float* const* parts, int R, int64_t n, float* out);
 /* every rank's final value of the simulated recursive-doubling all-reduce
  * (for the invariant that all ranks agree); `rank_out` has R entries */
 void  oracle_treefold_all_ranks(const float* vals, int R, float* rank_out);
+
+/* ---- optimiser step after TreeFold: global-norm clip + AdamW ----
+ * Recipe ([P4] "Premises and limits"): AdamW(beta1 0.9, beta2 0.95, eps 1e-8),
+ * decoupled weight decay 0.1, gradient clipping at global L2 norm 1.0.  The
+ * pages give no operation order; this one is fixed (binary32, flushed):
+ *   sumsq = canon_sum(g_i (x) g_i) over the flat gradient; norm = sqrt(sumsq)
+ *   coef  = min(max_norm (/) (norm (+) 1e-6), 1);  g' = g (x) coef
+ *   b^t by right-to-left binary exponentiation: r = 1, base = b; for each bit
+ *   of t from the lowest: if set r = r (x) base; then base = base (x) base
+ *   m = (b1 (x) m) (+) ((1 (-) b1) (x) g');  v = (b2 (x) v) (+) ((1 (-) b2) (x) (g' (x) g'))
+ *   mh = m (/) (1 (-) b1^t);  vh = v (/) (1 (-) b2^t)
+ *   p = (p (x) (1 (-) (lr (x) wd))) (-) (lr (x) (mh (/) (sqrt(vh) (+) eps)))   */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay, max_norm;
+} oracle_adamw_hparams;
+float oracle_sumsq(const float* g, int64_t n);
+float oracle_pow_t(float b, int64_t t);
+float oracle_clip_coef(float sumsq, float max_norm);
+void oracle_adamw_step(float* p, float* m, float* v, const float* g, int64_t n, float sumsq,
+                       const oracle_adamw_hparams* hp, int64_t t);
 
 /* threads the parallel loops use (1 when built without OpenMP) */
 int oracle_threads(void);

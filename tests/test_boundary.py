@@ -157,5 +157,30 @@ def test_launch_cfg_validation(L):
         repro.repro_set_launch_cfg(reset=True)
 
 
+def test_optimiser_argument_checks(L):
+    hp = repro.AdamWHparams(4.5e-4, 0.9, 0.95, 1e-8, 0.1, 1.0)
+    f = L.repro_adamw_step
+    B = 1 << 32
+    assert f(B, B * 2, B * 3, B * 4, 100, B * 5, None, 1, None) == -1          # no hparams
+    assert f(B, B * 2, B * 3, B * 4, 100, B * 5, ctypes.byref(hp), 0, None) == -1   # t < 1
+    assert f(B, B * 2, B * 3, B * 4, -1, B * 5, ctypes.byref(hp), 1, None) == -2
+    assert f(None, None, None, None, 0, None, ctypes.byref(hp), 1, None) == 0  # empty
+    assert f(B + 4, B * 2, B * 3, B * 4, 100, B * 5, ctypes.byref(hp), 1, None) == -3
+    assert f(B, B, B * 3, B * 4, 100, B * 5, ctypes.byref(hp), 1, None) == -8  # p is m
+    assert L.repro_sumsq(B, 0, B * 2, B * 3, 1 << 20, None) == -2
+    assert L.repro_sumsq(B, 1000, B * 2, None, 0, None) == -7
+    assert L.repro_sumsq(None, 1000, B * 2, B * 3, 1 << 20, None) == -1
+    assert repro.repro_sumsq_ws_bytes(10 ** 6) == repro.repro_wscale_ws_bytes(10 ** 6)
+
+
+def test_running_sum_checks(L):
+    P = ctypes.c_void_p
+    parts = (P * 3)(A, A * 2, A * 3)
+    assert L.repro_running_sum(parts, 0, 10, A * 4, None) == -1
+    assert L.repro_running_sum(parts, 3, -1, A * 4, None) == -2
+    assert L.repro_running_sum(parts, 3, 10, A * 3, None) == -8       # out overlaps parts[2]
+    assert L.repro_running_sum(parts, 3, 0, A * 4, None) == 0
+
+
 def test_launch_counter_readable(L):
     assert repro.repro_launch_count() >= 0

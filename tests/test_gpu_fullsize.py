@@ -32,18 +32,16 @@ def _samples(rng, rows, cols):
     return rr, cc
 
 
-@pytest.mark.parametrize("name", ["attn_out", "gate_up", "down_accum", "block"])
+@pytest.mark.parametrize("name", ["attn_out", "gate_up", "down_accum", "block", "block_audit"])
 def test_fullsize_sampled(orc, name):
     R.repro_set_launch_cfg(reset=True)
     wl = inputs.WORKLOADS[name]
     host = S.generate_host_inputs(wl)
     hp = S.HotPathStep(wl, host)
+    hp.use_optimizer = False      # the weights stay the inputs the oracle sees
     st = torch.cuda.current_stream()
-    if wl.replicas > 1:
-        hp.TF, tf = None, hp.TF
-        hp.run(st)
-        hp.prepare_replicas(st)
-        hp.TF = tf
+    if wl.replicas > 1 or wl.shards > 1:
+        hp.prepare(st)
     hp.run(st)
     torch.cuda.synchronize()
     assert R.repro_device_check() == 0
@@ -81,9 +79,13 @@ def test_fullsize_sampled(orc, name):
         G_flat_idx.append(offs[i] + n_idx * lin.k_in + k_idx)
         G_oracle.append(g)
 
+    idx = np.concatenate(G_flat_idx)
+    g = np.concatenate(G_oracle)
+    if wl.shards > 1:
+        shards = [g] + [orc.grad_accum(g, host.shard_noise[s][idx]) for s in range(1, wl.shards)]
+        g = orc.running_sum(shards)
+        G.assert_bits_equal(G.host(hp.G2)[idx], g, f"{name} level-2 running sum")
     if wl.replicas > 1:
-        idx = np.concatenate(G_flat_idx)
-        g = np.concatenate(G_oracle)
         parts = [g] + [orc.grad_accum(g, host.noise[r][idx]) for r in range(1, wl.replicas)]
         G.assert_bits_equal(G.host(hp.TF)[idx], orc.treefold(parts), f"{name} TreeFold")
 

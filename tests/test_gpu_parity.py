@@ -316,3 +316,31 @@ def test_tiny_workload_end_to_end(orc):
                            ("Y", G.host(y_t), y), ("dX", G.host(dx_t), dx),
                            ("dW", G.host(dw_t), dw), ("TreeFold", G.host(tf_t), tf)]:
         G.assert_bits_equal(got, exp, name)
+
+
+# ----------------------------------------------------------------- level 2
+
+@pytest.mark.parametrize("S_", [1, 2, 3, 5, 8, 9, 16, 64])
+def test_running_sum(orc, S_):
+    rng = np.random.default_rng(300 + S_)
+    n = 4099
+    parts = [(rng.standard_normal(n) * 10.0 ** rng.integers(-3, 3, n)).astype(np.float32)
+             for _ in range(S_)]
+    parts[0][:4] = [1e-40, -0.0, 2.0 ** 24, -1e-40]
+    ts = [G.dev(p) for p in parts]
+    out = torch.empty_like(ts[0])
+    R.repro_running_sum(ts, out)
+    G.assert_bits_equal(G.host(out), orc.running_sum(parts), f"running sum S={S_}")
+    R.repro_running_sum(ts, ts[0])                       # in place into the first partial
+    G.assert_bits_equal(G.host(ts[0]), orc.running_sum(parts), f"running sum in place S={S_}")
+
+
+def test_running_sum_equals_streaming_accumulation():
+    rng = np.random.default_rng(7)
+    parts = [G.dev((rng.standard_normal(10_000) * 1e-3).astype(np.float32)) for _ in range(8)]
+    out = torch.empty_like(parts[0])
+    R.repro_running_sum(parts, out)
+    acc = parts[0].clone()
+    for p in parts[1:]:
+        R.repro_grad_accum(acc, p)
+    G.assert_bits_equal(G.host(out), G.host(acc), "one pass vs streaming")

@@ -131,3 +131,37 @@ def test_grad_accum_order_matters(orc):
     g1, g2 = np.array([1.0], np.float32), np.array([-1e8], np.float32)
     assert orc.grad_accum(orc.grad_accum(acc, g1), g2)[0] == 0.0
     assert orc.grad_accum(orc.grad_accum(acc, g2), g1)[0] == 1.0
+
+
+# ----------------------------------------------------------------- level 2
+
+def test_running_sum_is_the_textbook_left_fold(orc):
+    rng = np.random.default_rng(17)
+    for S in [1, 2, 3, 8, 13]:
+        parts = [(rng.standard_normal(257) * 10.0 ** rng.integers(-3, 4, 257)).astype(np.float32)
+                 for _ in range(S)]
+        parts[0][:2] = [1e-40, -0.0]
+        got = orc.running_sum(parts)
+        for i in range(257):
+            acc = float(parts[0][i])          # first partial taken as it is
+            for s in range(1, S):
+                acc = _add(acc, parts[s][i])
+            assert f32_to_bits(got[i]) == f32_to_bits(acc), (S, i)
+
+
+def test_running_sum_equals_streaming_accumulation(orc):
+    # one resident partial: acc = P0, then acc (+)= P_s in shard order
+    rng = np.random.default_rng(18)
+    parts = [(rng.standard_normal(1000) * 1e-3).astype(np.float32) for _ in range(8)]
+    acc = parts[0].copy()
+    for p in parts[1:]:
+        acc = orc.grad_accum(acc, p)
+    assert np.array_equal(orc.running_sum(parts).view(np.uint32), acc.view(np.uint32))
+
+
+def test_running_sum_order_is_observable(orc):
+    parts = [np.array([2.0 ** 24], np.float32), np.array([1.0], np.float32),
+             np.array([1.0], np.float32), np.array([2.0], np.float32)]
+    # ((2^24 + 1) + 1) + 2 = 2^24 + 2, but (2^24 + 2) + (1 + 1) order differs from a tree
+    assert orc.running_sum(parts)[0] == 2.0 ** 24 + 2
+    assert orc.running_sum(parts[::-1])[0] == 2.0 ** 24 + 4
