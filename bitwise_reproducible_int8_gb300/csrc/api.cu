@@ -11,7 +11,8 @@ namespace repro {
 
 namespace {
 
-LaunchCfg g_cfg = {-1, -1, -1, 0, 3};
+constexpr int kDefaultBwdKernel = 7;   // operand prep + tensor-copy-fed kernel
+LaunchCfg g_cfg = {-1, -1, -1, 0, kDefaultBwdKernel};
 
 constexpr int kMaxDevices = 64;
 int g_arch_ok[kMaxDevices];   // 0 unknown, 1 GB300, -1 other
@@ -149,7 +150,7 @@ uint64_t repro_launch_count(void) { return (uint64_t)__atomic_load_n(&g_launches
 int repro_set_launch_cfg(const repro_launch_cfg* cfg)
 {
     if (!cfg) {
-        g_cfg = LaunchCfg{-1, -1, -1, 0, 3};
+        g_cfg = LaunchCfg{-1, -1, -1, 0, kDefaultBwdKernel};
         return REPRO_OK;
     }
     if (cfg->bwd_segment_log2 < -1 || cfg->bwd_segment_log2 > 8)
@@ -160,13 +161,13 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
         return REPRO_ERR_ARG;
     if (cfg->elementwise_blocks < -1 || cfg->elementwise_blocks > (1 << 20))
         return REPRO_ERR_ARG;
-    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 5)
+    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 7)
         return REPRO_ERR_ARG;
     g_cfg.bwd_segment_log2 = cfg->bwd_segment_log2;
     g_cfg.reduce_block_log2 = cfg->reduce_block_log2;
     g_cfg.fwd_path = cfg->fwd_path;
     g_cfg.elementwise_blocks = cfg->elementwise_blocks < 0 ? 0 : cfg->elementwise_blocks;
-    g_cfg.bwd_kernel = cfg->bwd_kernel < 0 ? 3 : cfg->bwd_kernel;
+    g_cfg.bwd_kernel = cfg->bwd_kernel < 0 ? kDefaultBwdKernel : cfg->bwd_kernel;
     return REPRO_OK;
 }
 

@@ -34,28 +34,12 @@
 // No atomics: each output is written by exactly one thread.
 #include <float.h>
 
+#include "bwd_common.cuh"
 #include "common.cuh"
 #include "internal.h"
 
 namespace repro {
 namespace {
-
-constexpr int BT = 64;       // output tile edge
-constexpr int CH = 64;       // chunk length of the canonical order
-constexpr int MAXLVL = 8;    // stack levels: up to 256 chunks per segment
-
-struct BwdArgs {
-    const float* dy;
-    const int8_t* q;
-    const float* scale;
-    float* out;
-    float* ws;
-    int64_t I, J, R;   // output rows, output columns, reduction length
-    int64_t ldy;       // row stride of dY (= N)
-    int seg_log2;
-    int nseg;
-    int accumulate;
-};
 
 // A[r][i] for the chunk starting at reduction index r0 (valid rows < valid)
 template <bool DW>
@@ -1811,7 +1795,12 @@ int kernel_for(int64_t ldy, int64_t J)
     return k;
 }
 
-int tile_rows(int kernel) { return kernel == 5 ? BI6 : (kernel >= 3 ? BI4 : BT); }
+int tile_rows(int kernel)
+{
+    if (kernel == 7)
+        return BWD_TMA_ROWS;
+    return kernel == 6 ? BWD_WS_ROWS : (kernel == 5 ? BI6 : (kernel >= 3 ? BI4 : BT));
+}
 
 // Segment size when the launch configuration leaves it open.  One CTA runs
 // per SM, so a grid of tiles that is not close to a whole number of waves
@@ -1854,7 +1843,7 @@ int resolve_seg(int seg_log2, int64_t I, int64_t J, int64_t R, int64_t ldy)
 template <bool DW>
 cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out, int64_t I,
                 int64_t J, int64_t R, int64_t ldy, int seg_log2, bool accumulate, float* ws,
-                cudaStream_t st)
+                float* opnd, cudaStream_t st)
 {
     if (I == 0 || J == 0)
         return cudaSuccess;
@@ -1879,6 +1868,7 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
     a.seg_log2 = seg_log2;
     a.nseg = (int)nseg_for(R, seg_log2);
     a.accumulate = accumulate ? 1 : 0;
+    a.err = device_error_word();
     dim3 grid((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BT), (unsigned)a.nseg);
     // the staged kernels need 16-byte-aligned rows: dY rows (N % 4) and int8
     // rows (J % 16); other shapes take the register-prefetch kernel
@@ -1886,6 +1876,20 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
     const bool aligned = kernel >= 2;
     if (kernel == 0) {
         k_bwd<DW><<<grid, 256, 0, st>>>(a);
+    } else if (kernel == 7 && aligned) {
+        if (!a.err || !opnd)
+            return cudaErrorInvalidValue;
+        dim3 gt((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BWD_TMA_ROWS), (unsigned)a.nseg);
+        cudaError_t e = launch_bwd_tma<DW>(a, q, opnd, gt, st);
+        if (e != cudaSuccess)
+            return e;
+    } else if (kernel == 6 && aligned) {
+        if (!a.err)
+            return cudaErrorInvalidValue;
+        dim3 gw((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BWD_WS_ROWS), (unsigned)a.nseg);
+        cudaError_t e = launch_bwd_ws<DW>(a, gw, st);
+        if (e != cudaSuccess)
+            return e;
     } else if (kernel == 5 && aligned) {
         cudaError_t e = cudaFuncSetAttribute(k_bwd6<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)BWD6_SMEM);
@@ -1936,28 +1940,53 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
 
 } // namespace
 
-size_t bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int seg_log2)
+// workspace: segment partials first, then (tensor-copy kernel only) the
+// prepared operands, 256-byte aligned
+static int64_t seg_region_bytes(int64_t M, int64_t N, int64_t K, int seg_log2)
 {
     // dX: I = M, J = K, R = N, dY rows of N; dW: I = N, J = K, R = M
     const int64_t sx = nseg_for(N, resolve_seg(seg_log2, M, K, N, N));
     const int64_t sw = nseg_for(M, resolve_seg(seg_log2, N, K, M, N));
     const int64_t bx = sx > 1 ? sx * M * K : 0;
     const int64_t bw = sw > 1 ? sw * N * K : 0;
-    return (size_t)((bx > bw ? bx : bw) * (int64_t)sizeof(float));
+    return (bx > bw ? bx : bw) * (int64_t)sizeof(float);
+}
+
+static bool uses_operand_region(int64_t N, int64_t K)
+{
+    return kernel_for(N, K) == 7;
+}
+
+size_t bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int seg_log2)
+{
+    const int64_t seg = seg_region_bytes(M, N, K, seg_log2);
+    if (!uses_operand_region(N, K))
+        return (size_t)seg;
+    return (size_t)(((seg + 255) & ~(int64_t)255) + (int64_t)bwd_tma_operand_bytes(M, N, K));
+}
+
+static float* operand_region(float* ws, int64_t M, int64_t N, int64_t K, int seg_log2)
+{
+    if (!ws || !uses_operand_region(N, K))
+        return nullptr;
+    const int64_t seg = seg_region_bytes(M, N, K, seg_log2);
+    return reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + ((seg + 255) & ~(int64_t)255));
 }
 
 cudaError_t launch_bwd_dx(const float* dy, const int8_t* wq, const float* s_w, float* dx,
                           int64_t M, int64_t N, int64_t K, int seg_log2, float* ws,
                           cudaStream_t st)
 {
-    return run<false>(dy, wq, s_w, dx, M, K, N, N, seg_log2, false, ws, st);
+    return run<false>(dy, wq, s_w, dx, M, K, N, N, seg_log2, false, ws,
+                      operand_region(ws, M, N, K, seg_log2), st);
 }
 
 cudaError_t launch_bwd_dw(const float* dy, const int8_t* xq, const float* s_x, float* dw,
                           int64_t M, int64_t N, int64_t K, int seg_log2, bool accumulate,
                           float* ws, cudaStream_t st)
 {
-    return run<true>(dy, xq, s_x, dw, N, K, M, N, seg_log2, accumulate, ws, st);
+    return run<true>(dy, xq, s_x, dw, N, K, M, N, seg_log2, accumulate, ws,
+                     operand_region(ws, M, N, K, seg_log2), st);
 }
 
 } // namespace repro

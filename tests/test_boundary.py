@@ -113,15 +113,25 @@ def test_linear_bwd_argument_checks(L):
 
 def test_bwd_workspace_follows_segments(L):
     try:
-        repro.repro_set_launch_cfg(bwd_segment_log2=8)
+        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=3)
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 0
-        repro.repro_set_launch_cfg(bwd_segment_log2=4)
+        repro.repro_set_launch_cfg(bwd_segment_log2=4, bwd_kernel=3)
         # dW: 256 chunks / 16 = 16 segments of N x K partials
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 16 * 2048 * 2048 * 4
         f = L.repro_linear_bwd
         B = 1 << 32   # widely spaced fake addresses: nothing overlaps
         assert f(B, B * 2, B * 3, B * 4, B * 4 + 4, B * 5, B * 6, 16384, 8, 8, 0, None, 0,
                  None) == -7
+        # the tensor-copy kernel adds its prepared operands after the partials:
+        # max(dY^T + W^, dY + X^) = 2 * 16384 * 2048 floats here
+        opnd = 2 * 16384 * 2048 * 4
+        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=7)
+        assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == opnd
+        repro.repro_set_launch_cfg(bwd_segment_log2=4, bwd_kernel=7)
+        assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 16 * 2048 * 2048 * 4 + opnd
+        # rows that are not 16-byte aligned take the register-prefetch kernel: no operand region
+        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=7)
+        assert repro.repro_linear_bwd_ws_bytes(64, 30, 20) == 0
     finally:
         repro.repro_set_launch_cfg(reset=True)
 
