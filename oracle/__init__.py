@@ -324,3 +324,6 @@ def adamw_step(p, m, v, g, s: float, t: int, lr=4.5e-4, beta1=0.9, beta2=0.95, e
 
 def threads() -> int:
     return int(lib().oracle_threads())
+
+
+from .merkle import LEAF_BYTES as HASH_LEAF_BYTES, state_hash, mth, audit_path  # noqa: E402,F401

@@ -57,3 +57,10 @@ def treefold_cases():
         vals = np.array([float(v) for v in toks[1:]], dtype=np.float32)
         assert vals.size == R
         yield vals, int(rhs.split()[0], 16)
+
+
+def sha256_vectors():
+    """Yields (message bytes, expected digest bytes)."""
+    for line in _lines("sha256_vectors.txt"):
+        msg, dig = line.split()
+        yield (b"" if msg == "-" else bytes.fromhex(msg)), bytes.fromhex(dig)
