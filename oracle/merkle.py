@@ -28,7 +28,7 @@ from __future__ import annotations
 import hashlib
 from typing import Iterable, List, Sequence
 
-LEAF_BYTES = 65536
+LEAF_BYTES = 4096
 
 
 def sha256(b: bytes) -> bytes:

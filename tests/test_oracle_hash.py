@@ -112,4 +112,4 @@ def test_every_byte_and_the_leaf_order_matter():
 
 def test_exported_from_package():
     assert oracle.state_hash is SH.state_hash
-    assert oracle.HASH_LEAF_BYTES == 65536
+    assert oracle.HASH_LEAF_BYTES == 4096
