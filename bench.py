@@ -336,6 +336,9 @@ def run_ours(args, wl):
                 gbs = nbytes * args.steps / (c_ms / 1e3) / 1e9
                 other[cls] = {"achieved_gbs": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
                               "ms_per_step": c_ms / args.steps}
+                if cls == "state_hash":
+                    other[cls]["bound"] = "alu (SHA-256 compressions on the integer pipe)"
+
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(wl_r, host, args.cpu_frac_log2)
@@ -384,6 +387,7 @@ def hbm_bytes(hp) -> dict:
     if hp.use_optimizer:
         out["sumsq"] = 4 * hp.n_grad
         out["adamw"] = 28 * hp.n_grad
+        out["state_hash"] = 12 * hp.n_grad   # parameters + two moments read once
     if hp.dW_tmp is not None:
         out["accum"] = 12 * nw * (J - 1)
     return out

@@ -488,4 +488,50 @@ int repro_treefold(const float* const* parts, int R, int64_t n, float* out, void
     return status_of(launch_treefold(parts, R, n, out, stream_grid(n / 4), as_stream(stream)));
 }
 
+size_t repro_state_hash_ws_bytes(const int64_t* nbytes, int nbuf)
+{
+    if (nbuf < 0 || nbuf > REPRO_HASH_MAX_BUFFERS || (nbuf > 0 && !nbytes))
+        return 0;
+    for (int b = 0; b < nbuf; ++b)
+        if (nbytes[b] < 0)
+            return 0;
+    return hash_ws_bytes(hash_leaf_count(nbytes, nbuf, REPRO_HASH_LEAF_BYTES));
+}
+
+int repro_state_hash(const void* const* bufs, const int64_t* nbytes, int nbuf, uint8_t* digest,
+                     void* ws, size_t ws_bytes, void* stream)
+{
+    if (nbuf < 0 || nbuf > REPRO_HASH_MAX_BUFFERS || !digest)
+        return REPRO_ERR_ARG;
+    if (nbuf > 0 && (!bufs || !nbytes))
+        return REPRO_ERR_ARG;
+    for (int b = 0; b < nbuf; ++b) {
+        if (nbytes[b] < 0)
+            return REPRO_ERR_SHAPE;
+        if (nbytes[b] > 0 && !bufs[b])
+            return REPRO_ERR_ARG;
+        if (nbytes[b] > 0 && !al16(bufs[b]))
+            return REPRO_ERR_ALIGN;
+    }
+    if (!al16(digest))
+        return REPRO_ERR_ALIGN;
+    const size_t need = hash_ws_bytes(hash_leaf_count(nbytes, nbuf, REPRO_HASH_LEAF_BYTES));
+    if (need > 0) {
+        if (!ws || ws_bytes < need)
+            return REPRO_ERR_WORKSPACE;
+        if (!al16(ws))
+            return REPRO_ERR_ALIGN;
+        if (overlap(ws, need, digest, 32))
+            return REPRO_ERR_ALIAS;
+        for (int b = 0; b < nbuf; ++b)
+            if (overlap(ws, need, bufs[b], (size_t)nbytes[b]))
+                return REPRO_ERR_ALIAS;
+    }
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_state_hash(bufs, nbytes, nbuf, REPRO_HASH_LEAF_BYTES, digest, ws,
+                                       as_stream(stream)));
+}
+
 } // extern "C"

@@ -74,4 +74,10 @@ cudaError_t launch_running_sum(const float* const* parts, int S, int64_t n, floa
 cudaError_t launch_treefold(const float* const* parts, int R, int64_t n, float* out, int grid,
                             cudaStream_t st);
 
+// ---- state hash (k_hash.cu)
+int64_t hash_leaf_count(const int64_t* nbytes, int nbuf, int64_t leaf_bytes);
+size_t hash_ws_bytes(int64_t nleaves);
+cudaError_t launch_state_hash(const void* const* bufs, const int64_t* nbytes, int nbuf,
+                              int64_t leaf_bytes, uint8_t* digest, void* ws, cudaStream_t st);
+
 } // namespace repro

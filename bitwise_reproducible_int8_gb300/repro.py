@@ -68,6 +68,9 @@ _SIGNATURES = {
     "repro_sumsq_ws_bytes": (_sz, [_i64]),
     "repro_adamw_step": (_int, [_vp, _vp, _vp, _vp, _i64, _vp, ctypes.POINTER(AdamWHparams),
                                 _i64, _vp]),
+    "repro_state_hash": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_i64), _int, _vp, _vp, _sz,
+                                _vp]),
+    "repro_state_hash_ws_bytes": (_sz, [ctypes.POINTER(_i64), _int]),
     "repro_status_str": (ctypes.c_char_p, [_int]),
     "repro_version": (_int, []),
     "repro_device_check": (_int, [_vp]),
@@ -244,6 +247,37 @@ def repro_treefold(parts, out: torch.Tensor, stream=None) -> None:
     arr = (_vp * max(R, 1))(*[_ptr(p, torch.float32, "part") for p in parts])
     _check("repro_treefold", lib().repro_treefold(arr, R, n, _ptr(out, torch.float32, "out"),
                                                   _stream(stream)))
+
+
+REPRO_HASH_LEAF_BYTES = 4096
+
+
+def _hash_tables(buffers):
+    nb = len(buffers)
+    ptrs = (_vp * max(nb, 1))(*[_ptr(b, None, "buffer") if b.numel() else None for b in buffers])
+    sizes = (_i64 * max(nb, 1))(*[b.numel() * b.element_size() for b in buffers])
+    return ptrs, sizes, nb
+
+
+def repro_state_hash_ws_bytes(buffers) -> int:
+    """Workspace for hashing these tensors (their bytes, in order)."""
+    _, sizes, nb = _hash_tables(buffers)
+    return int(lib().repro_state_hash_ws_bytes(sizes, nb))
+
+
+def repro_state_hash(buffers, digest: torch.Tensor, ws=None, stream=None) -> None:
+    """digest (32 uint8, device) <- Merkle Tree Hash of the tensors' bytes."""
+    for b in buffers:
+        if not b.is_contiguous():
+            raise ValueError("state buffers must be contiguous")
+    ptrs, sizes, nb = _hash_tables(buffers)
+    if digest.numel() != 32 or digest.dtype != torch.uint8:
+        raise ValueError("digest must be 32 uint8")
+    if ws is None:
+        ws = _workspace(int(lib().repro_state_hash_ws_bytes(sizes, nb)), digest.device)
+    _check("repro_state_hash", lib().repro_state_hash(
+        ptrs, sizes, nb, _ptr(digest, torch.uint8, "digest"), _ptr(ws, None, "ws"),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def repro_sumsq_ws_bytes(n: int) -> int:

@@ -121,6 +121,11 @@ class HotPathStep:
             self.sumsq = torch.zeros(1, dtype=torch.float32, device=dev)
             self.ws_sumsq = torch.empty(max(R.repro_sumsq_ws_bytes(n_grad), 16),
                                         dtype=torch.uint8, device=dev)
+            # per-step state hash of (parameters, first moment, second moment)
+            self.state = [self.Wflat, self.m, self.v]
+            self.digest = torch.zeros(32, dtype=torch.uint8, device=dev)
+            self.ws_hash = torch.empty(max(R.repro_state_hash_ws_bytes(self.state), 16),
+                                       dtype=torch.uint8, device=dev)
 
     # ------------------------------------------------------------------ step
 
@@ -211,6 +216,9 @@ class HotPathStep:
             self._ev(timers, "adamw", s)
             R.repro_adamw_step(self.Wflat, self.m, self.v, grad, self.sumsq, self.step_t, stream=s)
             self._end(timers, "adamw", s)
+            self._ev(timers, "state_hash", s)
+            R.repro_state_hash(self.state, self.digest, ws=self.ws_hash, stream=s)
+            self._end(timers, "state_hash", s)
 
     def prepare_replicas(self, stream: torch.cuda.Stream) -> None:
         """Q_s = G (+) shard_noise_s (s = 1..S-1), then G_2 = running sum, then

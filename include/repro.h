@@ -215,6 +215,31 @@ int repro_adamw_step(float* p, float* m, float* v, const float* g, int64_t n,
                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * Per-step state hash ([rit] paragraph 4, [limits]: a hash of the state is
+ * recorded after every step and a replay must reproduce it; the pages hash on
+ * the host and name on-device hashing as future work).  The pages fix no
+ * construction; the library's is the Merkle Tree Hash of RFC 6962 section
+ * 2.1 over SHA-256 (FIPS 180-4):
+ *   leaves: each buffer cut into REPRO_HASH_LEAF_BYTES consecutive bytes (the
+ *     last leaf of a buffer may be shorter; an empty buffer has none), the
+ *     buffers' leaves in buffer order;
+ *   MTH({}) = SHA-256(""), MTH({d}) = SHA-256(0x00 || d),
+ *   MTH(D[0:n]) = SHA-256(0x01 || MTH(D[0:k]) || MTH(D[k:n])), k the largest
+ *     power of two below n.
+ * bufs, nbytes: HOST arrays of nbuf (0 .. REPRO_HASH_MAX_BUFFERS) device
+ *   pointers (16-byte aligned; NULL allowed when the size is 0) and byte
+ *   counts.  digest: 32 bytes of DEVICE memory (16-byte aligned), written in
+ *   the standard SHA-256 byte order.  ws: repro_state_hash_ws_bytes bytes
+ *   (0 for a single leaf), not overlapping the buffers or the digest.
+ * Hashing is integer work: the bits never depend on the launch.
+ * ------------------------------------------------------------------------ */
+#define REPRO_HASH_LEAF_BYTES 4096
+#define REPRO_HASH_MAX_BUFFERS 64
+int repro_state_hash(const void* const* bufs, const int64_t* nbytes, int nbuf,
+                     uint8_t* digest, void* ws, size_t ws_bytes, void* stream);
+size_t repro_state_hash_ws_bytes(const int64_t* nbytes, int nbuf);
+
+/* ------------------------------------------------------------------------
  * Housekeeping.
  * repro_status_str: static description of a status code.
  * repro_version: REPRO_VERSION.

@@ -194,3 +194,40 @@ def test_running_sum_checks(L):
 
 def test_launch_counter_readable(L):
     assert repro.repro_launch_count() >= 0
+
+
+def test_state_hash_argument_checks(L):
+    f = L.repro_state_hash
+    P = ctypes.c_void_p
+    I = ctypes.c_int64
+    ptrs = lambda *v: (P * max(len(v), 1))(*v)          # noqa: E731
+    sizes = lambda *v: (I * max(len(v), 1))(*v)         # noqa: E731
+    D = A * 8   # digest
+    W = A * 16  # workspace
+    assert f(ptrs(A), sizes(10), -1, D, W, 1 << 20, None) == -1          # nbuf < 0
+    assert f(ptrs(A), sizes(10), 65, D, W, 1 << 20, None) == -1          # nbuf > 64
+    assert f(ptrs(A), sizes(10), 1, None, W, 1 << 20, None) == -1        # no digest
+    assert f(None, None, 1, D, W, 1 << 20, None) == -1                   # no tables
+    assert f(ptrs(A), sizes(-1), 1, D, W, 1 << 20, None) == -2           # negative size
+    assert f(ptrs(None), sizes(10), 1, D, W, 1 << 20, None) == -1        # null buffer
+    assert f(ptrs(A + 4), sizes(10), 1, D, W, 1 << 20, None) == -3       # misaligned buffer
+    assert f(ptrs(A), sizes(10), 1, D + 8, W, 1 << 20, None) == -3       # misaligned digest
+    big = 3 * 4096
+    assert f(ptrs(A), sizes(big), 1, D, None, 0, None) == -7             # 3 leaves need ws
+    assert f(ptrs(A), sizes(big), 1, D, W, 64, None) == -7               # too small
+    assert f(ptrs(A), sizes(big), 1, W + 32, W, 1 << 20, None) == -8     # digest inside ws
+    assert f(ptrs(W), sizes(big), 1, D, W, 1 << 20, None) == -8          # ws over a buffer
+    # valid arguments reach the architecture check (no GPU here)
+    assert f(ptrs(None), sizes(0), 1, D, None, 0, None) in (-4, -5)      # empty state
+    assert f(ptrs(A), sizes(10), 1, D, None, 0, None) in (-4, -5)        # one leaf: no ws
+
+
+def test_state_hash_ws_bytes(L):
+    I = ctypes.c_int64
+    g = L.repro_state_hash_ws_bytes
+    assert g((I * 1)(0), 1) == 0
+    assert g((I * 1)(4096), 1) == 0                     # one leaf: straight into the digest
+    assert g((I * 2)(4096, 1), 2) == 256 + 256          # two leaves, one parent
+    n = 1000 * 4096 + 5                                   # 1001 leaves + 501 parents
+    assert g((I * 1)(n), 1) == ((1001 * 32 + 255) // 256) * 256 + ((501 * 32 + 255) // 256) * 256
+    assert g((I * 1)(-1), 1) == 0

@@ -94,8 +94,9 @@ def test_two_training_steps_tiny(orc):
     mbs = [(inputs.activation(wl, 0, j), inputs.upstream_grad(wl, 0, j)) for j in range(2)]
     noise = [inputs.replica_noise(wl, r, W0.size).reshape(W0.shape) for r in range(1, 4)]
 
-    # oracle
+    # oracle; the per-step state hash log covers (W, m, v) after each update
     W, m, v = W0.copy(), np.zeros_like(W0), np.zeros_like(W0)
+    log = []
     for t in (1, 2):
         s_w = orc.wscale(W, 0)
         wq = orc.quant_i8(W, s_w)
@@ -109,6 +110,7 @@ def test_two_training_steps_tiny(orc):
         parts = [acc] + [orc.grad_accum(acc, nz) for nz in noise]
         g = orc.treefold(parts).reshape(W.shape)
         W, m, v = orc.adamw_step(W, m, v, g, orc.sumsq(g), t, **HP)
+        log.append(orc.state_hash([W.tobytes(), m.tobytes(), v.tobytes()]))
 
     # GPU through the C ABI
     tW, tm, tv = G.dev(W0), torch.zeros(W0.shape, device="cuda"), torch.zeros(W0.shape, device="cuda")
@@ -135,6 +137,10 @@ def test_two_training_steps_tiny(orc):
         R.repro_treefold(reps, tf)
         R.repro_sumsq(tf, ss)
         R.repro_adamw_step(tW, tm, tv, tf, ss, t, **HP)
+        digest = torch.zeros(32, dtype=torch.uint8, device="cuda")
+        R.repro_state_hash([tW, tm, tv], digest)
+        assert bytes(G.host(digest)) == log[t - 1], f"state hash after step {t}"
+    assert log[0] != log[1]
     G.assert_bits_equal(G.host(tW), W, "W after two steps")
     G.assert_bits_equal(G.host(tm), m, "m after two steps")
     G.assert_bits_equal(G.host(tv), v, "v after two steps")
