@@ -104,6 +104,21 @@ def lib() -> ctypes.CDLL:
             "oracle_clip_coef": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
             "oracle_adamw_step": (None, [_f32p, _f32p, _f32p, _f32p, _i64, ctypes.c_float,
                                          ctypes.POINTER(AdamWHparams), _i64]),
+            "oracle_exp": (ctypes.c_float, [ctypes.c_float]),
+            "oracle_attn_quant_p": (ctypes.c_int, [ctypes.c_float]),
+            "oracle_attn_fx": (ctypes.c_int64, [ctypes.c_float]),
+            "oracle_attn_fix2f": (ctypes.c_float, [_i64]),
+            "oracle_attn_fwd": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p, _f32p,
+                                       _i64, _i64, _i64, _i64, _i64, _i64]),
+            "oracle_attn_fwd_rows": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _i64p, _i64,
+                                            _f32p, _f32p, _f32p, _i64, _i64, _i64, _i64, _i64,
+                                            _i64]),
+            "oracle_attn_bwd": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p, _f32p,
+                                       _f32p, _f32p, _f32p, _f32p, _i64, _i64, _i64, _i64, _i64,
+                                       _i64]),
+            "oracle_attn_bwd_rows": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p,
+                                            _f32p, _f32p, _i64p, _i64, _f32p, _i64p, _i64, _f32p,
+                                            _f32p, _i64, _i64, _i64, _i64, _i64, _i64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -324,6 +339,89 @@ def adamw_step(p, m, v, g, s: float, t: int, lr=4.5e-4, beta1=0.9, beta2=0.95, e
 
 def threads() -> int:
     return int(lib().oracle_threads())
+
+
+# ---------------------------------------------------------------- attention
+
+def exp(x: float) -> np.float32:
+    """The softmax's e^x (Cody-Waite reduction + degree-7 Taylor, binary32)."""
+    return np.float32(lib().oracle_exp(float(x)))
+
+
+def attn_quant_p(p: float) -> int:
+    return int(lib().oracle_attn_quant_p(float(p)))
+
+
+def attn_fx(x: float) -> int:
+    return int(lib().oracle_attn_fx(float(x)))
+
+
+def attn_fix2f(a: int) -> np.float32:
+    return np.float32(lib().oracle_attn_fix2f(int(a)))
+
+
+def _attn_shapes(q, k):
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    assert k.shape == (B, T, Hkv, D) and Hq % Hkv == 0
+    return B, T, Hq, Hkv, D
+
+
+def attn_fwd(q, k, vq, s_v: float, W: int):
+    """q [B,T,Hq,D], k and vq [B,T,Hkv,D] -> (o [B,T,Hq,D], m [B,T,Hq], l [B,T,Hq])."""
+    q, k, vq = _f32(q), _f32(k), _i8(vq)
+    B, T, Hq, Hkv, D = _attn_shapes(q, k)
+    o = np.empty((B, T, Hq, D), np.float32)
+    m = np.empty((B, T, Hq), np.float32)
+    l = np.empty((B, T, Hq), np.float32)
+    lib().oracle_attn_fwd(_p(q, _f32p), _p(k, _f32p), _p(vq, _i8p), float(s_v), _p(o, _f32p),
+                          _p(m, _f32p), _p(l, _f32p), B, T, Hq, Hkv, D, int(W))
+    return o, m, l
+
+
+def attn_fwd_rows(q, k, vq, s_v: float, W: int, rows):
+    """Rows given as flat (b, i, h) indices -> (o [n,D], m [n], l [n])."""
+    q, k, vq = _f32(q), _f32(k), _i8(vq)
+    B, T, Hq, Hkv, D = _attn_shapes(q, k)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    o = np.empty((n, D), np.float32)
+    m = np.empty(n, np.float32)
+    l = np.empty(n, np.float32)
+    lib().oracle_attn_fwd_rows(_p(q, _f32p), _p(k, _f32p), _p(vq, _i8p), float(s_v),
+                               _p(rows, _i64p), n, _p(o, _f32p), _p(m, _f32p), _p(l, _f32p),
+                               B, T, Hq, Hkv, D, int(W))
+    return o, m, l
+
+
+def attn_bwd(q, k, vq, s_v: float, o, dout, m, l, W: int):
+    """-> (dq [B,T,Hq,D], dk [B,T,Hkv,D], dv [B,T,Hkv,D])."""
+    q, k, vq, o, dout, m, l = _f32(q), _f32(k), _i8(vq), _f32(o), _f32(dout), _f32(m), _f32(l)
+    B, T, Hq, Hkv, D = _attn_shapes(q, k)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(k)
+    lib().oracle_attn_bwd(_p(q, _f32p), _p(k, _f32p), _p(vq, _i8p), float(s_v), _p(o, _f32p),
+                          _p(dout, _f32p), _p(m, _f32p), _p(l, _f32p), _p(dq, _f32p),
+                          _p(dk, _f32p), _p(dv, _f32p), B, T, Hq, Hkv, D, int(W))
+    return dq, dk, dv
+
+
+def attn_bwd_rows(q, k, vq, s_v: float, o, dout, m, l, W: int, qrows, krows):
+    """dq for flat (b, i, h) rows qrows, dk and dv for flat (b, j, g) rows krows."""
+    q, k, vq, o, dout, m, l = _f32(q), _f32(k), _i8(vq), _f32(o), _f32(dout), _f32(m), _f32(l)
+    B, T, Hq, Hkv, D = _attn_shapes(q, k)
+    qrows = np.ascontiguousarray(qrows, dtype=np.int64)
+    krows = np.ascontiguousarray(krows, dtype=np.int64)
+    dq = np.empty((qrows.size, D), np.float32)
+    dk = np.empty((krows.size, D), np.float32)
+    dv = np.empty((krows.size, D), np.float32)
+    lib().oracle_attn_bwd_rows(_p(q, _f32p), _p(k, _f32p), _p(vq, _i8p), float(s_v),
+                               _p(o, _f32p), _p(dout, _f32p), _p(m, _f32p), _p(l, _f32p),
+                               _p(qrows, _i64p), qrows.size, _p(dq, _f32p), _p(krows, _i64p),
+                               krows.size, _p(dk, _f32p), _p(dv, _f32p), B, T, Hq, Hkv, D,
+                               int(W))
+    return dq, dk, dv
 
 
 from .merkle import LEAF_BYTES as HASH_LEAF_BYTES, state_hash, mth, audit_path  # noqa: E402,F401

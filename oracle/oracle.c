@@ -446,6 +446,321 @@ void oracle_adamw_step(float* p, float* m, float* v, const float* g, int64_t n, 
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* Attention with int8 P.V ([P4] "How to use": inside flash attention the    */
+/* P.V product runs on int8 while the QK^T logits and the softmax stay in    */
+/* high precision; the attention backward accumulates dQ in 64-bit fixed     */
+/* point).  The pages fix no operation order; the readings taken here:       */
+/*   logits  s_ij = canon_d(q_id (x) k_jd) (x) c, c = 1 (/) sqrt(D);         */
+/*   keys    j in [lo_i, i], lo_i = max(0, i - W + 1) for a sliding window  */
+/*           of W tokens, 0 for W = 0 (full causal); GQA: query head h      */
+/*           reads kv head h / (Hq / Hkv);                                   */
+/*   m_i     = max_j s_ij (exact, so the softmax is taken in two passes);    */
+/*   p_ij    = exp_r(s_ij (-) m_i), l_i = canon_j(p_ij) over j ascending;    */
+/*   int8 P  P_ij = clamp(rint(p_ij (x) 127), 0, 127); V = V_q with scale s_v;*/
+/*   o_id    = (i2f(sum_j P_ij V_q,jd) (x) s_v) (/) (l_i (x) 127), the       */
+/*           integer sum exact.                                              */
+/* Layout: q, o [B][T][Hq][D]; k, v [B][T][Hkv][D]; m, l [B][T][Hq].         */
+/* ------------------------------------------------------------------------ */
+
+/* e^x: range reduction of Cody and Waite ("Software Manual for the          */
+/* Elementary Functions", 1980) with ln 2 split as C1 + C2, C1 = 355/512     */
+/* (exact in 9 bits, so k (x) C1 is exact), then the degree-7 Taylor         */
+/* polynomial of e^r in Horner form with binary32 coefficients RN(1/n!),     */
+/* then the exact scaling by 2^k; every operation rounded and flushed.       */
+#define EXP_LOG2E 1.44269502162933349609375f  /* RN(1/ln 2) */
+#define EXP_C1 0.693359375f                   /* 355/512 */
+#define EXP_C2 -2.12194440e-4f                /* RN(ln 2 - 355/512) */
+
+float oracle_exp(float x)
+{
+    const float kf = nearbyintf(oracle_mul(x, EXP_LOG2E)); /* ties to even */
+    const float r = oracle_add(oracle_add(x, -oracle_mul(kf, EXP_C1)), -oracle_mul(kf, EXP_C2));
+    static const float c[8] = {1.0f, 1.0f, 0.5f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f,
+                               1.0f / 720.0f, 1.0f / 5040.0f};
+    float p = c[7];
+    for (int n = 6; n >= 0; --n)
+        p = oracle_add(oracle_mul(p, r), c[n]);
+    if (kf < -126.0f)
+        return 0.0f;
+    return oracle_flush(ldexpf(p, (int)kf));
+}
+
+static float attn_c(int64_t D)
+{
+    return oracle_div(1.0f, oracle_sqrt((float)D));
+}
+
+static int64_t attn_lo(int64_t i, int64_t W)
+{
+    return (W > 0 && i - W + 1 > 0) ? i - W + 1 : 0;
+}
+
+static float attn_logit(const float* q, const float* k, int64_t b, int64_t i, int64_t j,
+                        int64_t h, int64_t g, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
+                        float c, float* tmp)
+{
+    const float* qi = q + ((b * T + i) * Hq + h) * D;
+    const float* kj = k + ((b * T + j) * Hkv + g) * D;
+    for (int64_t d = 0; d < D; ++d)
+        tmp[d] = oracle_mul(qi[d], kj[d]);
+    return oracle_mul(oracle_canon_sum(tmp, D), c);
+}
+
+int oracle_attn_quant_p(float p)
+{
+    float r = nearbyintf(oracle_mul(p, 127.0f));
+    if (r > 127.0f)
+        r = 127.0f;
+    if (r < 0.0f)
+        r = 0.0f;
+    return (int)r;
+}
+
+/* one query row: o[D], m, l */
+static void attn_fwd_row(const float* q, const float* k, const int8_t* vq, float s_v,
+                         int64_t b, int64_t i, int64_t h, int64_t T, int64_t Hq, int64_t Hkv,
+                         int64_t D, int64_t W, float* o, float* m_out, float* l_out)
+{
+    const int64_t g = h / (Hq / Hkv), lo = attn_lo(i, W), n = i - lo + 1;
+    const float c = attn_c(D);
+    float* s = (float*)malloc((size_t)n * sizeof(float));
+    float* tmp = (float*)malloc((size_t)(D > n ? D : n) * sizeof(float));
+    int64_t* acc = (int64_t*)calloc((size_t)D, sizeof(int64_t));
+    float m = 0.0f;
+    for (int64_t t = 0; t < n; ++t) {
+        s[t] = attn_logit(q, k, b, i, lo + t, h, g, T, Hq, Hkv, D, c, tmp);
+        if (t == 0 || s[t] > m)
+            m = s[t];
+    }
+    for (int64_t t = 0; t < n; ++t) {
+        const float p = oracle_exp(oracle_add(s[t], -m));
+        tmp[t] = p;
+        const int pq = oracle_attn_quant_p(p);
+        const int8_t* vj = vq + ((b * T + lo + t) * Hkv + g) * D;
+        for (int64_t d = 0; d < D; ++d)
+            acc[d] += (int64_t)pq * vj[d];
+    }
+    const float l = oracle_canon_sum(tmp, n);
+    const float den = oracle_mul(l, 127.0f);
+    for (int64_t d = 0; d < D; ++d)
+        o[d] = oracle_div(oracle_mul(oracle_i2f(acc[d]), s_v), den);
+    *m_out = m;
+    *l_out = l;
+    free(s);
+    free(tmp);
+    free(acc);
+}
+
+void oracle_attn_fwd(const float* q, const float* k, const int8_t* vq, float s_v, float* o,
+                     float* mrow, float* lrow, int64_t B, int64_t T, int64_t Hq, int64_t Hkv,
+                     int64_t D, int64_t W)
+{
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t r = 0; r < B * T * Hq; ++r) {
+        const int64_t h = r % Hq, bi = r / Hq, i = bi % T, b = bi / T;
+        attn_fwd_row(q, k, vq, s_v, b, i, h, T, Hq, Hkv, D, W, o + r * D, mrow + r, lrow + r);
+    }
+}
+
+void oracle_attn_fwd_rows(const float* q, const float* k, const int8_t* vq, float s_v,
+                          const int64_t* rows, int64_t nrows, float* o, float* mrow,
+                          float* lrow, int64_t B, int64_t T, int64_t Hq, int64_t Hkv,
+                          int64_t D, int64_t W)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < nrows; ++t) {
+        const int64_t r = rows[t];
+        const int64_t h = r % Hq, bi = r / Hq, i = bi % T, b = bi / T;
+        attn_fwd_row(q, k, vq, s_v, b, i, h, T, Hq, Hkv, D, W, o + t * D, mrow + t, lrow + t);
+    }
+}
+
+/* Backward (straight-through for both quantisations):                        */
+/*   a_ij  = p_ij (/) l_i, p_ij recomputed as in the forward from m_i;        */
+/*   V^_jd = i2f(V_q,jd) (x) s_v;  Dr_i = canon_d(dO_id (x) O_id);            */
+/*   dA_ij = canon_d(dO_id (x) V^_jd);  dS_ij = a_ij (x) (dA_ij (-) Dr_i);    */
+/*   dQ_id = (fix2f(sum over key tiles t of fx(T_t))) (x) c, where T_t is the */
+/*     left-to-right sum over the valid keys j of the 64-aligned key tile t   */
+/*     of dS_ij (x) k_jd (seeded with the first such term), fx(x) = the       */
+/*     nearest int64 to x * 2^48 (ties to even, saturating) and fix2f(A) =    */
+/*     flush(i2f(A) * 2^-48): the tile partials are accumulated in 64-bit     */
+/*     fixed point, exactly and in any order;                                 */
+/*   dK_jd = (fold) (x) c and dV_jd = (fold), where the terms dS_ij (x) q_id  */
+/*     (dK) and a_ij (x) dO_id (dV) run over the query heads h of kv head g   */
+/*     in ascending order and, within a head, over the valid queries i;       */
+/*     they are grouped by 64-aligned query tile, each group summed left to   */
+/*     right from its first term, and the group partials folded left in      */
+/*     (head, tile) order.                                                    */
+#define ATTN_FIX_BITS 48
+#define ATTN_TILE 64
+
+int64_t oracle_attn_fx(float x)
+{
+    const double v = nearbyint((double)oracle_flush(x) * 281474976710656.0); /* exact */
+    if (v >= 9223372036854775807.0)
+        return INT64_MAX;
+    if (v <= -9223372036854775808.0)
+        return INT64_MIN;
+    return (int64_t)v;
+}
+
+float oracle_attn_fix2f(int64_t a)
+{
+    return oracle_flush(oracle_i2f(a) * (1.0f / 281474976710656.0f)); /* exact but for the flush */
+}
+
+static float attn_drow(const float* o, const float* dout, int64_t r, int64_t D, float* tmp)
+{
+    for (int64_t d = 0; d < D; ++d)
+        tmp[d] = oracle_mul(dout[r * D + d], o[r * D + d]);
+    return oracle_canon_sum(tmp, D);
+}
+
+/* a_ij and dS_ij for one (query row, key) pair */
+static void attn_pair(const float* q, const float* k, const int8_t* vq, float s_v,
+                      const float* dout, const float* mrow, const float* lrow, float drow,
+                      int64_t b, int64_t i, int64_t j, int64_t h, int64_t g, int64_t T,
+                      int64_t Hq, int64_t Hkv, int64_t D, float c, float* tmp, float* a_out,
+                      float* ds_out)
+{
+    const int64_t r = (b * T + i) * Hq + h;
+    const float s = attn_logit(q, k, b, i, j, h, g, T, Hq, Hkv, D, c, tmp);
+    const float a = oracle_div(oracle_exp(oracle_add(s, -mrow[r])), lrow[r]);
+    const int8_t* vj = vq + ((b * T + j) * Hkv + g) * D;
+    for (int64_t d = 0; d < D; ++d)
+        tmp[d] = oracle_mul(dout[r * D + d], oracle_mul(oracle_i2f(vj[d]), s_v));
+    const float dA = oracle_canon_sum(tmp, D);
+    *a_out = a;
+    *ds_out = oracle_mul(a, oracle_add(dA, -drow));
+}
+
+static void attn_dq_row(const float* q, const float* k, const int8_t* vq, float s_v,
+                        const float* o, const float* dout, const float* mrow, const float* lrow,
+                        int64_t b, int64_t i, int64_t h, int64_t T, int64_t Hq, int64_t Hkv,
+                        int64_t D, int64_t W, float* dq)
+{
+    const int64_t g = h / (Hq / Hkv), lo = attn_lo(i, W), r = (b * T + i) * Hq + h;
+    const float c = attn_c(D);
+    float* tmp = (float*)malloc((size_t)D * sizeof(float));
+    float* part = (float*)malloc((size_t)D * sizeof(float));
+    int64_t* acc = (int64_t*)calloc((size_t)D, sizeof(int64_t));
+    const float drow = attn_drow(o, dout, r, D, tmp);
+    for (int64_t t0 = (lo / ATTN_TILE) * ATTN_TILE; t0 <= i; t0 += ATTN_TILE) {
+        const int64_t jb = t0 > lo ? t0 : lo, je = t0 + ATTN_TILE - 1 < i ? t0 + ATTN_TILE - 1 : i;
+        for (int64_t j = jb; j <= je; ++j) {
+            float a, ds;
+            attn_pair(q, k, vq, s_v, dout, mrow, lrow, drow, b, i, j, h, g, T, Hq, Hkv, D, c,
+                      tmp, &a, &ds);
+            const float* kj = k + ((b * T + j) * Hkv + g) * D;
+            for (int64_t d = 0; d < D; ++d) {
+                const float t = oracle_mul(ds, kj[d]);
+                part[d] = j == jb ? t : oracle_add(part[d], t);
+            }
+        }
+        for (int64_t d = 0; d < D; ++d)
+            acc[d] += oracle_attn_fx(part[d]);
+    }
+    for (int64_t d = 0; d < D; ++d)
+        dq[d] = oracle_mul(oracle_attn_fix2f(acc[d]), c);
+    free(tmp);
+    free(part);
+    free(acc);
+}
+
+static void attn_dkdv_row(const float* q, const float* k, const int8_t* vq, float s_v,
+                          const float* o, const float* dout, const float* mrow,
+                          const float* lrow, int64_t b, int64_t j, int64_t g, int64_t T,
+                          int64_t Hq, int64_t Hkv, int64_t D, int64_t W, float* dk, float* dv)
+{
+    const int64_t G = Hq / Hkv;
+    const float c = attn_c(D);
+    const int64_t ihi = (W > 0 && j + W - 1 < T - 1) ? j + W - 1 : T - 1;
+    float* tmp = (float*)malloc((size_t)D * sizeof(float));
+    float* pk = (float*)malloc((size_t)D * sizeof(float));
+    float* pv = (float*)malloc((size_t)D * sizeof(float));
+    float* fk = (float*)malloc((size_t)D * sizeof(float));
+    float* fv = (float*)malloc((size_t)D * sizeof(float));
+    int first_group = 1;
+    for (int64_t hh = 0; hh < G; ++hh) {
+        const int64_t h = g * G + hh;
+        for (int64_t t0 = (j / ATTN_TILE) * ATTN_TILE; t0 <= ihi; t0 += ATTN_TILE) {
+            const int64_t ib = t0 > j ? t0 : j;
+            const int64_t ie = t0 + ATTN_TILE - 1 < ihi ? t0 + ATTN_TILE - 1 : ihi;
+            for (int64_t i = ib; i <= ie; ++i) {
+                const int64_t r = (b * T + i) * Hq + h;
+                const float drow = attn_drow(o, dout, r, D, tmp);
+                float a, ds;
+                attn_pair(q, k, vq, s_v, dout, mrow, lrow, drow, b, i, j, h, g, T, Hq, Hkv, D,
+                          c, tmp, &a, &ds);
+                const float* qi = q + r * D;
+                const float* di = dout + r * D;
+                for (int64_t d = 0; d < D; ++d) {
+                    const float tk = oracle_mul(ds, qi[d]);
+                    const float tv = oracle_mul(a, di[d]);
+                    pk[d] = i == ib ? tk : oracle_add(pk[d], tk);
+                    pv[d] = i == ib ? tv : oracle_add(pv[d], tv);
+                }
+            }
+            for (int64_t d = 0; d < D; ++d) {
+                fk[d] = first_group ? pk[d] : oracle_add(fk[d], pk[d]);
+                fv[d] = first_group ? pv[d] : oracle_add(fv[d], pv[d]);
+            }
+            first_group = 0;
+        }
+    }
+    for (int64_t d = 0; d < D; ++d) {
+        dk[d] = oracle_mul(fk[d], c);
+        dv[d] = fv[d];
+    }
+    free(tmp);
+    free(pk);
+    free(pv);
+    free(fk);
+    free(fv);
+}
+
+void oracle_attn_bwd(const float* q, const float* k, const int8_t* vq, float s_v, const float* o,
+                     const float* dout, const float* mrow, const float* lrow, float* dq, float* dk,
+                     float* dv, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
+                     int64_t W)
+{
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < B * T * Hq; ++r) {
+        const int64_t h = r % Hq, bi = r / Hq, i = bi % T, b = bi / T;
+        attn_dq_row(q, k, vq, s_v, o, dout, mrow, lrow, b, i, h, T, Hq, Hkv, D, W, dq + r * D);
+    }
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t r = 0; r < B * T * Hkv; ++r) {
+        const int64_t g = r % Hkv, bj = r / Hkv, j = bj % T, b = bj / T;
+        attn_dkdv_row(q, k, vq, s_v, o, dout, mrow, lrow, b, j, g, T, Hq, Hkv, D, W, dk + r * D,
+                      dv + r * D);
+    }
+}
+
+/* sampled rows: dq for query rows qrows[] (flat (b, i, h) indices), dk/dv for
+ * key rows krows[] (flat (b, j, g) indices) */
+void oracle_attn_bwd_rows(const float* q, const float* k, const int8_t* vq, float s_v,
+                          const float* o, const float* dout, const float* mrow,
+                          const float* lrow, const int64_t* qrows, int64_t nq, float* dq,
+                          const int64_t* krows, int64_t nk, float* dk, float* dv, int64_t B,
+                          int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t W)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < nq; ++t) {
+        const int64_t r = qrows[t];
+        const int64_t h = r % Hq, bi = r / Hq, i = bi % T, b = bi / T;
+        attn_dq_row(q, k, vq, s_v, o, dout, mrow, lrow, b, i, h, T, Hq, Hkv, D, W, dq + t * D);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < nk; ++t) {
+        const int64_t r = krows[t];
+        const int64_t g = r % Hkv, bj = r / Hkv, j = bj % T, b = bj / T;
+        attn_dkdv_row(q, k, vq, s_v, o, dout, mrow, lrow, b, j, g, T, Hq, Hkv, D, W, dk + t * D,
+                      dv + t * D);
+    }
+}
+
 int oracle_threads(void)
 {
 #ifdef _OPENMP

@@ -131,6 +131,28 @@ void oracle_adamw_step(float* p, float* m, float* v, const float* g, int64_t n, 
                        const oracle_adamw_hparams* hp, int64_t t);
 
 /* threads the parallel loops use (1 when built without OpenMP) */
+/* Attention with int8 P.V (see oracle.c for the readings and the order). */
+float oracle_exp(float x);
+int oracle_attn_quant_p(float p);
+int64_t oracle_attn_fx(float x);
+float oracle_attn_fix2f(int64_t a);
+void oracle_attn_fwd(const float* q, const float* k, const int8_t* vq, float s_v, float* o,
+                     float* mrow, float* lrow, int64_t B, int64_t T, int64_t Hq, int64_t Hkv,
+                     int64_t D, int64_t W);
+void oracle_attn_fwd_rows(const float* q, const float* k, const int8_t* vq, float s_v,
+                          const int64_t* rows, int64_t nrows, float* o, float* mrow,
+                          float* lrow, int64_t B, int64_t T, int64_t Hq, int64_t Hkv,
+                          int64_t D, int64_t W);
+void oracle_attn_bwd(const float* q, const float* k, const int8_t* vq, float s_v, const float* o,
+                     const float* dout, const float* mrow, const float* lrow, float* dq, float* dk,
+                     float* dv, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
+                     int64_t W);
+void oracle_attn_bwd_rows(const float* q, const float* k, const int8_t* vq, float s_v,
+                          const float* o, const float* dout, const float* mrow,
+                          const float* lrow, const int64_t* qrows, int64_t nq, float* dq,
+                          const int64_t* krows, int64_t nk, float* dk, float* dv, int64_t B,
+                          int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t W);
+
 int oracle_threads(void);
 
 #ifdef __cplusplus
