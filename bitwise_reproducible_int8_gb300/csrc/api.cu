@@ -488,6 +488,35 @@ int repro_treefold(const float* const* parts, int R, int64_t n, float* out, void
     return status_of(launch_treefold(parts, R, n, out, stream_grid(n / 4), as_stream(stream)));
 }
 
+int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v, float* o,
+                   float* m, float* l, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
+                   int64_t W, void* stream)
+{
+    if (B < 0 || T < 0 || Hq < 1 || Hkv < 1 || W < 0)
+        return REPRO_ERR_SHAPE;
+    if (D != REPRO_ATTN_HEAD_DIM || Hq % Hkv != 0 || T > REPRO_ATTN_MAX_T || Hq > 65535 ||
+        B > 65535)
+        return REPRO_ERR_SHAPE;
+    if (!q || !k || !vq || !s_v || !o || !m || !l)
+        return REPRO_ERR_ARG;
+    if (!al16(q) || !al16(k) || !al16(vq) || !al16(o) || !al4(s_v) || !al4(m) || !al4(l))
+        return REPRO_ERR_ALIGN;
+    if (B == 0 || T == 0)
+        return REPRO_OK;
+    const size_t nq = (size_t)(B * T * Hq * D) * 4, nk = (size_t)(B * T * Hkv * D);
+    const size_t nr = (size_t)(B * T * Hq) * 4;
+    if (overlap(o, nq, q, nq) || overlap(o, nq, k, nk * 4) || overlap(o, nq, vq, nk) ||
+        overlap(m, nr, o, nq) || overlap(l, nr, o, nq) || overlap(m, nr, l, nr) ||
+        overlap(m, nr, q, nq) || overlap(l, nr, q, nq) || overlap(m, nr, k, nk * 4) ||
+        overlap(l, nr, k, nk * 4) || overlap(m, nr, vq, nk) || overlap(l, nr, vq, nk) ||
+        overlap(o, nq, s_v, 4) || overlap(m, nr, s_v, 4) || overlap(l, nr, s_v, 4))
+        return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_attn_fwd(q, k, vq, s_v, o, m, l, B, T, Hq, Hkv, W, as_stream(stream)));
+}
+
 size_t repro_state_hash_ws_bytes(const int64_t* nbytes, int nbuf)
 {
     if (nbuf < 0 || nbuf > REPRO_HASH_MAX_BUFFERS || (nbuf > 0 && !nbytes))

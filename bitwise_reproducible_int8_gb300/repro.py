@@ -71,6 +71,8 @@ _SIGNATURES = {
     "repro_state_hash": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_i64), _int, _vp, _vp, _sz,
                                 _vp]),
     "repro_state_hash_ws_bytes": (_sz, [ctypes.POINTER(_i64), _int]),
+    "repro_attn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                              _i64, _vp]),
     "repro_status_str": (ctypes.c_char_p, [_int]),
     "repro_version": (_int, []),
     "repro_device_check": (_int, [_vp]),
@@ -247,6 +249,20 @@ def repro_treefold(parts, out: torch.Tensor, stream=None) -> None:
     arr = (_vp * max(R, 1))(*[_ptr(p, torch.float32, "part") for p in parts])
     _check("repro_treefold", lib().repro_treefold(arr, R, n, _ptr(out, torch.float32, "out"),
                                                   _stream(stream)))
+
+
+def repro_attn_fwd(q: torch.Tensor, k: torch.Tensor, vq: torch.Tensor, s_v: torch.Tensor,
+                   o: torch.Tensor, m: torch.Tensor, l: torch.Tensor, W: int = 0,
+                   stream=None) -> None:
+    """q, o [B,T,Hq,128] fp32; k [B,T,Hkv,128] fp32; vq [B,T,Hkv,128] int8;
+    s_v [1]; m, l [B,T,Hq] outputs.  W: sliding window (0: full causal)."""
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    _check("repro_attn_fwd", lib().repro_attn_fwd(
+        _ptr(q, torch.float32, "q"), _ptr(k, torch.float32, "k"), _ptr(vq, torch.int8, "vq"),
+        _ptr(s_v, torch.float32, "s_v"), _ptr(o, torch.float32, "o"),
+        _ptr(m, torch.float32, "m"), _ptr(l, torch.float32, "l"), B, T, Hq, Hkv, D, int(W),
+        _stream(stream)))
 
 
 REPRO_HASH_LEAF_BYTES = 4096

@@ -215,6 +215,38 @@ int repro_adamw_step(float* p, float* m, float* v, const float* g, int64_t n,
                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * Attention with int8 P.V ([use]: inside flash attention the P.V product runs
+ * on int8 while the QK^T logits and the softmax stay in high precision).  The
+ * pages fix no order; the library's, per query row i of head h (every
+ * operation binary32, rounded, subnormals flushed, never fused):
+ *   keys j in [lo_i, i]: causal, lo_i = max(0, i - W + 1) for a sliding
+ *     window of W tokens (W = 0: full causal); head h reads kv head
+ *     h / (Hq / Hkv) (grouped-query attention);
+ *   s_ij = canon_d(q_id (x) k_jd) (x) c, c = 1 (/) sqrt(128);
+ *   m_i = max_j s_ij, exact (a zero maximum is +0);
+ *   p_ij = exp_r(s_ij (-) m_i), where exp_r is Cody-Waite range reduction
+ *     with ln 2 = 0x1.63p-1 + (-0x1.bd0106p-13), k = rint(x (x) 0x1.715476p+0),
+ *     r = (x (-) k (x) C1) (-) k (x) C2, the degree-7 Taylor polynomial in
+ *     Horner form with coefficients RN(1/n!), times 2^k (0 for k < -126);
+ *   l_i = canon_j(p_ij), j ascending from lo_i;
+ *   P_ij = clamp(rint(p_ij (x) 127), 0, 127) (int8), and with V as int8 codes
+ *     V_q and per-tensor scale s_v (repro_wscale AMAX + repro_quant_i8):
+ *   o_id = (i2f(sum_j P_ij V_q,jd) (x) s_v) (/) (l_i (x) 127), the integer
+ *     sum exact.
+ * q, o: [B][T][Hq][128] fp32; k: [B][T][Hkv][128] fp32; vq: [B][T][Hkv][128]
+ * int8; s_v: 1 float (device); m, l: [B][T][Hq] fp32 outputs (row maxima and
+ * sums, the backward's inputs).  All DEVICE pointers, 16-byte aligned (m, l
+ * and s_v 4-byte).  D must be 128, Hq a multiple of Hkv, T <= 131072 (the
+ * exact int32 P.V bound), B and Hq <= 65535 (REPRO_ERR_SHAPE otherwise).
+ * o, m, l must not overlap the inputs or each other (REPRO_ERR_ALIAS).
+ * ------------------------------------------------------------------------ */
+#define REPRO_ATTN_HEAD_DIM 128
+#define REPRO_ATTN_MAX_T 131072
+int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
+                   float* o, float* m, float* l, int64_t B, int64_t T, int64_t Hq,
+                   int64_t Hkv, int64_t D, int64_t W, void* stream);
+
+/* ------------------------------------------------------------------------
  * Per-step state hash ([rit] paragraph 4, [limits]: a hash of the state is
  * recorded after every step and a replay must reproduce it; the pages hash on
  * the host and name on-device hashing as future work).  The pages fix no

@@ -468,16 +468,17 @@ void oracle_adamw_step(float* p, float* m, float* v, const float* g, int64_t n, 
 /* (exact in 9 bits, so k (x) C1 is exact), then the degree-7 Taylor         */
 /* polynomial of e^r in Horner form with binary32 coefficients RN(1/n!),     */
 /* then the exact scaling by 2^k; every operation rounded and flushed.       */
-#define EXP_LOG2E 1.44269502162933349609375f  /* RN(1/ln 2) */
-#define EXP_C1 0.693359375f                   /* 355/512 */
-#define EXP_C2 -2.12194440e-4f                /* RN(ln 2 - 355/512) */
+#define EXP_LOG2E 0x1.715476p+0f   /* RN(1/ln 2) */
+#define EXP_C1 0x1.63p-1f            /* 355/512 */
+#define EXP_C2 -0x1.bd0106p-13f      /* RN(ln 2 - 355/512) */
 
 float oracle_exp(float x)
 {
     const float kf = nearbyintf(oracle_mul(x, EXP_LOG2E)); /* ties to even */
     const float r = oracle_add(oracle_add(x, -oracle_mul(kf, EXP_C1)), -oracle_mul(kf, EXP_C2));
-    static const float c[8] = {1.0f, 1.0f, 0.5f, 1.0f / 6.0f, 1.0f / 24.0f, 1.0f / 120.0f,
-                               1.0f / 720.0f, 1.0f / 5040.0f};
+    /* RN(1/n!), n = 0..7 */
+    static const float c[8] = {1.0f, 1.0f, 0.5f, 0x1.555556p-3f, 0x1.555556p-5f, 0x1.111112p-7f,
+                               0x1.6c16c2p-10f, 0x1.a01a02p-13f};
     float p = c[7];
     for (int n = 6; n >= 0; --n)
         p = oracle_add(oracle_mul(p, r), c[n]);
@@ -533,6 +534,8 @@ static void attn_fwd_row(const float* q, const float* k, const int8_t* vq, float
         if (t == 0 || s[t] > m)
             m = s[t];
     }
+    if (m == 0.0f)
+        m = 0.0f; /* a zero maximum is stored as +0 */
     for (int64_t t = 0; t < n; ++t) {
         const float p = oracle_exp(oracle_add(s[t], -m));
         tmp[t] = p;

@@ -231,3 +231,22 @@ def test_state_hash_ws_bytes(L):
     n = 1000 * 4096 + 5                                   # 1001 leaves + 501 parents
     assert g((I * 1)(n), 1) == ((1001 * 32 + 255) // 256) * 256 + ((501 * 32 + 255) // 256) * 256
     assert g((I * 1)(-1), 1) == 0
+
+
+def test_attn_fwd_argument_checks(L):
+    f = L.repro_attn_fwd
+    Q, K, V, S, O, M, Lr = A, A * 2, A * 3, A * 4, A * 5, A * 6, A * 7
+    args = lambda **k: [k.get("q", Q), k.get("k", K), k.get("vq", V), k.get("sv", S),   # noqa: E731
+                        k.get("o", O), k.get("m", M), k.get("l", Lr), k.get("B", 1),
+                        k.get("T", 8), k.get("Hq", 4), k.get("Hkv", 2), k.get("D", 128),
+                        k.get("W", 0), None]
+    assert f(*args(D=64)) == -2                      # head dim must be 128
+    assert f(*args(Hkv=3)) == -2                     # Hq multiple of Hkv
+    assert f(*args(T=131073)) == -2                  # exact int32 P.V bound
+    assert f(*args(W=-1)) == -2
+    assert f(*args(q=None)) == -1
+    assert f(*args(o=O + 4)) == -3                   # misaligned
+    assert f(*args(o=Q)) == -8                       # o over q
+    assert f(*args(m=Lr)) == -8                      # m over l
+    assert f(*args(B=0)) == 0                        # nothing to do
+    assert f(*args()) in (-4, -5)                    # valid: reaches the architecture check
