@@ -517,6 +517,62 @@ int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float
     return status_of(launch_attn_fwd(q, k, vq, s_v, o, m, l, B, T, Hq, Hkv, W, as_stream(stream)));
 }
 
+size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq)
+{
+    if (B <= 0 || T <= 0 || Hq <= 0)
+        return 0;
+    return attn_bwd_ws_bytes(B, T, Hq);
+}
+
+int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
+                   const float* o, const float* dout, const float* m, const float* l, float* dq,
+                   float* dk, float* dv, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
+                   int64_t W, void* ws, size_t ws_bytes, void* stream)
+{
+    if (B < 0 || T < 0 || Hq < 1 || Hkv < 1 || W < 0)
+        return REPRO_ERR_SHAPE;
+    if (D != REPRO_ATTN_HEAD_DIM || Hq % Hkv != 0 || T > REPRO_ATTN_MAX_T || Hkv > 65535 ||
+        B > 65535)
+        return REPRO_ERR_SHAPE;
+    if (!q || !k || !vq || !s_v || !o || !dout || !m || !l || !dq || !dk || !dv)
+        return REPRO_ERR_ARG;
+    if (!al16(q) || !al16(k) || !al16(vq) || !al16(o) || !al16(dout) || !al16(dq) || !al16(dk) ||
+        !al16(dv) || !al4(s_v) || !al4(m) || !al4(l))
+        return REPRO_ERR_ALIGN;
+    if (B == 0 || T == 0)
+        return REPRO_OK;
+    const size_t nq = (size_t)(B * T * Hq * D) * 4, nk = (size_t)(B * T * Hkv * D);
+    const size_t nr = (size_t)(B * T * Hq) * 4;
+    const void* ins[8] = {q, k, vq, s_v, o, dout, m, l};
+    const size_t insz[8] = {nq, nk * 4, nk, 4, nq, nq, nr, nr};
+    void* outs[3] = {dq, dk, dv};
+    const size_t outsz[3] = {nq, nk * 4, nk * 4};
+    for (int x = 0; x < 3; ++x) {
+        for (int y = 0; y < 8; ++y)
+            if (overlap(outs[x], outsz[x], ins[y], insz[y]))
+                return REPRO_ERR_ALIAS;
+        for (int y = x + 1; y < 3; ++y)
+            if (overlap(outs[x], outsz[x], outs[y], outsz[y]))
+                return REPRO_ERR_ALIAS;
+    }
+    const size_t need = attn_bwd_ws_bytes(B, T, Hq);
+    if (!ws || ws_bytes < need)
+        return REPRO_ERR_WORKSPACE;
+    if (!al16(ws))
+        return REPRO_ERR_ALIGN;
+    for (int y = 0; y < 8; ++y)
+        if (overlap(ws, need, ins[y], insz[y]))
+            return REPRO_ERR_ALIAS;
+    for (int x = 0; x < 3; ++x)
+        if (overlap(ws, need, outs[x], outsz[x]))
+            return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, B, T, Hq, Hkv, W,
+                                     ws, as_stream(stream)));
+}
+
 size_t repro_state_hash_ws_bytes(const int64_t* nbytes, int nbuf)
 {
     if (nbuf < 0 || nbuf > REPRO_HASH_MAX_BUFFERS || (nbuf > 0 && !nbytes))

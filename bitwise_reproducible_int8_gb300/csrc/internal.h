@@ -79,6 +79,12 @@ cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, co
                             float* o, float* m, float* l, int64_t B, int64_t T, int64_t Hq,
                             int64_t Hkv, int64_t W, cudaStream_t st);
 
+size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq);
+cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
+                            const float* o, const float* dout, const float* m, const float* l,
+                            float* dq, float* dk, float* dv, int64_t B, int64_t T, int64_t Hq,
+                            int64_t Hkv, int64_t W, void* ws, cudaStream_t st);
+
 // ---- state hash (k_hash.cu)
 int64_t hash_leaf_count(const int64_t* nbytes, int nbuf, int64_t leaf_bytes);
 size_t hash_ws_bytes(int64_t nleaves);

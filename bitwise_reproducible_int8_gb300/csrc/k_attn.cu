@@ -354,7 +354,390 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Backward (straight-through for both quantisations), per the readings:
+//   a_ij  = p_ij (/) l_i (p recomputed from m_i as in the forward)
+//   Dr_i  = canon_d(dO_id (x) O_id)
+//   dA_ij = canon_d(dO_id (x) V^_jd),  V^ = i2f(V_q) (x) s_v
+//   dS_ij = a_ij (x) (dA_ij (-) Dr_i)
+//   dQ_id = fix2f(sum over 64-aligned key tiles of fx(T_tile)) (x) c, T_tile
+//           the left-to-right sum over the tile's valid keys of dS_ij (x) k_jd;
+//           fx(x) = nearest int64 to x * 2^48 (ties to even, saturating):
+//           the tile partials meet in 64-bit fixed point through integer
+//           atomics, exact in any order;
+//   dK_jd = (fold) (x) c, dV_jd = (fold): terms dS_ij (x) q_id and
+//           a_ij (x) dO_id over the query heads of kv head g (ascending) and
+//           the 64-aligned query tiles (ascending), each tile summed left to
+//           right from its first valid term, the tile partials folded left.
+// k_attn_bwd: one CTA per (64-key tile, kv head, sequence) visits its query
+// tiles in that order, so dK and dV stay in registers; dQ tile partials go
+// to an int64 accumulator with atomicAdd and are converted at the end.
+// ---------------------------------------------------------------------------
+
+constexpr int PR = 132;   // pitch (floats) of the row-major 64 x 128 tiles
+
+struct AttnBwdArgs {
+    const float* q;
+    const float* k;
+    const int8_t* vq;
+    const float* s_v;
+    const float* dout;
+    const float* m;
+    const float* l;
+    const float* drow;
+    unsigned long long* dq_acc;
+    float* dk;
+    float* dv;
+    int64_t T, Hq, Hkv, W;
+    float c;
+};
+
+constexpr size_t BWD_SMEM = (size_t)(4 * AT * PR + 2 * AT * PS + 3 * AT) * 4;
+
+// 64 rows of a [.., H, 128] tensor into t[r][d] (pitch PR), flushed; rows
+// outside [0, T) read as 0
+__device__ __forceinline__ void load_tile_r(float* __restrict__ t, const float* __restrict__ src,
+                                            int64_t row0, int64_t T, int64_t row_stride, int tid)
+{
+#pragma unroll
+    for (int it = 0; it < (AT * HD / 4) / NT; ++it) {
+        const int e = tid + it * NT;
+        const int r = e >> 5, c4 = e & 31;
+        const int64_t row = row0 + r;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row >= 0 && row < T)
+            v = flush4(*reinterpret_cast<const float4*>(src + row * row_stride + 4 * c4));
+        *reinterpret_cast<float4*>(t + r * PR + 4 * c4) = v;
+    }
+}
+
+// out[r][c] = canon_d(X[ty+16r][d] (x) Y[tx+16c][d]), d = 0..127: two chunks
+// of 64 summed left to right from their first product, then one pairwise add
+__device__ __forceinline__ void tile_dot(float (&out)[4][4], const float* __restrict__ X,
+                                         const float* __restrict__ Y, int ty, int tx)
+{
+    float t0[4][4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float acc[4][4];
+#pragma unroll 2
+        for (int d4 = 0; d4 < 16; ++d4) {
+            const int d = half * 64 + 4 * d4;
+            float4 xv[4], yv[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                xv[r] = *reinterpret_cast<const float4*>(X + (ty + 16 * r) * PR + d);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                yv[c] = *reinterpret_cast<const float4*>(Y + (tx + 16 * c) * PR + d);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float xe = e == 0 ? xv[r].x : (e == 1 ? xv[r].y : (e == 2 ? xv[r].z : xv[r].w));
+                        const float ye = e == 0 ? yv[c].x : (e == 1 ? yv[c].y : (e == 2 ? yv[c].z : yv[c].w));
+                        const float p = fmul_rn(xe, ye);
+                        acc[r][c] = (d4 == 0 && e == 0) ? p : fadd_ftz(acc[r][c], p);
+                    }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                if (half == 0)
+                    t0[r][c] = acc[r][c];
+                else
+                    out[r][c] = fadd_ftz(t0[r][c], acc[r][c]);
+            }
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
+{
+    extern __shared__ __align__(16) float smb[];
+    float* Ks = smb;                     // [AT][PR] keys of this tile
+    float* Vs = Ks + AT * PR;            // [AT][PR] dequantised values
+    float* Qs = Vs + AT * PR;            // [AT][PR] queries of the current tile
+    float* Gs = Qs + AT * PR;            // [AT][PR] dO of the current tile
+    float* As = Gs + AT * PR;            // [AT][PS] a_ij, row i, column j
+    float* Ss = As + AT * PS;            // [AT][PS] dS_ij
+    float* rm = Ss + AT * PS;            // [AT] m_i
+    float* rl = rm + AT;                 // [AT] l_i
+    float* rd = rl + AT;                 // [AT] Dr_i
+
+    const int tid = threadIdx.x;
+    const int ty = tid >> 4, tx = tid & 15;        // 4 x 4 tile: rows ty+16r, cols tx+16c
+    const int grp = tid >> 5, dg = tid & 31;       // 8 rows grp*8.., 4 columns 4dg..
+    const int64_t b = blockIdx.z, g = blockIdx.y, j0 = (int64_t)blockIdx.x * AT;
+    const int64_t T = a.T, W = a.W, Hq = a.Hq, Hkv = a.Hkv, G = Hq / Hkv;
+    const int64_t qstride = Hq * HD, kstride = Hkv * HD;
+    const float c = a.c;
+
+    load_tile_r(Ks, a.k + (b * T * Hkv + g) * HD, j0, T, kstride, tid);
+    {
+        const float sv = flush(*a.s_v);
+        const int8_t* vb = a.vq + (b * T * Hkv + g) * HD;
+#pragma unroll
+        for (int it = 0; it < (AT * HD / 4) / NT; ++it) {
+            const int e = tid + it * NT;
+            const int r = e >> 5, c4 = e & 31;
+            const int64_t row = j0 + r;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row < T) {
+                const int w = *reinterpret_cast<const int*>(vb + row * kstride + 4 * c4);
+                v = make_float4(dequant((int)(int8_t)w, sv), dequant((int)(int8_t)(w >> 8), sv),
+                                dequant((int)(int8_t)(w >> 16), sv), dequant((int)(int8_t)(w >> 24), sv));
+            }
+            *reinterpret_cast<float4*>(Vs + r * PR + 4 * c4) = v;
+        }
+    }
+
+    // dK / dV state: keys grp*8 + r, columns 4dg + e
+    float fk[8][4], fv[8][4];
+    bool started[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        started[r] = false;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            fk[r][e] = fv[r][e] = 0.f;
+    }
+
+    const int64_t ilast = W > 0 ? min(T - 1, j0 + AT - 1 + W - 1) : T - 1;
+    for (int64_t hh = 0; hh < G; ++hh) {
+        const int64_t h = g * G + hh;
+        for (int64_t i0 = j0; i0 <= ilast; i0 += AT) {
+            __syncthreads();   // previous tile's readers are done
+            load_tile_r(Qs, a.q + (b * T * Hq + h) * HD, i0, T, qstride, tid);
+            load_tile_r(Gs, a.dout + (b * T * Hq + h) * HD, i0, T, qstride, tid);
+            if (tid < AT) {
+                const int64_t i = i0 + tid;
+                const int64_t rr = (b * T + i) * Hq + h;
+                rm[tid] = i < T ? a.m[rr] : 0.f;
+                rl[tid] = i < T ? a.l[rr] : 1.f;
+                rd[tid] = i < T ? a.drow[rr] : 0.f;
+            }
+            __syncthreads();
+
+            // a and dS for the 64 x 64 pairs (query row ty+16r, key tx+16cc)
+            {
+                float sv[4][4], dav[4][4];
+                tile_dot(sv, Qs, Ks, ty, tx);
+                tile_dot(dav, Gs, Vs, ty, tx);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int ir = ty + 16 * r;
+                    const int64_t i = i0 + ir;
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const int jc = tx + 16 * cc;
+                        const int64_t j = j0 + jc;
+                        float av = 0.f, dsv = 0.f;
+                        if (i < T && j <= i && (W == 0 || i - j < W)) {
+                            const float s = fmul_flush(sv[r][cc], c);
+                            const float p = exp_r(fadd_ftz(s, -rm[ir]));
+                            av = flush(__fdiv_rn(p, rl[ir]));
+                            dsv = fmul_flush(av, fadd_ftz(dav[r][cc], -rd[ir]));
+                        }
+                        As[ir * PS + jc] = av;
+                        Ss[ir * PS + jc] = dsv;
+                    }
+                }
+            }
+            __syncthreads();
+
+            // dQ tile partials: rows grp*8 + r, columns 4dg + e, over the valid
+            // keys of this tile left to right, then into 64-bit fixed point
+            {
+                float part[8][4];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int ir = grp * 8 + r;
+                    const int64_t i = i0 + ir;
+                    const int64_t jb = max(j0, W > 0 ? i - W + 1 : (int64_t)0);
+                    const int64_t je = min(i, j0 + AT - 1);
+                    if (i >= T || jb > je)
+                        continue;
+                    for (int64_t j = jb; j <= je; ++j) {
+                        const int jc = (int)(j - j0);
+                        const float ds = Ss[ir * PS + jc];
+                        const float4 kv = *reinterpret_cast<const float4*>(Ks + jc * PR + 4 * dg);
+                        const float t0 = fmul_rn(ds, kv.x), t1 = fmul_rn(ds, kv.y);
+                        const float t2 = fmul_rn(ds, kv.z), t3 = fmul_rn(ds, kv.w);
+                        if (j == jb) {
+                            part[r][0] = flush(t0);
+                            part[r][1] = flush(t1);
+                            part[r][2] = flush(t2);
+                            part[r][3] = flush(t3);
+                        } else {
+                            part[r][0] = fadd_ftz(part[r][0], t0);
+                            part[r][1] = fadd_ftz(part[r][1], t1);
+                            part[r][2] = fadd_ftz(part[r][2], t2);
+                            part[r][3] = fadd_ftz(part[r][3], t3);
+                        }
+                    }
+                    unsigned long long* dst = a.dq_acc + ((b * T + i) * Hq + h) * HD + 4 * dg;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const long long fx = __float2ll_rn(fmul_rn(part[r][e], 0x1p48f));
+                        atomicAdd(dst + e, (unsigned long long)fx);
+                    }
+                }
+            }
+
+            // dK / dV tile partials: keys grp*8 + r, columns 4dg + e, over the
+            // valid query rows of this tile left to right, then folded
+            {
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const int jr = grp * 8 + r;
+                    const int64_t j = j0 + jr;
+                    const int64_t ib = max(i0, j);
+                    const int64_t ie = min(min(i0 + AT - 1, T - 1), W > 0 ? j + W - 1 : T - 1);
+                    if (j >= T || ib > ie)
+                        continue;
+                    float pk[4], pv[4];
+                    for (int64_t i = ib; i <= ie; ++i) {
+                        const int ir = (int)(i - i0);
+                        const float av = As[ir * PS + jr], dsv = Ss[ir * PS + jr];
+                        const float4 qv = *reinterpret_cast<const float4*>(Qs + ir * PR + 4 * dg);
+                        const float4 gv = *reinterpret_cast<const float4*>(Gs + ir * PR + 4 * dg);
+                        const float k0 = fmul_rn(dsv, qv.x), k1 = fmul_rn(dsv, qv.y);
+                        const float k2 = fmul_rn(dsv, qv.z), k3 = fmul_rn(dsv, qv.w);
+                        const float v0 = fmul_rn(av, gv.x), v1 = fmul_rn(av, gv.y);
+                        const float v2 = fmul_rn(av, gv.z), v3 = fmul_rn(av, gv.w);
+                        if (i == ib) {
+                            pk[0] = flush(k0); pk[1] = flush(k1); pk[2] = flush(k2); pk[3] = flush(k3);
+                            pv[0] = flush(v0); pv[1] = flush(v1); pv[2] = flush(v2); pv[3] = flush(v3);
+                        } else {
+                            pk[0] = fadd_ftz(pk[0], k0); pk[1] = fadd_ftz(pk[1], k1);
+                            pk[2] = fadd_ftz(pk[2], k2); pk[3] = fadd_ftz(pk[3], k3);
+                            pv[0] = fadd_ftz(pv[0], v0); pv[1] = fadd_ftz(pv[1], v1);
+                            pv[2] = fadd_ftz(pv[2], v2); pv[3] = fadd_ftz(pv[3], v3);
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        fk[r][e] = started[r] ? fadd_ftz(fk[r][e], pk[e]) : pk[e];
+                        fv[r][e] = started[r] ? fadd_ftz(fv[r][e], pv[e]) : pv[e];
+                    }
+                    started[r] = true;
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int64_t j = j0 + grp * 8 + r;
+        if (j >= T)
+            continue;
+        const int64_t off = ((b * T + j) * Hkv + g) * HD + 4 * dg;
+        *reinterpret_cast<float4*>(a.dk + off) =
+            make_float4(fmul_flush(fk[r][0], c), fmul_flush(fk[r][1], c), fmul_flush(fk[r][2], c),
+                        fmul_flush(fk[r][3], c));
+        *reinterpret_cast<float4*>(a.dv + off) = make_float4(fv[r][0], fv[r][1], fv[r][2], fv[r][3]);
+    }
+}
+
+// Dr_i = canon_d(dO_id (x) O_id) for 64 rows per CTA (rows contiguous, 128 floats)
+__global__ void __launch_bounds__(NT) k_attn_drow(const float* __restrict__ o,
+                                                 const float* __restrict__ dout,
+                                                 float* __restrict__ drow, int64_t nrows)
+{
+    __shared__ float prod[AT * 129];
+    const int tid = threadIdx.x;
+    const int64_t r0 = (int64_t)blockIdx.x * AT;
+#pragma unroll
+    for (int it = 0; it < (AT * HD / 4) / NT; ++it) {
+        const int e = tid + it * NT;
+        const int r = e >> 5, c4 = e & 31;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+        if (r0 + r < nrows) {
+            x = flush4(*reinterpret_cast<const float4*>(dout + (r0 + r) * HD + 4 * c4));
+            y = flush4(*reinterpret_cast<const float4*>(o + (r0 + r) * HD + 4 * c4));
+        }
+        prod[r * 129 + 4 * c4 + 0] = fmul_rn(x.x, y.x);
+        prod[r * 129 + 4 * c4 + 1] = fmul_rn(x.y, y.y);
+        prod[r * 129 + 4 * c4 + 2] = fmul_rn(x.z, y.z);
+        prod[r * 129 + 4 * c4 + 3] = fmul_rn(x.w, y.w);
+    }
+    __syncthreads();
+    if (tid < AT && r0 + tid < nrows) {
+        const float* p = prod + tid * 129;
+        float t0 = flush(p[0]);
+        for (int d = 1; d < 64; ++d)
+            t0 = fadd_ftz(t0, p[d]);
+        float t1 = flush(p[64]);
+        for (int d = 65; d < 128; ++d)
+            t1 = fadd_ftz(t1, p[d]);
+        drow[r0 + tid] = fadd_ftz(t0, t1);
+    }
+}
+
+// dQ = flush(i2f(acc) * 2^-48) (x) c
+__global__ void __launch_bounds__(NT) k_attn_dq_final(const unsigned long long* __restrict__ acc,
+                                                     float* __restrict__ dq, int64_t n, float c)
+{
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const float f = flush(fmul_rn(__ll2float_rn((long long)acc[e]), 0x1p-48f));
+        dq[e] = fmul_flush(f, c);
+    }
+}
+
 } // namespace
+
+size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq)
+{
+    const int64_t rows = B * T * Hq;
+    return (size_t)(((rows * HD * 8 + 255) & ~(int64_t)255) + rows * 4);
+}
+
+cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
+                            const float* o, const float* dout, const float* m, const float* l,
+                            float* dq, float* dk, float* dv, int64_t B, int64_t T, int64_t Hq,
+                            int64_t Hkv, int64_t W, void* ws, cudaStream_t st)
+{
+    const int64_t rows = B * T * Hq;
+    unsigned long long* acc = static_cast<unsigned long long*>(ws);
+    float* drow = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                           ((rows * HD * 8 + 255) & ~(int64_t)255));
+    const float c = 1.0f / sqrtf(128.0f);   // correctly rounded sqrt and division on the host
+    cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)(rows * HD * 8), st);
+    if (e != cudaSuccess)
+        return e;
+    k_attn_drow<<<(unsigned)((rows + AT - 1) / AT), NT, 0, st>>>(o, dout, drow, rows);
+    AttnBwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.vq = vq;
+    a.s_v = s_v;
+    a.dout = dout;
+    a.m = m;
+    a.l = l;
+    a.drow = drow;
+    a.dq_acc = acc;
+    a.dk = dk;
+    a.dv = dv;
+    a.T = T;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.W = W;
+    a.c = c;
+    e = cudaFuncSetAttribute(k_attn_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BWD_SMEM);
+    if (e != cudaSuccess)
+        return e;
+    dim3 grid((unsigned)((T + AT - 1) / AT), (unsigned)Hkv, (unsigned)B);
+    k_attn_bwd<<<grid, NT, BWD_SMEM, st>>>(a);
+    const int64_t n = rows * HD;
+    int nb = num_sms() * 8;
+    k_attn_dq_final<<<nb, NT, 0, st>>>(acc, dq, n, c);
+    count_launches(3);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                             float* o, float* m, float* l, int64_t B, int64_t T, int64_t Hq,

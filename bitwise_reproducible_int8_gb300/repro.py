@@ -73,6 +73,9 @@ _SIGNATURES = {
     "repro_state_hash_ws_bytes": (_sz, [ctypes.POINTER(_i64), _int]),
     "repro_attn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                               _i64, _vp]),
+    "repro_attn_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
+                              _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+    "repro_attn_bwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
     "repro_status_str": (ctypes.c_char_p, [_int]),
     "repro_version": (_int, []),
     "repro_device_check": (_int, [_vp]),
@@ -263,6 +266,26 @@ def repro_attn_fwd(q: torch.Tensor, k: torch.Tensor, vq: torch.Tensor, s_v: torc
         _ptr(s_v, torch.float32, "s_v"), _ptr(o, torch.float32, "o"),
         _ptr(m, torch.float32, "m"), _ptr(l, torch.float32, "l"), B, T, Hq, Hkv, D, int(W),
         _stream(stream)))
+
+
+def repro_attn_bwd_ws_bytes(B: int, T: int, Hq: int) -> int:
+    return int(lib().repro_attn_bwd_ws_bytes(int(B), int(T), int(Hq)))
+
+
+def repro_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, W: int = 0, ws=None,
+                   stream=None) -> None:
+    """dq [B,T,Hq,128], dk and dv [B,T,Hkv,128] from the forward's inputs,
+    output o, row statistics m, l and the upstream gradient dout."""
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    if ws is None:
+        ws = _workspace(repro_attn_bwd_ws_bytes(B, T, Hq), q.device)
+    f32 = torch.float32
+    _check("repro_attn_bwd", lib().repro_attn_bwd(
+        _ptr(q, f32, "q"), _ptr(k, f32, "k"), _ptr(vq, torch.int8, "vq"), _ptr(s_v, f32, "s_v"),
+        _ptr(o, f32, "o"), _ptr(dout, f32, "dout"), _ptr(m, f32, "m"), _ptr(l, f32, "l"),
+        _ptr(dq, f32, "dq"), _ptr(dk, f32, "dk"), _ptr(dv, f32, "dv"), B, T, Hq, Hkv, D, int(W),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 REPRO_HASH_LEAF_BYTES = 4096

@@ -247,6 +247,36 @@ int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float
                    int64_t Hkv, int64_t D, int64_t W, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Attention backward ([use]: the attention backward accumulates dQ in 64-bit
+ * fixed point for reproducibility).  Straight-through for the quantisation
+ * of P and V; the library's order, with p recomputed from the forward's m:
+ *   a_ij = p_ij (/) l_i;  V^_jd = i2f(V_q,jd) (x) s_v;
+ *   Dr_i = canon_d(dO_id (x) O_id);  dA_ij = canon_d(dO_id (x) V^_jd);
+ *   dS_ij = a_ij (x) (dA_ij (-) Dr_i);
+ *   dQ_id = fix2f(sum over 64-aligned key tiles t of fx(S_t)) (x) c, where
+ *     S_t is the left-to-right sum over the valid keys of tile t of
+ *     dS_ij (x) k_jd (seeded with the first term), fx(x) = the nearest int64
+ *     to x * 2^48 (ties to even, saturating) and fix2f(A) = i2f(A) * 2^-48,
+ *     flushed: the key tiles' partials meet in 64-bit fixed point, exactly
+ *     and in any order;
+ *   dK_jd = F_K (x) c and dV_jd = F_V, where the terms dS_ij (x) q_id (F_K)
+ *     and a_ij (x) dO_id (F_V) run over the query heads of kv head g in
+ *     ascending order and, within a head, over the valid queries i, grouped
+ *     by 64-aligned query tile; each group is summed left to right from its
+ *     first term and the group partials are folded left in (head, tile) order.
+ * Inputs as repro_attn_fwd plus o (its output), dout [B][T][Hq][128] and its
+ * m, l; outputs dq [B][T][Hq][128], dk, dv [B][T][Hkv][128] (DEVICE, 16-byte
+ * aligned, no overlaps).  ws: repro_attn_bwd_ws_bytes(B, T, Hq) bytes (the
+ * int64 dQ accumulator and the Dr_i), not overlapping anything else.
+ * ------------------------------------------------------------------------ */
+int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
+                   const float* o, const float* dout, const float* m, const float* l,
+                   float* dq, float* dk, float* dv, int64_t B, int64_t T, int64_t Hq,
+                   int64_t Hkv, int64_t D, int64_t W, void* ws, size_t ws_bytes,
+                   void* stream);
+size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq);
+
+/* ------------------------------------------------------------------------
  * Per-step state hash ([rit] paragraph 4, [limits]: a hash of the state is
  * recorded after every step and a replay must reproduce it; the pages hash on
  * the host and name on-device hashing as future work).  The pages fix no

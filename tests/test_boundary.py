@@ -250,3 +250,28 @@ def test_attn_fwd_argument_checks(L):
     assert f(*args(m=Lr)) == -8                      # m over l
     assert f(*args(B=0)) == 0                        # nothing to do
     assert f(*args()) in (-4, -5)                    # valid: reaches the architecture check
+
+
+def test_attn_bwd_argument_checks(L):
+    f = L.repro_attn_bwd
+    names = ["q", "k", "vq", "sv", "o", "dout", "m", "l", "dq", "dk", "dv"]
+    base = {n: A * (i + 1) for i, n in enumerate(names)}
+    W_ = A * 32
+
+    def args(**kw):
+        v = dict(base, **{k: kw[k] for k in kw if k in base})
+        return [v[n] for n in names] + [kw.get("B", 1), kw.get("T", 8), kw.get("Hq", 4),
+                                        kw.get("Hkv", 2), kw.get("D", 128), kw.get("W", 0),
+                                        kw.get("ws", W_), kw.get("wsb", 1 << 24), None]
+    assert f(*args(D=96)) == -2
+    assert f(*args(Hkv=3)) == -2
+    assert f(*args(dq=None)) == -1
+    assert f(*args(dk=A * 2 + 4)) == -3
+    assert f(*args(dq=A)) == -8                           # dq over q
+    assert f(*args(dv=A * 10)) == -8                      # dv over dk
+    assert f(*args(ws=None, wsb=0)) == -7
+    assert f(*args(wsb=16)) == -7
+    assert f(*args(ws=A)) == -8                           # ws over q
+    assert f(*args(B=0)) == 0
+    assert f(*args()) in (-4, -5)
+    assert repro.repro_attn_bwd_ws_bytes(1, 8, 4) == 8 * 4 * 128 * 8 + 8 * 4 * 4

@@ -85,3 +85,57 @@ def test_attn_fwd_repeatable():
     b = gpu_attn_fwd(q, k, vq, s_v, 100)
     for x, y in zip(a, b):
         assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+def gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W):
+    B, T, Hq, _ = q.shape
+    Hkv = k.shape[2]
+    dq = torch.empty((B, T, Hq, D), device="cuda")
+    dk = torch.empty((B, T, Hkv, D), device="cuda")
+    dv = torch.empty((B, T, Hkv, D), device="cuda")
+    R.repro_attn_bwd(G.dev(q), G.dev(k), G.dev(vq), G.scalar(s_v), G.dev(o), G.dev(dout),
+                     G.dev(m), G.dev(l), dq, dk, dv, W)
+    torch.cuda.synchronize()
+    assert R.repro_device_check() == 0
+    return G.host(dq), G.host(dk), G.host(dv)
+
+
+@pytest.mark.parametrize("W", [0, 1, 7, 64, 100])
+@pytest.mark.parametrize("B,T,Hq,Hkv", SHAPES)
+def test_attn_bwd_matches_oracle(orc, B, T, Hq, Hkv, W):
+    q, k, vq, s_v = _case(B * 1000 + T * 10 + W + 7, B, T, Hq, Hkv)
+    o, m, l = orc.attn_fwd(q, k, vq, s_v, W)
+    dout = (np.random.default_rng(T + W).standard_normal(o.shape) * 1e-3).astype(np.float32)
+    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    rq, rk, rv = orc.attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    G.assert_bits_equal(dv, rv, f"dv T={T} W={W}")
+    G.assert_bits_equal(dk, rk, f"dk T={T} W={W}")
+    G.assert_bits_equal(dq, rq, f"dq T={T} W={W}")
+
+
+@pytest.mark.parametrize("W", [512, 0])
+def test_attn_bwd_full_size_sampled(orc, W):
+    B, T, Hq, Hkv = 4, 4096, 16, 4
+    q, k, vq, s_v = _case(200 + W, B, T, Hq, Hkv)
+    o, m, l = gpu_attn_fwd(q, k, vq, s_v, W)          # forward parity is tested above
+    dout = (np.random.default_rng(W + 1).standard_normal(o.shape) * 1e-3).astype(np.float32)
+    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    rng = np.random.default_rng(W + 2)
+    qrows = np.unique(np.concatenate([rng.integers(0, B * T * Hq, 24), [0, B * T * Hq - 1,
+                                      (2 * T + 700) * Hq + 5]]))
+    krows = np.unique(np.concatenate([rng.integers(0, B * T * Hkv, 24), [0, B * T * Hkv - 1,
+                                      (1 * T + 4095) * Hkv + 2, (3 * T + 63) * Hkv + 1]]))
+    rq, rk, rv = orc.attn_bwd_rows(q, k, vq, s_v, o, dout, m, l, W, qrows, krows)
+    G.assert_bits_equal(dq.reshape(-1, D)[qrows], rq, "dq rows")
+    G.assert_bits_equal(dk.reshape(-1, D)[krows], rk, "dk rows")
+    G.assert_bits_equal(dv.reshape(-1, D)[krows], rv, "dv rows")
+
+
+def test_attn_bwd_repeatable():
+    q, k, vq, s_v = _case(4, 2, 300, 8, 2)
+    o, m, l = gpu_attn_fwd(q, k, vq, s_v, 100)
+    dout = (np.random.default_rng(0).standard_normal(o.shape) * 1e-3).astype(np.float32)
+    a = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, 100)
+    b = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, 100)
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
