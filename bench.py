@@ -444,13 +444,270 @@ def measure_e2e(hp, host, steps, stream, world):
             "ms_per_step": ms / steps}
 
 
+# ---------------------------------------------------------------- attention leg
+
+def attn_pairs(aw) -> int:
+    """Valid (query, key) pairs per step: sum over rows of min(i + 1, W)."""
+    T, W = aw.seq_len, aw.window
+    if W <= 0 or W >= T:
+        per_seq = T * (T + 1) // 2
+    else:
+        per_seq = W * (W + 1) // 2 + (T - W) * W
+    return per_seq * aw.sequences * aw.heads_q
+
+
+def attn_oracle_sample(aw, q, k, v, do, frac_log2: int) -> tuple:
+    """The oracle on a uniform 2^-k sample of one step's rows: V's scale and
+    codes in full, the forward of 1/2^k of the query rows, dQ of 1/2^k of the
+    query rows and dK, dV of 1/2^k of the key rows.  Returns (s, tokens)."""
+    import oracle as orc
+    f = 1 << frac_log2
+    nq, nk = aw.tokens * aw.heads_q, aw.tokens * aw.heads_kv
+    rng = np.random.default_rng(12345)
+    qrows = np.sort(rng.choice(nq, max(1, nq // f), replace=False))
+    krows = np.sort(rng.choice(nk, max(1, nk // f), replace=False))
+    t0 = time.perf_counter()
+    s_v = orc.wscale(v, 1)
+    vq = orc.quant_i8(v, s_v).reshape(v.shape)
+    o_s, m_s, l_s = orc.attn_fwd_rows(q, k, vq, s_v, aw.window, qrows)
+    sec = time.perf_counter() - t0
+    # the backward reads o, m, l of every row it touches: the sampled query
+    # rows carry their own from the timed forward; the other rows (reached by
+    # dK/dV) get placeholder statistics -- the same work per row, values unchecked
+    o = np.zeros((aw.tokens * aw.heads_q, q.shape[-1]), np.float32)
+    m = np.zeros(aw.tokens * aw.heads_q, np.float32)
+    l = np.ones(aw.tokens * aw.heads_q, np.float32)
+    o[qrows], m[qrows], l[qrows] = o_s, m_s, l_s
+    t1 = time.perf_counter()
+    orc.attn_bwd_rows(q, k, vq, s_v, o.reshape(q.shape), do, m.reshape(q.shape[:3]),
+                      l.reshape(q.shape[:3]), aw.window, qrows, krows)
+    sec += time.perf_counter() - t1
+    return sec, aw.tokens / f
+
+
+def _attn_sample_text(aw, frac_log2, toks, sec=None):
+    t = (f"{aw.name}: 1/{1 << frac_log2} of one step's rows -- forward and dQ of "
+         f"{max(1, aw.tokens * aw.heads_q >> frac_log2)} query rows, dK and dV of "
+         f"{max(1, aw.tokens * aw.heads_kv >> frac_log2)} key rows (dK/dV of unsampled query "
+         f"rows use placeholder statistics: same work, not checked), V's scale and codes in "
+         f"full; credited {toks:.1f} tokens")
+    return t + (f"; {sec:.2f} s" if sec is not None else "")
+
+
+def run_attn(args, aw):
+    import torch
+
+    from bitwise_reproducible_int8_gb300 import build_lib
+    from bitwise_reproducible_int8_gb300 import repro as R
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or not os.path.exists(build_lib.LIB):
+        build_lib.build()
+    if world > 1:
+        dist.barrier()
+    aw_r = dataclasses.replace(aw, seed=aw.seed + 1000 * rank)   # replicas only: own data
+    q, k, v, do = inputs.attn_inputs(aw_r)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    dev = torch.device("cuda", local)
+    tq, tk, tv, tdo = (torch.from_numpy(x).to(dev) for x in (q, k, v, do))
+    vq = torch.empty(v.shape, dtype=torch.int8, device=dev)
+    s_v = torch.zeros(1, device=dev)
+    o = torch.empty(q.shape, device=dev)
+    m = torch.empty(q.shape[:3], device=dev)
+    l = torch.empty(q.shape[:3], device=dev)
+    dq = torch.empty(q.shape, device=dev)
+    dk = torch.empty(k.shape, device=dev)
+    dv = torch.empty(k.shape, device=dev)
+    ws_s = torch.empty(max(R.repro_wscale_ws_bytes(v.size), 16), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(R.repro_attn_bwd_ws_bytes(B, T, Hq), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    timers = {}
+
+    def ev(cls):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        timers.setdefault(cls, []).append([e, None])
+
+    def end(cls):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        timers[cls][-1][1] = e
+
+    def one_step(timed):
+        if timed:
+            ev("vscale")
+        R.repro_wscale(tv, R.REPRO_SCALE_ACT_AMAX, s_v, ws=ws_s, stream=stream)
+        if timed:
+            end("vscale")
+            ev("vquant")
+        R.repro_quant_i8(tv, s_v, vq, stream=stream)
+        if timed:
+            end("vquant")
+            ev("attn_fwd")
+        R.repro_attn_fwd(tq, tk, vq, s_v, o, m, l, aw.window, stream=stream)
+        if timed:
+            end("attn_fwd")
+            ev("attn_bwd")
+        R.repro_attn_bwd(tq, tk, vq, s_v, o, tdo, m, l, dq, dk, dv, aw.window, ws=ws_b,
+                         stream=stream)
+        if timed:
+            end("attn_bwd")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step(False)
+    stream.synchronize()
+    if R.repro_device_check(stream) != 0:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = R.repro_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(args.steps):
+            one_step(True)
+        t_end.record(stream)
+    stream.synchronize()
+    launches = R.repro_launch_count() - launches0
+    clk = clocks.stop()
+    ms = t_start.elapsed_time(t_end)
+    if R.repro_device_check(stream) != 0:
+        raise RuntimeError("device error during the timed steps")
+    per_class = {kk: sum(a.elapsed_time(b) for a, b in vv) for kk, vv in timers.items()}
+    ms_max = max_over_ranks(ms, world, "cuda")
+    value = whole_job_tokens_per_s(aw.tokens, args.steps, world, ms_max)
+
+    # e2e: every step copies q, k, v, dO from pinned host memory and reads dq,
+    # dk, dv back, through the same calls
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (torch.from_numpy(x).pin_memory() for x in (q, k, v, do))
+        hdq = torch.empty(dq.shape).pin_memory()
+        hdk = torch.empty(dk.shape).pin_memory()
+        hdv = torch.empty(dv.shape).pin_memory()
+        with torch.cuda.stream(stream):
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            for _ in range(args.steps):
+                tq.copy_(hq, non_blocking=True)
+                tk.copy_(hk, non_blocking=True)
+                tv.copy_(hv, non_blocking=True)
+                tdo.copy_(hdo, non_blocking=True)
+                one_step(False)
+                hdq.copy_(dq, non_blocking=True)
+                hdk.copy_(dk, non_blocking=True)
+                hdv.copy_(dv, non_blocking=True)
+            a1.record(stream)
+        stream.synchronize()
+        e_ms = a0.elapsed_time(a1)
+        e2e = {"value": whole_job_tokens_per_s(aw.tokens, args.steps, world,
+                                               max_over_ranks(e_ms, world, "cuda")),
+               "unit": UNIT,
+               "h2d_bytes_per_step": int(4 * (q.size + k.size + v.size + do.size)),
+               "d2h_bytes_per_step": int(4 * (dq.numel() + dk.numel() + dv.numel())),
+               "ms_per_step": e_ms / args.steps}
+
+    if rank == 0:
+        peaks = load_peaks()
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        fp32_peak = sms * 128 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        pairs = attn_pairs(aw)
+        # algorithmic FP32 work per valid (query, key) pair: the logits once in
+        # the forward (2 * 128), and in the backward the logits, dA, dQ, dK
+        # and dV dot products (5 * 2 * 128); P.V is integer work (dp4a)
+        fwd_ops, bwd_ops = 2 * D * pairs, 10 * D * pairs
+        f_ms, b_ms = per_class.get("attn_fwd", 0.0), per_class.get("attn_bwd", 0.0)
+        ach = (fwd_ops + bwd_ops) * args.steps / ((f_ms + b_ms) / 1e3) / 1e12
+        roofline = {
+            "bound": "alu", "kernel": "k_attn_fwd + k_attn_bwd (canonical-order fp32 logits, "
+                                      "softmax and gradients; int8 P.V)",
+            "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s", "frac": ach / fp32_peak,
+            "peak_note": f"FP32 pipe: {sms} SMs x 128 lanes x {peaks.get('sm_max_mhz', 2070.0):.0f}"
+                         " MHz, one FMUL or FADD per lane per clock (no FMA may be used)",
+            "traffic": None, "launches": 4 * args.steps,
+            "flops_per_launch": (fwd_ops + bwd_ops) / 2,
+            "avg_launch_ms": (f_ms + b_ms) / (2 * args.steps),
+            "fwd_frac": fwd_ops * args.steps / (f_ms / 1e3) / 1e12 / fp32_peak if f_ms else None,
+            "bwd_frac": bwd_ops * args.steps / (b_ms / 1e3) / 1e12 / fp32_peak if b_ms else None,
+        }
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            import oracle as orc
+            orc.build()
+            sec, toks = attn_oracle_sample(aw_r, q, k, v, do, args.cpu_frac_log2)
+            cpu = {"value": toks / sec, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
+                   "sample": _attn_sample_text(aw, args.cpu_frac_log2, toks, sec)}
+        line = {
+            "metric": "tokens/s bit-exact int8 P.V attention fwd+bwd (1 GB300); % of FP32 roofline",
+            "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32/i8", "data": "synthetic",
+            "config": {"workload": aw.name, "tokens_per_step": aw.tokens,
+                       "sequences": aw.sequences, "seq_len": aw.seq_len, "heads_q": aw.heads_q,
+                       "heads_kv": aw.heads_kv, "head_dim": D, "window": aw.window,
+                       "pairs_per_step": pairs, "parallelism": "replicas only",
+                       "l2": "inputs larger than L2: q, k, v, dO and outputs ~0.7 GB"},
+            "roofline": roofline,
+            "ms_per_step_by_call": {kk: vv / args.steps for kk, vv in per_class.items()},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk, "peaks_source": peaks["source"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_attn_reference(args, aw):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle as orc
+    orc.build()
+    q, k, v, do = inputs.attn_inputs(aw)
+    for _ in range(args.warmup):
+        attn_oracle_sample(aw, q, k, v, do, args.ref_frac_log2)
+    runs = [attn_oracle_sample(aw, q, k, v, do, args.ref_frac_log2) for _ in range(args.steps)]
+    total = sum(r[0] for r in runs)
+    toks = sum(r[1] for r in runs)
+    value = toks / total
+    line = {
+        "metric": "tokens/s bit-exact int8 P.V attention fwd+bwd (1 GB300); % of FP32 roofline",
+        "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32/i8", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": aw.name, "tokens_per_step": aw.tokens,
+                   "sample_fraction": 1.0 / (1 << args.ref_frac_log2),
+                   "parallelism": "replicas only"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
+                         "sample": _attn_sample_text(aw, args.ref_frac_log2, toks / args.steps)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="block", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--workload", default="block",
+                    choices=sorted(inputs.WORKLOADS) + sorted(inputs.ATTN_WORKLOADS))
     ap.add_argument("--unfused-accum", action="store_true",
                     help="accumulate dW with repro_grad_accum instead of the fused epilogue")
     ap.add_argument("--no-e2e", action="store_true")
@@ -464,6 +721,11 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.workload in inputs.ATTN_WORKLOADS:
+        aw = inputs.ATTN_WORKLOADS[args.workload]
+        if args.impl == "reference":
+            return run_attn_reference(args, aw)
+        return run_attn(args, aw)
     wl = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)

@@ -29,6 +29,7 @@ BLOCK = 1 << 20
 
 # stream ids (one independent stream per tensor role)
 S_X, S_W, S_DY, S_NOISE, S_A, S_B = 1, 2, 3, 4, 5, 6
+S_Q, S_K, S_V, S_DO = 7, 8, 9, 10
 
 
 def _threads() -> int:
@@ -163,3 +164,49 @@ def small_case(seed: int, M: int, N: int, K: int, x_std=1.0, w_std=0.02, dy_std=
     """Random shapes for parity tests: (X[M,K], W[N,K], dY[M,N])."""
     return (normal(seed, S_X, (M, K), x_std), normal(seed, S_W, (N, K), w_std),
             normal(seed, S_DY, (M, N), dy_std))
+
+
+# ------------------------------------------------------------------ attention
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """One micro-batch through an attention layer: `sequences` x `seq_len`
+    tokens, grouped-query heads of HEAD_DIM, causal with a sliding window of
+    `window` tokens (0: full causal).  q and k stand for the post-QK-norm
+    (gainless RMSNorm) vectors, unit RMS per head, so N(0, 1) entries; v ~ N(0, 1);
+    the upstream gradient dO ~ N(0, 1e-3)."""
+    name: str
+    sequences: int
+    seq_len: int
+    heads_q: int
+    heads_kv: int
+    window: int
+    seed: int
+    description: str = field(default="", compare=False)
+
+    @property
+    def tokens(self) -> int:
+        return self.sequences * self.seq_len
+
+
+ATTN_WORKLOADS = {
+    # the pages' layers: 512-token sliding window, every fifth and the last layer full causal
+    "attn_swa": AttnWorkload("attn_swa", 4, 4096, HEADS_Q, HEADS_KV, 512, 300,
+                             "one 16,384-token micro-batch (4 x 4096) through a sliding-window "
+                             "layer: 16 query / 4 KV heads of 128, window 512"),
+    "attn_causal": AttnWorkload("attn_causal", 4, 4096, HEADS_Q, HEADS_KV, 0, 301,
+                                "one 16,384-token micro-batch (4 x 4096) through a full-causal "
+                                "layer: 16 query / 4 KV heads of 128"),
+    "attn_tiny": AttnWorkload("attn_tiny", 1, 130, 4, 2, 64, 302,
+                              "130 tokens, 4 query / 2 KV heads, window 64"),
+}
+
+
+def attn_inputs(aw: AttnWorkload):
+    """(q [B,T,Hq,128], k [B,T,Hkv,128], v [B,T,Hkv,128], dO [B,T,Hq,128]) float32."""
+    B, T = aw.sequences, aw.seq_len
+    q = normal(aw.seed, S_Q, (B, T, aw.heads_q, HEAD_DIM))
+    k = normal(aw.seed, S_K, (B, T, aw.heads_kv, HEAD_DIM))
+    v = normal(aw.seed, S_V, (B, T, aw.heads_kv, HEAD_DIM))
+    do = normal(aw.seed, S_DO, (B, T, aw.heads_q, HEAD_DIM), 1e-3)
+    return q, k, v, do
