@@ -36,11 +36,11 @@ from bitwise_reproducible_int8_gb300 import inputs  # noqa: E402
 
 METRIC = "tokens/s bit-exact int8-QAT linear fwd+bwd (1 GB300); % of int8/FP32/HBM roofline"
 
-# DRAM bytes (read + write) per backward launch of the default kernel, averaged over
-# the 160 backward launches of one block step, from one ncu capture of
+# DRAM bytes (read + write) per backward launch, averaged over the 160 backward
+# launches of the block workload's 4 captured steps, from one ncu capture of
 # dram__bytes_read.sum + dram__bytes_write.sum (single pass) on a GB300.  Valid only
 # for that kernel and workload; anything else reports null.
-BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd4"): 544.7e6}
+BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd4"): 544.7e6, ("block", "k_bwd_tma"): 1660.5e6}
 UNIT = "tokens/s"
 
 
