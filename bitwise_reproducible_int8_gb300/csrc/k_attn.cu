@@ -392,7 +392,46 @@ struct AttnBwdArgs {
     float c;
 };
 
-constexpr size_t BWD_SMEM = (size_t)(4 * AT * PR + 2 * AT * PS + 3 * AT) * 4;
+constexpr int PB = 68;    // pitch (floats) of the a, dS and transposed dS tiles
+
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t w[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+          "=r"(w[7]), "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]),
+          "=r"(w[14]), "=r"(w[15]), "=r"(w[16]), "=r"(w[17]), "=r"(w[18]), "=r"(w[19]),
+          "=r"(w[20]), "=r"(w[21]), "=r"(w[22]), "=r"(w[23]), "=r"(w[24]), "=r"(w[25]),
+          "=r"(w[26]), "=r"(w[27]), "=r"(w[28]), "=r"(w[29]), "=r"(w[30]), "=r"(w[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        v[e] = __uint_as_float(w[e]);
+}
+
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&v)[32])
+{
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+        w[e] = __float_as_uint(v[e]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
+        "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
+        "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+constexpr size_t BWD_SMEM = (size_t)(4 * AT * PR + 3 * AT * PB + 3 * AT) * 4 + 16;
 
 // 64 rows of a [.., H, 128] tensor into t[r][d] (pitch PR), flushed; rows
 // outside [0, T) read as 0
@@ -461,11 +500,13 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
     float* Vs = Ks + AT * PR;            // [AT][PR] dequantised values
     float* Qs = Vs + AT * PR;            // [AT][PR] queries of the current tile
     float* Gs = Qs + AT * PR;            // [AT][PR] dO of the current tile
-    float* As = Gs + AT * PR;            // [AT][PS] a_ij, row i, column j
-    float* Ss = As + AT * PS;            // [AT][PS] dS_ij
-    float* rm = Ss + AT * PS;            // [AT] m_i
+    float* As = Gs + AT * PR;            // [AT][PB] a_ij, row i, column j
+    float* Ss = As + AT * PB;            // [AT][PB] dS_ij
+    float* St = Ss + AT * PB;            // [AT][PB] dS transposed: row j, column i
+    float* rm = St + AT * PB;            // [AT] m_i
     float* rl = rm + AT;                 // [AT] l_i
     float* rd = rl + AT;                 // [AT] Dr_i
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(rd + AT);
 
     const int tid = threadIdx.x;
     const int ty = tid >> 4, tx = tid & 15;        // 4 x 4 tile: rows ty+16r, cols tx+16c
@@ -494,16 +535,25 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
         }
     }
 
-    // dK / dV state: keys grp*8 + r, columns 4dg + e
-    float fk[8][4], fv[8][4];
+    // dK / dV fold state (keys grp*8 + r, columns 4dg + e) lives in tensor
+    // memory: thread lane 32*(warp%4) + lane, columns (warp/4)*64 + [0, 32)
+    // for dK and + [32, 64) for dV, element r*4 + e
+    if (tid < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(tslot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const int warp = tid >> 5;
+    const uint32_t tfold =
+        *tslot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 64);
     bool started[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
+    for (int r = 0; r < 8; ++r)
         started[r] = false;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            fk[r][e] = fv[r][e] = 0.f;
-    }
 
     const int64_t ilast = W > 0 ? min(T - 1, j0 + AT - 1 + W - 1) : T - 1;
     for (int64_t hh = 0; hh < G; ++hh) {
@@ -541,43 +591,80 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                             av = flush(__fdiv_rn(p, rl[ir]));
                             dsv = fmul_flush(av, fadd_ftz(dav[r][cc], -rd[ir]));
                         }
-                        As[ir * PS + jc] = av;
-                        Ss[ir * PS + jc] = dsv;
+                        As[ir * PB + jc] = av;
+                        Ss[ir * PB + jc] = dsv;
+                        St[jc * PB + ir] = dsv;
                     }
                 }
             }
             __syncthreads();
 
             // dQ tile partials: rows grp*8 + r, columns 4dg + e, over the valid
-            // keys of this tile left to right, then into 64-bit fixed point
+            // keys of this tile left to right, then into 64-bit fixed point.
+            // Key index outermost; a tile where every row sees all 64 keys takes
+            // the packed path (pairs of rows), edge tiles the predicated one.
             {
-                float part[8][4];
+                int jb[8], je[8];
+                bool full = true;
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
-                    const int ir = grp * 8 + r;
-                    const int64_t i = i0 + ir;
-                    const int64_t jb = max(j0, W > 0 ? i - W + 1 : (int64_t)0);
-                    const int64_t je = min(i, j0 + AT - 1);
-                    if (i >= T || jb > je)
-                        continue;
-                    for (int64_t j = jb; j <= je; ++j) {
-                        const int jc = (int)(j - j0);
-                        const float ds = Ss[ir * PS + jc];
+                    const int64_t i = i0 + grp * 8 + r;
+                    const int64_t lo = W > 0 ? i - W + 1 : (int64_t)0;
+                    jb[r] = (int)(max(j0, lo) - j0);
+                    je[r] = (int)(min(i, j0 + AT - 1) - j0);
+                    if (i >= T)
+                        jb[r] = AT, je[r] = -1;
+                    full = full && jb[r] == 0 && je[r] == AT - 1;
+                }
+                float part[8][4];
+                if (full) {
+                    u64 pp[4][4];   // [row pair][column]
+#pragma unroll 2
+                    for (int jc = 0; jc < AT; ++jc) {
+                        const ulonglong2 s03 = *reinterpret_cast<const ulonglong2*>(St + jc * PB + grp * 8);
+                        const ulonglong2 s47 = *reinterpret_cast<const ulonglong2*>(St + jc * PB + grp * 8 + 4);
                         const float4 kv = *reinterpret_cast<const float4*>(Ks + jc * PR + 4 * dg);
-                        const float t0 = fmul_rn(ds, kv.x), t1 = fmul_rn(ds, kv.y);
-                        const float t2 = fmul_rn(ds, kv.z), t3 = fmul_rn(ds, kv.w);
-                        if (j == jb) {
-                            part[r][0] = flush(t0);
-                            part[r][1] = flush(t1);
-                            part[r][2] = flush(t2);
-                            part[r][3] = flush(t3);
-                        } else {
-                            part[r][0] = fadd_ftz(part[r][0], t0);
-                            part[r][1] = fadd_ftz(part[r][1], t1);
-                            part[r][2] = fadd_ftz(part[r][2], t2);
-                            part[r][3] = fadd_ftz(part[r][3], t3);
+                        const u64 P[4] = {s03.x, s03.y, s47.x, s47.y};
+                        const u64 Dk[4] = {pack2(kv.x, kv.x), pack2(kv.y, kv.y), pack2(kv.z, kv.z),
+                                           pack2(kv.w, kv.w)};
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const u64 t = fmul2_rn(P[q2], Dk[e]);
+                                pp[q2][e] = jc == 0 ? fadd2_ftz(t, pack2(-0.0f, -0.0f))
+                                                    : fadd2_ftz(pp[q2][e], t);
+                            }
+                    }
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            unpack2(pp[q2][e], part[2 * q2][e], part[2 * q2 + 1][e]);
+                } else {
+                    for (int jc = 0; jc < AT; ++jc) {
+                        const float4 s03 = *reinterpret_cast<const float4*>(St + jc * PB + grp * 8);
+                        const float4 s47 = *reinterpret_cast<const float4*>(St + jc * PB + grp * 8 + 4);
+                        const float4 kv = *reinterpret_cast<const float4*>(Ks + jc * PR + 4 * dg);
+                        const float sd[8] = {s03.x, s03.y, s03.z, s03.w, s47.x, s47.y, s47.z, s47.w};
+                        const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            if (jc < jb[r] || jc > je[r])
+                                continue;
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float t = fmul_rn(sd[r], kk[e]);
+                                part[r][e] = jc == jb[r] ? flush(t) : fadd_ftz(part[r][e], t);
+                            }
                         }
                     }
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    if (jb[r] > je[r])
+                        continue;
+                    const int64_t i = i0 + grp * 8 + r;
                     unsigned long long* dst = a.dq_acc + ((b * T + i) * Hq + h) * HD + 4 * dg;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -588,57 +675,115 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
             }
 
             // dK / dV tile partials: keys grp*8 + r, columns 4dg + e, over the
-            // valid query rows of this tile left to right, then folded
+            // valid query rows of this tile left to right, then folded.  Query
+            // index outermost; the packed path pairs keys.  dK first, then dV
+            // (one partial set live at a time).
             {
+                int ib[8], ie[8];
+                bool full = true;
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
-                    const int jr = grp * 8 + r;
-                    const int64_t j = j0 + jr;
-                    const int64_t ib = max(i0, j);
-                    const int64_t ie = min(min(i0 + AT - 1, T - 1), W > 0 ? j + W - 1 : T - 1);
-                    if (j >= T || ib > ie)
-                        continue;
-                    float pk[4], pv[4];
-                    for (int64_t i = ib; i <= ie; ++i) {
-                        const int ir = (int)(i - i0);
-                        const float av = As[ir * PS + jr], dsv = Ss[ir * PS + jr];
-                        const float4 qv = *reinterpret_cast<const float4*>(Qs + ir * PR + 4 * dg);
-                        const float4 gv = *reinterpret_cast<const float4*>(Gs + ir * PR + 4 * dg);
-                        const float k0 = fmul_rn(dsv, qv.x), k1 = fmul_rn(dsv, qv.y);
-                        const float k2 = fmul_rn(dsv, qv.z), k3 = fmul_rn(dsv, qv.w);
-                        const float v0 = fmul_rn(av, gv.x), v1 = fmul_rn(av, gv.y);
-                        const float v2 = fmul_rn(av, gv.z), v3 = fmul_rn(av, gv.w);
-                        if (i == ib) {
-                            pk[0] = flush(k0); pk[1] = flush(k1); pk[2] = flush(k2); pk[3] = flush(k3);
-                            pv[0] = flush(v0); pv[1] = flush(v1); pv[2] = flush(v2); pv[3] = flush(v3);
-                        } else {
-                            pk[0] = fadd_ftz(pk[0], k0); pk[1] = fadd_ftz(pk[1], k1);
-                            pk[2] = fadd_ftz(pk[2], k2); pk[3] = fadd_ftz(pk[3], k3);
-                            pv[0] = fadd_ftz(pv[0], v0); pv[1] = fadd_ftz(pv[1], v1);
-                            pv[2] = fadd_ftz(pv[2], v2); pv[3] = fadd_ftz(pv[3], v3);
+                    const int64_t j = j0 + grp * 8 + r;
+                    ib[r] = (int)(max(i0, j) - i0);
+                    ie[r] = (int)(min(min(i0 + AT - 1, T - 1), W > 0 ? j + W - 1 : T - 1) - i0);
+                    if (j >= T)
+                        ib[r] = AT, ie[r] = -1;
+                    full = full && ib[r] == 0 && ie[r] == AT - 1;
+                }
+#pragma unroll 1
+                for (int which = 0; which < 2; ++which) {
+                    // which 0: dK terms dS_ij (x) q_id; which 1: dV terms a_ij (x) dO_id
+                    const float* Wt = which == 0 ? Ss : As;
+                    const float* Xr = which == 0 ? Qs : Gs;
+                    float pt[8][4];
+                    if (full) {
+                        u64 pp[4][4];   // [key pair][column]
+#pragma unroll 2
+                        for (int ir = 0; ir < AT; ++ir) {
+                            const ulonglong2 w03 = *reinterpret_cast<const ulonglong2*>(Wt + ir * PB + grp * 8);
+                            const ulonglong2 w47 = *reinterpret_cast<const ulonglong2*>(Wt + ir * PB + grp * 8 + 4);
+                            const float4 xv = *reinterpret_cast<const float4*>(Xr + ir * PR + 4 * dg);
+                            const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
+                            const u64 X2[4] = {pack2(xv.x, xv.x), pack2(xv.y, xv.y), pack2(xv.z, xv.z),
+                                               pack2(xv.w, xv.w)};
+#pragma unroll
+                            for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const u64 t = fmul2_rn(P[q2], X2[e]);
+                                    pp[q2][e] = ir == 0 ? fadd2_ftz(t, pack2(-0.0f, -0.0f))
+                                                        : fadd2_ftz(pp[q2][e], t);
+                                }
+                        }
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                unpack2(pp[q2][e], pt[2 * q2][e], pt[2 * q2 + 1][e]);
+                    } else {
+                        for (int ir = 0; ir < AT; ++ir) {
+                            const float4 w03 = *reinterpret_cast<const float4*>(Wt + ir * PB + grp * 8);
+                            const float4 w47 = *reinterpret_cast<const float4*>(Wt + ir * PB + grp * 8 + 4);
+                            const float4 xv = *reinterpret_cast<const float4*>(Xr + ir * PR + 4 * dg);
+                            const float w8[8] = {w03.x, w03.y, w03.z, w03.w, w47.x, w47.y, w47.z, w47.w};
+                            const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                if (ir < ib[r] || ir > ie[r])
+                                    continue;
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float t = fmul_rn(w8[r], xx[e]);
+                                    pt[r][e] = ir == ib[r] ? flush(t) : fadd_ftz(pt[r][e], t);
+                                }
+                            }
                         }
                     }
+                    // fold (keys and their ranges are the same for every lane of a warp)
+                    float f[32];
+                    const uint32_t ta = tfold + (uint32_t)(32 * which);
+                    tm_ld32(ta, f);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        fk[r][e] = started[r] ? fadd_ftz(fk[r][e], pk[e]) : pk[e];
-                        fv[r][e] = started[r] ? fadd_ftz(fv[r][e], pv[e]) : pv[e];
+                    for (int r = 0; r < 8; ++r) {
+                        if (ib[r] > ie[r])
+                            continue;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            f[r * 4 + e] = started[r] ? fadd_ftz(f[r * 4 + e], pt[r][e]) : pt[r][e];
                     }
-                    started[r] = true;
+                    tm_st32(ta, f);
                 }
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (ib[r] <= ie[r])
+                        started[r] = true;
             }
         }
     }
 
+    {
+        float fk[32], fv[32];
+        tm_ld32(tfold, fk);
+        tm_ld32(tfold + 32, fv);
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int64_t j = j0 + grp * 8 + r;
-        if (j >= T)
-            continue;
-        const int64_t off = ((b * T + j) * Hkv + g) * HD + 4 * dg;
-        *reinterpret_cast<float4*>(a.dk + off) =
-            make_float4(fmul_flush(fk[r][0], c), fmul_flush(fk[r][1], c), fmul_flush(fk[r][2], c),
-                        fmul_flush(fk[r][3], c));
-        *reinterpret_cast<float4*>(a.dv + off) = make_float4(fv[r][0], fv[r][1], fv[r][2], fv[r][3]);
+        for (int r = 0; r < 8; ++r) {
+            const int64_t j = j0 + grp * 8 + r;
+            if (j >= T)
+                continue;
+            const int64_t off = ((b * T + j) * Hkv + g) * HD + 4 * dg;
+            *reinterpret_cast<float4*>(a.dk + off) =
+                make_float4(fmul_flush(fk[4 * r], c), fmul_flush(fk[4 * r + 1], c),
+                            fmul_flush(fk[4 * r + 2], c), fmul_flush(fk[4 * r + 3], c));
+            *reinterpret_cast<float4*>(a.dv + off) =
+                make_float4(fv[4 * r], fv[4 * r + 1], fv[4 * r + 2], fv[4 * r + 3]);
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (tid < 32) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(*tslot)
+                     : "memory");
     }
 }
 
