@@ -291,10 +291,24 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
         // chunk-of-64 / pairwise-tree stack
         if (tid < AT && my_i < T) {
             const int64_t cb = max(my_lo, j0), ce = min(my_i, j0 + AT - 1);
-            for (int64_t jj = cb; jj <= ce; ++jj) {
-                const float p = Ps[tid * PS + (int)(jj - j0)];
-                cs = (pos & 63) == 0 ? p : fadd_ftz(cs, p);
-                ++pos;
+            const float* prow = Ps + tid * PS;   // column jj - j0
+            int64_t jj = cb;
+            while (jj <= ce) {
+                // one run up to the next chunk boundary: left to right, seeded
+                // with the chunk's first term
+                const int room = 64 - (int)(pos & 63);
+                const int len = (int)min((int64_t)room, ce - jj + 1);
+                int k = 0;
+                const float* pr = prow + (int)(jj - j0);
+                if ((pos & 63) == 0) {
+                    cs = pr[0];
+                    k = 1;
+                }
+#pragma unroll 8
+                for (; k < len; ++k)
+                    cs = fadd_ftz(cs, pr[k]);
+                jj += len;
+                pos += len;
                 if ((pos & 63) == 0 || pos == my_n) {
                     const int64_t c = (pos - 1) >> 6;
                     float acc_t = cs;
