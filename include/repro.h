@@ -140,6 +140,11 @@ size_t repro_linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K);
  * ws: at least repro_linear_bwd_ws_bytes(M, N, K) bytes for the current
  * launch configuration.  Long reductions, and grids too small to fill whole
  * waves of SMs, are split into aligned segments whose partials live there.
+ * With the default kernel (16-byte-aligned rows: N % 4 == 0, K % 16 == 0) the
+ * call first writes its prepared operands there too -- flushed dY (transposed
+ * for dX) and the dequantised int8 operand, max(N*pad4(M) + N*K, M*N + M*K)
+ * floats after the segment partials -- and the main kernel reads them with
+ * tensor copies; the values, and so the bits, are those defined above.
  * M, N <= 4194240 (REPRO_ERR_SHAPE otherwise).
  * dx and dw must not overlap dy, xq or wq (REPRO_ERR_ALIAS).
  * ------------------------------------------------------------------------ */
