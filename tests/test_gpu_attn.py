@@ -139,3 +139,24 @@ def test_attn_bwd_repeatable():
     b = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, 100)
     for x, y in zip(a, b):
         assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+def test_attn_at_the_maximum_length(orc):
+    # T = 131,072 is the longest sequence for which the exact int32 P.V sum
+    # (at most 127 * 127 * T) fits; one head, full causal, sampled rows
+    B, T, Hq, Hkv = 1, 131072, 1, 1
+    q, k, vq, s_v = _case(131072, B, T, Hq, Hkv)
+    vq[:] = 127                                  # the largest codes
+    o, m, l = gpu_attn_fwd(q, k, vq, s_v, 0)
+    rows = np.array([0, 1, 4095, 65536, T - 2, T - 1])
+    ro, rm, rl = orc.attn_fwd_rows(q, k, vq, s_v, 0, rows)
+    G.assert_bits_equal(o.reshape(-1, D)[rows], ro, "o rows")
+    G.assert_bits_equal(m.reshape(-1)[rows], rm, "m rows")
+    G.assert_bits_equal(l.reshape(-1)[rows], rl, "l rows")
+    dout = (np.random.default_rng(1).standard_normal(o.shape) * 1e-3).astype(np.float32)
+    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, 0)
+    krows = np.array([0, 1, T - 1])
+    rq, rk, rv = orc.attn_bwd_rows(q, k, vq, s_v, o, dout, m, l, 0, rows, krows)
+    G.assert_bits_equal(dq.reshape(-1, D)[rows], rq, "dq rows")
+    G.assert_bits_equal(dk.reshape(-1, D)[krows], rk, "dk rows")
+    G.assert_bits_equal(dv.reshape(-1, D)[krows], rv, "dv rows")

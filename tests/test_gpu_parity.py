@@ -105,6 +105,23 @@ def test_forward(orc, M, N, K, path):
 
 
 @pytest.mark.parametrize("path", [0, 1])
+def test_forward_at_the_maximum_reduction(orc, path):
+    # K = 133,144 is the largest K for which |acc| <= 127 * 127 * K fits int32;
+    # codes at the clamp make row 0 reach 2,147,479,576
+    R.repro_set_launch_cfg(fwd_path=path)
+    K = 133144
+    rng = np.random.default_rng(5)
+    xq = rng.integers(-127, 128, (5, K)).astype(np.int8)
+    wq = rng.integers(-127, 128, (7, K)).astype(np.int8)
+    xq[0] = 127
+    wq[0] = 127
+    wq[1] = -127
+    y = G.gpu_fwd(xq, wq, np.float32(1.0), np.float32(1.0))
+    G.assert_bits_equal(y, orc.linear_fwd(xq, wq, 1.0, 1.0), "fwd K max")
+    assert orc.int_dot(xq, wq, 0, 0) == 127 * 127 * K
+
+
+@pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("K", [1024, 1040, 2048, 5632])
 def test_forward_adversarial(orc, K, path):
     R.repro_set_launch_cfg(fwd_path=path)
@@ -156,6 +173,17 @@ def test_backward_launch_invariance(orc, seg, kernel):
     dx, dw = G.gpu_bwd(dy, xq, wq, np.float32(0.03), np.float32(0.003))
     G.assert_bits_equal(dx, orc.linear_bwd_dx(dy, wq, np.float32(0.003)), f"dx seg {seg}")
     G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, np.float32(0.03)), f"dw seg {seg}")
+
+
+def test_backward_long_reduction(orc):
+    # dW over 70,000 tokens: 1094 chunks, more than one 256-chunk segment at the
+    # default launch, so the segment partials meet in the pairwise passes
+    rng = np.random.default_rng(70000)
+    M, N, K = 70000, 8, 32
+    dy = (rng.standard_normal((M, N)) * 1e-3).astype(np.float32)
+    xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    _, dw = G.gpu_bwd(dy, xq, None, np.float32(0.031), None, want_dx=False)
+    G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, np.float32(0.031)), "dw M=70000")
 
 
 def test_backward_discriminators(orc):
