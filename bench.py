@@ -525,6 +525,8 @@ def run_attn(args, aw):
     dv = torch.empty(k.shape, device=dev)
     ws_s = torch.empty(max(R.repro_wscale_ws_bytes(v.size), 16), dtype=torch.uint8, device=dev)
     ws_b = torch.empty(R.repro_attn_bwd_ws_bytes(B, T, Hq), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(max(R.repro_attn_fwd_ws_bytes(B, T, Hq, aw.window), 16), dtype=torch.uint8,
+                       device=dev)   # the forward's logit cache
     stream = torch.cuda.Stream()
     timers = {}
 
@@ -549,7 +551,7 @@ def run_attn(args, aw):
         if timed:
             end("vquant")
             ev("attn_fwd")
-        R.repro_attn_fwd(tq, tk, vq, s_v, o, m, l, aw.window, stream=stream)
+        R.repro_attn_fwd(tq, tk, vq, s_v, o, m, l, aw.window, ws=ws_f, stream=stream)
         if timed:
             end("attn_fwd")
             ev("attn_bwd")

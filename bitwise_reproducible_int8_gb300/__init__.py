@@ -10,7 +10,8 @@ from .repro import (  # noqa: F401
     REPRO_SCALE_WEIGHT_MEANABS, ReproError, lib, repro_device_check, repro_grad_accum,
     repro_launch_count, repro_linear_bwd, repro_linear_bwd_ws_bytes, repro_linear_fwd,
     repro_linear_fwd_ws_bytes, repro_running_sum, repro_sumsq, repro_sumsq_ws_bytes,
-    repro_adamw_step, repro_attn_bwd, repro_attn_bwd_ws_bytes, repro_attn_fwd, repro_quant_i8,
+    repro_adamw_step, repro_attn_bwd, repro_attn_bwd_ws_bytes, repro_attn_fwd, repro_attn_fwd_ws_bytes,
+    repro_quant_i8,
     repro_set_launch_cfg, repro_state_hash, repro_state_hash_ws_bytes, repro_status_str,
     repro_treefold, repro_version, repro_wscale, repro_wscale_ws_bytes, REPRO_HASH_LEAF_BYTES,
 )

@@ -488,9 +488,16 @@ int repro_treefold(const float* const* parts, int R, int64_t n, float* out, void
     return status_of(launch_treefold(parts, R, n, out, stream_grid(n / 4), as_stream(stream)));
 }
 
+size_t repro_attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W)
+{
+    if (B <= 0 || T <= 0 || Hq <= 0 || W < 0 || T > REPRO_ATTN_MAX_T)
+        return 0;
+    return attn_fwd_ws_bytes(B, T, Hq, W);
+}
+
 int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v, float* o,
                    float* m, float* l, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
-                   int64_t W, void* stream)
+                   int64_t W, void* ws, size_t ws_bytes, void* stream)
 {
     if (B < 0 || T < 0 || Hq < 1 || Hkv < 1 || W < 0)
         return REPRO_ERR_SHAPE;
@@ -511,10 +518,23 @@ int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float
         overlap(l, nr, k, nk * 4) || overlap(m, nr, vq, nk) || overlap(l, nr, vq, nk) ||
         overlap(o, nq, s_v, 4) || overlap(m, nr, s_v, 4) || overlap(l, nr, s_v, 4))
         return REPRO_ERR_ALIAS;
+    if (ws) {
+        const size_t need = attn_fwd_ws_bytes(B, T, Hq, W);
+        if (ws_bytes < need)
+            return REPRO_ERR_WORKSPACE;
+        if (!al16(ws))
+            return REPRO_ERR_ALIGN;
+        const void* bufs[7] = {q, k, vq, s_v, o, m, l};
+        const size_t sz[7] = {nq, nk * 4, nk, 4, nq, nr, nr};
+        for (int x = 0; x < 7; ++x)
+            if (overlap(ws, need, bufs[x], sz[x]))
+                return REPRO_ERR_ALIAS;
+    }
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
-    return status_of(launch_attn_fwd(q, k, vq, s_v, o, m, l, B, T, Hq, Hkv, W, as_stream(stream)));
+    return status_of(
+        launch_attn_fwd(q, k, vq, s_v, o, m, l, B, T, Hq, Hkv, W, ws, as_stream(stream)));
 }
 
 size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq)

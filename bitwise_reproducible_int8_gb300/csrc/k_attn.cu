@@ -45,9 +45,25 @@ struct AttnFwdArgs {
     float* o;
     float* m;
     float* l;
+    float* cache;      // optional: pass-1 logits, read back by pass 2 (NULL: recompute)
     int64_t T, Hq, Hkv, W;
+    int64_t tiles_bh;  // cached logit tiles per (sequence, head)
     float c;
 };
+
+// key tiles visited by query tiles 0 .. qt-1 (tile u visits tiles
+// max(0, 64u - W + 1) / 64 .. u): the offset of query tile qt's logits in the
+// per-(sequence, head) cache, in 64 x 64 tiles
+__host__ __device__ __forceinline__ int64_t tile_prefix(int64_t qt, int64_t W)
+{
+    if (W <= 0)
+        return qt * (qt + 1) / 2;
+    const int64_t D = W - 1;
+    const int64_t c1 = (D + 63) / 64;   // every tile past the first ones visits c1 + 1 tiles
+    const int64_t us = D / 64 + 1;      // first query tile whose window starts after key 0
+    const int64_t mq = qt < us ? qt : us;
+    return mq * (mq + 1) / 2 + (qt > us ? (qt - us) * (c1 + 1) : 0);
+}
 
 constexpr size_t FWD_SMEM = (size_t)(2 * HD * PT + AT * PS) * 4 + (size_t)(AT * PP) * 4 +
                             (size_t)(AT / 4 * HD) * 4 + (size_t)(AT * (MAXL + 1)) * 4 +
@@ -180,6 +196,11 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
     const int64_t jlo = W > 0 ? max((int64_t)0, i0 - W + 1) : 0;
     const int64_t jhi = min(i0 + AT - 1, T - 1);
     const int64_t t_lo = jlo / AT, t_hi = jhi / AT;
+    // this CTA's cached logits: tile t at (t - t_lo) * 4096 floats, thread tid's
+    // 16 values (its 4 x 4 outputs as 8 packed pairs) at tid * 16
+    float* cache = a.cache ? a.cache + ((b * a.Hq + h) * a.tiles_bh +
+                                        tile_prefix((int64_t)blockIdx.x, W)) * (AT * AT)
+                           : nullptr;
 
     load_tile_t(Qt, qbase, i0, T, qstride, tid);
 
@@ -192,6 +213,12 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
         __syncthreads();
         u64 s[8];
         logits4x4(s, Qt, Kt, ty, tx, a.c);
+        if (cache) {
+            ulonglong2* dst = reinterpret_cast<ulonglong2*>(cache + (t - t_lo) * (AT * AT) + tid * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[e] = make_ulonglong2(s[2 * e], s[2 * e + 1]);
+        }
 #pragma unroll
         for (int ip = 0; ip < 2; ++ip)
 #pragma unroll
@@ -239,7 +266,8 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
     for (int64_t t = t_lo; t <= t_hi; ++t) {
         const int64_t j0 = t * AT;
         __syncthreads();   // Kt, Ps, Pp, Vp free
-        load_tile_t(Kt, kbase, j0, T, kstride, tid);
+        if (!cache)
+            load_tile_t(Kt, kbase, j0, T, kstride, tid);
         // V codes as packed words: Vp[jq][d] = bytes of keys 4jq .. 4jq+3 at column d
 #pragma unroll
         for (int it = 0; it < (AT / 4 * HD / 4) / NT; ++it) {
@@ -263,7 +291,18 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
         __syncthreads();
         {
             u64 s[8];
-            logits4x4(s, Qt, Kt, ty, tx, a.c);
+            if (cache) {
+                const ulonglong2* src =
+                    reinterpret_cast<const ulonglong2*>(cache + (t - t_lo) * (AT * AT) + tid * 16);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const ulonglong2 v = src[e];
+                    s[2 * e] = v.x;
+                    s[2 * e + 1] = v.y;
+                }
+            } else {
+                logits4x4(s, Qt, Kt, ty, tx, a.c);
+            }
 #pragma unroll
             for (int ip = 0; ip < 2; ++ip)
 #pragma unroll
@@ -898,9 +937,15 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
     return cudaGetLastError();
 }
 
+size_t attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W)
+{
+    const int64_t nqt = (T + AT - 1) / AT;
+    return (size_t)(B * Hq * tile_prefix(nqt, W) * (AT * AT) * 4);
+}
+
 cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                             float* o, float* m, float* l, int64_t B, int64_t T, int64_t Hq,
-                            int64_t Hkv, int64_t W, cudaStream_t st)
+                            int64_t Hkv, int64_t W, void* cache, cudaStream_t st)
 {
     AttnFwdArgs a;
     a.q = q;
@@ -914,6 +959,8 @@ cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, co
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.W = W;
+    a.cache = static_cast<float*>(cache);
+    a.tiles_bh = tile_prefix((T + AT - 1) / AT, W);
     a.c = 1.0f / sqrtf(128.0f);   // correctly rounded sqrt and division on the host
     cudaError_t e = cudaFuncSetAttribute(k_attn_fwd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)FWD_SMEM);

@@ -72,7 +72,8 @@ _SIGNATURES = {
                                 _vp]),
     "repro_state_hash_ws_bytes": (_sz, [ctypes.POINTER(_i64), _int]),
     "repro_attn_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
-                              _i64, _vp]),
+                              _i64, _vp, _sz, _vp]),
+    "repro_attn_fwd_ws_bytes": (_sz, [_i64, _i64, _i64, _i64]),
     "repro_attn_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
                               _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
     "repro_attn_bwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
@@ -254,18 +255,25 @@ def repro_treefold(parts, out: torch.Tensor, stream=None) -> None:
                                                   _stream(stream)))
 
 
+def repro_attn_fwd_ws_bytes(B: int, T: int, Hq: int, W: int = 0) -> int:
+    return int(lib().repro_attn_fwd_ws_bytes(int(B), int(T), int(Hq), int(W)))
+
+
 def repro_attn_fwd(q: torch.Tensor, k: torch.Tensor, vq: torch.Tensor, s_v: torch.Tensor,
-                   o: torch.Tensor, m: torch.Tensor, l: torch.Tensor, W: int = 0,
+                   o: torch.Tensor, m: torch.Tensor, l: torch.Tensor, W: int = 0, ws=None,
                    stream=None) -> None:
     """q, o [B,T,Hq,128] fp32; k [B,T,Hkv,128] fp32; vq [B,T,Hkv,128] int8;
-    s_v [1]; m, l [B,T,Hq] outputs.  W: sliding window (0: full causal)."""
+    s_v [1]; m, l [B,T,Hq] outputs.  W: sliding window (0: full causal).
+    ws: optional logit cache of repro_attn_fwd_ws_bytes bytes (None: the
+    second pass recomputes the logits; same bits)."""
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check("repro_attn_fwd", lib().repro_attn_fwd(
         _ptr(q, torch.float32, "q"), _ptr(k, torch.float32, "k"), _ptr(vq, torch.int8, "vq"),
         _ptr(s_v, torch.float32, "s_v"), _ptr(o, torch.float32, "o"),
         _ptr(m, torch.float32, "m"), _ptr(l, torch.float32, "l"), B, T, Hq, Hkv, D, int(W),
-        _stream(stream)))
+        _ptr(ws, None, "ws"), ws_bytes, _stream(stream)))
 
 
 def repro_attn_bwd_ws_bytes(B: int, T: int, Hq: int) -> int:

@@ -244,12 +244,20 @@ int repro_adamw_step(float* p, float* m, float* v, const float* g, int64_t n,
  * and s_v 4-byte).  D must be 128, Hq a multiple of Hkv, T <= 131072 (the
  * exact int32 P.V bound), B and Hq <= 65535 (REPRO_ERR_SHAPE otherwise).
  * o, m, l must not overlap the inputs or each other (REPRO_ERR_ALIAS).
+ * The exact maximum needs the logits twice.  ws (optional, DEVICE): with at
+ * least repro_attn_fwd_ws_bytes(B, T, Hq, W) bytes the first pass stores its
+ * logits there and the second reads them back; with ws == NULL the second pass
+ * recomputes them.  Same bits either way.  The cache holds every visited
+ * 64 x 64 logit tile: about 4 * 64 * (W + 64) bytes per query row and head for a
+ * window W, 2 * T bytes per query row and head for full causal.
  * ------------------------------------------------------------------------ */
 #define REPRO_ATTN_HEAD_DIM 128
 #define REPRO_ATTN_MAX_T 131072
 int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                    float* o, float* m, float* l, int64_t B, int64_t T, int64_t Hq,
-                   int64_t Hkv, int64_t D, int64_t W, void* stream);
+                   int64_t Hkv, int64_t D, int64_t W, void* ws, size_t ws_bytes,
+                   void* stream);
+size_t repro_attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);
 
 /* ------------------------------------------------------------------------
  * Attention backward ([use]: the attention backward accumulates dQ in 64-bit

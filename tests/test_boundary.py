@@ -239,8 +239,13 @@ def test_attn_fwd_argument_checks(L):
     args = lambda **k: [k.get("q", Q), k.get("k", K), k.get("vq", V), k.get("sv", S),   # noqa: E731
                         k.get("o", O), k.get("m", M), k.get("l", Lr), k.get("B", 1),
                         k.get("T", 8), k.get("Hq", 4), k.get("Hkv", 2), k.get("D", 128),
-                        k.get("W", 0), None]
+                        k.get("W", 0), k.get("ws", None), k.get("wsb", 0), None]
     assert f(*args(D=64)) == -2                      # head dim must be 128
+    need = repro.repro_attn_fwd_ws_bytes(1, 8, 4, 0)
+    assert need == 4 * 64 * 64 * 4                   # one query tile, one key tile, 4 heads
+    assert f(*args(ws=A * 16, wsb=need - 1)) == -7   # logit cache too small
+    assert f(*args(ws=A * 16 + 8, wsb=need)) == -3   # misaligned cache
+    assert f(*args(ws=Q, wsb=need)) == -8            # cache over q
     assert f(*args(Hkv=3)) == -2                     # Hq multiple of Hkv
     assert f(*args(T=131073)) == -2                  # exact int32 P.V bound
     assert f(*args(W=-1)) == -2

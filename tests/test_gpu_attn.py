@@ -23,12 +23,16 @@ def _case(seed, B, T, Hq, Hkv):
     return q, k, vq, s_v
 
 
-def gpu_attn_fwd(q, k, vq, s_v, W):
+def gpu_attn_fwd(q, k, vq, s_v, W, cache=True):
     B, T, Hq, _ = q.shape
     o = torch.empty((B, T, Hq, D), device="cuda")
     m = torch.empty((B, T, Hq), device="cuda")
     l = torch.empty((B, T, Hq), device="cuda")
-    R.repro_attn_fwd(G.dev(q), G.dev(k), G.dev(vq), G.scalar(s_v), o, m, l, W)
+    ws = None
+    if cache:
+        ws = torch.empty(max(R.repro_attn_fwd_ws_bytes(B, T, Hq, W), 16), dtype=torch.uint8,
+                         device="cuda")
+    R.repro_attn_fwd(G.dev(q), G.dev(k), G.dev(vq), G.scalar(s_v), o, m, l, W, ws=ws)
     torch.cuda.synchronize()
     assert R.repro_device_check() == 0
     return G.host(o), G.host(m), G.host(l)
@@ -38,11 +42,12 @@ SHAPES = [(1, 1, 4, 2), (1, 5, 4, 2), (1, 63, 2, 2), (1, 64, 4, 1), (2, 65, 4, 2
           (1, 130, 8, 2), (2, 200, 4, 4), (1, 257, 4, 2)]
 
 
+@pytest.mark.parametrize("cache", [True, False], ids=["cached", "recomputed"])
 @pytest.mark.parametrize("W", [0, 1, 7, 64, 100])
 @pytest.mark.parametrize("B,T,Hq,Hkv", SHAPES)
-def test_attn_fwd_matches_oracle(orc, B, T, Hq, Hkv, W):
+def test_attn_fwd_matches_oracle(orc, B, T, Hq, Hkv, W, cache):
     q, k, vq, s_v = _case(B * 1000 + T * 10 + W, B, T, Hq, Hkv)
-    o, m, l = gpu_attn_fwd(q, k, vq, s_v, W)
+    o, m, l = gpu_attn_fwd(q, k, vq, s_v, W, cache)
     ro, rm, rl = orc.attn_fwd(q, k, vq, s_v, W)
     G.assert_bits_equal(m, rm, f"m T={T} W={W}")
     G.assert_bits_equal(l, rl, f"l T={T} W={W}")
@@ -64,10 +69,13 @@ def test_attn_fwd_large_logits_and_zero_rows(orc):
 @pytest.mark.parametrize("W", [512, 0])
 def test_attn_fwd_full_size_sampled(orc, W):
     # one micro-batch of the decoder: 4 sequences x 4096 tokens, 16 query and
-    # 4 kv heads of 128; sliding window of 512 or full causal
+    # 4 kv heads of 128; sliding window of 512 or full causal; both logit paths
     B, T, Hq, Hkv = 4, 4096, 16, 4
     q, k, vq, s_v = _case(100 + W, B, T, Hq, Hkv)
     o, m, l = gpu_attn_fwd(q, k, vq, s_v, W)
+    o2, m2, l2 = gpu_attn_fwd(q, k, vq, s_v, W, cache=False)
+    for x, y in ((o, o2), (m, m2), (l, l2)):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
     rng = np.random.default_rng(W)
     nrow = B * T * Hq
     rows = np.unique(np.concatenate([rng.integers(0, nrow, 40), [0, 1, nrow - 1],
@@ -147,7 +155,7 @@ def test_attn_at_the_maximum_length(orc):
     B, T, Hq, Hkv = 1, 131072, 1, 1
     q, k, vq, s_v = _case(131072, B, T, Hq, Hkv)
     vq[:] = 127                                  # the largest codes
-    o, m, l = gpu_attn_fwd(q, k, vq, s_v, 0)
+    o, m, l = gpu_attn_fwd(q, k, vq, s_v, 0, cache=False)   # the cache would be 34 GB
     rows = np.array([0, 1, 4095, 65536, T - 2, T - 1])
     ro, rm, rl = orc.attn_fwd_rows(q, k, vq, s_v, 0, rows)
     G.assert_bits_equal(o.reshape(-1, D)[rows], ro, "o rows")
