@@ -695,23 +695,59 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                         for (int e = 0; e < 4; ++e)
                             unpack2(pp[q2][e], part[2 * q2][e], part[2 * q2 + 1][e]);
                 } else {
-                    for (int jc = 0; jc < AT; ++jc) {
-                        const float4 s03 = *reinterpret_cast<const float4*>(St + jc * PB + grp * 8);
-                        const float4 s47 = *reinterpret_cast<const float4*>(St + jc * PB + grp * 8 + 4);
+                    // mask-edge tile: a pair of rows takes the packed step where both
+                    // rows are valid and already seeded, the scalar steps elsewhere
+                    int pb[4], pe[4], lo_all = AT, hi_all = -1;
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        pb[q2] = max(jb[2 * q2], jb[2 * q2 + 1]) + 1;
+                        pe[q2] = min(je[2 * q2], je[2 * q2 + 1]);
+                        lo_all = min(lo_all, min(jb[2 * q2], jb[2 * q2 + 1]));
+                        hi_all = max(hi_all, max(je[2 * q2], je[2 * q2 + 1]));
+                    }
+                    u64 pp[4][4];
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            pp[q2][e] = 0ull;
+                    for (int jc = lo_all; jc <= hi_all; ++jc) {
+                        const ulonglong2 s03 = *reinterpret_cast<const ulonglong2*>(St + jc * PB + grp * 8);
+                        const ulonglong2 s47 = *reinterpret_cast<const ulonglong2*>(St + jc * PB + grp * 8 + 4);
                         const float4 kv = *reinterpret_cast<const float4*>(Ks + jc * PR + 4 * dg);
-                        const float sd[8] = {s03.x, s03.y, s03.z, s03.w, s47.x, s47.y, s47.z, s47.w};
+                        const u64 P[4] = {s03.x, s03.y, s47.x, s47.y};
                         const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            if (jc < jb[r] || jc > je[r])
-                                continue;
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            if (jc >= pb[q2] && jc <= pe[q2]) {
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float t = fmul_rn(sd[r], kk[e]);
-                                part[r][e] = jc == jb[r] ? flush(t) : fadd_ftz(part[r][e], t);
+                                for (int e = 0; e < 4; ++e)
+                                    pp[q2][e] = fadd2_ftz(pp[q2][e], fmul2_rn(P[q2], pack2(kk[e], kk[e])));
+                            } else {
+                                float sa, sb;
+                                unpack2(P[q2], sa, sb);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    float la, lb;
+                                    unpack2(pp[q2][e], la, lb);
+                                    if (jc >= jb[2 * q2] && jc <= je[2 * q2]) {
+                                        const float t = fmul_rn(sa, kk[e]);
+                                        la = jc == jb[2 * q2] ? flush(t) : fadd_ftz(la, t);
+                                    }
+                                    if (jc >= jb[2 * q2 + 1] && jc <= je[2 * q2 + 1]) {
+                                        const float t = fmul_rn(sb, kk[e]);
+                                        lb = jc == jb[2 * q2 + 1] ? flush(t) : fadd_ftz(lb, t);
+                                    }
+                                    pp[q2][e] = pack2(la, lb);
+                                }
                             }
                         }
                     }
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            unpack2(pp[q2][e], part[2 * q2][e], part[2 * q2 + 1][e]);
                 }
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
@@ -774,23 +810,59 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                             for (int e = 0; e < 4; ++e)
                                 unpack2(pp[q2][e], pt[2 * q2][e], pt[2 * q2 + 1][e]);
                     } else {
-                        for (int ir = 0; ir < AT; ++ir) {
-                            const float4 w03 = *reinterpret_cast<const float4*>(Wt + ir * PB + grp * 8);
-                            const float4 w47 = *reinterpret_cast<const float4*>(Wt + ir * PB + grp * 8 + 4);
+                        // mask-edge tile: a pair of keys takes the packed step where
+                        // both keys are valid and already seeded, scalar steps elsewhere
+                        int pb[4], pe[4], lo_all = AT, hi_all = -1;
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            pb[q2] = max(ib[2 * q2], ib[2 * q2 + 1]) + 1;
+                            pe[q2] = min(ie[2 * q2], ie[2 * q2 + 1]);
+                            lo_all = min(lo_all, min(ib[2 * q2], ib[2 * q2 + 1]));
+                            hi_all = max(hi_all, max(ie[2 * q2], ie[2 * q2 + 1]));
+                        }
+                        u64 pp[4][4];
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                pp[q2][e] = 0ull;
+                        for (int ir = lo_all; ir <= hi_all; ++ir) {
+                            const ulonglong2 w03 = *reinterpret_cast<const ulonglong2*>(Wt + ir * PB + grp * 8);
+                            const ulonglong2 w47 = *reinterpret_cast<const ulonglong2*>(Wt + ir * PB + grp * 8 + 4);
                             const float4 xv = *reinterpret_cast<const float4*>(Xr + ir * PR + 4 * dg);
-                            const float w8[8] = {w03.x, w03.y, w03.z, w03.w, w47.x, w47.y, w47.z, w47.w};
+                            const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
                             const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                            for (int r = 0; r < 8; ++r) {
-                                if (ir < ib[r] || ir > ie[r])
-                                    continue;
+                            for (int q2 = 0; q2 < 4; ++q2) {
+                                if (ir >= pb[q2] && ir <= pe[q2]) {
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float t = fmul_rn(w8[r], xx[e]);
-                                    pt[r][e] = ir == ib[r] ? flush(t) : fadd_ftz(pt[r][e], t);
+                                    for (int e = 0; e < 4; ++e)
+                                        pp[q2][e] = fadd2_ftz(pp[q2][e], fmul2_rn(P[q2], pack2(xx[e], xx[e])));
+                                } else {
+                                    float wa, wb;
+                                    unpack2(P[q2], wa, wb);
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        float la, lb;
+                                        unpack2(pp[q2][e], la, lb);
+                                        if (ir >= ib[2 * q2] && ir <= ie[2 * q2]) {
+                                            const float t = fmul_rn(wa, xx[e]);
+                                            la = ir == ib[2 * q2] ? flush(t) : fadd_ftz(la, t);
+                                        }
+                                        if (ir >= ib[2 * q2 + 1] && ir <= ie[2 * q2 + 1]) {
+                                            const float t = fmul_rn(wb, xx[e]);
+                                            lb = ir == ib[2 * q2 + 1] ? flush(t) : fadd_ftz(lb, t);
+                                        }
+                                        pp[q2][e] = pack2(la, lb);
+                                    }
                                 }
                             }
                         }
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                unpack2(pp[q2][e], pt[2 * q2][e], pt[2 * q2 + 1][e]);
                     }
                     // fold (keys and their ranges are the same for every lane of a warp)
                     float f[32];
