@@ -556,7 +556,7 @@ def run_attn(args, aw):
             end("attn_fwd")
             ev("attn_bwd")
         R.repro_attn_bwd(tq, tk, vq, s_v, o, tdo, m, l, dq, dk, dv, aw.window, ws=ws_b,
-                         stream=stream)
+                         fwd_ws=ws_f, stream=stream)
         if timed:
             end("attn_bwd")
 
@@ -625,9 +625,10 @@ def run_attn(args, aw):
         fp32_peak = sms * 128 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         pairs = attn_pairs(aw)
         # algorithmic FP32 work per valid (query, key) pair: the logits once in
-        # the forward (2 * 128), and in the backward the logits, dA, dQ, dK
-        # and dV dot products (5 * 2 * 128); P.V is integer work (dp4a)
-        fwd_ops, bwd_ops = 2 * D * pairs, 10 * D * pairs
+        # the forward (2 * 128), and in the backward the dA, dQ, dK and dV dot
+        # products (4 * 2 * 128) -- the backward reads the forward's logits from
+        # its cache instead of recomputing them; P.V is integer work (dp4a)
+        fwd_ops, bwd_ops = 2 * D * pairs, 8 * D * pairs
         f_ms, b_ms = per_class.get("attn_fwd", 0.0), per_class.get("attn_bwd", 0.0)
         ach = (fwd_ops + bwd_ops) * args.steps / ((f_ms + b_ms) / 1e3) / 1e12
         roofline = {

@@ -547,7 +547,8 @@ size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq)
 int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                    const float* o, const float* dout, const float* m, const float* l, float* dq,
                    float* dk, float* dv, int64_t B, int64_t T, int64_t Hq, int64_t Hkv, int64_t D,
-                   int64_t W, void* ws, size_t ws_bytes, void* stream)
+                   int64_t W, void* ws, size_t ws_bytes, const void* fwd_ws, size_t fwd_ws_bytes,
+                   void* stream)
 {
     if (B < 0 || T < 0 || Hq < 1 || Hkv < 1 || W < 0)
         return REPRO_ERR_SHAPE;
@@ -586,11 +587,23 @@ int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float
     for (int x = 0; x < 3; ++x)
         if (overlap(ws, need, outs[x], outsz[x]))
             return REPRO_ERR_ALIAS;
+    if (fwd_ws) {
+        const size_t fneed = attn_fwd_ws_bytes(B, T, Hq, W);
+        if (fwd_ws_bytes < fneed)
+            return REPRO_ERR_WORKSPACE;
+        if (!al16(fwd_ws))
+            return REPRO_ERR_ALIGN;
+        if (overlap(fwd_ws, fneed, ws, need))
+            return REPRO_ERR_ALIAS;
+        for (int x = 0; x < 3; ++x)
+            if (overlap(fwd_ws, fneed, outs[x], outsz[x]))
+                return REPRO_ERR_ALIAS;
+    }
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
     return status_of(launch_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, B, T, Hq, Hkv, W,
-                                     ws, as_stream(stream)));
+                                     ws, fwd_ws, as_stream(stream)));
 }
 
 size_t repro_state_hash_ws_bytes(const int64_t* nbytes, int nbuf)

@@ -84,7 +84,8 @@ size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq);
 cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                             const float* o, const float* dout, const float* m, const float* l,
                             float* dq, float* dk, float* dv, int64_t B, int64_t T, int64_t Hq,
-                            int64_t Hkv, int64_t W, void* ws, cudaStream_t st);
+                            int64_t Hkv, int64_t W, void* ws, const void* lcache,
+                            cudaStream_t st);
 
 // ---- state hash (k_hash.cu)
 int64_t hash_leaf_count(const int64_t* nbytes, int nbuf, int64_t leaf_bytes);

@@ -441,7 +441,9 @@ struct AttnBwdArgs {
     unsigned long long* dq_acc;
     float* dk;
     float* dv;
+    const float* lcache;   // optional: the forward's logit cache for these inputs
     int64_t T, Hq, Hkv, W;
+    int64_t tiles_bh;
     float c;
 };
 
@@ -627,7 +629,25 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
             // a and dS for the 64 x 64 pairs (query row ty+16r, key tx+16cc)
             {
                 float sv[4][4], dav[4][4];
-                tile_dot(sv, Qs, Ks, ty, tx);
+                if (a.lcache) {
+                    // the forward's logits of this (query tile, key tile): forward
+                    // thread f = (i/4)*16 + j/4 holds pair (2*((i%4)/2) + ..) -- float
+                    // f*16 + 2*(((i%4)/2)*4 + j%4) + i%2, already scaled by c
+                    const int64_t qt = i0 / AT;
+                    const int64_t tlo = (W > 0 ? max((int64_t)0, i0 - W + 1) : (int64_t)0) / AT;
+                    const float* tile = a.lcache + ((b * Hq + h) * a.tiles_bh + tile_prefix(qt, W) +
+                                                    (j0 / AT - tlo)) * (AT * AT);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int cc = 0; cc < 4; ++cc) {
+                            const int ir = ty + 16 * r, jc = tx + 16 * cc;
+                            const int f = (ir >> 2) * 16 + (jc >> 2);
+                            sv[r][cc] = tile[f * 16 + 2 * (((ir & 3) >> 1) * 4 + (jc & 3)) + (ir & 1)];
+                        }
+                } else {
+                    tile_dot(sv, Qs, Ks, ty, tx);
+                }
                 tile_dot(dav, Gs, Vs, ty, tx);
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -639,7 +659,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                         const int64_t j = j0 + jc;
                         float av = 0.f, dsv = 0.f;
                         if (i < T && j <= i && (W == 0 || i - j < W)) {
-                            const float s = fmul_flush(sv[r][cc], c);
+                            const float s = a.lcache ? sv[r][cc] : fmul_flush(sv[r][cc], c);
                             const float p = exp_r(fadd_ftz(s, -rm[ir]));
                             av = flush(__fdiv_rn(p, rl[ir]));
                             dsv = fmul_flush(av, fadd_ftz(dav[r][cc], -rd[ir]));
@@ -969,7 +989,8 @@ size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq)
 cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                             const float* o, const float* dout, const float* m, const float* l,
                             float* dq, float* dk, float* dv, int64_t B, int64_t T, int64_t Hq,
-                            int64_t Hkv, int64_t W, void* ws, cudaStream_t st)
+                            int64_t Hkv, int64_t W, void* ws, const void* lcache,
+                            cudaStream_t st)
 {
     const int64_t rows = B * T * Hq;
     unsigned long long* acc = static_cast<unsigned long long*>(ws);
@@ -992,10 +1013,12 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
     a.dq_acc = acc;
     a.dk = dk;
     a.dv = dv;
+    a.lcache = static_cast<const float*>(lcache);
     a.T = T;
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.W = W;
+    a.tiles_bh = tile_prefix((T + AT - 1) / AT, W);
     a.c = c;
     e = cudaFuncSetAttribute(k_attn_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BWD_SMEM);
     if (e != cudaSuccess)

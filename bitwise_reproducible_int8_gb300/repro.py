@@ -75,7 +75,7 @@ _SIGNATURES = {
                               _i64, _vp, _sz, _vp]),
     "repro_attn_fwd_ws_bytes": (_sz, [_i64, _i64, _i64, _i64]),
     "repro_attn_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
-                              _i64, _i64, _i64, _i64, _vp, _sz, _vp]),
+                              _i64, _i64, _i64, _i64, _vp, _sz, _vp, _sz, _vp]),
     "repro_attn_bwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
     "repro_status_str": (ctypes.c_char_p, [_int]),
     "repro_version": (_int, []),
@@ -281,9 +281,10 @@ def repro_attn_bwd_ws_bytes(B: int, T: int, Hq: int) -> int:
 
 
 def repro_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, W: int = 0, ws=None,
-                   stream=None) -> None:
+                   fwd_ws=None, stream=None) -> None:
     """dq [B,T,Hq,128], dk and dv [B,T,Hkv,128] from the forward's inputs,
-    output o, row statistics m, l and the upstream gradient dout."""
+    output o, row statistics m, l and the upstream gradient dout.  fwd_ws:
+    optionally the logit cache repro_attn_fwd filled for these inputs."""
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
     if ws is None:
@@ -293,7 +294,8 @@ def repro_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, W: int = 0, ws=None
         _ptr(q, f32, "q"), _ptr(k, f32, "k"), _ptr(vq, torch.int8, "vq"), _ptr(s_v, f32, "s_v"),
         _ptr(o, f32, "o"), _ptr(dout, f32, "dout"), _ptr(m, f32, "m"), _ptr(l, f32, "l"),
         _ptr(dq, f32, "dq"), _ptr(dk, f32, "dk"), _ptr(dv, f32, "dv"), B, T, Hq, Hkv, D, int(W),
-        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(fwd_ws, None, "fwd_ws"),
+        fwd_ws.numel() * fwd_ws.element_size() if fwd_ws is not None else 0, _stream(stream)))
 
 
 REPRO_HASH_LEAF_BYTES = 4096

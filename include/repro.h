@@ -281,12 +281,15 @@ size_t repro_attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);
  * m, l; outputs dq [B][T][Hq][128], dk, dv [B][T][Hkv][128] (DEVICE, 16-byte
  * aligned, no overlaps).  ws: repro_attn_bwd_ws_bytes(B, T, Hq) bytes (the
  * int64 dQ accumulator and the Dr_i), not overlapping anything else.
+ * fwd_ws (optional): the logit cache repro_attn_fwd filled for these same
+ * inputs, unchanged since; the backward then reads s_ij from it instead of
+ * recomputing them (same bits).  NULL recomputes.
  * ------------------------------------------------------------------------ */
 int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                    const float* o, const float* dout, const float* m, const float* l,
                    float* dq, float* dk, float* dv, int64_t B, int64_t T, int64_t Hq,
                    int64_t Hkv, int64_t D, int64_t W, void* ws, size_t ws_bytes,
-                   void* stream);
+                   const void* fwd_ws, size_t fwd_ws_bytes, void* stream);
 size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq);
 
 /* ------------------------------------------------------------------------

@@ -267,7 +267,8 @@ def test_attn_bwd_argument_checks(L):
         v = dict(base, **{k: kw[k] for k in kw if k in base})
         return [v[n] for n in names] + [kw.get("B", 1), kw.get("T", 8), kw.get("Hq", 4),
                                         kw.get("Hkv", 2), kw.get("D", 128), kw.get("W", 0),
-                                        kw.get("ws", W_), kw.get("wsb", 1 << 24), None]
+                                        kw.get("ws", W_), kw.get("wsb", 1 << 24),
+                                        kw.get("fws", None), kw.get("fwsb", 0), None]
     assert f(*args(D=96)) == -2
     assert f(*args(Hkv=3)) == -2
     assert f(*args(dq=None)) == -1
@@ -279,4 +280,6 @@ def test_attn_bwd_argument_checks(L):
     assert f(*args(ws=A)) == -8                           # ws over q
     assert f(*args(B=0)) == 0
     assert f(*args()) in (-4, -5)
+    assert f(*args(fws=A * 64, fwsb=16)) == -7            # logit cache too small
+    assert f(*args(fws=W_, fwsb=1 << 20)) == -8           # logit cache over ws
     assert repro.repro_attn_bwd_ws_bytes(1, 8, 4) == 8 * 4 * 128 * 8 + 8 * 4 * 4

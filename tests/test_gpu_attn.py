@@ -23,7 +23,7 @@ def _case(seed, B, T, Hq, Hkv):
     return q, k, vq, s_v
 
 
-def gpu_attn_fwd(q, k, vq, s_v, W, cache=True):
+def gpu_attn_fwd(q, k, vq, s_v, W, cache=True, keep_cache=False):
     B, T, Hq, _ = q.shape
     o = torch.empty((B, T, Hq, D), device="cuda")
     m = torch.empty((B, T, Hq), device="cuda")
@@ -35,6 +35,8 @@ def gpu_attn_fwd(q, k, vq, s_v, W, cache=True):
     R.repro_attn_fwd(G.dev(q), G.dev(k), G.dev(vq), G.scalar(s_v), o, m, l, W, ws=ws)
     torch.cuda.synchronize()
     assert R.repro_device_check() == 0
+    if keep_cache:
+        return G.host(o), G.host(m), G.host(l), ws
     return G.host(o), G.host(m), G.host(l)
 
 
@@ -95,26 +97,31 @@ def test_attn_fwd_repeatable():
         assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
 
 
-def gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W):
+def gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=None):
     B, T, Hq, _ = q.shape
     Hkv = k.shape[2]
     dq = torch.empty((B, T, Hq, D), device="cuda")
     dk = torch.empty((B, T, Hkv, D), device="cuda")
     dv = torch.empty((B, T, Hkv, D), device="cuda")
     R.repro_attn_bwd(G.dev(q), G.dev(k), G.dev(vq), G.scalar(s_v), G.dev(o), G.dev(dout),
-                     G.dev(m), G.dev(l), dq, dk, dv, W)
+                     G.dev(m), G.dev(l), dq, dk, dv, W, fwd_ws=fwd_ws)
     torch.cuda.synchronize()
     assert R.repro_device_check() == 0
     return G.host(dq), G.host(dk), G.host(dv)
 
 
+@pytest.mark.parametrize("logits", ["recomputed", "cached"])
 @pytest.mark.parametrize("W", [0, 1, 7, 64, 100])
 @pytest.mark.parametrize("B,T,Hq,Hkv", SHAPES)
-def test_attn_bwd_matches_oracle(orc, B, T, Hq, Hkv, W):
+def test_attn_bwd_matches_oracle(orc, B, T, Hq, Hkv, W, logits):
     q, k, vq, s_v = _case(B * 1000 + T * 10 + W + 7, B, T, Hq, Hkv)
-    o, m, l = orc.attn_fwd(q, k, vq, s_v, W)
+    fwd_ws = None
+    if logits == "cached":
+        o, m, l, fwd_ws = gpu_attn_fwd(q, k, vq, s_v, W, keep_cache=True)
+    else:
+        o, m, l = orc.attn_fwd(q, k, vq, s_v, W)
     dout = (np.random.default_rng(T + W).standard_normal(o.shape) * 1e-3).astype(np.float32)
-    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=fwd_ws)
     rq, rk, rv = orc.attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
     G.assert_bits_equal(dv, rv, f"dv T={T} W={W}")
     G.assert_bits_equal(dk, rk, f"dk T={T} W={W}")
@@ -125,9 +132,12 @@ def test_attn_bwd_matches_oracle(orc, B, T, Hq, Hkv, W):
 def test_attn_bwd_full_size_sampled(orc, W):
     B, T, Hq, Hkv = 4, 4096, 16, 4
     q, k, vq, s_v = _case(200 + W, B, T, Hq, Hkv)
-    o, m, l = gpu_attn_fwd(q, k, vq, s_v, W)          # forward parity is tested above
+    o, m, l, fws = gpu_attn_fwd(q, k, vq, s_v, W, keep_cache=True)   # forward parity: above
     dout = (np.random.default_rng(W + 1).standard_normal(o.shape) * 1e-3).astype(np.float32)
-    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=fws)
+    dq2, dk2, dv2 = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    for x, y in ((dq, dq2), (dk, dk2), (dv, dv2)):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
     rng = np.random.default_rng(W + 2)
     qrows = np.unique(np.concatenate([rng.integers(0, B * T * Hq, 24), [0, B * T * Hq - 1,
                                       (2 * T + 700) * Hq + 5]]))
