@@ -139,6 +139,7 @@ const char* repro_status_str(int s)
     case REPRO_ERR_TIMEOUT: return "a bounded device-side wait gave up";
     case REPRO_ERR_WORKSPACE: return "workspace missing or too small";
     case REPRO_ERR_ALIAS: return "buffers that must not overlap do";
+    case REPRO_ERR_SELFTEST: return "the tensor-core forward differs from the exact CUDA-core forward";
     default: return "unknown status";
     }
 }
@@ -169,6 +170,26 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
     g_cfg.elementwise_blocks = cfg->elementwise_blocks < 0 ? 0 : cfg->elementwise_blocks;
     g_cfg.bwd_kernel = cfg->bwd_kernel < 0 ? kDefaultBwdKernel : cfg->bwd_kernel;
     return REPRO_OK;
+}
+
+size_t repro_selftest_ws_bytes(void)
+{
+    return selftest_ws_bytes();
+}
+
+int repro_selftest(void* ws, size_t ws_bytes, void* stream)
+{
+    if (!ws || ws_bytes < selftest_ws_bytes())
+        return REPRO_ERR_WORKSPACE;
+    if (!al16(ws))
+        return REPRO_ERR_ALIGN;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    const int r = run_selftest(ws, as_stream(stream));
+    if (r < 0)
+        return REPRO_ERR_LAUNCH;
+    return r == 0 ? REPRO_OK : REPRO_ERR_SELFTEST;
 }
 
 int repro_device_check(void* stream)

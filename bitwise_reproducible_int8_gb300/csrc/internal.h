@@ -87,6 +87,10 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
                             int64_t Hkv, int64_t W, void* ws, const void* lcache,
                             cudaStream_t st);
 
+// ---- forward exactness self-test (k_selftest.cu)
+size_t selftest_ws_bytes();
+int run_selftest(void* ws, cudaStream_t st);
+
 // ---- state hash (k_hash.cu)
 int64_t hash_leaf_count(const int64_t* nbytes, int nbuf, int64_t leaf_bytes);
 size_t hash_ws_bytes(int64_t nleaves);

@@ -77,6 +77,8 @@ _SIGNATURES = {
     "repro_attn_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
                               _i64, _i64, _i64, _i64, _vp, _sz, _vp, _sz, _vp]),
     "repro_attn_bwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
+    "repro_selftest": (_int, [_vp, _sz, _vp]),
+    "repro_selftest_ws_bytes": (_sz, []),
     "repro_status_str": (ctypes.c_char_p, [_int]),
     "repro_version": (_int, []),
     "repro_device_check": (_int, [_vp]),
@@ -296,6 +298,14 @@ def repro_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, W: int = 0, ws=None
         _ptr(dq, f32, "dq"), _ptr(dk, f32, "dk"), _ptr(dv, f32, "dv"), B, T, Hq, Hkv, D, int(W),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(fwd_ws, None, "fwd_ws"),
         fwd_ws.numel() * fwd_ws.element_size() if fwd_ws is not None else 0, _stream(stream)))
+
+
+def repro_selftest(device=None, stream=None) -> int:
+    """Runs the tensor-core forward's exactness self-test; returns the status
+    (REPRO_OK when every output matches the exact CUDA-core path)."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    ws = _workspace(int(lib().repro_selftest_ws_bytes()), dev)
+    return int(lib().repro_selftest(_ptr(ws, None, "ws"), ws.numel(), _stream(stream)))
 
 
 REPRO_HASH_LEAF_BYTES = 4096

@@ -71,7 +71,8 @@ typedef enum {
     REPRO_ERR_LAUNCH = -5,    /* the CUDA runtime reported an error while enqueueing */
     REPRO_ERR_TIMEOUT = -6,   /* a bounded device-side wait gave up (repro_device_check) */
     REPRO_ERR_WORKSPACE = -7, /* workspace NULL or smaller than *_ws_bytes() */
-    REPRO_ERR_ALIAS = -8      /* two buffers that must not overlap do */
+    REPRO_ERR_ALIAS = -8,     /* two buffers that must not overlap do */
+    REPRO_ERR_SELFTEST = -9   /* repro_selftest found the tensor-core forward inexact */
 } repro_status;
 
 typedef enum {
@@ -368,6 +369,20 @@ int repro_wscale_noalloc(const float* x, int64_t n, int mode, int qmax, float* s
                          void* stream);
 
 const char* repro_status_str(int status);
+
+/* ------------------------------------------------------------------------
+ * Exactness self-test of the tensor-core forward ([use]: the int8 forward
+ * must be exact).  The forward's tensor-core path relies on fp32 accumulation
+ * over 512-term K-slices of integer products staying exact, which the
+ * hardware documentation does not state; this runs it and the CUDA-core
+ * (dp4a) path on adversarial codes (all at the clamp, alternating signs, a
+ * sign flip at the slice boundary, hashed codes; K = 1024, unit scales) and
+ * compares every output bit.  Synchronises `stream`.  ws: device workspace of
+ * repro_selftest_ws_bytes() bytes.  Returns REPRO_OK, REPRO_ERR_SELFTEST on a
+ * mismatch, or an argument / launch error.
+ * ------------------------------------------------------------------------ */
+int repro_selftest(void* ws, size_t ws_bytes, void* stream);
+size_t repro_selftest_ws_bytes(void);
 int repro_version(void);
 int repro_device_check(void* stream);
 uint64_t repro_launch_count(void);

@@ -30,7 +30,7 @@ def test_exports_every_declared_symbol(L):
 
 def test_status_strings_and_version(L):
     assert repro.repro_version() == 1
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         assert repro.repro_status_str(code) != "unknown status"
     assert repro.repro_status_str(-99) == "unknown status"
 
@@ -283,3 +283,12 @@ def test_attn_bwd_argument_checks(L):
     assert f(*args(fws=A * 64, fwsb=16)) == -7            # logit cache too small
     assert f(*args(fws=W_, fwsb=1 << 20)) == -8           # logit cache over ws
     assert repro.repro_attn_bwd_ws_bytes(1, 8, 4) == 8 * 4 * 128 * 8 + 8 * 4 * 4
+
+
+def test_selftest_arguments(L):
+    need = L.repro_selftest_ws_bytes()
+    assert need >= 128 * 1024 * 2 + 2 * 128 * 128 * 4
+    assert L.repro_selftest(None, 0, None) == -7
+    assert L.repro_selftest(A, need - 1, None) == -7
+    assert L.repro_selftest(A + 4, need, None) == -3
+    assert L.repro_selftest(A, need, None) in (-4, -5)   # valid: reaches the architecture check

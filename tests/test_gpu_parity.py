@@ -104,6 +104,11 @@ def test_forward(orc, M, N, K, path):
                         f"fwd {M}x{N}x{K}")
 
 
+def test_tensor_core_forward_selftest():
+    # adversarial codes through the tensor-core path and the exact dp4a path
+    assert R.repro_selftest() == R.REPRO_OK
+
+
 @pytest.mark.parametrize("path", [0, 1])
 def test_forward_at_the_maximum_reduction(orc, path):
     # K = 133,144 is the largest K for which |acc| <= 127 * 127 * K fits int32;
