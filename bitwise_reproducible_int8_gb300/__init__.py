@@ -13,5 +13,6 @@ from .repro import (  # noqa: F401
     repro_adamw_step, repro_attn_bwd, repro_attn_bwd_ws_bytes, repro_attn_fwd, repro_attn_fwd_ws_bytes,
     repro_quant_i8,
     repro_selftest, repro_set_launch_cfg, repro_state_hash, repro_state_hash_ws_bytes, repro_status_str,
-    repro_treefold, repro_version, repro_wscale, repro_wscale_ws_bytes, REPRO_HASH_LEAF_BYTES,
+    repro_treefold, repro_version, repro_wait_probe, repro_wscale, repro_wscale_ws_bytes,
+    REPRO_HASH_LEAF_BYTES,
 )

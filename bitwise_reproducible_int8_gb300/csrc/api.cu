@@ -192,6 +192,17 @@ int repro_selftest(void* ws, size_t ws_bytes, void* stream)
     return r == 0 ? REPRO_OK : REPRO_ERR_SELFTEST;
 }
 
+int repro_wait_probe(int arrive, void* stream)
+{
+    if (arrive != 0 && arrive != 1)
+        return REPRO_ERR_ARG;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return launch_wait_probe(arrive, as_stream(stream)) == cudaSuccess ? REPRO_OK
+                                                                       : REPRO_ERR_LAUNCH;
+}
+
 int repro_device_check(void* stream)
 {
     if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess)

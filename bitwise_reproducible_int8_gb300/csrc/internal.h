@@ -87,6 +87,9 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
                             int64_t Hkv, int64_t W, void* ws, const void* lcache,
                             cudaStream_t st);
 
+// ---- bounded-wait probe (k_bwd_tma.cu)
+cudaError_t launch_wait_probe(int arrive, cudaStream_t st);
+
 // ---- forward exactness self-test (k_selftest.cu)
 size_t selftest_ws_bytes();
 int run_selftest(void* ws, cudaStream_t st);

@@ -402,6 +402,25 @@ __global__ void __launch_bounds__(NTH, 1)
         atomicExch(a.err, 1);
 }
 
+// ---------------------------------------------------------------- wait probe
+
+// One thread waits, with the pipeline's bounded wait, on a barrier phase that
+// completes only if `arrive` is set.  Without the arrival the wait gives up
+// after WAIT_CYCLES, the error word is set exactly as a stalled pipeline sets
+// it, and the kernel returns.
+__global__ void __launch_bounds__(32) k_wait_probe(int* err, int arrive)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0)
+        return;
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (arrive)
+        mbar_arrive(&bar);
+    if (!mbar_wait(&bar, 0))
+        atomicExch(err, 1);
+}
+
 // ---------------------------------------------------------------- operand prep
 
 // out[e] = float(q[e]) (x) s, flushed; 16 codes per thread per step
@@ -552,5 +571,12 @@ cudaError_t launch_bwd_tma(const BwdArgs& a0, const int8_t* q, float* opnd, dim3
 
 template cudaError_t launch_bwd_tma<false>(const BwdArgs&, const int8_t*, float*, dim3, cudaStream_t);
 template cudaError_t launch_bwd_tma<true>(const BwdArgs&, const int8_t*, float*, dim3, cudaStream_t);
+
+cudaError_t launch_wait_probe(int arrive, cudaStream_t st)
+{
+    k_wait_probe<<<1, 32, 0, st>>>(device_error_word(), arrive);
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 } // namespace repro

@@ -82,6 +82,7 @@ _SIGNATURES = {
     "repro_status_str": (ctypes.c_char_p, [_int]),
     "repro_version": (_int, []),
     "repro_device_check": (_int, [_vp]),
+    "repro_wait_probe": (_int, [_int, _vp]),
     "repro_launch_count": (ctypes.c_uint64, []),
     "repro_set_launch_cfg": (_int, [ctypes.POINTER(LaunchCfg)]),
 }
@@ -382,6 +383,11 @@ def repro_launch_count() -> int:
 
 def repro_device_check(stream=None) -> int:
     return int(lib().repro_device_check(_stream(stream)))
+
+
+def repro_wait_probe(arrive: int, stream=None) -> int:
+    """Enqueue the bounded-wait probe; arrive=0 makes the wait run out."""
+    return int(lib().repro_wait_probe(int(arrive), _stream(stream)))
 
 
 def repro_set_launch_cfg(bwd_segment_log2: int = -1, reduce_block_log2: int = -1,

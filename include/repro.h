@@ -383,6 +383,19 @@ const char* repro_status_str(int status);
  * ------------------------------------------------------------------------ */
 int repro_selftest(void* ws, size_t ws_bytes, void* stream);
 size_t repro_selftest_ws_bytes(void);
+/* ------------------------------------------------------------------------
+ * Failure-detection hook.  Every pipeline wait in the library is bounded: a
+ * wait that is not satisfied within about two seconds at the boost clock
+ * sets the device error word, lets the kernel return, and is reported by
+ * repro_device_check() as REPRO_ERR_TIMEOUT, leaving the CUDA context usable.
+ * repro_wait_probe enqueues one thread that performs that same bounded wait
+ * on a shared-memory barrier phase which completes only when `arrive` is 1.
+ * With arrive = 0 nothing completes it, so the wait runs out (about two
+ * seconds) and the next repro_device_check() returns REPRO_ERR_TIMEOUT (and
+ * clears the word); with arrive = 1 it returns at once and sets nothing.
+ * Enqueues only.  arrive outside {0, 1} -> REPRO_ERR_ARG.
+ * ------------------------------------------------------------------------ */
+int repro_wait_probe(int arrive, void* stream);
 int repro_version(void);
 int repro_device_check(void* stream);
 uint64_t repro_launch_count(void);

@@ -292,3 +292,9 @@ def test_selftest_arguments(L):
     assert L.repro_selftest(A, need - 1, None) == -7
     assert L.repro_selftest(A + 4, need, None) == -3
     assert L.repro_selftest(A, need, None) in (-4, -5)   # valid: reaches the architecture check
+
+
+def test_wait_probe_arguments(L):
+    assert L.repro_wait_probe(2, None) == -1
+    assert L.repro_wait_probe(-1, None) == -1
+    assert L.repro_wait_probe(0, None) in (-4, -5)   # valid: reaches the architecture check
