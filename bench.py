@@ -313,7 +313,8 @@ def run_ours(args, wl):
         achieved = bwd_ops / (bwd_ms / 1000.0) / 1e12 if bwd_ms > 0 else 0.0
         nb = launch_counts.get("bwd_dx", 0) + launch_counts.get("bwd_dw", 0)
         kname = {0: "k_bwd", 1: "k_bwd2", 2: "k_bwd3", 3: "k_bwd4", 4: "k_bwd5",
-                 5: "k_bwd6", 6: "k_bwd_ws", 7: "k_bwd_tma"}[args.bwd_kernel if args.bwd_kernel >= 0 else 7]
+                 5: "k_bwd6", 6: "k_bwd_ws", 7: "k_bwd_tma",
+                 8: "k_bwd_tma<self-issue>"}[args.bwd_kernel if args.bwd_kernel >= 0 else 8]
         roofline = {
             "bound": "alu", "kernel": f"{kname} (dX and dW, canonical-order fp32)",
             "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",

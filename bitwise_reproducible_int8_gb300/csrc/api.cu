@@ -11,7 +11,7 @@ namespace repro {
 
 namespace {
 
-constexpr int kDefaultBwdKernel = 7;   // operand prep + tensor-copy-fed kernel
+constexpr int kDefaultBwdKernel = 8;   // operand prep + tensor-copy-fed kernel, self-issued copies
 LaunchCfg g_cfg = {-1, -1, -1, 0, kDefaultBwdKernel};
 
 constexpr int kMaxDevices = 64;
@@ -162,7 +162,7 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
         return REPRO_ERR_ARG;
     if (cfg->elementwise_blocks < -1 || cfg->elementwise_blocks > (1 << 20))
         return REPRO_ERR_ARG;
-    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 7)
+    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 8)
         return REPRO_ERR_ARG;
     g_cfg.bwd_segment_log2 = cfg->bwd_segment_log2;
     g_cfg.reduce_block_log2 = cfg->reduce_block_log2;

@@ -35,11 +35,12 @@ cudaError_t launch_bwd_ws(const BwdArgs& a, dim3 grid, cudaStream_t st);
 // tensor-copy-fed kernel (k_bwd_tma.cu): 128 x 64 output tile per CTA, same
 // alignment needs; prepares its operands (flushed dY, dequantised int8
 // operand) in `opnd`, a 256-byte aligned workspace region of
-// bwd_tma_operand_bytes(M, N, K) bytes
+// bwd_tma_operand_bytes(M, N, K) bytes.  self_issue: the compute warps issue
+// the copies themselves (no producer warp, three tree levels in registers)
 constexpr int BWD_TMA_ROWS = 128;
 size_t bwd_tma_operand_bytes(int64_t M, int64_t N, int64_t K);
 template <bool DW>
 cudaError_t launch_bwd_tma(const BwdArgs& a, const int8_t* q, float* opnd, dim3 grid,
-                           cudaStream_t st);
+                           bool self_issue, cudaStream_t st);
 
 } // namespace repro

@@ -1797,7 +1797,7 @@ int kernel_for(int64_t ldy, int64_t J)
 
 int tile_rows(int kernel)
 {
-    if (kernel == 7)
+    if (kernel >= 7)
         return BWD_TMA_ROWS;
     return kernel == 6 ? BWD_WS_ROWS : (kernel == 5 ? BI6 : (kernel >= 3 ? BI4 : BT));
 }
@@ -1876,11 +1876,11 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
     const bool aligned = kernel >= 2;
     if (kernel == 0) {
         k_bwd<DW><<<grid, 256, 0, st>>>(a);
-    } else if (kernel == 7 && aligned) {
+    } else if (kernel >= 7 && aligned) {
         if (!a.err || !opnd)
             return cudaErrorInvalidValue;
         dim3 gt((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BWD_TMA_ROWS), (unsigned)a.nseg);
-        cudaError_t e = launch_bwd_tma<DW>(a, q, opnd, gt, st);
+        cudaError_t e = launch_bwd_tma<DW>(a, q, opnd, gt, kernel == 8, st);
         if (e != cudaSuccess)
             return e;
     } else if (kernel == 6 && aligned) {
@@ -1954,7 +1954,7 @@ static int64_t seg_region_bytes(int64_t M, int64_t N, int64_t K, int seg_log2)
 
 static bool uses_operand_region(int64_t N, int64_t K)
 {
-    return kernel_for(N, K) == 7;
+    return kernel_for(N, K) >= 7;
 }
 
 size_t bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int seg_log2)

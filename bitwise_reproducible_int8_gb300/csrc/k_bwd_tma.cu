@@ -25,8 +25,8 @@
 //     tensor) into a 4-stage ring guarded by full/empty mbarriers;
 //   * 8 compute warps own the 128 x 64 output tile, 8 x 4 outputs per thread,
 //     packed f32x2 multiply and add, reading the ring stage in place;
-//   * tree levels 0..REGL-1 in registers, the rest in tensor memory (thread:
-//     lane 32*(warp%4) + lane, columns (warp/4)*256 + 32*(level-REGL)).
+//   * tree levels 0..RL-1 in registers, the rest in tensor memory (thread:
+//     lane 32*(warp%4) + lane, columns (warp/4)*256 + 32*(level-RL)).
 // Every wait is bounded: past the limit the CTA records a failure in the
 // device error word, lets its copies land, frees its tensor memory and exits.
 #include <cuda.h>
@@ -50,7 +50,6 @@ constexpr int B_BYTES = CH * BT * 4;           // 16384: B[r][j]
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int CTRL_OFF = STG * STAGE_BYTES;
 constexpr size_t SMEM_BYTES = 1024 + (size_t)CTRL_OFF + 128;   // + alignment slack
-constexpr int REGL = 1;                        // tree levels kept in registers
 constexpr long long WAIT_CYCLES = 4000000000LL;   // ~2 s at the boost clock
 
 __device__ __forceinline__ uint32_t su32(const void* p)
@@ -207,8 +206,14 @@ __device__ __forceinline__ void chunk_sum(u64 (&acc)[16], const float* __restric
     }
 }
 
-template <bool DW>
-__global__ void __launch_bounds__(NTH, 1)
+// SELF = false: one producer warp issues the copies, RL = 1 tree level in
+// registers (9 warps: at most 168 registers a thread).  SELF = true: no
+// producer warp; compute thread 0 refills the stage of chunk c - 2 with chunk
+// c - 2 + STG at the start of chunk c, and with 8 warps (255 registers a
+// thread) RL = 3 levels stay in registers, so tensor memory is touched once
+// every 8 chunks instead of every other chunk.
+template <bool DW, bool SELF, int RL>
+__global__ void __launch_bounds__(SELF ? NC : NTH, 1)
     k_bwd_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
               const BwdArgs a)
 {
@@ -234,6 +239,21 @@ __global__ void __launch_bounds__(NTH, 1)
     auto stA = [&](int s) { return reinterpret_cast<float*>(smt + s * STAGE_BYTES); };
     auto stB = [&](int s) { return reinterpret_cast<float*>(smt + s * STAGE_BYTES + A_BYTES); };
     auto valid_of = [&](int cs) { return (int)min((int64_t)CH, a.R - (cbeg + cs) * CH); };
+    auto issue = [&](int cs) {
+        const int s = cs % STG;
+        const int r0 = (int)((cbeg + cs) * CH);
+        mbar_expect_tx(&full[s], STAGE_BYTES);
+        tma_load_2d(stA(s), &map_a, (int)i0, r0, &full[s]);
+        tma_load_2d(stB(s), &map_b, (int)j0, r0, &full[s]);
+    };
+    // the last copy into every stage has landed (bounded); false on a timeout
+    auto drain = [&](int issued) {
+        bool fine = true;
+        for (int cs = issued - 1; cs >= 0 && cs >= issued - STG; --cs)
+            if (!mbar_wait(&full[cs % STG], (cs / STG) & 1))
+                fine = false;
+        return fine;
+    };
 
     if (tid == 0) {
         for (int s = 0; s < STG; ++s) {
@@ -256,7 +276,7 @@ __global__ void __launch_bounds__(NTH, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    if (warp == NC / 32) {
+    if (!SELF && warp == NC / 32) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             int issued = 0;
@@ -268,16 +288,12 @@ __global__ void __launch_bounds__(NTH, 1)
                 }
                 if (*(volatile int*)comp_fail)
                     break;
-                const int r0 = (int)((cbeg + cs) * CH);
-                mbar_expect_tx(&full[s], STAGE_BYTES);
-                tma_load_2d(stA(s), &map_a, (int)i0, r0, &full[s]);
-                tma_load_2d(stB(s), &map_b, (int)j0, r0, &full[s]);
+                issue(cs);
                 issued = cs + 1;
             }
             // let the last copy into every stage land before the CTA can exit
-            for (int cs = issued - 1; cs >= 0 && cs >= issued - STG; --cs)
-                if (!mbar_wait(&full[cs % STG], (cs / STG) & 1))
-                    *prod_fail = 1;
+            if (!drain(issued))
+                *prod_fail = 1;
         }
     } else {
         // -------------------------------------------------------------- compute
@@ -286,13 +302,20 @@ __global__ void __launch_bounds__(NTH, 1)
         const uint32_t tbase =
             *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 256);
 
-        u64 S[REGL][16];
+        const bool issuer = SELF && tid == 0;
+        int issued = 0;
+        if (issuer) {
+            for (; issued < n && issued < STG; ++issued)
+                issue(issued);
+        }
+
+        u64 S[RL][16];
         u64 acc[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
             acc[e] = 0ull;
 #pragma unroll
-        for (int l = 0; l < REGL; ++l)
+        for (int l = 0; l < RL; ++l)
 #pragma unroll
             for (int e = 0; e < 16; ++e)
                 S[l][e] = 0ull;
@@ -300,6 +323,19 @@ __global__ void __launch_bounds__(NTH, 1)
         bool ok = true;
         for (int cs = 0; cs < n; ++cs) {
             const int s = cs % STG;
+            if (SELF && warp == 0) {
+                // refill the stage every warp released two chunks ago
+                if (lane == 0 && issued == cs + 2 && issued < n) {
+                    const int rc = issued - STG;
+                    if (mbar_wait(&empty[rc % STG], (rc / STG) & 1)) {
+                        issue(issued);
+                        ++issued;
+                    } else {
+                        *prod_fail = 1;
+                    }
+                }
+                __syncwarp();
+            }
             const bool got = mbar_wait(&full[s], (cs / STG) & 1);
             if (__any_sync(0xffffffffu, !got)) {
                 ok = false;
@@ -320,20 +356,20 @@ __global__ void __launch_bounds__(NTH, 1)
                     if (tz == t) {
 #pragma unroll
                         for (int l = 0; l < t; ++l) {
-                            if (l < REGL) {
+                            if (l < RL) {
 #pragma unroll
                                 for (int e = 0; e < 16; ++e)
-                                    acc[e] = fadd2_ftz(S[l < REGL ? l : 0][e], acc[e]);
+                                    acc[e] = fadd2_ftz(S[l < RL ? l : 0][e], acc[e]);
                             } else {
-                                tmem_fold32(tbase + (uint32_t)(32 * (l - REGL)), acc);
+                                tmem_fold32(tbase + (uint32_t)(32 * (l - RL)), acc);
                             }
                         }
-                        if (t < REGL) {
+                        if (t < RL) {
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
-                                S[t < REGL ? t : 0][e] = acc[e];
+                                S[t < RL ? t : 0][e] = acc[e];
                         } else {
-                            tmem_st32(tbase + (uint32_t)(32 * (t - REGL)), acc);
+                            tmem_st32(tbase + (uint32_t)(32 * (t - RL)), acc);
                         }
                     }
                 }
@@ -341,17 +377,20 @@ __global__ void __launch_bounds__(NTH, 1)
 #pragma unroll
                 for (int l = 0; l < MAXLVL; ++l) {
                     if ((cs >> l) & 1) {
-                        if (l < REGL) {
+                        if (l < RL) {
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
-                                acc[e] = fadd2_ftz(S[l < REGL ? l : 0][e], acc[e]);
+                                acc[e] = fadd2_ftz(S[l < RL ? l : 0][e], acc[e]);
                         } else {
-                            tmem_fold32(tbase + (uint32_t)(32 * (l - REGL)), acc);
+                            tmem_fold32(tbase + (uint32_t)(32 * (l - RL)), acc);
                         }
                     }
                 }
             }
         }
+
+        if (issuer && !drain(issued))
+            *prod_fail = 1;
 
         if (ok) {
             // row 8ty + 2ip + h, column 4tx + j is lane h of acc[ip*4 + j]
@@ -537,7 +576,7 @@ size_t bwd_tma_operand_bytes(int64_t M, int64_t N, int64_t K)
 
 template <bool DW>
 cudaError_t launch_bwd_tma(const BwdArgs& a0, const int8_t* q, float* opnd, dim3 grid,
-                           cudaStream_t st)
+                           bool self_issue, cudaStream_t st)
 {
     BwdArgs a = a0;
     const int eb = 8 * num_sms();
@@ -561,16 +600,19 @@ cudaError_t launch_bwd_tma(const BwdArgs& a0, const int8_t* q, float* opnd, dim3
     CUtensorMap ma, mb;
     if (!make_map(&ma, Aop, a.R, a.I, lda, TI) || !make_map(&mb, Bop, a.R, a.J, a.J, BT))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_tma<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    auto kern = self_issue ? k_bwd_tma<DW, true, 3> : k_bwd_tma<DW, false, 1>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
-    k_bwd_tma<DW><<<grid, NTH, SMEM_BYTES, st>>>(ma, mb, a);
+    kern<<<grid, self_issue ? NC : NTH, SMEM_BYTES, st>>>(ma, mb, a);
     return cudaGetLastError();
 }
 
-template cudaError_t launch_bwd_tma<false>(const BwdArgs&, const int8_t*, float*, dim3, cudaStream_t);
-template cudaError_t launch_bwd_tma<true>(const BwdArgs&, const int8_t*, float*, dim3, cudaStream_t);
+template cudaError_t launch_bwd_tma<false>(const BwdArgs&, const int8_t*, float*, dim3, bool,
+                                           cudaStream_t);
+template cudaError_t launch_bwd_tma<true>(const BwdArgs&, const int8_t*, float*, dim3, bool,
+                                          cudaStream_t);
 
 cudaError_t launch_wait_probe(int arrive, cudaStream_t st)
 {

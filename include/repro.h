@@ -338,12 +338,14 @@ typedef struct {
     int reduce_block_log2;  /* -1: default; else 2^k chunk partials per block in repro_wscale (0..10) */
     int fwd_path;           /* -1: default (tensor cores when K % 8 == 0); 0: CUDA cores; 1: tensor cores */
     int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
-    int bwd_kernel;         /* -1: default (7); 0: plain; 1: register prefetch; 2: staged;
+    int bwd_kernel;         /* -1: default (8); 0: plain; 1: register prefetch; 2: staged;
                                3: staged wide tile; 4: wide tile with the tree in tensor
                                memory; 5: twelve-warp wide tile; 6: warp-specialised wide
                                tile (producer and compute warps, tree in tensor memory);
                                7: operands prepared once per call, then fed by tensor
-                               copies (2-7 need 16-byte-aligned rows, else 1) */
+                               copies from a producer warp; 8: as 7, the compute warps
+                               issue the copies and keep three tree levels in registers
+                               (2-8 need 16-byte-aligned rows, else 1) */
 } repro_launch_cfg;
 
 /* ------------------------------------------------------------------------

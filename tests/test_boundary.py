@@ -129,6 +129,8 @@ def test_bwd_workspace_follows_segments(L):
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == opnd
         repro.repro_set_launch_cfg(bwd_segment_log2=4, bwd_kernel=7)
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 16 * 2048 * 2048 * 4 + opnd
+        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=8)   # same region
+        assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == opnd
         # rows that are not 16-byte aligned take the register-prefetch kernel: no operand region
         repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=7)
         assert repro.repro_linear_bwd_ws_bytes(64, 30, 20) == 0
@@ -161,6 +163,9 @@ def test_launch_cfg_validation(L):
             repro.repro_set_launch_cfg(reduce_block_log2=11)
         with pytest.raises(repro.ReproError):
             repro.repro_set_launch_cfg(fwd_path=2)
+        with pytest.raises(repro.ReproError):
+            repro.repro_set_launch_cfg(bwd_kernel=9)
+        repro.repro_set_launch_cfg(bwd_kernel=8)
         repro.repro_set_launch_cfg(bwd_segment_log2=0, reduce_block_log2=0, fwd_path=0,
                                    elementwise_blocks=152)
     finally:

@@ -151,7 +151,7 @@ BWD_SHAPES = [(1, 1, 1), (3, 1, 5), (64, 128, 256), (200, 130, 70), (257, 64, 65
               (257, 68, 96), (100, 4100, 32), (1000, 300, 16), (70, 132, 48), (300, 260, 80)]
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("M,N,K", BWD_SHAPES)
 def test_backward(orc, M, N, K, kernel):
     R.repro_set_launch_cfg(bwd_kernel=kernel)
@@ -165,7 +165,7 @@ def test_backward(orc, M, N, K, kernel):
     G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, s_x), f"dw {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("seg", [0, 1, 2, 3, 4, 8])
 def test_backward_launch_invariance(orc, seg, kernel):
     # long reductions split into aligned segments of 2^seg chunks, by either kernel
