@@ -212,6 +212,31 @@ __device__ __forceinline__ void chunk_sum(u64 (&acc)[16], const float* __restric
 // c - 2 + STG at the start of chunk c, and with 8 warps (255 registers a
 // thread) RL = 3 levels stay in registers, so tensor memory is touched once
 // every 8 chunks instead of every other chunk.
+// rows 0 .. CH-2 of a full chunk with row 0 already in (a03, a47, b); on
+// return (a03, a47, b) hold row CH-1, loaded but not yet multiplied
+__device__ __forceinline__ void chunk_head(u64 (&acc)[16], const float* __restrict__ Ar,
+                                           const float* __restrict__ Br, ulonglong2& a03,
+                                           ulonglong2& a47, float4& b)
+{
+    {
+        const ulonglong2 c03 = a03, c47 = a47;
+        const float4 cb = b;
+        a03 = *reinterpret_cast<const ulonglong2*>(Ar + TI);
+        a47 = *reinterpret_cast<const ulonglong2*>(Ar + TI + 4);
+        b = *reinterpret_cast<const float4*>(Br + BT);
+        step<true>(acc, c03, c47, cb);
+    }
+#pragma unroll 31
+    for (int r = 1; r < CH - 1; ++r) {
+        const ulonglong2 c03 = a03, c47 = a47;
+        const float4 cb = b;
+        a03 = *reinterpret_cast<const ulonglong2*>(Ar + (r + 1) * TI);
+        a47 = *reinterpret_cast<const ulonglong2*>(Ar + (r + 1) * TI + 4);
+        b = *reinterpret_cast<const float4*>(Br + (r + 1) * BT);
+        step<false>(acc, c03, c47, cb);
+    }
+}
+
 template <bool DW, bool SELF, int RL>
 __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
     k_bwd_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -321,7 +346,30 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
                 S[l][e] = 0ull;
 
         bool ok = true;
-        for (int cs = 0; cs < n; ++cs) {
+        // SELF: the next chunk's full wait and its row-0 loads are made before
+        // the current chunk's last row is multiplied, so they overlap it
+        ulonglong2 n03 = {0ull, 0ull}, n47 = {0ull, 0ull};
+        float4 nb = make_float4(0.f, 0.f, 0.f, 0.f);
+        auto wait_full = [&](int c) {
+            const bool got = mbar_wait(&full[c % STG], (c / STG) & 1);
+            return !__any_sync(0xffffffffu, !got);
+        };
+        auto load_row0 = [&](int c) {
+            const float* Ar = stA(c % STG) + 8 * ty;
+            n03 = *reinterpret_cast<const ulonglong2*>(Ar);
+            n47 = *reinterpret_cast<const ulonglong2*>(Ar + 4);
+            nb = *reinterpret_cast<const float4*>(stB(c % STG) + 4 * tx);
+        };
+        if (SELF && n > 0) {
+            if (wait_full(0)) {
+                load_row0(0);
+            } else {
+                ok = false;
+                if (lane == 0)
+                    *comp_fail = 1;
+            }
+        }
+        for (int cs = 0; ok && cs < n; ++cs) {
             const int s = cs % STG;
             if (SELF && warp == 0) {
                 // refill the stage every warp released two chunks ago
@@ -336,17 +384,41 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
                 }
                 __syncwarp();
             }
-            const bool got = mbar_wait(&full[s], (cs / STG) & 1);
-            if (__any_sync(0xffffffffu, !got)) {
-                ok = false;
+            const int valid = valid_of(cs);
+            if (SELF && valid == CH) {
+                chunk_head(acc, stA(s) + 8 * ty, stB(s) + 4 * tx, n03, n47, nb);
+                const ulonglong2 l03 = n03, l47 = n47;
+                const float4 lb = nb;
+                bool next_ok = true;
+                if (cs + 1 < n) {
+                    next_ok = wait_full(cs + 1);
+                    if (next_ok)
+                        load_row0(cs + 1);
+                }
+                __syncwarp();   // every lane's reads of stage s precede lane 0's release
                 if (lane == 0)
-                    *comp_fail = 1;
-                break;
+                    mbar_arrive(&empty[s]);
+                step<false>(acc, l03, l47, lb);
+                if (!next_ok) {
+                    ok = false;
+                    if (lane == 0)
+                        *comp_fail = 1;
+                    break;
+                }
+            } else {
+                // SELF: only the reduction's last chunk is partial, and its
+                // full wait was made at the end of the chunk before
+                if (!SELF && !wait_full(cs)) {
+                    ok = false;
+                    if (lane == 0)
+                        *comp_fail = 1;
+                    break;
+                }
+                chunk_sum(acc, stA(s) + 8 * ty, stB(s) + 4 * tx, valid);
+                __syncwarp();   // every lane's reads of stage s precede lane 0's release
+                if (lane == 0)
+                    mbar_arrive(&empty[s]);
             }
-            chunk_sum(acc, stA(s) + 8 * ty, stB(s) + 4 * tx, valid_of(cs));
-            __syncwarp();   // every lane's reads of stage s precede lane 0's release
-            if (lane == 0)
-                mbar_arrive(&empty[s]);
 
             // tree over chunk partials (cs counted from the segment start)
             if (cs + 1 < n) {
