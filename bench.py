@@ -40,7 +40,8 @@ METRIC = "tokens/s bit-exact int8-QAT linear fwd+bwd (1 GB300); % of int8/FP32/H
 # launches of the block workload's 4 captured steps, from one ncu capture of
 # dram__bytes_read.sum + dram__bytes_write.sum (single pass) on a GB300.  Valid only
 # for that kernel and workload; anything else reports null.
-BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd4"): 544.7e6, ("block", "k_bwd_tma"): 1660.5e6}
+BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd4"): 544.7e6, ("block", "k_bwd_tma"): 1660.5e6,
+                          ("block", "k_bwd_tma<self-issue>"): 1655.5e6}
 UNIT = "tokens/s"
 
 
@@ -266,6 +267,15 @@ def run_ours(args, wl):
     stream.synchronize()
     if R.repro_device_check(stream) != 0:
         raise RuntimeError("device error during warm-up")
+    graph, graph_launches = None, 0
+    if args.graph:
+        # the step captured once into a CUDA graph, replayed per step
+        l0 = R.repro_launch_count()
+        graph = hp.capture(stream)
+        graph_launches = R.repro_launch_count() - l0
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
 
     # ---- device-timed region: K steps, inputs resident in HBM
     timers = {}
@@ -281,10 +291,15 @@ def run_ours(args, wl):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for _ in range(args.steps):
-            hp.run(stream, timers=timers)
+            if graph is not None:
+                graph.replay()
+            else:
+                hp.run(stream, timers=timers)
         t_end.record(stream)
     stream.synchronize()
     launches = R.repro_launch_count() - launches0
+    if graph is not None:
+        launches = graph_launches * args.steps
     clk = clocks.stop()
     torch.cuda.synchronize()
     if world > 1:
@@ -292,6 +307,13 @@ def run_ours(args, wl):
     ms = t_start.elapsed_time(t_end)
     if R.repro_device_check(stream) != 0:
         raise RuntimeError("device error during the timed steps")
+    if graph is not None:
+        # graph replays carry no per-call events: split the step by call from
+        # the same number of eager steps, timed call by call
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                hp.run(stream, timers=timers)
+        stream.synchronize()
     per_class = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in timers.items()}
     launch_counts = {k: len(v) for k, v in timers.items()}
 
@@ -354,8 +376,12 @@ def run_ours(args, wl):
                        "parallelism": "replicas only",
                        "accumulation": "unfused repro_grad_accum" if args.unfused_accum
                        else "fused into the dW epilogue",
-                       "l2": f"inputs larger than L2: {resident_gb(hp):.1f} GB resident, "
-                             "streamed once per step"},
+                       "l2": (f"inputs larger than L2: {resident_gb(hp):.1f} GB resident, "
+                              "streamed once per step") if resident_gb(hp) > 0.129 else
+                             (f"inputs fit in L2 ({resident_gb(hp) * 1e3:.1f} MB resident): a "
+                              "launch-latency case, L2 not flushed"),
+                       "launch": "one CUDA graph replay per step" if graph is not None
+                       else "eager calls"},
             "roofline": roofline, "other_kernels": other,
             "ms_per_step_by_call": {k: v / args.steps for k, v in per_class.items()},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
@@ -528,6 +554,7 @@ def run_attn(args, aw):
     ws_b = torch.empty(R.repro_attn_bwd_ws_bytes(B, T, Hq), dtype=torch.uint8, device=dev)
     ws_f = torch.empty(max(R.repro_attn_fwd_ws_bytes(B, T, Hq, aw.window), 16), dtype=torch.uint8,
                        device=dev)   # the forward's logit cache
+    torch.cuda.synchronize()   # s_v's fill ran on the default stream
     stream = torch.cuda.Stream()
     timers = {}
 
@@ -715,6 +742,9 @@ def main(argv=None):
     ap.add_argument("--unfused-accum", action="store_true",
                     help="accumulate dW with repro_grad_accum instead of the fused epilogue")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture one step into a CUDA graph and time its replays "
+                         "(launch-bound workloads; not with the optimizer)")
     ap.add_argument("--bwd-kernel", type=int, default=-1,
                     help="backward kernel variant (launch-configuration hook; -1: default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -126,6 +126,8 @@ class HotPathStep:
             self.digest = torch.zeros(32, dtype=torch.uint8, device=dev)
             self.ws_hash = torch.empty(max(R.repro_state_hash_ws_bytes(self.state), 16),
                                        dtype=torch.uint8, device=dev)
+        # the zero fills above ran on the current stream; steps may run on another
+        torch.cuda.synchronize(dev)
 
     # ------------------------------------------------------------------ step
 
@@ -219,6 +221,22 @@ class HotPathStep:
             self._ev(timers, "state_hash", s)
             R.repro_state_hash(self.state, self.digest, ws=self.ws_hash, stream=s)
             self._end(timers, "state_hash", s)
+
+    def capture(self, stream: torch.cuda.Stream) -> "torch.cuda.CUDAGraph":
+        """Capture one step into a CUDA graph.  Every call only enqueues on the
+        caller's stream, allocates nothing and never synchronises, so the whole
+        step captures; replaying the graph repeats its launches with one host
+        call.  Run `prepare()` (replicated workloads) and a warm-up step first.
+        A step with AdamW cannot be captured: the step count t is a host
+        argument of repro_adamw_step and would be frozen in the graph."""
+        if self.use_optimizer:
+            raise RuntimeError("a step with the optimizer cannot be captured: t is a host argument")
+        if self.TF is not None and self.parts is None:
+            raise RuntimeError("prepare_replicas() must run before capturing a step with TreeFold")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            self.run(stream)
+        return g
 
     def prepare_replicas(self, stream: torch.cuda.Stream) -> None:
         """Q_s = G (+) shard_noise_s (s = 1..S-1), then G_2 = running sum, then
