@@ -548,6 +548,45 @@ __device__ __forceinline__ void tile_dot(float (&out)[4][4], const float* __rest
     }
 }
 
+// pp[q2][e] = sum over r = 0..63, left to right from the first (flushed)
+// term, of W[r][2q2 .. 2q2+1] (x) X[r][e] for a thread's 8 x 4 block: W rows
+// of pitch pw at Wp, X rows of pitch px at Xp; operands one step ahead
+__device__ __forceinline__ void full_sum64(u64 (&pp)[4][4], const float* __restrict__ Wp, int pw,
+                                           const float* __restrict__ Xp, int px)
+{
+    ulonglong2 w03 = *reinterpret_cast<const ulonglong2*>(Wp);
+    ulonglong2 w47 = *reinterpret_cast<const ulonglong2*>(Wp + 4);
+    float4 xv = *reinterpret_cast<const float4*>(Xp);
+    {
+        const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
+        const u64 X2[4] = {pack2(xv.x, xv.x), pack2(xv.y, xv.y), pack2(xv.z, xv.z),
+                           pack2(xv.w, xv.w)};
+        w03 = *reinterpret_cast<const ulonglong2*>(Wp + pw);
+        w47 = *reinterpret_cast<const ulonglong2*>(Wp + pw + 4);
+        xv = *reinterpret_cast<const float4*>(Xp + px);
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                pp[q2][e] = fadd2_ftz(fmul2_rn(P[q2], X2[e]), pack2(-0.0f, -0.0f));
+    }
+#pragma unroll 9
+    for (int r = 1; r < AT; ++r) {
+        const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
+        const u64 X2[4] = {pack2(xv.x, xv.x), pack2(xv.y, xv.y), pack2(xv.z, xv.z),
+                           pack2(xv.w, xv.w)};
+        const int rn = r + 1 < AT ? r + 1 : r;
+        w03 = *reinterpret_cast<const ulonglong2*>(Wp + rn * pw);
+        w47 = *reinterpret_cast<const ulonglong2*>(Wp + rn * pw + 4);
+        xv = *reinterpret_cast<const float4*>(Xp + rn * px);
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                pp[q2][e] = fadd2_ftz(pp[q2][e], fmul2_rn(P[q2], X2[e]));
+    }
+}
+
 __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
 {
     extern __shared__ __align__(16) float smb[];
@@ -692,23 +731,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                 float part[8][4];
                 if (full) {
                     u64 pp[4][4];   // [row pair][column]
-#pragma unroll 2
-                    for (int jc = 0; jc < AT; ++jc) {
-                        const ulonglong2 s03 = *reinterpret_cast<const ulonglong2*>(St + jc * PB + grp * 8);
-                        const ulonglong2 s47 = *reinterpret_cast<const ulonglong2*>(St + jc * PB + grp * 8 + 4);
-                        const float4 kv = *reinterpret_cast<const float4*>(Ks + jc * PR + 4 * dg);
-                        const u64 P[4] = {s03.x, s03.y, s47.x, s47.y};
-                        const u64 Dk[4] = {pack2(kv.x, kv.x), pack2(kv.y, kv.y), pack2(kv.z, kv.z),
-                                           pack2(kv.w, kv.w)};
-#pragma unroll
-                        for (int q2 = 0; q2 < 4; ++q2)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const u64 t = fmul2_rn(P[q2], Dk[e]);
-                                pp[q2][e] = jc == 0 ? fadd2_ftz(t, pack2(-0.0f, -0.0f))
-                                                    : fadd2_ftz(pp[q2][e], t);
-                            }
-                    }
+                    full_sum64(pp, St + grp * 8, PB, Ks + 4 * dg, PR);
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2)
 #pragma unroll
@@ -731,10 +754,20 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             pp[q2][e] = 0ull;
+                    ulonglong2 n03 = {0ull, 0ull}, n47 = {0ull, 0ull};
+                    float4 nkv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (lo_all <= hi_all) {
+                        n03 = *reinterpret_cast<const ulonglong2*>(St + lo_all * PB + grp * 8);
+                        n47 = *reinterpret_cast<const ulonglong2*>(St + lo_all * PB + grp * 8 + 4);
+                        nkv = *reinterpret_cast<const float4*>(Ks + lo_all * PR + 4 * dg);
+                    }
                     for (int jc = lo_all; jc <= hi_all; ++jc) {
-                        const ulonglong2 s03 = *reinterpret_cast<const ulonglong2*>(St + jc * PB + grp * 8);
-                        const ulonglong2 s47 = *reinterpret_cast<const ulonglong2*>(St + jc * PB + grp * 8 + 4);
-                        const float4 kv = *reinterpret_cast<const float4*>(Ks + jc * PR + 4 * dg);
+                        const ulonglong2 s03 = n03, s47 = n47;
+                        const float4 kv = nkv;
+                        const int jn = jc < hi_all ? jc + 1 : jc;
+                        n03 = *reinterpret_cast<const ulonglong2*>(St + jn * PB + grp * 8);
+                        n47 = *reinterpret_cast<const ulonglong2*>(St + jn * PB + grp * 8 + 4);
+                        nkv = *reinterpret_cast<const float4*>(Ks + jn * PR + 4 * dg);
                         const u64 P[4] = {s03.x, s03.y, s47.x, s47.y};
                         const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
@@ -807,23 +840,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                     float pt[8][4];
                     if (full) {
                         u64 pp[4][4];   // [key pair][column]
-#pragma unroll 2
-                        for (int ir = 0; ir < AT; ++ir) {
-                            const ulonglong2 w03 = *reinterpret_cast<const ulonglong2*>(Wt + ir * PB + grp * 8);
-                            const ulonglong2 w47 = *reinterpret_cast<const ulonglong2*>(Wt + ir * PB + grp * 8 + 4);
-                            const float4 xv = *reinterpret_cast<const float4*>(Xr + ir * PR + 4 * dg);
-                            const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
-                            const u64 X2[4] = {pack2(xv.x, xv.x), pack2(xv.y, xv.y), pack2(xv.z, xv.z),
-                                               pack2(xv.w, xv.w)};
-#pragma unroll
-                            for (int q2 = 0; q2 < 4; ++q2)
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const u64 t = fmul2_rn(P[q2], X2[e]);
-                                    pp[q2][e] = ir == 0 ? fadd2_ftz(t, pack2(-0.0f, -0.0f))
-                                                        : fadd2_ftz(pp[q2][e], t);
-                                }
-                        }
+                        full_sum64(pp, Wt + grp * 8, PB, Xr + 4 * dg, PR);
 #pragma unroll
                         for (int q2 = 0; q2 < 4; ++q2)
 #pragma unroll
@@ -846,10 +863,20 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
                                 pp[q2][e] = 0ull;
+                        ulonglong2 n03 = {0ull, 0ull}, n47 = {0ull, 0ull};
+                        float4 nxv = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (lo_all <= hi_all) {
+                            n03 = *reinterpret_cast<const ulonglong2*>(Wt + lo_all * PB + grp * 8);
+                            n47 = *reinterpret_cast<const ulonglong2*>(Wt + lo_all * PB + grp * 8 + 4);
+                            nxv = *reinterpret_cast<const float4*>(Xr + lo_all * PR + 4 * dg);
+                        }
                         for (int ir = lo_all; ir <= hi_all; ++ir) {
-                            const ulonglong2 w03 = *reinterpret_cast<const ulonglong2*>(Wt + ir * PB + grp * 8);
-                            const ulonglong2 w47 = *reinterpret_cast<const ulonglong2*>(Wt + ir * PB + grp * 8 + 4);
-                            const float4 xv = *reinterpret_cast<const float4*>(Xr + ir * PR + 4 * dg);
+                            const ulonglong2 w03 = n03, w47 = n47;
+                            const float4 xv = nxv;
+                            const int rn = ir < hi_all ? ir + 1 : ir;
+                            n03 = *reinterpret_cast<const ulonglong2*>(Wt + rn * PB + grp * 8);
+                            n47 = *reinterpret_cast<const ulonglong2*>(Wt + rn * PB + grp * 8 + 4);
+                            nxv = *reinterpret_cast<const float4*>(Xr + rn * PR + 4 * dg);
                             const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
                             const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
