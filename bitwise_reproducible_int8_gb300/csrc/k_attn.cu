@@ -130,24 +130,40 @@ __device__ __forceinline__ void logits4x4(u64 (&s)[8], const float* __restrict__
                                           const float* __restrict__ Kt, int ty, int tx, float c)
 {
     u64 t0[8];
+    const float* qp = Qt + 4 * ty;
+    const float* kp = Kt + 4 * tx;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
+        // operands are loaded one step ahead of their products
+        const int d0 = half * 64;
         u64 acc[8];
-#pragma unroll 4
-        for (int dd = 0; dd < 64; ++dd) {
-            const int d = half * 64 + dd;
-            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(Qt + d * PT + 4 * ty);
-            const float4 kb = *reinterpret_cast<const float4*>(Kt + d * PT + 4 * tx);
+        ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qp + d0 * PT);
+        float4 kb = *reinterpret_cast<const float4*>(kp + d0 * PT);
+        {
             const u64 P[2] = {qa.x, qa.y};
             const u64 D[4] = {pack2(kb.x, kb.x), pack2(kb.y, kb.y), pack2(kb.z, kb.z),
                               pack2(kb.w, kb.w)};
+            qa = *reinterpret_cast<const ulonglong2*>(qp + (d0 + 1) * PT);
+            kb = *reinterpret_cast<const float4*>(kp + (d0 + 1) * PT);
 #pragma unroll
             for (int ip = 0; ip < 2; ++ip)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const u64 p = fmul2_rn(P[ip], D[j]);
-                    acc[ip * 4 + j] = dd == 0 ? p : fadd2_ftz(acc[ip * 4 + j], p);
-                }
+                for (int j = 0; j < 4; ++j)
+                    acc[ip * 4 + j] = fmul2_rn(P[ip], D[j]);
+        }
+#pragma unroll 9
+        for (int dd = 1; dd < 64; ++dd) {
+            const u64 P[2] = {qa.x, qa.y};
+            const u64 D[4] = {pack2(kb.x, kb.x), pack2(kb.y, kb.y), pack2(kb.z, kb.z),
+                              pack2(kb.w, kb.w)};
+            const int dn = d0 + (dd + 1 < 64 ? dd + 1 : dd);
+            qa = *reinterpret_cast<const ulonglong2*>(qp + dn * PT);
+            kb = *reinterpret_cast<const float4*>(kp + dn * PT);
+#pragma unroll
+            for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    acc[ip * 4 + j] = fadd2_ftz(acc[ip * 4 + j], fmul2_rn(P[ip], D[j]));
         }
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
