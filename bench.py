@@ -423,7 +423,10 @@ def hbm_bytes(hp) -> dict:
 def measure_e2e(hp, host, steps, stream, world):
     """Same steps through the public API with host buffers: every step copies
     its inputs from pinned host memory (weights, then each micro-batch's X and
-    dY on a copy stream overlapped with compute) and reads the result back."""
+    dY, on a copy stream) and reads the result back.  Each input buffer is
+    refilled as soon as the previous step has read it for the last time, so
+    step s+1's copies overlap step s's later micro-batches; with the optimizer
+    on, the weights wait for the whole previous step (it updates them)."""
     import torch
     L, J = len(hp.wl.linears), hp.wl.microbatches
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
@@ -436,24 +439,36 @@ def measure_e2e(hp, host, steps, stream, world):
         sum(t.numel() * 4 for r in hdY for t in r)
     d2h = res.numel() * 4
     copy = torch.cuda.Stream()
+    prev_done = [None]
 
     def one_step():
         evs = []
-        copy.wait_stream(stream)
+        done = [torch.cuda.Event() for _ in range(J + 1)]
         with torch.cuda.stream(copy):
+            if prev_done[0] is None or hp.use_optimizer:
+                copy.wait_stream(stream)
+            else:
+                copy.wait_event(prev_done[0][J])
             for i in range(L):
                 hp.W[i].copy_(hW[i], non_blocking=True)
             for j in range(J):
+                if prev_done[0] is not None and not hp.use_optimizer:
+                    copy.wait_event(prev_done[0][j])
                 for i in range(L):
                     hp.X[i][j].copy_(hX[i][j], non_blocking=True)
                     hp.dY[i][j].copy_(hdY[i][j], non_blocking=True)
                 e = torch.cuda.Event()
                 e.record(copy)
                 evs.append(e)
-        hp.run(stream, wait_events=evs)
+        hp.run(stream, wait_events=evs, done_events=done)
+        prev_done[0] = done
         with torch.cuda.stream(stream):
             out_host.copy_(res, non_blocking=True)
 
+    # the inputs are the same every step, so every step's result must equal
+    # the device-resident step's, bit for bit (a refill that raced a read
+    # would show here); without the optimizer only, which changes W
+    expect = None if hp.use_optimizer else res.detach().cpu().clone()
     with torch.cuda.stream(stream):
         one_step()
     stream.synchronize()
@@ -465,6 +480,8 @@ def measure_e2e(hp, host, steps, stream, world):
         one_step()
     b.record(stream)
     stream.synchronize()
+    if expect is not None and not torch.equal(out_host.view(torch.int32), expect.view(torch.int32)):
+        raise RuntimeError("end-to-end steps changed the result bits")
     ms = max_over_ranks(a.elapsed_time(b), world, "cuda")
     return {"value": whole_job_tokens_per_s(hp.tokens(), steps, world, ms), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

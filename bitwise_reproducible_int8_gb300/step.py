@@ -147,10 +147,15 @@ class HotPathStep:
         timers[cls][-1][1] = e
 
     def run(self, stream: torch.cuda.Stream, timers: dict | None = None,
-            wait_events: list | None = None) -> None:
+            wait_events: list | None = None, done_events: list | None = None) -> None:
         """Enqueue one step on `stream`.  With `timers`, records a CUDA event
         pair around every call, grouped by call class.  `wait_events[j]`, if
-        given, is waited on before micro-batch j's first use of its inputs."""
+        given, is waited on before micro-batch j's first use of its inputs.
+        `done_events`, if given (J + 1 events), records done_events[j] once
+        micro-batch j's X and dY have been read for the last time and
+        done_events[J] once the weights W have been (they are read only by the
+        scale and quantise calls at the start of the step), so a producer can
+        refill each input as soon as this step is done with it."""
         wl, s = self.wl, stream
         L, J = len(wl.linears), wl.microbatches
         sw = lambda i: self.s_w[i:i + 1]  # noqa: E731
@@ -165,6 +170,8 @@ class HotPathStep:
             self._ev(timers, "quant_w", s)
             R.repro_quant_i8(self.W[i], sw(i), self.Wq[i], stream=s)
             self._end(timers, "quant_w", s)
+        if done_events is not None:
+            done_events[J].record(s)
         for j in range(J):
             if wait_events is not None and j > 0 and wait_events[j] is not None:
                 s.wait_event(wait_events[j])
@@ -197,6 +204,8 @@ class HotPathStep:
                     self._ev(timers, "accum", s)
                     R.repro_grad_accum(self.Gv[i], self.dW_tmp[i], stream=s)
                     self._end(timers, "accum", s)
+            if done_events is not None:
+                done_events[j].record(s)
         level2 = self.G
         if self.G2 is not None and self.shard_parts is not None:
             self._ev(timers, "running_sum", s)
