@@ -142,8 +142,18 @@ def mul(a: F32, b: F32) -> F32:
 
 def div(a: F32, b: F32) -> F32:
     a, b = flush(a), flush(b)
-    assert a.kind == "fin" and b.kind == "fin" and not b.is_zero()
-    return flush(round_to_f32(a.neg != b.neg, a.mag / b.mag))
+    neg = a.neg != b.neg
+    # IEEE 754 special operands: NaN propagates; inf/inf and 0/0 are invalid
+    # (NaN); inf/finite is inf; finite/inf is a signed zero; x/0 is inf
+    if a.kind == "nan" or b.kind == "nan":
+        return F32(False, None, "nan")
+    if a.kind == "inf":
+        return F32(False, None, "nan") if b.kind == "inf" else F32(neg, None, "inf")
+    if b.kind == "inf":
+        return F32(neg, Fraction(0))
+    if b.is_zero():
+        return F32(False, None, "nan") if a.is_zero() else F32(neg, None, "inf")
+    return flush(round_to_f32(neg, a.mag / b.mag))
 
 
 def sqrt(a: F32) -> F32:
@@ -182,6 +192,8 @@ def quant(x: F32, s: F32, qmax: int = 127) -> int:
     if s.is_zero():
         return 0
     v = div(x, s)
+    if v.kind == "nan":
+        return 0
     if v.kind == "inf":
         return -qmax if v.neg else qmax
     q = rint_half_even(v)

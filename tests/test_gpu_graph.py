@@ -113,3 +113,54 @@ def test_attention_graph_replays_match_eager(W):
         for i, (t, e) in enumerate(zip(outs, eager)):
             assert np.array_equal(_bits(t), e), f"attention output {i} differs after a replay"
     assert R.repro_device_check(st) == R.REPRO_OK
+
+
+def test_overlapped_input_refill_keeps_bits():
+    # the end-to-end pattern: each step's inputs are copied from pinned host
+    # memory on a copy stream, each buffer refilled as soon as the previous step
+    # has last read it (run()'s done events); every step's result must be the
+    # device-resident step's, bit for bit
+    wl = MID
+    st, cp = torch.cuda.Stream(), torch.cuda.Stream()
+    hp = S.HotPathStep(wl)
+    with torch.cuda.stream(st):
+        hp.prepare(st)
+        hp.run(st)
+    st.synchronize()
+    expect = _bits(hp.result())
+    L, J = len(wl.linears), wl.microbatches
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    hX = [[pin(hp.host.X[i][j]) for j in range(J)] for i in range(L)]
+    hdY = [[pin(hp.host.dY[i][j]) for j in range(J)] for i in range(L)]
+    hW = [pin(hp.host.W[i]) for i in range(L)]
+    out = torch.empty(hp.result().shape, dtype=torch.float32, pin_memory=True)
+    for t in hp.X[0] + hp.X[1] + hp.dY[0] + hp.dY[1] + hp.W:
+        t.fill_(float("nan"))   # every input must come from the copies
+    torch.cuda.synchronize()
+    prev = None
+    for _ in range(3):
+        done = [torch.cuda.Event() for _ in range(J + 1)]
+        evs = []
+        with torch.cuda.stream(cp):
+            if prev is None:
+                cp.wait_stream(st)
+            else:
+                cp.wait_event(prev[J])
+            for i in range(L):
+                hp.W[i].copy_(hW[i], non_blocking=True)
+            for j in range(J):
+                if prev is not None:
+                    cp.wait_event(prev[j])
+                for i in range(L):
+                    hp.X[i][j].copy_(hX[i][j], non_blocking=True)
+                    hp.dY[i][j].copy_(hdY[i][j], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(cp)
+                evs.append(e)
+        hp.run(st, wait_events=evs, done_events=done)
+        prev = done
+        with torch.cuda.stream(st):
+            out.copy_(hp.result(), non_blocking=True)
+        st.synchronize()
+        assert np.array_equal(out.numpy().view(np.uint32), expect)
+    assert R.repro_device_check(st) == R.REPRO_OK
