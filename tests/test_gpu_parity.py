@@ -223,6 +223,30 @@ def test_backward_flush_cases(orc):
         G.assert_bits_equal(dx, orc.linear_bwd_dx(dy, wq, s_w), f"flush s_w={s_w}")
 
 
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7, 8])
+def test_backward_subnormal_dy_every_kernel(orc, kernel):
+    # subnormal upstream gradients against codes of 127 at scale 1: unflushed,
+    # 1e-40 (x) 127 = 1.27e-38 would be a normal product, so a missed flush of
+    # dY changes dX and dW; the shape is aligned, so kernels 2-8 take their
+    # fast paths (dW over 130 tokens: three chunks, a ragged tail)
+    R.repro_set_launch_cfg(bwd_kernel=kernel)
+    rng = np.random.default_rng(40)
+    M, N, K = 130, 68, 32
+    dy = (rng.standard_normal((M, N)) * 1e-3).astype(np.float32)
+    dy[::3, ::2] = 1e-40
+    dy[1::5, 1::3] = -1e-40
+    dy[7] = 1e-40                                         # a whole row
+    dy[:, 5] = -1e-40                                     # a whole column
+    xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    xq[::2] = 127
+    wq[::2] = -127
+    one = np.float32(1.0)
+    dx, dw = G.gpu_bwd(dy, xq, wq, one, one)
+    G.assert_bits_equal(dx, orc.linear_bwd_dx(dy, wq, one), f"dx kernel {kernel}")
+    G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, one), f"dw kernel {kernel}")
+
+
 def test_backward_accumulate_flag(orc):
     rng = np.random.default_rng(21)
     M, N, K = 300, 130, 68
