@@ -42,6 +42,9 @@ constexpr int TILE_BYTES = TM * TK * 2;   // 16 KB, the same for A and B
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 256;
 constexpr size_t SMEM_BYTES = 1024 + 2 * STAGES * TILE_BYTES + 256;
+constexpr int EPI_PITCH = TN + 4;  // floats per staged output row (conflict-free both ways)
+static_assert(4 * 32 * EPI_PITCH * 4 <= 2 * STAGES * TILE_BYTES,
+              "the epilogue staging must fit in the operand ring");
 constexpr long long WAIT_CYCLES = 4000000000LL;   // ~2 s at the boost clock
 
 struct Smem {
@@ -290,19 +293,30 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
         } else {
             const float sx = flush(*s_x), sw = flush(*s_w);
             const int row = m0 + 32 * q + lane;
-            if (row < M) {
-                float* dst = y + (int64_t)row * N + n0;
-                if ((N & 3) == 0 && n0 + TN <= N) {
+            if ((N & 3) == 0 && n0 + TN <= N) {
+                // every MMA has completed (the last slice's barrier), so no copy or
+                // MMA touches the operand ring any more: each warp stages its 32 x
+                // 128 block there (pitch EPI_PITCH) and stores whole rows, 512
+                // contiguous bytes per warp instruction
+                float* stg = reinterpret_cast<float*>(base) + q * (32 * EPI_PITCH);
 #pragma unroll
-                    for (int j = 0; j < TN; j += 4) {
-                        float4 o;
-                        o.x = fmul_flush(fmul_flush(__int2float_rn(acc[j + 0]), sx), sw);
-                        o.y = fmul_flush(fmul_flush(__int2float_rn(acc[j + 1]), sx), sw);
-                        o.z = fmul_flush(fmul_flush(__int2float_rn(acc[j + 2]), sx), sw);
-                        o.w = fmul_flush(fmul_flush(__int2float_rn(acc[j + 3]), sx), sw);
-                        *reinterpret_cast<float4*>(dst + j) = o;
-                    }
-                } else {
+                for (int j = 0; j < TN; j += 4) {
+                    float4 o;
+                    o.x = fmul_flush(fmul_flush(__int2float_rn(acc[j + 0]), sx), sw);
+                    o.y = fmul_flush(fmul_flush(__int2float_rn(acc[j + 1]), sx), sw);
+                    o.z = fmul_flush(fmul_flush(__int2float_rn(acc[j + 2]), sx), sw);
+                    o.w = fmul_flush(fmul_flush(__int2float_rn(acc[j + 3]), sx), sw);
+                    *reinterpret_cast<float4*>(stg + lane * EPI_PITCH + j) = o;
+                }
+                __syncwarp();
+                const int rows = min(32, M - (m0 + 32 * q));
+                for (int r = 0; r < rows; ++r) {
+                    const float4 v = *reinterpret_cast<const float4*>(stg + r * EPI_PITCH + 4 * lane);
+                    *reinterpret_cast<float4*>(y + (int64_t)(m0 + 32 * q + r) * N + n0 + 4 * lane) = v;
+                }
+            } else if (row < M) {
+                float* dst = y + (int64_t)row * N + n0;
+                {
 #pragma unroll
                     for (int j = 0; j < TN; ++j)
                         if (n0 + j < N)
