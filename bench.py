@@ -343,6 +343,9 @@ def run_ours(args, wl):
             "frac": achieved / fp32_peak if fp32_peak else None,
             "peak_note": f"FP32 pipe: {sms} SMs x 128 lanes x {peaks.get('sm_max_mhz', 2070.0):.0f} MHz,"
                          " one FMUL or FADD per lane per clock (no FMA may be used)",
+            # the same work as a FLOP fraction of the peak that counts an FFMA as
+            # two FLOPs; without FMA this can reach at most 0.5
+            "flop_frac_of_ffma_peak": achieved / (2 * fp32_peak) if fp32_peak else None,
             "traffic": BWD_TRAFFIC_PER_LAUNCH.get((wl.name, kname)), "launches": nb,
             "flops_per_launch": bwd_ops / nb if nb else None,
             "avg_launch_ms": bwd_ms / nb if nb else None,
