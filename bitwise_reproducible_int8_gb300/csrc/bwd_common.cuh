@@ -1,5 +1,6 @@
 // bwd_common.cuh -- argument block and tile constants shared by the backward
-// kernels (k_bwd.cu: single-role kernels; k_bwd_ws.cu: warp-specialised kernel).
+// kernels (k_bwd.cu: single-role kernels; k_bwd_ws.cu: warp-specialised kernel;
+// k_bwd_tma.cu: tensor-copy-fed kernel).
 #pragma once
 
 #include <cuda_runtime.h>

@@ -26,13 +26,13 @@
 // Every wait is bounded: past the limit the CTA records a failure in the
 // device error word, lets its copies land, frees its tensor memory and exits.
 #include "bwd_common.cuh"
+#include "bwd_tile.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace repro {
 namespace {
-
-typedef unsigned long long u64;
 
 constexpr int NC = 256;                              // compute threads (warps 0-7)
 constexpr int NP = 128;                              // producer threads (warps 8-11)
@@ -47,46 +47,6 @@ constexpr int COMP_STAGE = COMPA_BYTES + COMPB_BYTES;
 constexpr int CTRL_OFF = 2 * RAW_STAGE + 2 * COMP_STAGE;
 constexpr size_t SMEM_BYTES = (size_t)CTRL_OFF + 64;
 constexpr int REGL = 1;                              // tree levels kept in registers
-constexpr long long WAIT_CYCLES = 4000000000LL;      // ~2 s at the boost clock
-
-__device__ __forceinline__ uint32_t su32(const void* p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* b)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(su32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// true once the phase with this parity has completed; false after the limit
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity)
-{
-    const long long t0 = clock64();
-    while (!mbar_test(b, parity)) {
-        if (clock64() - t0 > WAIT_CYCLES)
-            return false;
-    }
-    return true;
-}
 
 __device__ __forceinline__ void producer_sync()
 {
@@ -98,47 +58,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(su32(dst)), "l"(src),
                  "r"(src_bytes)
                  : "memory");
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const u64 (&v)[16])
-{
-    uint32_t w[32];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        w[2 * e] = (uint32_t)(v[e] & 0xffffffffull);
-        w[2 * e + 1] = (uint32_t)(v[e] >> 32);
-    }
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
-        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
-        "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
-        "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// acc[e] <- level[e] (+) acc[e]: the level holds the left operand
-__device__ __forceinline__ void tmem_fold32(uint32_t taddr, u64 (&acc)[16])
-{
-    uint32_t w[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
-          "=r"(w[7]), "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]),
-          "=r"(w[14]), "=r"(w[15]), "=r"(w[16]), "=r"(w[17]), "=r"(w[18]), "=r"(w[19]),
-          "=r"(w[20]), "=r"(w[21]), "=r"(w[22]), "=r"(w[23]), "=r"(w[24]), "=r"(w[25]),
-          "=r"(w[26]), "=r"(w[27]), "=r"(w[28]), "=r"(w[29]), "=r"(w[30]), "=r"(w[31])
-        : "r"(taddr)
-        : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-        acc[e] = fadd2_ftz((u64)w[2 * e] | ((u64)w[2 * e + 1] << 32), acc[e]);
 }
 
 // raw copy of the chunk starting at reduction index r0 by producer thread p:
@@ -218,22 +137,6 @@ __device__ __forceinline__ void transform(float* __restrict__ As, float* __restr
                             dequant((int)(int8_t)(words[u] >> 16), s),
                             dequant((int)(int8_t)(words[u] >> 24), s));
     }
-}
-
-// one reduction step: rows 8ty..8ty+7 as 4 pairs, columns 4tx..4tx+3
-template <bool FIRST>
-__device__ __forceinline__ void step(u64 (&acc)[16], const ulonglong2& a03, const ulonglong2& a47,
-                                     const float4& b)
-{
-    const u64 P[4] = {a03.x, a03.y, a47.x, a47.y};
-    const u64 D[4] = {pack2(b.x, b.x), pack2(b.y, b.y), pack2(b.z, b.z), pack2(b.w, b.w)};
-#pragma unroll
-    for (int ip = 0; ip < 4; ++ip)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const u64 p = fmul2_rn(P[ip], D[j]);
-            acc[ip * 4 + j] = FIRST ? p : fadd2_ftz(acc[ip * 4 + j], p);
-        }
 }
 
 // the chunk's left-to-right sums for this thread's 32 outputs

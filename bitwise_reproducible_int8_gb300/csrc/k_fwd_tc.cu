@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace repro {
 namespace {
@@ -45,7 +46,6 @@ constexpr size_t SMEM_BYTES = 1024 + 2 * STAGES * TILE_BYTES + 256;
 constexpr int EPI_PITCH = TN + 4;  // floats per staged output row (conflict-free both ways)
 static_assert(4 * 32 * EPI_PITCH * 4 <= 2 * STAGES * TILE_BYTES,
               "the epilogue staging must fit in the operand ring");
-constexpr long long WAIT_CYCLES = 4000000000LL;   // ~2 s at the boost clock
 
 struct Smem {
     uint64_t full[STAGES];
@@ -56,62 +56,6 @@ struct Smem {
     uint32_t tmem_base;
     int failed;
 };
-
-__device__ __forceinline__ uint32_t su32(const void* p)
-{
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* b)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(su32(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// true once the phase with this parity has completed; false after the limit
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity)
-{
-    const long long t0 = clock64();
-    while (!mbar_test(b, parity)) {
-        if (clock64() - t0 > WAIT_CYCLES)
-            return false;
-    }
-    return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(su32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(su32(bar))
-        : "memory");
-}
 
 // shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (stride byte offset), descriptor version 1
