@@ -35,6 +35,7 @@
 #include <float.h>
 
 #include "bwd_common.cuh"
+#include "bwd_tile.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -297,8 +298,6 @@ __global__ void __launch_bounds__(256, 1) k_bwd(const BwdArgs a)
 
 constexpr int STAGE_FLOATS = 3 * CH * BT;                       // A, B dup lo, B dup hi
 constexpr size_t BWD2_SMEM = 2 * STAGE_FLOATS * sizeof(float);  // 96 KB
-
-typedef unsigned long long u64;
 
 template <bool DW>
 __device__ __forceinline__ void fetch_a(float4 (&v)[4], const BwdArgs& a, int64_t i0, int64_t r0,
@@ -956,22 +955,6 @@ __device__ __forceinline__ void transform4(float* __restrict__ As, float* __rest
                         dequant((int)(int8_t)(words[u] >> 24), s));
 }
 
-// one reduction step: rows 8ty..8ty+7 as 4 pairs, columns 4tx..4tx+3
-template <bool FIRST>
-__device__ __forceinline__ void step4(u64 (&acc)[16], const ulonglong2& a03, const ulonglong2& a47,
-                                      const float4& b)
-{
-    const u64 P[4] = {a03.x, a03.y, a47.x, a47.y};
-    const u64 D[4] = {pack2(b.x, b.x), pack2(b.y, b.y), pack2(b.z, b.z), pack2(b.w, b.w)};
-#pragma unroll
-    for (int ip = 0; ip < 4; ++ip)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const u64 p = fmul2_rn(P[ip], D[j]);
-            acc[ip * 4 + j] = FIRST ? p : fadd2_ftz(acc[ip * 4 + j], p);
-        }
-}
-
 template <bool DW>
 __global__ void __launch_bounds__(256, 1) k_bwd4(const BwdArgs a)
 {
@@ -1035,7 +1018,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd4(const BwdArgs a)
                 a47 = *reinterpret_cast<const ulonglong2*>(Ar + BI4 + 4);
                 b = *reinterpret_cast<const float4*>(Br + BT);
             }
-            step4<true>(acc, c03, c47, cb);
+            step<true>(acc, c03, c47, cb);
         }
         if (valid == CH) {
 #pragma unroll 7
@@ -1046,7 +1029,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd4(const BwdArgs a)
                 a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4);
                 a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4 + 4);
                 b = *reinterpret_cast<const float4*>(Br + rn * BT);
-                step4<false>(acc, c03, c47, cb);
+                step<false>(acc, c03, c47, cb);
             }
         } else {
             for (int r = 1; r < valid; ++r) {
@@ -1056,7 +1039,7 @@ __global__ void __launch_bounds__(256, 1) k_bwd4(const BwdArgs a)
                 a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4);
                 a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI4 + 4);
                 b = *reinterpret_cast<const float4*>(Br + rn * BT);
-                step4<false>(acc, c03, c47, cb);
+                step<false>(acc, c03, c47, cb);
             }
         }
 
@@ -1155,26 +1138,6 @@ constexpr int RAW5_STAGE = RAW4_A_BYTES + RAW4_B_BYTES;          // 38912
 constexpr int COMP5_STAGE = COMP4_A_BYTES + COMP4_B_BYTES;       // 49152
 constexpr size_t BWD5_SMEM = 2 * (size_t)RAW5_STAGE + 2 * (size_t)COMP5_STAGE + 16;
 constexpr int REG5 = 2;                                          // levels in registers
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const u64 (&v)[16])
-{
-    uint32_t w[32];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        w[2 * e] = (uint32_t)(v[e] & 0xffffffffull);
-        w[2 * e + 1] = (uint32_t)(v[e] >> 32);
-    }
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
-        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15]),
-        "r"(w[16]), "r"(w[17]), "r"(w[18]), "r"(w[19]), "r"(w[20]), "r"(w[21]), "r"(w[22]), "r"(w[23]),
-        "r"(w[24]), "r"(w[25]), "r"(w[26]), "r"(w[27]), "r"(w[28]), "r"(w[29]), "r"(w[30]), "r"(w[31])
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 
 __device__ __forceinline__ void tmem_ld32_u64(uint32_t taddr, u64 (&v)[16])
 {
@@ -1617,7 +1580,7 @@ __global__ void __launch_bounds__(NT6, 1) k_bwd6(const BwdArgs a)
                 a47 = *reinterpret_cast<const ulonglong2*>(Ar + BI6 + 4);
                 b = *reinterpret_cast<const float4*>(Br + BT);
             }
-            step4<true>(acc, c03, c47, cb);
+            step<true>(acc, c03, c47, cb);
         }
         if (valid == CH) {
 #pragma unroll 7
@@ -1628,7 +1591,7 @@ __global__ void __launch_bounds__(NT6, 1) k_bwd6(const BwdArgs a)
                 a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI6);
                 a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI6 + 4);
                 b = *reinterpret_cast<const float4*>(Br + rn * BT);
-                step4<false>(acc, c03, c47, cb);
+                step<false>(acc, c03, c47, cb);
             }
         } else {
             for (int r = 1; r < valid; ++r) {
@@ -1638,7 +1601,7 @@ __global__ void __launch_bounds__(NT6, 1) k_bwd6(const BwdArgs a)
                 a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI6);
                 a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * BI6 + 4);
                 b = *reinterpret_cast<const float4*>(Br + rn * BT);
-                step4<false>(acc, c03, c47, cb);
+                step<false>(acc, c03, c47, cb);
             }
         }
 
