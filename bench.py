@@ -257,7 +257,8 @@ def run_ours(args, wl):
         dist.barrier()
     wl_r = replica_workload(wl, rank)
     host = S.generate_host_inputs(wl_r)
-    hp = S.HotPathStep(wl_r, host, fused_accum=not args.unfused_accum)
+    hp = S.HotPathStep(wl_r, host, fused_accum=not args.unfused_accum,
+                       dw_stream=not args.no_dw_stream)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         if wl_r.replicas > 1 or wl_r.shards > 1:
@@ -314,6 +315,11 @@ def run_ours(args, wl):
             for _ in range(args.steps):
                 hp.run(stream, timers=timers)
         stream.synchronize()
+    pairs = timers.pop("bwd_pair", None)
+    pair_ms = n_pairs = None
+    if pairs:
+        pair_ms = sum(max(f.elapsed_time(dx), f.elapsed_time(dw)) for f, dx, dw in pairs)
+        n_pairs = len(pairs)
     per_class = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in timers.items()}
     launch_counts = {k: len(v) for k, v in timers.items()}
 
@@ -329,14 +335,30 @@ def run_ours(args, wl):
         peaks = load_peaks()
         sms = torch.cuda.get_device_properties(local).multi_processor_count
         fl = hp.flops()
-        bwd_ms = per_class.get("bwd_dx", 0.0) + per_class.get("bwd_dw", 0.0)
         bwd_ops = (fl["bwd_dx_fp32_ops"] + fl["bwd_dw_fp32_ops"]) * args.steps
+        if pair_ms is not None:
+            # dX and dW of a linear run concurrently: the unit is the pair, timed
+            # from the fork to the later of its two ends (the forward launched
+            # between them included, so the rate errs low)
+            bwd_ms, n_units = pair_ms, n_pairs
+        else:
+            bwd_ms = per_class.get("bwd_dx", 0.0) + per_class.get("bwd_dw", 0.0)
+            n_units = None
         fp32_peak = sms * 128 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         achieved = bwd_ops / (bwd_ms / 1000.0) / 1e12 if bwd_ms > 0 else 0.0
         nb = launch_counts.get("bwd_dx", 0) + launch_counts.get("bwd_dw", 0)
         kname = {0: "k_bwd", 1: "k_bwd2", 2: "k_bwd3", 3: "k_bwd4", 4: "k_bwd5",
                  5: "k_bwd6", 6: "k_bwd_ws", 7: "k_bwd_tma",
                  8: "k_bwd_tma<self-issue>"}[args.bwd_kernel if args.bwd_kernel >= 0 else 8]
+        traffic = BWD_TRAFFIC_PER_LAUNCH.get((wl.name, kname))
+        unit_note = None
+        if n_units:
+            unit_note = ("one unit = the dX and dW launches of one linear and micro-batch, run "
+                         "concurrently on two streams; its time runs from the fork to the later "
+                         "of the two ends and includes the forward launched between them; "
+                         "traffic is the two launches' (each measured alone under ncu)")
+            traffic = 2 * traffic if traffic is not None else None
+        per_unit = n_units if n_units else nb
         roofline = {
             "bound": "alu", "kernel": f"{kname} (dX and dW, canonical-order fp32)",
             "achieved": achieved, "peak": fp32_peak, "unit": "TFLOP/s",
@@ -346,10 +368,13 @@ def run_ours(args, wl):
             # the same work as a FLOP fraction of the peak that counts an FFMA as
             # two FLOPs; without FMA this can reach at most 0.5
             "flop_frac_of_ffma_peak": achieved / (2 * fp32_peak) if fp32_peak else None,
-            "traffic": BWD_TRAFFIC_PER_LAUNCH.get((wl.name, kname)), "launches": nb,
-            "flops_per_launch": bwd_ops / nb if nb else None,
-            "avg_launch_ms": bwd_ms / nb if nb else None,
+            "traffic": traffic, "launches": nb,
+            "flops_per_launch": bwd_ops / per_unit if per_unit else None,
+            "avg_launch_ms": bwd_ms / per_unit if per_unit else None,
         }
+        if unit_note:
+            roofline["units"] = n_units
+            roofline["unit_note"] = unit_note
         other = {}
         fwd_ms = per_class.get("fwd", 0.0)
         if fwd_ms > 0:
@@ -377,6 +402,8 @@ def run_ours(args, wl):
                        "linears": [f"{l.name} {l.n_out}x{l.k_in}" for l in wl.linears],
                        "replicas": wl.replicas, "shards": wl.shards,
                        "parallelism": "replicas only",
+                       "streams": "dW on a second stream, concurrent with the forward and dX"
+                       if hp.s_dw is not None else "one stream",
                        "accumulation": "unfused repro_grad_accum" if args.unfused_accum
                        else "fused into the dW epilogue",
                        "l2": (f"inputs larger than L2: {resident_gb(hp):.1f} GB resident, "
@@ -387,6 +414,7 @@ def run_ours(args, wl):
                        else "eager calls"},
             "roofline": roofline, "other_kernels": other,
             "ms_per_step_by_call": {k: v / args.steps for k, v in per_class.items()},
+            "overlapping_calls": ["bwd_dw", "fwd", "bwd_dx"] if hp.s_dw is not None else [],
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk, "peaks_source": peaks["source"],
         }
@@ -446,17 +474,19 @@ def measure_e2e(hp, host, steps, stream, world):
 
     def one_step():
         evs = []
-        done = [torch.cuda.Event() for _ in range(J + 1)]
+        done = [None] * (J + 1)
         with torch.cuda.stream(copy):
             if prev_done[0] is None or hp.use_optimizer:
                 copy.wait_stream(stream)
             else:
-                copy.wait_event(prev_done[0][J])
+                for ev in prev_done[0][J]:
+                    copy.wait_event(ev)
             for i in range(L):
                 hp.W[i].copy_(hW[i], non_blocking=True)
             for j in range(J):
                 if prev_done[0] is not None and not hp.use_optimizer:
-                    copy.wait_event(prev_done[0][j])
+                    for ev in prev_done[0][j]:
+                        copy.wait_event(ev)
                 for i in range(L):
                     hp.X[i][j].copy_(hX[i][j], non_blocking=True)
                     hp.dY[i][j].copy_(hdY[i][j], non_blocking=True)
@@ -762,6 +792,9 @@ def main(argv=None):
     ap.add_argument("--unfused-accum", action="store_true",
                     help="accumulate dW with repro_grad_accum instead of the fused epilogue")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-dw-stream", action="store_true",
+                    help="run each dW after its dX on the one stream (default: dW on a "
+                         "second stream, concurrent with the forward and dX)")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step into a CUDA graph and time its replays "
                          "(launch-bound workloads; not with the optimizer)")

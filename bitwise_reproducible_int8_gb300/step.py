@@ -67,7 +67,7 @@ class HotPathStep:
                "accum", "treefold")
 
     def __init__(self, wl: inputs.Workload, host: HostInputs | None = None,
-                 fused_accum: bool = True, device: str = "cuda"):
+                 fused_accum: bool = True, device: str = "cuda", dw_stream: bool = True):
         self.wl = wl
         self.fused_accum = fused_accum
         self.host = host if host is not None else generate_host_inputs(wl)
@@ -103,6 +103,12 @@ class HotPathStep:
                                     device=dev)
         need = max(R.repro_linear_bwd_ws_bytes(M, l.n_out, l.k_in) for l in wl.linears)
         self.ws_bwd = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+        # dW on a second stream, concurrent with the forward and dX of the same
+        # linear (its own workspace): each fills the other's part-empty last waves
+        self.s_dw = torch.cuda.Stream(device=dev) if dw_stream else None
+        self.ws_bwd_dw = None
+        if dw_stream and need > 0:
+            self.ws_bwd_dw = torch.empty(need, dtype=torch.uint8, device=dev)
         need = max(R.repro_linear_fwd_ws_bytes(M, l.n_out, l.k_in) for l in wl.linears)
         self.ws_fwd = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
         self.parts = None
@@ -148,16 +154,21 @@ class HotPathStep:
 
     def run(self, stream: torch.cuda.Stream, timers: dict | None = None,
             wait_events: list | None = None, done_events: list | None = None) -> None:
-        """Enqueue one step on `stream`.  With `timers`, records a CUDA event
-        pair around every call, grouped by call class.  `wait_events[j]`, if
-        given, is waited on before micro-batch j's first use of its inputs.
-        `done_events`, if given (J + 1 events), records done_events[j] once
-        micro-batch j's X and dY have been read for the last time and
-        done_events[J] once the weights W have been (they are read only by the
-        scale and quantise calls at the start of the step), so a producer can
-        refill each input as soon as this step is done with it."""
+        """Enqueue one step on `stream` (and, with dw_stream, its dW calls on
+        the step's second stream, joined back before the folds).  With
+        `timers`, records a CUDA event pair around every call, grouped by call
+        class, and for concurrent dX/dW the fork event with both end events
+        under "bwd_pair".  `wait_events[j]`, if given, is waited on before
+        micro-batch j's first use of its inputs.  `done_events`, if given (a
+        list of J + 1 slots), receives in slot j the events after which
+        micro-batch j's X and dY are no longer read, and in slot J those for
+        the weights W (read only by the scale and quantise calls at the start
+        of the step), so a producer can refill each input as soon as this step
+        is done with it."""
         wl, s = self.wl, stream
         L, J = len(wl.linears), wl.microbatches
+        s2 = self.s_dw
+        dw_done = [None] * L
         sw = lambda i: self.s_w[i:i + 1]  # noqa: E731
         sx = lambda i: self.s_x[i:i + 1]  # noqa: E731
         if wait_events is not None and wait_events[0] is not None:
@@ -171,18 +182,30 @@ class HotPathStep:
             R.repro_quant_i8(self.W[i], sw(i), self.Wq[i], stream=s)
             self._end(timers, "quant_w", s)
         if done_events is not None:
-            done_events[J].record(s)
+            e = torch.cuda.Event()
+            e.record(s)
+            done_events[J] = [e]
         for j in range(J):
             if wait_events is not None and j > 0 and wait_events[j] is not None:
                 s.wait_event(wait_events[j])
             for i in range(L):
                 X, dY = self.X[i][j], self.dY[i][j]
+                if dw_done[i] is not None:
+                    s.wait_event(dw_done[i])   # Xq[i] and s_x[i] are rewritten next
                 self._ev(timers, "wscale_x", s)
                 R.repro_wscale(X, R.REPRO_SCALE_ACT_AMAX, sx(i), ws=self.ws_scale, stream=s)
                 self._end(timers, "wscale_x", s)
                 self._ev(timers, "quant_x", s)
                 R.repro_quant_i8(X, sx(i), self.Xq[i], stream=s)
                 self._end(timers, "quant_x", s)
+                fork = None
+                if s2 is not None:
+                    fork = torch.cuda.Event(enable_timing=timers is not None)
+                    fork.record(s)
+                    s2.wait_event(fork)
+                    self._dw(i, j, dY, sx(i), s2, timers)
+                    dw_done[i] = torch.cuda.Event()
+                    dw_done[i].record(s2)
                 self._ev(timers, "fwd", s)
                 R.repro_linear_fwd(self.Xq[i], self.Wq[i], sx(i), sw(i), self.Y[i],
                                    ws=self.ws_fwd, stream=s)
@@ -191,21 +214,18 @@ class HotPathStep:
                 R.repro_linear_bwd(dY, None, self.Wq[i], None, sw(i), dx=self.dX[i], dw=None,
                                    ws=self.ws_bwd, stream=s)
                 self._end(timers, "bwd_dx", s)
-                if j == 0 or self.fused_accum:
-                    self._ev(timers, "bwd_dw", s)
-                    R.repro_linear_bwd(dY, self.Xq[i], None, sx(i), None, dx=None,
-                                       dw=self.Gv[i], accumulate=j > 0, ws=self.ws_bwd, stream=s)
-                    self._end(timers, "bwd_dw", s)
-                else:
-                    self._ev(timers, "bwd_dw", s)
-                    R.repro_linear_bwd(dY, self.Xq[i], None, sx(i), None, dx=None,
-                                       dw=self.dW_tmp[i], ws=self.ws_bwd, stream=s)
-                    self._end(timers, "bwd_dw", s)
-                    self._ev(timers, "accum", s)
-                    R.repro_grad_accum(self.Gv[i], self.dW_tmp[i], stream=s)
-                    self._end(timers, "accum", s)
+                if s2 is None:
+                    self._dw(i, j, dY, sx(i), s, timers)
+                elif timers is not None:
+                    timers.setdefault("bwd_pair", []).append(
+                        [fork, timers["bwd_dx"][-1][1], timers["bwd_dw"][-1][1]])
             if done_events is not None:
-                done_events[j].record(s)
+                e = torch.cuda.Event()
+                e.record(s)
+                done_events[j] = [e] + ([dw_done[L - 1]] if s2 is not None else [])
+        for d in dw_done:
+            if d is not None:
+                s.wait_event(d)   # join the dW stream before the folds
         level2 = self.G
         if self.G2 is not None and self.shard_parts is not None:
             self._ev(timers, "running_sum", s)
@@ -246,6 +266,24 @@ class HotPathStep:
         with torch.cuda.graph(g, stream=stream):
             self.run(stream)
         return g
+
+    def _dw(self, i: int, j: int, dY, sx, st, timers) -> None:
+        """dW of linear i for micro-batch j on stream `st`: fused into G, or
+        into a scratch buffer then accumulated (the first micro-batch is a copy)."""
+        ws = self.ws_bwd_dw if st is self.s_dw else self.ws_bwd
+        if j == 0 or self.fused_accum:
+            self._ev(timers, "bwd_dw", st)
+            R.repro_linear_bwd(dY, self.Xq[i], None, sx, None, dx=None, dw=self.Gv[i],
+                               accumulate=j > 0, ws=ws, stream=st)
+            self._end(timers, "bwd_dw", st)
+        else:
+            self._ev(timers, "bwd_dw", st)
+            R.repro_linear_bwd(dY, self.Xq[i], None, sx, None, dx=None, dw=self.dW_tmp[i],
+                               ws=ws, stream=st)
+            self._end(timers, "bwd_dw", st)
+            self._ev(timers, "accum", st)
+            R.repro_grad_accum(self.Gv[i], self.dW_tmp[i], stream=st)
+            self._end(timers, "accum", st)
 
     def prepare_replicas(self, stream: torch.cuda.Stream) -> None:
         """Q_s = G (+) shard_noise_s (s = 1..S-1), then G_2 = running sum, then

@@ -139,18 +139,20 @@ def test_overlapped_input_refill_keeps_bits():
     torch.cuda.synchronize()
     prev = None
     for _ in range(3):
-        done = [torch.cuda.Event() for _ in range(J + 1)]
+        done = [None] * (J + 1)
         evs = []
         with torch.cuda.stream(cp):
             if prev is None:
                 cp.wait_stream(st)
             else:
-                cp.wait_event(prev[J])
+                for ev in prev[J]:
+                    cp.wait_event(ev)
             for i in range(L):
                 hp.W[i].copy_(hW[i], non_blocking=True)
             for j in range(J):
                 if prev is not None:
-                    cp.wait_event(prev[j])
+                    for ev in prev[j]:
+                        cp.wait_event(ev)
                 for i in range(L):
                     hp.X[i][j].copy_(hX[i][j], non_blocking=True)
                     hp.dY[i][j].copy_(hdY[i][j], non_blocking=True)
@@ -164,3 +166,22 @@ def test_overlapped_input_refill_keeps_bits():
         st.synchronize()
         assert np.array_equal(out.numpy().view(np.uint32), expect)
     assert R.repro_device_check(st) == R.REPRO_OK
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "unfused"])
+def test_dw_stream_matches_one_stream(fused):
+    # dW on its own stream (concurrent with the forward and dX) and dW after dX
+    # on the one stream give the same bits
+    outs = []
+    for dw_stream in (True, False):
+        hp = S.HotPathStep(MID, fused_accum=fused, dw_stream=dw_stream)
+        st = torch.cuda.Stream()
+        with torch.cuda.stream(st):
+            hp.prepare(st)
+            hp.run(st)
+            hp.run(st)
+        st.synchronize()
+        outs.append([_bits(t) for t in [hp.result(), hp.G] + hp.dX + hp.Y])
+        assert R.repro_device_check(st) == R.REPRO_OK
+    for i, (a, b) in enumerate(zip(*outs)):
+        assert np.array_equal(a, b), f"output {i} differs between one and two streams"
