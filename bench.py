@@ -258,7 +258,7 @@ def run_ours(args, wl):
     wl_r = replica_workload(wl, rank)
     host = S.generate_host_inputs(wl_r)
     hp = S.HotPathStep(wl_r, host, fused_accum=not args.unfused_accum,
-                       dw_stream=not args.no_dw_stream)
+                       dw_stream=False if args.no_dw_stream else None)
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         if wl_r.replicas > 1 or wl_r.shards > 1:
@@ -794,7 +794,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dw-stream", action="store_true",
                     help="run each dW after its dX on the one stream (default: dW on a "
-                         "second stream, concurrent with the forward and dX)")
+                         "second stream, concurrent with the forward and dX, for linears of "
+                         "at least 2^30 multiply-adds)")
     ap.add_argument("--graph", action="store_true",
                     help="capture one step into a CUDA graph and time its replays "
                          "(launch-bound workloads; not with the optimizer)")

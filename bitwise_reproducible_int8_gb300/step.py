@@ -67,7 +67,7 @@ class HotPathStep:
                "accum", "treefold")
 
     def __init__(self, wl: inputs.Workload, host: HostInputs | None = None,
-                 fused_accum: bool = True, device: str = "cuda", dw_stream: bool = True):
+                 fused_accum: bool = True, device: str = "cuda", dw_stream: bool | None = None):
         self.wl = wl
         self.fused_accum = fused_accum
         self.host = host if host is not None else generate_host_inputs(wl)
@@ -104,7 +104,12 @@ class HotPathStep:
         need = max(R.repro_linear_bwd_ws_bytes(M, l.n_out, l.k_in) for l in wl.linears)
         self.ws_bwd = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
         # dW on a second stream, concurrent with the forward and dX of the same
-        # linear (its own workspace): each fills the other's part-empty last waves
+        # linear (its own workspace): each fills the other's part-empty last
+        # waves.  By default only when a linear's backward is long enough for
+        # that to matter (2^30 multiply-adds); launch-bound steps would only pay
+        # for the extra events.
+        if dw_stream is None:
+            dw_stream = min(M * l.n_out * l.k_in for l in wl.linears) >= (1 << 30)
         self.s_dw = torch.cuda.Stream(device=dev) if dw_stream else None
         self.ws_bwd_dw = None
         if dw_stream and need > 0:

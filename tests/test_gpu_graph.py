@@ -40,10 +40,11 @@ MID = inputs.Workload("graph_mid", 4096, (inputs.Linear("a", 512, 256), inputs.L
                       2, 3, 40, 50, "graph capture case", 2)
 
 
-@pytest.mark.parametrize("wl", [inputs.WORKLOADS["tiny"], MID], ids=["tiny", "mid"])
-def test_step_graph_replays_match_eager(wl):
+@pytest.mark.parametrize("wl,dw_stream", [(inputs.WORKLOADS["tiny"], False), (MID, False),
+                                          (MID, True)], ids=["tiny", "mid", "mid-two-streams"])
+def test_step_graph_replays_match_eager(wl, dw_stream):
     st = torch.cuda.Stream()
-    hp = S.HotPathStep(wl)
+    hp = S.HotPathStep(wl, dw_stream=dw_stream)
     with torch.cuda.stream(st):
         if wl.replicas > 1 or wl.shards > 1:
             hp.prepare(st)
@@ -122,7 +123,7 @@ def test_overlapped_input_refill_keeps_bits():
     # device-resident step's, bit for bit
     wl = MID
     st, cp = torch.cuda.Stream(), torch.cuda.Stream()
-    hp = S.HotPathStep(wl)
+    hp = S.HotPathStep(wl, dw_stream=True)   # inputs read on both streams
     with torch.cuda.stream(st):
         hp.prepare(st)
         hp.run(st)
