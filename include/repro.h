@@ -43,6 +43,10 @@
  *     when the arguments are invalid.  Device pointers must be 16-byte aligned.
  *   - The library allocates no device memory: calls that need scratch space
  *     take a caller-provided workspace and report its size through *_ws_bytes.
+ *     A workspace belongs to one call at a time: calls that may run at the
+ *     same time (on different streams) need different workspaces.  Calls on
+ *     different streams that touch different buffers may overlap freely; the
+ *     results do not depend on how they overlap.
  *   - The library keeps no state between calls except a per-device
  *     architecture check, the launch-configuration override and the device
  *     error word read by repro_device_check().
