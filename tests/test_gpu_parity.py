@@ -270,6 +270,36 @@ def test_backward_empty_reduction(orc):
     assert np.all(G.host(dx).view(np.uint32) == 0)
 
 
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7, 8])
+def test_zero_weights_and_activations_every_kernel(orc, kernel):
+    # all-zero W and X: both scales are +0, every code is 0, and every
+    # backward product is a signed zero, so the sign of each dX and dW element
+    # comes from the seeded chunk sums and the pairwise tree alone
+    # (+0 (+) -0 = +0, -0 (+) -0 = -0); rows and columns of dY that are
+    # entirely negative give -0 results, mixed ones +0
+    R.repro_set_launch_cfg(bwd_kernel=kernel)
+    rng = np.random.default_rng(41)
+    M, N, K = 130, 136, 32
+    w = np.zeros((N, K), np.float32)
+    x = np.zeros((M, K), np.float32)
+    x[3, :4] = -0.0
+    s_w = G.gpu_scale(w, 0)
+    s_x = G.gpu_scale(x, 1)
+    G.assert_bits_equal(np.float32(s_w), orc.wscale(w, 0), "s_w of zeros")
+    G.assert_bits_equal(np.float32(s_x), orc.wscale(x, 1), "s_x of zeros")
+    wq, xq = G.gpu_quant(w, s_w), G.gpu_quant(x, s_x)
+    assert not wq.any() and not xq.any()
+    dy = np.abs(rng.standard_normal((M, N))).astype(np.float32) * 1e-3
+    dy[::2] *= -1                                   # whole negative rows
+    dy[:, 7] = -np.abs(dy[:, 7])                    # a whole negative column
+    dy[5, :70] = -1e-3                              # negative across the first chunk only
+    G.assert_bits_equal(G.gpu_fwd(xq, wq, s_x, s_w), orc.linear_fwd(xq, wq, s_x, s_w), "fwd 0")
+    dx, dw = G.gpu_bwd(dy, xq, wq, s_x, s_w)
+    G.assert_bits_equal(dx, orc.linear_bwd_dx(dy, wq, s_w), f"dx of zero weights, kernel {kernel}")
+    G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, s_x), f"dw of zero activations, kernel {kernel}")
+    assert (dx.view(np.uint32) == 0x80000000).any() and (dx.view(np.uint32) == 0).any()
+
+
 # ----------------------------------------------------------------- reductions
 
 @pytest.mark.parametrize("n", [1, 3, 4, 5, 1000, 65536 + 3])
