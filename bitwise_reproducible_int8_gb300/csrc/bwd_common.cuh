@@ -44,4 +44,15 @@ template <bool DW>
 cudaError_t launch_bwd_tma(const BwdArgs& a, const int8_t* q, float* opnd, dim3 grid,
                            bool self_issue, cudaStream_t st);
 
+// tile heights of the staged wide variants (k_bwd_staged.cu): 3 and 4, and 5
+constexpr int BWD_WIDE_ROWS = 128;
+constexpr int BWD_WIDE12_ROWS = 192;
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// variants 0-5 (k_bwd_staged.cu): launches variant `kernel` over a's outputs,
+// grid (J tiles, I tiles, segments)
+template <bool DW>
+cudaError_t launch_bwd_staged(int kernel, const BwdArgs& a, cudaStream_t st);
+
 } // namespace repro
