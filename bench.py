@@ -380,6 +380,9 @@ def run_ours(args, wl):
         if fwd_ms > 0:
             other["fwd_int8"] = {"achieved_tops": fl["fwd_int_ops"] * args.steps / (fwd_ms / 1e3) / 1e12,
                                  "ms_per_step": fwd_ms / args.steps}
+            if hp.s_dw is not None:
+                other["fwd_int8"]["note"] = ("overlaps a dW on the other stream: a lower bound; "
+                                             "--no-dw-stream times it alone")
         gbytes = hbm_bytes(hp)
         for cls, nbytes in gbytes.items():
             c_ms = per_class.get(cls, 0.0)
