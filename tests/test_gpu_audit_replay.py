@@ -37,12 +37,12 @@ CONFIGS = [
 ]
 
 
-def _replay(host, cfg, steps=2):
+def _replay(host, cfg, steps=2, dw_stream=None):
     R.repro_set_launch_cfg(reset=True)
     if cfg:
         R.repro_set_launch_cfg(**cfg)
     try:
-        hp = S.HotPathStep(WL, host)
+        hp = S.HotPathStep(WL, host, dw_stream=dw_stream)
         st = torch.cuda.current_stream()
         hp.prepare(st)
         log = []
@@ -59,6 +59,7 @@ def _replay(host, cfg, steps=2):
 def test_replay_under_other_launch_configurations_gives_the_same_hashes():
     host = S.generate_host_inputs(WL)
     logs = [_replay(host, cfg) for cfg in CONFIGS]
+    logs.append(_replay(host, {}, dw_stream=True))   # dW on its own stream
     assert logs[0][0] != logs[0][1]            # the state moved
     for other in logs[1:]:
         assert other == logs[0]
