@@ -603,6 +603,32 @@ __device__ __forceinline__ void full_sum64(u64 (&pp)[4][4], const float* __restr
     }
 }
 
+// pp[q2][e] (+)= W[r][2q2 .. 2q2+1] (x) X[r][e] for r = lo .. hi, left to
+// right, when every row pair of the thread's block is valid and already seeded
+// over that range (the middle of a mask-edge tile); operands one step ahead
+__device__ __forceinline__ void packed_range(u64 (&pp)[4][4], const float* __restrict__ Wp, int pw,
+                                             const float* __restrict__ Xp, int px, int lo, int hi)
+{
+    ulonglong2 w03 = *reinterpret_cast<const ulonglong2*>(Wp + lo * pw);
+    ulonglong2 w47 = *reinterpret_cast<const ulonglong2*>(Wp + lo * pw + 4);
+    float4 xv = *reinterpret_cast<const float4*>(Xp + lo * px);
+#pragma unroll 4
+    for (int r = lo; r <= hi; ++r) {
+        const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
+        const u64 X2[4] = {pack2(xv.x, xv.x), pack2(xv.y, xv.y), pack2(xv.z, xv.z),
+                           pack2(xv.w, xv.w)};
+        const int rn = r < hi ? r + 1 : r;
+        w03 = *reinterpret_cast<const ulonglong2*>(Wp + rn * pw);
+        w47 = *reinterpret_cast<const ulonglong2*>(Wp + rn * pw + 4);
+        xv = *reinterpret_cast<const float4*>(Xp + rn * px);
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                pp[q2][e] = fadd2_ftz(pp[q2][e], fmul2_rn(P[q2], X2[e]));
+    }
+}
+
 __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
 {
     extern __shared__ __align__(16) float smb[];
@@ -770,47 +796,65 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             pp[q2][e] = 0ull;
-                    ulonglong2 n03 = {0ull, 0ull}, n47 = {0ull, 0ull};
-                    float4 nkv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (lo_all <= hi_all) {
-                        n03 = *reinterpret_cast<const ulonglong2*>(St + lo_all * PB + grp * 8);
-                        n47 = *reinterpret_cast<const ulonglong2*>(St + lo_all * PB + grp * 8 + 4);
-                        nkv = *reinterpret_cast<const float4*>(Ks + lo_all * PR + 4 * dg);
-                    }
-                    for (int jc = lo_all; jc <= hi_all; ++jc) {
-                        const ulonglong2 s03 = n03, s47 = n47;
-                        const float4 kv = nkv;
-                        const int jn = jc < hi_all ? jc + 1 : jc;
-                        n03 = *reinterpret_cast<const ulonglong2*>(St + jn * PB + grp * 8);
-                        n47 = *reinterpret_cast<const ulonglong2*>(St + jn * PB + grp * 8 + 4);
-                        nkv = *reinterpret_cast<const float4*>(Ks + jn * PR + 4 * dg);
-                        const u64 P[4] = {s03.x, s03.y, s47.x, s47.y};
-                        const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
+                    // keys [from, to] through the per-pair predicated steps
+                    auto edge_steps = [&](int from, int to) {
+                        ulonglong2 n03 = {0ull, 0ull}, n47 = {0ull, 0ull};
+                        float4 nkv = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (from <= to) {
+                            n03 = *reinterpret_cast<const ulonglong2*>(St + from * PB + grp * 8);
+                            n47 = *reinterpret_cast<const ulonglong2*>(St + from * PB + grp * 8 + 4);
+                            nkv = *reinterpret_cast<const float4*>(Ks + from * PR + 4 * dg);
+                        }
+                        for (int jc = from; jc <= to; ++jc) {
+                            const ulonglong2 s03 = n03, s47 = n47;
+                            const float4 kv = nkv;
+                            const int jn = jc < to ? jc + 1 : jc;
+                            n03 = *reinterpret_cast<const ulonglong2*>(St + jn * PB + grp * 8);
+                            n47 = *reinterpret_cast<const ulonglong2*>(St + jn * PB + grp * 8 + 4);
+                            nkv = *reinterpret_cast<const float4*>(Ks + jn * PR + 4 * dg);
+                            const u64 P[4] = {s03.x, s03.y, s47.x, s47.y};
+                            const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-                        for (int q2 = 0; q2 < 4; ++q2) {
-                            if (jc >= pb[q2] && jc <= pe[q2]) {
+                            for (int q2 = 0; q2 < 4; ++q2) {
+                                if (jc >= pb[q2] && jc <= pe[q2]) {
 #pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    pp[q2][e] = fadd2_ftz(pp[q2][e], fmul2_rn(P[q2], pack2(kk[e], kk[e])));
-                            } else {
-                                float sa, sb;
-                                unpack2(P[q2], sa, sb);
+                                    for (int e = 0; e < 4; ++e)
+                                        pp[q2][e] = fadd2_ftz(pp[q2][e], fmul2_rn(P[q2], pack2(kk[e], kk[e])));
+                                } else {
+                                    float sa, sb;
+                                    unpack2(P[q2], sa, sb);
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    float la, lb;
-                                    unpack2(pp[q2][e], la, lb);
-                                    if (jc >= jb[2 * q2] && jc <= je[2 * q2]) {
-                                        const float t = fmul_rn(sa, kk[e]);
-                                        la = jc == jb[2 * q2] ? flush(t) : fadd_ftz(la, t);
+                                    for (int e = 0; e < 4; ++e) {
+                                        float la, lb;
+                                        unpack2(pp[q2][e], la, lb);
+                                        if (jc >= jb[2 * q2] && jc <= je[2 * q2]) {
+                                            const float t = fmul_rn(sa, kk[e]);
+                                            la = jc == jb[2 * q2] ? flush(t) : fadd_ftz(la, t);
+                                        }
+                                        if (jc >= jb[2 * q2 + 1] && jc <= je[2 * q2 + 1]) {
+                                            const float t = fmul_rn(sb, kk[e]);
+                                            lb = jc == jb[2 * q2 + 1] ? flush(t) : fadd_ftz(lb, t);
+                                        }
+                                        pp[q2][e] = pack2(la, lb);
                                     }
-                                    if (jc >= jb[2 * q2 + 1] && jc <= je[2 * q2 + 1]) {
-                                        const float t = fmul_rn(sb, kk[e]);
-                                        lb = jc == jb[2 * q2 + 1] ? flush(t) : fadd_ftz(lb, t);
-                                    }
-                                    pp[q2][e] = pack2(la, lb);
                                 }
                             }
                         }
+                    };
+                    // keys where every pair takes the packed step run without the
+                    // per-pair tests (same operations); the ragged ends keep them
+                    int mid_lo = 0, mid_hi = AT - 1;
+#pragma unroll
+                    for (int q2 = 0; q2 < 4; ++q2) {
+                        mid_lo = max(mid_lo, pb[q2]);
+                        mid_hi = min(mid_hi, pe[q2]);
+                    }
+                    if (mid_lo <= mid_hi) {
+                        edge_steps(lo_all, mid_lo - 1);
+                        packed_range(pp, St + grp * 8, PB, Ks + 4 * dg, PR, mid_lo, mid_hi);
+                        edge_steps(mid_hi + 1, hi_all);
+                    } else {
+                        edge_steps(lo_all, hi_all);
                     }
 #pragma unroll
                     for (int q2 = 0; q2 < 4; ++q2)
@@ -879,47 +923,65 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
                                 pp[q2][e] = 0ull;
-                        ulonglong2 n03 = {0ull, 0ull}, n47 = {0ull, 0ull};
-                        float4 nxv = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (lo_all <= hi_all) {
-                            n03 = *reinterpret_cast<const ulonglong2*>(Wt + lo_all * PB + grp * 8);
-                            n47 = *reinterpret_cast<const ulonglong2*>(Wt + lo_all * PB + grp * 8 + 4);
-                            nxv = *reinterpret_cast<const float4*>(Xr + lo_all * PR + 4 * dg);
-                        }
-                        for (int ir = lo_all; ir <= hi_all; ++ir) {
-                            const ulonglong2 w03 = n03, w47 = n47;
-                            const float4 xv = nxv;
-                            const int rn = ir < hi_all ? ir + 1 : ir;
-                            n03 = *reinterpret_cast<const ulonglong2*>(Wt + rn * PB + grp * 8);
-                            n47 = *reinterpret_cast<const ulonglong2*>(Wt + rn * PB + grp * 8 + 4);
-                            nxv = *reinterpret_cast<const float4*>(Xr + rn * PR + 4 * dg);
-                            const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
-                            const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
+                        // query rows [from, to] through the per-pair predicated steps
+                        auto edge_steps = [&](int from, int to) {
+                            ulonglong2 n03 = {0ull, 0ull}, n47 = {0ull, 0ull};
+                            float4 nxv = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (from <= to) {
+                                n03 = *reinterpret_cast<const ulonglong2*>(Wt + from * PB + grp * 8);
+                                n47 = *reinterpret_cast<const ulonglong2*>(Wt + from * PB + grp * 8 + 4);
+                                nxv = *reinterpret_cast<const float4*>(Xr + from * PR + 4 * dg);
+                            }
+                            for (int ir = from; ir <= to; ++ir) {
+                                const ulonglong2 w03 = n03, w47 = n47;
+                                const float4 xv = nxv;
+                                const int rn = ir < to ? ir + 1 : ir;
+                                n03 = *reinterpret_cast<const ulonglong2*>(Wt + rn * PB + grp * 8);
+                                n47 = *reinterpret_cast<const ulonglong2*>(Wt + rn * PB + grp * 8 + 4);
+                                nxv = *reinterpret_cast<const float4*>(Xr + rn * PR + 4 * dg);
+                                const u64 P[4] = {w03.x, w03.y, w47.x, w47.y};
+                                const float xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                            for (int q2 = 0; q2 < 4; ++q2) {
-                                if (ir >= pb[q2] && ir <= pe[q2]) {
+                                for (int q2 = 0; q2 < 4; ++q2) {
+                                    if (ir >= pb[q2] && ir <= pe[q2]) {
 #pragma unroll
-                                    for (int e = 0; e < 4; ++e)
-                                        pp[q2][e] = fadd2_ftz(pp[q2][e], fmul2_rn(P[q2], pack2(xx[e], xx[e])));
-                                } else {
-                                    float wa, wb;
-                                    unpack2(P[q2], wa, wb);
+                                        for (int e = 0; e < 4; ++e)
+                                            pp[q2][e] = fadd2_ftz(pp[q2][e], fmul2_rn(P[q2], pack2(xx[e], xx[e])));
+                                    } else {
+                                        float wa, wb;
+                                        unpack2(P[q2], wa, wb);
 #pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        float la, lb;
-                                        unpack2(pp[q2][e], la, lb);
-                                        if (ir >= ib[2 * q2] && ir <= ie[2 * q2]) {
-                                            const float t = fmul_rn(wa, xx[e]);
-                                            la = ir == ib[2 * q2] ? flush(t) : fadd_ftz(la, t);
+                                        for (int e = 0; e < 4; ++e) {
+                                            float la, lb;
+                                            unpack2(pp[q2][e], la, lb);
+                                            if (ir >= ib[2 * q2] && ir <= ie[2 * q2]) {
+                                                const float t = fmul_rn(wa, xx[e]);
+                                                la = ir == ib[2 * q2] ? flush(t) : fadd_ftz(la, t);
+                                            }
+                                            if (ir >= ib[2 * q2 + 1] && ir <= ie[2 * q2 + 1]) {
+                                                const float t = fmul_rn(wb, xx[e]);
+                                                lb = ir == ib[2 * q2 + 1] ? flush(t) : fadd_ftz(lb, t);
+                                            }
+                                            pp[q2][e] = pack2(la, lb);
                                         }
-                                        if (ir >= ib[2 * q2 + 1] && ir <= ie[2 * q2 + 1]) {
-                                            const float t = fmul_rn(wb, xx[e]);
-                                            lb = ir == ib[2 * q2 + 1] ? flush(t) : fadd_ftz(lb, t);
-                                        }
-                                        pp[q2][e] = pack2(la, lb);
                                     }
                                 }
                             }
+                        };
+                        // rows where every pair takes the packed step run without the
+                        // per-pair tests (same operations); the ragged ends keep them
+                        int mid_lo = 0, mid_hi = AT - 1;
+#pragma unroll
+                        for (int q2 = 0; q2 < 4; ++q2) {
+                            mid_lo = max(mid_lo, pb[q2]);
+                            mid_hi = min(mid_hi, pe[q2]);
+                        }
+                        if (mid_lo <= mid_hi) {
+                            edge_steps(lo_all, mid_lo - 1);
+                            packed_range(pp, Wt + grp * 8, PB, Xr + 4 * dg, PR, mid_lo, mid_hi);
+                            edge_steps(mid_hi + 1, hi_all);
+                        } else {
+                            edge_steps(lo_all, hi_all);
                         }
 #pragma unroll
                         for (int q2 = 0; q2 < 4; ++q2)
