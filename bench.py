@@ -456,11 +456,13 @@ def hbm_bytes(hp) -> dict:
 
 def measure_e2e(hp, host, steps, stream, world):
     """Same steps through the public API with host buffers: every step copies
-    its inputs from pinned host memory (weights, then each micro-batch's X and
-    dY, on a copy stream) and reads the result back.  Each input buffer is
-    refilled as soon as the previous step has read it for the last time, so
-    step s+1's copies overlap step s's later micro-batches; with the optimizer
-    on, the weights wait for the whole previous step (it updates them)."""
+    its inputs from pinned host memory (micro-batch 0's X and dY, the weights,
+    then the other micro-batches, on a copy stream) and reads the result back.  X and dY are double
+    buffered across steps: step s+1 copies into the set step s-1 used, as soon
+    as step s-1 has read each buffer for the last time, so its copies overlap
+    step s.  The weights are one buffer, refilled once the previous step's
+    scale and quantise calls have read them (with the optimizer on, once the
+    whole previous step is done, since it updates them)."""
     import torch
     L, J = len(hp.wl.linears), hp.wl.microbatches
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
@@ -473,31 +475,45 @@ def measure_e2e(hp, host, steps, stream, world):
         sum(t.numel() * 4 for r in hdY for t in r)
     d2h = res.numel() * 4
     copy = torch.cuda.Stream()
-    prev_done = [None]
+    sets = [(hp.X, hp.dY),
+            ([[torch.empty_like(t) for t in row] for row in hp.X],
+             [[torch.empty_like(t) for t in row] for row in hp.dY])]
+    torch.cuda.synchronize()
+    released = [None, None]   # per buffer set: the release events of its last step
+    w_released = [None]
+    count = [0]
 
     def one_step():
-        evs = []
+        k = count[0]
+        count[0] += 1
+        hp.X, hp.dY = sets[k % 2]
+        prev = released[k % 2]
+        evs = [None] * J
         done = [None] * (J + 1)
         with torch.cuda.stream(copy):
-            if prev_done[0] is None or hp.use_optimizer:
+            if k == 0:
                 copy.wait_stream(stream)
-            else:
-                for ev in prev_done[0][J]:
-                    copy.wait_event(ev)
-            for i in range(L):
-                hp.W[i].copy_(hW[i], non_blocking=True)
             for j in range(J):
-                if prev_done[0] is not None and not hp.use_optimizer:
-                    for ev in prev_done[0][j]:
+                if prev is not None:
+                    for ev in prev[j]:
                         copy.wait_event(ev)
                 for i in range(L):
                     hp.X[i][j].copy_(hX[i][j], non_blocking=True)
                     hp.dY[i][j].copy_(hdY[i][j], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(copy)
-                evs.append(e)
+                if j == 0:
+                    # the weights right after micro-batch 0: the step starts with them
+                    if hp.use_optimizer:
+                        copy.wait_stream(stream)
+                    elif w_released[0] is not None:
+                        for ev in w_released[0]:
+                            copy.wait_event(ev)
+                    for i in range(L):
+                        hp.W[i].copy_(hW[i], non_blocking=True)
+                evs[j] = torch.cuda.Event()
+                evs[j].record(copy)
         hp.run(stream, wait_events=evs, done_events=done)
-        prev_done[0] = done
+        released[k % 2] = done
+        w_released[0] = done[J]
         with torch.cuda.stream(stream):
             out_host.copy_(res, non_blocking=True)
 
@@ -607,6 +623,7 @@ def run_attn(args, aw):
     ws_b = torch.empty(R.repro_attn_bwd_ws_bytes(B, T, Hq), dtype=torch.uint8, device=dev)
     ws_f = torch.empty(max(R.repro_attn_fwd_ws_bytes(B, T, Hq, aw.window), 16), dtype=torch.uint8,
                        device=dev)   # the forward's logit cache
+    dev_bufs = (tq, tk, tv, tdo, dq, dk, dv)
     torch.cuda.synchronize()   # s_v's fill ran on the default stream
     stream = torch.cuda.Stream()
     timers = {}
@@ -621,7 +638,8 @@ def run_attn(args, aw):
         e.record(stream)
         timers[cls][-1][1] = e
 
-    def one_step(timed):
+    def one_step(timed, bufs=None):
+        tq, tk, tv, tdo, dq, dk, dv = bufs if bufs is not None else dev_bufs
         if timed:
             ev("vscale")
         R.repro_wscale(tv, R.REPRO_SCALE_ACT_AMAX, s_v, ws=ws_s, stream=stream)
@@ -670,28 +688,58 @@ def run_attn(args, aw):
     value = whole_job_tokens_per_s(aw.tokens, args.steps, world, ms_max)
 
     # e2e: every step copies q, k, v, dO from pinned host memory and reads dq,
-    # dk, dv back, through the same calls
+    # dk, dv back, through the same calls.  Inputs and outputs are double
+    # buffered across steps: step s+1's uploads (copy stream) overlap step s,
+    # step s's downloads (a third stream) overlap step s+1, and a buffer set is
+    # refilled or rewritten only once step s-1 (its last user) is done with it
     e2e = None
     if not args.no_e2e:
         hq, hk, hv, hdo = (torch.from_numpy(x).pin_memory() for x in (q, k, v, do))
         hdq = torch.empty(dq.shape).pin_memory()
         hdk = torch.empty(dk.shape).pin_memory()
         hdv = torch.empty(dv.shape).pin_memory()
-        with torch.cuda.stream(stream):
-            a0 = torch.cuda.Event(enable_timing=True)
-            a1 = torch.cuda.Event(enable_timing=True)
-            a0.record(stream)
-            for _ in range(args.steps):
-                tq.copy_(hq, non_blocking=True)
-                tk.copy_(hk, non_blocking=True)
-                tv.copy_(hv, non_blocking=True)
-                tdo.copy_(hdo, non_blocking=True)
-                one_step(False)
-                hdq.copy_(dq, non_blocking=True)
-                hdk.copy_(dk, non_blocking=True)
-                hdv.copy_(dv, non_blocking=True)
-            a1.record(stream)
+        # the inputs are the same every step: the last download must equal the
+        # device-resident step's gradients, bit for bit
+        expect = [t.detach().cpu().clone() for t in dev_bufs[4:]]
+        sets = [dev_bufs, tuple(torch.empty_like(t) for t in dev_bufs)]
+        up, down = torch.cuda.Stream(), torch.cuda.Stream()
+        torch.cuda.synchronize()
+        in_free, out_free = [None, None], [None, None]
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        up.wait_stream(stream)
+        last_down = None
+        for step in range(args.steps):
+            cur = sets[step % 2]
+            with torch.cuda.stream(up):
+                if in_free[step % 2] is not None:
+                    up.wait_event(in_free[step % 2])
+                for d, h in zip(cur[:4], (hq, hk, hv, hdo)):
+                    d.copy_(h, non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(up)
+            stream.wait_event(ready)
+            if out_free[step % 2] is not None:
+                stream.wait_event(out_free[step % 2])
+            with torch.cuda.stream(stream):
+                one_step(False, cur)
+                done = torch.cuda.Event()
+                done.record(stream)
+            in_free[step % 2] = done
+            with torch.cuda.stream(down):
+                down.wait_event(done)
+                for h, d in zip((hdq, hdk, hdv), cur[4:]):
+                    h.copy_(d, non_blocking=True)
+                last_down = torch.cuda.Event()
+                last_down.record(down)
+            out_free[step % 2] = last_down
+        stream.wait_event(last_down)
+        a1.record(stream)
         stream.synchronize()
+        for h, e in zip((hdq, hdk, hdv), expect):
+            if not torch.equal(h.view(torch.int32), e.view(torch.int32)):
+                raise RuntimeError("end-to-end attention steps changed the gradient bits")
         e_ms = a0.elapsed_time(a1)
         e2e = {"value": whole_job_tokens_per_s(aw.tokens, args.steps, world,
                                                max_over_ranks(e_ms, world, "cuda")),
