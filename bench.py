@@ -482,6 +482,10 @@ def measure_e2e(hp, host, steps, stream, world):
     released = [None, None]   # per buffer set: the release events of its last step
     w_released = [None]
     count = [0]
+    # the TreeFold output is rewritten only at the end of the next step, so its
+    # read-back runs on a stream of its own and that step's TreeFold waits for it
+    down = torch.cuda.Stream() if hp.TF is not None else None
+    read_done = [None]
 
     def one_step():
         k = count[0]
@@ -511,11 +515,21 @@ def measure_e2e(hp, host, steps, stream, world):
                         hp.W[i].copy_(hW[i], non_blocking=True)
                 evs[j] = torch.cuda.Event()
                 evs[j].record(copy)
-        hp.run(stream, wait_events=evs, done_events=done)
+        hp.run(stream, wait_events=evs, done_events=done,
+               fold_wait_events=[read_done[0]] if read_done[0] is not None else None)
         released[k % 2] = done
         w_released[0] = done[J]
-        with torch.cuda.stream(stream):
-            out_host.copy_(res, non_blocking=True)
+        if down is None:
+            with torch.cuda.stream(stream):
+                out_host.copy_(res, non_blocking=True)
+        else:
+            step_end = torch.cuda.Event()
+            step_end.record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(step_end)
+                out_host.copy_(res, non_blocking=True)
+                read_done[0] = torch.cuda.Event()
+                read_done[0].record(down)
 
     # the inputs are the same every step, so every step's result must equal
     # the device-resident step's, bit for bit (a refill that raced a read
@@ -530,6 +544,8 @@ def measure_e2e(hp, host, steps, stream, world):
     a.record(stream)
     for _ in range(steps):
         one_step()
+    if read_done[0] is not None:
+        stream.wait_event(read_done[0])   # the last read-back is inside the timed region
     b.record(stream)
     stream.synchronize()
     if expect is not None and not torch.equal(out_host.view(torch.int32), expect.view(torch.int32)):

@@ -158,7 +158,8 @@ class HotPathStep:
         timers[cls][-1][1] = e
 
     def run(self, stream: torch.cuda.Stream, timers: dict | None = None,
-            wait_events: list | None = None, done_events: list | None = None) -> None:
+            wait_events: list | None = None, done_events: list | None = None,
+            fold_wait_events: list | None = None) -> None:
         """Enqueue one step on `stream` (and, with dw_stream, its dW calls on
         the step's second stream, joined back before the folds).  With
         `timers`, records a CUDA event pair around every call, grouped by call
@@ -169,7 +170,9 @@ class HotPathStep:
         micro-batch j's X and dY are no longer read, and in slot J those for
         the weights W (read only by the scale and quantise calls at the start
         of the step), so a producer can refill each input as soon as this step
-        is done with it."""
+        is done with it.  `fold_wait_events`, if given, are waited on before
+        TreeFold rewrites its output (a reader of the previous step's result
+        may still be copying it out)."""
         wl, s = self.wl, stream
         L, J = len(wl.linears), wl.microbatches
         s2 = self.s_dw
@@ -238,6 +241,8 @@ class HotPathStep:
             self._end(timers, "running_sum", s)
             level2 = self.G2
         if self.TF is not None and not getattr(self, "skip_treefold", False):
+            for ev in fold_wait_events or ():
+                s.wait_event(ev)
             if self.parts is None:
                 raise RuntimeError("prepare_replicas() must run before a step with TreeFold")
             self._ev(timers, "treefold", s)
