@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
             } else {
                 logits4x4(s, Qt, Kt, ty, tx, a.c);
             }
+            float pv[16];   // this thread's p, in the cache's layout (pair e, lane h at 2e + h)
 #pragma unroll
             for (int ip = 0; ip < 2; ++ip)
 #pragma unroll
@@ -336,10 +337,19 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
                         if (i < T && jj >= lo && jj <= i)
                             p = exp_r(fadd_ftz(lane_of(s, ip, j, hh), -m));
                         Ps[r * PS + 4 * tx + j] = p;
+                        pv[2 * (ip * 4 + j) + hh] = p;
                         word |= (uint32_t)quant_p(p) << (8 * j);
                     }
                     Pp[r * PP + tx] = (int)word;
                 }
+            if (cache) {
+                // the cache now holds p in place of each logit: the backward
+                // reads p from it instead of evaluating e^x again
+                float4* dst = reinterpret_cast<float4*>(cache + (t - t_lo) * (AT * AT) + tid * 16);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_float4(pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3]);
+            }
         }
         __syncthreads();
         // row sums: the valid p of this tile, left to right, through the
@@ -711,9 +721,10 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
             {
                 float sv[4][4], dav[4][4];
                 if (a.lcache) {
-                    // the forward's logits of this (query tile, key tile): forward
-                    // thread f = (i/4)*16 + j/4 holds pair (2*((i%4)/2) + ..) -- float
-                    // f*16 + 2*(((i%4)/2)*4 + j%4) + i%2, already scaled by c
+                    // the forward's cache of this (query tile, key tile), which holds
+                    // p_ij = e^(s_ij - m_i) once the forward has run: forward thread
+                    // f = (i/4)*16 + j/4 keeps pair (i, j) at float
+                    // f*16 + 2*(((i%4)/2)*4 + j%4) + i%2
                     const int64_t qt = i0 / AT;
                     const int64_t tlo = (W > 0 ? max((int64_t)0, i0 - W + 1) : (int64_t)0) / AT;
                     const float* tile = a.lcache + ((b * Hq + h) * a.tiles_bh + tile_prefix(qt, W) +
@@ -740,8 +751,9 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                         const int64_t j = j0 + jc;
                         float av = 0.f, dsv = 0.f;
                         if (i < T && j <= i && (W == 0 || i - j < W)) {
-                            const float s = a.lcache ? sv[r][cc] : fmul_flush(sv[r][cc], c);
-                            const float p = exp_r(fadd_ftz(s, -rm[ir]));
+                            // with the forward's cache, sv already holds p
+                            const float p = a.lcache ? sv[r][cc]
+                                                     : exp_r(fadd_ftz(fmul_flush(sv[r][cc], c), -rm[ir]));
                             av = flush(__fdiv_rn(p, rl[ir]));
                             dsv = fmul_flush(av, fadd_ftz(dav[r][cc], -rd[ir]));
                         }

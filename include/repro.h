@@ -251,8 +251,9 @@ int repro_adamw_step(float* p, float* m, float* v, const float* g, int64_t n,
  * o, m, l must not overlap the inputs or each other (REPRO_ERR_ALIAS).
  * The exact maximum needs the logits twice.  ws (optional, DEVICE): with at
  * least repro_attn_fwd_ws_bytes(B, T, Hq, W) bytes the first pass stores its
- * logits there and the second reads them back; with ws == NULL the second pass
- * recomputes them.  Same bits either way.  The cache holds every visited
+ * logits there and the second reads them back and replaces each by
+ * p_ij = e^(s_ij - m_i) (0 for masked pairs), which repro_attn_bwd can reuse;
+ * with ws == NULL the second pass recomputes the logits.  Same bits either way.  The cache holds every visited
  * 64 x 64 logit tile: about 4 * 64 * (W + 64) bytes per query row and head for a
  * window W, 2 * T bytes per query row and head for full causal.
  * ------------------------------------------------------------------------ */
@@ -286,9 +287,9 @@ size_t repro_attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);
  * m, l; outputs dq [B][T][Hq][128], dk, dv [B][T][Hkv][128] (DEVICE, 16-byte
  * aligned, no overlaps).  ws: repro_attn_bwd_ws_bytes(B, T, Hq) bytes (the
  * int64 dQ accumulator and the Dr_i), not overlapping anything else.
- * fwd_ws (optional): the logit cache repro_attn_fwd filled for these same
- * inputs, unchanged since; the backward then reads s_ij from it instead of
- * recomputing them (same bits).  NULL recomputes.
+ * fwd_ws (optional): the cache repro_attn_fwd filled for these same inputs,
+ * unchanged since; the backward then reads p_ij from it instead of computing
+ * the logits and e^x again (same bits).  NULL recomputes.
  * ------------------------------------------------------------------------ */
 int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                    const float* o, const float* dout, const float* m, const float* l,
