@@ -128,6 +128,56 @@ def test_attn_bwd_matches_oracle(orc, B, T, Hq, Hkv, W, logits):
     G.assert_bits_equal(dq, rq, f"dq T={T} W={W}")
 
 
+@pytest.mark.parametrize("logits", ["recomputed", "cached"])
+@pytest.mark.parametrize("W", [63, 65, 127, 128, 129, 192])
+@pytest.mark.parametrize("B,T,Hq,Hkv", [(1, 300, 4, 2), (2, 257, 4, 1)])
+def test_attn_bwd_windows_around_tile_multiples(orc, B, T, Hq, Hkv, W, logits):
+    # a window edge just below, on and above a multiple of the 64-row tile
+    # moves where each warp's fully valid middle range starts and ends
+    q, k, vq, s_v = _case(B * 7 + T + W, B, T, Hq, Hkv)
+    fwd_ws = None
+    if logits == "cached":
+        o, m, l, fwd_ws = gpu_attn_fwd(q, k, vq, s_v, W, keep_cache=True)
+    else:
+        o, m, l = orc.attn_fwd(q, k, vq, s_v, W)
+    dout = (np.random.default_rng(W).standard_normal(o.shape) * 1e-3).astype(np.float32)
+    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=fwd_ws)
+    rq, rk, rv = orc.attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    G.assert_bits_equal(dv, rv, f"dv T={T} W={W}")
+    G.assert_bits_equal(dk, rk, f"dk T={T} W={W}")
+    G.assert_bits_equal(dq, rq, f"dq T={T} W={W}")
+
+
+@pytest.mark.parametrize("W", [0, 100])
+def test_attn_bwd_underflowing_probabilities(orc, W):
+    # logits spread over hundreds: most p underflow to 0, so a and dS are
+    # exact zeros and many backward terms are signed zeros, which the canonical
+    # sums must keep with their signs
+    B, T, Hq, Hkv = 1, 200, 4, 2
+    q, k, vq, s_v = _case(91 + W, B, T, Hq, Hkv)
+    q *= np.float32(40.0)
+    o, m, l, fwd_ws = gpu_attn_fwd(q, k, vq, s_v, W, keep_cache=True)
+    ro, rm, rl = orc.attn_fwd(q, k, vq, s_v, W)
+    G.assert_bits_equal(o, ro, "o")
+    dout = (np.random.default_rng(5).standard_normal(o.shape) * 1e-3).astype(np.float32)
+    rq, rk, rv = orc.attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    for fws in (fwd_ws, None):
+        dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=fws)
+        G.assert_bits_equal(dv, rv, "dv")
+        G.assert_bits_equal(dk, rk, "dk")
+        G.assert_bits_equal(dq, rq, "dq")
+    # the regime is real: many valid pairs sit far below their row maximum,
+    # where e^(s - m) is an exact 0 in binary32 (checked in float64 here)
+    g = np.arange(Hq) // (Hq // Hkv)
+    s = np.einsum("bthd,bjhd->bhtj", q.astype(np.float64), k[:, :, g].astype(np.float64))
+    s /= np.sqrt(128.0)
+    t, j = np.arange(T)[:, None], np.arange(T)[None, :]
+    valid = (j <= t) & ((W == 0) | (t - j < W))
+    s = np.where(valid, s, -np.inf)
+    below = (s - s.max(axis=-1, keepdims=True)) < -110.0
+    assert below[..., valid].mean() > 0.3
+
+
 @pytest.mark.parametrize("W", [512, 0])
 def test_attn_bwd_full_size_sampled(orc, W):
     B, T, Hq, Hkv = 4, 4096, 16, 4
