@@ -47,19 +47,34 @@ k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __re
     const int cnt = (int)min((int64_t)nb, C - c0);
     const int64_t e0 = c0 * 64;
 
-    for (int g = threadIdx.x; g < cnt * 16; g += blockDim.x) {
-        const int ch = g >> 4, p = g & 15;
-        const int64_t e = e0 + (int64_t)g * 4;
-        float4 v;
-        if (e + 4 <= n) {
-            v = __ldg(reinterpret_cast<const float4*>(x + e));
-        } else {
-            v.x = (e + 0 < n) ? x[e + 0] : 0.f;
-            v.y = (e + 1 < n) ? x[e + 1] : 0.f;
-            v.z = (e + 2 < n) ? x[e + 2] : 0.f;
-            v.w = (e + 3 < n) ? x[e + 3] : 0.f;
+    if (cnt == P1_CHUNKS && blockDim.x == P1_CHUNKS && e0 + P1_CHUNKS * 64 <= n) {
+        // a full block: all 16 of the thread's loads in flight before any store
+        float4 v[16];
+        const float4* x4 = reinterpret_cast<const float4*>(x + e0);
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            v[u] = __ldg(x4 + threadIdx.x + u * P1_CHUNKS);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int g = threadIdx.x + u * P1_CHUNKS;
+            const int ch = g >> 4, p = g & 15;
+            S[ch * 16 + (p ^ (ch & 15))] = v[u];
         }
-        S[ch * 16 + (p ^ (ch & 15))] = v;
+    } else {
+        for (int g = threadIdx.x; g < cnt * 16; g += blockDim.x) {
+            const int ch = g >> 4, p = g & 15;
+            const int64_t e = e0 + (int64_t)g * 4;
+            float4 v;
+            if (e + 4 <= n) {
+                v = __ldg(reinterpret_cast<const float4*>(x + e));
+            } else {
+                v.x = (e + 0 < n) ? x[e + 0] : 0.f;
+                v.y = (e + 1 < n) ? x[e + 1] : 0.f;
+                v.z = (e + 2 < n) ? x[e + 2] : 0.f;
+                v.w = (e + 3 < n) ? x[e + 3] : 0.f;
+            }
+            S[ch * 16 + (p ^ (ch & 15))] = v;
+        }
     }
     __syncthreads();
 
@@ -157,8 +172,20 @@ k_amax_partial(const float* __restrict__ x, int64_t n, float* __restrict__ part)
     float m = 0.f;
     const int64_t nv = n >> 2;
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
-         i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // four independent loads in flight per step (the maximum is order-free)
+    for (; i + 3 * stride < nv; i += 4 * stride) {
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            v[u] = __ldg(x4 + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            m = fmaxf(m, fmaxf(fmaxf(absflush(v[u].x), absflush(v[u].y)),
+                               fmaxf(absflush(v[u].z), absflush(v[u].w))));
+    }
+    for (; i < nv; i += stride) {
         const float4 v = __ldg(x4 + i);
         m = fmaxf(m, fmaxf(fmaxf(absflush(v.x), absflush(v.y)), fmaxf(absflush(v.z), absflush(v.w))));
     }
