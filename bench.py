@@ -247,8 +247,8 @@ def run_ours(args, wl):
 
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
-    if args.bwd_kernel >= 0:
-        R.repro_set_launch_cfg(bwd_kernel=args.bwd_kernel)
+    if args.bwd_kernel >= 0 or args.fwd_path >= 0:
+        R.repro_set_launch_cfg(bwd_kernel=args.bwd_kernel, fwd_path=args.fwd_path)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     if rank == 0 or not os.path.exists(build_lib.LIB):
@@ -868,6 +868,8 @@ def main(argv=None):
                          "(launch-bound workloads; not with the optimizer)")
     ap.add_argument("--bwd-kernel", type=int, default=-1,
                     help="backward kernel variant (launch-configuration hook; -1: default)")
+    ap.add_argument("--fwd-path", type=int, default=-1,
+                    help="forward path (launch-configuration hook; -1: default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-frac-log2", type=int, default=10,
                     help="the oracle's timed sample is 2^-k of one step's work")

@@ -158,7 +158,7 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
         return REPRO_ERR_ARG;
     if (cfg->reduce_block_log2 < -1 || cfg->reduce_block_log2 > 10)
         return REPRO_ERR_ARG;
-    if (cfg->fwd_path < -1 || cfg->fwd_path > 1)
+    if (cfg->fwd_path < -1 || cfg->fwd_path > 2)
         return REPRO_ERR_ARG;
     if (cfg->elementwise_blocks < -1 || cfg->elementwise_blocks > (1 << 20))
         return REPRO_ERR_ARG;
@@ -314,7 +314,8 @@ int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x, const
     if (st != REPRO_OK)
         return st;
     if (tc)
-        return status_of(launch_fwd_tc(xq, wq, s_x, s_w, y, M, N, K, ws, as_stream(stream)));
+        return status_of(launch_fwd_tc(xq, wq, s_x, s_w, y, M, N, K, ws, g_cfg.fwd_path != 2,
+                                       as_stream(stream)));
     return status_of(launch_fwd_cuda_core(xq, wq, s_x, s_w, y, M, N, K, as_stream(stream)));
 }
 

@@ -13,7 +13,7 @@ namespace repro {
 struct LaunchCfg {
     int bwd_segment_log2;   // chunks per backward reduction segment = 2^k (0..8)
     int reduce_block_log2;  // chunk partials per block in the scale reduction (0..10)
-    int fwd_path;           // 0: CUDA-core exact path, 1: tensor-core path
+    int fwd_path;           // 0: CUDA-core exact path, 1: tensor cores 128 x 256 tiles, 2: 128 x 128
     int elementwise_blocks; // 0: default grid for streaming kernels
     int bwd_kernel;         // 0: plain backward kernel, 1: pipelined packed kernel
 };
@@ -56,7 +56,8 @@ cudaError_t launch_fwd_cuda_core(const int8_t* xq, const int8_t* wq, const float
 bool fwd_tc_supported(int64_t M, int64_t N, int64_t K);
 size_t fwd_tc_ws_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_fwd_tc(const int8_t* xq, const int8_t* wq, const float* s_x, const float* s_w,
-                          float* y, int64_t M, int64_t N, int64_t K, void* ws, cudaStream_t st);
+                          float* y, int64_t M, int64_t N, int64_t K, void* ws, bool wide,
+                          cudaStream_t st);
 
 // ---- backward (k_bwd.cu)
 size_t bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int seg_log2);

@@ -10,22 +10,32 @@
 // its integer exactly; the epilogue converts every slice to int32 and adds the
 // slices exactly.  Y = (float(acc) (x) s_x) (x) s_w, two flushed multiplies.
 //
-// Kernel structure (one 128 x 128 output tile per CTA, two CTAs per SM):
-//   warp 0      TMA producer: bf16 A/B tiles of 128 rows x 64 K, 128-byte
-//               swizzle, 3-stage ring (full/empty mbarriers);
-//   warp 1      allocates 256 TMEM columns (two 128-column fp32 accumulators)
-//               and one thread issues the MMAs (M=128, N=128, K=16), committing
-//               each stage back to the producer and each K-slice to the
-//               epilogue;
-//   warps 2-5   epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (its rows),
-//               converts the slice to int32 and accumulates in registers, then
-//               frees the accumulator for the slice after next.
+// Kernel structure: persistent, one CTA per SM, each CTA walking output tiles
+// of 128 rows x TN columns (TN = 128 or 256) in a fixed round-robin order:
+//   warp 0      TMA producer: bf16 A (128 x 64 K) and B (TN x 64 K) tiles,
+//               128-byte swizzle, a ring of 192 KB of stages (full/empty
+//               mbarriers), running straight on into the next tile;
+//   warp 1      allocates all 512 TMEM columns as 512/TN fp32 accumulators of
+//               TN columns, used in turn by consecutive K-slices of consecutive
+//               tiles; one thread issues the MMAs (M=128, N=TN, K=16),
+//               committing each stage back to the producer and each K-slice to
+//               the epilogue, so the next tile's products start while the
+//               epilogue is still converting and storing the last one;
+//   warps 2..   epilogue, TN/32 warps: warp w reads TMEM lanes 32*(w%4) .. +31
+//               (its rows) and 128 of the tile's columns, converts each slice
+//               to int32 and accumulates in registers, frees the accumulator,
+//               and at the tile's end scales, stages 32 x 32 blocks in its own
+//               128-byte-swizzled shared buffer and writes them with TMA tensor
+//               stores that drain while the next tile computes.
 // Every wait is bounded (about two seconds of clock64); on expiry the kernel
 // records an error in the device error word, lets in-flight copies land,
 // frees tensor memory and returns.  repro_device_check reports it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -35,23 +45,35 @@ namespace repro {
 namespace {
 
 constexpr int TM = 128;            // tile rows (M)
-constexpr int TN = 128;            // tile columns (N)
 constexpr int TK = 64;             // K per stage: one 128-byte swizzle row of bf16
-constexpr int STAGES = 3;
 constexpr int SLICE_KB = 8;        // k-blocks per exact slice: 8 * 64 = 512
-constexpr int TILE_BYTES = TM * TK * 2;   // 16 KB, the same for A and B
-constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;
-constexpr size_t SMEM_BYTES = 1024 + 2 * STAGES * TILE_BYTES + 256;
-constexpr int EPI_PITCH = TN + 4;  // floats per staged output row (conflict-free both ways)
-static_assert(4 * 32 * EPI_PITCH * 4 <= 2 * STAGES * TILE_BYTES,
-              "the epilogue staging must fit in the operand ring");
+constexpr int A_BYTES = TM * TK * 2;   // 16 KB
+constexpr int RING_BYTES = 192 * 1024;
+constexpr int STG_BYTES = 32 * 32 * 4;  // one epilogue warp's 32 x 32 fp32 staging block
+constexpr uint32_t TMEM_COLS = 512;
 
+// tile width TN = 128 (6 stages, 4 accumulators, 4 epilogue warps) or 256
+// (4 stages, 2 accumulators, 8 epilogue warps, a quarter fewer operand bytes
+// per multiply); each epilogue warp owns 32 rows x 128 columns of a tile
+template <int TN>
+struct Cfg {
+    static constexpr int B_BYTES = TN * TK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = RING_BYTES / STAGE_BYTES;
+    static constexpr int NBUF = (int)TMEM_COLS / TN;
+    static constexpr int EPI_WARPS = TN / 32;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr size_t SMEM_BYTES = 1024 + (size_t)RING_BYTES + EPI_WARPS * STG_BYTES + 256;
+    static_assert(STAGES * STAGE_BYTES == RING_BYTES, "whole stages");
+    static_assert(SMEM_BYTES <= 227 * 1024, "fits one SM's shared memory");
+};
+
+constexpr int MAX_STAGES = 6, MAX_BUF = 4;
 struct Smem {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t dfull[2];
-    uint64_t dempty[2];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
+    uint64_t dfull[MAX_BUF];
+    uint64_t dempty[MAX_BUF];
     uint64_t done;
     uint32_t tmem_base;
     int failed;
@@ -66,17 +88,22 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
 }
 
 // instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = 128, M = 128
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TN >> 3) << 17) |
-                           ((uint32_t)(TM >> 4) << 24);
+// K-major, N = TN, M = 128
+template <int TN>
+__host__ __device__ constexpr uint32_t idesc()
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TN >> 3) << 17) |
+           ((uint32_t)(TM >> 4) << 24);
+}
 
+template <int TN>
 __device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t acc)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
-        "l"(a), "l"(b), "r"(IDESC), "r"(acc)
+        "l"(a), "l"(b), "r"(idesc<TN>()), "r"(acc)
         : "memory");
 }
 
@@ -104,22 +131,60 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : R8(0), R8(8)
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
 #undef R8
 
-__global__ void __launch_bounds__(THREADS, 2)
-k_fwd_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-         const float* __restrict__ s_x, const float* __restrict__ s_w, float* __restrict__ y,
-         int M, int N, int K, int* __restrict__ err)
+// 32 x 32 fp32 block from shared memory (128-byte swizzle) to Y at column x,
+// row yr; the tensor map clips the parts beyond M and N
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int yr)
 {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(yr), "r"(su32(src))
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// tile t of the CTA's round-robin walk, row-major over (row block, column block)
+__device__ __forceinline__ void tile_origin(int t, int tiles_n, int tn, int& m0, int& n0)
+{
+    m0 = (t / tiles_n) * TM;
+    n0 = (t % tiles_n) * tn;
+}
+
+// shared memory admits one CTA per SM; the second bound only caps the narrow
+// tile's registers at the wide tile's 168, which keeps both free of spills
+template <int TN>
+__global__ void __launch_bounds__(Cfg<TN>::THREADS, TN == 128 ? 2 : 1)
+k_fwd_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+         const __grid_constant__ CUtensorMap map_y, int y_tma, const float* __restrict__ s_x,
+         const float* __restrict__ s_w, float* __restrict__ y, int M, int N, int K,
+         int* __restrict__ err)
+{
+    using C = Cfg<TN>;
+    constexpr int STAGES = C::STAGES, NBUF = C::NBUF;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte-swizzled tiles need 1024-byte alignment in the shared window
     uint8_t* base = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
     uint8_t* A = base;                                   // STAGES x 16 KB
-    uint8_t* B = base + STAGES * TILE_BYTES;             // STAGES x 16 KB
-    Smem* sm = reinterpret_cast<Smem*>(base + 2 * STAGES * TILE_BYTES);
+    uint8_t* B = base + STAGES * A_BYTES;                // STAGES x TN/128 x 16 KB
+    uint8_t* STG = base + RING_BYTES;                    // EPI_WARPS x 4 KB
+    Smem* sm = reinterpret_cast<Smem*>(STG + C::EPI_WARPS * STG_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
+    const int tiles_n = (N + TN - 1) / TN;
+    const int tiles = ((M + TM - 1) / TM) * tiles_n;
     const int KB = (K + TK - 1) / TK;
     const int NS = (KB + SLICE_KB - 1) / SLICE_KB;
 
@@ -128,9 +193,9 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
             mbar_init(&sm->full[s], 1);
             mbar_init(&sm->empty[s], 1);
         }
-        for (int d = 0; d < 2; ++d) {
+        for (int d = 0; d < NBUF; ++d) {
             mbar_init(&sm->dfull[d], 1);
-            mbar_init(&sm->dempty[d], 4);
+            mbar_init(&sm->dempty[d], C::EPI_WARPS);
         }
         mbar_init(&sm->done, 1);
         sm->failed = 0;
@@ -152,49 +217,60 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
 
     if (warp == 0) {
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < KB; ++kb) {
-                const int s = kb % STAGES;
-                if (kb >= STAGES && !mbar_wait(&sm->empty[s], ((kb / STAGES) - 1) & 1)) {
-                    sm->failed = 1;
-                    break;
+            int g = 0;   // k-blocks issued over all of this CTA's tiles
+            for (int t = blockIdx.x; t < tiles && !*(volatile int*)&sm->failed; t += gridDim.x) {
+                int m0, n0;
+                tile_origin(t, tiles_n, TN, m0, n0);
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    if (g >= STAGES && !mbar_wait(&sm->empty[s], ((g / STAGES) - 1) & 1)) {
+                        sm->failed = 1;
+                        break;
+                    }
+                    if (*(volatile int*)&sm->failed)
+                        break;
+                    mbar_expect_tx(&sm->full[s], C::STAGE_BYTES);
+                    tma_load_2d(A + s * A_BYTES, &map_a, kb * TK, m0, &sm->full[s]);
+                    tma_load_2d(B + s * C::B_BYTES, &map_b, kb * TK, n0, &sm->full[s]);
                 }
                 if (*(volatile int*)&sm->failed)
                     break;
-                mbar_expect_tx(&sm->full[s], 2 * TILE_BYTES);
-                tma_load_2d(A + s * TILE_BYTES, &map_a, kb * TK, m0, &sm->full[s]);
-                tma_load_2d(B + s * TILE_BYTES, &map_b, kb * TK, n0, &sm->full[s]);
-                issued = kb + 1;
             }
             // let the last copy into every stage land before the CTA can exit
-            for (int kb = issued - 1; kb >= 0 && kb >= issued - STAGES; --kb)
-                if (!mbar_wait(&sm->full[kb % STAGES], (kb / STAGES) & 1))
+            for (int h = g - 1; h >= 0 && h >= g - STAGES; --h)
+                if (!mbar_wait(&sm->full[h % STAGES], (h / STAGES) & 1))
                     sm->failed = 1;
         }
     } else if (warp == 1) {
         if (lane == 0) {
             bool ok = true;
-            for (int kb = 0; kb < KB && ok; ++kb) {
-                const int s = kb % STAGES;
-                const int sl = kb / SLICE_KB, d = sl & 1;
-                if (kb % SLICE_KB == 0 && sl >= 2 && !mbar_wait(&sm->dempty[d], ((sl >> 1) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                if (!mbar_wait(&sm->full[s], (kb / STAGES) & 1)) {
-                    ok = false;
-                    break;
-                }
-                fence_after();
-                const uint64_t a0 = sdesc(su32(A + s * TILE_BYTES));
-                const uint64_t b0 = sdesc(su32(B + s * TILE_BYTES));
+            int g = 0, sg = 0;   // k-blocks and K-slices consumed over all tiles
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    const int d = sg % NBUF;
+                    if (kb % SLICE_KB == 0 && sg >= NBUF &&
+                        !mbar_wait(&sm->dempty[d], ((sg / NBUF) - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(&sm->full[s], (g / STAGES) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint64_t a0 = sdesc(su32(A + s * A_BYTES));
+                    const uint64_t b0 = sdesc(su32(B + s * C::B_BYTES));
 #pragma unroll
-                for (int k = 0; k < TK / 16; ++k)
-                    mma_bf16(tmem + (uint32_t)(d * TN), a0 + 2 * k, b0 + 2 * k,
-                             (kb % SLICE_KB != 0 || k != 0) ? 1u : 0u);
-                mma_commit(&sm->empty[s]);
-                if (kb % SLICE_KB == SLICE_KB - 1 || kb == KB - 1)
-                    mma_commit(&sm->dfull[d]);
+                    for (int k = 0; k < TK / 16; ++k)
+                        mma_bf16<TN>(tmem + (uint32_t)(d * TN), a0 + 2 * k, b0 + 2 * k,
+                                     (kb % SLICE_KB != 0 || k != 0) ? 1u : 0u);
+                    mma_commit(&sm->empty[s]);
+                    if (kb % SLICE_KB == SLICE_KB - 1 || kb == KB - 1) {
+                        mma_commit(&sm->dfull[d]);
+                        ++sg;
+                    }
+                }
             }
             if (!ok)
                 sm->failed = 1;
@@ -204,70 +280,84 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
                 sm->failed = 1;
         }
     } else {
-        // epilogue: rows m0 + 32*q + lane, columns n0 .. n0+127
+        // epilogue: rows m0 + 32*q + lane, columns n0 + 128*h .. + 127
         const int q = warp & 3;
-        int acc[TN];
-#pragma unroll
-        for (int j = 0; j < TN; ++j)
-            acc[j] = 0;
+        const int ew = warp - 2;              // epilogue warp 0 .. EPI_WARPS-1
+        const int h = ew >> 2;                // column half (TN = 256)
+        const float sx = flush(*s_x), sw = flush(*s_w);
+        float* stg = reinterpret_cast<float*>(STG + ew * STG_BYTES);
         bool ok = true;
-        for (int sl = 0; sl < NS; ++sl) {
-            const int d = sl & 1;
-            if (!mbar_wait(&sm->dfull[d], (sl >> 1) & 1)) {
-                ok = false;
-                break;
-            }
-            fence_after();
+        int sg = 0;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            int m0, n0;
+            tile_origin(t, tiles_n, TN, m0, n0);
+            const int nc = n0 + 128 * h;
+            int acc[128];
 #pragma unroll
-            for (int c = 0; c < TN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * TN + 32 * c), v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    acc[32 * c + e] += __float2int_rn(__uint_as_float(v[e]));
-            }
-            fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&sm->dempty[d]);
-        }
-        if (!ok) {
-            if (lane == 0)
-                sm->failed = 1;
-        } else {
-            const float sx = flush(*s_x), sw = flush(*s_w);
-            const int row = m0 + 32 * q + lane;
-            if ((N & 3) == 0 && n0 + TN <= N) {
-                // every MMA has completed (the last slice's barrier), so no copy or
-                // MMA touches the operand ring any more: each warp stages its 32 x
-                // 128 block there (pitch EPI_PITCH) and stores whole rows, 512
-                // contiguous bytes per warp instruction
-                float* stg = reinterpret_cast<float*>(base) + q * (32 * EPI_PITCH);
-#pragma unroll
-                for (int j = 0; j < TN; j += 4) {
-                    float4 o;
-                    o.x = fmul_flush(fmul_flush(__int2float_rn(acc[j + 0]), sx), sw);
-                    o.y = fmul_flush(fmul_flush(__int2float_rn(acc[j + 1]), sx), sw);
-                    o.z = fmul_flush(fmul_flush(__int2float_rn(acc[j + 2]), sx), sw);
-                    o.w = fmul_flush(fmul_flush(__int2float_rn(acc[j + 3]), sx), sw);
-                    *reinterpret_cast<float4*>(stg + lane * EPI_PITCH + j) = o;
+            for (int j = 0; j < 128; ++j)
+                acc[j] = 0;
+            for (int sl = 0; sl < NS; ++sl, ++sg) {
+                const int d = sg % NBUF;
+                if (!mbar_wait(&sm->dfull[d], (sg / NBUF) & 1)) {
+                    ok = false;
+                    break;
                 }
+                fence_after();
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(d * TN + 128 * h + 16 * c), v);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        acc[16 * c + e] += __float2int_rn(__uint_as_float(v[e]));
+                }
+                fence_before();
                 __syncwarp();
-                const int rows = min(32, M - (m0 + 32 * q));
-                for (int r = 0; r < rows; ++r) {
-                    const float4 v = *reinterpret_cast<const float4*>(stg + r * EPI_PITCH + 4 * lane);
-                    *reinterpret_cast<float4*>(y + (int64_t)(m0 + 32 * q + r) * N + n0 + 4 * lane) = v;
-                }
-            } else if (row < M) {
-                float* dst = y + (int64_t)row * N + n0;
-                {
+                if (lane == 0)
+                    mbar_arrive(&sm->dempty[d]);
+            }
+            if (!ok)
+                break;
+            const int r0 = m0 + 32 * q;
+            if (y_tma) {
+                // 32 x 32 blocks: lane writes its row's eight 16-byte chunks at
+                // the 128-byte-swizzled positions (chunk k of row r at k ^ (r % 8)),
+                // then one TMA store writes the block; the buffer is reused once
+                // the previous store has read it
 #pragma unroll
-                    for (int j = 0; j < TN; ++j)
-                        if (n0 + j < N)
-                            dst[j] = fmul_flush(fmul_flush(__int2float_rn(acc[j]), sx), sw);
+                for (int c = 0; c < 4; ++c) {
+                    if (r0 < M && nc + 32 * c < N) {   // warp-uniform
+                        if (lane == 0)
+                            bulk_wait_read();
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int j = 32 * c + 4 * k;
+                            float4 o;
+                            o.x = fmul_flush(fmul_flush(__int2float_rn(acc[j + 0]), sx), sw);
+                            o.y = fmul_flush(fmul_flush(__int2float_rn(acc[j + 1]), sx), sw);
+                            o.z = fmul_flush(fmul_flush(__int2float_rn(acc[j + 2]), sx), sw);
+                            o.w = fmul_flush(fmul_flush(__int2float_rn(acc[j + 3]), sx), sw);
+                            *reinterpret_cast<float4*>(stg + lane * 32 + 4 * (k ^ (lane & 7))) = o;
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0)
+                            tma_store_2d(&map_y, stg, nc + 32 * c, r0);
+                    }
                 }
+            } else if (r0 + lane < M) {
+                float* dst = y + (int64_t)(r0 + lane) * N + nc;
+#pragma unroll
+                for (int j = 0; j < 128; ++j)
+                    if (nc + j < N)
+                        dst[j] = fmul_flush(fmul_flush(__int2float_rn(acc[j]), sx), sw);
             }
         }
+        if (!ok && lane == 0)
+            sm->failed = 1;
+        if (lane == 0)
+            bulk_wait_all();
     }
 
     fence_before();
@@ -327,15 +417,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// [rows x K] bf16, row-major; box 64 (K) x 128 (rows), 128-byte swizzle
-bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K)
+// [rows x K] bf16, row-major; box 64 (K) x box_rows, 128-byte swizzle
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows)
 {
     auto fn = encode_fn();
     if (!fn)
         return false;
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-    cuuint32_t box[2] = {(cuuint32_t)TK, (cuuint32_t)TM};
+    cuuint32_t box[2] = {(cuuint32_t)TK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -344,6 +434,47 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K)
 }
 
 inline int64_t align256(int64_t b) { return (b + 255) & ~(int64_t)255; }
+
+// Y [M x N] fp32, row-major; box 32 x 32, 128-byte swizzle (the epilogue's
+// staging layout); needs a row pitch that is a multiple of 16 bytes
+bool make_y_map(CUtensorMap* map, float* y, int64_t M, int64_t N)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)N * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int TN>
+cudaError_t run_tile(const __nv_bfloat16* xa, const __nv_bfloat16* wb, const float* s_x,
+                     const float* s_w, float* y, int64_t M, int64_t N, int64_t K, int* err,
+                     cudaStream_t st)
+{
+    using C = Cfg<TN>;
+    CUtensorMap ma, mb, my;
+    memset(&my, 0, sizeof(my));
+    if (!make_map(&ma, xa, M, K, TM) || !make_map(&mb, wb, N, K, TN))
+        return cudaErrorInvalidValue;
+    const int y_tma = (N % 4) == 0;
+    if (y_tma && !make_y_map(&my, y, M, N))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_fwd_tc<TN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::SMEM_BYTES);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t tiles = ((M + TM - 1) / TM) * ((N + TN - 1) / TN);
+    const unsigned grid = (unsigned)std::min<int64_t>(tiles, num_sms());
+    k_fwd_tc<TN><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ma, mb, my, y_tma, s_x, s_w, y, (int)M,
+                                                         (int)N, (int)K, err);
+    count_launches(1);
+    return cudaGetLastError();
+}
 
 } // namespace
 
@@ -359,7 +490,8 @@ size_t fwd_tc_ws_bytes(int64_t M, int64_t N, int64_t K)
 }
 
 cudaError_t launch_fwd_tc(const int8_t* xq, const int8_t* wq, const float* s_x, const float* s_w,
-                          float* y, int64_t M, int64_t N, int64_t K, void* ws, cudaStream_t st)
+                          float* y, int64_t M, int64_t N, int64_t K, void* ws, bool wide,
+                          cudaStream_t st)
 {
     __nv_bfloat16* xa = static_cast<__nv_bfloat16*>(ws);
     __nv_bfloat16* wb = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) +
@@ -368,20 +500,11 @@ cudaError_t launch_fwd_tc(const int8_t* xq, const int8_t* wq, const float* s_x, 
     k_i8_to_bf16<<<grid_c, 256, 0, st>>>(xq, xa, M * K);
     k_i8_to_bf16<<<grid_c, 256, 0, st>>>(wq, wb, N * K);
     count_launches(2);
-    CUtensorMap ma, mb;
-    if (!make_map(&ma, xa, M, K) || !make_map(&mb, wb, N, K))
-        return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_fwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
-    if (e != cudaSuccess)
-        return e;
     int* err = device_error_word();
     if (!err)
         return cudaErrorInvalidValue;
-    dim3 grid((unsigned)((N + TN - 1) / TN), (unsigned)((M + TM - 1) / TM));
-    k_fwd_tc<<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, s_x, s_w, y, (int)M, (int)N, (int)K, err);
-    count_launches(1);
-    return cudaGetLastError();
+    return wide ? run_tile<256>(xa, wb, s_x, s_w, y, M, N, K, err, st)
+                : run_tile<128>(xa, wb, s_x, s_w, y, M, N, K, err, st);
 }
 
 } // namespace repro

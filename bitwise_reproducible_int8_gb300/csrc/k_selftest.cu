@@ -4,7 +4,8 @@
 // the fp32 accumulator holding every partial sum over a 512-term K-slice
 // exactly (each is an integer below 2^23).  The hardware documentation does
 // not promise how the tensor core adds inside a slice, so this check runs the
-// tensor-core path and the CUDA-core dp4a path (exact by construction) on
+// tensor-core path (both tile widths, 128 x 256 and 128 x 128) and the
+// CUDA-core dp4a path (exact by construction) on
 // adversarial codes -- every code at the clamp, alternating signs, a sign flip
 // at the slice boundary, one small term among large ones, hashed codes -- and
 // compares the outputs bit for bit.  With unit scales and K = 1024 every
@@ -14,7 +15,7 @@
 namespace repro {
 namespace {
 
-constexpr int ST_M = 128, ST_N = 128, ST_K = 1024;
+constexpr int ST_M = 128, ST_N = 256, ST_K = 1024;
 
 __device__ __forceinline__ int hashed_code(uint32_t r, uint32_t c)
 {
@@ -101,12 +102,17 @@ int run_selftest(void* ws, cudaStream_t st)
     count_launches(1);
     if (cudaGetLastError() != cudaSuccess)
         return -1;
-    if (launch_fwd_tc(xq, wq, scales, scales + 1, y_tc, ST_M, ST_N, ST_K, tc_ws, st) != cudaSuccess)
-        return -1;
     if (launch_fwd_cuda_core(xq, wq, scales, scales + 1, y_cc, ST_M, ST_N, ST_K, st) != cudaSuccess)
         return -1;
-    k_selftest_compare<<<(ST_M * ST_N + 255) / 256, 256, 0, st>>>(y_tc, y_cc, ST_M * ST_N, flag);
-    count_launches(1);
+    // both tensor-core tile widths (128 x 128 and 128 x 256), each against the
+    // CUDA-core output
+    for (int wide = 0; wide < 2; ++wide) {
+        if (launch_fwd_tc(xq, wq, scales, scales + 1, y_tc, ST_M, ST_N, ST_K, tc_ws, wide != 0,
+                          st) != cudaSuccess)
+            return -1;
+        k_selftest_compare<<<(ST_M * ST_N + 255) / 256, 256, 0, st>>>(y_tc, y_cc, ST_M * ST_N, flag);
+        count_launches(1);
+    }
     int h = 0;
     if (cudaMemcpyAsync(&h, flag, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)

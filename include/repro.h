@@ -341,7 +341,9 @@ typedef struct {
     int bwd_segment_log2;   /* -1: chosen per shape (whole-wave CTA counts); else 2^k chunks
                                per backward reduction segment (0..8) */
     int reduce_block_log2;  /* -1: default; else 2^k chunk partials per block in repro_wscale (0..10) */
-    int fwd_path;           /* -1: default (tensor cores when K % 8 == 0); 0: CUDA cores; 1: tensor cores */
+    int fwd_path;           /* -1: default (tensor cores, 128 x 256 output tiles, when K % 8 == 0);
+                               0: CUDA cores; 1: tensor cores, 128 x 256 tiles; 2: tensor cores,
+                               128 x 128 tiles */
     int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
     int bwd_kernel;         /* -1: default (8); 0: plain; 1: register prefetch; 2: staged;
                                3: staged wide tile; 4: wide tile with the tree in tensor

@@ -162,10 +162,11 @@ def test_launch_cfg_validation(L):
         with pytest.raises(repro.ReproError):
             repro.repro_set_launch_cfg(reduce_block_log2=11)
         with pytest.raises(repro.ReproError):
-            repro.repro_set_launch_cfg(fwd_path=2)
+            repro.repro_set_launch_cfg(fwd_path=3)
         with pytest.raises(repro.ReproError):
             repro.repro_set_launch_cfg(bwd_kernel=9)
         repro.repro_set_launch_cfg(bwd_kernel=8)
+        repro.repro_set_launch_cfg(fwd_path=2)
         repro.repro_set_launch_cfg(bwd_segment_log2=0, reduce_block_log2=0, fwd_path=0,
                                    elementwise_blocks=152)
     finally:

@@ -89,10 +89,11 @@ def test_quant_half_integers(orc):
 # ----------------------------------------------------------------- forward
 
 FWD_SHAPES = [(1, 1, 1), (3, 5, 7), (64, 128, 256), (130, 70, 200), (65, 129, 1040),
-              (200, 96, 2048), (17, 300, 33), (257, 129, 5632), (128, 128, 8), (300, 260, 520)]
+              (200, 96, 2048), (17, 300, 33), (257, 129, 5632), (128, 128, 8), (300, 260, 520),
+              (130, 384, 1024), (200, 500, 1536), (129, 514, 1032), (256, 512, 4096)]
 
 
-@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("path", [0, 1, 2])
 @pytest.mark.parametrize("M,N,K", FWD_SHAPES)
 def test_forward(orc, M, N, K, path):
     R.repro_set_launch_cfg(fwd_path=path)
@@ -109,7 +110,7 @@ def test_tensor_core_forward_selftest():
     assert R.repro_selftest() == R.REPRO_OK
 
 
-@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("path", [0, 1, 2])
 def test_forward_at_the_maximum_reduction(orc, path):
     # K = 133,144 is the largest K for which |acc| <= 127 * 127 * K fits int32;
     # codes at the clamp make row 0 reach 2,147,479,576
@@ -126,7 +127,7 @@ def test_forward_at_the_maximum_reduction(orc, path):
     assert orc.int_dot(xq, wq, 0, 0) == 127 * 127 * K
 
 
-@pytest.mark.parametrize("path", [0, 1])
+@pytest.mark.parametrize("path", [0, 1, 2])
 @pytest.mark.parametrize("K", [1024, 1040, 2048, 5632])
 def test_forward_adversarial(orc, K, path):
     R.repro_set_launch_cfg(fwd_path=path)
