@@ -105,6 +105,26 @@ def test_forward(orc, M, N, K, path):
                         f"fwd {M}x{N}x{K}")
 
 
+# more output tiles than SMs, so the persistent tensor-core forward walks
+# several tiles per CTA and its K-slice counters and accumulator buffers carry
+# across tiles: ragged rows and columns, row pitches with and without 16-byte
+# multiples (TMA-store and register-store epilogues), one to three K-slices
+FWD_MULTI_TILE = [(1300, 4100, 1096), (1300, 4099, 1096), (2177, 2052, 520), (4096, 4096, 64)]
+
+
+@pytest.mark.parametrize("path", [0, 1, 2])
+@pytest.mark.parametrize("M,N,K", FWD_MULTI_TILE)
+def test_forward_many_tiles_per_cta(orc, M, N, K, path):
+    R.repro_set_launch_cfg(fwd_path=path)
+    rng = np.random.default_rng(M * 7 + N + K)
+    xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    wq = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    s_x, s_w = np.float32(0.0213), np.float32(0.00391)
+    want = orc.linear_fwd(xq, wq, s_x, s_w)
+    for _ in range(2):   # and the same bits on a second call
+        G.assert_bits_equal(G.gpu_fwd(xq, wq, s_x, s_w), want, f"fwd {M}x{N}x{K} path {path}")
+
+
 def test_tensor_core_forward_selftest():
     # adversarial codes through the tensor-core path and the exact dp4a path
     assert R.repro_selftest() == R.REPRO_OK
