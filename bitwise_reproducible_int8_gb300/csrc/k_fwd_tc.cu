@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 #include "pipeline.cuh"
 
 namespace repro {
@@ -214,6 +215,9 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
     __syncthreads();
     fence_after();
     const uint32_t tmem = sm->tmem_base;
+    // the set-up above touches no global memory; everything below may read
+    // what the kernels before this one on the stream wrote
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -376,6 +380,8 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUte
 __global__ void __launch_bounds__(256)
 k_i8_to_bf16(const int8_t* __restrict__ q, __nv_bfloat16* __restrict__ out, int64_t n)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t nv = n >> 4;
     const int4* q16 = reinterpret_cast<const int4*>(q);
     uint4* o = reinterpret_cast<uint4*>(out);
@@ -470,10 +476,10 @@ cudaError_t run_tile(const __nv_bfloat16* xa, const __nv_bfloat16* wb, const flo
         return e;
     const int64_t tiles = ((M + TM - 1) / TM) * ((N + TN - 1) / TN);
     const unsigned grid = (unsigned)std::min<int64_t>(tiles, num_sms());
-    k_fwd_tc<TN><<<grid, C::THREADS, C::SMEM_BYTES, st>>>(ma, mb, my, y_tma, s_x, s_w, y, (int)M,
-                                                         (int)N, (int)K, err);
+    e = launch_pdl(k_fwd_tc<TN>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, st, ma, mb, my, y_tma,
+                   s_x, s_w, y, (int)M, (int)N, (int)K, err);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 } // namespace
@@ -497,9 +503,12 @@ cudaError_t launch_fwd_tc(const int8_t* xq, const int8_t* wq, const float* s_x, 
     __nv_bfloat16* wb = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) +
                                                           align256(2 * M * K));
     const int grid_c = num_sms() * 8;
-    k_i8_to_bf16<<<grid_c, 256, 0, st>>>(xq, xa, M * K);
-    k_i8_to_bf16<<<grid_c, 256, 0, st>>>(wq, wb, N * K);
+    cudaError_t e = launch_pdl(k_i8_to_bf16, dim3(grid_c), dim3(256), 0, st, xq, xa, M * K);
+    if (e == cudaSuccess)
+        e = launch_pdl(k_i8_to_bf16, dim3(grid_c), dim3(256), 0, st, wq, wb, N * K);
     count_launches(2);
+    if (e != cudaSuccess)
+        return e;
     int* err = device_error_word();
     if (!err)
         return cudaErrorInvalidValue;

@@ -12,6 +12,7 @@
 // 16-byte loads and one 16-byte store; the grid is a multiple of the SM count.
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace repro {
 namespace {
@@ -35,6 +36,8 @@ __global__ void __launch_bounds__(256)
 k_quant(const float* __restrict__ x, int64_t n, const float* __restrict__ scale, int qmax,
         int8_t* __restrict__ q)
 {
+    pdl_wait();
+    pdl_trigger();
     const float s = flush(*scale);
     const int64_t nv = n >> 4;
     const float4* x4 = reinterpret_cast<const float4*>(x);
@@ -74,9 +77,9 @@ k_quant(const float* __restrict__ x, int64_t n, const float* __restrict__ scale,
 cudaError_t launch_quant(const float* x, int64_t n, const float* scale, int qmax, int8_t* q,
                          int grid, cudaStream_t st)
 {
-    k_quant<<<grid, 256, 0, st>>>(x, n, scale, qmax, q);
+    const cudaError_t e = launch_pdl(k_quant, dim3(grid), dim3(256), 0, st, x, n, scale, qmax, q);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 } // namespace repro

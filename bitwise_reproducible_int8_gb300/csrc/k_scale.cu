@@ -15,6 +15,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch.cuh"
 
 namespace repro {
 namespace {
@@ -41,6 +42,8 @@ k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __re
 {
     __shared__ float4 S[P1_CHUNKS * 16];
     __shared__ float T[P1_CHUNKS];
+    pdl_wait();
+    pdl_trigger();
     const int nb = 1 << blk_log2;
     const int64_t C = (n + 63) >> 6;
     const int64_t c0 = (int64_t)blockIdx.x * nb;
@@ -137,6 +140,8 @@ k_tree_pass(const float* __restrict__ in, int64_t cnt_total, int blk_log2,
             float* __restrict__ scale_out)
 {
     __shared__ float T[P2_MAX];
+    pdl_wait();
+    pdl_trigger();
     const int nb = 1 << blk_log2;
     const int64_t b0 = (int64_t)blockIdx.x * nb;
     const int cnt = (int)min((int64_t)nb, cnt_total - b0);
@@ -169,6 +174,8 @@ __device__ __forceinline__ float absflush(float v)
 __global__ void __launch_bounds__(256)
 k_amax_partial(const float* __restrict__ x, int64_t n, float* __restrict__ part)
 {
+    pdl_wait();
+    pdl_trigger();
     float m = 0.f;
     const int64_t nv = n >> 2;
     const float4* x4 = reinterpret_cast<const float4*>(x);
@@ -208,6 +215,7 @@ k_amax_partial(const float* __restrict__ x, int64_t n, float* __restrict__ part)
 __global__ void __launch_bounds__(1024)
 k_amax_final(const float* __restrict__ part, int cnt, int qmax, float* __restrict__ scale_out)
 {
+    pdl_wait();
     float m = 0.f;
     for (int i = threadIdx.x; i < cnt; i += blockDim.x)
         m = fmaxf(m, part[i]);
@@ -266,19 +274,21 @@ static cudaError_t canonical_sum(const float* x, int64_t n, int square, int qmax
     float* regA = static_cast<float*>(ws);
     float* regB = regA + cnt + 32;
     float* scale_out = out;
-    if (square)
-        k_absum_chunks<1><<<(unsigned)cnt, P1_CHUNKS, 0, st>>>(x, n, p1, regA);
-    else
-        k_absum_chunks<0><<<(unsigned)cnt, P1_CHUNKS, 0, st>>>(x, n, p1, regA);
+    cudaError_t e = launch_pdl(square ? k_absum_chunks<1> : k_absum_chunks<0>, dim3((unsigned)cnt),
+                               dim3(P1_CHUNKS), 0, st, x, n, p1, regA);
     count_launches(1);
+    if (e != cudaSuccess)
+        return e;
     float* src = regA;
     float* dst = regB;
     for (;;) {
         const int64_t grid = cdiv(cnt, (int64_t)1 << p2);
         const int final_pass = grid == 1 ? (square ? 2 : 1) : 0;
-        k_tree_pass<<<(unsigned)grid, P2_MAX, 0, st>>>(src, cnt, p2, dst, final_pass, n, qmax,
-                                                       scale_out);
+        e = launch_pdl(k_tree_pass, dim3((unsigned)grid), dim3(P2_MAX), 0, st, src, cnt, p2, dst,
+                       final_pass, n, qmax, scale_out);
         count_launches(1);
+        if (e != cudaSuccess)
+            return e;
         if (final_pass)
             break;
         cnt = grid;
@@ -312,10 +322,11 @@ cudaError_t launch_wscale_amax(const float* x, int64_t n, int qmax, float* scale
                                int grid, cudaStream_t st)
 {
     float* part = static_cast<float*>(ws);
-    k_amax_partial<<<grid, 256, 0, st>>>(x, n, part);
-    k_amax_final<<<1, 1024, 0, st>>>(part, grid, qmax, scale_out);
+    cudaError_t e = launch_pdl(k_amax_partial, dim3(grid), dim3(256), 0, st, x, n, part);
+    if (e == cudaSuccess)
+        e = launch_pdl(k_amax_final, dim3(1), dim3(1024), 0, st, part, grid, qmax, scale_out);
     count_launches(2);
-    return cudaGetLastError();
+    return e;
 }
 
 } // namespace repro
