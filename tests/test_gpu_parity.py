@@ -63,6 +63,18 @@ def test_scale_launch_invariance(orc, blk):
     G.assert_bits_equal(np.float32(G.gpu_scale(x, 0)), ref, f"block 2^{blk}")
 
 
+@pytest.mark.parametrize("n", [1, 100, 700_003])
+@pytest.mark.parametrize("grid", [1, 7, 152, 5000])
+def test_amax_grid_invariance(orc, n, grid):
+    # the launch-configuration hook sets the amax grid (capped by the
+    # workspace's partial slots); the maximum is exact whatever the split
+    rng = np.random.default_rng(n + grid)
+    x = rng.standard_normal(n).astype(np.float32)
+    ref = np.float32(orc.wscale(x, 1))
+    R.repro_set_launch_cfg(elementwise_blocks=grid)
+    G.assert_bits_equal(np.float32(G.gpu_scale(x, 1)), ref, f"amax n {n} grid {grid}")
+
+
 # ----------------------------------------------------------------- quantiser
 
 @pytest.mark.parametrize("n", [1, 15, 16, 17, 1000, 65536 + 9])
