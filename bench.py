@@ -41,7 +41,7 @@ METRIC = "tokens/s bit-exact int8-QAT linear fwd+bwd (1 GB300); % of int8/FP32/H
 # dram__bytes_read.sum + dram__bytes_write.sum (single pass) on a GB300.  Valid only
 # for that kernel and workload; anything else reports null.
 BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd4"): 544.7e6, ("block", "k_bwd_tma"): 1660.5e6,
-                          ("block", "k_bwd_tma<self-issue>"): 1655.5e6}
+                          ("block", "k_bwd_tma<self-issue>"): 1654.9e6}
 UNIT = "tokens/s"
 
 
