@@ -420,7 +420,19 @@ __global__ void __launch_bounds__(32) k_wait_probe(int* err, int arrive)
 
 // ---------------------------------------------------------------- operand prep
 
-// out[e] = float(q[e]) (x) s, flushed; 16 codes per thread per step
+// 16 codes -> 4 float4 of dequantised, flushed values
+__device__ __forceinline__ void dequant16(const int4 w, float s, float4* o)
+{
+    const int words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        o[u] = make_float4(dequant((int)(int8_t)(words[u]), s), dequant((int)(int8_t)(words[u] >> 8), s),
+                           dequant((int)(int8_t)(words[u] >> 16), s),
+                           dequant((int)(int8_t)(words[u] >> 24), s));
+}
+
+// out[e] = float(q[e]) (x) s, flushed; 16 codes per thread per load, four
+// loads in flight per step
 __global__ void __launch_bounds__(256)
     k_dequant_f32(const int8_t* __restrict__ q, const float* __restrict__ scale,
                   float* __restrict__ out, int64_t n)
@@ -429,17 +441,19 @@ __global__ void __launch_bounds__(256)
     const int64_t nv = n >> 4;
     const int4* q16 = reinterpret_cast<const int4*>(q);
     float4* o = reinterpret_cast<float4*>(out);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int4 w = q16[i];
-        const int words[4] = {w.x, w.y, w.z, w.w};
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < nv; i += 4 * stride) {
+        int4 w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            o[4 * i + u] = make_float4(dequant((int)(int8_t)(words[u]), s),
-                                       dequant((int)(int8_t)(words[u] >> 8), s),
-                                       dequant((int)(int8_t)(words[u] >> 16), s),
-                                       dequant((int)(int8_t)(words[u] >> 24), s));
+            w[u] = __ldg(q16 + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            dequant16(w[u], s, o + 4 * (i + u * stride));
     }
+    for (; i < nv; i += stride)
+        dequant16(__ldg(q16 + i), s, o + 4 * i);
     if (blockIdx.x == 0) {
         const int64_t i = (nv << 4) + threadIdx.x;
         if (threadIdx.x < 16 && i < n)
@@ -461,7 +475,8 @@ __global__ void __launch_bounds__(256)
 
 // out[c][r] = flush(x[r][c]) for x [rows x cols]; out row pitch ldo floats.
 // 32 x 32 tiles through shared memory (padded: conflict-free both ways),
-// tiles visited grid-stride.
+// tiles visited grid-stride.  (Moving four tiles per step, for more loads in
+// flight, made it slower on GB300: 184 vs 131 us per block-workload launch.)
 __global__ void __launch_bounds__(256)
     k_flush_transpose(const float* __restrict__ x, float* __restrict__ out, int64_t rows,
                       int64_t cols, int64_t ldo)
