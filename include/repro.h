@@ -344,7 +344,9 @@ typedef struct {
     int fwd_path;           /* -1: default (tensor cores, 128 x 256 output tiles, when K % 8 == 0);
                                0: CUDA cores; 1: tensor cores, 128 x 256 tiles; 2: tensor cores,
                                128 x 128 tiles */
-    int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels */
+    int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels and of
+                               the activation-scale pass (that one capped at the
+                               ceil(n / 64) + 64 partial slots of its workspace) */
     int bwd_kernel;         /* -1: default (8); 0: plain; 1: register prefetch; 2: staged;
                                3: staged wide tile; 4: wide tile with the tree in tensor
                                memory; 5: twelve-warp wide tile; 6: warp-specialised wide
