@@ -447,13 +447,13 @@ __global__ void __launch_bounds__(256)
         int4 w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            w[u] = __ldg(q16 + i + u * stride);
+            w[u] = ld_stream(q16 + i + u * stride);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
             dequant16(w[u], s, o + 4 * (i + u * stride));
     }
     for (; i < nv; i += stride)
-        dequant16(__ldg(q16 + i), s, o + 4 * i);
+        dequant16(ld_stream(q16 + i), s, o + 4 * i);
     if (blockIdx.x == 0) {
         const int64_t i = (nv << 4) + threadIdx.x;
         if (threadIdx.x < 16 && i < n)
@@ -470,7 +470,7 @@ __global__ void __launch_bounds__(256)
     float4* o4 = reinterpret_cast<float4*>(out);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
          i += (int64_t)gridDim.x * blockDim.x)
-        o4[i] = flush4(x4[i]);
+        o4[i] = flush4(ld_stream(x4 + i));
 }
 
 // out[c][r] = flush(x[r][c]) for x [rows x cols]; out row pitch ldo floats.

@@ -387,7 +387,7 @@ k_i8_to_bf16(const int8_t* __restrict__ q, __nv_bfloat16* __restrict__ out, int6
     uint4* o = reinterpret_cast<uint4*>(out);
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
          i += (int64_t)gridDim.x * blockDim.x) {
-        const int4 w = __ldg(q16 + i);
+        const int4 w = ld_stream(q16 + i);
         const int words[4] = {w.x, w.y, w.z, w.w};
         uint32_t h[8];
 #pragma unroll

@@ -83,7 +83,7 @@ k_adamw(float* __restrict__ p, float* __restrict__ m, float* __restrict__ v,
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
          i += (int64_t)gridDim.x * blockDim.x) {
         float4 pp = p4[i], mm = m4[i], vv = v4[i];
-        const float4 gg = __ldg(g4 + i);
+        const float4 gg = ld_stream(g4 + i);
         update(pp.x, mm.x, vv.x, gg.x, c);
         update(pp.y, mm.y, vv.y, gg.y, c);
         update(pp.z, mm.z, vv.z, gg.z, c);

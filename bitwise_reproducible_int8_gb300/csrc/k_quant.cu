@@ -48,10 +48,10 @@ k_quant(const float* __restrict__ x, int64_t n, const float* __restrict__ scale,
             q16[i] = make_uint4(0, 0, 0, 0);
     } else {
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
-            const float4 a = __ldg(x4 + 4 * i + 0);
-            const float4 b = __ldg(x4 + 4 * i + 1);
-            const float4 c = __ldg(x4 + 4 * i + 2);
-            const float4 d = __ldg(x4 + 4 * i + 3);
+            const float4 a = ld_stream(x4 + 4 * i + 0);
+            const float4 b = ld_stream(x4 + 4 * i + 1);
+            const float4 c = ld_stream(x4 + 4 * i + 2);
+            const float4 d = ld_stream(x4 + 4 * i + 3);
             uint4 o;
             o.x = pack4(quant_one(a.x, s, qmax), quant_one(a.y, s, qmax), quant_one(a.z, s, qmax),
                         quant_one(a.w, s, qmax));

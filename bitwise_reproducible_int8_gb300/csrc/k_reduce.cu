@@ -20,7 +20,7 @@ k_grad_accum(float* __restrict__ acc, const float* __restrict__ g, int64_t n)
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
          i += (int64_t)gridDim.x * blockDim.x) {
         float4 a = a4[i];
-        const float4 b = __ldg(g4 + i);
+        const float4 b = ld_stream(g4 + i);
         a.x = fadd_ftz(a.x, b.x);
         a.y = fadd_ftz(a.y, b.y);
         a.z = fadd_ftz(a.z, b.z);
@@ -74,7 +74,7 @@ k_treefold(const Parts parts, int64_t n, float* out)
         float x[R], y[R], z[R], w[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(parts.p[r]) + i);
+            const float4 v = ld_stream(reinterpret_cast<const float4*>(parts.p[r]) + i);
             x[r] = v.x;
             y[r] = v.y;
             z[r] = v.z;
@@ -128,10 +128,10 @@ k_running_sum(const Parts parts, int64_t n, float* out)
     const int64_t nv = n >> 2;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
          i += (int64_t)gridDim.x * blockDim.x) {
-        float4 a = __ldg(reinterpret_cast<const float4*>(parts.p[0]) + i);
+        float4 a = ld_stream(reinterpret_cast<const float4*>(parts.p[0]) + i);
 #pragma unroll
         for (int s = 1; s < S; ++s) {
-            const float4 b = __ldg(reinterpret_cast<const float4*>(parts.p[s]) + i);
+            const float4 b = ld_stream(reinterpret_cast<const float4*>(parts.p[s]) + i);
             a.x = fadd_ftz(a.x, b.x);
             a.y = fadd_ftz(a.y, b.y);
             a.z = fadd_ftz(a.z, b.z);

@@ -56,7 +56,7 @@ k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __re
         const float4* x4 = reinterpret_cast<const float4*>(x + e0);
 #pragma unroll
         for (int u = 0; u < 16; ++u)
-            v[u] = __ldg(x4 + threadIdx.x + u * P1_CHUNKS);
+            v[u] = ld_stream(x4 + threadIdx.x + u * P1_CHUNKS);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             const int g = threadIdx.x + u * P1_CHUNKS;
@@ -186,14 +186,14 @@ k_amax_partial(const float* __restrict__ x, int64_t n, float* __restrict__ part)
         float4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            v[u] = __ldg(x4 + i + u * stride);
+            v[u] = ld_stream(x4 + i + u * stride);
 #pragma unroll
         for (int u = 0; u < 4; ++u)
             m = fmaxf(m, fmaxf(fmaxf(absflush(v[u].x), absflush(v[u].y)),
                                fmaxf(absflush(v[u].z), absflush(v[u].w))));
     }
     for (; i < nv; i += stride) {
-        const float4 v = __ldg(x4 + i);
+        const float4 v = ld_stream(x4 + i);
         m = fmaxf(m, fmaxf(fmaxf(absflush(v.x), absflush(v.y)), fmaxf(absflush(v.z), absflush(v.w))));
     }
     if (blockIdx.x == 0 && threadIdx.x < (n & 3))
