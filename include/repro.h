@@ -387,8 +387,9 @@ const char* repro_status_str(int status);
  * over 512-term K-slices of integer products staying exact, which the
  * hardware documentation does not state; this runs it and the CUDA-core
  * (dp4a) path on adversarial codes (all at the clamp, alternating signs, a
- * sign flip at the slice boundary, hashed codes; K = 1024, unit scales) and
- * compares every output bit.  Synchronises `stream`.  ws: device workspace of
+ * sign flip at the slice boundary, hashed codes; 128 x 256 outputs, K = 1024,
+ * unit scales) and compares every output bit, for both tensor-core tile
+ * widths (128 x 256, the default, and 128 x 128).  Synchronises `stream`.  ws: device workspace of
  * repro_selftest_ws_bytes() bytes.  Returns REPRO_OK, REPRO_ERR_SELFTEST on a
  * mismatch, or an argument / launch error.
  * ------------------------------------------------------------------------ */
