@@ -40,8 +40,7 @@ METRIC = "tokens/s bit-exact int8-QAT linear fwd+bwd (1 GB300); % of int8/FP32/H
 # launches of the block workload's 4 captured steps, from one ncu capture of
 # dram__bytes_read.sum + dram__bytes_write.sum (single pass) on a GB300.  Valid only
 # for that kernel and workload; anything else reports null.
-BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd4"): 544.7e6, ("block", "k_bwd_tma"): 1660.5e6,
-                          ("block", "k_bwd_tma<self-issue>"): 1654.9e6}
+BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd_tma"): 1654.9e6}
 UNIT = "tokens/s"
 
 
@@ -347,9 +346,7 @@ def run_ours(args, wl):
         fp32_peak = sms * 128 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         achieved = bwd_ops / (bwd_ms / 1000.0) / 1e12 if bwd_ms > 0 else 0.0
         nb = launch_counts.get("bwd_dx", 0) + launch_counts.get("bwd_dw", 0)
-        kname = {0: "k_bwd", 1: "k_bwd2", 2: "k_bwd3", 3: "k_bwd4", 4: "k_bwd5",
-                 5: "k_bwd6", 6: "k_bwd_ws", 7: "k_bwd_tma",
-                 8: "k_bwd_tma<self-issue>"}[args.bwd_kernel if args.bwd_kernel >= 0 else 8]
+        kname = {1: "k_bwd_prefetch", 8: "k_bwd_tma"}[args.bwd_kernel if args.bwd_kernel >= 0 else 8]
         traffic = BWD_TRAFFIC_PER_LAUNCH.get((wl.name, kname))
         unit_note = None
         if n_units:
@@ -872,7 +869,8 @@ def main(argv=None):
                     help="capture one step into a CUDA graph and time its replays "
                          "(launch-bound workloads; not with the optimizer)")
     ap.add_argument("--bwd-kernel", type=int, default=-1,
-                    help="backward kernel variant (launch-configuration hook; -1: default)")
+                    help="backward kernel (launch-configuration hook; -1: default 8, the "
+                         "tensor-copy-fed kernel; 1: the register-prefetch kernel)")
     ap.add_argument("--fwd-path", type=int, default=-1,
                     help="forward path (launch-configuration hook; -1: default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librepro.so")
 
-SOURCES = ["api.cu", "k_scale.cu", "k_quant.cu", "k_fwd.cu", "k_fwd_tc.cu", "k_bwd.cu", "k_bwd_staged.cu", "k_bwd_ws.cu", "k_bwd_tma.cu",
+SOURCES = ["api.cu", "k_scale.cu", "k_quant.cu", "k_fwd.cu", "k_fwd_tc.cu", "k_bwd.cu", "k_bwd_prefetch.cu", "k_bwd_tma.cu",
            "k_reduce.cu", "k_scale_noalloc.cu", "k_optim.cu", "k_hash.cu", "k_attn.cu", "k_selftest.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

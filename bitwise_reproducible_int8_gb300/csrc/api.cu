@@ -11,7 +11,7 @@ namespace repro {
 
 namespace {
 
-constexpr int kDefaultBwdKernel = 8;   // operand prep + tensor-copy-fed kernel, self-issued copies
+constexpr int kDefaultBwdKernel = 8;   // operand prep + tensor-copy-fed kernel
 LaunchCfg g_cfg = {-1, -1, -1, 0, kDefaultBwdKernel};
 
 constexpr int kMaxDevices = 64;
@@ -95,8 +95,6 @@ inline bool overlap(const void* a, size_t na, const void* b, size_t nb)
     return x < y + nb && y < x + na;
 }
 
-inline int status_of(cudaError_t e) { return e == cudaSuccess ? REPRO_OK : REPRO_ERR_LAUNCH; }
-
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 // grid of a streaming kernel: one 256-thread CTA per 256 work items, at most
@@ -164,7 +162,7 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
         return REPRO_ERR_ARG;
     if (cfg->elementwise_blocks < -1 || cfg->elementwise_blocks > (1 << 20))
         return REPRO_ERR_ARG;
-    if (cfg->bwd_kernel < -1 || cfg->bwd_kernel > 8)
+    if (cfg->bwd_kernel != -1 && cfg->bwd_kernel != 1 && cfg->bwd_kernel != 8)
         return REPRO_ERR_ARG;
     g_cfg.bwd_segment_log2 = cfg->bwd_segment_log2;
     g_cfg.reduce_block_log2 = cfg->reduce_block_log2;
@@ -372,7 +370,9 @@ int repro_linear_bwd(const float* dy, const int8_t* xq, const int8_t* wq, const 
         if (!al16(ws))
             return REPRO_ERR_ALIGN;
         if (overlap(ws, ws_bytes, dx, dxb) || overlap(ws, ws_bytes, dw, dwb) ||
-            overlap(ws, ws_bytes, dy, dyb))
+            overlap(ws, ws_bytes, dy, dyb) || overlap(ws, ws_bytes, xq, xqb) ||
+            overlap(ws, ws_bytes, wq, wqb) || overlap(ws, ws_bytes, s_x, 4) ||
+            overlap(ws, ws_bytes, s_w, 4))
             return REPRO_ERR_ALIAS;
     }
     int st = check_arch();

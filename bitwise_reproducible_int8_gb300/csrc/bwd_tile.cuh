@@ -1,7 +1,6 @@
-// bwd_tile.cuh -- the 8 x 4 packed thread tile of the wide-tile backward
-// kernels (k_bwd.cu variants 3-5, k_bwd_ws.cu, k_bwd_tma.cu): one reduction
-// step of rounded multiplies and flushed adds, and the tree levels kept in
-// tensor memory.
+// bwd_tile.cuh -- the 8 x 4 packed thread tile of the default backward kernel
+// (k_bwd_tma.cu): one reduction step of rounded multiplies and flushed adds,
+// and the tree levels kept in tensor memory.
 #pragma once
 
 #include <cuda_runtime.h>

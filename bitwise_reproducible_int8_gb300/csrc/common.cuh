@@ -104,6 +104,18 @@ __device__ __forceinline__ int4 ld_stream(const int4* p)
     return v;
 }
 
+// the same streaming hints on the coherent path, for data the kernel may also
+// write (an input that aliases the output): .nc is defined only for memory
+// that stays read-only for the kernel's whole lifetime
+__device__ __forceinline__ float4 ld_stream_coherent(const float4* p)
+{
+    float4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::256B.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ float4 flush4(float4 v)
 {
     return make_float4(flush(v.x), flush(v.y), flush(v.z), flush(v.w));

@@ -15,7 +15,7 @@ struct LaunchCfg {
     int reduce_block_log2;  // chunk partials per block in the scale reduction (0..10)
     int fwd_path;           // 0: CUDA-core exact path, 1: tensor cores 128 x 256 tiles, 2: 128 x 128
     int elementwise_blocks; // 0: default grid for streaming kernels
-    int bwd_kernel;         // 0: plain backward kernel, 1: pipelined packed kernel
+    int bwd_kernel;         // 8: tensor-copy-fed kernel (default), 1: register-prefetch kernel
 };
 
 const LaunchCfg& launch_cfg();
@@ -23,6 +23,8 @@ int num_sms();
 int* device_error_word();   // device address of the bounded-wait error flag
 int arch_status();          // REPRO_OK when the current device is a GB300
 void count_launches(int k); // adds k to the process-wide launch counter
+// status code of a CUDA runtime result, the same for every entry point
+inline int status_of(cudaError_t e) { return e == cudaSuccess ? 0 : -5; }   // REPRO_OK / REPRO_ERR_LAUNCH
 
 // ---- scale (k_scale.cu)
 size_t wscale_ws_bytes(int64_t n, int block_log2);

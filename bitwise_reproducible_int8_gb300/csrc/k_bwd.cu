@@ -13,9 +13,10 @@
 // dequantised int8 operand with j = k (B[r,j] = q[r,j] (x) s).
 //
 // Parallel over outputs only; each output's sequence of roundings is fixed:
-//   * a CTA owns an output tile and each thread a block of it; the variants
-//     (0-5 in k_bwd_staged.cu, 6 in k_bwd_ws.cu, 7-8 in k_bwd_tma.cu, 8 the
-//     default) differ only in how operands reach the products;
+//   * a CTA owns an output tile and each thread a block of it; the two
+//     kernels (k_bwd_tma.cu, the default, for 16-byte-aligned rows, and
+//     k_bwd_prefetch.cu for any rows) differ only in how operands reach the
+//     products;
 //   * the reduction advances one 64-term chunk at a time: the chunk's A and B
 //     slices sit in shared memory (dY flushed, the int8 operand dequantised
 //     and flushed), then every thread runs the 64 steps of the chunk for each
@@ -77,24 +78,19 @@ int64_t nseg_for(int64_t R, int seg_log2)
     return cdiv(cdiv(R, CH), (int64_t)1 << seg_log2);
 }
 
-// kernel variant actually launched for a shape (the staged kernels need
-// 16-byte-aligned rows) and its tile height
+// kernel launched for a shape: the tensor-copy-fed kernel (8) needs
+// 16-byte-aligned rows of dY (N % 4 == 0) and of the int8 operand
+// (J % 16 == 0); other shapes, or the launch-configuration hook's 1, take the
+// register-prefetch kernel (1)
+constexpr int KERNEL_TMA = 8, KERNEL_PREFETCH = 1;
+
 int kernel_for(int64_t ldy, int64_t J)
 {
-    const int k = launch_cfg().bwd_kernel;
     const bool aligned = (ldy % 4) == 0 && (J % 16) == 0;
-    if (k >= 2 && !aligned)
-        return 1;
-    return k;
+    return (aligned && launch_cfg().bwd_kernel == KERNEL_TMA) ? KERNEL_TMA : KERNEL_PREFETCH;
 }
 
-int tile_rows(int kernel)
-{
-    if (kernel >= 7)
-        return BWD_TMA_ROWS;
-    return kernel == 6 ? BWD_WS_ROWS
-                       : (kernel == 5 ? BWD_WIDE12_ROWS : (kernel >= 3 ? BWD_WIDE_ROWS : BT));
-}
+int tile_rows(int kernel) { return kernel == KERNEL_TMA ? BWD_TMA_ROWS : BT; }
 
 // Segment size when the launch configuration leaves it open.  One CTA runs
 // per SM, so a grid of tiles that is not close to a whole number of waves
@@ -163,29 +159,17 @@ cudaError_t run(const float* dy, const int8_t* q, const float* scale, float* out
     a.nseg = (int)nseg_for(R, seg_log2);
     a.accumulate = accumulate ? 1 : 0;
     a.err = device_error_word();
-    // the staged kernels need 16-byte-aligned rows: dY rows (N % 4) and int8
-    // rows (J % 16); other shapes take the register-prefetch kernel
-    const int kernel = kernel_for(ldy, J);
-    const bool aligned = kernel >= 2;
-    if (kernel >= 7 && aligned) {
+    cudaError_t e;
+    if (kernel_for(ldy, J) == KERNEL_TMA) {
         if (!a.err || !opnd)
             return cudaErrorInvalidValue;
         dim3 gt((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BWD_TMA_ROWS), (unsigned)a.nseg);
-        cudaError_t e = launch_bwd_tma<DW>(a, q, opnd, gt, kernel == 8, st);
-        if (e != cudaSuccess)
-            return e;
-    } else if (kernel == 6 && aligned) {
-        if (!a.err)
-            return cudaErrorInvalidValue;
-        dim3 gw((unsigned)cdiv(J, BT), (unsigned)cdiv(I, BWD_WS_ROWS), (unsigned)a.nseg);
-        cudaError_t e = launch_bwd_ws<DW>(a, gw, st);
-        if (e != cudaSuccess)
-            return e;
+        e = launch_bwd_tma<DW>(a, q, opnd, gt, st);
     } else {
-        cudaError_t e = launch_bwd_staged<DW>(kernel, a, st);
-        if (e != cudaSuccess)
-            return e;
+        e = launch_bwd_prefetch<DW>(a, st);
     }
+    if (e != cudaSuccess)
+        return e;
     count_launches(1);
     if (a.nseg > 1) {
         for (int s = 1; s < a.nseg; s *= 2) {
@@ -214,7 +198,7 @@ static int64_t seg_region_bytes(int64_t M, int64_t N, int64_t K, int seg_log2)
 
 static bool uses_operand_region(int64_t N, int64_t K)
 {
-    return kernel_for(N, K) >= 7;
+    return kernel_for(N, K) == KERNEL_TMA;
 }
 
 size_t bwd_ws_bytes(int64_t M, int64_t N, int64_t K, int seg_log2)

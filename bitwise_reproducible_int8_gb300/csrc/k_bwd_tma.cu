@@ -20,13 +20,18 @@
 // memory, so the bits of dX and dW are unchanged.
 //
 // The main kernel then only moves bytes and computes:
-//   * one producer warp: one thread issues two 2D tensor copies per 64-term
-//     chunk (A: 64 x 128 floats, B: 64 x 64 floats, zero fill outside the
-//     tensor) into a 4-stage ring guarded by full/empty mbarriers;
-//   * 8 compute warps own the 128 x 64 output tile, 8 x 4 outputs per thread,
-//     packed f32x2 multiply and add, reading the ring stage in place;
-//   * tree levels 0..RL-1 in registers, the rest in tensor memory (thread:
-//     lane 32*(warp%4) + lane, columns (warp/4)*256 + 32*(level-RL)).
+//   * 8 warps own the 128 x 64 output tile, 8 x 4 outputs per thread, packed
+//     f32x2 multiply and add, reading a 4-stage shared-memory ring in place;
+//   * thread 0 also issues the copies: two 2D tensor copies per 64-term chunk
+//     (A: 64 x 128 floats, B: 64 x 64 floats, zero fill outside the tensor),
+//     the ring guarded by full/empty mbarriers.  The prologue fills the four
+//     stages; at the start of chunk c it refills the stage that every warp
+//     released at the end of chunk c - 2 with chunk c + 2, so no warp runs
+//     more than two chunks ahead of warp 0 and every wait ends;
+//   * with 8 warps a thread may hold 255 registers, so tree levels 0..RL-1
+//     (RL = 3) stay in registers and the rest live in tensor memory (thread:
+//     lane 32*(warp%4) + lane, columns (warp/4)*256 + 32*(level-RL)), touched
+//     once every 8 chunks.
 // Every wait is bounded: past the limit the CTA records a failure in the
 // device error word, lets its copies land, frees its tensor memory and exits.
 #include <cuda.h>
@@ -41,8 +46,8 @@
 namespace repro {
 namespace {
 
-constexpr int NC = 256;                        // compute threads (warps 0-7)
-constexpr int NTH = NC + 32;                   // + one producer warp
+constexpr int NC = 256;                        // threads (8 warps)
+constexpr int RL = 3;                          // tree levels kept in registers
 constexpr int TI = BWD_TMA_ROWS;               // 128 tile rows (i)
 constexpr int STG = 4;                         // ring stages
 constexpr int A_BYTES = CH * TI * 4;           // 32768: A[r][i]
@@ -92,12 +97,6 @@ __device__ __forceinline__ void chunk_sum(u64 (&acc)[16], const float* __restric
     }
 }
 
-// SELF = false: one producer warp issues the copies, RL = 1 tree level in
-// registers (9 warps: at most 168 registers a thread).  SELF = true: no
-// producer warp; compute thread 0 refills the stage of chunk c - 2 with chunk
-// c - 2 + STG at the start of chunk c, and with 8 warps (255 registers a
-// thread) RL = 3 levels stay in registers, so tensor memory is touched once
-// every 8 chunks instead of every other chunk.
 // rows 0 .. CH-2 of a full chunk with row 0 already in (a03, a47, b); on
 // return (a03, a47, b) hold row CH-1, loaded but not yet multiplied
 __device__ __forceinline__ void chunk_head(u64 (&acc)[16], const float* __restrict__ Ar,
@@ -123,8 +122,8 @@ __device__ __forceinline__ void chunk_head(u64 (&acc)[16], const float* __restri
     }
 }
 
-template <bool DW, bool SELF, int RL>
-__global__ void __launch_bounds__(SELF ? NC : NTH, 1)
+template <bool DW>
+__global__ void __launch_bounds__(NC, 1)
     k_bwd_tma(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
               const BwdArgs a)
 {
@@ -132,8 +131,8 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
     // tensor copies want 128-byte aligned destinations; align the ring to 1024
     uint8_t* smt = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smt_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smt + CTRL_OFF);   // [STG], producer -> compute
-    uint64_t* empty = full + STG;                                   // [STG], compute -> producer
+    uint64_t* full = reinterpret_cast<uint64_t*>(smt + CTRL_OFF);   // [STG], copies landed
+    uint64_t* empty = full + STG;                                   // [STG], stage released
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty + STG);
     int* prod_fail = reinterpret_cast<int*>(tmem_slot + 1);
     int* comp_fail = prod_fail + 1;
@@ -187,33 +186,13 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-    if (!SELF && warp == NC / 32) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int issued = 0;
-            for (int cs = 0; cs < n; ++cs) {
-                const int s = cs % STG;
-                if (cs >= STG && !mbar_wait(&empty[s], ((cs / STG) - 1) & 1)) {
-                    *prod_fail = 1;
-                    break;
-                }
-                if (*(volatile int*)comp_fail)
-                    break;
-                issue(cs);
-                issued = cs + 1;
-            }
-            // let the last copy into every stage land before the CTA can exit
-            if (!drain(issued))
-                *prod_fail = 1;
-        }
-    } else {
-        // -------------------------------------------------------------- compute
+    {
         const int ty = (warp >> 1) * 4 + (lane >> 3);   // rows 8ty .. 8ty+7
         const int tx = (warp & 1) * 8 + (lane & 7);     // cols 4tx .. 4tx+3
         const uint32_t tbase =
             *tmem_slot + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)((warp >> 2) * 256);
 
-        const bool issuer = SELF && tid == 0;
+        const bool issuer = tid == 0;
         int issued = 0;
         if (issuer) {
             for (; issued < n && issued < STG; ++issued)
@@ -232,8 +211,8 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
                 S[l][e] = 0ull;
 
         bool ok = true;
-        // SELF: the next chunk's full wait and its row-0 loads are made before
-        // the current chunk's last row is multiplied, so they overlap it
+        // the next chunk's full wait and its row-0 loads are made before the
+        // current chunk's last row is multiplied, so they overlap it
         ulonglong2 n03 = {0ull, 0ull}, n47 = {0ull, 0ull};
         float4 nb = make_float4(0.f, 0.f, 0.f, 0.f);
         auto wait_full = [&](int c) {
@@ -246,7 +225,7 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
             n47 = *reinterpret_cast<const ulonglong2*>(Ar + 4);
             nb = *reinterpret_cast<const float4*>(stB(c % STG) + 4 * tx);
         };
-        if (SELF && n > 0) {
+        if (n > 0) {
             if (wait_full(0)) {
                 load_row0(0);
             } else {
@@ -257,7 +236,7 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
         }
         for (int cs = 0; ok && cs < n; ++cs) {
             const int s = cs % STG;
-            if (SELF && warp == 0) {
+            if (warp == 0) {
                 // refill the stage every warp released two chunks ago
                 if (lane == 0 && issued == cs + 2 && issued < n) {
                     const int rc = issued - STG;
@@ -271,7 +250,7 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
                 __syncwarp();
             }
             const int valid = valid_of(cs);
-            if (SELF && valid == CH) {
+            if (valid == CH) {
                 chunk_head(acc, stA(s) + 8 * ty, stB(s) + 4 * tx, n03, n47, nb);
                 const ulonglong2 l03 = n03, l47 = n47;
                 const float4 lb = nb;
@@ -292,14 +271,8 @@ __global__ void __launch_bounds__(SELF ? NC : NTH, 1)
                     break;
                 }
             } else {
-                // SELF: only the reduction's last chunk is partial, and its
-                // full wait was made at the end of the chunk before
-                if (!SELF && !wait_full(cs)) {
-                    ok = false;
-                    if (lane == 0)
-                        *comp_fail = 1;
-                    break;
-                }
+                // only the reduction's last chunk is partial, and its full
+                // wait was made at the end of the chunk before
                 chunk_sum(acc, stA(s) + 8 * ty, stB(s) + 4 * tx, valid);
                 __syncwarp();   // every lane's reads of stage s precede lane 0's release
                 if (lane == 0)
@@ -549,7 +522,7 @@ size_t bwd_tma_operand_bytes(int64_t M, int64_t N, int64_t K)
 
 template <bool DW>
 cudaError_t launch_bwd_tma(const BwdArgs& a0, const int8_t* q, float* opnd, dim3 grid,
-                           bool self_issue, cudaStream_t st)
+                           cudaStream_t st)
 {
     BwdArgs a = a0;
     const int eb = 8 * num_sms();
@@ -573,18 +546,18 @@ cudaError_t launch_bwd_tma(const BwdArgs& a0, const int8_t* q, float* opnd, dim3
     CUtensorMap ma, mb;
     if (!make_map(&ma, Aop, a.R, a.I, lda, TI) || !make_map(&mb, Bop, a.R, a.J, a.J, BT))
         return cudaErrorInvalidValue;
-    auto kern = self_issue ? k_bwd_tma<DW, true, 3> : k_bwd_tma<DW, false, 1>;
+    auto kern = k_bwd_tma<DW>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess)
         return e;
-    kern<<<grid, self_issue ? NC : NTH, SMEM_BYTES, st>>>(ma, mb, a);
+    kern<<<grid, NC, SMEM_BYTES, st>>>(ma, mb, a);
     return cudaGetLastError();
 }
 
-template cudaError_t launch_bwd_tma<false>(const BwdArgs&, const int8_t*, float*, dim3, bool,
+template cudaError_t launch_bwd_tma<false>(const BwdArgs&, const int8_t*, float*, dim3,
                                            cudaStream_t);
-template cudaError_t launch_bwd_tma<true>(const BwdArgs&, const int8_t*, float*, dim3, bool,
+template cudaError_t launch_bwd_tma<true>(const BwdArgs&, const int8_t*, float*, dim3,
                                           cudaStream_t);
 
 cudaError_t launch_wait_probe(int arrive, cudaStream_t st)

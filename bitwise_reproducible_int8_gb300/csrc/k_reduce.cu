@@ -4,7 +4,10 @@
 // and TreeFold, which folds R replica partials in the pairing order of a
 // recursive-doubling all-reduce.  Both are elementwise and HBM-bound: 16-byte
 // loads and stores, grid a multiple of the SM count, one pass over all R
-// inputs for TreeFold.
+// inputs for TreeFold.  The output of TreeFold and of the running sum may be
+// the first part itself, so that part is read on the coherent path (each
+// element is read before the same thread writes it); the others, which never
+// overlap the output, stream through the read-only path.
 #include "common.cuh"
 #include "internal.h"
 
@@ -74,7 +77,8 @@ k_treefold(const Parts parts, int64_t n, float* out)
         float x[R], y[R], z[R], w[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const float4 v = ld_stream(reinterpret_cast<const float4*>(parts.p[r]) + i);
+            const float4* src = reinterpret_cast<const float4*>(parts.p[r]) + i;
+            const float4 v = r == 0 ? ld_stream_coherent(src) : ld_stream(src);
             x[r] = v.x;
             y[r] = v.y;
             z[r] = v.z;
@@ -128,7 +132,7 @@ k_running_sum(const Parts parts, int64_t n, float* out)
     const int64_t nv = n >> 2;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv;
          i += (int64_t)gridDim.x * blockDim.x) {
-        float4 a = ld_stream(reinterpret_cast<const float4*>(parts.p[0]) + i);
+        float4 a = ld_stream_coherent(reinterpret_cast<const float4*>(parts.p[0]) + i);
 #pragma unroll
         for (int s = 1; s < S; ++s) {
             const float4 b = ld_stream(reinterpret_cast<const float4*>(parts.p[s]) + i);

@@ -11,14 +11,19 @@
 //
 // The array (REPRO_NOALLOC_SCRATCH_FLOATS floats, 256 KB) is a static
 // __device__ variable: every GPU that loads the library holds it until the
-// process exits.  Host code cannot use its name as a device address, so the
-// first call on each device, with that device current, looks the address up
-// with cudaGetSymbolAddress and caches it; make that first call before any
-// stream capture.  All calls share the one array and it keeps whatever the
-// last call left there; the kernels overwrite every partial before reading it,
-// so nothing needs clearing.  Two calls whose work overlaps on the GPU (for
-// example on two streams of the same device) race on the array: serialise
-// them.
+// process exits.  Host code cannot use its name as a device address, so each
+// call looks the address up with cudaGetSymbolAddress, with the call's device
+// current, and keeps it per device.  A call made while its stream is being
+// captured into a CUDA graph uses the kept address instead (a lookup may not
+// be legal then), so the first call on a device must come before any stream
+// capture; calls outside capture look it up again, which also picks up the
+// new address after a cudaDeviceReset.  All calls share the one array and it
+// keeps whatever the last call left there; the kernels overwrite every
+// partial before reading it, so nothing needs clearing.  Two calls whose work
+// overlaps on the GPU (for example on two streams of the same device) race on
+// the array: serialise them.
+#include <atomic>
+
 #include "internal.h"
 #include "repro.h"
 
@@ -28,7 +33,22 @@ namespace {
 static __device__ __align__(256) float g_noalloc_scratch[REPRO_NOALLOC_SCRATCH_FLOATS];
 
 constexpr int kMaxDev = 64;
-float* g_scratch_addr[kMaxDev];
+std::atomic<float*> g_scratch_addr[kMaxDev];   // last looked-up address per device
+
+// the array's device address on device `dev` (current), or nullptr
+float* scratch_address(int dev, cudaStream_t s)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess)
+        return nullptr;
+    if (cs != cudaStreamCaptureStatusNone)
+        return g_scratch_addr[dev].load(std::memory_order_acquire);
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+        return nullptr;
+    g_scratch_addr[dev].store(static_cast<float*>(p), std::memory_order_release);
+    return static_cast<float*>(p);
+}
 
 } // namespace
 } // namespace repro
@@ -54,22 +74,16 @@ extern "C" int repro_wscale_noalloc(const float* x, int64_t n, int mode, int qma
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
         return REPRO_ERR_LAUNCH;
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
-            return REPRO_ERR_LAUNCH;
-        g_scratch_addr[dev] = static_cast<float*>(p);
-    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e;
+    float* scratch = scratch_address(dev, s);
+    if (!scratch)
+        return REPRO_ERR_LAUNCH;   // no lookup possible (e.g. first call inside a capture)
     if (mode == REPRO_SCALE_WEIGHT_MEANABS) {
         // the default block split always: its partials fit the array for every
         // n up to REPRO_NOALLOC_MAX_N
         if (wscale_ws_bytes(n, -1) > sizeof(float) * REPRO_NOALLOC_SCRATCH_FLOATS)
             return REPRO_ERR_SHAPE;
-        e = launch_wscale_meanabs(x, n, qmax, scale_out, g_scratch_addr[dev], -1, s);
-    } else {
-        e = launch_wscale_amax(x, n, qmax, scale_out, g_scratch_addr[dev], amax_grid(n), s);
+        return status_of(launch_wscale_meanabs(x, n, qmax, scale_out, scratch, -1, s));
     }
-    return e == cudaSuccess ? REPRO_OK : REPRO_ERR_LAUNCH;
+    return status_of(launch_wscale_amax(x, n, qmax, scale_out, scratch, amax_grid(n), s));
 }

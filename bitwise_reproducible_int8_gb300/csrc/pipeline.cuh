@@ -1,5 +1,5 @@
 // pipeline.cuh -- shared-memory barrier and tensor-copy helpers for the
-// pipelined kernels (k_fwd_tc.cu, k_bwd_ws.cu, k_bwd_tma.cu).  Every wait is
+// pipelined kernels (k_fwd_tc.cu, k_bwd_tma.cu).  Every wait is
 // bounded: mbar_wait gives up after WAIT_CYCLES and returns false, and the
 // caller records the failure in the device error word and unwinds.
 #pragma once

@@ -19,7 +19,7 @@ REPRO_OK = 0
 STATUS_NAMES = {
     0: "REPRO_OK", -1: "REPRO_ERR_ARG", -2: "REPRO_ERR_SHAPE", -3: "REPRO_ERR_ALIGN",
     -4: "REPRO_ERR_ARCH", -5: "REPRO_ERR_LAUNCH", -6: "REPRO_ERR_TIMEOUT",
-    -7: "REPRO_ERR_WORKSPACE", -8: "REPRO_ERR_ALIAS",
+    -7: "REPRO_ERR_WORKSPACE", -8: "REPRO_ERR_ALIAS", -9: "REPRO_ERR_SELFTEST",
 }
 REPRO_SCALE_WEIGHT_MEANABS = 0
 REPRO_SCALE_ACT_AMAX = 1

@@ -151,7 +151,8 @@ size_t repro_linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K);
  * floats after the segment partials -- and the main kernel reads them with
  * tensor copies; the values, and so the bits, are those defined above.
  * M, N <= 4194240 (REPRO_ERR_SHAPE otherwise).
- * dx and dw must not overlap dy, xq or wq (REPRO_ERR_ALIAS).
+ * dx and dw must not overlap dy, xq or wq, and ws must overlap none of the
+ * other buffers (REPRO_ERR_ALIAS).
  * ------------------------------------------------------------------------ */
 #define REPRO_BWD_DW_ACCUMULATE 1
 int repro_linear_bwd(const float* dy, const int8_t* xq, const int8_t* wq,
@@ -347,14 +348,10 @@ typedef struct {
     int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels and of
                                the activation-scale pass (that one capped at the
                                ceil(n / 64) + 64 partial slots of its workspace) */
-    int bwd_kernel;         /* -1: default (8); 0: plain; 1: register prefetch; 2: staged;
-                               3: staged wide tile; 4: wide tile with the tree in tensor
-                               memory; 5: twelve-warp wide tile; 6: warp-specialised wide
-                               tile (producer and compute warps, tree in tensor memory);
-                               7: operands prepared once per call, then fed by tensor
-                               copies from a producer warp; 8: as 7, the compute warps
-                               issue the copies and keep three tree levels in registers
-                               (2-8 need 16-byte-aligned rows, else 1) */
+    int bwd_kernel;         /* -1: default (8); 8: operands prepared once per call, then fed
+                               to the products by tensor copies (needs 16-byte-aligned rows:
+                               N % 4 == 0 and K % 16 == 0, else 1 runs); 1: register-prefetch
+                               kernel, any row alignment.  Other values: REPRO_ERR_ARG */
 } repro_launch_cfg;
 
 /* ------------------------------------------------------------------------
@@ -368,11 +365,14 @@ typedef struct {
  * scratch is a fixed array of REPRO_NOALLOC_SCRATCH_FLOATS floats (256 KB)
  * inside the library, held by every GPU that loads the library until the
  * process exits.  n may be at most REPRO_NOALLOC_MAX_N (REPRO_ERR_SHAPE
- * otherwise); the block split is always the default one.  The first call on a
- * device, made with that device current, looks up the array's device address
- * (make it before any stream capture).  Calls share the array and race if
- * their work overlaps on the GPU; nothing in it needs clearing.  Allocates
- * nothing.
+ * otherwise); the block split is always the default one.  Each call outside
+ * a stream capture looks up the array's device address on the current device
+ * (so a cudaDeviceReset is picked up by the next such call); a call made
+ * during a capture reuses the address the last lookup on that device found,
+ * so the first call on a device must come before any stream capture (a first
+ * call inside a capture returns REPRO_ERR_LAUNCH and launches nothing).
+ * Calls share the array and race if their work overlaps on the GPU; nothing
+ * in it needs clearing.  Allocates nothing.
  * ------------------------------------------------------------------------ */
 #define REPRO_NOALLOC_SCRATCH_FLOATS 65536
 #define REPRO_NOALLOC_MAX_N 535822336LL   /* 65408 blocks of 8192 elements */

@@ -113,9 +113,9 @@ def test_linear_bwd_argument_checks(L):
 
 def test_bwd_workspace_follows_segments(L):
     try:
-        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=3)
+        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=1)
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 0
-        repro.repro_set_launch_cfg(bwd_segment_log2=4, bwd_kernel=3)
+        repro.repro_set_launch_cfg(bwd_segment_log2=4, bwd_kernel=1)
         # dW: 256 chunks / 16 = 16 segments of N x K partials
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 16 * 2048 * 2048 * 4
         f = L.repro_linear_bwd
@@ -125,14 +125,20 @@ def test_bwd_workspace_follows_segments(L):
         # the tensor-copy kernel adds its prepared operands after the partials:
         # max(dY^T + W^, dY + X^) = 2 * 16384 * 2048 floats here
         opnd = 2 * 16384 * 2048 * 4
-        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=7)
+        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=8)
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == opnd
-        repro.repro_set_launch_cfg(bwd_segment_log2=4, bwd_kernel=7)
+        repro.repro_set_launch_cfg(bwd_segment_log2=4, bwd_kernel=8)
         assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == 16 * 2048 * 2048 * 4 + opnd
-        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=8)   # same region
-        assert repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048) == opnd
+        # the workspace may overlap no operand: the backward writes prepared
+        # operands there before it reads xq / wq / the scales
+        need = repro.repro_linear_bwd_ws_bytes(16384, 2048, 2048)
+        args = [B, B * 2, B * 3, B * 4, B * 4 + 4, B * 5, B * 6, 16384, 2048, 2048, 0]
+        assert f(*args, B * 8, need, None) != -8   # (no GPU here: arch or launch status)
+        assert f(*args, B * 2, need, None) == -8   # ws overlaps xq
+        assert f(*args, B * 3, need, None) == -8   # ws overlaps wq
+        assert f(*args, B * 4 - 16, need, None) == -8   # ws overlaps s_x and s_w
         # rows that are not 16-byte aligned take the register-prefetch kernel: no operand region
-        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=7)
+        repro.repro_set_launch_cfg(bwd_segment_log2=8, bwd_kernel=8)
         assert repro.repro_linear_bwd_ws_bytes(64, 30, 20) == 0
     finally:
         repro.repro_set_launch_cfg(reset=True)
@@ -163,8 +169,10 @@ def test_launch_cfg_validation(L):
             repro.repro_set_launch_cfg(reduce_block_log2=11)
         with pytest.raises(repro.ReproError):
             repro.repro_set_launch_cfg(fwd_path=3)
-        with pytest.raises(repro.ReproError):
-            repro.repro_set_launch_cfg(bwd_kernel=9)
+        for k in (0, 2, 7, 9):   # only the two shipped kernels, 1 and 8
+            with pytest.raises(repro.ReproError):
+                repro.repro_set_launch_cfg(bwd_kernel=k)
+        repro.repro_set_launch_cfg(bwd_kernel=1)
         repro.repro_set_launch_cfg(bwd_kernel=8)
         repro.repro_set_launch_cfg(fwd_path=2)
         repro.repro_set_launch_cfg(bwd_segment_log2=0, reduce_block_log2=0, fwd_path=0,

@@ -31,7 +31,7 @@ WL = inputs.Workload("audit_small", 256,
 
 CONFIGS = [
     {},
-    {"bwd_kernel": 3, "bwd_segment_log2": 0, "elementwise_blocks": 7, "reduce_block_log2": 2,
+    {"bwd_kernel": 8, "bwd_segment_log2": 0, "elementwise_blocks": 7, "reduce_block_log2": 2,
      "fwd_path": 0},
     {"bwd_kernel": 1, "bwd_segment_log2": 1, "elementwise_blocks": 1, "reduce_block_log2": 0},
 ]

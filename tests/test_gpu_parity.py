@@ -179,12 +179,16 @@ def test_forward_adversarial(orc, K, path):
 
 # ----------------------------------------------------------------- backward
 
+# the two shipped backward kernels: 8 (default, tensor-copy fed, 16-byte-aligned
+# rows) and 1 (register prefetch, any rows); unaligned shapes run 1 either way
+BWD_KERNELS = [1, 8]
+
 BWD_SHAPES = [(1, 1, 1), (3, 1, 5), (64, 128, 256), (200, 130, 70), (257, 64, 65),
               (130, 257, 96), (64, 64, 64), (1000, 300, 17), (96, 4100, 20),
               (257, 68, 96), (100, 4100, 32), (1000, 300, 16), (70, 132, 48), (300, 260, 80)]
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("kernel", BWD_KERNELS)
 @pytest.mark.parametrize("M,N,K", BWD_SHAPES)
 def test_backward(orc, M, N, K, kernel):
     R.repro_set_launch_cfg(bwd_kernel=kernel)
@@ -198,7 +202,7 @@ def test_backward(orc, M, N, K, kernel):
     G.assert_bits_equal(dw, orc.linear_bwd_dw(dy, xq, s_x), f"dw {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("kernel", BWD_KERNELS)
 @pytest.mark.parametrize("seg", [0, 1, 2, 3, 4, 8])
 def test_backward_launch_invariance(orc, seg, kernel):
     # long reductions split into aligned segments of 2^seg chunks, by either kernel
@@ -256,11 +260,11 @@ def test_backward_flush_cases(orc):
         G.assert_bits_equal(dx, orc.linear_bwd_dx(dy, wq, s_w), f"flush s_w={s_w}")
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("kernel", BWD_KERNELS)
 def test_backward_subnormal_dy_every_kernel(orc, kernel):
     # subnormal upstream gradients against codes of 127 at scale 1: unflushed,
     # 1e-40 (x) 127 = 1.27e-38 would be a normal product, so a missed flush of
-    # dY changes dX and dW; the shape is aligned, so kernels 2-8 take their
+    # dY changes dX and dW; the shape is aligned, so kernel 8 takes its
     # fast paths (dW over 130 tokens: three chunks, a ragged tail)
     R.repro_set_launch_cfg(bwd_kernel=kernel)
     rng = np.random.default_rng(40)
@@ -303,7 +307,7 @@ def test_backward_empty_reduction(orc):
     assert np.all(G.host(dx).view(np.uint32) == 0)
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("kernel", BWD_KERNELS)
 def test_zero_weights_and_activations_every_kernel(orc, kernel):
     # all-zero W and X: both scales are +0, every code is 0, and every
     # backward product is a signed zero, so the sign of each dX and dW element

@@ -5,7 +5,8 @@ device memory -- their allocations belong to another owner, or their loop must
 never call cudaMalloc because it would synchronise the device.  Its scratch is
 a fixed array inside the library that every call reuses, so these tests call it
 through the C ABI several times in a row, on inputs of different sizes, and
-require exactly the bits of repro_wscale (which takes a caller workspace).
+require exactly the bits of the CPU oracle and of repro_wscale (which takes a
+caller workspace), up to the largest size the header accepts.
 This file is collected last on purpose.
 """
 import ctypes
@@ -35,21 +36,50 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("mode", [0, 1])
-def test_noalloc_matches_the_workspace_entry_point(mode):
+def test_noalloc_matches_the_workspace_entry_point(orc, mode):
     R.repro_set_launch_cfg(reset=True)
     rng = np.random.default_rng(42 + mode)
     # the largest first: the calls after it reuse a scratch array that still
     # holds its partials
     sizes = [23068672, 8192 * 3 + 17, 1000, 1]
     for n in sizes:
-        x = torch.from_numpy((rng.standard_normal(n) * 0.02).astype(np.float32)).cuda()
+        xh = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        x = torch.from_numpy(xh).cuda()
+        ref = torch.empty(1, device="cuda")
+        R.repro_wscale(x, mode, ref)
+        exp = int(np.float32(orc.wscale(xh, mode)).view(np.int32))
+        assert _bits(ref) == exp, (mode, n)
+        for _ in range(2):
+            out = torch.full((1,), float("nan"), device="cuda")
+            assert _noalloc(x, mode, out) == R.REPRO_OK
+            torch.cuda.synchronize()
+            assert _bits(out) == exp, (mode, n)
+    assert R.repro_device_check() == R.REPRO_OK
+
+
+def test_noalloc_at_the_largest_accepted_size(orc):
+    # n = REPRO_NOALLOC_MAX_N fills the scratch array exactly with the weight
+    # scale's partials (65408 block sums, then the tree pass's and the slack);
+    # 2.1 GB of fp32 on the device
+    n = REPRO_NOALLOC_MAX_N
+    xh = np.empty(n, dtype=np.float32)
+    step = 1 << 24
+    for lo in range(0, n, step):   # a fixed mixed-sign pattern, built in slices
+        i = np.arange(lo, min(lo + step, n), dtype=np.int64)
+        xh[lo:lo + i.size] = (i * 7919 % 2001 - 1000).astype(np.float32) * np.float32(1e-5)
+    x = torch.from_numpy(xh).cuda()
+    for mode in (0, 1):
+        exp = int(np.float32(orc.wscale(xh, mode)).view(np.int32))
         ref = torch.empty(1, device="cuda")
         R.repro_wscale(x, mode, ref)
         for _ in range(2):
             out = torch.full((1,), float("nan"), device="cuda")
             assert _noalloc(x, mode, out) == R.REPRO_OK
             torch.cuda.synchronize()
-            assert _bits(out) == _bits(ref), (mode, n)
+            assert _bits(out) == exp, mode
+        assert _bits(ref) == exp, mode
+    del x
+    torch.cuda.empty_cache()
     assert R.repro_device_check() == R.REPRO_OK
 
 
