@@ -69,63 +69,68 @@ _i64 = ctypes.c_int64
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        path = build()
-        L = ctypes.CDLL(path)
-        sig = {
-            "oracle_flush": (ctypes.c_float, [ctypes.c_float]),
-            "oracle_add": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
-            "oracle_mul": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
-            "oracle_div": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
-            "oracle_sqrt": (ctypes.c_float, [ctypes.c_float]),
-            "oracle_i2f": (ctypes.c_float, [_i64]),
-            "oracle_quant_one": (ctypes.c_int, [ctypes.c_float, ctypes.c_float, ctypes.c_int]),
-            "oracle_canon_sum": (ctypes.c_float, [_f32p, _i64]),
-            "oracle_wscale": (ctypes.c_float, [_f32p, _i64, ctypes.c_int, ctypes.c_int]),
-            "oracle_quant_i8": (None, [_f32p, _i64, ctypes.c_float, ctypes.c_int, _i8p]),
-            "oracle_linear_fwd": (None, [_i8p, _i8p, ctypes.c_float, ctypes.c_float, _f32p,
-                                         _i64, _i64, _i64]),
-            "oracle_linear_fwd_at": (None, [_i8p, _i8p, ctypes.c_float, ctypes.c_float,
-                                            _i64, _i64, _i64, _i64p, _i64p, _i64, _f32p]),
-            "oracle_int_dot": (ctypes.c_int64, [_i8p, _i8p, _i64, _i64, _i64]),
-            "oracle_linear_bwd_dx": (None, [_f32p, _i8p, ctypes.c_float, _f32p, _i64, _i64, _i64]),
-            "oracle_linear_bwd_dw": (None, [_f32p, _i8p, ctypes.c_float, _f32p, _i64, _i64, _i64]),
-            "oracle_linear_bwd_dx_at": (None, [_f32p, _i8p, ctypes.c_float, _i64, _i64, _i64,
-                                               _i64p, _i64p, _i64, _f32p]),
-            "oracle_linear_bwd_dw_at": (None, [_f32p, _i8p, ctypes.c_float, _i64, _i64, _i64,
-                                               _i64p, _i64p, _i64, _f32p]),
-            "oracle_grad_accum": (None, [_f32p, _f32p, _i64]),
-            "oracle_running_sum": (None, [ctypes.POINTER(_f32p), ctypes.c_int, _i64, _f32p]),
-            "oracle_treefold_one": (ctypes.c_float, [_f32p, ctypes.c_int]),
-            "oracle_treefold": (None, [ctypes.POINTER(_f32p), ctypes.c_int, _i64, _f32p]),
-            "oracle_treefold_all_ranks": (None, [_f32p, ctypes.c_int, _f32p]),
-            "oracle_threads": (ctypes.c_int, []),
-            "oracle_sumsq": (ctypes.c_float, [_f32p, _i64]),
-            "oracle_pow_t": (ctypes.c_float, [ctypes.c_float, _i64]),
-            "oracle_clip_coef": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
-            "oracle_adamw_step": (None, [_f32p, _f32p, _f32p, _f32p, _i64, ctypes.c_float,
-                                         ctypes.POINTER(AdamWHparams), _i64]),
-            "oracle_exp": (ctypes.c_float, [ctypes.c_float]),
-            "oracle_attn_quant_p": (ctypes.c_int, [ctypes.c_float]),
-            "oracle_attn_fx": (ctypes.c_int64, [ctypes.c_float]),
-            "oracle_attn_fix2f": (ctypes.c_float, [_i64]),
-            "oracle_attn_fwd": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p, _f32p,
-                                       _i64, _i64, _i64, _i64, _i64, _i64]),
-            "oracle_attn_fwd_rows": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _i64p, _i64,
-                                            _f32p, _f32p, _f32p, _i64, _i64, _i64, _i64, _i64,
-                                            _i64]),
-            "oracle_attn_bwd": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p, _f32p,
-                                       _f32p, _f32p, _f32p, _f32p, _i64, _i64, _i64, _i64, _i64,
-                                       _i64]),
-            "oracle_attn_bwd_rows": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p,
-                                            _f32p, _f32p, _i64p, _i64, _f32p, _i64p, _i64, _f32p,
-                                            _f32p, _i64, _i64, _i64, _i64, _i64, _i64]),
-        }
-        for name, (res, args) in sig.items():
-            fn = getattr(L, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = L
+        _lib = load(build())
     return _lib
+
+
+def load(path: str) -> ctypes.CDLL:
+    """Open a compiled oracle library at `path` and declare its signatures
+    (the tests also load copies built with a planted mistake)."""
+    L = ctypes.CDLL(path)
+    sig = {
+        "oracle_flush": (ctypes.c_float, [ctypes.c_float]),
+        "oracle_add": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+        "oracle_mul": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+        "oracle_div": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+        "oracle_sqrt": (ctypes.c_float, [ctypes.c_float]),
+        "oracle_i2f": (ctypes.c_float, [_i64]),
+        "oracle_quant_one": (ctypes.c_int, [ctypes.c_float, ctypes.c_float, ctypes.c_int]),
+        "oracle_canon_sum": (ctypes.c_float, [_f32p, _i64]),
+        "oracle_wscale": (ctypes.c_float, [_f32p, _i64, ctypes.c_int, ctypes.c_int]),
+        "oracle_quant_i8": (None, [_f32p, _i64, ctypes.c_float, ctypes.c_int, _i8p]),
+        "oracle_linear_fwd": (None, [_i8p, _i8p, ctypes.c_float, ctypes.c_float, _f32p,
+                                     _i64, _i64, _i64]),
+        "oracle_linear_fwd_at": (None, [_i8p, _i8p, ctypes.c_float, ctypes.c_float,
+                                        _i64, _i64, _i64, _i64p, _i64p, _i64, _f32p]),
+        "oracle_int_dot": (ctypes.c_int64, [_i8p, _i8p, _i64, _i64, _i64]),
+        "oracle_linear_bwd_dx": (None, [_f32p, _i8p, ctypes.c_float, _f32p, _i64, _i64, _i64]),
+        "oracle_linear_bwd_dw": (None, [_f32p, _i8p, ctypes.c_float, _f32p, _i64, _i64, _i64]),
+        "oracle_linear_bwd_dx_at": (None, [_f32p, _i8p, ctypes.c_float, _i64, _i64, _i64,
+                                           _i64p, _i64p, _i64, _f32p]),
+        "oracle_linear_bwd_dw_at": (None, [_f32p, _i8p, ctypes.c_float, _i64, _i64, _i64,
+                                           _i64p, _i64p, _i64, _f32p]),
+        "oracle_grad_accum": (None, [_f32p, _f32p, _i64]),
+        "oracle_running_sum": (None, [ctypes.POINTER(_f32p), ctypes.c_int, _i64, _f32p]),
+        "oracle_treefold_one": (ctypes.c_float, [_f32p, ctypes.c_int]),
+        "oracle_treefold": (None, [ctypes.POINTER(_f32p), ctypes.c_int, _i64, _f32p]),
+        "oracle_treefold_all_ranks": (None, [_f32p, ctypes.c_int, _f32p]),
+        "oracle_threads": (ctypes.c_int, []),
+        "oracle_sumsq": (ctypes.c_float, [_f32p, _i64]),
+        "oracle_pow_t": (ctypes.c_float, [ctypes.c_float, _i64]),
+        "oracle_clip_coef": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
+        "oracle_adamw_step": (None, [_f32p, _f32p, _f32p, _f32p, _i64, ctypes.c_float,
+                                     ctypes.POINTER(AdamWHparams), _i64]),
+        "oracle_exp": (ctypes.c_float, [ctypes.c_float]),
+        "oracle_attn_quant_p": (ctypes.c_int, [ctypes.c_float]),
+        "oracle_attn_fx": (ctypes.c_int64, [ctypes.c_float]),
+        "oracle_attn_fix2f": (ctypes.c_float, [_i64]),
+        "oracle_attn_fwd": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p, _f32p,
+                                   _i64, _i64, _i64, _i64, _i64, _i64]),
+        "oracle_attn_fwd_rows": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _i64p, _i64,
+                                        _f32p, _f32p, _f32p, _i64, _i64, _i64, _i64, _i64,
+                                        _i64]),
+        "oracle_attn_bwd": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p, _f32p,
+                                   _f32p, _f32p, _f32p, _f32p, _i64, _i64, _i64, _i64, _i64,
+                                   _i64]),
+        "oracle_attn_bwd_rows": (None, [_f32p, _f32p, _i8p, ctypes.c_float, _f32p, _f32p,
+                                        _f32p, _f32p, _i64p, _i64, _f32p, _i64p, _i64, _f32p,
+                                        _f32p, _i64, _i64, _i64, _i64, _i64, _i64]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
 
 
 # ---------------------------------------------------------------- helpers

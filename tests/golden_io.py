@@ -64,3 +64,41 @@ def sha256_vectors():
     for line in _lines("sha256_vectors.txt"):
         msg, dig = line.split()
         yield (b"" if msg == "-" else bytes.fromhex(msg)), bytes.fromhex(dig)
+
+
+def _value(tok: str) -> float:
+    """A decimal literal or a signed power of two written as [-]2^e."""
+    if "^" in tok:
+        neg = tok.startswith("-")
+        base, e = tok.lstrip("-").split("^")
+        assert base == "2"
+        v = 2.0 ** int(e)
+        return -v if neg else v
+    return float(tok)
+
+
+def _range(tok: str):
+    lo, _, hi = tok.partition("-")
+    return int(lo), int(hi) if hi else int(lo)
+
+
+def attn_order_cases():
+    """Yields dicts: name, kind, T, W, Hq, Hkv, row, col, bits, times_c and
+    assign = [(tensor, i_lo, i_hi, h, d_lo, d_hi, value)]."""
+    for line in _lines("attn_order.txt"):
+        toks = line.split()
+        name, kind = toks[0], toks[1]
+        T, W, Hq, Hkv, row, col = (int(t) for t in toks[2:8])
+        exp = toks[8]
+        times_c = exp.startswith("c*")
+        bits = int(exp[2:] if times_c else exp, 16)
+        assign = []
+        for a in toks[9:]:
+            lhs, val = a.split("=")
+            tensor, idx = lhs.split("[")
+            i_t, h_t, d_t = idx.rstrip("]").split(",")
+            i_lo, i_hi = _range(i_t)
+            d_lo, d_hi = _range(d_t)
+            assign.append((tensor, i_lo, i_hi, int(h_t), d_lo, d_hi, _value(val)))
+        yield dict(name=name, kind=kind, T=T, W=W, Hq=Hq, Hkv=Hkv, row=row, col=col, bits=bits,
+                   times_c=times_c, assign=assign)
