@@ -285,6 +285,98 @@ int repro_quant_i8(const float* x, int64_t n, const float* scale, int qmax, int8
                                   as_stream(stream)));
 }
 
+size_t repro_wscale_multi_ws_bytes(const int64_t* ns, int count)
+{
+    if (!ns || count < 1 || count > REPRO_MAX_TENSORS)
+        return 0;
+    for (int t = 0; t < count; ++t)
+        if (ns[t] <= 0)
+            return 0;
+    return wscale_multi_ws_bytes(ns, count);
+}
+
+int repro_wscale_multi(const float* const* xs, const int64_t* ns, int count, int mode, int qmax,
+                       float* scales_out, void* ws, size_t ws_bytes, void* stream)
+{
+    if (!xs || !ns || !scales_out || count < 1 || count > REPRO_MAX_TENSORS)
+        return REPRO_ERR_ARG;
+    if (mode != REPRO_SCALE_WEIGHT_MEANABS && mode != REPRO_SCALE_ACT_AMAX)
+        return REPRO_ERR_ARG;
+    if (qmax != REPRO_QMAX)
+        return REPRO_ERR_ARG;
+    for (int t = 0; t < count; ++t) {
+        if (!xs[t])
+            return REPRO_ERR_ARG;
+        if (ns[t] <= 0)
+            return REPRO_ERR_SHAPE;
+        if (!al16(xs[t]))
+            return REPRO_ERR_ALIGN;
+    }
+    if (!al4(scales_out))
+        return REPRO_ERR_ALIGN;
+    const size_t need = wscale_multi_ws_bytes(ns, count);
+    if (!ws || ws_bytes < need)
+        return REPRO_ERR_WORKSPACE;
+    if (!al16(ws))
+        return REPRO_ERR_ALIGN;
+    const size_t sb = (size_t)count * 4;
+    if (overlap(ws, ws_bytes, scales_out, sb))
+        return REPRO_ERR_ALIAS;
+    for (int t = 0; t < count; ++t)
+        if (overlap(ws, ws_bytes, xs[t], (size_t)ns[t] * 4) ||
+            overlap(scales_out, sb, xs[t], (size_t)ns[t] * 4))
+            return REPRO_ERR_ALIAS;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_wscale_multi(xs, ns, count, mode, qmax, scales_out, ws,
+                                         g_cfg.reduce_block_log2, as_stream(stream)));
+}
+
+int repro_quant_i8_multi(const float* const* xs, const int64_t* ns, int count,
+                         const float* scales, int qmax, int8_t* const* q_outs, void* stream)
+{
+    if (!xs || !ns || !q_outs || !scales || count < 1 || count > REPRO_MAX_TENSORS)
+        return REPRO_ERR_ARG;
+    if (qmax != REPRO_QMAX)
+        return REPRO_ERR_ARG;
+    int64_t total = 0;
+    for (int t = 0; t < count; ++t) {
+        if (ns[t] < 0)
+            return REPRO_ERR_SHAPE;
+        if (ns[t] == 0)
+            continue;
+        if (!xs[t] || !q_outs[t])
+            return REPRO_ERR_ARG;
+        if (!al16(xs[t]) || !al16(q_outs[t]))
+            return REPRO_ERR_ALIGN;
+        total += ns[t];
+    }
+    if (!al4(scales))
+        return REPRO_ERR_ALIGN;
+    const size_t sb = (size_t)count * 4;
+    for (int t = 0; t < count; ++t) {
+        if (ns[t] == 0)
+            continue;
+        if (overlap(q_outs[t], (size_t)ns[t], scales, sb))
+            return REPRO_ERR_ALIAS;
+        for (int u = 0; u < count; ++u) {
+            if (ns[u] == 0)
+                continue;
+            if (overlap(q_outs[t], (size_t)ns[t], xs[u], (size_t)ns[u] * 4) ||
+                (u != t && overlap(q_outs[t], (size_t)ns[t], q_outs[u], (size_t)ns[u])))
+                return REPRO_ERR_ALIAS;
+        }
+    }
+    if (total == 0)
+        return REPRO_OK;
+    int st = check_arch();
+    if (st != REPRO_OK)
+        return st;
+    return status_of(launch_quant_multi(xs, ns, count, scales, qmax, q_outs,
+                                        stream_grid(total / 16, 32), as_stream(stream)));
+}
+
 size_t repro_linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (!use_tc(M, N, K))

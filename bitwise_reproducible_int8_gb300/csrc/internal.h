@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #define REPRO_MAX_PARTS_INTERNAL 64
+#define REPRO_MAX_TENSORS_INTERNAL 64
 
 namespace repro {
 
@@ -33,6 +34,11 @@ cudaError_t launch_wscale_meanabs(const float* x, int64_t n, int qmax, float* sc
 cudaError_t launch_wscale_amax(const float* x, int64_t n, int qmax, float* scale_out,
                                void* ws, int grid, cudaStream_t st);
 int amax_grid(int64_t n);
+// several tensors in one pass: scales[t] of xs[t] (mode 0 weight, 1 activation)
+size_t wscale_multi_ws_bytes(const int64_t* ns, int count);
+cudaError_t launch_wscale_multi(const float* const* xs, const int64_t* ns, int count, int mode,
+                                int qmax, float* scales, void* ws, int block_log2,
+                                cudaStream_t st);
 
 cudaError_t launch_sumsq(const float* x, int64_t n, float* out, void* ws, int block_log2,
                          cudaStream_t st);
@@ -48,6 +54,9 @@ cudaError_t launch_adamw(float* p, float* m, float* v, const float* g, int64_t n
 // ---- quantiser (k_quant.cu)
 cudaError_t launch_quant(const float* x, int64_t n, const float* scale, int qmax, int8_t* q,
                          int grid, cudaStream_t st);
+cudaError_t launch_quant_multi(const float* const* xs, const int64_t* ns, int count,
+                               const float* scales, int qmax, int8_t* const* qs, int grid,
+                               cudaStream_t st);
 
 // ---- forward (k_fwd.cu)
 cudaError_t launch_fwd_cuda_core(const int8_t* xq, const int8_t* wq, const float* s_x,

@@ -36,17 +36,16 @@ __device__ __forceinline__ float term(float x)
     return SQUARE ? fmul_rn(x, x) : fabsf(x);
 }
 
+// the canonical sum of block `blk` (chunks [blk*2^k, (blk+1)*2^k)) of x into *out
 template <int SQUARE>
-__global__ void __launch_bounds__(P1_CHUNKS)
-k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __restrict__ part)
+__device__ __forceinline__ void absum_block(const float* __restrict__ x, int64_t n, int blk_log2,
+                                            int64_t blk, float* __restrict__ out)
 {
     __shared__ float4 S[P1_CHUNKS * 16];
     __shared__ float T[P1_CHUNKS];
-    pdl_wait();
-    pdl_trigger();
     const int nb = 1 << blk_log2;
     const int64_t C = (n + 63) >> 6;
-    const int64_t c0 = (int64_t)blockIdx.x * nb;
+    const int64_t c0 = blk * nb;
     const int cnt = (int)min((int64_t)nb, C - c0);
     const int64_t e0 = c0 * 64;
 
@@ -119,7 +118,16 @@ k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __re
         __syncthreads();
     }
     if (threadIdx.x == 0)
-        part[blockIdx.x] = T[0];
+        *out = T[0];
+}
+
+template <int SQUARE>
+__global__ void __launch_bounds__(P1_CHUNKS)
+k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __restrict__ part)
+{
+    pdl_wait();
+    pdl_trigger();
+    absum_block<SQUARE>(x, n, blk_log2, blockIdx.x, part + blockIdx.x);
 }
 
 // s_w = (2 (x) (S (/) float(n))) (/) sqrt(float(q_max)); every operand and
@@ -235,6 +243,129 @@ k_amax_final(const float* __restrict__ part, int cnt, int qmax, float* __restric
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// ------------------------------------------------------- several tensors
+
+// The tensors of one call: phase-1 blocks of all of them form one grid, the
+// blocks of tensor t being [blk0[t], blk0[t+1]).
+struct MultiArgs {
+    const float* x[REPRO_MAX_TENSORS_INTERNAL];
+    int64_t n[REPRO_MAX_TENSORS_INTERNAL];
+    int64_t blk0[REPRO_MAX_TENSORS_INTERNAL + 1];
+    int count;
+};
+
+// tensor owning phase-1 block b (blk0 ascending, blk0[0] = 0)
+__device__ __forceinline__ int tensor_of(const MultiArgs& a, int64_t b)
+{
+    int lo = 0, hi = a.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.blk0[mid] <= b)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(P1_CHUNKS)
+k_absum_chunks_multi(const __grid_constant__ MultiArgs a, int blk_log2, float* __restrict__ part)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int t = tensor_of(a, blockIdx.x);
+    absum_block<0>(a.x[t], a.n[t], blk_log2, blockIdx.x - a.blk0[t], part + blockIdx.x);
+}
+
+constexpr int TREE_MULTI_MAX = 8192;   // block partials one tree CTA holds
+
+// one CTA per tensor: the stride-doubling tree over the tensor's block
+// partials (at most TREE_MULTI_MAX), then its weight scale
+__global__ void __launch_bounds__(1024)
+k_tree_multi(const __grid_constant__ MultiArgs a, const float* __restrict__ part, int qmax,
+             float* __restrict__ scales)
+{
+    __shared__ float T[TREE_MULTI_MAX];
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x;
+    const int64_t b0 = a.blk0[t];
+    const int cnt = (int)(a.blk0[t + 1] - b0);
+    for (int j = threadIdx.x; j < cnt; j += blockDim.x)
+        T[j] = part[b0 + j];
+    __syncthreads();
+    for (int s = 1; s < cnt; s <<= 1) {
+        for (int j = threadIdx.x * 2 * s; j + s < cnt; j += blockDim.x * 2 * s)
+            T[j] = fadd_ftz(T[j], T[j + s]);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0)
+        scales[t] = weight_scale_from_sum(T[0], a.n[t], qmax);
+}
+
+constexpr int AMAX_BLOCK = 8192;   // elements per phase-1 CTA of the multi amax
+
+__global__ void __launch_bounds__(256)
+k_amax_multi(const __grid_constant__ MultiArgs a, float* __restrict__ part)
+{
+    pdl_wait();
+    pdl_trigger();
+    const int t = tensor_of(a, blockIdx.x);
+    const float* x = a.x[t];
+    const int64_t n = a.n[t];
+    const int64_t e0 = (int64_t)(blockIdx.x - a.blk0[t]) * AMAX_BLOCK;
+    float m = 0.f;
+    if (e0 + AMAX_BLOCK <= n) {
+        const float4* x4 = reinterpret_cast<const float4*>(x + e0);
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            v[u] = ld_stream(x4 + threadIdx.x + u * 256);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            m = fmaxf(m, fmaxf(fmaxf(absflush(v[u].x), absflush(v[u].y)),
+                               fmaxf(absflush(v[u].z), absflush(v[u].w))));
+    } else {
+        for (int64_t e = e0 + threadIdx.x; e < n; e += 256)
+            m = fmaxf(m, absflush(x[e]));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float W[8];
+    if ((threadIdx.x & 31) == 0)
+        W[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 8; ++w)
+            m = fmaxf(m, W[w]);
+        part[blockIdx.x] = m;
+    }
+}
+
+__global__ void __launch_bounds__(1024)
+k_amax_final_multi(const __grid_constant__ MultiArgs a, const float* __restrict__ part, int qmax,
+                   float* __restrict__ scales)
+{
+    pdl_wait();
+    const int t = blockIdx.x;
+    float m = 0.f;
+    for (int64_t i = a.blk0[t] + threadIdx.x; i < a.blk0[t + 1]; i += blockDim.x)
+        m = fmaxf(m, part[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __shared__ float W[32];
+    if ((threadIdx.x & 31) == 0)
+        W[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < 32; ++w)
+            m = fmaxf(m, W[w]);
+        scales[t] = flush(__fdiv_rn(m, __int2float_rn(qmax)));
+    }
+}
+
 } // namespace
 
 // Phase-1 block of 2^min(k,7) chunks, tree passes of 2^max(k,1) partials
@@ -316,6 +447,73 @@ int amax_grid(int64_t n)
     const int64_t want = cdiv(n, 256 * 4 * 4);
     const int64_t cap = (int64_t)num_sms() * 4;
     return (int)(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+// phase-1 blocks per tensor for the multi-tensor calls: 2^p1 chunks each
+// (weight scale) or AMAX_BLOCK elements (activation scale)
+static int64_t multi_blocks(int64_t n, int mode, int p1)
+{
+    return mode == 0 ? cdiv(cdiv(n, 64), (int64_t)1 << p1) : cdiv(n, AMAX_BLOCK);
+}
+
+size_t wscale_multi_ws_bytes(const int64_t* ns, int count)
+{
+    // the block partials of every tensor at the finest split (one chunk per
+    // block, the launch-configuration hook's smallest), or one tensor's
+    // workspace on the multi-pass path, whichever is larger
+    int64_t total = 0, single = 0;
+    for (int t = 0; t < count; ++t) {
+        total += cdiv(ns[t], 64) + 64;
+        const int64_t one = (int64_t)(wscale_ws_bytes(ns[t], 0) / sizeof(float));
+        single = one > single ? one : single;
+    }
+    return (size_t)((total > single ? total : single) + 64) * sizeof(float);
+}
+
+cudaError_t launch_wscale_multi(const float* const* xs, const int64_t* ns, int count, int mode,
+                                int qmax, float* scales, void* ws, int block_log2,
+                                cudaStream_t st)
+{
+    int p1, p2;
+    split_blocks(block_log2, p1, p2);
+    MultiArgs a;
+    a.count = count;
+    a.blk0[0] = 0;
+    bool one_pass = true;
+    for (int t = 0; t < count; ++t) {
+        a.x[t] = xs[t];
+        a.n[t] = ns[t];
+        const int64_t nb = multi_blocks(ns[t], mode, p1);
+        a.blk0[t + 1] = a.blk0[t] + nb;
+        if (mode == 0 && nb > TREE_MULTI_MAX)
+            one_pass = false;
+    }
+    if (!one_pass) {
+        // a tensor too large for one tree CTA: each tensor on its own,
+        // through the single-tensor passes (same bits)
+        for (int t = 0; t < count; ++t) {
+            cudaError_t e = canonical_sum(xs[t], ns[t], 0, qmax, scales + t, ws, block_log2, st);
+            if (e != cudaSuccess)
+                return e;
+        }
+        return cudaSuccess;
+    }
+    float* part = static_cast<float*>(ws);
+    const unsigned grid = (unsigned)a.blk0[count];
+    cudaError_t e;
+    if (mode == 0) {
+        e = launch_pdl(k_absum_chunks_multi, dim3(grid), dim3(P1_CHUNKS), 0, st, a, p1, part);
+        if (e == cudaSuccess)
+            e = launch_pdl(k_tree_multi, dim3((unsigned)count), dim3(1024), 0, st, a,
+                           (const float*)part, qmax, scales);
+    } else {
+        e = launch_pdl(k_amax_multi, dim3(grid), dim3(256), 0, st, a, part);
+        if (e == cudaSuccess)
+            e = launch_pdl(k_amax_final_multi, dim3((unsigned)count), dim3(1024), 0, st, a,
+                           (const float*)part, qmax, scales);
+    }
+    count_launches(2);
+    return e;
 }
 
 cudaError_t launch_wscale_amax(const float* x, int64_t n, int qmax, float* scale_out, void* ws,

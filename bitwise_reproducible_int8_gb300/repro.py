@@ -56,6 +56,11 @@ _SIGNATURES = {
     "repro_wscale_ws_bytes": (_sz, [_i64]),
     "repro_wscale_noalloc": (_int, [_vp, _i64, _int, _int, _vp, _vp]),
     "repro_quant_i8": (_int, [_vp, _i64, _vp, _int, _vp, _vp]),
+    "repro_wscale_multi": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_i64), _int, _int, _int,
+                                  _vp, _vp, _sz, _vp]),
+    "repro_wscale_multi_ws_bytes": (_sz, [ctypes.POINTER(_i64), _int]),
+    "repro_quant_i8_multi": (_int, [ctypes.POINTER(_vp), ctypes.POINTER(_i64), _int, _vp, _int,
+                                    ctypes.POINTER(_vp), _vp]),
     "repro_linear_fwd": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _vp]),
     "repro_linear_fwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
     "repro_linear_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int,
@@ -183,6 +188,44 @@ def repro_quant_i8(x: torch.Tensor, scale: torch.Tensor, q_out: torch.Tensor,
     _check("repro_quant_i8", lib().repro_quant_i8(
         _ptr(x, torch.float32, "x"), x.numel(), _ptr(scale, torch.float32, "scale"), int(qmax),
         _ptr(q_out, torch.int8, "q_out"), _stream(stream)))
+
+
+def _tables(tensors, dtype, name):
+    n = len(tensors)
+    ptrs = (_vp * max(n, 1))(*[_ptr(t, dtype, name) for t in tensors])
+    sizes = (_i64 * max(n, 1))(*[int(t.numel()) for t in tensors])
+    return ptrs, sizes
+
+
+def repro_wscale_multi_ws_bytes(sizes) -> int:
+    arr = (_i64 * max(len(sizes), 1))(*[int(v) for v in sizes])
+    return int(lib().repro_wscale_multi_ws_bytes(arr, len(sizes)))
+
+
+def repro_wscale_multi(xs, mode: int, scales_out: torch.Tensor, ws=None,
+                       qmax: int = REPRO_QMAX, stream=None) -> None:
+    """scales_out[t] <- the scale of xs[t] (mode 0 weight, 1 activation) for
+    every t, in one pass; the bits of repro_wscale on each tensor."""
+    ptrs, sizes = _tables(xs, torch.float32, "x")
+    if scales_out.numel() < len(xs):
+        raise ValueError("scales_out needs one float per tensor")
+    if ws is None:
+        ws = _workspace(repro_wscale_multi_ws_bytes([x.numel() for x in xs]), xs[0].device)
+    _check("repro_wscale_multi", lib().repro_wscale_multi(
+        ptrs, sizes, len(xs), int(mode), int(qmax), _ptr(scales_out, torch.float32, "scales_out"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def repro_quant_i8_multi(xs, scales: torch.Tensor, q_outs, qmax: int = REPRO_QMAX,
+                         stream=None) -> None:
+    """q_outs[t] <- int8 codes of xs[t] with scales[t], every t in one launch."""
+    if len(q_outs) != len(xs) or any(q.numel() != x.numel() for q, x in zip(q_outs, xs)):
+        raise ValueError("one q_out of x's size per tensor")
+    ptrs, sizes = _tables(xs, torch.float32, "x")
+    qptrs, _ = _tables(q_outs, torch.int8, "q_out")
+    _check("repro_quant_i8_multi", lib().repro_quant_i8_multi(
+        ptrs, sizes, len(xs), _ptr(scales, torch.float32, "scales"), int(qmax), qptrs,
+        _stream(stream)))
 
 
 def repro_linear_fwd_ws_bytes(M: int, N: int, K: int) -> int:

@@ -1,7 +1,8 @@
 """One step of the hot path over a workload, through the C ABI.
 
-A step is, for every linear of the workload:
-  re-pin the weight scale and quantise the weights (once per step);
+A step is, for the linears of the workload:
+  re-pin every weight scale, then quantise every weight (once per step, one
+  multi-tensor call each);
 then for every micro-batch j and linear i:
   activation scale -> quantise X -> int8 forward -> dX -> dW, with dW
   accumulated into the linear's gradient in micro-batch order (level 1 of the
@@ -101,6 +102,9 @@ class HotPathStep:
         n_max = max(n_max, *(x.numel() for i in range(L) for x in self.X[i]))
         self.ws_scale = torch.empty(max(R.repro_wscale_ws_bytes(n_max), 16), dtype=torch.uint8,
                                     device=dev)
+        self.ws_wmulti = torch.empty(
+            max(R.repro_wscale_multi_ws_bytes([w.numel() for w in self.W]), 16),
+            dtype=torch.uint8, device=dev)
         need = max(R.repro_linear_bwd_ws_bytes(M, l.n_out, l.k_in) for l in wl.linears)
         self.ws_bwd = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
         # dW on a second stream, concurrent with the forward and dX of the same
@@ -181,14 +185,14 @@ class HotPathStep:
         sx = lambda i: self.s_x[i:i + 1]  # noqa: E731
         if wait_events is not None and wait_events[0] is not None:
             s.wait_event(wait_events[0])
-        for i in range(L):
-            self._ev(timers, "wscale_w", s)
-            R.repro_wscale(self.W[i], R.REPRO_SCALE_WEIGHT_MEANABS, sw(i), ws=self.ws_scale,
-                           stream=s)
-            self._end(timers, "wscale_w", s)
-            self._ev(timers, "quant_w", s)
-            R.repro_quant_i8(self.W[i], sw(i), self.Wq[i], stream=s)
-            self._end(timers, "quant_w", s)
+        # every weight's scale, then every weight's codes: one pass each
+        self._ev(timers, "wscale_w", s)
+        R.repro_wscale_multi(self.W, R.REPRO_SCALE_WEIGHT_MEANABS, self.s_w, ws=self.ws_wmulti,
+                             stream=s)
+        self._end(timers, "wscale_w", s)
+        self._ev(timers, "quant_w", s)
+        R.repro_quant_i8_multi(self.W, self.s_w, self.Wq, stream=s)
+        self._end(timers, "quant_w", s)
         if done_events is not None:
             e = torch.cuda.Event()
             e.record(s)

@@ -112,6 +112,28 @@ int repro_quant_i8(const float* x, int64_t n, const float* scale, int qmax,
                    int8_t* q_out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Several tensors at once ([use], [limits]: the weight scale is re-pinned
+ * from the weights every optimiser step, and every linear's weights are then
+ * quantised): the same results, bit for bit, as repro_wscale on each xs[t]
+ * (into scales_out[t]) and repro_quant_i8 of each xs[t] with scales[t] (into
+ * q_outs[t]), in one pass over all of them -- one launch for the quantiser,
+ * two for the scales -- so a step's weights do not pay one short launch
+ * chain per tensor.
+ * xs, ns, q_outs: HOST arrays of `count` (1 .. REPRO_MAX_TENSORS) device
+ * pointers and element counts; scales_out / scales: `count` floats (DEVICE).
+ * repro_wscale_multi: every ns[t] >= 1; ws of repro_wscale_multi_ws_bytes
+ * bytes (0 returned for invalid sizes); scales_out must not overlap the xs.
+ * repro_quant_i8_multi: ns[t] == 0 skips tensor t; no q_out may overlap an x,
+ * the scales or another q_out.  Errors as the single-tensor calls.
+ * ------------------------------------------------------------------------ */
+#define REPRO_MAX_TENSORS 64
+int repro_wscale_multi(const float* const* xs, const int64_t* ns, int count, int mode, int qmax,
+                       float* scales_out, void* ws, size_t ws_bytes, void* stream);
+size_t repro_wscale_multi_ws_bytes(const int64_t* ns, int count);
+int repro_quant_i8_multi(const float* const* xs, const int64_t* ns, int count,
+                         const float* scales, int qmax, int8_t* const* q_outs, void* stream);
+
+/* ------------------------------------------------------------------------
  * Forward ([use]; [abstract]).  acc[m,n] = sum_k Xq[m,k]*Wq[n,k] computed
  * exactly as an integer (so its order cannot matter), then
  * Y[m,n] = (float(acc) (x) s_x) (x) s_w -- two unfused multiplies, left to

@@ -55,6 +55,38 @@ def test_wscale_ws_bytes_covers_all_blocks(L):
     assert repro.repro_wscale_ws_bytes(0) == 0
 
 
+def test_multi_tensor_argument_checks(L):
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    B = 1 << 32
+    xs = (P * 3)(B, B * 2, B * 3)
+    ns = (I64 * 3)(100, 64, 4097)
+    need = repro.repro_wscale_multi_ws_bytes([100, 64, 4097])
+    assert need >= 4 * (2 + 1 + 65)
+    assert repro.repro_wscale_multi_ws_bytes([100, 0]) == 0
+    assert repro.repro_wscale_multi_ws_bytes([]) == 0
+    f = L.repro_wscale_multi
+    ws = B * 8
+    assert f(xs, ns, 0, 0, 127, B * 4, ws, need, None) == -1            # no tensors
+    assert f(xs, ns, 65, 0, 127, B * 4, ws, need, None) == -1           # too many
+    assert f(xs, ns, 3, 2, 127, B * 4, ws, need, None) == -1            # mode
+    assert f(xs, ns, 3, 0, 126, B * 4, ws, need, None) == -1            # q_max
+    assert f(xs, (I64 * 3)(100, 0, 5), 3, 0, 127, B * 4, ws, need, None) == -2
+    assert f((P * 3)(B, B * 2 + 4, B * 3), ns, 3, 0, 127, B * 4, ws, need, None) == -3
+    assert f(xs, ns, 3, 0, 127, B * 4, ws, need - 4, None) == -7        # small workspace
+    assert f(xs, ns, 3, 0, 127, B * 2 + 8, ws, need, None) == -8        # scales inside x[1]
+    assert f(xs, ns, 3, 0, 127, B * 4, B * 3, need, None) == -8         # ws overlaps x[2]
+    assert f(xs, ns, 3, 0, 127, B * 4, ws, need, None) not in (-1, -2, -3, -7, -8)
+    g = L.repro_quant_i8_multi
+    qs = (P * 3)(B * 5, B * 6, B * 7)
+    assert g(xs, ns, 3, B * 4, 126, qs, None) == -1
+    assert g(xs, (I64 * 3)(1, -1, 1), 3, B * 4, 127, qs, None) == -2
+    assert g(xs, ns, 3, B * 4, 127, (P * 3)(B * 5, B * 6 + 8, B * 7), None) == -3
+    assert g(xs, ns, 3, B * 4, 127, (P * 3)(B * 5, B * 5 + 64, B * 7), None) == -8   # q0, q1 overlap
+    assert g(xs, ns, 3, B * 4, 127, (P * 3)(B * 5, B * 2, B * 7), None) == -8        # q1 over x1
+    assert g(xs, (I64 * 3)(0, 0, 0), 3, B * 4, 127, qs, None) == 0       # nothing to do
+    assert g(xs, ns, 3, B * 4, 127, qs, None) not in (-1, -2, -3, -8)
+
+
 def test_quant_argument_checks(L):
     f = L.repro_quant_i8
     assert f(A, 10, A + 4096, 126, A * 2, None) == -1

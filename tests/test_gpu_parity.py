@@ -468,3 +468,55 @@ def test_running_sum_equals_streaming_accumulation():
     for p in parts[1:]:
         R.repro_grad_accum(acc, p)
     G.assert_bits_equal(G.host(out), G.host(acc), "one pass vs streaming")
+
+
+# ----------------------------------------------------------- several tensors
+
+MULTI_SIZES = [[1], [5, 64, 65], [8192 * 3 + 17, 1000, 1, 16, 17], [300_001, 700_003, 63, 8192]]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("sizes", MULTI_SIZES, ids=lambda s: "x".join(map(str, s)))
+def test_multi_tensor_scale_and_quant(orc, sizes, mode):
+    # one call over several tensors: the oracle's bits for every tensor's
+    # scale, then every tensor's codes with its own scale
+    rng = np.random.default_rng(sum(sizes) + mode)
+    xh = [_specials(rng, n) if n > 20 else (rng.standard_normal(n) * 0.02).astype(np.float32)
+          for n in sizes]
+    xs = [G.dev(x) for x in xh]
+    scales = torch.full((len(sizes),), float("nan"), device="cuda")
+    R.repro_wscale_multi(xs, mode, scales)
+    got = G.host(scales)
+    exp = np.array([orc.wscale(x, mode) for x in xh], dtype=np.float32)
+    G.assert_bits_equal(got, exp, f"multi scale mode {mode}")
+    qs = [torch.empty(n, dtype=torch.int8, device="cuda") for n in sizes]
+    R.repro_quant_i8_multi(xs, scales, qs)
+    for x, q, s in zip(xh, qs, exp):
+        G.assert_bits_equal(G.host(q), orc.quant_i8(x, s), f"multi quant n {x.size}")
+
+
+@pytest.mark.parametrize("blk", [0, 3, 7])
+@pytest.mark.parametrize("grid", [0, 1, 5, 3000])
+def test_multi_tensor_launch_invariance(orc, blk, grid):
+    # block split (at 2^0 chunks per block the 700,003-element tensor needs
+    # more partials than one tree CTA holds: every tensor then takes the
+    # single-tensor passes) and the quantiser's grid, including fewer CTAs
+    # than tensors
+    sizes = [700_003, 100, 64 * 129, 17]
+    rng = np.random.default_rng(blk * 10 + grid)
+    xh = [(rng.standard_normal(n) * 0.02).astype(np.float32) for n in sizes]
+    xs = [G.dev(x) for x in xh]
+    exp = np.array([orc.wscale(x, 0) for x in xh], dtype=np.float32)
+    R.repro_set_launch_cfg(reduce_block_log2=blk, elementwise_blocks=grid)
+    scales = torch.empty(len(sizes), device="cuda")
+    R.repro_wscale_multi(xs, 0, scales)
+    G.assert_bits_equal(G.host(scales), exp, f"block 2^{blk}")
+    qs = [torch.empty(n, dtype=torch.int8, device="cuda") for n in sizes]
+    R.repro_quant_i8_multi(xs, scales, qs)
+    for x, q, s in zip(xh, qs, exp):
+        G.assert_bits_equal(G.host(q), orc.quant_i8(x, s), f"grid {grid} n {x.size}")
+    # a zero scale gives zero codes, as in the single-tensor quantiser
+    zs = torch.zeros(len(sizes), device="cuda")
+    R.repro_quant_i8_multi(xs, zs, qs)
+    for q in qs:
+        assert not G.host(q).any()
