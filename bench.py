@@ -141,100 +141,175 @@ def whole_job_tokens_per_s(tokens_per_rank_step: int, steps: int, world: int,
 
 # ---------------------------------------------------------------- oracle leg
 
-def oracle_sample_step(wl, host, frac_log2: int) -> tuple:
-    """The oracle, as it stands, over a uniform 2^-k slice of one step's work:
-    scales and int8 codes in full (they are O(n)); the forward and dX for the
-    first M/2^k tokens of every micro-batch; dW for the first N/2^k rows of
-    every weight, reduced over all M tokens; accumulation and TreeFold over
-    that slice of the gradient.  Returns (seconds, tokens credited)."""
-    import oracle as orc
-    L, J, M = len(wl.linears), wl.microbatches, wl.tokens
-    f = 1 << frac_log2
-    m_s = max(1, M // f)
-    n_s = [max(1, -(-l.n_out // f)) for l in wl.linears]
-    dY_cols = [[np.ascontiguousarray(host.dY[i][j][:, :n_s[i]]) for j in range(J)]
+class OracleSample:
+    """The oracle, as it stands, timed on samples of one step's work, part by
+    part, each part's time divided by the fraction of that part's work its
+    sample holds, so that the estimate of a whole step does not depend on the
+    sample size.  Every sample is a run of consecutive output elements (the
+    first 1/2^k of each tensor in row-major order), computed through the
+    oracle's calls for given elements, which parallelise over elements:
+      weights      weight scale + codes of the first 1/2^k of every weight;
+      activations  activation scale + codes of the first 1/2^k of every X;
+      forward      the first 1/2^k of every Y (fraction weighted by K);
+      dx           the first 1/2^k of every dX (weighted by N);
+      dw           the first 1/2^k of every dW (each output reduces all M tokens);
+      accumulate   the micro-batch accumulation of that dW sample;
+      treefold     TreeFold over that sample of the gradient.
+    The sampled outputs need every token's codes: prepare() computes them with
+    the oracle once, untimed."""
+
+    PARTS = ("weights", "activations", "forward", "dx", "dw", "accumulate", "treefold")
+
+    def __init__(self, wl, host):
+        import oracle as orc
+        orc.build()
+        self.orc, self.wl, self.host = orc, wl, host
+        self.prepared = False
+
+    def prepare(self):
+        orc, wl, h = self.orc, self.wl, self.host
+        L, J = len(wl.linears), wl.microbatches
+        self.s_w = [orc.wscale(h.W[i], 0) for i in range(L)]
+        self.wq = [orc.quant_i8(h.W[i], self.s_w[i]) for i in range(L)]
+        self.s_x = [[orc.wscale(h.X[i][j], 1) for j in range(J)] for i in range(L)]
+        self.xq = [[orc.quant_i8(h.X[i][j], self.s_x[i][j]) for j in range(J)] for i in range(L)]
+        self.prepared = True
+
+    def run(self, frac_log2: int, threads: int | None = None) -> dict:
+        """Times one sampled step; returns {"parts": {name: (sec, fraction)},
+        "timed_s": seconds spent, "step_s": extrapolated seconds of a whole step}."""
+        import time as _t
+        orc, wl, h = self.orc, self.wl, self.host
+        if not self.prepared:
+            self.prepare()
+        saved = orc.threads()
+        if threads:
+            orc.set_threads(threads)
+        f = 1 << frac_log2
+        L, J, M = len(wl.linears), wl.microbatches, wl.tokens
+        lins = wl.linears
+        cut = lambda total: max(1, -(-total // f))  # noqa: E731
+        sy = [cut(M * l.n_out) for l in lins]          # sampled outputs of Y
+        sx = [cut(M * l.k_in) for l in lins]           # of dX (and of X's codes)
+        sg = [cut(l.n_out * l.k_in) for l in lins]     # of dW (and of W's codes)
+        flat = lambda cnt, cols: (np.arange(cnt, dtype=np.int64) // cols,  # noqa: E731
+                                  np.arange(cnt, dtype=np.int64) % cols)
+        iy = [flat(sy[i], lins[i].n_out) for i in range(L)]
+        ix = [flat(sx[i], lins[i].k_in) for i in range(L)]
+        ig = [flat(sg[i], lins[i].k_in) for i in range(L)]
+        W_s = [np.ascontiguousarray(h.W[i].reshape(-1)[:sg[i]]) for i in range(L)]
+        X_s = [[np.ascontiguousarray(h.X[i][j].reshape(-1)[:sx[i]]) for j in range(J)]
                for i in range(L)]
-    noise = []
-    if wl.replicas > 1:
-        offs = np.cumsum([0] + [l.n_out * l.k_in for l in wl.linears])
-        idx = np.concatenate([offs[i] + np.arange(n_s[i] * l.k_in)
-                              for i, l in enumerate(wl.linears)])
-        noise = [host.noise[r][idx] for r in range(1, wl.replicas)]
-    t0 = time.perf_counter()
-    s_w = [orc.wscale(host.W[i], 0) for i in range(L)]
-    wq = [orc.quant_i8(host.W[i], s_w[i]) for i in range(L)]
-    G = [None] * L
-    for j in range(J):
-        for i in range(L):
-            X, dY = host.X[i][j], host.dY[i][j]
-            s_x = orc.wscale(X, 1)
-            xq = orc.quant_i8(X, s_x)
-            orc.linear_fwd(xq[:m_s], wq[i], s_x, s_w[i])
-            orc.linear_bwd_dx(dY[:m_s], wq[i], s_w[i])
-            dw = orc.linear_bwd_dw(dY_cols[i][j], xq, s_x)
-            G[i] = dw if G[i] is None else orc.grad_accum(G[i], dw)
-    sec = time.perf_counter() - t0
-    if wl.replicas > 1:
-        g = np.concatenate([x.ravel() for x in G])
-        parts = [g] + [orc.grad_accum(g, nz) for nz in noise]   # replica set-up, untimed
-        t1 = time.perf_counter()
-        orc.treefold(parts)
-        sec += time.perf_counter() - t1
-    # credit tokens in proportion to the MACs done: forward, dX and dW each
-    # cost M * sum(N K) per micro-batch in the full step
-    rho_dw = sum(n * l.k_in for n, l in zip(n_s, wl.linears)) / \
-        sum(l.n_out * l.k_in for l in wl.linears)
-    frac = (2.0 * m_s / M + rho_dw) / 3.0
-    return sec, wl.tokens * J * frac
+        t = dict.fromkeys(self.PARTS, 0.0)
+        try:
+            t0 = _t.perf_counter()
+            for i in range(L):
+                orc.quant_i8(W_s[i], orc.wscale(W_s[i], 0))
+            t["weights"] = _t.perf_counter() - t0
+            G = [None] * L
+            for j in range(J):
+                for i in range(L):
+                    xq, s_x, wq, s_w = self.xq[i][j], self.s_x[i][j], self.wq[i], self.s_w[i]
+                    dY = h.dY[i][j]
+                    t0 = _t.perf_counter()
+                    orc.quant_i8(X_s[i][j], orc.wscale(X_s[i][j], 1))
+                    t1 = _t.perf_counter()
+                    orc.linear_fwd_at(xq, wq, s_x, s_w, *iy[i])
+                    t2 = _t.perf_counter()
+                    orc.linear_bwd_dx_at(dY, wq, s_w, *ix[i])
+                    t3 = _t.perf_counter()
+                    dw = orc.linear_bwd_dw_at(dY, xq, s_x, *ig[i])
+                    t4 = _t.perf_counter()
+                    G[i] = dw if G[i] is None else orc.grad_accum(G[i], dw)
+                    t5 = _t.perf_counter()
+                    t["activations"] += t1 - t0
+                    t["forward"] += t2 - t1
+                    t["dx"] += t3 - t2
+                    t["dw"] += t4 - t3
+                    t["accumulate"] += t5 - t4
+            if wl.replicas > 1:
+                g = np.concatenate(G)
+                offs = np.cumsum([0] + [l.n_out * l.k_in for l in lins])
+                idx = np.concatenate([offs[i] + np.arange(sg[i]) for i in range(L)])
+                parts = [g] + [orc.grad_accum(g, h.noise[r][idx]) for r in range(1, wl.replicas)]
+                t0 = _t.perf_counter()
+                orc.treefold(parts)
+                t["treefold"] = _t.perf_counter() - t0
+        finally:
+            orc.set_threads(saved)
+        nk = sum(l.n_out * l.k_in for l in lins)
+        mk = sum(M * l.k_in for l in lins)
+        frac = {"weights": sum(sg) / nk, "activations": sum(sx) / mk,
+                "forward": sum(sy[i] * lins[i].k_in for i in range(L)) / (M * nk),
+                "dx": sum(sx[i] * lins[i].n_out for i in range(L)) / (M * nk),
+                "dw": sum(sg) / nk, "accumulate": sum(sg) / nk, "treefold": sum(sg) / nk}
+        if J < 2:
+            frac["accumulate"] = 1.0   # nothing to accumulate: zero time, any fraction
+        if wl.replicas <= 1:
+            frac["treefold"] = 1.0
+        parts = {k: (t[k], frac[k]) for k in self.PARTS}
+        return {"parts": parts, "timed_s": sum(t.values()),
+                "step_s": sum(sec / fr for sec, fr in parts.values()),
+                "threads": threads or saved}
 
 
-def _sample_text(wl, frac_log2, toks):
-    return (f"{wl.name}: about 1/{1 << frac_log2} of one step's work -- forward and dX for the "
-            f"first {max(1, wl.tokens >> frac_log2)} tokens of each of {wl.microbatches} "
-            f"micro-batches, dW for the first ceil(N/{1 << frac_log2}) rows of every weight "
-            f"over all tokens, scales and int8 codes in full, TreeFold over that slice; "
-            f"credited {toks:.1f} tokens (in proportion to the MACs done)")
+def _sample_text(wl, frac_log2, r) -> str:
+    parts = ", ".join(f"{k} {sec:.2f} s / {fr:.2e}" for k, (sec, fr) in r["parts"].items())
+    return (f"{wl.name}: the first 1/{1 << frac_log2} of the outputs of every call of one step "
+            f"(Y, dX, dW, codes, the gradient's accumulation and TreeFold), each part of the "
+            f"step timed on its own sample and divided by that sample's fraction of the part's "
+            f"work (multiply-adds or elements); parts [time / fraction]: {parts}; "
+            f"{r['timed_s']:.2f} s timed on {r['threads']} threads, a whole step extrapolated to "
+            f"{r['step_s']:.0f} s")
 
 
-def cpu_baseline(wl, host, frac_log2: int) -> dict:
-    import oracle as orc
-    orc.build()
-    sec, toks = oracle_sample_step(wl, host, frac_log2)
-    return {"value": toks / sec, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
-            "sample": _sample_text(wl, frac_log2, toks) + f"; {sec:.2f} s"}
+def cpu_baseline(wl, host, frac_log2: int, one_core_extra_log2: int = 2) -> dict:
+    """The oracle on every host core (the reported value), and on one core on a
+    2^-extra smaller slice (extrapolated the same way)."""
+    smp = OracleSample(wl, host)
+    smp.prepare()
+    r = smp.run(frac_log2)
+    tokens = wl.tokens * wl.microbatches
+    r1 = smp.run(frac_log2 + one_core_extra_log2, threads=1)
+    return {"value": tokens / r["step_s"], "unit": UNIT, "cores": r["threads"], "kind": "oracle",
+            "sample": _sample_text(wl, frac_log2, r),
+            "one_core": {"value": tokens / r1["step_s"], "unit": UNIT, "cores": 1,
+                         "sample": _sample_text(wl, frac_log2 + one_core_extra_log2, r1),
+                         "extrapolated": True}}
 
 
 def run_reference(args, wl):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    import oracle as orc
     from bitwise_reproducible_int8_gb300 import step as S
-    orc.build()
     host = S.generate_host_inputs(wl)
+    smp = OracleSample(wl, host)
+    smp.prepare()                       # every token's codes, once, untimed
     for _ in range(args.warmup):
-        oracle_sample_step(wl, host, args.ref_frac_log2)
-    runs = [oracle_sample_step(wl, host, args.ref_frac_log2) for _ in range(args.steps)]
-    total = sum(r[0] for r in runs)
-    toks = sum(r[1] for r in runs)
-    value = toks / total
+        smp.run(args.ref_frac_log2)
+    runs = [smp.run(args.ref_frac_log2) for _ in range(args.steps)]
+    step_s = sum(r["step_s"] for r in runs) / len(runs)
+    timed = sum(r["timed_s"] for r in runs)
+    value = wl.tokens * wl.microbatches / step_s
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * timed / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8/f32",
         "data": "synthetic", "impl": "reference",
         "config": {"workload": wl.name, "tokens_per_step": wl.tokens * wl.microbatches,
                    "sample_fraction": 1.0 / (1 << args.ref_frac_log2),
+                   "ms_per_step_is": "the sampled slices' timed ms; value extrapolates each part "
+                                     "of the step by its own fraction",
+                   "extrapolated_s_per_full_step": step_s,
                    "parallelism": "replicas only"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.threads(), "kind": "oracle",
-                         "sample": _sample_text(wl, args.ref_frac_log2, toks / args.steps)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": runs[0]["threads"],
+                         "kind": "oracle", "sample": _sample_text(wl, args.ref_frac_log2, runs[-1])},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
-
-# ---------------------------------------------------------------- our leg
 
 def run_ours(args, wl):
     import torch

@@ -105,6 +105,7 @@ def load(path: str) -> ctypes.CDLL:
         "oracle_treefold": (None, [ctypes.POINTER(_f32p), ctypes.c_int, _i64, _f32p]),
         "oracle_treefold_all_ranks": (None, [_f32p, ctypes.c_int, _f32p]),
         "oracle_threads": (ctypes.c_int, []),
+        "oracle_set_threads": (None, [ctypes.c_int]),
         "oracle_sumsq": (ctypes.c_float, [_f32p, _i64]),
         "oracle_pow_t": (ctypes.c_float, [ctypes.c_float, _i64]),
         "oracle_clip_coef": (ctypes.c_float, [ctypes.c_float, ctypes.c_float]),
@@ -344,6 +345,11 @@ def adamw_step(p, m, v, g, s: float, t: int, lr=4.5e-4, beta1=0.9, beta2=0.95, e
 
 def threads() -> int:
     return int(lib().oracle_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads of the parallel loops over output elements (bits unchanged)."""
+    lib().oracle_set_threads(int(n))
 
 
 # ---------------------------------------------------------------- attention

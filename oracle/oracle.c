@@ -772,3 +772,15 @@ int oracle_threads(void)
     return 1;
 #endif
 }
+
+/* threads for the parallel loops over output elements from now on (n >= 1);
+ * no element's sequence of operations depends on it */
+void oracle_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -154,6 +154,7 @@ void oracle_attn_bwd_rows(const float* q, const float* k, const int8_t* vq, floa
                           int64_t T, int64_t Hq, int64_t Hkv, int64_t D, int64_t W);
 
 int oracle_threads(void);
+void oracle_set_threads(int n);
 
 #ifdef __cplusplus
 }

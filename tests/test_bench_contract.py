@@ -28,3 +28,24 @@ def test_reference_line_keeps_the_contract():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_oracle_sample_fractions():
+    # the CPU baseline times each part of a step on a sample and divides by
+    # the sample's share of that part's work: at 2^-0 the sample is the whole
+    # step (every fraction 1, nothing extrapolated); at 2^-3 every part's
+    # share is about 1/8 (rounded up to whole outputs)
+    sys.path.insert(0, ROOT)
+    import bench
+    from bitwise_reproducible_int8_gb300 import inputs
+    from bitwise_reproducible_int8_gb300 import step as S
+    wl = inputs.WORKLOADS["tiny"]
+    smp = bench.OracleSample(wl, S.generate_host_inputs(wl))
+    r0 = smp.run(0)
+    assert all(fr == 1.0 for _, fr in r0["parts"].values())
+    assert abs(r0["step_s"] - r0["timed_s"]) < 1e-9
+    r3 = smp.run(3, threads=1)
+    assert r3["threads"] == 1
+    for name, (_, fr) in r3["parts"].items():
+        if name != "accumulate":       # one micro-batch: nothing to accumulate
+            assert 0.125 <= fr < 0.13, (name, fr)
