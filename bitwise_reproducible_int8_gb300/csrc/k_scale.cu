@@ -23,11 +23,6 @@ namespace {
 constexpr int P1_CHUNKS = 128;   // chunks (and threads) per phase-1 CTA
 constexpr int P2_MAX = 1024;     // partials (and threads) per tree-pass CTA
 
-// Phase 1: CTA b sums chunks [b*2^k, (b+1)*2^k) (k <= 7) and reduces their
-// partials with the stride-doubling tree.  The CTA's slice of x is staged in
-// shared memory with coalesced 16-byte loads; chunk j's 16 float4 are stored
-// XOR-swizzled (slot p ^ (j & 15)) so both the fill and the per-thread reads
-// are free of bank conflicts.
 // term of the canonical sum: |x| (weight scale) or x (x) x (squared norm); a
 // subnormal x gives a term the first add reads as zero either way
 template <int SQUARE>
@@ -36,50 +31,58 @@ __device__ __forceinline__ float term(float x)
     return SQUARE ? fmul_rn(x, x) : fabsf(x);
 }
 
-// the canonical sum of block `blk` (chunks [blk*2^k, (blk+1)*2^k)) of x into *out
-template <int SQUARE>
-__device__ __forceinline__ void absum_block(const float* __restrict__ x, int64_t n, int blk_log2,
-                                            int64_t blk, float* __restrict__ out)
+// The tensors of one call (one, or all of a step's weights): their phase-1
+// blocks form one range, the blocks of tensor t being [blk0[t], blk0[t+1]).
+struct MultiArgs {
+    const float* x[REPRO_MAX_TENSORS_INTERNAL];
+    int64_t n[REPRO_MAX_TENSORS_INTERNAL];
+    int64_t blk0[REPRO_MAX_TENSORS_INTERNAL + 1];
+    int count;
+};
+
+// tensor owning phase-1 block b (blk0 ascending, blk0[0] = 0)
+__device__ __forceinline__ int tensor_of(const MultiArgs& a, int64_t b)
 {
-    __shared__ float4 S[P1_CHUNKS * 16];
-    __shared__ float T[P1_CHUNKS];
-    const int nb = 1 << blk_log2;
-    const int64_t C = (n + 63) >> 6;
-    const int64_t c0 = blk * nb;
-    const int cnt = (int)min((int64_t)nb, C - c0);
-    const int64_t e0 = c0 * 64;
-
-    if (cnt == P1_CHUNKS && blockDim.x == P1_CHUNKS && e0 + P1_CHUNKS * 64 <= n) {
-        // a full block: all 16 of the thread's loads in flight before any store
-        float4 v[16];
-        const float4* x4 = reinterpret_cast<const float4*>(x + e0);
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-            v[u] = ld_stream(x4 + threadIdx.x + u * P1_CHUNKS);
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int g = threadIdx.x + u * P1_CHUNKS;
-            const int ch = g >> 4, p = g & 15;
-            S[ch * 16 + (p ^ (ch & 15))] = v[u];
-        }
-    } else {
-        for (int g = threadIdx.x; g < cnt * 16; g += blockDim.x) {
-            const int ch = g >> 4, p = g & 15;
-            const int64_t e = e0 + (int64_t)g * 4;
-            float4 v;
-            if (e + 4 <= n) {
-                v = __ldg(reinterpret_cast<const float4*>(x + e));
-            } else {
-                v.x = (e + 0 < n) ? x[e + 0] : 0.f;
-                v.y = (e + 1 < n) ? x[e + 1] : 0.f;
-                v.z = (e + 2 < n) ? x[e + 2] : 0.f;
-                v.w = (e + 3 < n) ? x[e + 3] : 0.f;
-            }
-            S[ch * 16 + (p ^ (ch & 15))] = v;
-        }
+    int lo = 0, hi = a.count - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.blk0[mid] <= b)
+            lo = mid;
+        else
+            hi = mid - 1;
     }
-    __syncthreads();
+    return lo;
+}
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16-byte asynchronous copy global -> shared; bytes past src_bytes read as 0
+__device__ __forceinline__ void cp_async16(uint32_t sdst, const void* gsrc, int src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(sdst), "l"(gsrc),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// The canonical sum of one block of 2^k (k <= 7) chunks staged in shared
+// memory: chunk j's 16 float4 sit XOR-swizzled at S[j*16 + (p ^ (j & 15))],
+// so the fill and the per-thread reads are free of bank conflicts.  One
+// thread sums one chunk left to right (elements past n are never read), then
+// the stride-doubling tree over the cnt chunk partials in T.  Every thread of
+// the CTA must call it; the result is valid in every thread.
+template <int SQUARE>
+__device__ __forceinline__ float block_sum(const float4* __restrict__ S, float* __restrict__ T,
+                                           int64_t n, int64_t e0, int cnt)
+{
     for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
         const int64_t lo = e0 + (int64_t)j * 64;
         const int len = (int)min((int64_t)64, n - lo);
@@ -110,24 +113,70 @@ __device__ __forceinline__ void absum_block(const float* __restrict__ x, int64_t
         T[j] = a;
     }
     __syncthreads();
-
     for (int s = 1; s < cnt; s <<= 1) {
         const int j = threadIdx.x * 2 * s;
         if (j + s < cnt)
             T[j] = fadd_ftz(T[j], T[j + s]);
         __syncthreads();
     }
-    if (threadIdx.x == 0)
-        *out = T[0];
+    return T[0];
 }
 
+constexpr int P1_STAGES = 3;                                       // blocks in flight per CTA
+constexpr size_t P1_SMEM = (size_t)P1_STAGES * P1_CHUNKS * 16 * sizeof(float4);   // 96 KB
+
+// Phase 1, persistent: CTA c takes blocks c, c + G, c + 2G, ... (G CTAs, two
+// per SM) of all the call's tensors.  Each block's 32 KB is copied into a
+// three-stage shared-memory ring with 16-byte asynchronous copies (zero fill
+// past the tensor's end), two blocks ahead of the one being summed, so the
+// SM's share of HBM bandwidth stays busy while the chunk sums and the tree of
+// the current block run.  Writes one partial per block.
 template <int SQUARE>
 __global__ void __launch_bounds__(P1_CHUNKS)
-k_absum_chunks(const float* __restrict__ x, int64_t n, int blk_log2, float* __restrict__ part)
+k_absum_pipe(const __grid_constant__ MultiArgs a, int blk_log2, float* __restrict__ part)
 {
+    extern __shared__ __align__(16) float4 ring[];
+    __shared__ float T[P1_CHUNKS];
     pdl_wait();
     pdl_trigger();
-    absum_block<SQUARE>(x, n, blk_log2, blockIdx.x, part + blockIdx.x);
+    const int64_t total = a.blk0[a.count];
+    const int nb = 1 << blk_log2;
+    const int64_t step = gridDim.x;
+    auto issue = [&](int64_t b, int stage) {
+        if (b < total) {
+            const int t = tensor_of(a, b);
+            const float* x = a.x[t];
+            const int64_t n = a.n[t];
+            const int64_t e0 = (b - a.blk0[t]) * (int64_t)nb * 64;
+            float4* S = ring + stage * (P1_CHUNKS * 16);
+            for (int g = threadIdx.x; g < nb * 16; g += P1_CHUNKS) {
+                const int ch = g >> 4, p = g & 15;
+                const int64_t e = e0 + (int64_t)g * 4;
+                const int bytes = e >= n ? 0 : (int)min((int64_t)16, (n - e) * 4);
+                cp_async16(smem_u32(&S[ch * 16 + (p ^ (ch & 15))]),
+                           bytes ? static_cast<const void*>(x + e) : static_cast<const void*>(x),
+                           bytes);
+            }
+        }
+        cp_async_commit();   // one group per block, empty past the end
+    };
+    int64_t b = blockIdx.x;
+    issue(b, 0);
+    issue(b + step, 1);
+    for (int i = 0; b < total; b += step, ++i) {
+        cp_async_wait<1>();   // this thread's copies of block b have landed
+        __syncthreads();      // everyone's have; everyone is done with block b - step
+        issue(b + 2 * step, (i + 2) % P1_STAGES);
+        const int t = tensor_of(a, b);
+        const int64_t n = a.n[t];
+        const int64_t c0 = (b - a.blk0[t]) * nb;
+        const int cnt = (int)min((int64_t)nb, ((n + 63) >> 6) - c0);
+        const float v =
+            block_sum<SQUARE>(ring + (i % P1_STAGES) * (P1_CHUNKS * 16), T, n, c0 * 64, cnt);
+        if (threadIdx.x == 0)
+            part[b] = v;
+    }
+    cp_async_wait<0>();
 }
 
 // s_w = (2 (x) (S (/) float(n))) (/) sqrt(float(q_max)); every operand and
@@ -245,38 +294,6 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------- several tensors
 
-// The tensors of one call: phase-1 blocks of all of them form one grid, the
-// blocks of tensor t being [blk0[t], blk0[t+1]).
-struct MultiArgs {
-    const float* x[REPRO_MAX_TENSORS_INTERNAL];
-    int64_t n[REPRO_MAX_TENSORS_INTERNAL];
-    int64_t blk0[REPRO_MAX_TENSORS_INTERNAL + 1];
-    int count;
-};
-
-// tensor owning phase-1 block b (blk0 ascending, blk0[0] = 0)
-__device__ __forceinline__ int tensor_of(const MultiArgs& a, int64_t b)
-{
-    int lo = 0, hi = a.count - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.blk0[mid] <= b)
-            lo = mid;
-        else
-            hi = mid - 1;
-    }
-    return lo;
-}
-
-__global__ void __launch_bounds__(P1_CHUNKS)
-k_absum_chunks_multi(const __grid_constant__ MultiArgs a, int blk_log2, float* __restrict__ part)
-{
-    pdl_wait();
-    pdl_trigger();
-    const int t = tensor_of(a, blockIdx.x);
-    absum_block<0>(a.x[t], a.n[t], blk_log2, blockIdx.x - a.blk0[t], part + blockIdx.x);
-}
-
 constexpr int TREE_MULTI_MAX = 8192;   // block partials one tree CTA holds
 
 // one CTA per tensor: the stride-doubling tree over the tensor's block
@@ -392,6 +409,24 @@ size_t wscale_ws_bytes(int64_t n, int block_log2)
     return (size_t)(c1 + c2 + 64) * sizeof(float);
 }
 
+// phase 1 over the blocks of a.count tensors (a.blk0 filled): one block
+// partial per block into part
+static cudaError_t launch_phase1(const MultiArgs& a, int square, int p1, float* part,
+                                 cudaStream_t st)
+{
+    auto kern = square ? k_absum_pipe<1> : k_absum_pipe<0>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)P1_SMEM);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t blocks = a.blk0[a.count];
+    const int64_t cap = 2 * (int64_t)num_sms();   // two 97 KB CTAs per SM
+    const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
+    e = launch_pdl(kern, dim3(grid), dim3(P1_CHUNKS), P1_SMEM, st, a, p1, part);
+    count_launches(1);
+    return e;
+}
+
 // canonical sum of |x_i| (square = 0) or x_i (x) x_i (square = 1); with
 // square = 0 the last pass turns the sum into the weight scale, with
 // square = 1 it stores the sum
@@ -405,9 +440,13 @@ static cudaError_t canonical_sum(const float* x, int64_t n, int square, int qmax
     float* regA = static_cast<float*>(ws);
     float* regB = regA + cnt + 32;
     float* scale_out = out;
-    cudaError_t e = launch_pdl(square ? k_absum_chunks<1> : k_absum_chunks<0>, dim3((unsigned)cnt),
-                               dim3(P1_CHUNKS), 0, st, x, n, p1, regA);
-    count_launches(1);
+    MultiArgs a;
+    a.count = 1;
+    a.x[0] = x;
+    a.n[0] = n;
+    a.blk0[0] = 0;
+    a.blk0[1] = cnt;
+    cudaError_t e = launch_phase1(a, square, p1, regA, st);
     if (e != cudaSuccess)
         return e;
     float* src = regA;
@@ -502,17 +541,18 @@ cudaError_t launch_wscale_multi(const float* const* xs, const int64_t* ns, int c
     const unsigned grid = (unsigned)a.blk0[count];
     cudaError_t e;
     if (mode == 0) {
-        e = launch_pdl(k_absum_chunks_multi, dim3(grid), dim3(P1_CHUNKS), 0, st, a, p1, part);
+        e = launch_phase1(a, 0, p1, part, st);
         if (e == cudaSuccess)
             e = launch_pdl(k_tree_multi, dim3((unsigned)count), dim3(1024), 0, st, a,
                            (const float*)part, qmax, scales);
+        count_launches(1);
     } else {
         e = launch_pdl(k_amax_multi, dim3(grid), dim3(256), 0, st, a, part);
         if (e == cudaSuccess)
             e = launch_pdl(k_amax_final_multi, dim3((unsigned)count), dim3(1024), 0, st, a,
                            (const float*)part, qmax, scales);
+        count_launches(2);
     }
-    count_launches(2);
     return e;
 }
 
