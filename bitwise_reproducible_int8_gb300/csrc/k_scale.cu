@@ -13,6 +13,8 @@
 // Activation scale: max|x| / q_max; the maximum is exact, so any order works.
 #include <float.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 #include "launch.cuh"
@@ -73,53 +75,75 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// The canonical sum of one block of 2^k (k <= 7) chunks staged in shared
-// memory: chunk j's 16 float4 sit XOR-swizzled at S[j*16 + (p ^ (j & 15))],
-// so the fill and the per-thread reads are free of bank conflicts.  One
-// thread sums one chunk left to right (elements past n are never read), then
-// the stride-doubling tree over the cnt chunk partials in T.  Every thread of
-// the CTA must call it; the result is valid in every thread.
-template <int SQUARE>
-__device__ __forceinline__ float block_sum(const float4* __restrict__ S, float* __restrict__ T,
-                                           int64_t n, int64_t e0, int cnt)
+// Thread j's chunk of a block staged in shared memory (chunk j's 16 float4
+// sit XOR-swizzled at S[j*16 + (p ^ (j & 15))], so the fill and these reads
+// are free of bank conflicts), copied to registers.
+__device__ __forceinline__ void chunk_to_regs(const float4* __restrict__ S, int j, float4 (&v)[16])
 {
-    for (int j = threadIdx.x; j < cnt; j += blockDim.x) {
-        const int64_t lo = e0 + (int64_t)j * 64;
-        const int len = (int)min((int64_t)64, n - lo);
-        float a;
-        if (len == 64) {
-            float4 v = S[j * 16 + (0 ^ (j & 15))];
-            a = term<SQUARE>(v.x);
-            a = fadd_ftz(a, term<SQUARE>(v.y));
-            a = fadd_ftz(a, term<SQUARE>(v.z));
-            a = fadd_ftz(a, term<SQUARE>(v.w));
 #pragma unroll
-            for (int p = 1; p < 16; ++p) {
-                v = S[j * 16 + (p ^ (j & 15))];
-                a = fadd_ftz(a, term<SQUARE>(v.x));
-                a = fadd_ftz(a, term<SQUARE>(v.y));
-                a = fadd_ftz(a, term<SQUARE>(v.z));
-                a = fadd_ftz(a, term<SQUARE>(v.w));
-            }
-        } else {
-            a = 0.f;
-            for (int i = 0; i < len; ++i) {
-                const float4 v = S[j * 16 + ((i >> 2) ^ (j & 15))];
-                const int u = i & 3;
-                const float t = term<SQUARE>(u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w);
-                a = (i == 0) ? t : fadd_ftz(a, t);
-            }
+    for (int p = 0; p < 16; ++p)
+        v[p] = S[j * 16 + (p ^ (j & 15))];
+}
+
+// Left-to-right sum of the chunk's first len (1..64) terms, seeded with the
+// first term.
+template <int SQUARE>
+__device__ __forceinline__ float chunk_sum(const float4 (&v)[16], int len)
+{
+    float a = term<SQUARE>(v[0].x);
+    if (len == 64) {
+        a = fadd_ftz(a, term<SQUARE>(v[0].y));
+        a = fadd_ftz(a, term<SQUARE>(v[0].z));
+        a = fadd_ftz(a, term<SQUARE>(v[0].w));
+#pragma unroll
+        for (int p = 1; p < 16; ++p) {
+            a = fadd_ftz(a, term<SQUARE>(v[p].x));
+            a = fadd_ftz(a, term<SQUARE>(v[p].y));
+            a = fadd_ftz(a, term<SQUARE>(v[p].z));
+            a = fadd_ftz(a, term<SQUARE>(v[p].w));
         }
-        T[j] = a;
+    } else {
+#pragma unroll
+        for (int i = 1; i < 64; ++i) {
+            const float4 q = v[i >> 2];
+            const float x = (i & 3) == 0 ? q.x : (i & 3) == 1 ? q.y : (i & 3) == 2 ? q.z : q.w;
+            if (i < len)
+                a = fadd_ftz(a, term<SQUARE>(x));
+        }
     }
+    return a;
+}
+
+// The stride-doubling tree over the cnt (<= 128) chunk partials of a block,
+// partial j held by thread j of the 128-thread CTA: levels 1..16 inside each
+// warp with shuffles (lane j, j a multiple of 2s, adds lane j+s's partial
+// when j+s < cnt -- the tree's own pairs), levels 32 and 64 by thread 0 over
+// the four warps' partials in W.  Every thread must call it; the result is
+// valid in thread 0.
+__device__ __forceinline__ float block_tree(float a, float* __restrict__ W, int cnt)
+{
+    const int j = threadIdx.x, lane = j & 31;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, a, s);
+        if ((lane & (2 * s - 1)) == 0 && j + s < cnt)
+            a = fadd_ftz(a, o);
+    }
+    if (lane == 0)
+        W[j >> 5] = a;
     __syncthreads();
-    for (int s = 1; s < cnt; s <<= 1) {
-        const int j = threadIdx.x * 2 * s;
-        if (j + s < cnt)
-            T[j] = fadd_ftz(T[j], T[j + s]);
-        __syncthreads();
+    float r = 0.f;
+    if (j == 0) {
+        r = W[0];
+        float r2 = W[2];
+        if (32 < cnt)
+            r = fadd_ftz(r, W[1]);
+        if (96 < cnt)
+            r2 = fadd_ftz(r2, W[3]);
+        if (64 < cnt)
+            r = fadd_ftz(r, r2);
     }
-    return T[0];
+    return r;
 }
 
 constexpr int P1_STAGES = 3;                                       // blocks in flight per CTA
@@ -128,15 +152,16 @@ constexpr size_t P1_SMEM = (size_t)P1_STAGES * P1_CHUNKS * 16 * sizeof(float4); 
 // Phase 1, persistent: CTA c takes blocks c, c + G, c + 2G, ... (G CTAs, two
 // per SM) of all the call's tensors.  Each block's 32 KB is copied into a
 // three-stage shared-memory ring with 16-byte asynchronous copies (zero fill
-// past the tensor's end), two blocks ahead of the one being summed, so the
-// SM's share of HBM bandwidth stays busy while the chunk sums and the tree of
-// the current block run.  Writes one partial per block.
+// past the tensor's end).  When a block has landed, every thread moves its
+// own chunk into registers and the stage is refilled at once, so three
+// blocks (192 KB per SM) stay in flight while the chunk sums and the tree of
+// the current block run from registers.  Writes one partial per block.
 template <int SQUARE>
 __global__ void __launch_bounds__(P1_CHUNKS)
 k_absum_pipe(const __grid_constant__ MultiArgs a, int blk_log2, float* __restrict__ part)
 {
     extern __shared__ __align__(16) float4 ring[];
-    __shared__ float T[P1_CHUNKS];
+    __shared__ float W[P1_CHUNKS / 32];
     pdl_wait();
     pdl_trigger();
     const int64_t total = a.blk0[a.count];
@@ -149,6 +174,19 @@ k_absum_pipe(const __grid_constant__ MultiArgs a, int blk_log2, float* __restric
             const int64_t n = a.n[t];
             const int64_t e0 = (b - a.blk0[t]) * (int64_t)nb * 64;
             float4* S = ring + stage * (P1_CHUNKS * 16);
+            if (nb == P1_CHUNKS && e0 + P1_CHUNKS * 64 <= n) {
+                // a full block: float4 g = tid + 128u is chunk (tid >> 4) + 8u,
+                // part tid & 15, so only the swizzle's parity in u varies
+                const int ch0 = threadIdx.x >> 4, p = threadIdx.x & 15;
+                const float* src = x + e0 + 4 * threadIdx.x;
+                const uint32_t d0 = smem_u32(S + ch0 * 16 + (p ^ ch0));
+                const uint32_t d1 = smem_u32(S + ch0 * 16 + (p ^ (ch0 + 8)));
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    cp_async16((u & 1 ? d1 : d0) + (uint32_t)(u * 128 * 16), src + 512 * u, 16);
+                cp_async_commit();
+                return;
+            }
             for (int g = threadIdx.x; g < nb * 16; g += P1_CHUNKS) {
                 const int ch = g >> 4, p = g & 15;
                 const int64_t e = e0 + (int64_t)g * 4;
@@ -161,20 +199,28 @@ k_absum_pipe(const __grid_constant__ MultiArgs a, int blk_log2, float* __restric
         cp_async_commit();   // one group per block, empty past the end
     };
     int64_t b = blockIdx.x;
-    issue(b, 0);
-    issue(b + step, 1);
+#pragma unroll
+    for (int s0 = 0; s0 < P1_STAGES; ++s0)
+        issue(b + s0 * step, s0);
     for (int i = 0; b < total; b += step, ++i) {
-        cp_async_wait<1>();   // this thread's copies of block b have landed
-        __syncthreads();      // everyone's have; everyone is done with block b - step
-        issue(b + 2 * step, (i + 2) % P1_STAGES);
+        cp_async_wait<P1_STAGES - 1>();   // this thread's copies of block b have landed
+        __syncthreads();                  // everyone's have
+        const int stage = i % P1_STAGES;
+        const int j = threadIdx.x;
+        float4 v[16];
+        chunk_to_regs(ring + stage * (P1_CHUNKS * 16), j, v);
+        __syncthreads();                  // everyone has read the stage: refill it
+        issue(b + P1_STAGES * step, stage);
         const int t = tensor_of(a, b);
         const int64_t n = a.n[t];
         const int64_t c0 = (b - a.blk0[t]) * nb;
         const int cnt = (int)min((int64_t)nb, ((n + 63) >> 6) - c0);
-        const float v =
-            block_sum<SQUARE>(ring + (i % P1_STAGES) * (P1_CHUNKS * 16), T, n, c0 * 64, cnt);
-        if (threadIdx.x == 0)
-            part[b] = v;
+        float sum = 0.f;
+        if (j < cnt)
+            sum = chunk_sum<SQUARE>(v, (int)min((int64_t)64, n - (c0 + j) * 64));
+        const float r = block_tree(sum, W, cnt);
+        if (j == 0)
+            part[b] = r;
     }
     cp_async_wait<0>();
 }
@@ -294,30 +340,56 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------- several tensors
 
-constexpr int TREE_MULTI_MAX = 8192;   // block partials one tree CTA holds
+constexpr int TREE_MULTI_MAX = 8192;   // block partials one tree CTA holds (1024 x 8)
 
-// one CTA per tensor: the stride-doubling tree over the tensor's block
-// partials (at most TREE_MULTI_MAX), then its weight scale
+// one CTA of 1024 threads per tensor: the stride-doubling tree over the
+// tensor's block partials, then its weight scale.  Thread t holds partials
+// 8t .. 8t+7 and takes levels 1, 2, 4 in registers; levels 8 .. 128 run across
+// the lanes of a warp with shuffles, levels 256 .. 4096 across the warps'
+// partials in warp 0 -- at every level partial j (j a multiple of 2s) adds
+// partial j + s when j + s < cnt, as the tree defines.
 __global__ void __launch_bounds__(1024)
 k_tree_multi(const __grid_constant__ MultiArgs a, const float* __restrict__ part, int qmax,
              float* __restrict__ scales)
 {
-    __shared__ float T[TREE_MULTI_MAX];
+    __shared__ float W[32];
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x;
     const int64_t b0 = a.blk0[t];
     const int cnt = (int)(a.blk0[t + 1] - b0);
-    for (int j = threadIdx.x; j < cnt; j += blockDim.x)
-        T[j] = part[b0 + j];
-    __syncthreads();
-    for (int s = 1; s < cnt; s <<= 1) {
-        for (int j = threadIdx.x * 2 * s; j + s < cnt; j += blockDim.x * 2 * s)
-            T[j] = fadd_ftz(T[j], T[j + s]);
-        __syncthreads();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float v[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        v[r] = 8 * tid + r < cnt ? part[b0 + 8 * tid + r] : 0.f;
+#pragma unroll
+    for (int s = 1; s < 8; s <<= 1)
+#pragma unroll
+        for (int r = 0; r < 8; r += 2 * s)
+            if (8 * tid + r + s < cnt)
+                v[r] = fadd_ftz(v[r], v[r + s]);
+    float x = v[0];
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {   // element stride 8s
+        const float o = __shfl_down_sync(0xffffffffu, x, s);
+        if ((lane & (2 * s - 1)) == 0 && 8 * (tid + s) < cnt)
+            x = fadd_ftz(x, o);
     }
-    if (threadIdx.x == 0)
-        scales[t] = weight_scale_from_sum(T[0], a.n[t], qmax);
+    if (lane == 0)
+        W[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        x = W[lane];
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {   // element stride 256s
+            const float o = __shfl_down_sync(0xffffffffu, x, s);
+            if ((lane & (2 * s - 1)) == 0 && 256 * (lane + s) < cnt)
+                x = fadd_ftz(x, o);
+        }
+        if (lane == 0)
+            scales[t] = weight_scale_from_sum(x, a.n[t], qmax);
+    }
 }
 
 constexpr int AMAX_BLOCK = 8192;   // elements per phase-1 CTA of the multi amax
@@ -415,14 +487,34 @@ static cudaError_t launch_phase1(const MultiArgs& a, int square, int p1, float* 
                                  cudaStream_t st)
 {
     auto kern = square ? k_absum_pipe<1> : k_absum_pipe<0>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)P1_SMEM);
+    // the 96 KB ring needs the opt-in shared-memory size, set once per device
+    // and kernel (a host call that takes microseconds, kept off every launch)
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> opted[2][kMaxDev];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    if (dev >= kMaxDev || opted[square][dev].load(std::memory_order_acquire) == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P1_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        if (dev < kMaxDev)
+            opted[square][dev].store(1, std::memory_order_release);
+    }
     const int64_t blocks = a.blk0[a.count];
-    const int64_t cap = 2 * (int64_t)num_sms();   // two 97 KB CTAs per SM
+    // two 97 KB CTAs per SM, unless the launch-configuration hook sets the grid
+    const int64_t cap = launch_cfg().elementwise_blocks > 0 ? launch_cfg().elementwise_blocks
+                                                            : 2 * (int64_t)num_sms();
     const unsigned grid = (unsigned)(blocks < cap ? blocks : cap);
     e = launch_pdl(kern, dim3(grid), dim3(P1_CHUNKS), P1_SMEM, st, a, p1, part);
+    if (e == cudaErrorInvalidValue) {
+        // the opt-in was lost (the device was reset since): set it again
+        (void)cudaGetLastError();
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P1_SMEM);
+        if (e == cudaSuccess)
+            e = launch_pdl(kern, dim3(grid), dim3(P1_CHUNKS), P1_SMEM, st, a, p1, part);
+    }
     count_launches(1);
     return e;
 }

@@ -367,9 +367,10 @@ typedef struct {
     int fwd_path;           /* -1: default (tensor cores, 128 x 256 output tiles, when K % 8 == 0);
                                0: CUDA cores; 1: tensor cores, 128 x 256 tiles; 2: tensor cores,
                                128 x 128 tiles */
-    int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels and of
-                               the activation-scale pass (that one capped at the
-                               ceil(n / 64) + 64 partial slots of its workspace) */
+    int elementwise_blocks; /* -1 or 0: default; else grid size of streaming kernels, of
+                               the weight scale's first pass and of the activation-scale
+                               pass (that one capped at the ceil(n / 64) + 64 partial
+                               slots of its workspace) */
     int bwd_kernel;         /* -1: default (8); 8: operands prepared once per call, then fed
                                to the products by tensor copies (needs 16-byte-aligned rows:
                                N % 4 == 0 and K % 16 == 0, else 1 runs); 1: register-prefetch

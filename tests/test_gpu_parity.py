@@ -520,3 +520,17 @@ def test_multi_tensor_launch_invariance(orc, blk, grid):
     R.repro_quant_i8_multi(xs, zs, qs)
     for q in qs:
         assert not G.host(q).any()
+
+
+@pytest.mark.parametrize("extra", [0, 1])
+def test_multi_tensor_scale_at_the_one_pass_limit(orc, extra):
+    # 8192 blocks of 8192 elements is the most one tree CTA takes; one element
+    # more sends the call through the single-tensor passes: same bits either way
+    n = 8192 * 8192 + extra
+    rng = np.random.default_rng(81 + extra)
+    xh = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    small = (rng.standard_normal(1000) * 0.02).astype(np.float32)
+    scales = torch.empty(2, device="cuda")
+    R.repro_wscale_multi([G.dev(xh), G.dev(small)], 0, scales)
+    exp = np.array([orc.wscale(xh, 0), orc.wscale(small, 0)], dtype=np.float32)
+    G.assert_bits_equal(G.host(scales), exp, f"n {n}")
