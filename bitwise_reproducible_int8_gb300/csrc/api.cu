@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "repro.h"
 
@@ -12,13 +14,19 @@ namespace repro {
 namespace {
 
 constexpr int kDefaultBwdKernel = 8;   // operand prep + tensor-copy-fed kernel
-LaunchCfg g_cfg = {-1, -1, -1, 0, kDefaultBwdKernel};
+LaunchCfg g_cfg = {-1, -1, -1, 0, kDefaultBwdKernel, -1};
 
 constexpr int kMaxDevices = 64;
 int g_arch_ok[kMaxDevices];   // 0 unknown, 1 GB300, -1 other
 int g_sms[kMaxDevices];
 
 __device__ int g_device_error;   // set by bounded device-side waits
+
+// exactness of the tensor-core forward on each device: 0 not checked yet,
+// 1 the self-test passed, -1 it failed (every forward then takes the exact
+// CUDA-core path); and a failure that repro_device_check has not reported yet
+std::atomic<int> g_tc_state[kMaxDevices];
+std::atomic<int> g_tc_notice[kMaxDevices];
 
 unsigned long long g_launches;    // kernels enqueued by this library
 
@@ -119,6 +127,38 @@ bool use_tc(int64_t M, int64_t N, int64_t K)
     return g_cfg.fwd_path != 0 && fwd_tc_supported(M, N, K);
 }
 
+// Whether a default-path forward may use the tensor cores on the current
+// device: 1 yes, 0 take the CUDA-core path, negative a CUDA error.  The first
+// call on a device runs the exactness self-test in `ws` (at least
+// selftest_ws_bytes()) and synchronises `stream`; a call made while `stream`
+// is being captured cannot, so before the check has run it takes the exact
+// CUDA-core path.
+int tc_gate(void* ws, cudaStream_t stream)
+{
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices)
+        return -1;
+    if (g_cfg.fwd_selftest == 1) {   // test hook: act as if the check had failed
+        g_tc_notice[dev].store(1);
+        return 0;
+    }
+    const int state = g_tc_state[dev].load();
+    if (state != 0)
+        return state > 0 ? 1 : 0;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess)
+        return -1;
+    if (cs != cudaStreamCaptureStatusNone)
+        return 0;
+    const int r = run_selftest(ws, stream);
+    if (r < 0)
+        return -1;
+    g_tc_state[dev].store(r == 0 ? 1 : -1);
+    if (r != 0)
+        g_tc_notice[dev].store(1);
+    return r == 0 ? 1 : 0;
+}
+
 } // namespace
 
 namespace repro {
@@ -151,7 +191,7 @@ uint64_t repro_launch_count(void) { return (uint64_t)__atomic_load_n(&g_launches
 int repro_set_launch_cfg(const repro_launch_cfg* cfg)
 {
     if (!cfg) {
-        g_cfg = LaunchCfg{-1, -1, -1, 0, kDefaultBwdKernel};
+        g_cfg = LaunchCfg{-1, -1, -1, 0, kDefaultBwdKernel, -1};
         return REPRO_OK;
     }
     if (cfg->bwd_segment_log2 < -1 || cfg->bwd_segment_log2 > 8)
@@ -164,11 +204,14 @@ int repro_set_launch_cfg(const repro_launch_cfg* cfg)
         return REPRO_ERR_ARG;
     if (cfg->bwd_kernel != -1 && cfg->bwd_kernel != 1 && cfg->bwd_kernel != 8)
         return REPRO_ERR_ARG;
+    if (cfg->fwd_selftest != -1 && cfg->fwd_selftest != 1)
+        return REPRO_ERR_ARG;
     g_cfg.bwd_segment_log2 = cfg->bwd_segment_log2;
     g_cfg.reduce_block_log2 = cfg->reduce_block_log2;
     g_cfg.fwd_path = cfg->fwd_path;
     g_cfg.elementwise_blocks = cfg->elementwise_blocks < 0 ? 0 : cfg->elementwise_blocks;
     g_cfg.bwd_kernel = cfg->bwd_kernel < 0 ? kDefaultBwdKernel : cfg->bwd_kernel;
+    g_cfg.fwd_selftest = cfg->fwd_selftest;
     return REPRO_OK;
 }
 
@@ -189,6 +232,9 @@ int repro_selftest(void* ws, size_t ws_bytes, void* stream)
     const int r = run_selftest(ws, as_stream(stream));
     if (r < 0)
         return REPRO_ERR_LAUNCH;
+    const int dev = current_device();
+    if (dev >= 0 && dev < kMaxDevices)
+        g_tc_state[dev].store(r == 0 ? 1 : -1);   // the forward's gate uses this result
     return r == 0 ? REPRO_OK : REPRO_ERR_SELFTEST;
 }
 
@@ -216,6 +262,9 @@ int repro_device_check(void* stream)
             return REPRO_ERR_LAUNCH;
         return REPRO_ERR_TIMEOUT;
     }
+    const int dev = current_device();
+    if (dev >= 0 && dev < kMaxDevices && g_tc_notice[dev].exchange(0) != 0)
+        return REPRO_ERR_SELFTEST;
     return REPRO_OK;
 }
 
@@ -377,11 +426,19 @@ int repro_quant_i8_multi(const float* const* xs, const int64_t* ns, int count,
                                         stream_grid(total / 16, 32), as_stream(stream)));
 }
 
+// tensor-core shapes: the bf16 copies, and room for the once-per-device
+// exactness check that may run first
+static size_t fwd_ws_need(int64_t M, int64_t N, int64_t K)
+{
+    const size_t a = fwd_tc_ws_bytes(M, N, K), b = selftest_ws_bytes();
+    return a > b ? a : b;
+}
+
 size_t repro_linear_fwd_ws_bytes(int64_t M, int64_t N, int64_t K)
 {
     if (!use_tc(M, N, K))
         return 0;
-    return fwd_tc_ws_bytes(M, N, K);
+    return fwd_ws_need(M, N, K);
 }
 
 int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x, const float* s_w,
@@ -400,9 +457,9 @@ int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x, const
     if (overlap(y, ybytes, xq, (size_t)(M * K)) || overlap(y, ybytes, wq, (size_t)(N * K)) ||
         overlap(y, ybytes, s_x, 4) || overlap(y, ybytes, s_w, 4))
         return REPRO_ERR_ALIAS;
-    const bool tc = use_tc(M, N, K);
+    bool tc = use_tc(M, N, K);
     if (tc) {
-        const size_t need = fwd_tc_ws_bytes(M, N, K);
+        const size_t need = fwd_ws_need(M, N, K);
         if (!ws || ws_bytes < need)
             return REPRO_ERR_WORKSPACE;
         if (!al16(ws))
@@ -415,6 +472,12 @@ int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x, const
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    if (tc && g_cfg.fwd_path < 1) {   // the default path is gated; explicit tile paths are not
+        const int gate = tc_gate(ws, as_stream(stream));
+        if (gate < 0)
+            return REPRO_ERR_LAUNCH;
+        tc = gate == 1;
+    }
     if (tc)
         return status_of(launch_fwd_tc(xq, wq, s_x, s_w, y, M, N, K, ws, g_cfg.fwd_path != 2,
                                        as_stream(stream)));

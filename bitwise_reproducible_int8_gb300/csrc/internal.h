@@ -17,6 +17,7 @@ struct LaunchCfg {
     int fwd_path;           // 0: CUDA-core exact path, 1: tensor cores 128 x 256 tiles, 2: 128 x 128
     int elementwise_blocks; // 0: default grid for streaming kernels
     int bwd_kernel;         // 8: tensor-copy-fed kernel (default), 1: register-prefetch kernel
+    int fwd_selftest;       // -1: gate the tensor-core forward on its self-test; 1: treat it as failed
 };
 
 const LaunchCfg& launch_cfg();

@@ -91,7 +91,10 @@ k_treefold(const Parts parts, int64_t n, float* out)
             o = make_float4(treefold_lane<R>(x), treefold_lane<R>(y), treefold_lane<R>(z),
                             treefold_lane<R>(w));
         }
-        reinterpret_cast<float4*>(out)[i] = o;
+        // evict-first: the folded gradient leaves the step (the optimiser or
+        // the host reads it next), so its lines are written back now instead
+        // of lingering dirty in L2 into the next kernel's reads
+        __stcs(reinterpret_cast<float4*>(out) + i, o);
     }
     if (blockIdx.x == 0 && threadIdx.x < (n & 3)) {
         const int64_t i = (nv << 2) + threadIdx.x;

@@ -7,9 +7,12 @@
 // tensor-core path (both tile widths, 128 x 256 and 128 x 128) and the
 // CUDA-core dp4a path (exact by construction) on
 // adversarial codes -- every code at the clamp, alternating signs, a sign flip
-// at the slice boundary, one small term among large ones, hashed codes -- and
-// compares the outputs bit for bit.  With unit scales and K = 1024 every
-// output is an integer below 2^24, exact in fp32, so a wrong integer shows.
+// at the slice boundary, one small term among large ones, a slice whose
+// running sum reaches 511 * 16129 = 8,241,919 (just below 2^23) before a last
+// product of +-1 (so the accumulator's lowest integer bit is probed at the top
+// of its range), hashed codes -- and compares the outputs bit for bit.  With
+// unit scales and K = 1024 every output is an integer below 2^24, exact in
+// fp32, so a wrong integer shows.
 #include "internal.h"
 
 namespace repro {
@@ -33,6 +36,7 @@ __device__ __forceinline__ int x_code(int r, int c)
     case 1: return (c & 1) ? -127 : 127;
     case 2: return c == r ? 1 : 127;
     case 3: return -127;
+    case 5: return (c & 511) == 511 ? (((r >> 3) & 1) ? -1 : 1) : 127;
     default: return hashed_code((uint32_t)r, (uint32_t)c);
     }
 }
@@ -44,6 +48,7 @@ __device__ __forceinline__ int w_code(int n, int c)
     case 1: return -127;
     case 2: return (c & 1) ? 127 : -127;
     case 3: return c < 512 ? 127 : -127;
+    case 5: return (c & 511) == 511 ? 1 : 127;
     default: return hashed_code((uint32_t)(n + 7919), (uint32_t)c);
     }
 }

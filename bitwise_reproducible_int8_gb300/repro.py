@@ -43,7 +43,7 @@ class AdamWHparams(ctypes.Structure):
 class LaunchCfg(ctypes.Structure):
     _fields_ = [("bwd_segment_log2", ctypes.c_int), ("reduce_block_log2", ctypes.c_int),
                 ("fwd_path", ctypes.c_int), ("elementwise_blocks", ctypes.c_int),
-                ("bwd_kernel", ctypes.c_int)]
+                ("bwd_kernel", ctypes.c_int), ("fwd_selftest", ctypes.c_int)]
 
 
 _vp = ctypes.c_void_p
@@ -435,9 +435,10 @@ def repro_wait_probe(arrive: int, stream=None) -> int:
 
 def repro_set_launch_cfg(bwd_segment_log2: int = -1, reduce_block_log2: int = -1,
                          fwd_path: int = -1, elementwise_blocks: int = -1, bwd_kernel: int = -1,
-                         reset: bool = False):
+                         fwd_selftest: int = -1, reset: bool = False):
     if reset:
         _check("repro_set_launch_cfg", lib().repro_set_launch_cfg(None))
         return
-    cfg = LaunchCfg(bwd_segment_log2, reduce_block_log2, fwd_path, elementwise_blocks, bwd_kernel)
+    cfg = LaunchCfg(bwd_segment_log2, reduce_block_log2, fwd_path, elementwise_blocks, bwd_kernel,
+                    fwd_selftest)
     _check("repro_set_launch_cfg", lib().repro_set_launch_cfg(ctypes.byref(cfg)))

@@ -145,6 +145,15 @@ int repro_quant_i8_multi(const float* const* xs, const int64_t* ns, int count,
  * copies of the codes, which the call writes into `ws` (at least
  * repro_linear_fwd_ws_bytes(M, N, K) bytes; 0 for shapes that use the exact
  * CUDA-core path).  Too small a workspace -> REPRO_ERR_WORKSPACE.
+ * The tensor-core path is exact only if the tensor core adds integer products
+ * exactly inside each 512-term slice, which the hardware documentation does
+ * not state; so the first such call on a device first runs the check of
+ * repro_selftest in `ws` and synchronises `stream` (once per device and
+ * process).  If the check fails, that call and every later one on the device
+ * take the exact CUDA-core path, and the next repro_device_check returns
+ * REPRO_ERR_SELFTEST.  A call made while `stream` is being captured into a
+ * CUDA graph cannot synchronise: before the check has run on the device it
+ * takes the CUDA-core path (so make one call before capturing).
  * ------------------------------------------------------------------------ */
 int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x,
                      const float* s_w, float* y, int64_t M, int64_t N, int64_t K,
@@ -351,8 +360,10 @@ size_t repro_state_hash_ws_bytes(const int64_t* nbytes, int nbuf);
  * repro_status_str: static description of a status code.
  * repro_version: REPRO_VERSION.
  * repro_device_check: synchronises `stream`, then reads and clears the
- *   device error word set by bounded device-side waits; returns REPRO_OK or
- *   REPRO_ERR_TIMEOUT (or REPRO_ERR_LAUNCH if the stream reported an error).
+ *   device error word set by bounded device-side waits; returns REPRO_OK,
+ *   REPRO_ERR_TIMEOUT, or REPRO_ERR_SELFTEST once after the forward's
+ *   exactness check failed on the current device (REPRO_ERR_LAUNCH if the
+ *   stream reported an error).
  * repro_launch_count: number of kernels this library has enqueued in this
  *   process (all devices, all streams); a diagnostic for counting launches.
  * repro_set_launch_cfg: test hook that changes how work is split across
@@ -375,6 +386,9 @@ typedef struct {
                                to the products by tensor copies (needs 16-byte-aligned rows:
                                N % 4 == 0 and K % 16 == 0, else 1 runs); 1: register-prefetch
                                kernel, any row alignment.  Other values: REPRO_ERR_ARG */
+    int fwd_selftest;       /* -1: default (the tensor-core forward runs only on a device whose
+                               exactness self-test has passed, see repro_linear_fwd); 1: test
+                               hook that acts as if the self-test had failed on every device */
 } repro_launch_cfg;
 
 /* ------------------------------------------------------------------------
@@ -410,11 +424,14 @@ const char* repro_status_str(int status);
  * over 512-term K-slices of integer products staying exact, which the
  * hardware documentation does not state; this runs it and the CUDA-core
  * (dp4a) path on adversarial codes (all at the clamp, alternating signs, a
- * sign flip at the slice boundary, hashed codes; 128 x 256 outputs, K = 1024,
+ * sign flip at the slice boundary, a slice whose running sum reaches
+ * 511 * 127 * 127 just below 2^23 before a product of +-1, hashed codes;
+ * 128 x 256 outputs, K = 1024,
  * unit scales) and compares every output bit, for both tensor-core tile
  * widths (128 x 256, the default, and 128 x 128).  Synchronises `stream`.  ws: device workspace of
  * repro_selftest_ws_bytes() bytes.  Returns REPRO_OK, REPRO_ERR_SELFTEST on a
- * mismatch, or an argument / launch error.
+ * mismatch, or an argument / launch error.  The result also decides, for the
+ * current device, whether later default-path forwards use the tensor cores.
  * ------------------------------------------------------------------------ */
 int repro_selftest(void* ws, size_t ws_bytes, void* stream);
 size_t repro_selftest_ws_bytes(void);

@@ -116,6 +116,9 @@ def test_linear_fwd_workspace(L):
         repro.repro_set_launch_cfg(fwd_path=1)
         need = repro.repro_linear_fwd_ws_bytes(16384, 2048, 2048)
         assert need >= 2 * (16384 + 2048) * 2048
+        # small tensor-core shapes still leave room for the once-per-device
+        # exactness check the first call runs in the workspace
+        assert repro.repro_linear_fwd_ws_bytes(8, 8, 8) == L.repro_selftest_ws_bytes()
         assert repro.repro_linear_fwd_ws_bytes(16, 16, 12) == 0     # K % 8 != 0: CUDA cores
         B = 1 << 32
         assert L.repro_linear_fwd(B, B * 2, B * 3, B * 3 + 4, B * 4, 16384, 2048, 2048,
@@ -206,6 +209,10 @@ def test_launch_cfg_validation(L):
                 repro.repro_set_launch_cfg(bwd_kernel=k)
         repro.repro_set_launch_cfg(bwd_kernel=1)
         repro.repro_set_launch_cfg(bwd_kernel=8)
+        for v in (0, 2):
+            with pytest.raises(repro.ReproError):
+                repro.repro_set_launch_cfg(fwd_selftest=v)
+        repro.repro_set_launch_cfg(fwd_selftest=1)
         repro.repro_set_launch_cfg(fwd_path=2)
         repro.repro_set_launch_cfg(bwd_segment_log2=0, reduce_block_log2=0, fwd_path=0,
                                    elementwise_blocks=152)

@@ -105,3 +105,67 @@ def test_repeat_and_stream_determinism():
     for got, exp, what in zip([G.host(t) for t in (hp.Y[0], hp.dX[0], hp.G)], ref,
                               ["Y", "dX", "dW"]):
         G.assert_bits_equal(got, exp, f"repeat {what}")
+
+
+def _band_rows(total, width):
+    return np.concatenate([np.arange(width), np.arange(total - width, total)]).astype(np.int64)
+
+
+@pytest.mark.parametrize("name", ["gate_up", "down_accum"])
+def test_fullsize_whole_tile_bands(orc, name):
+    # every element of whole tile bands at the full sizes: the first and last
+    # 128-row bands of Y and dX (every column: the forward's and dX kernel's
+    # first and last tile rows), and the first and last 64-column bands of
+    # the accumulated dW (every row: the dW kernel's first and last tile
+    # columns, across every reduction segment)
+    R.repro_set_launch_cfg(reset=True)
+    wl = inputs.WORKLOADS[name]
+    host = S.generate_host_inputs(wl)
+    hp = S.HotPathStep(wl, host)
+    hp.run(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    assert R.repro_device_check() == 0
+    lin, J, M = wl.linears[0], wl.microbatches, wl.tokens
+    W = host.W[0]
+    s_w = orc.wscale(W, 0)
+    wq = orc.quant_i8(W, s_w)
+    rows = _band_rows(M, 128)
+    cols = _band_rows(lin.k_in, 64)
+    # dW bands: every row n, columns in the two bands, accumulated over J
+    n_all = np.repeat(np.arange(lin.n_out, dtype=np.int64), cols.size)
+    k_all = np.tile(cols, lin.n_out)
+    g = None
+    for j in range(J):
+        X, dY = host.X[0][j], host.dY[0][j]
+        s_x = orc.wscale(X, 1)
+        xq = orc.quant_i8(X, s_x)
+        dw = orc.linear_bwd_dw_at(dY, xq, s_x, n_all, k_all)
+        g = dw if g is None else orc.grad_accum(g, dw)
+    G.assert_bits_equal(G.host(hp.Gv[0])[:, cols].ravel(), g, f"{name} dW column bands")
+    # Y and dX bands of the last micro-batch (still resident)
+    m_y = np.repeat(rows, lin.n_out)
+    c_y = np.tile(np.arange(lin.n_out, dtype=np.int64), rows.size)
+    G.assert_bits_equal(G.host(hp.Y[0])[rows].ravel(),
+                        orc.linear_fwd_at(xq, wq, s_x, s_w, m_y, c_y), f"{name} Y row bands")
+    m_x = np.repeat(rows, lin.k_in)
+    c_x = np.tile(np.arange(lin.k_in, dtype=np.int64), rows.size)
+    G.assert_bits_equal(G.host(hp.dX[0])[rows].ravel(),
+                        orc.linear_bwd_dx_at(dY, wq, s_w, m_x, c_x), f"{name} dX row bands")
+
+
+def test_block_steps_repeat_bit_for_bit():
+    # the benchmark's own set-up (dW on its second stream, fused accumulation,
+    # TreeFold over six replicas): two steps give the same TreeFold bytes
+    R.repro_set_launch_cfg(reset=True)
+    wl = inputs.WORKLOADS["block"]
+    hp = S.HotPathStep(wl)
+    assert hp.s_dw is not None
+    st = torch.cuda.Stream()
+    hp.prepare(st)
+    hp.run(st)
+    st.synchronize()
+    first = G.host(hp.TF).copy()
+    hp.run(st)
+    st.synchronize()
+    assert R.repro_device_check() == 0
+    G.assert_bits_equal(G.host(hp.TF), first, "block TreeFold, second step")

@@ -142,6 +142,47 @@ def test_tensor_core_forward_selftest():
     assert R.repro_selftest() == R.REPRO_OK
 
 
+def _fwd_launches(xq, wq, s_x, s_w):
+    torch.cuda.synchronize()
+    before = R.repro_launch_count()
+    y = G.gpu_fwd(xq, wq, s_x, s_w)
+    return y, R.repro_launch_count() - before
+
+
+def test_forward_gate_takes_the_tensor_cores_after_a_passed_check(orc):
+    # default path: the device's exactness check has passed (it runs on the
+    # first tensor-core call; every later call goes straight to the tensor
+    # cores: two int8 -> bf16 widening passes and the tensor-core kernel)
+    rng = np.random.default_rng(5)
+    xq = rng.integers(-127, 128, (300, 1024)).astype(np.int8)
+    wq = rng.integers(-127, 128, (260, 1024)).astype(np.int8)
+    s_x, s_w = np.float32(0.0371), np.float32(0.00284)
+    G.gpu_fwd(xq, wq, s_x, s_w)
+    assert R.repro_device_check() == R.REPRO_OK        # no failed check to report
+    y, n = _fwd_launches(xq, wq, s_x, s_w)
+    G.assert_bits_equal(y, orc.linear_fwd(xq, wq, s_x, s_w), "gated forward")
+    assert n == 3, n
+
+
+def test_forward_gate_falls_back_to_the_exact_path(orc):
+    # the test hook acts as if the check had failed: the same call takes the
+    # CUDA-core (dp4a) kernel alone, gives the oracle's bits, and the next
+    # device check reports the failure once
+    R.repro_set_launch_cfg(fwd_selftest=1)
+    rng = np.random.default_rng(6)
+    xq = rng.integers(-127, 128, (300, 1024)).astype(np.int8)
+    wq = rng.integers(-127, 128, (260, 1024)).astype(np.int8)
+    s_x, s_w = np.float32(0.0371), np.float32(0.00284)
+    y, n = _fwd_launches(xq, wq, s_x, s_w)
+    G.assert_bits_equal(y, orc.linear_fwd(xq, wq, s_x, s_w), "fallback forward")
+    assert n == 1, n
+    assert R.repro_device_check() == -9                 # REPRO_ERR_SELFTEST
+    assert R.repro_device_check() == R.REPRO_OK
+    R.repro_set_launch_cfg(reset=True)
+    y, n = _fwd_launches(xq, wq, s_x, s_w)
+    assert n == 3 and R.repro_device_check() == R.REPRO_OK
+
+
 @pytest.mark.parametrize("path", [0, 1, 2])
 def test_forward_at_the_maximum_reduction(orc, path):
     # K = 133,144 is the largest K for which |acc| <= 127 * 127 * K fits int32;
