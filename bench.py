@@ -40,7 +40,13 @@ METRIC = "tokens/s bit-exact int8-QAT linear fwd+bwd (1 GB300); % of int8/FP32/H
 # launches of the block workload's 4 captured steps, from one ncu capture of
 # dram__bytes_read.sum + dram__bytes_write.sum (single pass) on a GB300.  Valid only
 # for that kernel and workload; anything else reports null.
-BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd_tma"): 1654.9e6}
+# DRAM bytes per backward launch: mean over the block step's eight launch shapes,
+# from one ncu capture (-k regex:k_bwd_tma -c 8, dram__bytes_read.sum +
+# dram__bytes_write.sum) of the one-micro-batch profiling case block_1mb
+BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd_tma"): 1649.5e6, ("block_1mb", "k_bwd_tma"): 1649.5e6}
+BWD_TRAFFIC_SOURCE = ("profiles/k_bwd_tma_traffic_block.md: ncu -k regex:k_bwd_tma -c 8 "
+                      "--metrics dram__bytes_read.sum,dram__bytes_write.sum on block_1mb "
+                      "(the block step's eight backward shapes), mean per launch")
 UNIT = "tokens/s"
 
 
@@ -440,7 +446,9 @@ def run_ours(args, wl):
             # the same work as a FLOP fraction of the peak that counts an FFMA as
             # two FLOPs; without FMA this can reach at most 0.5
             "flop_frac_of_ffma_peak": achieved / (2 * fp32_peak) if fp32_peak else None,
-            "traffic": traffic, "launches": nb,
+            "traffic": traffic,
+            "traffic_source": BWD_TRAFFIC_SOURCE if traffic is not None else None,
+            "launches": nb,
             "flops_per_launch": bwd_ops / per_unit if per_unit else None,
             "avg_launch_ms": bwd_ms / per_unit if per_unit else None,
         }

@@ -130,6 +130,11 @@ WORKLOADS = {
     # profiling case: a few GB on the device, TreeFold inputs (6 x 92 MB) larger than L2
     "gate_up_r6": Workload("gate_up_r6", TOKENS_PER_MICROBATCH, (GATE_UP,), 1, 6, 0, 0,
                            "gate+up projection, one micro-batch, TreeFold over R=6"),
+    # profiling case for the backward's DRAM traffic: the block's four linears,
+    # one micro-batch, no folds -- every backward launch shape of the block
+    # step once, about 5 GB on the device
+    "block_1mb": Workload("block_1mb", TOKENS_PER_MICROBATCH, (QKV, O_PROJ, GATE_UP, DOWN), 1, 0,
+                          100, 0, "block linears, one micro-batch, no TreeFold"),
     # profiling case for the audit calls: the block's four weights (so the hashed
     # state, 541 MB, and the 8 shard partials exceed L2) with one 2,048-token
     # micro-batch, about 3.5 GB on the device
