@@ -127,6 +127,16 @@ bool use_tc(int64_t M, int64_t N, int64_t K)
     return g_cfg.fwd_path != 0 && fwd_tc_supported(M, N, K);
 }
 
+// 1 when the current device's exactness check has passed (the test hook's
+// forced failure aside), else 0; never runs the check
+int tc_state_passed()
+{
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices || g_cfg.fwd_selftest == 1)
+        return 0;
+    return g_tc_state[dev].load() > 0 ? 1 : 0;
+}
+
 // Whether a default-path forward may use the tensor cores on the current
 // device: 1 yes, 0 take the CUDA-core path, negative a CUDA error.  The first
 // call on a device runs the exactness self-test in `ws` (at least
@@ -733,8 +743,18 @@ int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    // P.V on the tensor cores needs the logit cache and a device whose exactness
+    // check has passed (run here, in the cache's space, if it has not run yet)
+    bool tc = false;
+    if (ws && g_cfg.fwd_path != 0) {
+        const int gate = ws_bytes >= selftest_ws_bytes() ? tc_gate(ws, as_stream(stream))
+                                                         : tc_state_passed();
+        if (gate < 0)
+            return REPRO_ERR_LAUNCH;
+        tc = gate == 1;
+    }
     return status_of(
-        launch_attn_fwd(q, k, vq, s_v, o, m, l, B, T, Hq, Hkv, W, ws, as_stream(stream)));
+        launch_attn_fwd(q, k, vq, s_v, o, m, l, B, T, Hq, Hkv, W, ws, tc, as_stream(stream)));
 }
 
 size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq)

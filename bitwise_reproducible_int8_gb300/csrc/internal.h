@@ -91,7 +91,7 @@ cudaError_t launch_treefold(const float* const* parts, int R, int64_t n, float* 
 size_t attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);
 cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                             float* o, float* m, float* l, int64_t B, int64_t T, int64_t Hq,
-                            int64_t Hkv, int64_t W, void* cache, cudaStream_t st);
+                            int64_t Hkv, int64_t W, void* cache, bool tc, cudaStream_t st);
 
 size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq);
 cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,

@@ -1,0 +1,86 @@
+// umma.cuh -- the 5th-generation tensor-core pieces shared by the exact
+// int8 forward (k_fwd_tc.cu) and the attention's P.V (k_attn.cu): shared-
+// memory matrix descriptors for 128-byte-swizzled K-major bf16 tiles, the
+// kind::f16 instruction descriptor with an fp32 accumulator, the MMA issue
+// and commit, and tensor-memory loads.
+//
+// Operand layout these descriptors expect: a tile of rows of 64 bf16 (128
+// bytes); row r's 16-byte chunk c at byte (r / 8) * 1024 + (r % 8) * 128 +
+// ((c ^ (r % 8)) * 16), the tile 1024-byte aligned -- the layout a TMA copy
+// with 128-byte swizzle writes.  Successive K = 16 slices of a 64-wide tile
+// start 32 bytes apart (descriptor + 2).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pipeline.cuh"
+
+namespace repro {
+
+constexpr int UMMA_M = 128;   // rows of every MMA issued here
+
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = TN, M = 128
+template <int TN>
+__host__ __device__ constexpr uint32_t idesc()
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TN >> 3) << 17) |
+           ((uint32_t)(UMMA_M >> 4) << 24);
+}
+
+template <int TN>
+__device__ __forceinline__ void mma_bf16(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+        "l"(a), "l"(b), "r"(idesc<TN>()), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            su32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+#define R8(i) "=r"(v[i + 0]), "=r"(v[i + 1]), "=r"(v[i + 2]), "=r"(v[i + 3]), "=r"(v[i + 4]), \
+              "=r"(v[i + 5]), "=r"(v[i + 6]), "=r"(v[i + 7])
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : R8(0), R8(8), R8(16), R8(24)
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : R8(0), R8(8)
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+#undef R8
+
+} // namespace repro

@@ -285,7 +285,13 @@ int repro_adamw_step(float* p, float* m, float* v, const float* g, int64_t n,
  * least repro_attn_fwd_ws_bytes(B, T, Hq, W) bytes the first pass stores its
  * logits there and the second reads them back and replaces each by
  * p_ij = e^(s_ij - m_i) (0 for masked pairs), which repro_attn_bwd can reuse;
- * with ws == NULL the second pass recomputes the logits.  Same bits either way.  The cache holds every visited
+ * with ws == NULL the second pass recomputes the logits.  Same bits either way.
+ * With the cache, P.V runs on the tensor cores (the int8 codes as bf16 into
+ * tcgen05 kind::f16, fp32 accumulation over exact slices of 512 keys, each
+ * converted to int32) on a device whose forward exactness check has passed
+ * (repro_linear_fwd: run here in `ws` if it has not run yet, when ws holds at
+ * least repro_selftest_ws_bytes()); otherwise, and without the cache, with
+ * dp4a on CUDA cores.  The integer sum, and so every bit, is the same.  The cache holds every visited
  * 64 x 64 logit tile: about 4 * 64 * (W + 64) bytes per query row and head for a
  * window W, 2 * T bytes per query row and head for full causal.
  * ------------------------------------------------------------------------ */

@@ -11,6 +11,15 @@ import gpu_helpers as G
 
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(scope="module", autouse=True)
+def _exactness_checked():
+    # the device's tensor-core exactness check runs first, so every cached
+    # forward below takes the tensor-core P.V route (small caches cannot hold
+    # the check's scratch and would otherwise take the CUDA-core route until a
+    # larger call had run it)
+    assert R.repro_selftest() == R.REPRO_OK
+
 D = 128
 
 
@@ -41,15 +50,30 @@ def gpu_attn_fwd(q, k, vq, s_v, W, cache=True, keep_cache=False):
 
 
 SHAPES = [(1, 1, 4, 2), (1, 5, 4, 2), (1, 63, 2, 2), (1, 64, 4, 1), (2, 65, 4, 2),
-          (1, 130, 8, 2), (2, 200, 4, 4), (1, 257, 4, 2)]
+          (1, 130, 8, 2), (2, 200, 4, 4), (1, 257, 4, 2), (1, 600, 4, 2)]
+
+# cached: the logit cache on, P.V on the tensor cores (the default); cached_dp4a:
+# the cache on, P.V on CUDA cores (the launch-configuration hook's fwd_path 0);
+# recomputed: no cache, P.V on CUDA cores.  T = 600 with W = 0 spans more than
+# 512 keys, so the tensor-core route reads back two exact slices.
+ROUTES = ["cached", "cached_dp4a", "recomputed"]
 
 
-@pytest.mark.parametrize("cache", [True, False], ids=["cached", "recomputed"])
+@pytest.fixture
+def route(request):
+    R.repro_set_launch_cfg(reset=True)
+    if request.param == "cached_dp4a":
+        R.repro_set_launch_cfg(fwd_path=0)
+    yield request.param
+    R.repro_set_launch_cfg(reset=True)
+
+
+@pytest.mark.parametrize("route", ROUTES, indirect=True)
 @pytest.mark.parametrize("W", [0, 1, 7, 64, 100])
 @pytest.mark.parametrize("B,T,Hq,Hkv", SHAPES)
-def test_attn_fwd_matches_oracle(orc, B, T, Hq, Hkv, W, cache):
+def test_attn_fwd_matches_oracle(orc, B, T, Hq, Hkv, W, route):
     q, k, vq, s_v = _case(B * 1000 + T * 10 + W, B, T, Hq, Hkv)
-    o, m, l = gpu_attn_fwd(q, k, vq, s_v, W, cache)
+    o, m, l = gpu_attn_fwd(q, k, vq, s_v, W, route != "recomputed")
     ro, rm, rl = orc.attn_fwd(q, k, vq, s_v, W)
     G.assert_bits_equal(m, rm, f"m T={T} W={W}")
     G.assert_bits_equal(l, rl, f"l T={T} W={W}")
@@ -228,3 +252,24 @@ def test_attn_at_the_maximum_length(orc):
     G.assert_bits_equal(dq.reshape(-1, D)[rows], rq, "dq rows")
     G.assert_bits_equal(dk.reshape(-1, D)[krows], rk, "dk rows")
     G.assert_bits_equal(dv.reshape(-1, D)[krows], rv, "dv rows")
+
+
+def test_attn_fwd_gate_falls_back_to_dp4a(orc):
+    # with the forward's exactness check reported failed (test hook), the
+    # cached forward computes P.V on CUDA cores: same bits, failure reported
+    q, k, vq, s_v = _case(77, 1, 600, 4, 2)
+    R.repro_set_launch_cfg(fwd_selftest=1)
+    try:
+        B, T, Hq, _ = q.shape
+        o = torch.empty((B, T, Hq, D), device="cuda")
+        m = torch.empty((B, T, Hq), device="cuda")
+        l = torch.empty((B, T, Hq), device="cuda")
+        ws = torch.empty(R.repro_attn_fwd_ws_bytes(B, T, Hq, 0), dtype=torch.uint8, device="cuda")
+        R.repro_attn_fwd(G.dev(q), G.dev(k), G.dev(vq), G.scalar(s_v), o, m, l, 0, ws=ws)
+        assert R.repro_device_check() == -9        # the failed check, reported once
+        assert R.repro_device_check() == 0
+    finally:
+        R.repro_set_launch_cfg(reset=True)
+    ro, rm, rl = orc.attn_fwd(q, k, vq, s_v, 0)
+    G.assert_bits_equal(G.host(o), ro, "o")
+    G.assert_bits_equal(G.host(l), rl, "l")
