@@ -53,20 +53,37 @@ __device__ __forceinline__ void tmem_fold32(uint32_t taddr, u64 (&acc)[16])
         acc[e] = fadd2_ftz((u64)w[2 * e] | ((u64)w[2 * e + 1] << 32), acc[e]);
 }
 
-// one reduction step: rows 8ty..8ty+7 as 4 pairs, columns 4tx..4tx+3
+// one reduction step: rows 8ty..8ty+7 as 4 pairs, columns 4tx..4tx+3.  The
+// products of row pair ip+1 are formed before the adds of row pair ip, so no
+// add waits on the multiply just issued; every accumulator still sees its
+// own product, then its one add, in the same order
 template <bool FIRST>
 __device__ __forceinline__ void step(u64 (&acc)[16], const ulonglong2& a03, const ulonglong2& a47,
                                      const float4& b)
 {
     const u64 P[4] = {a03.x, a03.y, a47.x, a47.y};
     const u64 D[4] = {pack2(b.x, b.x), pack2(b.y, b.y), pack2(b.z, b.z), pack2(b.w, b.w)};
+    u64 cur[4];
 #pragma unroll
-    for (int ip = 0; ip < 4; ++ip)
+    for (int j = 0; j < 4; ++j)
+        cur[j] = fmul2_rn(P[0], D[j]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const u64 p = fmul2_rn(P[ip], D[j]);
-            acc[ip * 4 + j] = FIRST ? p : fadd2_ftz(acc[ip * 4 + j], p);
+    for (int ip = 0; ip < 4; ++ip) {
+        u64 nxt[4];
+        if (ip + 1 < 4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                nxt[j] = fmul2_rn(P[ip + 1], D[j]);
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            acc[ip * 4 + j] = FIRST ? cur[j] : fadd2_ftz(acc[ip * 4 + j], cur[j]);
+        if (ip + 1 < 4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                cur[j] = nxt[j];
+        }
+    }
 }
 
 } // namespace repro

@@ -28,10 +28,11 @@
 //     stages; at the start of chunk c it refills the stage that every warp
 //     released at the end of chunk c - 2 with chunk c + 2, so no warp runs
 //     more than two chunks ahead of warp 0 and every wait ends;
-//   * with 8 warps a thread may hold 255 registers, so tree levels 0..RL-1
-//     (RL = 3) stay in registers and the rest live in tensor memory (thread:
-//     lane 32*(warp%4) + lane, columns (warp/4)*256 + 32*(level-RL)), touched
-//     once every 8 chunks.
+//   * with 8 warps a thread may hold 255 registers: tree levels 0..RL-1
+//     (RL = 2) stay in registers, beside the products formed one row pair
+//     ahead of their adds, and the rest live in tensor memory (thread: lane
+//     32*(warp%4) + lane, columns (warp/4)*256 + 32*(level-RL)), touched once
+//     every 4 chunks.
 // Every wait is bounded: past the limit the CTA records a failure in the
 // device error word, lets its copies land, frees its tensor memory and exits.
 #include <cuda.h>
@@ -47,7 +48,7 @@ namespace repro {
 namespace {
 
 constexpr int NC = 256;                        // threads (8 warps)
-constexpr int RL = 3;                          // tree levels kept in registers
+constexpr int RL = 2;                          // tree levels kept in registers
 constexpr int TI = BWD_TMA_ROWS;               // 128 tile rows (i)
 constexpr int STG = 4;                         // ring stages
 constexpr int A_BYTES = CH * TI * 4;           // 32768: A[r][i]
