@@ -261,6 +261,10 @@ class OracleSample:
 
 def _sample_text(wl, frac_log2, r) -> str:
     parts = ", ".join(f"{k} {sec:.2f} s / {fr:.2e}" for k, (sec, fr) in r["parts"].items())
+    if frac_log2 == 0:
+        parts = ", ".join(f"{k} {sec:.3f} s" for k, (sec, _) in r["parts"].items())
+        return (f"{wl.name}: the whole step, every output of every call; parts: {parts}; "
+                f"{r['timed_s']:.3f} s on {r['threads']} threads")
     return (f"{wl.name}: the first 1/{1 << frac_log2} of the outputs of every call of one step "
             f"(Y, dX, dW, codes, the gradient's accumulation and TreeFold), each part of the "
             f"step timed on its own sample and divided by that sample's fraction of the part's "
@@ -270,18 +274,25 @@ def _sample_text(wl, frac_log2, r) -> str:
 
 
 def cpu_baseline(wl, host, frac_log2: int, one_core_extra_log2: int = 2) -> dict:
-    """The oracle on every host core (the reported value), and on one core on a
-    2^-extra smaller slice (extrapolated the same way)."""
+    """The oracle on every host core (the reported value), and on one core.  A
+    small step (under 2^30 multiply-adds, the single-linear 64-token case) runs
+    whole both times; a larger one is sampled, the one-core sample 2^-extra the
+    size of the all-core one, both extrapolated part by part."""
     smp = OracleSample(wl, host)
     smp.prepare()
-    r = smp.run(frac_log2)
     tokens = wl.tokens * wl.microbatches
-    r1 = smp.run(frac_log2 + one_core_extra_log2, threads=1)
+    macs = tokens * sum(l.n_out * l.k_in for l in wl.linears)
+    small = macs < (1 << 30)   # a sample's fixed per-call costs would swamp it: run it whole
+    if small:
+        frac_log2 = 0
+    r = smp.run(frac_log2)
+    one_log2 = 0 if small else frac_log2 + one_core_extra_log2
+    r1 = smp.run(one_log2, threads=1)
     return {"value": tokens / r["step_s"], "unit": UNIT, "cores": r["threads"], "kind": "oracle",
             "sample": _sample_text(wl, frac_log2, r),
             "one_core": {"value": tokens / r1["step_s"], "unit": UNIT, "cores": 1,
-                         "sample": _sample_text(wl, frac_log2 + one_core_extra_log2, r1),
-                         "extrapolated": True}}
+                         "sample": _sample_text(wl, one_log2, r1),
+                         "extrapolated": one_log2 > 0}}
 
 
 def run_reference(args, wl):
