@@ -21,6 +21,7 @@
 // row sums through the canonical-order chunk/tree stack (one thread per row)
 // and accumulates P.V with dp4a (exact int32).  Logits: 256 threads own 4 x 4
 // outputs each, packed f32x2 products over d with the chunk-of-64 order.
+#include "bwd_tile.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "umma.cuh"
@@ -71,6 +72,10 @@ constexpr size_t FWD_SMEM = (size_t)(2 * HD * PT + AT * PS) * 4 + (size_t)(AT * 
                             (size_t)(AT / 4 * HD) * 4 + (size_t)(AT * (MAXL + 1)) * 4 +
                             (size_t)(3 * AT) * 4;
 
+// pass 1's second key tile lives in pass 2's scratch (Ps .. stk)
+static_assert(HD * PT <= AT * PS + AT * PP + AT / 4 * HD + AT * (MAXL + 1),
+              "second key tile does not fit in the pass-2 scratch");
+
 // e^x: the reduction, polynomial and scaling stated above
 __device__ __forceinline__ float exp_r(float x)
 {
@@ -96,6 +101,44 @@ __device__ __forceinline__ float exp_r(float x)
     return flush(fmul_rn(p, __int_as_float((k + 127) << 23)));
 }
 
+// e^x of two lanes: the same operations as exp_r, lane by lane, with the
+// reduction and the polynomial on packed pairs
+__device__ __forceinline__ float exp_scale(float p, float kf)
+{
+    if (kf < -126.0f)
+        return 0.0f;
+    if (kf > 254.0f)
+        return __int_as_float(0x7f800000);
+    const int k = (int)kf;
+    if (k > 127)
+        return flush(fmul_rn(fmul_rn(p, 0x1p127f), __int_as_float((k - 127 + 127) << 23)));
+    return flush(fmul_rn(p, __int_as_float((k + 127) << 23)));
+}
+
+__device__ __forceinline__ u64 exp_r2(u64 x)
+{
+    const u64 z = pack2(-0.0f, -0.0f);
+    x = fadd2_ftz(x, z);
+    float t0, t1;
+    unpack2(fadd2_ftz(fmul2_rn(x, pack2(0x1.715476p+0f, 0x1.715476p+0f)), z), t0, t1);
+    const float k0 = rintf(t0), k1 = rintf(t1);
+    const u64 kf = pack2(k0, k1);
+    // x (-) RN(kf c1), then (-) RN(kf c2); the negated products are RN(kf (-c))
+    const u64 r = fadd2_ftz(fadd2_ftz(x, fadd2_ftz(fmul2_rn(kf, pack2(-0x1.63p-1f, -0x1.63p-1f)), z)),
+                            fadd2_ftz(fmul2_rn(kf, pack2(0x1.bd0106p-13f, 0x1.bd0106p-13f)), z));
+    u64 p = pack2(0x1.a01a02p-13f, 0x1.a01a02p-13f);
+    p = fadd2_ftz(fmul2_rn(p, r), pack2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+    p = fadd2_ftz(fmul2_rn(p, r), pack2(0x1.111112p-7f, 0x1.111112p-7f));
+    p = fadd2_ftz(fmul2_rn(p, r), pack2(0x1.555556p-5f, 0x1.555556p-5f));
+    p = fadd2_ftz(fmul2_rn(p, r), pack2(0x1.555556p-3f, 0x1.555556p-3f));
+    p = fadd2_ftz(fmul2_rn(p, r), pack2(0.5f, 0.5f));
+    p = fadd2_ftz(fmul2_rn(p, r), pack2(1.0f, 1.0f));
+    p = fadd2_ftz(fmul2_rn(p, r), pack2(1.0f, 1.0f));
+    float p0, p1;
+    unpack2(p, p0, p1);
+    return pack2(exp_scale(p0, k0), exp_scale(p1, k1));
+}
+
 __device__ __forceinline__ int quant_p(float p)
 {
     float r = rintf(fmul_flush(p, 127.0f));
@@ -105,80 +148,113 @@ __device__ __forceinline__ int quant_p(float p)
 
 // tile of 64 rows x 128 floats of a [.., H, 128] tensor, flushed and
 // transposed into t[d][r] (pitch PT); rows outside [0, T) read as 0.
-// Warp lanes cover 8 rows x 4 float4 columns per step.
-__device__ __forceinline__ void load_tile_t(float* __restrict__ t, const float* __restrict__ src,
-                                            int64_t row0, int64_t T, int64_t row_stride, int tid)
+// Warp lanes cover 8 rows x 4 float4 columns per step; step it covers
+// d = 16 it .. 16 it + 15, so steps 0-3 and 4-7 are the two halves of d.
+// tile_fetch / tile_put split one half into its global loads and its shared
+// stores, so the loads of the next tile can be in flight during a product
+__device__ __forceinline__ void tile_fetch(float4 (&v)[4], const float* __restrict__ src,
+                                           int64_t row0, int64_t T, int64_t row_stride, int tid,
+                                           int half)
 {
 #pragma unroll
-    for (int it = 0; it < (AT * HD / 4) / NT; ++it) {
+    for (int u = 0; u < 4; ++u) {
+        const int it = 4 * half + u;
         const int e = tid + it * NT;            // 2048 float4 pieces
         const int lane = e & 31, w = e >> 5;    // w: 64 groups of 8 rows x 4 columns
         const int r = (w & 7) * 8 + (lane & 7);
         const int c4 = (w >> 3) * 4 + (lane >> 3);
         const int64_t row = row0 + r;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (row >= 0 && row < T)
-            v = flush4(*reinterpret_cast<const float4*>(src + row * row_stride + 4 * c4));
-        t[(4 * c4 + 0) * PT + r] = v.x;
-        t[(4 * c4 + 1) * PT + r] = v.y;
-        t[(4 * c4 + 2) * PT + r] = v.z;
-        t[(4 * c4 + 3) * PT + r] = v.w;
+            v[u] = *reinterpret_cast<const float4*>(src + row * row_stride + 4 * c4);
+    }
+}
+
+__device__ __forceinline__ void tile_put(float* __restrict__ t, const float4 (&v)[4], int tid,
+                                         int half)
+{
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int it = 4 * half + u;
+        const int e = tid + it * NT;
+        const int lane = e & 31, w = e >> 5;
+        const int r = (w & 7) * 8 + (lane & 7);
+        const int c4 = (w >> 3) * 4 + (lane >> 3);
+        const float4 f = flush4(v[u]);
+        t[(4 * c4 + 0) * PT + r] = f.x;
+        t[(4 * c4 + 1) * PT + r] = f.y;
+        t[(4 * c4 + 2) * PT + r] = f.z;
+        t[(4 * c4 + 3) * PT + r] = f.w;
+    }
+}
+
+__device__ __forceinline__ void load_tile_t(float* __restrict__ t, const float* __restrict__ src,
+                                            int64_t row0, int64_t T, int64_t row_stride, int tid)
+{
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        float4 v[4];
+        tile_fetch(v, src, row0, T, row_stride, tid, half);
+        tile_put(t, v, tid, half);
     }
 }
 
 // the thread's 4 x 4 logits: rows 4ty..4ty+3 (as 2 packed pairs), columns
-// 4tx..4tx+3; canonical order over d: two chunks of 64, then one pairwise add
+// 4tx..4tx+3; canonical order over d: two chunks of 64, then one pairwise add.
+// logit_chunk is one chunk's left-to-right sum (d0 = 0 or 64), logit_finish the
+// pairwise add and the scaling
+__device__ __forceinline__ void logit_chunk(u64 (&acc)[8], const float* __restrict__ Qt,
+                                            const float* __restrict__ Kt, int ty, int tx, int d0)
+{
+    // operands are loaded one step ahead of their products
+    const float* qp = Qt + 4 * ty;
+    const float* kp = Kt + 4 * tx;
+    ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qp + d0 * PT);
+    float4 kb = *reinterpret_cast<const float4*>(kp + d0 * PT);
+    {
+        const u64 P[2] = {qa.x, qa.y};
+        const u64 D[4] = {pack2(kb.x, kb.x), pack2(kb.y, kb.y), pack2(kb.z, kb.z),
+                          pack2(kb.w, kb.w)};
+        qa = *reinterpret_cast<const ulonglong2*>(qp + (d0 + 1) * PT);
+        kb = *reinterpret_cast<const float4*>(kp + (d0 + 1) * PT);
+#pragma unroll
+        for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                acc[ip * 4 + j] = fmul2_rn(P[ip], D[j]);
+    }
+#pragma unroll 9
+    for (int dd = 1; dd < 64; ++dd) {
+        const u64 P[2] = {qa.x, qa.y};
+        const u64 D[4] = {pack2(kb.x, kb.x), pack2(kb.y, kb.y), pack2(kb.z, kb.z),
+                          pack2(kb.w, kb.w)};
+        const int dn = d0 + (dd + 1 < 64 ? dd + 1 : dd);
+        qa = *reinterpret_cast<const ulonglong2*>(qp + dn * PT);
+        kb = *reinterpret_cast<const float4*>(kp + dn * PT);
+#pragma unroll
+        for (int ip = 0; ip < 2; ++ip)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                acc[ip * 4 + j] = fadd2_ftz(acc[ip * 4 + j], fmul2_rn(P[ip], D[j]));
+    }
+}
+
+__device__ __forceinline__ void logit_finish(u64 (&s)[8], const u64 (&t0)[8], const u64 (&t1)[8],
+                                             float c)
+{
+    const u64 cc = pack2(c, c);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)   // (x) c, flushed
+        s[e] = fadd2_ftz(fmul2_rn(fadd2_ftz(t0[e], t1[e]), cc), pack2(-0.0f, -0.0f));
+}
+
 __device__ __forceinline__ void logits4x4(u64 (&s)[8], const float* __restrict__ Qt,
                                           const float* __restrict__ Kt, int ty, int tx, float c)
 {
-    u64 t0[8];
-    const float* qp = Qt + 4 * ty;
-    const float* kp = Kt + 4 * tx;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        // operands are loaded one step ahead of their products
-        const int d0 = half * 64;
-        u64 acc[8];
-        ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(qp + d0 * PT);
-        float4 kb = *reinterpret_cast<const float4*>(kp + d0 * PT);
-        {
-            const u64 P[2] = {qa.x, qa.y};
-            const u64 D[4] = {pack2(kb.x, kb.x), pack2(kb.y, kb.y), pack2(kb.z, kb.z),
-                              pack2(kb.w, kb.w)};
-            qa = *reinterpret_cast<const ulonglong2*>(qp + (d0 + 1) * PT);
-            kb = *reinterpret_cast<const float4*>(kp + (d0 + 1) * PT);
-#pragma unroll
-            for (int ip = 0; ip < 2; ++ip)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    acc[ip * 4 + j] = fmul2_rn(P[ip], D[j]);
-        }
-#pragma unroll 9
-        for (int dd = 1; dd < 64; ++dd) {
-            const u64 P[2] = {qa.x, qa.y};
-            const u64 D[4] = {pack2(kb.x, kb.x), pack2(kb.y, kb.y), pack2(kb.z, kb.z),
-                              pack2(kb.w, kb.w)};
-            const int dn = d0 + (dd + 1 < 64 ? dd + 1 : dd);
-            qa = *reinterpret_cast<const ulonglong2*>(qp + dn * PT);
-            kb = *reinterpret_cast<const float4*>(kp + dn * PT);
-#pragma unroll
-            for (int ip = 0; ip < 2; ++ip)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    acc[ip * 4 + j] = fadd2_ftz(acc[ip * 4 + j], fmul2_rn(P[ip], D[j]));
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            if (half == 0)
-                t0[e] = acc[e];
-            else
-                s[e] = fadd2_ftz(t0[e], acc[e]);
-        }
-    }
-    const u64 cc = pack2(c, c);
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-        s[e] = fadd2_ftz(fmul2_rn(s[e], cc), pack2(-0.0f, -0.0f));   // (x) c, flushed
+    u64 t0[8], t1[8];
+    logit_chunk(t0, Qt, Kt, ty, tx, 0);
+    logit_chunk(t1, Qt, Kt, ty, tx, 64);
+    logit_finish(s, t0, t1, c);
 }
 
 // logit (row 4ty + 2ip + h, column 4tx + j) is lane h of s[ip*4 + j]
@@ -280,14 +356,42 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
     }
 
     // ---------------------------------------------------------- pass 1: maxima
+    // the key tiles alternate between Kt and K2 (pass 2's scratch, idle until
+    // then); tile t + 1 is fetched while tile t's logits are formed, so each
+    // tile needs one barrier
+    float* K2 = Ps;
+    {
+        float4 v[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            tile_fetch(v, kbase, t_lo * AT, T, kstride, tid, half);
+            tile_put(Kt, v, tid, half);
+        }
+    }
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     for (int64_t t = t_lo; t <= t_hi; ++t) {
         const int64_t j0 = t * AT;
-        __syncthreads();   // previous tile's readers are done with Kt
-        load_tile_t(Kt, kbase, j0, T, kstride, tid);
-        __syncthreads();
+        const bool odd = ((t - t_lo) & 1) != 0;
+        const float* Kc = odd ? K2 : Kt;
+        float* Kn = odd ? Kt : K2;
+        const bool more = t < t_hi;
+        __syncthreads();   // tile t is in Kc, and every reader of Kn (tile t - 1) is done
         u64 s[8];
-        logits4x4(s, Qt, Kt, ty, tx, a.c);
+        {
+            u64 t0[8], t1[8];
+            float4 v[4];
+            if (more)
+                tile_fetch(v, kbase, j0 + AT, T, kstride, tid, 0);
+            logit_chunk(t0, Qt, Kc, ty, tx, 0);
+            if (more) {
+                tile_put(Kn, v, tid, 0);
+                tile_fetch(v, kbase, j0 + AT, T, kstride, tid, 1);
+            }
+            logit_chunk(t1, Qt, Kc, ty, tx, 64);
+            if (more)
+                tile_put(Kn, v, tid, 1);
+            logit_finish(s, t0, t1, a.c);
+        }
         if (cache) {
             ulonglong2* dst = reinterpret_cast<ulonglong2*>(cache + (t - t_lo) * (AT * AT) + tid * 16);
 #pragma unroll
@@ -601,6 +705,645 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
             a.l[(b * T + i) * a.Hq + h] = lrow[rr];
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Default forward route (logit cache and tensor-core P.V), two kernels.
+//
+// k_attn_logits: pass 1 -- every logit of the window written to the cache and
+// the exact row maxima written to m -- as a banded product in the canonical
+// order over d.  A CTA holds two groups of 128 threads; each group takes its
+// own query tiles (64 rows, one head, one sequence) in turn.  A thread owns 8
+// rows x 4 keys of a 64 x 64 tile (rows as packed pairs: the tile of the
+// linear backward, bwd_tile.cuh), so it loads 12 floats per 32 outputs per d.
+// The group's Q^T tile is staged once per query tile; the K^T tiles of all its
+// query tiles stream through a two-stage ring filled by bulk copies from an
+// image of K (k_attn_kimg: per (sequence, kv head, 64-key tile) the flushed
+// K^T[d][key], 32 KB) and released per warp on an mbarrier, so no group-wide
+// barrier is taken per key tile.  The logits land in the cache in the same
+// layout as the other forward route's (4 x 4 blocks of 16 floats), which the
+// second pass and the backward read.
+//
+// k_attn_pv: pass 2 -- p, the int8 codes, the row sums and P.V -- one CTA of
+// 256 threads per query tile, two CTAs per SM.  The P and V^T tiles and the p
+// tile are double-buffered, so tile t + 1 is written while the MMA of tile t
+// runs and the row sums of tile t are read; V^T comes from the image of the V
+// codes (k_attn_vimg) by one bulk copy per tile.
+constexpr int LG_NT = 256;                       // threads per CTA: two groups
+constexpr int LG_G = 128;                        // threads per group
+constexpr uint32_t KIMG_TILE = HD * AT * 4;      // bytes of one K^T tile
+constexpr int LG_Q_BYTES = HD * PT * 4;          // Q^T [d][64 rows], pitch PT
+constexpr int LG_GROUP_BYTES = LG_Q_BYTES + 2 * (int)KIMG_TILE;
+constexpr size_t LG_SMEM = 2 * (size_t)LG_GROUP_BYTES;
+constexpr uint32_t VIMG_TILE = 128 * 64 * 2;     // bytes of one V^T tile
+static_assert(LG_GROUP_BYTES % 128 == 0, "group layout alignment");
+
+// K^T image: tile (b, g, t) holds the flushed K[b, 64 t + key, g, d] at
+// [d][key] (keys at or past T are 0).  One thread moves one float4 of d.
+// Also zeroes the work counter of k_attn_logits
+__global__ void k_attn_kimg(const float* __restrict__ k, float* __restrict__ img, int64_t T,
+                            int64_t Hkv, int64_t nkt, int64_t n, unsigned long long* counter)
+{
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *counter = 0;   // the logits kernel's work counter, for the launch after this one
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int key = (int)(e & (AT - 1));
+        const int d4 = (int)((e >> 6) & (HD / 4 - 1));
+        const int64_t tile = e >> 11;
+        const int64_t t = tile % nkt, bg = tile / nkt;
+        const int64_t bb = bg / Hkv, gg = bg % Hkv;
+        const int64_t j = t * AT + key;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < T)
+            v = flush4(*reinterpret_cast<const float4*>(k + ((bb * T + j) * Hkv + gg) * HD + 4 * d4));
+        float* dst = img + tile * (HD * AT) + (4 * d4) * AT + key;
+        dst[0] = v.x;
+        dst[AT] = v.y;
+        dst[2 * AT] = v.z;
+        dst[3 * AT] = v.w;
+    }
+}
+
+struct AttnLogitArgs {
+    const float* q;
+    const float* kimg;
+    float* cache;
+    float* m;
+    unsigned long long* counter;   // query tiles handed out (zero at launch)
+    int64_t T, Hq, Hkv, W, tiles_bh, nqt, nkt, items;
+    float c;
+    int* err;
+};
+
+// the k-th query tile handed out: the last query tiles of every (sequence,
+// head) first, so the longest windows start first and the shortest fill the end
+__device__ __forceinline__ int64_t item_of(const AttnLogitArgs& a, int64_t k)
+{
+    const int64_t bhs = a.items / a.nqt;
+    const int64_t qt = a.nqt - 1 - k / bhs, bh = k % bhs;
+    return bh * a.nqt + qt;
+}
+
+// one query tile's place: sequence, head, kv head, first row, key tiles
+struct QTile {
+    int64_t b, h, g;
+    int i0, t_lo, t_hi;
+};
+
+__device__ __forceinline__ QTile qtile_of(const AttnLogitArgs& a, int64_t item)
+{
+    QTile r;
+    const int qt = (int)(item % a.nqt);
+    const int64_t bh = item / a.nqt;
+    r.h = bh % a.Hq;
+    r.b = bh / a.Hq;
+    r.g = r.h / (a.Hq / a.Hkv);
+    r.i0 = qt * AT;
+    const int T = (int)a.T, W = (int)a.W;
+    const int jlo = W > 0 ? max(0, r.i0 - W + 1) : 0;
+    r.t_lo = jlo / AT;
+    r.t_hi = min(r.i0 + AT - 1, T - 1) / AT;
+    return r;
+}
+
+// one 64-term chunk of the thread's 8 x 4 sums, operands loaded one step ahead
+__device__ __forceinline__ void logit_chunk84(u64 (&acc)[16], const float* __restrict__ Ar,
+                                              const float* __restrict__ Br)
+{
+    ulonglong2 a03 = *reinterpret_cast<const ulonglong2*>(Ar);
+    ulonglong2 a47 = *reinterpret_cast<const ulonglong2*>(Ar + 4);
+    float4 b = *reinterpret_cast<const float4*>(Br);
+    {
+        const ulonglong2 c03 = a03, c47 = a47;
+        const float4 cb = b;
+        a03 = *reinterpret_cast<const ulonglong2*>(Ar + PT);
+        a47 = *reinterpret_cast<const ulonglong2*>(Ar + PT + 4);
+        b = *reinterpret_cast<const float4*>(Br + AT);
+        step<true>(acc, c03, c47, cb);
+    }
+#pragma unroll 9
+    for (int d = 1; d < 64; ++d) {
+        const ulonglong2 c03 = a03, c47 = a47;
+        const float4 cb = b;
+        const int dn = d + 1 < 64 ? d + 1 : d;
+        a03 = *reinterpret_cast<const ulonglong2*>(Ar + dn * PT);
+        a47 = *reinterpret_cast<const ulonglong2*>(Ar + dn * PT + 4);
+        b = *reinterpret_cast<const float4*>(Br + dn * AT);
+        step<false>(acc, c03, c47, cb);
+    }
+}
+
+__global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
+{
+    extern __shared__ __align__(128) uint8_t sml[];
+    __shared__ uint64_t full[2][2], empty[2][2];
+    __shared__ int64_t queue[2][4];   // per group: the query tiles handed to it, in order (-1: none left)
+    const int tid = threadIdx.x, gp = tid >> 7, lt = tid & (LG_G - 1);
+    const int lane = tid & 31;
+    const int ty = lt >> 4, tx = lt & 15;      // rows 8ty .. 8ty+7, keys 4tx .. 4tx+3
+    const int gbar = 1 + gp;
+    uint8_t* gbase = sml + (size_t)gp * LG_GROUP_BYTES;
+    float* Qt = reinterpret_cast<float*>(gbase);                   // [HD][PT]
+    float* Kr = reinterpret_cast<float*>(gbase + LG_Q_BYTES);      // [2][HD][AT]
+    if (tid == 0) {
+        for (int x = 0; x < 2; ++x)
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(&full[x][s], 1);
+                mbar_init(&empty[x][s], LG_G / 32);   // one arrival per warp
+            }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const int T = (int)a.T, W = (int)a.W;
+    const int64_t qstride = a.Hq * HD;
+
+    // issuer (group thread 0): takes the group's query tiles from the counter
+    // as it reaches them and walks their key tiles; it runs at most two key
+    // tiles ahead of the group, so at most three queue entries are live
+    int iss_k = 0, iss_t = 0;
+    bool have = false;
+    uint32_t issued = 0;
+    QTile iss_q;
+    auto take = [&](int kslot) {
+        const int64_t k = (int64_t)atomicAdd(a.counter, 1ull);
+        const int64_t item = k < a.items ? item_of(a, k) : -1;
+        queue[gp][kslot & 3] = item;
+        have = item >= 0;
+        if (have) {
+            iss_q = qtile_of(a, item);
+            iss_t = iss_q.t_lo;
+        }
+    };
+    auto issue_next = [&]() {
+        if (!have)
+            return;
+        const int s = issued & 1;
+        mbar_expect_tx(&full[gp][s], KIMG_TILE);
+        bulk_load(Kr + s * (HD * AT), a.kimg + ((iss_q.b * a.Hkv + iss_q.g) * a.nkt + iss_t) * (HD * AT),
+                  KIMG_TILE, &full[gp][s]);
+        ++issued;
+        if (++iss_t > iss_q.t_hi)
+            take(++iss_k);
+    };
+    if (lt == 0) {
+        take(0);
+        issue_next();
+        issue_next();
+    }
+
+    uint32_t used = 0;      // key tiles consumed by the group
+    bool fail = false, dead = false;
+    for (int kk = 0;; ++kk) {
+        // a failed wait anywhere in the group stops it at the next query tile;
+        // the barrier also frees Qt and publishes the issuer's queue entry
+        {
+            uint32_t r;
+            asm volatile(
+                "{\n\t.reg .pred q, o;\n\t"
+                "setp.ne.u32 q, %1, 0;\n\t"
+                "bar.red.or.pred o, %2, %3, q;\n\t"
+                "selp.u32 %0, 1, 0, o;\n\t}"
+                : "=r"(r)
+                : "r"((uint32_t)(fail || dead)), "r"(gbar), "n"(LG_G)
+                : "memory");
+            dead = r != 0;
+        }
+        const int64_t item = queue[gp][kk & 3];
+        if (dead || item < 0)
+            break;
+        const QTile qt = qtile_of(a, item);
+        // Q^T of this query tile, flushed: 64 rows x 32 float4, 16 per thread
+        {
+            const float* qbase = a.q + (qt.b * a.T * a.Hq + qt.h) * HD;
+#pragma unroll
+            for (int it = 0; it < (AT * HD / 4) / LG_G; ++it) {
+                const int e = lt + it * LG_G;
+                const int l8 = e & 31, w = e >> 5;     // 8 rows x 4 float4 per warp step
+                const int r = (w & 7) * 8 + (l8 & 7);
+                const int c4 = (w >> 3) * 4 + (l8 >> 3);
+                const int64_t row = qt.i0 + r;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (row < T)
+                    v = flush4(*reinterpret_cast<const float4*>(qbase + row * qstride + 4 * c4));
+                Qt[(4 * c4 + 0) * PT + r] = v.x;
+                Qt[(4 * c4 + 1) * PT + r] = v.y;
+                Qt[(4 * c4 + 2) * PT + r] = v.z;
+                Qt[(4 * c4 + 3) * PT + r] = v.w;
+            }
+        }
+        asm volatile("bar.sync %0, %1;" ::"r"(gbar), "n"(LG_G) : "memory");
+        float* cache = a.cache + ((qt.b * a.Hq + qt.h) * a.tiles_bh + tile_prefix(qt.i0 / AT, W)) * (AT * AT);
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            mx[e] = -INFINITY;
+        for (int t = qt.t_lo; t <= qt.t_hi; ++t) {
+            const int s = used & 1;
+            // the stage of the previous tile takes the tile after this one,
+            // once every warp has released it
+            if (lt == 0 && used >= 1 && issued == used + 1 && have) {
+                if (mbar_wait(&empty[gp][s ^ 1], ((used - 1) >> 1) & 1))
+                    issue_next();
+                else
+                    fail = true;
+            }
+            if (!mbar_wait(&full[gp][s], (used >> 1) & 1))
+                fail = true;
+            const float* Kc = Kr + s * (HD * AT);
+            u64 t0[16], t1[16];
+            logit_chunk84(t0, Qt + 8 * ty, Kc + 4 * tx);
+            logit_chunk84(t1, Qt + 64 * PT + 8 * ty, Kc + 64 * AT + 4 * tx);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[gp][s]);
+            ++used;
+            const u64 cc = pack2(a.c, a.c);
+            u64 sv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)   // (t0 + t1) (x) c, flushed
+                sv[e] = fadd2_ftz(fmul2_rn(fadd2_ftz(t0[e], t1[e]), cc), pack2(-0.0f, -0.0f));
+            {
+                // rows 8ty .. 8ty+3 are 4 x 4 block (2ty, tx) of the cached tile,
+                // rows 8ty+4 .. 8ty+7 block (2ty + 1, tx)
+                float* tile = cache + (int64_t)(t - qt.t_lo) * (AT * AT);
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    ulonglong2* dst = reinterpret_cast<ulonglong2*>(tile + ((2 * ty + blk) * 16 + tx) * 16);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        dst[e] = make_ulonglong2(sv[8 * blk + 2 * e], sv[8 * blk + 2 * e + 1]);
+                }
+            }
+            const int j0 = t * AT;
+            const bool inner = qt.i0 + AT - 1 < T && j0 + AT - 1 <= qt.i0 && (W == 0 || j0 >= qt.i0 + AT - W);
+#pragma unroll
+            for (int ip = 0; ip < 4; ++ip)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float lo, hi;
+                    unpack2(sv[ip * 4 + j], lo, hi);
+                    if (inner) {
+                        mx[2 * ip] = fmaxf(mx[2 * ip], lo);
+                        mx[2 * ip + 1] = fmaxf(mx[2 * ip + 1], hi);
+                    } else {
+                        const int jj = j0 + 4 * tx + j;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int i = qt.i0 + 8 * ty + 2 * ip + h;
+                            const int lo_i = W > 0 ? max(0, i - W + 1) : 0;
+                            if (i < T && jj >= lo_i && jj <= i)
+                                mx[2 * ip + h] = fmaxf(mx[2 * ip + h], h ? hi : lo);
+                        }
+                    }
+                }
+        }
+        // the rows' maxima over the 16 threads of each row group
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1)
+                mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], off));
+            if (mx[e] == 0.0f)
+                mx[e] = 0.0f;   // a zero maximum is +0
+        }
+        if (tx == 0)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int64_t i = qt.i0 + 8 * ty + e;
+                if (i < T)
+                    a.m[(qt.b * a.T + i) * a.Hq + qt.h] = mx[e];
+            }
+    }
+    // copies still in flight (only after a failed wait, or tiles issued ahead)
+    if (lt == 0)
+        while (used < issued && mbar_wait(&full[gp][used & 1], (used >> 1) & 1))
+            ++used;
+    if (fail)
+        atomicExch(a.err, 1);
+}
+
+// the V codes as the P.V's B operand: tile (b, g, t) holds V^T[d][key] for
+// the 64 keys of key tile t (keys at or past T are 0), bf16, in the 128-byte-
+// swizzled K-major layout of umma.cuh.  One thread writes one 16-byte chunk
+// (8 keys of one d)
+__global__ void k_attn_vimg(const int8_t* __restrict__ vq, uint8_t* __restrict__ img, int64_t T,
+                            int64_t Hkv, int64_t nkt, int64_t n_chunks)
+{
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_chunks;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int c8 = (int)(e & 7);
+        const int d = (int)((e >> 3) & (HD - 1));
+        const int64_t tile = e >> 10;
+        const int64_t t = tile % nkt, bg = tile / nkt;
+        const int64_t bb = bg / Hkv, gg = bg % Hkv;
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            int v2[2];
+#pragma unroll
+            for (int z = 0; z < 2; ++z) {
+                const int64_t j = t * AT + 8 * c8 + 2 * u + z;
+                v2[z] = j < T ? (int)vq[((bb * T + j) * Hkv + gg) * HD + d] : 0;
+            }
+            w[u] = bf16_bits(v2[0]) | (bf16_bits(v2[1]) << 16);
+        }
+        *reinterpret_cast<uint4*>(img + tile * VIMG_TILE + sw128_off(d, 8 * c8)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+constexpr int PV_TC_BYTES = 2 * (2 * TC_TILE_BYTES) + 1024;   // two (P, V^T) buffers + alignment
+constexpr int PV_PS_BYTES = 2 * AT * PS * 4;                  // two p tiles
+constexpr int PV_STK_BYTES = AT * (MAXL + 1) * 4;
+constexpr size_t PV_SMEM = (size_t)PV_TC_BYTES + PV_PS_BYTES + PV_STK_BYTES + 2 * AT * 4;
+
+struct AttnPVArgs {
+    AttnFwdArgs f;
+    const uint8_t* vimg;
+    int64_t nkt;
+};
+
+__global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
+{
+    extern __shared__ __align__(16) uint8_t smv[];
+    __shared__ uint64_t mma_bar[2], v_bar[2];
+    __shared__ uint32_t tmem_slot;
+    const AttnFwdArgs& a = pa.f;
+
+    const int lt = threadIdx.x;
+    const int ty = lt >> 4, tx = lt & 15;
+    // buffer x: P at tcb0 + 2 x TC_TILE_BYTES, V^T TC_TILE_BYTES after it
+    uint8_t* tcb0 = smv + ((1024u - (su32(smv) & 1023u)) & 1023u);
+    auto tcbuf = [&](int x) { return tcb0 + x * (2 * TC_TILE_BYTES); };
+    float* Psb = reinterpret_cast<float*>(smv + PV_TC_BYTES);   // [2][AT][PS]
+    float* stk = Psb + 2 * AT * PS;                             // [AT][MAXL+1]
+    float* mrow = stk + AT * (MAXL + 1);
+    float* lrow = mrow + AT;
+
+    const int T = (int)a.T, W = (int)a.W;
+    const int64_t b = blockIdx.z, h = blockIdx.y;
+    const int i0 = (int)blockIdx.x * AT;
+    const int64_t g = h / (a.Hq / a.Hkv);
+    const int jlo = W > 0 ? max(0, i0 - W + 1) : 0;
+    const int jhi = min(i0 + AT - 1, T - 1);
+    const int t_lo = jlo / AT, t_hi = jhi / AT;
+    float* cache = a.cache + ((b * a.Hq + h) * a.tiles_bh + tile_prefix((int64_t)blockIdx.x, W)) * (AT * AT);
+    const uint8_t* vsrc = pa.vimg + (b * a.Hkv + g) * pa.nkt * VIMG_TILE;
+
+    // one thread of the last warp issues the copies and the MMAs (the row
+    // sums run on the first two warps)
+    constexpr int ISSUER = NT - 32;
+    if (lt == 0) {
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&mma_bar[x], 1);
+            mbar_init(&v_bar[x], 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (lt < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
+                         su32(&tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (lt < AT) {
+        const int i = i0 + lt;
+        mrow[lt] = i < T ? a.m[(b * a.T + i) * a.Hq + h] : 0.0f;
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = tmem_slot;
+    uint32_t vn[2] = {0, 0}, vw[2] = {0, 0};   // V^T copies issued / seen complete, per buffer
+    if (lt == ISSUER) {   // V^T of the first tile
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_expect_tx(&v_bar[0], VIMG_TILE);
+        bulk_load(tcbuf(0) + TC_TILE_BYTES, vsrc + (int64_t)t_lo * VIMG_TILE, VIMG_TILE, &v_bar[0]);
+        vn[0] = 1;
+    }
+
+    // P.V outputs of this thread: query row tc_row, d 32 tc_cb .. + 31
+    const int wq = (lt >> 5) & 3;
+    const int tc_row = 32 * (wq & 1) + (lt & 31);
+    const int tc_cb = 2 * (wq >> 1) + (lt >> 7);
+    bool fail = false, dead = false;
+
+    const int my_i = i0 + lt;
+    const int my_lo = W > 0 ? max(0, my_i - W + 1) : 0;
+    const int my_n = my_i - my_lo + 1;
+    int pos = 0;
+    float cs = 0.f, lsum = 0.f;
+    int acc[4][8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            acc[r][u] = 0;
+    ulonglong2 sv4[4];
+    {
+        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(cache + lt * 16);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sv4[e] = src[e];
+    }
+    for (int t = t_lo; t <= t_hi; ++t) {
+        const int j0 = t * AT;
+        const int it = t - t_lo;
+        const int bf = it & 1;
+        const bool more = t < t_hi;
+        u64 s[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            s[2 * e] = sv4[e].x;
+            s[2 * e + 1] = sv4[e].y;
+        }
+        float pv[16];   // this thread's p, in the cache's layout (pair e, lane h at 2e + h)
+        uint32_t words[4] = {0, 0, 0, 0};
+        // every (query, key) pair of the tile valid: no per-pair test
+        const bool inner = i0 + AT - 1 < T && j0 + AT - 1 <= i0 && (W == 0 || j0 >= i0 + AT - W);
+#pragma unroll
+        for (int ip = 0; ip < 2; ++ip) {
+            const int r = 4 * ty + 2 * ip;   // rows r, r + 1 are the lanes of s[ip*4 + j]
+            const u64 nm = pack2(-mrow[r], -mrow[r + 1]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float p[2];
+                unpack2(exp_r2(fadd2_ftz(s[ip * 4 + j], nm)), p[0], p[1]);
+                if (!inner) {
+                    const int jj = j0 + 4 * tx + j;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int i = i0 + r + hh;
+                        const int lo = W > 0 ? max(0, i - W + 1) : 0;
+                        if (!(i < T && jj >= lo && jj <= i))
+                            p[hh] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    pv[2 * (ip * 4 + j) + hh] = p[hh];
+                    words[2 * ip + hh] |= (uint32_t)quant_p(p[hh]) << (8 * j);
+                }
+            }
+        }
+        if (more) {   // the next tile's logits, in flight until the next tile starts
+            const ulonglong2* src =
+                reinterpret_cast<const ulonglong2*>(cache + (int64_t)(t + 1 - t_lo) * (AT * AT) + lt * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sv4[e] = src[e];
+        }
+        // the P tile of this buffer was read by the MMA two tiles back
+        if (!dead && it >= 2 && !mbar_wait(&mma_bar[bf], ((it - 2) >> 1) & 1))
+            fail = true;
+        float* Ps = Psb + bf * (AT * PS);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int r = 4 * ty + rr;
+            const uint32_t word = words[rr];
+            // the four codes as bf16 at keys 4tx .. 4tx+3 of rows r and r + 64
+            const uint2 bw = make_uint2(
+                bf16_bits((int)(word & 0xff)) | (bf16_bits((int)((word >> 8) & 0xff)) << 16),
+                bf16_bits((int)((word >> 16) & 0xff)) | (bf16_bits((int)(word >> 24)) << 16));
+            *reinterpret_cast<uint2*>(tcbuf(bf) + sw128_off(r, 4 * tx)) = bw;
+            *reinterpret_cast<uint2*>(tcbuf(bf) + sw128_off(r + 64, 4 * tx)) = bw;
+            const int ip = rr >> 1, hh = rr & 1;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                Ps[r * PS + 4 * tx + j] = pv[2 * (ip * 4 + j) + hh];
+        }
+        {
+            // the cache now holds p in place of each logit: the backward
+            // reads p from it instead of evaluating e^x again
+            float4* dst = reinterpret_cast<float4*>(cache + (int64_t)it * (AT * AT) + lt * 16);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                dst[e] = make_float4(pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3]);
+        }
+        // the P tile's generic-proxy stores become visible to the tensor core
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        dead = __syncthreads_or(fail || dead) != 0;
+        if (lt == ISSUER && !dead) {
+            if (!mbar_wait(&v_bar[bf], (it >> 1) & 1)) {
+                fail = true;
+            } else {
+                ++vw[bf];
+                fence_after();
+                const uint64_t ad = sdesc(su32(tcbuf(bf))), bd = sdesc(su32(tcbuf(bf) + TC_TILE_BYTES));
+#pragma unroll
+                for (int k = 0; k < AT / 16; ++k)
+                    mma_bf16<HD>(tmem, ad + 2 * k, bd + 2 * k,
+                                 (it % TC_SLICE_TILES != 0 || k != 0) ? 1u : 0u);
+                mma_commit(&mma_bar[bf]);
+                if (more) {
+                    // V^T of the next tile into the other buffer, once the
+                    // MMA of the previous tile has read it
+                    const int nb = bf ^ 1;
+                    if (it >= 1 && !mbar_wait(&mma_bar[nb], ((it - 1) >> 1) & 1)) {
+                        fail = true;
+                    } else {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        mbar_expect_tx(&v_bar[nb], VIMG_TILE);
+                        bulk_load(tcbuf(nb) + TC_TILE_BYTES, vsrc + (int64_t)(t + 1) * VIMG_TILE, VIMG_TILE,
+                                  &v_bar[nb]);
+                        ++vn[nb];
+                    }
+                }
+            }
+        }
+        // row sums: the valid p of this tile, left to right, through the
+        // chunk-of-64 / pairwise-tree stack
+        if (lt < AT && my_i < T) {
+            const int cb = max(my_lo, j0), ce = min(my_i, j0 + AT - 1);
+            const float* prow = Ps + lt * PS;   // column jj - j0
+            int jj = cb;
+            while (jj <= ce) {
+                // one run up to the next chunk boundary: left to right, seeded
+                // with the chunk's first term
+                const int room = 64 - (pos & 63);
+                const int len = min(room, ce - jj + 1);
+                int k = 0;
+                const float* pr = prow + (jj - j0);
+                if ((pos & 63) == 0) {
+                    cs = pr[0];
+                    k = 1;
+                }
+#pragma unroll 8
+                for (; k < len; ++k)
+                    cs = fadd_ftz(cs, pr[k]);
+                jj += len;
+                pos += len;
+                if ((pos & 63) == 0 || pos == my_n) {
+                    const int c = (pos - 1) >> 6;
+                    float acc_t = cs;
+                    if (pos == my_n) {
+                        for (int lvl = 0; lvl < MAXL; ++lvl)
+                            if ((c >> lvl) & 1)
+                                acc_t = fadd_ftz(stk[lt * (MAXL + 1) + lvl], acc_t);
+                        lsum = acc_t;
+                    } else {
+                        const int tz = __ffs(~c) - 1;
+                        for (int lvl = 0; lvl < tz; ++lvl)
+                            acc_t = fadd_ftz(stk[lt * (MAXL + 1) + lvl], acc_t);
+                        stk[lt * (MAXL + 1) + tz] = acc_t;
+                    }
+                }
+            }
+        }
+        // end of an exact slice: add the accumulator to the int32 sums
+        if (!dead && (it % TC_SLICE_TILES == TC_SLICE_TILES - 1 || !more)) {
+            const bool got = __all_sync(0xffffffffu, mbar_wait(&mma_bar[bf], (it >> 1) & 1));
+            if (got) {
+                fence_after();
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * wq) << 16) + (uint32_t)(32 * tc_cb), v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    acc[e >> 3][e & 7] += __float2int_rn(__uint_as_float(v[e]));
+                fence_before();
+            } else {
+                fail = true;
+            }
+        }
+    }
+    if (lt < AT)
+        lrow[lt] = lsum;
+    __syncthreads();
+
+    const float sv = flush(*a.s_v);
+    const int64_t i = i0 + tc_row;
+    if (i < (int64_t)T) {
+        const float den = fmul_flush(lrow[tc_row], 127.0f);
+        float* dst = a.o + ((b * a.T + i) * a.Hq + h) * HD + 32 * tc_cb;
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+            float ov[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = 4 * c4 + u;
+                ov[u] = flush(__fdiv_rn(fmul_flush(__int2float_rn(acc[c >> 3][c & 7]), sv), den));
+            }
+            *reinterpret_cast<float4*>(dst + 4 * c4) = make_float4(ov[0], ov[1], ov[2], ov[3]);
+        }
+        if (tc_cb == 0)
+            a.l[(b * a.T + i) * a.Hq + h] = lrow[tc_row];
+    }
+
+    // after a failed wait, copies still in flight land before the CTA exits
+    if (lt == ISSUER)
+        for (int x = 0; x < 2; ++x)
+            while (vw[x] < vn[x] && mbar_wait(&v_bar[x], vw[x] & 1))
+                ++vw[x];
+    fence_before();
+    __syncthreads();
+    if (lt < 32) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+    }
+    if (fail)
+        atomicExch(a.err, 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -1319,10 +2062,18 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
     return cudaGetLastError();
 }
 
-size_t attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W)
+// the logit cache, then the V^T and K^T images of the tensor-core route
+// (sized for Hkv = Hq, its upper bound) and the logits kernel's work counter
+static size_t attn_cache_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W)
 {
     const int64_t nqt = (T + AT - 1) / AT;
     return (size_t)(B * Hq * tile_prefix(nqt, W) * (AT * AT) * 4);
+}
+
+size_t attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W)
+{
+    const int64_t nqt = (T + AT - 1) / AT;
+    return attn_cache_bytes(B, T, Hq, W) + (size_t)(B * Hq * nqt) * (VIMG_TILE + KIMG_TILE) + 16;
 }
 
 cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
@@ -1347,9 +2098,63 @@ cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, co
     a.err = device_error_word();
     if (!a.err)
         return cudaErrorInvalidValue;
-    // the tensor-core P.V keeps its tiles where pass 1's key tile was, so it
-    // needs pass 2 to read the logits from the cache
-    auto kern = (tc && cache) ? k_attn_fwd<true> : k_attn_fwd<false>;
+    if (tc && cache) {
+        // the K^T and V^T images after the cache, then the two passes
+        const int64_t nqt = (T + AT - 1) / AT;
+        uint8_t* vimg = static_cast<uint8_t*>(cache) + attn_cache_bytes(B, T, Hq, W);
+        float* kimg = reinterpret_cast<float*>(vimg + (size_t)(B * Hq * nqt) * VIMG_TILE);
+        auto* counter = reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(kimg) +
+                                                              (size_t)(B * Hq * nqt) * KIMG_TILE);
+        a.m = m;
+        if (a.W > T)
+            a.W = T;   // the same windows and cache layout; keeps W in 32 bits
+        const int64_t vchunks = B * Hkv * nqt * 1024, kn = B * Hkv * nqt * (AT * HD / 4);
+        const int64_t cap = (int64_t)num_sms() * 8;
+        k_attn_vimg<<<(int)std::min<int64_t>((vchunks + 255) / 256, cap), 256, 0, st>>>(vq, vimg, T, Hkv,
+                                                                                      nqt, vchunks);
+        k_attn_kimg<<<(int)std::min<int64_t>((kn + 255) / 256, cap), 256, 0, st>>>(k, kimg, T, Hkv, nqt,
+                                                                                  kn, counter);
+        count_launches(2);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+        AttnLogitArgs la;
+        la.q = q;
+        la.kimg = kimg;
+        la.cache = a.cache;
+        la.m = m;
+        la.counter = counter;
+        la.T = T;
+        la.Hq = Hq;
+        la.Hkv = Hkv;
+        la.W = a.W;
+        la.tiles_bh = a.tiles_bh;
+        la.nqt = nqt;
+        la.nkt = nqt;
+        la.items = B * Hq * nqt;
+        la.c = a.c;
+        la.err = a.err;
+        e = cudaFuncSetAttribute(k_attn_logits, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LG_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        const unsigned lgrid = (unsigned)std::min<int64_t>(num_sms(), (la.items + 1) / 2);
+        k_attn_logits<<<lgrid, LG_NT, LG_SMEM, st>>>(la);
+        count_launches(1);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+        AttnPVArgs pa;
+        pa.f = a;
+        pa.vimg = vimg;
+        pa.nkt = nqt;
+        e = cudaFuncSetAttribute(k_attn_pv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PV_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        k_attn_pv<<<dim3((unsigned)nqt, (unsigned)Hq, (unsigned)B), NT, PV_SMEM, st>>>(pa);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    auto kern = k_attn_fwd<false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)FWD_SMEM);
     if (e != cudaSuccess)

@@ -295,7 +295,10 @@ def test_attn_fwd_argument_checks(L):
                         k.get("W", 0), k.get("ws", None), k.get("wsb", 0), None]
     assert f(*args(D=64)) == -2                      # head dim must be 128
     need = repro.repro_attn_fwd_ws_bytes(1, 8, 4, 0)
-    assert need == 4 * 64 * 64 * 4                   # one query tile, one key tile, 4 heads
+    # one query tile, one key tile, 4 heads: the logit cache, then the V^T and
+    # K^T images of the tensor-core route (one 128 x 64 bf16 and one 128 x 64
+    # fp32 tile per head, Hkv <= Hq)
+    assert need == 4 * 64 * 64 * 4 + 4 * 128 * 64 * 2 + 4 * 128 * 64 * 4 + 16   # + work counter
     assert f(*args(ws=A * 16, wsb=need - 1)) == -7   # logit cache too small
     assert f(*args(ws=A * 16 + 8, wsb=need)) == -3   # misaligned cache
     assert f(*args(ws=Q, wsb=need)) == -8            # cache over q
