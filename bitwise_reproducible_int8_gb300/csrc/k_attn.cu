@@ -134,9 +134,21 @@ __device__ __forceinline__ u64 exp_r2(u64 x)
     p = fadd2_ftz(fmul2_rn(p, r), pack2(0.5f, 0.5f));
     p = fadd2_ftz(fmul2_rn(p, r), pack2(1.0f, 1.0f));
     p = fadd2_ftz(fmul2_rn(p, r), pack2(1.0f, 1.0f));
+    // 2^k exactly as a normal float for -126 <= k <= 127: both lanes scale in
+    // one packed multiply; any other lane takes exp_scale's branches
+    if (k0 >= -126.0f && k0 <= 127.0f && k1 >= -126.0f && k1 <= 127.0f) {
+        const u64 sc = pack2(__int_as_float(((int)k0 + 127) << 23), __int_as_float(((int)k1 + 127) << 23));
+        return fadd2_ftz(fmul2_rn(p, sc), z);
+    }
     float p0, p1;
     unpack2(p, p0, p1);
     return pack2(exp_scale(p0, k0), exp_scale(p1, k1));
+}
+
+// the int8 code of p as a float: rint(p (x) 127) clamped to [0, 127] (quant_p)
+__device__ __forceinline__ float quant_pf(float t)
+{
+    return fminf(fmaxf(rintf(t), 0.0f), 127.0f);
 }
 
 __device__ __forceinline__ int quant_p(float p)
@@ -838,7 +850,7 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
 {
     extern __shared__ __align__(128) uint8_t sml[];
     __shared__ uint64_t full[2][2], empty[2][2];
-    __shared__ int64_t queue[2][4];   // per group: the query tiles handed to it, in order (-1: none left)
+    __shared__ int64_t queue[2][8];   // per group: the query tiles handed to it, in order (-1: none left)
     const int tid = threadIdx.x, gp = tid >> 7, lt = tid & (LG_G - 1);
     const int lane = tid & 31;
     const int ty = lt >> 4, tx = lt & 15;      // rows 8ty .. 8ty+7, keys 4tx .. 4tx+3
@@ -860,18 +872,24 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
     const int64_t qstride = a.Hq * HD;
 
     // issuer (group thread 0): takes the group's query tiles from the counter
-    // as it reaches them and walks their key tiles; it runs at most two key
-    // tiles ahead of the group, so at most three queue entries are live
+    // one ahead of the one whose key tiles it walks, so the entry of query
+    // tile k + 1 is written before the first key tile of query tile k is
+    // issued -- and is visible to every thread that has waited on that copy.
+    // It runs at most two key tiles ahead of the group: at most four entries
+    // are live
     int iss_k = 0, iss_t = 0;
     bool have = false;
     uint32_t issued = 0;
     QTile iss_q;
     auto take = [&](int kslot) {
         const int64_t k = (int64_t)atomicAdd(a.counter, 1ull);
-        const int64_t item = k < a.items ? item_of(a, k) : -1;
-        queue[gp][kslot & 3] = item;
+        queue[gp][kslot & 7] = k < a.items ? item_of(a, k) : -1;
+    };
+    auto start = [&](int kslot) {   // walk query tile kslot (already taken)
+        const int64_t item = queue[gp][kslot & 7];
         have = item >= 0;
         if (have) {
+            take(kslot + 1);
             iss_q = qtile_of(a, item);
             iss_t = iss_q.t_lo;
         }
@@ -885,10 +903,11 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
                   KIMG_TILE, &full[gp][s]);
         ++issued;
         if (++iss_t > iss_q.t_hi)
-            take(++iss_k);
+            start(++iss_k);
     };
     if (lt == 0) {
         take(0);
+        start(0);
         issue_next();
         issue_next();
     }
@@ -910,7 +929,7 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
                 : "memory");
             dead = r != 0;
         }
-        const int64_t item = queue[gp][kk & 3];
+        const int64_t item = queue[gp][kk & 7];
         if (dead || item < 0)
             break;
         const QTile qt = qtile_of(a, item);
@@ -951,6 +970,19 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
             }
             if (!mbar_wait(&full[gp][s], (used >> 1) & 1))
                 fail = true;
+            if (t == qt.t_hi) {
+                // the next query tile's Q rows into L2 while this tile is formed
+                const int64_t nitem = queue[gp][(kk + 1) & 7];
+                if (nitem >= 0) {
+                    const QTile nq = qtile_of(a, nitem);
+                    const int64_t row = nq.i0 + (lt >> 1);
+                    if (row < T) {
+                        const float* src = a.q + ((nq.b * a.T + row) * a.Hq + nq.h) * HD + (lt & 1) * 64;
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 32));
+                    }
+                }
+            }
             const float* Kc = Kr + s * (HD * AT);
             u64 t0[16], t1[16];
             logit_chunk84(t0, Qt + 8 * ty, Kc + 4 * tx);
@@ -1153,25 +1185,32 @@ __global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
         const int it = t - t_lo;
         const int bf = it & 1;
         const bool more = t < t_hi;
+        // the P tile of this buffer was read by the MMA two tiles back (issued
+        // a whole tile ago, so this wait normally returns at once)
+        if (!dead && it >= 2 && !mbar_wait(&mma_bar[bf], ((it - 2) >> 1) & 1))
+            fail = true;
         u64 s[8];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             s[2 * e] = sv4[e].x;
             s[2 * e + 1] = sv4[e].y;
         }
-        float pv[16];   // this thread's p, in the cache's layout (pair e, lane h at 2e + h)
-        uint32_t words[4] = {0, 0, 0, 0};
+        u64 pp[8];       // this thread's p as the cache's pairs: rows (r, r + 1) of key j in pp[ip*4 + j]
+        uint32_t cw[8];  // bf16 codes: row 4ty + rr, keys 4tx + 2c, +1 in cw[2 rr + c]
         // every (query, key) pair of the tile valid: no per-pair test
         const bool inner = i0 + AT - 1 < T && j0 + AT - 1 <= i0 && (W == 0 || j0 >= i0 + AT - W);
+        const u64 z = pack2(-0.0f, -0.0f), c127 = pack2(127.0f, 127.0f);
 #pragma unroll
         for (int ip = 0; ip < 2; ++ip) {
             const int r = 4 * ty + 2 * ip;   // rows r, r + 1 are the lanes of s[ip*4 + j]
             const u64 nm = pack2(-mrow[r], -mrow[r + 1]);
+            uint32_t qb[2][4];               // float bits of the codes, per lane and key
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float p[2];
-                unpack2(exp_r2(fadd2_ftz(s[ip * 4 + j], nm)), p[0], p[1]);
+                u64 e2 = exp_r2(fadd2_ftz(s[ip * 4 + j], nm));
                 if (!inner) {
+                    float p[2];
+                    unpack2(e2, p[0], p[1]);
                     const int jj = j0 + 4 * tx + j;
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
@@ -1180,12 +1219,19 @@ __global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
                         if (!(i < T && jj >= lo && jj <= i))
                             p[hh] = 0.f;
                     }
+                    e2 = pack2(p[0], p[1]);
                 }
+                pp[ip * 4 + j] = e2;
+                float t0, t1;
+                unpack2(fadd2_ftz(fmul2_rn(e2, c127), z), t0, t1);
+                qb[0][j] = __float_as_uint(quant_pf(t0));
+                qb[1][j] = __float_as_uint(quant_pf(t1));
+            }
+            // a code (0 .. 127) as bf16 is the high half of its float
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    pv[2 * (ip * 4 + j) + hh] = p[hh];
-                    words[2 * ip + hh] |= (uint32_t)quant_p(p[hh]) << (8 * j);
-                }
+            for (int hh = 0; hh < 2; ++hh) {
+                cw[2 * (2 * ip + hh)] = __byte_perm(qb[hh][0], qb[hh][1], 0x7632);
+                cw[2 * (2 * ip + hh) + 1] = __byte_perm(qb[hh][2], qb[hh][3], 0x7632);
             }
         }
         if (more) {   // the next tile's logits, in flight until the next tile starts
@@ -1195,32 +1241,26 @@ __global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
             for (int e = 0; e < 4; ++e)
                 sv4[e] = src[e];
         }
-        // the P tile of this buffer was read by the MMA two tiles back
-        if (!dead && it >= 2 && !mbar_wait(&mma_bar[bf], ((it - 2) >> 1) & 1))
-            fail = true;
         float* Ps = Psb + bf * (AT * PS);
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
             const int r = 4 * ty + rr;
-            const uint32_t word = words[rr];
-            // the four codes as bf16 at keys 4tx .. 4tx+3 of rows r and r + 64
-            const uint2 bw = make_uint2(
-                bf16_bits((int)(word & 0xff)) | (bf16_bits((int)((word >> 8) & 0xff)) << 16),
-                bf16_bits((int)((word >> 16) & 0xff)) | (bf16_bits((int)(word >> 24)) << 16));
+            // the four codes at keys 4tx .. 4tx+3 of rows r and r + 64
+            const uint2 bw = make_uint2(cw[2 * rr], cw[2 * rr + 1]);
             *reinterpret_cast<uint2*>(tcbuf(bf) + sw128_off(r, 4 * tx)) = bw;
             *reinterpret_cast<uint2*>(tcbuf(bf) + sw128_off(r + 64, 4 * tx)) = bw;
             const int ip = rr >> 1, hh = rr & 1;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                Ps[r * PS + 4 * tx + j] = pv[2 * (ip * 4 + j) + hh];
+                Ps[r * PS + 4 * tx + j] = lane_of(pp, ip, j, hh);
         }
         {
             // the cache now holds p in place of each logit: the backward
             // reads p from it instead of evaluating e^x again
-            float4* dst = reinterpret_cast<float4*>(cache + (int64_t)it * (AT * AT) + lt * 16);
+            ulonglong2* dst = reinterpret_cast<ulonglong2*>(cache + (int64_t)it * (AT * AT) + lt * 16);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                dst[e] = make_float4(pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3]);
+                dst[e] = make_ulonglong2(pp[2 * e], pp[2 * e + 1]);
         }
         // the P tile's generic-proxy stores become visible to the tensor core
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
