@@ -14,13 +14,18 @@
 // degree-7 Taylor polynomial in Horner form with RN(1/n!) coefficients, exact
 // scaling by 2^k.
 //
-// k_attn_fwd: one CTA per (64-row query tile, query head, sequence).  The row
-// maximum must be exact before any p is quantised, so the key tiles of the
-// window are visited twice: pass 1 computes the logits and the row maxima,
-// pass 2 recomputes the same logits, forms p and the int8 codes, streams the
-// row sums through the canonical-order chunk/tree stack (one thread per row)
-// and accumulates P.V with dp4a (exact int32).  Logits: 256 threads own 4 x 4
-// outputs each, packed f32x2 products over d with the chunk-of-64 order.
+// The row maximum must be exact before any p is quantised, so the forward
+// visits the key tiles of the window twice: pass 1 computes the logits and the
+// row maxima, pass 2 forms p and the int8 codes, streams the row sums through
+// the canonical-order chunk/tree stack (one thread per row) and accumulates
+// P.V exactly.  Two routes:
+//   * with the logit cache and a device whose tensor-core exactness check has
+//     passed (the default): k_attn_logits (pass 1) and k_attn_pv (pass 2, P.V
+//     on the tensor cores), described before them below;
+//   * otherwise k_attn_fwd: one CTA per (64-row query tile, query head,
+//     sequence) runs both passes; pass 2 reads the cached logits or recomputes
+//     them, and P.V runs on dp4a (exact int32).  Logits: 256 threads own 4 x 4
+//     outputs each, packed f32x2 products over d with the chunk-of-64 order.
 #include "bwd_tile.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -277,21 +282,20 @@ __device__ __forceinline__ float lane_of(const u64 (&s)[8], int ip, int j, int h
     return h ? hi : lo;
 }
 
-// P.V on the tensor cores (TC, with the logit cache): per 64-key tile the P
-// codes go to shared memory as bf16 (exact for 0..127) in the 128-byte-
-// swizzled K-major layout of umma.cuh, rows 0-63 and again as rows 64-127, and
-// the V codes transposed, V^T[d][key], likewise; one thread issues
-// tcgen05.mma kind::f16, M = 128, N = 128, K = 64 (four K = 16 steps) into a
-// 128-column fp32 accumulator in tensor memory.  Every product is an integer
-// of magnitude at most 16129 and a slice of at most 512 keys sums to less than
-// 2^23, so each slice's accumulator is exact (the premise the forward's
-// exactness self-test checks on the device); after each slice the threads
-// convert it to int32 and add it to their registers.  The duplicated rows let
-// all eight warps read the accumulator: warp w reads tensor-memory lanes
-// 32 (w % 4) .. + 31, i.e. query row 32 (w % 2) + lane, columns
-// 32 (2 ((w % 4) / 2) + w / 4) .. + 31.  The two tiles live where the key tile
-// sits during pass 1 (pass 2 reads the logits from the cache).
-constexpr int TC_SLICE_TILES = 8;          // 512 keys per exact slice
+// P.V on the tensor cores (the default forward route, k_attn_pv below): per
+// 64-key tile the P codes go to shared memory as bf16 (exact for 0..127) in
+// the 128-byte-swizzled K-major layout of umma.cuh, rows 0-63 and again as
+// rows 64-127, beside V^T[d][key] likewise; one thread issues tcgen05.mma
+// kind::f16, M = 128, N = 128, K = 64 (four K = 16 steps) into a 128-column
+// fp32 accumulator in tensor memory.  Every product is an integer of magnitude
+// at most 16129, and a row's sum over a slice is exact in fp32 while it stays
+// below 2^23: a slice of at most 8 tiles holds at most 512 valid keys of a
+// row, and so does any slice when W <= 520 (520 x 16129 < 2^23).  After each
+// slice the threads convert the accumulator to int32 and add it to their
+// registers.  The duplicated rows let all eight warps read the accumulator:
+// warp w reads tensor-memory lanes 32 (w % 4) .. + 31, i.e. query row
+// 32 (w % 2) + lane, columns 32 (2 ((w % 4) / 2) + w / 4) .. + 31.
+constexpr int TC_SLICE_TILES = 8;          // 512 keys per exact slice (W > 520)
 constexpr int TC_TILE_BYTES = 128 * 128;   // 128 rows of 64 bf16
 
 // byte offset of element (row, col) in a 128-row x 64-column bf16 tile
@@ -306,7 +310,6 @@ __device__ __forceinline__ uint32_t bf16_bits(int v)
     return __float_as_uint((float)v) >> 16;   // exact: |v| <= 127
 }
 
-template <bool TC>
 __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
 {
     extern __shared__ __align__(16) float sma[];
@@ -339,33 +342,6 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
                            : nullptr;
 
     load_tile_t(Qt, qbase, i0, T, qstride, tid);
-
-    // tensor-core P.V (TC): accumulator in tensor memory, its barrier, and the
-    // P and V^T tiles, 1024-byte aligned inside the key tile's space
-    __shared__ uint64_t mma_bar;
-    __shared__ uint32_t tmem_slot;
-    uint8_t* tcA = nullptr;
-    uint8_t* tcB = nullptr;
-    uint32_t tmem = 0;
-    if constexpr (TC) {
-        uint8_t* kb = reinterpret_cast<uint8_t*>(Kt);
-        tcA = kb + ((1024u - (su32(kb) & 1023u)) & 1023u);
-        tcB = tcA + TC_TILE_BYTES;
-        if (tid == 0) {
-            mbar_init(&mma_bar, 1);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        }
-        if (tid < 32) {
-            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
-                             su32(&tmem_slot))
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        }
-        fence_before();
-        __syncthreads();
-        fence_after();
-        tmem = tmem_slot;
-    }
 
     // ---------------------------------------------------------- pass 1: maxima
     // the key tiles alternate between Kt and K2 (pass 2's scratch, idle until
@@ -446,14 +422,8 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
     int64_t pos = 0;
     float cs = 0.f, lsum = 0.f;
 
-    // P.V outputs of this thread.  dp4a: rows 4ri..4ri+3, d 8di..8di+7, acc[r][u];
-    // TC: row 32 (w % 2) + lane, d 32 cb .. + 31 with cb = 2 ((w % 4) / 2) + w / 4,
-    // acc[c / 8][c % 8] for column 32 cb + c (see above)
+    // P.V outputs of this thread: rows 4ri..4ri+3, d 8di..8di+7, acc[r][u]
     const int ri = tid >> 4, di = tid & 15;
-    const int wq = (tid >> 5) & 3;
-    const int tc_row = 32 * (wq & 1) + (tid & 31);
-    const int tc_cb = 2 * (wq >> 1) + (tid >> 7);
-    bool fail_local = false, tc_dead = false;
     int acc[4][8];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
@@ -463,45 +433,12 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
 
     for (int64_t t = t_lo; t <= t_hi; ++t) {
         const int64_t j0 = t * AT;
-        const int it = (int)(t - t_lo);
-        if constexpr (TC) {
-            // Kt-space tiles, Ps free; a failed wait anywhere stops the MMAs
-            tc_dead = tc_dead || __syncthreads_or(fail_local) != 0;
-            // the previous tile's MMAs read P and V^T: let them finish first
-            if (!tc_dead && it > 0 && !mbar_wait(&mma_bar, (it - 1) & 1))
-                fail_local = true;
-            // V^T[d][key] as bf16, keys in pairs (one 4-byte store per d).  In
-            // the swizzled layout the bank of a store depends on the key pair
-            // alone, so a warp's 32 lanes take the 32 key pairs of one d block:
-            // every store instruction is free of bank conflicts
-#pragma unroll
-            for (int itm = 0; itm < (AT / 2 * HD / 8) / NT; ++itm) {
-                const int e = tid + itm * NT;            // 512 items: d block (16) x key pair (32)
-                const int kp = e & 31, db = e >> 5;
-                const int64_t ja = j0 + 2 * kp, jb = ja + 1;
-                int2 va = make_int2(0, 0), vb = make_int2(0, 0);
-                if (ja < T)
-                    va = *reinterpret_cast<const int2*>(vbase + ja * kstride + 8 * db);
-                if (jb < T)
-                    vb = *reinterpret_cast<const int2*>(vbase + jb * kstride + 8 * db);
-                const int wa[2] = {va.x, va.y}, wb[2] = {vb.x, vb.y};
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int d = 8 * db + u;
-                    const int ca = (int)(int8_t)(wa[u >> 2] >> (8 * (u & 3)));
-                    const int cb = (int)(int8_t)(wb[u >> 2] >> (8 * (u & 3)));
-                    *reinterpret_cast<uint32_t*>(tcB + sw128_off(d, 2 * kp)) =
-                        bf16_bits(ca) | (bf16_bits(cb) << 16);
-                }
-            }
-        } else {
-            __syncthreads();   // Kt, Ps, Pp, Vp free
-        }
+        __syncthreads();   // Kt, Ps, Pp, Vp free
         if (!cache)
             load_tile_t(Kt, kbase, j0, T, kstride, tid);
         // V codes as packed words: Vp[jq][d] = bytes of keys 4jq .. 4jq+3 at column d
 #pragma unroll
-        for (int it = 0; !TC && it < (AT / 4 * HD / 4) / NT; ++it) {
+        for (int it = 0; it < (AT / 4 * HD / 4) / NT; ++it) {
             const int e = tid + it * NT;             // 512 items: jq (16) x d4 (32)
             const int jq = e >> 5, d4 = e & 31;
             int w[4];
@@ -555,16 +492,7 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
                         pv[2 * (ip * 4 + j) + hh] = p;
                         word |= (uint32_t)quant_p(p) << (8 * j);
                     }
-                    if constexpr (TC) {
-                        // the four codes as bf16 at keys 4tx .. 4tx+3 of rows r and r + 64
-                        const uint2 bw = make_uint2(
-                            bf16_bits((int)(word & 0xff)) | (bf16_bits((int)((word >> 8) & 0xff)) << 16),
-                            bf16_bits((int)((word >> 16) & 0xff)) | (bf16_bits((int)(word >> 24)) << 16));
-                        *reinterpret_cast<uint2*>(tcA + sw128_off(r, 4 * tx)) = bw;
-                        *reinterpret_cast<uint2*>(tcA + sw128_off(r + 64, 4 * tx)) = bw;
-                    } else {
-                        Pp[r * PP + tx] = (int)word;
-                    }
+                    Pp[r * PP + tx] = (int)word;
                 }
             if (cache) {
                 // the cache now holds p in place of each logit: the backward
@@ -575,22 +503,7 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
                     dst[e] = make_float4(pv[4 * e], pv[4 * e + 1], pv[4 * e + 2], pv[4 * e + 3]);
             }
         }
-        if constexpr (TC) {
-            // the tiles' generic-proxy stores become visible to the tensor core
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            tc_dead = tc_dead || __syncthreads_or(fail_local) != 0;
-            if (!tc_dead && tid == 0) {
-                fence_after();
-                const uint64_t ad = sdesc(su32(tcA)), bd = sdesc(su32(tcB));
-#pragma unroll
-                for (int k = 0; k < AT / 16; ++k)
-                    mma_bf16<HD>(tmem, ad + 2 * k, bd + 2 * k,
-                                 (it % TC_SLICE_TILES != 0 || k != 0) ? 1u : 0u);
-                mma_commit(&mma_bar);
-            }
-        } else {
-            __syncthreads();
-        }
+        __syncthreads();
         // row sums: the valid p of this tile, left to right, through the
         // chunk-of-64 / pairwise-tree stack
         if (tid < AT && my_i < T) {
@@ -630,26 +543,9 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
                 }
             }
         }
-        if constexpr (TC) {
-            // end of an exact slice: add the accumulator to the int32 sums
-            if (!tc_dead && (it % TC_SLICE_TILES == TC_SLICE_TILES - 1 || t == t_hi)) {
-                const bool got = __all_sync(0xffffffffu, mbar_wait(&mma_bar, it & 1));
-                if (got) {
-                    fence_after();
-                    uint32_t v[32];
-                    tmem_ld32(tmem + ((uint32_t)(32 * wq) << 16) + (uint32_t)(32 * tc_cb), v);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        acc[e >> 3][e & 7] += __float2int_rn(__uint_as_float(v[e]));
-                    fence_before();
-                } else {
-                    fail_local = true;
-                }
-            }
-        }
         // P.V, exact: 16 groups of 4 keys
 #pragma unroll 4
-        for (int jq = 0; !TC && jq < AT / 4; ++jq) {
+        for (int jq = 0; jq < AT / 4; ++jq) {
             const int4 v0 = *reinterpret_cast<const int4*>(Vp + jq * HD + 8 * di);
             const int4 v1 = *reinterpret_cast<const int4*>(Vp + jq * HD + 8 * di + 4);
             const int vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -668,36 +564,6 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
 
     // ---------------------------------------------------------------- epilogue
     const float sv = flush(*a.s_v);
-    if constexpr (TC) {
-        const int64_t i = i0 + tc_row;
-        if (i < T) {
-            const float den = fmul_flush(lrow[tc_row], 127.0f);
-            float* dst = a.o + ((b * T + i) * a.Hq + h) * HD + 32 * tc_cb;
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-                float ov[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c = 4 * c4 + u;
-                    ov[u] = flush(__fdiv_rn(fmul_flush(__int2float_rn(acc[c >> 3][c & 7]), sv), den));
-                }
-                *reinterpret_cast<float4*>(dst + 4 * c4) = make_float4(ov[0], ov[1], ov[2], ov[3]);
-            }
-            if (tc_cb == 0) {
-                a.m[(b * T + i) * a.Hq + h] = mrow[tc_row];
-                a.l[(b * T + i) * a.Hq + h] = lrow[tc_row];
-            }
-        }
-        fence_before();
-        __syncthreads();
-        if (tid < 32) {
-            fence_after();
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
-        }
-        if (fail_local)
-            atomicExch(a.err, 1);
-        return;
-    }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int rr = 4 * ri + r;
@@ -1161,6 +1027,9 @@ __global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
     const int tc_row = 32 * (wq & 1) + (lt & 31);
     const int tc_cb = 2 * (wq >> 1) + (lt >> 7);
     bool fail = false, dead = false;
+    // tiles per exact slice: a whole query tile when no row has more than 520
+    // valid keys (W <= 520), else 8
+    const int slice = (W > 0 && W <= 520) ? (1 << 30) : TC_SLICE_TILES;
 
     const int my_i = i0 + lt;
     const int my_lo = W > 0 ? max(0, my_i - W + 1) : 0;
@@ -1275,7 +1144,7 @@ __global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
 #pragma unroll
                 for (int k = 0; k < AT / 16; ++k)
                     mma_bf16<HD>(tmem, ad + 2 * k, bd + 2 * k,
-                                 (it % TC_SLICE_TILES != 0 || k != 0) ? 1u : 0u);
+                                 (it % slice != 0 || k != 0) ? 1u : 0u);
                 mma_commit(&mma_bar[bf]);
                 if (more) {
                     // V^T of the next tile into the other buffer, once the
@@ -1333,7 +1202,7 @@ __global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
             }
         }
         // end of an exact slice: add the accumulator to the int32 sums
-        if (!dead && (it % TC_SLICE_TILES == TC_SLICE_TILES - 1 || !more)) {
+        if (!dead && (it % slice == slice - 1 || !more)) {
             const bool got = __all_sync(0xffffffffu, mbar_wait(&mma_bar[bf], (it >> 1) & 1));
             if (got) {
                 fence_after();
@@ -2194,7 +2063,7 @@ cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, co
         count_launches(1);
         return cudaGetLastError();
     }
-    auto kern = k_attn_fwd<false>;
+    auto kern = k_attn_fwd;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)FWD_SMEM);
     if (e != cudaSuccess)
