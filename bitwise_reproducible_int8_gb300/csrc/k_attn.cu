@@ -956,6 +956,8 @@ constexpr int PV_TC_BYTES = 2 * (2 * TC_TILE_BYTES) + 1024;   // two (P, V^T) bu
 constexpr int PV_PS_BYTES = 2 * AT * PS * 4;                  // two p tiles
 constexpr int PV_STK_BYTES = AT * (MAXL + 1) * 4;
 constexpr size_t PV_SMEM = (size_t)PV_TC_BYTES + PV_PS_BYTES + PV_STK_BYTES + 2 * AT * 4;
+constexpr int PV_PROD = NT;             // producer threads: eight warps
+constexpr int PV_NTH = NT + 96;         // two row-sum warps and the MMA warp
 
 struct AttnPVArgs {
     AttnFwdArgs f;
@@ -963,15 +965,15 @@ struct AttnPVArgs {
     int64_t nkt;
 };
 
-__global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
+__global__ void __launch_bounds__(PV_NTH, 2) k_attn_pv(const AttnPVArgs pa)
 {
     extern __shared__ __align__(16) uint8_t smv[];
-    __shared__ uint64_t mma_bar[2], v_bar[2];
+    __shared__ uint64_t mma_bar[2], v_bar[2], ready[2], ps_free[2];
     __shared__ uint32_t tmem_slot;
+    __shared__ int dead_flag;
     const AttnFwdArgs& a = pa.f;
 
     const int lt = threadIdx.x;
-    const int ty = lt >> 4, tx = lt & 15;
     // buffer x: P at tcb0 + 2 x TC_TILE_BYTES, V^T TC_TILE_BYTES after it
     uint8_t* tcb0 = smv + ((1024u - (su32(smv) & 1023u)) & 1023u);
     auto tcbuf = [&](int x) { return tcb0 + x * (2 * TC_TILE_BYTES); };
@@ -989,19 +991,24 @@ __global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
     const int t_lo = jlo / AT, t_hi = jhi / AT;
     float* cache = a.cache + ((b * a.Hq + h) * a.tiles_bh + tile_prefix((int64_t)blockIdx.x, W)) * (AT * AT);
     const uint8_t* vsrc = pa.vimg + (b * a.Hkv + g) * pa.nkt * VIMG_TILE;
+    // tiles per exact slice: a whole query tile when no row has more than 520
+    // valid keys (W <= 520), else 8
+    const int slice = (W > 0 && W <= 520) ? (1 << 30) : TC_SLICE_TILES;
 
-    // one thread of the last warp issues the copies and the MMAs (the row
-    // sums run on the first two warps)
-    constexpr int ISSUER = NT - 32;
     if (lt == 0) {
         for (int x = 0; x < 2; ++x) {
             mbar_init(&mma_bar[x], 1);
             mbar_init(&v_bar[x], 1);
+            mbar_init(&ready[x], PV_PROD / 32);   // one arrival per producer warp
+            mbar_init(&ps_free[x], 2);            // one per consumer warp
         }
+        dead_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (lt < 32) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
+        // columns 0-127: the fp32 accumulator of the current slice; 128-255:
+        // the int32 sums of the finished slices
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(
                          su32(&tmem_slot))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -1014,244 +1021,302 @@ __global__ void __launch_bounds__(NT, 2) k_attn_pv(const AttnPVArgs pa)
     __syncthreads();
     fence_after();
     const uint32_t tmem = tmem_slot;
-    uint32_t vn[2] = {0, 0}, vw[2] = {0, 0};   // V^T copies issued / seen complete, per buffer
-    if (lt == ISSUER) {   // V^T of the first tile
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_expect_tx(&v_bar[0], VIMG_TILE);
-        bulk_load(tcbuf(0) + TC_TILE_BYTES, vsrc + (int64_t)t_lo * VIMG_TILE, VIMG_TILE, &v_bar[0]);
-        vn[0] = 1;
-    }
 
-    // P.V outputs of this thread: query row tc_row, d 32 tc_cb .. + 31
-    const int wq = (lt >> 5) & 3;
-    const int tc_row = 32 * (wq & 1) + (lt & 31);
-    const int tc_cb = 2 * (wq >> 1) + (lt >> 7);
-    bool fail = false, dead = false;
-    // tiles per exact slice: a whole query tile when no row has more than 520
-    // valid keys (W <= 520), else 8
-    const int slice = (W > 0 && W <= 520) ? (1 << 30) : TC_SLICE_TILES;
+    // bounded; returns false at once once any wait in the CTA has failed
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const long long t0 = clock64();
+        while (!mbar_test(bar, parity)) {
+            if (*reinterpret_cast<volatile int*>(&dead_flag))
+                return false;
+            if (clock64() - t0 > WAIT_CYCLES) {
+                atomicExch(&dead_flag, 1);
+                return false;
+            }
+        }
+        return true;
+    };
 
-    const int my_i = i0 + lt;
-    const int my_lo = W > 0 ? max(0, my_i - W + 1) : 0;
-    const int my_n = my_i - my_lo + 1;
-    int pos = 0;
-    float cs = 0.f, lsum = 0.f;
-    int acc[4][8];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            acc[r][u] = 0;
-    ulonglong2 sv4[4];
-    {
-        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(cache + lt * 16);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            sv4[e] = src[e];
-    }
-    for (int t = t_lo; t <= t_hi; ++t) {
-        const int j0 = t * AT;
-        const int it = t - t_lo;
-        const int bf = it & 1;
-        const bool more = t < t_hi;
-        // the P tile of this buffer was read by the MMA two tiles back (issued
-        // a whole tile ago, so this wait normally returns at once)
-        if (!dead && it >= 2 && !mbar_wait(&mma_bar[bf], ((it - 2) >> 1) & 1))
-            fail = true;
-        u64 s[8];
+    if (lt < PV_PROD) {
+        // ------------------------------------------------------------------
+        // producers: p, the codes and the P tile of every key tile
+        const int ty = lt >> 4, tx = lt & 15;
+        // logits of the next two tiles in flight
+        ulonglong2 sv4[4], sn4[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            s[2 * e] = sv4[e].x;
-            s[2 * e + 1] = sv4[e].y;
+            sv4[e] = reinterpret_cast<const ulonglong2*>(cache + lt * 16)[e];
+            if (t_lo < t_hi)
+                sn4[e] = reinterpret_cast<const ulonglong2*>(cache + AT * AT + lt * 16)[e];
         }
-        u64 pp[8];       // this thread's p as the cache's pairs: rows (r, r + 1) of key j in pp[ip*4 + j]
-        uint32_t cw[8];  // bf16 codes: row 4ty + rr, keys 4tx + 2c, +1 in cw[2 rr + c]
-        // every (query, key) pair of the tile valid: no per-pair test
-        const bool inner = i0 + AT - 1 < T && j0 + AT - 1 <= i0 && (W == 0 || j0 >= i0 + AT - W);
-        const u64 z = pack2(-0.0f, -0.0f), c127 = pack2(127.0f, 127.0f);
+        for (int t = t_lo; t <= t_hi; ++t) {
+            const int j0 = t * AT;
+            const int it = t - t_lo;
+            const int bf = it & 1;
+            const bool more = t < t_hi;
+            // the buffers of tile it - 2: read by its MMA and its row sums
+            if (it >= 2) {
+                wait(&mma_bar[bf], ((it - 2) >> 1) & 1);
+                wait(&ps_free[bf], ((it - 2) >> 1) & 1);
+            }
+            u64 s[8];
 #pragma unroll
-        for (int ip = 0; ip < 2; ++ip) {
-            const int r = 4 * ty + 2 * ip;   // rows r, r + 1 are the lanes of s[ip*4 + j]
-            const u64 nm = pack2(-mrow[r], -mrow[r + 1]);
-            uint32_t qb[2][4];               // float bits of the codes, per lane and key
+            for (int e = 0; e < 4; ++e) {
+                s[2 * e] = sv4[e].x;
+                s[2 * e + 1] = sv4[e].y;
+            }
+            u64 pp[8];       // p as the cache's pairs: rows (r, r + 1) of key j in pp[ip*4 + j]
+            uint32_t cw[8];  // bf16 codes: row 4ty + rr, keys 4tx + 2c, +1 in cw[2 rr + c]
+            // every (query, key) pair of the tile valid: no per-pair test
+            const bool inner = i0 + AT - 1 < T && j0 + AT - 1 <= i0 && (W == 0 || j0 >= i0 + AT - W);
+            const u64 z = pack2(-0.0f, -0.0f), c127 = pack2(127.0f, 127.0f);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                u64 e2 = exp_r2(fadd2_ftz(s[ip * 4 + j], nm));
-                if (!inner) {
-                    float p[2];
-                    unpack2(e2, p[0], p[1]);
-                    const int jj = j0 + 4 * tx + j;
+            for (int ip = 0; ip < 2; ++ip) {
+                const int r = 4 * ty + 2 * ip;   // rows r, r + 1 are the lanes of s[ip*4 + j]
+                const u64 nm = pack2(-mrow[r], -mrow[r + 1]);
+                uint32_t qb[2][4];               // float bits of the codes, per lane and key
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int i = i0 + r + hh;
-                        const int lo = W > 0 ? max(0, i - W + 1) : 0;
-                        if (!(i < T && jj >= lo && jj <= i))
-                            p[hh] = 0.f;
+                for (int j = 0; j < 4; ++j) {
+                    u64 e2 = exp_r2(fadd2_ftz(s[ip * 4 + j], nm));
+                    if (!inner) {
+                        float p[2];
+                        unpack2(e2, p[0], p[1]);
+                        const int jj = j0 + 4 * tx + j;
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int i = i0 + r + hh;
+                            const int lo = W > 0 ? max(0, i - W + 1) : 0;
+                            if (!(i < T && jj >= lo && jj <= i))
+                                p[hh] = 0.f;
+                        }
+                        e2 = pack2(p[0], p[1]);
                     }
-                    e2 = pack2(p[0], p[1]);
+                    pp[ip * 4 + j] = e2;
+                    float t0, t1;
+                    unpack2(fadd2_ftz(fmul2_rn(e2, c127), z), t0, t1);
+                    qb[0][j] = __float_as_uint(quant_pf(t0));
+                    qb[1][j] = __float_as_uint(quant_pf(t1));
                 }
-                pp[ip * 4 + j] = e2;
-                float t0, t1;
-                unpack2(fadd2_ftz(fmul2_rn(e2, c127), z), t0, t1);
-                qb[0][j] = __float_as_uint(quant_pf(t0));
-                qb[1][j] = __float_as_uint(quant_pf(t1));
+                // a code (0 .. 127) as bf16 is the high half of its float
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    cw[2 * (2 * ip + hh)] = __byte_perm(qb[hh][0], qb[hh][1], 0x7632);
+                    cw[2 * (2 * ip + hh) + 1] = __byte_perm(qb[hh][2], qb[hh][3], 0x7632);
+                }
             }
-            // a code (0 .. 127) as bf16 is the high half of its float
+            if (more) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                cw[2 * (2 * ip + hh)] = __byte_perm(qb[hh][0], qb[hh][1], 0x7632);
-                cw[2 * (2 * ip + hh) + 1] = __byte_perm(qb[hh][2], qb[hh][3], 0x7632);
+                for (int e = 0; e < 4; ++e)
+                    sv4[e] = sn4[e];
+                if (t + 1 < t_hi) {   // the logits two tiles ahead
+                    const ulonglong2* src =
+                        reinterpret_cast<const ulonglong2*>(cache + (int64_t)(it + 2) * (AT * AT) + lt * 16);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        sn4[e] = src[e];
+                }
+            }
+            float* Ps = Psb + bf * (AT * PS);
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const int r = 4 * ty + rr;
+                // the four codes at keys 4tx .. 4tx+3 of row r (rows 64-127 of
+                // the MMA's A are never read back: only lanes 0-63 hold rows)
+                *reinterpret_cast<uint2*>(tcbuf(bf) + sw128_off(r, 4 * tx)) = make_uint2(cw[2 * rr], cw[2 * rr + 1]);
+                const int ip = rr >> 1, hh = rr & 1;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    Ps[r * PS + 4 * tx + j] = lane_of(pp, ip, j, hh);
+            }
+            {
+                // the cache now holds p in place of each logit: the backward
+                // reads p from it instead of evaluating e^x again
+                ulonglong2* dst = reinterpret_cast<ulonglong2*>(cache + (int64_t)it * (AT * AT) + lt * 16);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    dst[e] = make_ulonglong2(pp[2 * e], pp[2 * e + 1]);
+            }
+            // the P tile's generic-proxy stores become visible to the tensor core
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if ((lt & 31) == 0)
+                mbar_arrive(&ready[bf]);
+        }
+    } else if (lt < PV_PROD + 64) {
+        // ------------------------------------------------------------------
+        // row-sum warps: row cl's sums; warp cl / 32 reads tensor-memory lanes
+        // 32 (cl / 32) .. + 31 (rows 0-63) at the end of every exact slice
+        const int cl = lt - PV_PROD;
+        const int lane = cl & 31;
+        const uint32_t trow = tmem + ((uint32_t)(32 * (cl >> 5)) << 16);
+        const int my_i = i0 + cl;
+        const int my_lo = W > 0 ? max(0, my_i - W + 1) : 0;
+        const int my_n = my_i - my_lo + 1;
+        int pos = 0;
+        float cs = 0.f, lsum = 0.f;
+        bool first_slice = true;
+        for (int t = t_lo; t <= t_hi; ++t) {
+            const int j0 = t * AT;
+            const int it = t - t_lo;
+            const int bf = it & 1;
+            const bool more = t < t_hi;
+            wait(&ready[bf], (it >> 1) & 1);
+            // the valid p of this tile, left to right, through the
+            // chunk-of-64 / pairwise-tree stack
+            if (my_i < T) {
+                const int cb = max(my_lo, j0), ce = min(my_i, j0 + AT - 1);
+                const float* prow = Psb + bf * (AT * PS) + cl * PS;   // column jj - j0
+                int jj = cb;
+                while (jj <= ce) {
+                    // one run up to the next chunk boundary: left to right,
+                    // seeded with the chunk's first term
+                    const int room = 64 - (pos & 63);
+                    const int len = min(room, ce - jj + 1);
+                    int k = 0;
+                    const float* pr = prow + (jj - j0);
+                    if ((pos & 63) == 0) {
+                        cs = pr[0];
+                        k = 1;
+                    }
+#pragma unroll 8
+                    for (; k < len; ++k)
+                        cs = fadd_ftz(cs, pr[k]);
+                    jj += len;
+                    pos += len;
+                    if ((pos & 63) == 0 || pos == my_n) {
+                        const int c = (pos - 1) >> 6;
+                        float acc_t = cs;
+                        if (pos == my_n) {
+                            for (int lvl = 0; lvl < MAXL; ++lvl)
+                                if ((c >> lvl) & 1)
+                                    acc_t = fadd_ftz(stk[cl * (MAXL + 1) + lvl], acc_t);
+                            lsum = acc_t;
+                        } else {
+                            const int tz = __ffs(~c) - 1;
+                            for (int lvl = 0; lvl < tz; ++lvl)
+                                acc_t = fadd_ftz(stk[cl * (MAXL + 1) + lvl], acc_t);
+                            stk[cl * (MAXL + 1) + tz] = acc_t;
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&ps_free[bf]);
+            // end of an exact slice: its accumulator, as int32, into the sums
+            if (it % slice == slice - 1 || !more) {
+                const bool got = __all_sync(0xffffffffu, wait(&mma_bar[bf], (it >> 1) & 1));
+                if (got) {
+                    fence_after();
+#pragma unroll
+                    for (int c = 0; c < HD / 16; ++c) {
+                        uint32_t v[16], u[16];
+                        tmem_ld16(trow + 16 * c, v);
+                        if (!first_slice)
+                            tmem_ld16(trow + 128 + 16 * c, u);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            u[e] = (first_slice ? 0u : u[e]) + (uint32_t)__float2int_rn(__uint_as_float(v[e]));
+                        tmem_st16(trow + 128 + 16 * c, u);
+                    }
+                    fence_before();
+                }
+                first_slice = false;
+                // the accumulator has been read before the MMA warp starts
+                // the next slice over it
+                asm volatile("bar.sync 3, 96;" ::: "memory");
             }
         }
-        if (more) {   // the next tile's logits, in flight until the next tile starts
-            const ulonglong2* src =
-                reinterpret_cast<const ulonglong2*>(cache + (int64_t)(t + 1 - t_lo) * (AT * AT) + lt * 16);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                sv4[e] = src[e];
+
+        lrow[cl] = lsum;
+        if (my_i < T)
+            a.l[(b * a.T + my_i) * a.Hq + h] = lsum;
+    } else {
+        // ------------------------------------------------------------------
+        // the MMA warp: lane 0 copies V^T and issues the MMAs
+        const bool issuer = lt == PV_PROD + 64;
+        uint32_t vn[2] = {0, 0}, vw[2] = {0, 0};   // V^T copies issued / seen complete
+        if (issuer) {   // V^T of the first tile
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(&v_bar[0], VIMG_TILE);
+            bulk_load(tcbuf(0) + TC_TILE_BYTES, vsrc + (int64_t)t_lo * VIMG_TILE, VIMG_TILE, &v_bar[0]);
+            vn[0] = 1;
         }
-        float* Ps = Psb + bf * (AT * PS);
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            const int r = 4 * ty + rr;
-            // the four codes at keys 4tx .. 4tx+3 of rows r and r + 64
-            const uint2 bw = make_uint2(cw[2 * rr], cw[2 * rr + 1]);
-            *reinterpret_cast<uint2*>(tcbuf(bf) + sw128_off(r, 4 * tx)) = bw;
-            *reinterpret_cast<uint2*>(tcbuf(bf) + sw128_off(r + 64, 4 * tx)) = bw;
-            const int ip = rr >> 1, hh = rr & 1;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                Ps[r * PS + 4 * tx + j] = lane_of(pp, ip, j, hh);
-        }
-        {
-            // the cache now holds p in place of each logit: the backward
-            // reads p from it instead of evaluating e^x again
-            ulonglong2* dst = reinterpret_cast<ulonglong2*>(cache + (int64_t)it * (AT * AT) + lt * 16);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                dst[e] = make_ulonglong2(pp[2 * e], pp[2 * e + 1]);
-        }
-        // the P tile's generic-proxy stores become visible to the tensor core
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        dead = __syncthreads_or(fail || dead) != 0;
-        if (lt == ISSUER && !dead) {
-            if (!mbar_wait(&v_bar[bf], (it >> 1) & 1)) {
-                fail = true;
-            } else {
+        for (int t = t_lo; t <= t_hi; ++t) {
+            const int it = t - t_lo;
+            const int bf = it & 1;
+            const bool more = t < t_hi;
+            if (issuer && wait(&ready[bf], (it >> 1) & 1) && wait(&v_bar[bf], (it >> 1) & 1)) {
                 ++vw[bf];
                 fence_after();
                 const uint64_t ad = sdesc(su32(tcbuf(bf))), bd = sdesc(su32(tcbuf(bf) + TC_TILE_BYTES));
 #pragma unroll
                 for (int k = 0; k < AT / 16; ++k)
-                    mma_bf16<HD>(tmem, ad + 2 * k, bd + 2 * k,
-                                 (it % slice != 0 || k != 0) ? 1u : 0u);
+                    mma_bf16<HD>(tmem, ad + 2 * k, bd + 2 * k, (it % slice != 0 || k != 0) ? 1u : 0u);
                 mma_commit(&mma_bar[bf]);
-                if (more) {
-                    // V^T of the next tile into the other buffer, once the
-                    // MMA of the previous tile has read it
-                    const int nb = bf ^ 1;
-                    if (it >= 1 && !mbar_wait(&mma_bar[nb], ((it - 1) >> 1) & 1)) {
-                        fail = true;
-                    } else {
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        mbar_expect_tx(&v_bar[nb], VIMG_TILE);
-                        bulk_load(tcbuf(nb) + TC_TILE_BYTES, vsrc + (int64_t)(t + 1) * VIMG_TILE, VIMG_TILE,
-                                  &v_bar[nb]);
-                        ++vn[nb];
-                    }
+                // V^T of the next tile into the other buffer, once the MMA of
+                // the previous tile has read it
+                if (more && (it == 0 || wait(&mma_bar[bf ^ 1], ((it - 1) >> 1) & 1))) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_expect_tx(&v_bar[bf ^ 1], VIMG_TILE);
+                    bulk_load(tcbuf(bf ^ 1) + TC_TILE_BYTES, vsrc + (int64_t)(t + 1) * VIMG_TILE, VIMG_TILE,
+                              &v_bar[bf ^ 1]);
+                    ++vn[bf ^ 1];
                 }
             }
-        }
-        // row sums: the valid p of this tile, left to right, through the
-        // chunk-of-64 / pairwise-tree stack
-        if (lt < AT && my_i < T) {
-            const int cb = max(my_lo, j0), ce = min(my_i, j0 + AT - 1);
-            const float* prow = Ps + lt * PS;   // column jj - j0
-            int jj = cb;
-            while (jj <= ce) {
-                // one run up to the next chunk boundary: left to right, seeded
-                // with the chunk's first term
-                const int room = 64 - (pos & 63);
-                const int len = min(room, ce - jj + 1);
-                int k = 0;
-                const float* pr = prow + (jj - j0);
-                if ((pos & 63) == 0) {
-                    cs = pr[0];
-                    k = 1;
-                }
-#pragma unroll 8
-                for (; k < len; ++k)
-                    cs = fadd_ftz(cs, pr[k]);
-                jj += len;
-                pos += len;
-                if ((pos & 63) == 0 || pos == my_n) {
-                    const int c = (pos - 1) >> 6;
-                    float acc_t = cs;
-                    if (pos == my_n) {
-                        for (int lvl = 0; lvl < MAXL; ++lvl)
-                            if ((c >> lvl) & 1)
-                                acc_t = fadd_ftz(stk[lt * (MAXL + 1) + lvl], acc_t);
-                        lsum = acc_t;
-                    } else {
-                        const int tz = __ffs(~c) - 1;
-                        for (int lvl = 0; lvl < tz; ++lvl)
-                            acc_t = fadd_ftz(stk[lt * (MAXL + 1) + lvl], acc_t);
-                        stk[lt * (MAXL + 1) + tz] = acc_t;
-                    }
-                }
-            }
-        }
-        // end of an exact slice: add the accumulator to the int32 sums
-        if (!dead && (it % slice == slice - 1 || !more)) {
-            const bool got = __all_sync(0xffffffffu, mbar_wait(&mma_bar[bf], (it >> 1) & 1));
-            if (got) {
+            __syncwarp();
+            if (it % slice == slice - 1 || !more) {
+                asm volatile("bar.sync 3, 96;" ::: "memory");   // the slice has been read
                 fence_after();
-                uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * wq) << 16) + (uint32_t)(32 * tc_cb), v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    acc[e >> 3][e & 7] += __float2int_rn(__uint_as_float(v[e]));
-                fence_before();
-            } else {
-                fail = true;
             }
         }
+        // copies still in flight (only after a failed wait) land before exit
+        if (issuer)
+            for (int x = 0; x < 2; ++x)
+                while (vw[x] < vn[x] && mbar_wait(&v_bar[x], vw[x] & 1))
+                    ++vw[x];
     }
-    if (lt < AT)
-        lrow[lt] = lsum;
+
+    fence_before();
     __syncthreads();
-
-    const float sv = flush(*a.s_v);
-    const int64_t i = i0 + tc_row;
-    if (i < (int64_t)T) {
-        const float den = fmul_flush(lrow[tc_row], 127.0f);
-        float* dst = a.o + ((b * a.T + i) * a.Hq + h) * HD + 32 * tc_cb;
+    fence_after();
+    // epilogue: o = (i2f(sum) (x) s_v) (/) (l (x) 127).  The six warps that can
+    // read tensor-memory lanes 0-63 (warps 0, 4, 8: rows 0-31; 1, 5, 9: rows
+    // 32-63) take 48, 48 and 32 of the 128 columns
+    {
+        const int w = lt >> 5;
+        if (w < 10 && (w & 3) < 2) {
+            const int q = w & 3, part = w >> 2;   // part 0, 1, 2 -> chunks 0-2, 3-5, 6-7
+            const int row = 32 * q + (lt & 31);
+            const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+            const int64_t i = i0 + row;
+            const float sv = flush(*a.s_v);
+            const float den = fmul_flush(lrow[row], 127.0f);
+            float* dst = a.o + ((b * a.T + i) * a.Hq + h) * HD;
+            const int c_end = part == 2 ? HD / 16 : 3 * part + 3;
+#pragma unroll 1
+            for (int c = 3 * part; c < c_end; ++c) {
+                uint32_t u[16];
+                tmem_ld16(trow + 128 + 16 * c, u);
+                if (i < (int64_t)T) {
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-            float ov[4];
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        float ov[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = 4 * c4 + u;
-                ov[u] = flush(__fdiv_rn(fmul_flush(__int2float_rn(acc[c >> 3][c & 7]), sv), den));
+                        for (int e = 0; e < 4; ++e)
+                            ov[e] = flush(__fdiv_rn(fmul_flush(__int2float_rn((int)u[4 * q4 + e]), sv), den));
+                        *reinterpret_cast<float4*>(dst + 16 * c + 4 * q4) = make_float4(ov[0], ov[1], ov[2], ov[3]);
+                    }
+                }
             }
-            *reinterpret_cast<float4*>(dst + 4 * c4) = make_float4(ov[0], ov[1], ov[2], ov[3]);
         }
-        if (tc_cb == 0)
-            a.l[(b * a.T + i) * a.Hq + h] = lrow[tc_row];
     }
-
-    // after a failed wait, copies still in flight land before the CTA exits
-    if (lt == ISSUER)
-        for (int x = 0; x < 2; ++x)
-            while (vw[x] < vn[x] && mbar_wait(&v_bar[x], vw[x] & 1))
-                ++vw[x];
     fence_before();
     __syncthreads();
     if (lt < 32) {
         fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem) : "memory");
     }
-    if (fail)
+    if (lt == 0 && dead_flag)
         atomicExch(a.err, 1);
 }
 
@@ -2059,7 +2124,7 @@ cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, co
         e = cudaFuncSetAttribute(k_attn_pv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PV_SMEM);
         if (e != cudaSuccess)
             return e;
-        k_attn_pv<<<dim3((unsigned)nqt, (unsigned)Hq, (unsigned)B), NT, PV_SMEM, st>>>(pa);
+        k_attn_pv<<<dim3((unsigned)nqt, (unsigned)Hq, (unsigned)B), PV_NTH, PV_SMEM, st>>>(pa);
         count_launches(1);
         return cudaGetLastError();
     }
