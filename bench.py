@@ -732,7 +732,7 @@ def run_attn(args, aw):
     dk = torch.empty(k.shape, device=dev)
     dv = torch.empty(k.shape, device=dev)
     ws_s = torch.empty(max(R.repro_wscale_ws_bytes(v.size), 16), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(R.repro_attn_bwd_ws_bytes(B, T, Hq), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(R.repro_attn_bwd_ws_bytes(B, T, Hq, aw.window), dtype=torch.uint8, device=dev)
     ws_f = torch.empty(max(R.repro_attn_fwd_ws_bytes(B, T, Hq, aw.window), 16), dtype=torch.uint8,
                        device=dev)   # the forward's logit cache
     dev_bufs = (tq, tk, tv, tdo, dq, dk, dv)

@@ -757,11 +757,11 @@ int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float
         launch_attn_fwd(q, k, vq, s_v, o, m, l, B, T, Hq, Hkv, W, ws, tc, as_stream(stream)));
 }
 
-size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq)
+size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W)
 {
-    if (B <= 0 || T <= 0 || Hq <= 0)
+    if (B <= 0 || T <= 0 || Hq <= 0 || W < -1 || T > REPRO_ATTN_MAX_T)
         return 0;
-    return attn_bwd_ws_bytes(B, T, Hq);
+    return attn_bwd_ws_bytes(B, T, Hq, W);
 }
 
 int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
@@ -796,7 +796,8 @@ int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float
             if (overlap(outs[x], outsz[x], outs[y], outsz[y]))
                 return REPRO_ERR_ALIAS;
     }
-    const size_t need = attn_bwd_ws_bytes(B, T, Hq);
+    // the cached route keeps its tiles and copies in ws too
+    const size_t need = attn_bwd_ws_bytes(B, T, Hq, fwd_ws ? W : -1);
     if (!ws || ws_bytes < need)
         return REPRO_ERR_WORKSPACE;
     if (!al16(ws))

@@ -93,7 +93,7 @@ cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, co
                             float* o, float* m, float* l, int64_t B, int64_t T, int64_t Hq,
                             int64_t Hkv, int64_t W, void* cache, bool tc, cudaStream_t st);
 
-size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq);
+size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);   // W = -1: without the cache
 cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                             const float* o, const float* dout, const float* m, const float* l,
                             float* dq, float* dk, float* dv, int64_t B, int64_t T, int64_t Hq,

@@ -611,7 +611,9 @@ constexpr int LG_NT = 256;                       // threads per CTA: two groups
 constexpr int LG_G = 128;                        // threads per group
 constexpr uint32_t KIMG_TILE = HD * AT * 4;      // bytes of one K^T tile
 constexpr int LG_Q_BYTES = HD * PT * 4;          // Q^T [d][64 rows], pitch PT
-constexpr int LG_GROUP_BYTES = LG_Q_BYTES + 2 * (int)KIMG_TILE;
+constexpr int LG_GROUP_BYTES = LG_Q_BYTES + 2 * (int)KIMG_TILE + 2 * AT * 4;   // + l, Dr rows (backward)
+constexpr int BT_P = 68;                         // pitch (floats) of the backward's a / dS tiles
+constexpr uint32_t BT_TILE = AT * BT_P * 4;      // bytes of one a or dS tile
 constexpr size_t LG_SMEM = 2 * (size_t)LG_GROUP_BYTES;
 constexpr uint32_t VIMG_TILE = 128 * 64 * 2;     // bytes of one V^T tile
 static_assert(LG_GROUP_BYTES % 128 == 0, "group layout alignment");
@@ -644,14 +646,19 @@ __global__ void k_attn_kimg(const float* __restrict__ k, float* __restrict__ img
 }
 
 struct AttnLogitArgs {
-    const float* q;
-    const float* kimg;
-    float* cache;
-    float* m;
+    const float* q;                // forward: q; backward: dO
+    const float* kimg;             // forward: the K^T image; backward: the V^T image
+    float* cache;                  // forward: written (logits); backward: read (p)
+    float* m;                      // forward: the row maxima
     unsigned long long* counter;   // query tiles handed out (zero at launch)
     int64_t T, Hq, Hkv, W, tiles_bh, nqt, nkt, items;
     float c;
     int* err;
+    // backward: l_i and Dr_i in; the a_ij and dS_ij tiles out ([64][BT_P] per tile)
+    const float* l;
+    const float* drow;
+    float* at;
+    float* st;
 };
 
 // the k-th query tile handed out: the last query tiles of every (sequence,
@@ -712,7 +719,8 @@ __device__ __forceinline__ void logit_chunk84(u64 (&acc)[16], const float* __res
     }
 }
 
-__global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
+template <bool BWD>
+__global__ void __launch_bounds__(LG_NT, 1) k_attn_rows(const AttnLogitArgs a)
 {
     extern __shared__ __align__(128) uint8_t sml[];
     __shared__ uint64_t full[2][2], empty[2][2];
@@ -724,6 +732,8 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
     uint8_t* gbase = sml + (size_t)gp * LG_GROUP_BYTES;
     float* Qt = reinterpret_cast<float*>(gbase);                   // [HD][PT]
     float* Kr = reinterpret_cast<float*>(gbase + LG_Q_BYTES);      // [2][HD][AT]
+    float* lrw = Kr + 2 * HD * AT;                                  // [AT] l_i (backward)
+    float* drw = lrw + AT;                                          // [AT] Dr_i (backward)
     if (tid == 0) {
         for (int x = 0; x < 2; ++x)
             for (int s = 0; s < 2; ++s) {
@@ -818,8 +828,18 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
                 Qt[(4 * c4 + 3) * PT + r] = v.w;
             }
         }
+        if constexpr (BWD) {
+            if (lt < AT) {
+                const int64_t i = qt.i0 + lt;
+                lrw[lt] = i < T ? a.l[(qt.b * a.T + i) * a.Hq + qt.h] : 1.0f;
+            } else {
+                const int64_t i = qt.i0 + lt - AT;
+                drw[lt - AT] = i < T ? a.drow[(qt.b * a.T + i) * a.Hq + qt.h] : 0.0f;
+            }
+        }
         asm volatile("bar.sync %0, %1;" ::"r"(gbar), "n"(LG_G) : "memory");
-        float* cache = a.cache + ((qt.b * a.Hq + qt.h) * a.tiles_bh + tile_prefix(qt.i0 / AT, W)) * (AT * AT);
+        const int64_t tile0 = (qt.b * a.Hq + qt.h) * a.tiles_bh + tile_prefix(qt.i0 / AT, W);
+        float* cache = a.cache + tile0 * (AT * AT);
         float mx[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -857,62 +877,124 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_logits(const AttnLogitArgs a)
             if (lane == 0)
                 mbar_arrive(&empty[gp][s]);
             ++used;
-            const u64 cc = pack2(a.c, a.c);
-            u64 sv[16];
+            if constexpr (!BWD) {
+                const u64 cc = pack2(a.c, a.c);
+                u64 sv[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)   // (t0 + t1) (x) c, flushed
-                sv[e] = fadd2_ftz(fmul2_rn(fadd2_ftz(t0[e], t1[e]), cc), pack2(-0.0f, -0.0f));
-            {
-                // rows 8ty .. 8ty+3 are 4 x 4 block (2ty, tx) of the cached tile,
-                // rows 8ty+4 .. 8ty+7 block (2ty + 1, tx)
-                float* tile = cache + (int64_t)(t - qt.t_lo) * (AT * AT);
+                for (int e = 0; e < 16; ++e)   // (t0 + t1) (x) c, flushed
+                    sv[e] = fadd2_ftz(fmul2_rn(fadd2_ftz(t0[e], t1[e]), cc), pack2(-0.0f, -0.0f));
+                {
+                    // rows 8ty .. 8ty+3 are 4 x 4 block (2ty, tx) of the cached tile,
+                    // rows 8ty+4 .. 8ty+7 block (2ty + 1, tx)
+                    float* tile = cache + (int64_t)(t - qt.t_lo) * (AT * AT);
 #pragma unroll
-                for (int blk = 0; blk < 2; ++blk) {
-                    ulonglong2* dst = reinterpret_cast<ulonglong2*>(tile + ((2 * ty + blk) * 16 + tx) * 16);
+                    for (int blk = 0; blk < 2; ++blk) {
+                        ulonglong2* dst = reinterpret_cast<ulonglong2*>(tile + ((2 * ty + blk) * 16 + tx) * 16);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        dst[e] = make_ulonglong2(sv[8 * blk + 2 * e], sv[8 * blk + 2 * e + 1]);
-                }
-            }
-            const int j0 = t * AT;
-            const bool inner = qt.i0 + AT - 1 < T && j0 + AT - 1 <= qt.i0 && (W == 0 || j0 >= qt.i0 + AT - W);
-#pragma unroll
-            for (int ip = 0; ip < 4; ++ip)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float lo, hi;
-                    unpack2(sv[ip * 4 + j], lo, hi);
-                    if (inner) {
-                        mx[2 * ip] = fmaxf(mx[2 * ip], lo);
-                        mx[2 * ip + 1] = fmaxf(mx[2 * ip + 1], hi);
-                    } else {
-                        const int jj = j0 + 4 * tx + j;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int i = qt.i0 + 8 * ty + 2 * ip + h;
-                            const int lo_i = W > 0 ? max(0, i - W + 1) : 0;
-                            if (i < T && jj >= lo_i && jj <= i)
-                                mx[2 * ip + h] = fmaxf(mx[2 * ip + h], h ? hi : lo);
-                        }
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_ulonglong2(sv[8 * blk + 2 * e], sv[8 * blk + 2 * e + 1]);
                     }
                 }
-        }
-        // the rows' maxima over the 16 threads of each row group
+                const int j0 = t * AT;
+                const bool inner = qt.i0 + AT - 1 < T && j0 + AT - 1 <= qt.i0 && (W == 0 || j0 >= qt.i0 + AT - W);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
+                for (int ip = 0; ip < 4; ++ip)
 #pragma unroll
-            for (int off = 1; off < 16; off <<= 1)
-                mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], off));
-            if (mx[e] == 0.0f)
-                mx[e] = 0.0f;   // a zero maximum is +0
+                    for (int j = 0; j < 4; ++j) {
+                        float lo, hi;
+                        unpack2(sv[ip * 4 + j], lo, hi);
+                        if (inner) {
+                            mx[2 * ip] = fmaxf(mx[2 * ip], lo);
+                            mx[2 * ip + 1] = fmaxf(mx[2 * ip + 1], hi);
+                        } else {
+                            const int jj = j0 + 4 * tx + j;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int i = qt.i0 + 8 * ty + 2 * ip + h;
+                                const int lo_i = W > 0 ? max(0, i - W + 1) : 0;
+                                if (i < T && jj >= lo_i && jj <= i)
+                                    mx[2 * ip + h] = fmaxf(mx[2 * ip + h], h ? hi : lo);
+                            }
+                        }
+                    }
+            } else {
+                // dA = (t0 (+) t1); with p from the forward's cache (the pairs
+                // sit where pass 1 wrote this thread's logits):
+                //   a = p (/) l_i, dS = a (x) (dA (-) Dr_i), both flushed, +0 off the window
+                const u64 z = pack2(-0.0f, -0.0f);
+                const float* ptile = cache + (int64_t)(t - qt.t_lo) * (AT * AT);
+                u64 pv[16];
+#pragma unroll
+                for (int blk = 0; blk < 2; ++blk) {
+                    const ulonglong2* src = reinterpret_cast<const ulonglong2*>(ptile + ((2 * ty + blk) * 16 + tx) * 16);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const ulonglong2 v = src[e];
+                        pv[8 * blk + 2 * e] = v.x;
+                        pv[8 * blk + 2 * e + 1] = v.y;
+                    }
+                }
+                const int j0 = t * AT;
+                const bool inner = qt.i0 + AT - 1 < T && j0 + AT - 1 <= qt.i0 && (W == 0 || j0 >= qt.i0 + AT - W);
+                float av[8][4], dv[8][4];   // rows 8ty + rr, keys 4tx + j
+#pragma unroll
+                for (int ip = 0; ip < 4; ++ip)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int e = ip * 4 + j, r0 = 8 * ty + 2 * ip;
+                        float p[2], aa[2];
+                        unpack2(pv[e], p[0], p[1]);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            aa[h] = flush(__fdiv_rn(p[h], lrw[r0 + h]));
+                        float d[2];
+                        unpack2(fadd2_ftz(fmul2_rn(pack2(aa[0], aa[1]),
+                                                   fadd2_ftz(fadd2_ftz(t0[e], t1[e]), pack2(-drw[r0], -drw[r0 + 1]))),
+                                          z),
+                                d[0], d[1]);
+                        if (!inner) {
+                            const int jj = j0 + 4 * tx + j;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int i = qt.i0 + r0 + h;
+                                const int lo_i = W > 0 ? max(0, i - W + 1) : 0;
+                                if (!(i < T && jj >= lo_i && jj <= i))
+                                    aa[h] = d[h] = 0.f;
+                            }
+                        }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            av[2 * ip + h][j] = aa[h];
+                            dv[2 * ip + h][j] = d[h];
+                        }
+                    }
+                const int64_t toff = (tile0 + (t - qt.t_lo)) * (int64_t)(AT * BT_P);
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int64_t off = toff + (8 * ty + rr) * BT_P + 4 * tx;
+                    *reinterpret_cast<float4*>(a.at + off) = make_float4(av[rr][0], av[rr][1], av[rr][2], av[rr][3]);
+                    *reinterpret_cast<float4*>(a.st + off) = make_float4(dv[rr][0], dv[rr][1], dv[rr][2], dv[rr][3]);
+                }
+            }
         }
-        if (tx == 0)
+        if constexpr (!BWD) {
+            // the rows' maxima over the 16 threads of each row group
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int64_t i = qt.i0 + 8 * ty + e;
-                if (i < T)
-                    a.m[(qt.b * a.T + i) * a.Hq + qt.h] = mx[e];
+#pragma unroll
+                for (int off = 1; off < 16; off <<= 1)
+                    mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], off));
+                if (mx[e] == 0.0f)
+                    mx[e] = 0.0f;   // a zero maximum is +0
             }
+            if (tx == 0)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int64_t i = qt.i0 + 8 * ty + e;
+                    if (i < T)
+                        a.m[(qt.b * a.T + i) * a.Hq + qt.h] = mx[e];
+                }
+        }
     }
     // copies still in flight (only after a failed wait, or tiles issued ahead)
     if (lt == 0)
@@ -1982,12 +2064,643 @@ __global__ void __launch_bounds__(NT) k_attn_dq_final(const unsigned long long* 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Backward, default route (with the forward's cache).  Same arithmetic and
+// orders as k_attn_bwd; the work is split by what each output needs:
+//   k_attn_bimg        flushed copies of K, Q and dO by 64-row tile, the
+//                      dequantised V^T by key tile, the work counters zeroed;
+//   k_attn_rows<true>  per query tile (the forward logits kernel's
+//                      structure): dA = canon_d(dO (x) V^), then a and dS from
+//                      the cached p, written as [row][key] tiles (pitch BT_P);
+//   k_attn_bdq         per query tile: each key tile's left-to-right dQ
+//                      partial, into 64-bit fixed point in registers (no
+//                      atomics), then dQ;
+//   k_attn_bdkv        per key tile: the dK and dV group partials, folded
+//                      left in (head, query tile) order in registers.
+constexpr uint32_t ROW_TILE = AT * HD * 4;   // 64 rows x 128 floats
+
+struct AttnBwdImg {
+    const float* k;
+    const int8_t* vq;
+    const float* s_v;
+    const float* q;
+    const float* dout;
+    float* vimg;   // [B][Hkv][nkt] x [d][key], dequantised and flushed
+    float* krow;   // [B][Hkv][nkt] x [key][d], flushed
+    float* qrow;   // [B][Hq][nkt] x [row][d], flushed
+    float* grow;   // [B][Hq][nkt] x [row][d], flushed dO
+    unsigned long long* counters;
+    int64_t B, T, Hq, Hkv, nkt;
+};
+
+// blockIdx.y: 0 V^T, 1 K rows, 2 Q rows, 3 dO rows; rows at or past T are 0
+__global__ void k_attn_bimg(const AttnBwdImg a)
+{
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 4)
+        a.counters[threadIdx.x] = 0;
+    const int part = blockIdx.y;
+    const int64_t H = part >= 2 ? a.Hq : a.Hkv;
+    const int64_t n = a.B * H * a.nkt * (AT * HD / 4);
+    const float sv = flush(*a.s_v);
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        if (part == 0) {   // key fastest: the transposed stores are contiguous
+            const int key = (int)(e & (AT - 1));
+            const int d4 = (int)((e >> 6) & (HD / 4 - 1));
+            const int64_t tile = e >> 11;
+            const int64_t t = tile % a.nkt, bh = tile / a.nkt;
+            const int64_t j = t * AT + key;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < a.T) {
+                const int w = *reinterpret_cast<const int*>(a.vq + ((bh / H * a.T + j) * H + bh % H) * HD + 4 * d4);
+                v = make_float4(dequant((int)(int8_t)w, sv), dequant((int)(int8_t)(w >> 8), sv),
+                                dequant((int)(int8_t)(w >> 16), sv), dequant((int)(int8_t)(w >> 24), sv));
+            }
+            float* dst = a.vimg + tile * (HD * AT) + (4 * d4) * AT + key;
+            dst[0] = v.x;
+            dst[AT] = v.y;
+            dst[2 * AT] = v.z;
+            dst[3 * AT] = v.w;
+        } else {           // d fastest: rows copied whole
+            const int d4 = (int)(e & (HD / 4 - 1));
+            const int key = (int)((e >> 5) & (AT - 1));
+            const int64_t tile = e >> 11;
+            const int64_t t = tile % a.nkt, bh = tile / a.nkt;
+            const int64_t j = t * AT + key;
+            const float* src = part == 1 ? a.k : (part == 2 ? a.q : a.dout);
+            float* img = part == 1 ? a.krow : (part == 2 ? a.qrow : a.grow);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < a.T)
+                v = flush4(*reinterpret_cast<const float4*>(src + ((bh / H * a.T + j) * H + bh % H) * HD + 4 * d4));
+            *reinterpret_cast<float4*>(img + tile * (AT * HD) + key * HD + 4 * d4) = v;
+        }
+    }
+}
+
+struct AttnDqArgs {
+    const float* st;     // dS tiles
+    const float* krow;   // flushed K rows
+    float* dq;
+    unsigned long long* counter;
+    int64_t T, Hq, Hkv, W, tiles_bh, nqt, nkt, items;
+    float c;
+    int* err;
+};
+
+constexpr int DQ_STAGE = (int)(BT_TILE + ROW_TILE);   // one dS tile and its K rows
+constexpr size_t DQ_SMEM = 2 * (size_t)DQ_STAGE;
+
+// dQ of one query tile at a time per CTA (256 threads, one CTA per SM): a thread owns
+// rows 4ty .. 4ty+3 and columns 8tx .. 8tx+7 as four packed pairs along d, so
+// a pair shares its row and its keys.  Per key tile: the left-to-right sum
+// over the row's valid keys, from the first (flushed) product, then
+// fx(x) = nearest int64 to x (x) 2^48 added in registers; at the end
+// dQ = fix2f(sum) (x) c.  The dS tile and the key tile's K rows arrive by bulk
+// copies into a two-stage ring released per warp; query tiles come from a
+// counter, longest windows first
+__global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smq[];
+    __shared__ uint64_t full[2], empty[2];
+    __shared__ int64_t queue[8];
+    const int lt = threadIdx.x, lane = lt & 31;
+    const int ty = lt >> 4, tx = lt & 15;
+    if (lt == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NT / 32);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int T = (int)a.T, W = (int)a.W;
+    auto tile_of = [&](const QTile& q, int t) {   // the cache tile of (query tile q, key tile t)
+        return ((q.b * a.Hq + q.h) * a.tiles_bh + tile_prefix(q.i0 / AT, W)) + (t - q.t_lo);
+    };
+    auto qtile = [&](int64_t item) {
+        QTile r;
+        const int qt = (int)(item % a.nqt);
+        const int64_t bh = item / a.nqt;
+        r.h = bh % a.Hq;
+        r.b = bh / a.Hq;
+        r.g = r.h / (a.Hq / a.Hkv);
+        r.i0 = qt * AT;
+        const int jlo = W > 0 ? max(0, r.i0 - W + 1) : 0;
+        r.t_lo = jlo / AT;
+        r.t_hi = min(r.i0 + AT - 1, T - 1) / AT;
+        return r;
+    };
+    auto item_k = [&](int64_t k) {   // longest windows first
+        const int64_t bhs = a.items / a.nqt;
+        return (a.nqt - 1 - k / bhs) * 1 + (k % bhs) * a.nqt;
+    };
+
+    // issuer (thread 0): as the logits kernel's
+    int iss_k = 0, iss_t = 0;
+    bool have = false;
+    uint32_t issued = 0;
+    QTile iss_q;
+    auto take = [&](int kslot) {
+        const int64_t k = (int64_t)atomicAdd(a.counter, 1ull);
+        queue[kslot & 7] = k < a.items ? item_k(k) : -1;
+    };
+    auto start = [&](int kslot) {
+        const int64_t item = queue[kslot & 7];
+        have = item >= 0;
+        if (have) {
+            take(kslot + 1);
+            iss_q = qtile(item);
+            iss_t = iss_q.t_lo;
+        }
+    };
+    auto issue_next = [&]() {
+        if (!have)
+            return;
+        const int s = issued & 1;
+        uint8_t* stage = smq + s * DQ_STAGE;
+        mbar_expect_tx(&full[s], BT_TILE + ROW_TILE);
+        bulk_load(stage, a.st + tile_of(iss_q, iss_t) * (AT * BT_P), BT_TILE, &full[s]);
+        bulk_load(stage + BT_TILE, a.krow + ((iss_q.b * a.Hkv + iss_q.g) * a.nkt + iss_t) * (AT * HD), ROW_TILE,
+                  &full[s]);
+        ++issued;
+        if (++iss_t > iss_q.t_hi)
+            start(++iss_k);
+    };
+    if (lt == 0) {
+        take(0);
+        start(0);
+        issue_next();
+        issue_next();
+    }
+
+    uint32_t used = 0;
+    bool fail = false, dead = false;
+    const u64 z = pack2(-0.0f, -0.0f);
+    for (int kk = 0;; ++kk) {
+        dead = __syncthreads_or(fail || dead) != 0;   // also publishes the queue entry
+        const int64_t item = queue[kk & 7];
+        if (dead || item < 0)
+            break;
+        const QTile qt = qtile(item);
+        unsigned long long acc[4][8];   // fixed-point sums, wrapping like the int64 adds they replace
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[r][e] = 0ull;
+        for (int t = qt.t_lo; t <= qt.t_hi; ++t) {
+            const int s = used & 1;
+            if (lt == 0 && used >= 1 && issued == used + 1 && have) {
+                if (mbar_wait(&empty[s ^ 1], ((used - 1) >> 1) & 1))
+                    issue_next();
+                else
+                    fail = true;
+            }
+            if (!mbar_wait(&full[s], (used >> 1) & 1))
+                fail = true;
+            const float* S = reinterpret_cast<const float*>(smq + s * DQ_STAGE) + 4 * ty * BT_P;
+            const float* Kr = reinterpret_cast<const float*>(smq + s * DQ_STAGE + BT_TILE) + 8 * tx;
+            const int j0 = t * AT;
+            int jb[4], je[4];
+            bool whole = true;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = qt.i0 + 4 * ty + r;
+                const int lo = W > 0 ? max(0, i - W + 1) : 0;
+                jb[r] = max(lo, j0) - j0;
+                je[r] = min(i, j0 + AT - 1) - j0;
+                if (i >= T)
+                    jb[r] = AT, je[r] = -1;
+                whole = whole && jb[r] == 0 && je[r] == AT - 1;
+            }
+            u64 pp[4][4];   // [row][pair of columns]
+            if (whole) {
+                float sv[4];
+                ulonglong2 k01, k23;
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    sv[r] = S[r * BT_P];
+                k01 = *reinterpret_cast<const ulonglong2*>(Kr);
+                k23 = *reinterpret_cast<const ulonglong2*>(Kr + 4);
+                {
+                    const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
+                    float c4[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        c4[r] = sv[r];
+                        sv[r] = S[r * BT_P + 1];
+                    }
+                    k01 = *reinterpret_cast<const ulonglong2*>(Kr + HD);
+                    k23 = *reinterpret_cast<const ulonglong2*>(Kr + HD + 4);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const u64 P = pack2(c4[r], c4[r]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            pp[r][q] = fadd2_ftz(fmul2_rn(P, D[q]), z);
+                    }
+                }
+#pragma unroll 7
+                for (int j = 1; j < AT; ++j) {
+                    const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
+                    float c4[4];
+                    const int jn = j + 1 < AT ? j + 1 : j;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        c4[r] = sv[r];
+                        sv[r] = S[r * BT_P + jn];
+                    }
+                    k01 = *reinterpret_cast<const ulonglong2*>(Kr + jn * HD);
+                    k23 = *reinterpret_cast<const ulonglong2*>(Kr + jn * HD + 4);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const u64 P = pack2(c4[r], c4[r]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            pp[r][q] = fadd2_ftz(pp[r][q], fmul2_rn(P, D[q]));
+                    }
+                }
+            } else {
+                // mask-edge tile: each row over its own range of keys
+                int lo_all = AT, hi_all = -1;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    lo_all = min(lo_all, jb[r]);
+                    hi_all = max(hi_all, je[r]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        pp[r][q] = 0ull;
+                }
+                for (int j = lo_all; j <= hi_all; ++j) {
+                    const ulonglong2 k01 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD);
+                    const ulonglong2 k23 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD + 4);
+                    const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        if (j < jb[r] || j > je[r])
+                            continue;
+                        const float sv = S[r * BT_P + j];
+                        const u64 P = pack2(sv, sv);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const u64 pr = fmul2_rn(P, D[q]);
+                            pp[r][q] = j == jb[r] ? fadd2_ftz(pr, z) : fadd2_ftz(pp[r][q], pr);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[s]);
+            ++used;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (jb[r] > je[r])
+                    continue;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float v0, v1;
+                    unpack2(pp[r][q], v0, v1);
+                    acc[r][2 * q] += (unsigned long long)__float2ll_rn(fmul_rn(v0, 0x1p48f));
+                    acc[r][2 * q + 1] += (unsigned long long)__float2ll_rn(fmul_rn(v1, 0x1p48f));
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int64_t i = qt.i0 + 4 * ty + r;
+            if (i >= T)
+                continue;
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                o[e] = fmul_flush(flush(fmul_rn(__ll2float_rn((long long)acc[r][e]), 0x1p-48f)), a.c);
+            float* dst = a.dq + ((qt.b * a.T + i) * a.Hq + qt.h) * HD + 8 * tx;
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+        }
+    }
+    if (lt == 0)
+        while (used < issued && mbar_wait(&full[used & 1], (used >> 1) & 1))
+            ++used;
+    if (fail)
+        atomicExch(a.err, 1);
+}
+
+struct AttnDkvArgs {
+    const float* at;     // a tiles
+    const float* st;     // dS tiles
+    const float* qrow;   // flushed Q rows
+    const float* grow;   // flushed dO rows
+    float* dk;
+    float* dv;
+    unsigned long long* counter;
+    int64_t B, T, Hq, Hkv, W, tiles_bh, nqt, items;
+    float c;
+    int* err;
+};
+
+constexpr int KV_STAGE = (int)(2 * BT_TILE + 2 * ROW_TILE);   // dS, a, Q rows, dO rows
+constexpr size_t KV_SMEM = 2 * (size_t)KV_STAGE;
+
+// dK and dV of one key tile at a time per CTA (256 threads, one CTA per SM).
+// A thread owns keys 4ty .. 4ty+3 and columns 8tx .. 8tx+7 as four packed
+// pairs along d, so a pair shares its key and its range of queries.  The
+// groups (query head of the kv head, 64-aligned query tile) come in ascending
+// order; per group each key's partial is the left-to-right sum over its valid
+// queries from the first (flushed) product, and the partials are folded left
+// in registers.  dK = F_K (x) c, dV = F_V.  A group's dS and a tiles and its
+// flushed Q and dO rows arrive by bulk copies into a two-stage ring released
+// per warp; key tiles come from a counter, longest first
+__global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
+{
+    extern __shared__ __align__(128) uint8_t smk[];
+    __shared__ uint64_t full[2], empty[2];
+    __shared__ int64_t queue[8];
+    const int lt = threadIdx.x, lane = lt & 31;
+    const int ty = lt >> 4, tx = lt & 15;
+    if (lt == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], NT / 32);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int T = (int)a.T, W = (int)a.W;
+    const int64_t G = a.Hq / a.Hkv;
+    // key tile: (sequence, kv head, tile) and its query tiles
+    struct KTile {
+        int64_t b, g;
+        int t, u_lo, u_hi;   // query tiles u_lo .. u_hi of every head in the group
+    };
+    auto ktile = [&](int64_t item) {
+        KTile r;
+        const int64_t bgs = a.B * a.Hkv;
+        r.t = (int)(item / bgs);
+        const int64_t bg = item % bgs;
+        r.b = bg / a.Hkv;
+        r.g = bg % a.Hkv;
+        r.u_lo = r.t;
+        const int last = W > 0 ? min(T - 1, r.t * AT + AT - 1 + W - 1) : T - 1;
+        r.u_hi = last / AT;
+        return r;
+    };
+    // the cache tile of (query tile u of head h, key tile t)
+    auto tile_of = [&](int64_t b, int64_t h, int u, int t) {
+        const int t_lo = (W > 0 ? max(0, u * AT - W + 1) : 0) / AT;
+        return (b * a.Hq + h) * a.tiles_bh + tile_prefix(u, W) + (t - t_lo);
+    };
+
+    // issuer (thread 0): the groups of each key tile in order
+    int iss_k = 0, iss_h = 0, iss_u = 0;
+    bool have = false;
+    uint32_t issued = 0;
+    KTile iss_q;
+    auto take = [&](int kslot) {
+        const int64_t k = (int64_t)atomicAdd(a.counter, 1ull);
+        queue[kslot & 7] = k < a.items ? k : -1;   // hand-out order: key tile 0 (longest) first
+    };
+    auto start = [&](int kslot) {
+        const int64_t item = queue[kslot & 7];
+        have = item >= 0;
+        if (have) {
+            take(kslot + 1);
+            iss_q = ktile(item);
+            iss_h = 0;
+            iss_u = iss_q.u_lo;
+        }
+    };
+    auto issue_next = [&]() {
+        if (!have)
+            return;
+        const int s = issued & 1;
+        uint8_t* stage = smk + s * KV_STAGE;
+        const int64_t h = iss_q.g * G + iss_h;
+        const int64_t tl = tile_of(iss_q.b, h, iss_u, iss_q.t) * (AT * BT_P);
+        const int64_t rl = ((iss_q.b * a.Hq + h) * a.nqt + iss_u) * (AT * HD);
+        mbar_expect_tx(&full[s], 2 * BT_TILE + 2 * ROW_TILE);
+        bulk_load(stage, a.st + tl, BT_TILE, &full[s]);
+        bulk_load(stage + BT_TILE, a.at + tl, BT_TILE, &full[s]);
+        bulk_load(stage + 2 * BT_TILE, a.qrow + rl, ROW_TILE, &full[s]);
+        bulk_load(stage + 2 * BT_TILE + ROW_TILE, a.grow + rl, ROW_TILE, &full[s]);
+        ++issued;
+        if (++iss_u > iss_q.u_hi) {
+            iss_u = iss_q.u_lo;
+            if (++iss_h == G)
+                start(++iss_k);
+        }
+    };
+    if (lt == 0) {
+        take(0);
+        start(0);
+        issue_next();
+        issue_next();
+    }
+
+    uint32_t used = 0;
+    bool fail = false, dead = false;
+    const u64 z = pack2(-0.0f, -0.0f);
+    for (int kk = 0;; ++kk) {
+        dead = __syncthreads_or(fail || dead) != 0;   // also publishes the queue entry
+        const int64_t item = queue[kk & 7];
+        if (dead || item < 0)
+            break;
+        const KTile kt = ktile(item);
+        const int j0 = kt.t * AT;
+        u64 fk[4][4], fv[4][4];   // [key][pair of columns]
+        bool started[4] = {false, false, false, false};
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                fk[r][q] = fv[r][q] = 0ull;
+        for (int hh = 0; hh < G; ++hh)
+            for (int u = kt.u_lo; u <= kt.u_hi; ++u) {
+                const int s = used & 1;
+                if (lt == 0 && used >= 1 && issued == used + 1 && have) {
+                    if (mbar_wait(&empty[s ^ 1], ((used - 1) >> 1) & 1))
+                        issue_next();
+                    else
+                        fail = true;
+                }
+                if (!mbar_wait(&full[s], (used >> 1) & 1))
+                    fail = true;
+                const uint8_t* stage = smk + s * KV_STAGE;
+                const float* S = reinterpret_cast<const float*>(stage) + 4 * ty;
+                const float* A = reinterpret_cast<const float*>(stage + BT_TILE) + 4 * ty;
+                const float* Qr = reinterpret_cast<const float*>(stage + 2 * BT_TILE) + 8 * tx;
+                const float* Gr = reinterpret_cast<const float*>(stage + 2 * BT_TILE + ROW_TILE) + 8 * tx;
+                const int i0 = u * AT;
+                int ib[4], ie[4];
+                bool whole = true;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int j = j0 + 4 * ty + r;
+                    ib[r] = max(i0, j) - i0;
+                    ie[r] = min(min(i0 + AT - 1, T - 1), W > 0 ? j + W - 1 : T - 1) - i0;
+                    if (j >= T)
+                        ib[r] = AT, ie[r] = -1;
+                    whole = whole && ib[r] == 0 && ie[r] == AT - 1;
+                }
+                u64 pk[4][4], pv[4][4];
+                if (whole) {
+                    float4 sw = *reinterpret_cast<const float4*>(S);
+                    float4 aw = *reinterpret_cast<const float4*>(A);
+                    ulonglong2 q01 = *reinterpret_cast<const ulonglong2*>(Qr);
+                    ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(Qr + 4);
+                    ulonglong2 g01 = *reinterpret_cast<const ulonglong2*>(Gr);
+                    ulonglong2 g23 = *reinterpret_cast<const ulonglong2*>(Gr + 4);
+#pragma unroll 4
+                    for (int i = 0; i < AT; ++i) {
+                        const float ws[4] = {sw.x, sw.y, sw.z, sw.w}, wa[4] = {aw.x, aw.y, aw.z, aw.w};
+                        const u64 DQ[4] = {q01.x, q01.y, q23.x, q23.y}, DG[4] = {g01.x, g01.y, g23.x, g23.y};
+                        const int in = i + 1 < AT ? i + 1 : i;
+                        sw = *reinterpret_cast<const float4*>(S + in * BT_P);
+                        aw = *reinterpret_cast<const float4*>(A + in * BT_P);
+                        q01 = *reinterpret_cast<const ulonglong2*>(Qr + in * HD);
+                        q23 = *reinterpret_cast<const ulonglong2*>(Qr + in * HD + 4);
+                        g01 = *reinterpret_cast<const ulonglong2*>(Gr + in * HD);
+                        g23 = *reinterpret_cast<const ulonglong2*>(Gr + in * HD + 4);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const u64 PS = pack2(ws[r], ws[r]), PA = pack2(wa[r], wa[r]);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const u64 xk = fmul2_rn(PS, DQ[q]), xv = fmul2_rn(PA, DG[q]);
+                                pk[r][q] = i == 0 ? fadd2_ftz(xk, z) : fadd2_ftz(pk[r][q], xk);
+                                pv[r][q] = i == 0 ? fadd2_ftz(xv, z) : fadd2_ftz(pv[r][q], xv);
+                            }
+                        }
+                    }
+                } else {
+                    // mask-edge group: each key over its own range of queries
+                    int lo_all = AT, hi_all = -1;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        lo_all = min(lo_all, ib[r]);
+                        hi_all = max(hi_all, ie[r]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            pk[r][q] = pv[r][q] = 0ull;
+                    }
+                    for (int i = lo_all; i <= hi_all; ++i) {
+                        const float4 sw = *reinterpret_cast<const float4*>(S + i * BT_P);
+                        const float4 aw = *reinterpret_cast<const float4*>(A + i * BT_P);
+                        const ulonglong2 q01 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD);
+                        const ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD + 4);
+                        const ulonglong2 g01 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD);
+                        const ulonglong2 g23 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD + 4);
+                        const float ws[4] = {sw.x, sw.y, sw.z, sw.w}, wa[4] = {aw.x, aw.y, aw.z, aw.w};
+                        const u64 DQ[4] = {q01.x, q01.y, q23.x, q23.y}, DG[4] = {g01.x, g01.y, g23.x, g23.y};
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            if (i < ib[r] || i > ie[r])
+                                continue;
+                            const u64 PS = pack2(ws[r], ws[r]), PA = pack2(wa[r], wa[r]);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const u64 xk = fmul2_rn(PS, DQ[q]), xv = fmul2_rn(PA, DG[q]);
+                                pk[r][q] = i == ib[r] ? fadd2_ftz(xk, z) : fadd2_ftz(pk[r][q], xk);
+                                pv[r][q] = i == ib[r] ? fadd2_ftz(xv, z) : fadd2_ftz(pv[r][q], xv);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&empty[s]);
+                ++used;
+                // fold the group partials, left to right over the groups
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (ib[r] > ie[r])
+                        continue;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        fk[r][q] = started[r] ? fadd2_ftz(fk[r][q], pk[r][q]) : pk[r][q];
+                        fv[r][q] = started[r] ? fadd2_ftz(fv[r][q], pv[r][q]) : pv[r][q];
+                    }
+                    started[r] = true;
+                }
+            }
+        const u64 cc = pack2(a.c, a.c);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int64_t j = j0 + 4 * ty + r;
+            if (j >= T)
+                continue;
+            const int64_t off = ((kt.b * a.T + j) * a.Hkv + kt.g) * HD + 8 * tx;
+            u64 k4[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                k4[q] = fadd2_ftz(fmul2_rn(fk[r][q], cc), z);   // dK = F_K (x) c, flushed
+            *reinterpret_cast<ulonglong2*>(a.dk + off) = make_ulonglong2(k4[0], k4[1]);
+            *reinterpret_cast<ulonglong2*>(a.dk + off + 4) = make_ulonglong2(k4[2], k4[3]);
+            *reinterpret_cast<ulonglong2*>(a.dv + off) = make_ulonglong2(fv[r][0], fv[r][1]);
+            *reinterpret_cast<ulonglong2*>(a.dv + off + 4) = make_ulonglong2(fv[r][2], fv[r][3]);
+        }
+    }
+    if (lt == 0)
+        while (used < issued && mbar_wait(&full[used & 1], (used >> 1) & 1))
+            ++used;
+    if (fail)
+        atomicExch(a.err, 1);
+}
+
+// the backward's workspace: Dr_i and the recomputing route's dQ accumulator,
+// then (with the cache) the a / dS tiles, the images and the work counters
+struct BwdWs {
+    unsigned long long* acc;
+    float* drow;
+    float* at;
+    float* st;
+    float* vimg;
+    float* krow;
+    float* qrow;
+    float* grow;
+    unsigned long long* counters;
+    size_t bytes;
+};
+
+static BwdWs bwd_ws_layout(void* ws, int64_t B, int64_t T, int64_t Hq, int64_t W)
+{
+    auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const uintptr_t base = reinterpret_cast<uintptr_t>(ws);   // 0: sizes only
+    const int64_t rows = B * T * Hq, nqt = (T + AT - 1) / AT;
+    BwdWs L = {};
+    size_t off = 0;
+    L.acc = reinterpret_cast<unsigned long long*>(base + off);
+    off = al(off + (size_t)(rows * HD * 8));
+    L.drow = reinterpret_cast<float*>(base + off);
+    off += (size_t)(rows * 4);
+    if (W < 0) {
+        L.bytes = off;
+        return L;
+    }
+    const size_t tiles = (size_t)(B * Hq * tile_prefix(nqt, W)), imgs = (size_t)(B * Hq * nqt);
+    auto take = [&](size_t bytes) {
+        off = al(off);
+        const uintptr_t p = base + off;
+        off += bytes;
+        return p;
+    };
+    L.at = reinterpret_cast<float*>(take(tiles * BT_TILE));
+    L.st = reinterpret_cast<float*>(take(tiles * BT_TILE));
+    L.vimg = reinterpret_cast<float*>(take(imgs * KIMG_TILE));
+    L.krow = reinterpret_cast<float*>(take(imgs * ROW_TILE));
+    L.qrow = reinterpret_cast<float*>(take(imgs * ROW_TILE));
+    L.grow = reinterpret_cast<float*>(take(imgs * ROW_TILE));
+    L.counters = reinterpret_cast<unsigned long long*>(take(64));
+    L.bytes = off;
+    return L;
+}
+
 } // namespace
 
-size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq)
+size_t attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W)
 {
-    const int64_t rows = B * T * Hq;
-    return (size_t)(((rows * HD * 8 + 255) & ~(int64_t)255) + rows * 4);
+    return bwd_ws_layout(nullptr, B, T, Hq, W).bytes;
 }
 
 cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
@@ -1997,14 +2710,16 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
                             cudaStream_t st)
 {
     const int64_t rows = B * T * Hq;
-    unsigned long long* acc = static_cast<unsigned long long*>(ws);
-    float* drow = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
-                                           ((rows * HD * 8 + 255) & ~(int64_t)255));
+    const BwdWs L = bwd_ws_layout(ws, B, T, Hq, lcache ? W : -1);
     const float c = 1.0f / sqrtf(128.0f);   // correctly rounded sqrt and division on the host
-    cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)(rows * HD * 8), st);
+    int* err = device_error_word();
+    if (!err)
+        return cudaErrorInvalidValue;
+    k_attn_drow<<<(unsigned)((rows + AT - 1) / AT), NT, 0, st>>>(o, dout, L.drow, rows);
+    count_launches(1);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    k_attn_drow<<<(unsigned)((rows + AT - 1) / AT), NT, 0, st>>>(o, dout, drow, rows);
     AttnBwdArgs a;
     a.q = q;
     a.k = k;
@@ -2013,8 +2728,8 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
     a.dout = dout;
     a.m = m;
     a.l = l;
-    a.drow = drow;
-    a.dq_acc = acc;
+    a.drow = L.drow;
+    a.dq_acc = L.acc;
     a.dk = dk;
     a.dv = dv;
     a.lcache = static_cast<const float*>(lcache);
@@ -2024,6 +2739,105 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
     a.W = W;
     a.tiles_bh = tile_prefix((T + AT - 1) / AT, W);
     a.c = c;
+    if (lcache) {
+        const int64_t nqt = (T + AT - 1) / AT, items = B * Hq * nqt;
+        const int64_t Wc = W > T ? T : W;   // the same windows and cache layout; W in 32 bits
+        const int64_t cap = (int64_t)num_sms() * 8;
+        AttnBwdImg im;
+        im.k = k;
+        im.vq = vq;
+        im.s_v = s_v;
+        im.q = q;
+        im.dout = dout;
+        im.vimg = L.vimg;
+        im.krow = L.krow;
+        im.qrow = L.qrow;
+        im.grow = L.grow;
+        im.counters = L.counters;
+        im.B = B;
+        im.T = T;
+        im.Hq = Hq;
+        im.Hkv = Hkv;
+        im.nkt = nqt;
+        const int64_t n_max = B * Hq * nqt * (AT * HD / 4);
+        k_attn_bimg<<<dim3((unsigned)std::min<int64_t>((n_max + 255) / 256, cap), 4), 256, 0, st>>>(im);
+        count_launches(1);
+        // dA, a and dS per query tile (the cache is only read in this mode)
+        AttnLogitArgs la;
+        la.q = dout;
+        la.kimg = L.vimg;
+        la.cache = const_cast<float*>(static_cast<const float*>(lcache));
+        la.m = nullptr;
+        la.counter = L.counters;
+        la.T = T;
+        la.Hq = Hq;
+        la.Hkv = Hkv;
+        la.W = Wc;
+        la.tiles_bh = a.tiles_bh;
+        la.nqt = nqt;
+        la.nkt = nqt;
+        la.items = items;
+        la.c = c;
+        la.err = err;
+        la.l = l;
+        la.drow = L.drow;
+        la.at = L.at;
+        la.st = L.st;
+        e = cudaFuncSetAttribute(k_attn_rows<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LG_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        k_attn_rows<true><<<(unsigned)std::min<int64_t>(num_sms(), (items + 1) / 2), LG_NT, LG_SMEM, st>>>(la);
+        count_launches(1);
+        // dQ per query tile
+        AttnDqArgs qa;
+        qa.st = L.st;
+        qa.krow = L.krow;
+        qa.dq = dq;
+        qa.counter = L.counters + 1;
+        qa.T = T;
+        qa.Hq = Hq;
+        qa.Hkv = Hkv;
+        qa.W = Wc;
+        qa.tiles_bh = a.tiles_bh;
+        qa.nqt = nqt;
+        qa.nkt = nqt;
+        qa.items = items;
+        qa.c = c;
+        qa.err = err;
+        e = cudaFuncSetAttribute(k_attn_bdq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        k_attn_bdq<<<(unsigned)std::min<int64_t>(num_sms(), items), NT, DQ_SMEM, st>>>(qa);
+        count_launches(1);
+        // dK and dV per key tile
+        AttnDkvArgs ka;
+        ka.at = L.at;
+        ka.st = L.st;
+        ka.qrow = L.qrow;
+        ka.grow = L.grow;
+        ka.dk = dk;
+        ka.dv = dv;
+        ka.counter = L.counters + 2;
+        ka.B = B;
+        ka.T = T;
+        ka.Hq = Hq;
+        ka.Hkv = Hkv;
+        ka.W = Wc;
+        ka.tiles_bh = a.tiles_bh;
+        ka.nqt = nqt;
+        ka.items = B * Hkv * nqt;
+        ka.c = c;
+        ka.err = err;
+        e = cudaFuncSetAttribute(k_attn_bdkv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)KV_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        k_attn_bdkv<<<(unsigned)std::min<int64_t>(num_sms(), ka.items), NT, KV_SMEM, st>>>(ka);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    e = cudaMemsetAsync(L.acc, 0, (size_t)(rows * HD * 8), st);
+    if (e != cudaSuccess)
+        return e;
     e = cudaFuncSetAttribute(k_attn_bwd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BWD_SMEM);
     if (e != cudaSuccess)
         return e;
@@ -2031,8 +2845,8 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
     k_attn_bwd<<<grid, NT, BWD_SMEM, st>>>(a);
     const int64_t n = rows * HD;
     int nb = num_sms() * 8;
-    k_attn_dq_final<<<nb, NT, 0, st>>>(acc, dq, n, c);
-    count_launches(3);
+    k_attn_dq_final<<<nb, NT, 0, st>>>(L.acc, dq, n, c);
+    count_launches(2);
     return cudaGetLastError();
 }
 
@@ -2108,11 +2922,11 @@ cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, co
         la.items = B * Hq * nqt;
         la.c = a.c;
         la.err = a.err;
-        e = cudaFuncSetAttribute(k_attn_logits, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LG_SMEM);
+        e = cudaFuncSetAttribute(k_attn_rows<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LG_SMEM);
         if (e != cudaSuccess)
             return e;
         const unsigned lgrid = (unsigned)std::min<int64_t>(num_sms(), (la.items + 1) / 2);
-        k_attn_logits<<<lgrid, LG_NT, LG_SMEM, st>>>(la);
+        k_attn_rows<false><<<lgrid, LG_NT, LG_SMEM, st>>>(la);
         count_launches(1);
         e = cudaGetLastError();
         if (e != cudaSuccess)

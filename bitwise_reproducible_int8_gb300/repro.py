@@ -81,7 +81,7 @@ _SIGNATURES = {
     "repro_attn_fwd_ws_bytes": (_sz, [_i64, _i64, _i64, _i64]),
     "repro_attn_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64,
                               _i64, _i64, _i64, _i64, _vp, _sz, _vp, _sz, _vp]),
-    "repro_attn_bwd_ws_bytes": (_sz, [_i64, _i64, _i64]),
+    "repro_attn_bwd_ws_bytes": (_sz, [_i64, _i64, _i64, _i64]),
     "repro_selftest": (_int, [_vp, _sz, _vp]),
     "repro_selftest_ws_bytes": (_sz, []),
     "repro_status_str": (ctypes.c_char_p, [_int]),
@@ -322,8 +322,10 @@ def repro_attn_fwd(q: torch.Tensor, k: torch.Tensor, vq: torch.Tensor, s_v: torc
         _ptr(ws, None, "ws"), ws_bytes, _stream(stream)))
 
 
-def repro_attn_bwd_ws_bytes(B: int, T: int, Hq: int) -> int:
-    return int(lib().repro_attn_bwd_ws_bytes(int(B), int(T), int(Hq)))
+def repro_attn_bwd_ws_bytes(B: int, T: int, Hq: int, W: int = 0) -> int:
+    """Workspace of repro_attn_bwd for window W; W = -1: a call without the
+    forward's cache."""
+    return int(lib().repro_attn_bwd_ws_bytes(int(B), int(T), int(Hq), int(W)))
 
 
 def repro_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, W: int = 0, ws=None,
@@ -334,7 +336,8 @@ def repro_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, W: int = 0, ws=None
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
     if ws is None:
-        ws = _workspace(repro_attn_bwd_ws_bytes(B, T, Hq), q.device)
+        ws = _workspace(repro_attn_bwd_ws_bytes(B, T, Hq, int(W) if fwd_ws is not None else -1),
+                        q.device)
     f32 = torch.float32
     _check("repro_attn_bwd", lib().repro_attn_bwd(
         _ptr(q, f32, "q"), _ptr(k, f32, "k"), _ptr(vq, torch.int8, "vq"), _ptr(s_v, f32, "s_v"),

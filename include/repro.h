@@ -323,18 +323,22 @@ size_t repro_attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);
  *     first term and the group partials are folded left in (head, tile) order.
  * Inputs as repro_attn_fwd plus o (its output), dout [B][T][Hq][128] and its
  * m, l; outputs dq [B][T][Hq][128], dk, dv [B][T][Hkv][128] (DEVICE, 16-byte
- * aligned, no overlaps).  ws: repro_attn_bwd_ws_bytes(B, T, Hq) bytes (the
- * int64 dQ accumulator and the Dr_i), not overlapping anything else.
+ * aligned, no overlaps).  ws: repro_attn_bwd_ws_bytes(B, T, Hq, W) bytes, not
+ * overlapping anything else: the Dr_i and, without fwd_ws, the int64 dQ
+ * accumulator; with fwd_ws also the a_ij and dS_ij tiles of the window and
+ * flushed copies of K, V^, Q and dO laid out for the three kernels of that
+ * route.  A call without fwd_ws needs only the first
+ * repro_attn_bwd_ws_bytes(B, T, Hq, -1) bytes.
  * fwd_ws (optional): the cache repro_attn_fwd filled for these same inputs,
- * unchanged since; the backward then reads p_ij from it instead of computing
- * the logits and e^x again (same bits).  NULL recomputes.
+ * unchanged since (read only); the backward then reads p_ij from it instead
+ * of computing the logits and e^x again (same bits).  NULL recomputes.
  * ------------------------------------------------------------------------ */
 int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                    const float* o, const float* dout, const float* m, const float* l,
                    float* dq, float* dk, float* dv, int64_t B, int64_t T, int64_t Hq,
                    int64_t Hkv, int64_t D, int64_t W, void* ws, size_t ws_bytes,
                    const void* fwd_ws, size_t fwd_ws_bytes, void* stream);
-size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq);
+size_t repro_attn_bwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);
 
 /* ------------------------------------------------------------------------
  * Per-step state hash ([rit] paragraph 4, [limits]: a hash of the state is

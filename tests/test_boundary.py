@@ -338,7 +338,13 @@ def test_attn_bwd_argument_checks(L):
     assert f(*args()) in (-4, -5)
     assert f(*args(fws=A * 64, fwsb=16)) == -7            # logit cache too small
     assert f(*args(fws=W_, fwsb=1 << 20)) == -8           # logit cache over ws
-    assert repro.repro_attn_bwd_ws_bytes(1, 8, 4) == 8 * 4 * 128 * 8 + 8 * 4 * 4
+    # without the forward's cache: the int64 dQ accumulator and Dr_i
+    assert repro.repro_attn_bwd_ws_bytes(1, 8, 4, -1) == 8 * 4 * 128 * 8 + 8 * 4 * 4
+    # with it (one query tile, one key tile, 4 heads): also the a and dS tiles
+    # (64 x 68 floats) and four 64 x 128-float images per head, 256-byte aligned
+    need = repro.repro_attn_bwd_ws_bytes(1, 8, 4, 0)
+    assert need >= 8 * 4 * 128 * 8 + 8 * 4 * 4 + 2 * 4 * 64 * 68 * 4 + 4 * 4 * 64 * 128 * 4 + 64
+    assert need == repro.repro_attn_bwd_ws_bytes(1, 8, 4, 100)   # one tile either way
 
 
 def test_selftest_arguments(L):

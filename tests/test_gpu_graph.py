@@ -86,7 +86,7 @@ def test_attention_graph_replays_match_eager(W):
                        device="cuda")
     ws_f = torch.empty(max(R.repro_attn_fwd_ws_bytes(B, T, Hq, W), 16), dtype=torch.uint8,
                        device="cuda")
-    ws_b = torch.empty(max(R.repro_attn_bwd_ws_bytes(B, T, Hq), 16), dtype=torch.uint8,
+    ws_b = torch.empty(max(R.repro_attn_bwd_ws_bytes(B, T, Hq, W), 16), dtype=torch.uint8,
                        device="cuda")
     st = torch.cuda.Stream()
     torch.cuda.synchronize()
