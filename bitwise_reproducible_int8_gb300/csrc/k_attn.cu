@@ -26,6 +26,8 @@
 //     sequence) runs both passes; pass 2 reads the cached logits or recomputes
 //     them, and P.V runs on dp4a (exact int32).  Logits: 256 threads own 4 x 4
 //     outputs each, packed f32x2 products over d with the chunk-of-64 order.
+#include <type_traits>
+
 #include "bwd_tile.cuh"
 #include "common.cuh"
 #include "internal.h"
@@ -2151,8 +2153,9 @@ constexpr int DQ_STAGE = (int)(BT_TILE + ROW_TILE);   // one dS tile and its K r
 constexpr size_t DQ_SMEM = 2 * (size_t)DQ_STAGE;
 
 // dQ of one query tile at a time per CTA (256 threads, one CTA per SM): a thread owns
-// rows 4ty .. 4ty+3 and columns 8tx .. 8tx+7 as four packed pairs along d, so
-// a pair shares its row and its keys.  Per key tile: the left-to-right sum
+// rows 4ty .. 4ty+3 and columns 4tx .. 4tx+3 and 64 + 4tx .. 64 + 4tx+3 (one
+// 16-byte load each, contiguous across the warp: no bank conflicts) as four
+// packed pairs along d, so a pair shares its row and its keys.  Per key tile: the left-to-right sum
 // over the row's valid keys, from the first (flushed) product, then
 // fx(x) = nearest int64 to x (x) 2^48 added in registers; at the end
 // dQ = fix2f(sum) (x) c.  The dS tile and the key tile's K rows arrive by bulk
@@ -2259,7 +2262,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
             if (!mbar_wait(&full[s], (used >> 1) & 1))
                 fail = true;
             const float* S = reinterpret_cast<const float*>(smq + s * DQ_STAGE) + 4 * ty * BT_P;
-            const float* Kr = reinterpret_cast<const float*>(smq + s * DQ_STAGE + BT_TILE) + 8 * tx;
+            const float* Kr = reinterpret_cast<const float*>(smq + s * DQ_STAGE + BT_TILE) + 4 * tx;
             const int j0 = t * AT;
             int jb[4], je[4];
             bool whole = true;
@@ -2281,7 +2284,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
                 for (int r = 0; r < 4; ++r)
                     sv[r] = S[r * BT_P];
                 k01 = *reinterpret_cast<const ulonglong2*>(Kr);
-                k23 = *reinterpret_cast<const ulonglong2*>(Kr + 4);
+                k23 = *reinterpret_cast<const ulonglong2*>(Kr + HD / 2);
                 {
                     const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
                     float c4[4];
@@ -2291,7 +2294,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
                         sv[r] = S[r * BT_P + 1];
                     }
                     k01 = *reinterpret_cast<const ulonglong2*>(Kr + HD);
-                    k23 = *reinterpret_cast<const ulonglong2*>(Kr + HD + 4);
+                    k23 = *reinterpret_cast<const ulonglong2*>(Kr + HD + HD / 2);
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         const u64 P = pack2(c4[r], c4[r]);
@@ -2311,13 +2314,33 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
                         sv[r] = S[r * BT_P + jn];
                     }
                     k01 = *reinterpret_cast<const ulonglong2*>(Kr + jn * HD);
-                    k23 = *reinterpret_cast<const ulonglong2*>(Kr + jn * HD + 4);
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const u64 P = pack2(c4[r], c4[r]);
+                    k23 = *reinterpret_cast<const ulonglong2*>(Kr + jn * HD + HD / 2);
+                    // the products of row r + 1 are formed before the adds of row
+                    // r, so no add waits on the multiply just issued
+                    u64 cur[4];
+                    {
+                        const u64 P = pack2(c4[0], c4[0]);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            pp[r][q] = fadd2_ftz(pp[r][q], fmul2_rn(P, D[q]));
+                            cur[q] = fmul2_rn(P, D[q]);
+                    }
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        u64 nxt[4];
+                        if (r + 1 < 4) {
+                            const u64 P = pack2(c4[r + 1], c4[r + 1]);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                nxt[q] = fmul2_rn(P, D[q]);
+                        }
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            pp[r][q] = fadd2_ftz(pp[r][q], cur[q]);
+                        if (r + 1 < 4) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                cur[q] = nxt[q];
+                        }
                     }
                 }
             } else {
@@ -2333,7 +2356,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
                 }
                 for (int j = lo_all; j <= hi_all; ++j) {
                     const ulonglong2 k01 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD);
-                    const ulonglong2 k23 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD + 4);
+                    const ulonglong2 k23 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD + HD / 2);
                     const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
@@ -2375,9 +2398,9 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 o[e] = fmul_flush(flush(fmul_rn(__ll2float_rn((long long)acc[r][e]), 0x1p-48f)), a.c);
-            float* dst = a.dq + ((qt.b * a.T + i) * a.Hq + qt.h) * HD + 8 * tx;
+            float* dst = a.dq + ((qt.b * a.T + i) * a.Hq + qt.h) * HD + 4 * tx;
             *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<float4*>(dst + HD / 2) = make_float4(o[4], o[5], o[6], o[7]);
         }
     }
     if (lt == 0)
@@ -2404,8 +2427,9 @@ constexpr int KV_STAGE = (int)(2 * BT_TILE + 2 * ROW_TILE);   // dS, a, Q rows, 
 constexpr size_t KV_SMEM = 2 * (size_t)KV_STAGE;
 
 // dK and dV of one key tile at a time per CTA (256 threads, one CTA per SM).
-// A thread owns keys 4ty .. 4ty+3 and columns 8tx .. 8tx+7 as four packed
-// pairs along d, so a pair shares its key and its range of queries.  The
+// A thread owns keys 4ty .. 4ty+3 and columns 4tx .. 4tx+3 and 64 + 4tx ..
+// 64 + 4tx+3 (conflict-free 16-byte loads) as four packed pairs along d, so a
+// pair shares its key and its range of queries.  The
 // groups (query head of the kv head, 64-aligned query tile) come in ascending
 // order; per group each key's partial is the left-to-right sum over its valid
 // queries from the first (flushed) product, and the partials are folded left
@@ -2529,8 +2553,8 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
                 const uint8_t* stage = smk + s * KV_STAGE;
                 const float* S = reinterpret_cast<const float*>(stage) + 4 * ty;
                 const float* A = reinterpret_cast<const float*>(stage + BT_TILE) + 4 * ty;
-                const float* Qr = reinterpret_cast<const float*>(stage + 2 * BT_TILE) + 8 * tx;
-                const float* Gr = reinterpret_cast<const float*>(stage + 2 * BT_TILE + ROW_TILE) + 8 * tx;
+                const float* Qr = reinterpret_cast<const float*>(stage + 2 * BT_TILE) + 4 * tx;
+                const float* Gr = reinterpret_cast<const float*>(stage + 2 * BT_TILE + ROW_TILE) + 4 * tx;
                 const int i0 = u * AT;
                 int ib[4], ie[4];
                 bool whole = true;
@@ -2548,31 +2572,54 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
                     float4 sw = *reinterpret_cast<const float4*>(S);
                     float4 aw = *reinterpret_cast<const float4*>(A);
                     ulonglong2 q01 = *reinterpret_cast<const ulonglong2*>(Qr);
-                    ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(Qr + 4);
+                    ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(Qr + HD / 2);
                     ulonglong2 g01 = *reinterpret_cast<const ulonglong2*>(Gr);
-                    ulonglong2 g23 = *reinterpret_cast<const ulonglong2*>(Gr + 4);
-#pragma unroll 4
-                    for (int i = 0; i < AT; ++i) {
-                        const float ws[4] = {sw.x, sw.y, sw.z, sw.w}, wa[4] = {aw.x, aw.y, aw.z, aw.w};
+                    ulonglong2 g23 = *reinterpret_cast<const ulonglong2*>(Gr + HD / 2);
+                    // one query row: the 8 (key, tensor) rows of products, those of
+                    // row x + 1 formed before the adds of row x; FIRST seeds the
+                    // sums with the flushed products
+                    auto row = [&](auto first_tag, int in) {
+                        constexpr bool FIRST = decltype(first_tag)::value;
+                        const float w8[8] = {sw.x, sw.y, sw.z, sw.w, aw.x, aw.y, aw.z, aw.w};
                         const u64 DQ[4] = {q01.x, q01.y, q23.x, q23.y}, DG[4] = {g01.x, g01.y, g23.x, g23.y};
-                        const int in = i + 1 < AT ? i + 1 : i;
                         sw = *reinterpret_cast<const float4*>(S + in * BT_P);
                         aw = *reinterpret_cast<const float4*>(A + in * BT_P);
                         q01 = *reinterpret_cast<const ulonglong2*>(Qr + in * HD);
-                        q23 = *reinterpret_cast<const ulonglong2*>(Qr + in * HD + 4);
+                        q23 = *reinterpret_cast<const ulonglong2*>(Qr + in * HD + HD / 2);
                         g01 = *reinterpret_cast<const ulonglong2*>(Gr + in * HD);
-                        g23 = *reinterpret_cast<const ulonglong2*>(Gr + in * HD + 4);
+                        g23 = *reinterpret_cast<const ulonglong2*>(Gr + in * HD + HD / 2);
+                        u64 cur[4];
+                        {
+                            const u64 P = pack2(w8[0], w8[0]);
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            const u64 PS = pack2(ws[r], ws[r]), PA = pack2(wa[r], wa[r]);
+                            for (int q = 0; q < 4; ++q)
+                                cur[q] = fmul2_rn(P, DQ[q]);
+                        }
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            u64 nxt[4];
+                            if (x + 1 < 8) {
+                                const u64 P = pack2(w8[x + 1], w8[x + 1]);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    nxt[q] = fmul2_rn(P, x + 1 < 4 ? DQ[q] : DG[q]);
+                            }
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
-                                const u64 xk = fmul2_rn(PS, DQ[q]), xv = fmul2_rn(PA, DG[q]);
-                                pk[r][q] = i == 0 ? fadd2_ftz(xk, z) : fadd2_ftz(pk[r][q], xk);
-                                pv[r][q] = i == 0 ? fadd2_ftz(xv, z) : fadd2_ftz(pv[r][q], xv);
+                                u64& acc = x < 4 ? pk[x][q] : pv[x - 4][q];
+                                acc = FIRST ? fadd2_ftz(cur[q], z) : fadd2_ftz(acc, cur[q]);
+                            }
+                            if (x + 1 < 8) {
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    cur[q] = nxt[q];
                             }
                         }
-                    }
+                    };
+                    row(std::true_type{}, 1);
+#pragma unroll 3
+                    for (int i = 1; i < AT; ++i)
+                        row(std::false_type{}, i + 1 < AT ? i + 1 : i);
                 } else {
                     // mask-edge group: each key over its own range of queries
                     int lo_all = AT, hi_all = -1;
@@ -2588,9 +2635,9 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
                         const float4 sw = *reinterpret_cast<const float4*>(S + i * BT_P);
                         const float4 aw = *reinterpret_cast<const float4*>(A + i * BT_P);
                         const ulonglong2 q01 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD);
-                        const ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD + 4);
+                        const ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD + HD / 2);
                         const ulonglong2 g01 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD);
-                        const ulonglong2 g23 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD + 4);
+                        const ulonglong2 g23 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD + HD / 2);
                         const float ws[4] = {sw.x, sw.y, sw.z, sw.w}, wa[4] = {aw.x, aw.y, aw.z, aw.w};
                         const u64 DQ[4] = {q01.x, q01.y, q23.x, q23.y}, DG[4] = {g01.x, g01.y, g23.x, g23.y};
 #pragma unroll
@@ -2630,15 +2677,15 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
             const int64_t j = j0 + 4 * ty + r;
             if (j >= T)
                 continue;
-            const int64_t off = ((kt.b * a.T + j) * a.Hkv + kt.g) * HD + 8 * tx;
+            const int64_t off = ((kt.b * a.T + j) * a.Hkv + kt.g) * HD + 4 * tx;
             u64 k4[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 k4[q] = fadd2_ftz(fmul2_rn(fk[r][q], cc), z);   // dK = F_K (x) c, flushed
             *reinterpret_cast<ulonglong2*>(a.dk + off) = make_ulonglong2(k4[0], k4[1]);
-            *reinterpret_cast<ulonglong2*>(a.dk + off + 4) = make_ulonglong2(k4[2], k4[3]);
+            *reinterpret_cast<ulonglong2*>(a.dk + off + HD / 2) = make_ulonglong2(k4[2], k4[3]);
             *reinterpret_cast<ulonglong2*>(a.dv + off) = make_ulonglong2(fv[r][0], fv[r][1]);
-            *reinterpret_cast<ulonglong2*>(a.dv + off + 4) = make_ulonglong2(fv[r][2], fv[r][3]);
+            *reinterpret_cast<ulonglong2*>(a.dv + off + HD / 2) = make_ulonglong2(fv[r][2], fv[r][3]);
         }
     }
     if (lt == 0)
