@@ -26,6 +26,7 @@
 //     sequence) runs both passes; pass 2 reads the cached logits or recomputes
 //     them, and P.V runs on dp4a (exact int32).  Logits: 256 threads own 4 x 4
 //     outputs each, packed f32x2 products over d with the chunk-of-64 order.
+#include <climits>
 #include <type_traits>
 
 #include "bwd_tile.cuh"
@@ -2139,6 +2140,29 @@ __global__ void k_attn_bimg(const AttnBwdImg a)
     }
 }
 
+// fx(v) = the nearest int64 to v (x) 2^48, ties to even, saturating -- what
+// the 64-bit rounding conversion gives, built from the float's bits with
+// 32-bit integer operations (the 64-bit conversion runs on the FP64 pipe).
+// y = RN(v (x) 2^48) is exact for a flushed v unless it overflows.  With
+// biased exponent e: below 150 (|y| < 2^23) the 32-bit rounding conversion is
+// exact; from 150 to 189 y is the integer significand (x) 2^(e - 150) < 2^63;
+// from 190 (|y| >= 2^63, or infinite) it saturates, and NaN gives 0.  Chosen
+// per lane without branches
+__device__ __forceinline__ unsigned long long fx48(float v)
+{
+    const float y = fmul_rn(v, 0x1p48f);
+    const uint32_t u = __float_as_uint(y);
+    const int e = (int)((u >> 23) & 0xffu);
+    const bool neg = (u >> 31) != 0;
+    const long long small = (long long)__float2int_rn(y);
+    const long long mag = (long long)((u & 0x7fffffu) | 0x800000u) << min(max(e - 150, 0), 39);
+    const long long big = neg ? -mag : mag;
+    long long sat = neg ? LLONG_MIN : LLONG_MAX;
+    if (e == 255 && (u & 0x7fffffu) != 0)
+        sat = 0;
+    return (unsigned long long)(e < 150 ? small : (e < 190 ? big : sat));
+}
+
 struct AttnDqArgs {
     const float* st;     // dS tiles
     const float* krow;   // flushed K rows
@@ -2152,7 +2176,7 @@ struct AttnDqArgs {
 constexpr int DQ_STAGE = (int)(BT_TILE + ROW_TILE);   // one dS tile and its K rows
 constexpr size_t DQ_SMEM = 2 * (size_t)DQ_STAGE;
 
-// dQ of one query tile at a time per CTA (256 threads, one CTA per SM): a thread owns
+// dQ of one query tile at a time per CTA (256 threads, two CTAs per SM): a thread owns
 // rows 4ty .. 4ty+3 and columns 4tx .. 4tx+3 and 64 + 4tx .. 64 + 4tx+3 (one
 // 16-byte load each, contiguous across the warp: no bank conflicts) as four
 // packed pairs along d, so a pair shares its row and its keys.  Per key tile: the left-to-right sum
@@ -2161,11 +2185,12 @@ constexpr size_t DQ_SMEM = 2 * (size_t)DQ_STAGE;
 // dQ = fix2f(sum) (x) c.  The dS tile and the key tile's K rows arrive by bulk
 // copies into a two-stage ring released per warp; query tiles come from a
 // counter, longest windows first
-__global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
+__global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
 {
     extern __shared__ __align__(128) uint8_t smq[];
     __shared__ uint64_t full[2], empty[2];
     __shared__ int64_t queue[8];
+    __shared__ uint32_t tmem_slot;
     const int lt = threadIdx.x, lane = lt & 31;
     const int ty = lt >> 4, tx = lt & 15;
     if (lt == 0) {
@@ -2175,7 +2200,20 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (lt < 32) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
+                         su32(&tmem_slot))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
     __syncthreads();
+    fence_after();
+    // this thread's 32 fixed-point sums live in its own tensor-memory lane:
+    // lane 32 (warp % 4) + lane, columns 64 (warp / 4) .. + 63 (two 32-bit
+    // columns per sum), keeping registers for two CTAs per SM
+    const uint32_t tacc =
+        tmem_slot + ((uint32_t)(32 * ((lt >> 5) & 3)) << 16) + (uint32_t)(64 * (lt >> 7));
     const int T = (int)a.T, W = (int)a.W;
     auto tile_of = [&](const QTile& q, int t) {   // the cache tile of (query tile q, key tile t)
         return ((q.b * a.Hq + q.h) * a.tiles_bh + tile_prefix(q.i0 / AT, W)) + (t - q.t_lo);
@@ -2245,12 +2283,6 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
         if (dead || item < 0)
             break;
         const QTile qt = qtile(item);
-        unsigned long long acc[4][8];   // fixed-point sums, wrapping like the int64 adds they replace
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                acc[r][e] = 0ull;
         for (int t = qt.t_lo; t <= qt.t_hi; ++t) {
             const int s = used & 1;
             if (lt == 0 && used >= 1 && issued == used + 1 && have) {
@@ -2376,36 +2408,64 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdq(const AttnDqArgs a)
             if (lane == 0)
                 mbar_arrive(&empty[s]);
             ++used;
+            // the tile partials into the fixed-point sums (wrapping like the
+            // int64 adds they replace); rows without keys here add nothing
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                if (jb[r] > je[r])
-                    continue;
+            for (int hf = 0; hf < 2; ++hf) {   // rows 2hf, 2hf + 1: 16 sums, 32 columns
+                u64 f[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float v0, v1;
-                    unpack2(pp[r][q], v0, v1);
-                    acc[r][2 * q] += (unsigned long long)__float2ll_rn(fmul_rn(v0, 0x1p48f));
-                    acc[r][2 * q + 1] += (unsigned long long)__float2ll_rn(fmul_rn(v1, 0x1p48f));
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int r = 2 * hf + rr;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float v0, v1;
+                        unpack2(pp[r][q], v0, v1);
+                        const bool any = jb[r] <= je[r];
+                        f[8 * rr + 2 * q] = any ? fx48(v0) : 0ull;
+                        f[8 * rr + 2 * q + 1] = any ? fx48(v1) : 0ull;
+                    }
                 }
+                if (t != qt.t_lo) {
+                    uint32_t w[32];
+                    tmem_ld32(tacc + 32 * hf, w);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        f[e] += (u64)w[2 * e] | ((u64)w[2 * e + 1] << 32);
+                }
+                tmem_st32(tacc + 32 * hf, f);
             }
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t w[32];
+            tmem_ld32(tacc + 32 * hf, w);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+            const int r = 2 * hf + rr;
             const int64_t i = qt.i0 + 4 * ty + r;
             if (i >= T)
                 continue;
             float o[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                o[e] = fmul_flush(flush(fmul_rn(__ll2float_rn((long long)acc[r][e]), 0x1p-48f)), a.c);
+            for (int e = 0; e < 8; ++e) {
+                const long long acc = (long long)((u64)w[2 * (8 * rr + e)] | ((u64)w[2 * (8 * rr + e) + 1] << 32));
+                o[e] = fmul_flush(flush(fmul_rn(__ll2float_rn(acc), 0x1p-48f)), a.c);
+            }
             float* dst = a.dq + ((qt.b * a.T + i) * a.Hq + qt.h) * HD + 4 * tx;
             *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<float4*>(dst + HD / 2) = make_float4(o[4], o[5], o[6], o[7]);
+            }
         }
     }
     if (lt == 0)
         while (used < issued && mbar_wait(&full[used & 1], (used >> 1) & 1))
             ++used;
+    fence_before();
+    __syncthreads();
+    if (lt < 32) {
+        fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem_slot) : "memory");
+    }
     if (fail)
         atomicExch(a.err, 1);
 }
@@ -2854,7 +2914,7 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
         e = cudaFuncSetAttribute(k_attn_bdq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DQ_SMEM);
         if (e != cudaSuccess)
             return e;
-        k_attn_bdq<<<(unsigned)std::min<int64_t>(num_sms(), items), NT, DQ_SMEM, st>>>(qa);
+        k_attn_bdq<<<(unsigned)std::min<int64_t>(2 * (int64_t)num_sms(), items), NT, DQ_SMEM, st>>>(qa);
         count_launches(1);
         // dK and dV per key tile
         AttnDkvArgs ka;

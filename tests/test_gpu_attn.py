@@ -173,6 +173,27 @@ def test_attn_bwd_windows_around_tile_multiples(orc, B, T, Hq, Hkv, W, logits):
 
 
 @pytest.mark.parametrize("W", [0, 100])
+def test_attn_bwd_fixed_point_magnitudes(orc, W):
+    # key rows scaled by powers of two from 2^-40 to 2^12, so the dQ tile
+    # partials T span the fixed-point conversion's ranges: |T 2^48| below 2^23
+    # (rounded to the nearest integer, ties to even) and far above it (exact);
+    # every dQ bit must still match the oracle's int64 sums
+    B, T, Hq, Hkv = 1, 150, 2, 1
+    q, k, vq, s_v = _case(171 + W, B, T, Hq, Hkv)
+    q *= np.float32(2.0 ** -12)            # the logits stay moderate despite the scaling
+    k *= np.exp2(np.arange(T) % 53 - 40).astype(np.float32)[None, :, None, None]
+    o, m, l, fwd_ws = gpu_attn_fwd(q, k, vq, s_v, W, keep_cache=True)
+    dout = np.random.default_rng(17).standard_normal(o.shape).astype(np.float32)
+    rq, rk, rv = orc.attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    assert np.abs(rq).max() > 1.0 and np.abs(rq[rq != 0]).min() < 2.0 ** -30
+    for fws in (fwd_ws, None):
+        dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=fws)
+        G.assert_bits_equal(dq, rq, "dq")
+        G.assert_bits_equal(dk, rk, "dk")
+        G.assert_bits_equal(dv, rv, "dv")
+
+
+@pytest.mark.parametrize("W", [0, 100])
 def test_attn_bwd_underflowing_probabilities(orc, W):
     # logits spread over hundreds: most p underflow to 0, so a and dS are
     # exact zeros and many backward terms are signed zeros, which the canonical
