@@ -20,7 +20,7 @@
 // the canonical-order chunk/tree stack (one thread per row) and accumulates
 // P.V exactly.  Two routes:
 //   * with the logit cache and a device whose tensor-core exactness check has
-//     passed (the default): k_attn_logits (pass 1) and k_attn_pv (pass 2, P.V
+//     passed (the default): k_attn_rows<false> (pass 1) and k_attn_pv (pass 2, P.V
 //     on the tensor cores), described before them below;
 //   * otherwise k_attn_fwd: one CTA per (64-row query tile, query head,
 //     sequence) runs both passes; pass 2 reads the cached logits or recomputes
@@ -591,9 +591,10 @@ __global__ void __launch_bounds__(NT, 2) k_attn_fwd(const AttnFwdArgs a)
 // ---------------------------------------------------------------------------
 // Default forward route (logit cache and tensor-core P.V), two kernels.
 //
-// k_attn_logits: pass 1 -- every logit of the window written to the cache and
+// k_attn_rows<false>: pass 1 -- every logit of the window written to the cache and
 // the exact row maxima written to m -- as a banded product in the canonical
-// order over d.  A CTA holds two groups of 128 threads; each group takes its
+// order over d.  (k_attn_rows<true> is the backward's dA / a / dS pass: the
+// same product of dO and V^, described with the backward below.)  A CTA holds two groups of 128 threads; each group takes its
 // own query tiles (64 rows, one head, one sequence) in turn.  A thread owns 8
 // rows x 4 keys of a 64 x 64 tile (rows as packed pairs: the tile of the
 // linear backward, bwd_tile.cuh), so it loads 12 floats per 32 outputs per d.
@@ -623,7 +624,7 @@ static_assert(LG_GROUP_BYTES % 128 == 0, "group layout alignment");
 
 // K^T image: tile (b, g, t) holds the flushed K[b, 64 t + key, g, d] at
 // [d][key] (keys at or past T are 0).  One thread moves one float4 of d.
-// Also zeroes the work counter of k_attn_logits
+// Also zeroes the work counter of k_attn_rows<false>
 __global__ void k_attn_kimg(const float* __restrict__ k, float* __restrict__ img, int64_t T,
                             int64_t Hkv, int64_t nkt, int64_t n, unsigned long long* counter)
 {
