@@ -2628,91 +2628,110 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
                         ib[r] = AT, ie[r] = -1;
                     whole = whole && ib[r] == 0 && ie[r] == AT - 1;
                 }
+                // one path per warp (the edge path's warp reductions need every lane)
+                whole = __all_sync(0xffffffffu, whole);
                 u64 pk[4][4], pv[4][4];
-                if (whole) {
-                    float4 sw = *reinterpret_cast<const float4*>(S);
-                    float4 aw = *reinterpret_cast<const float4*>(A);
-                    ulonglong2 q01 = *reinterpret_cast<const ulonglong2*>(Qr);
-                    ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(Qr + HD / 2);
-                    ulonglong2 g01 = *reinterpret_cast<const ulonglong2*>(Gr);
-                    ulonglong2 g23 = *reinterpret_cast<const ulonglong2*>(Gr + HD / 2);
-                    // one query row: the 8 (key, tensor) rows of products, those of
-                    // row x + 1 formed before the adds of row x; FIRST seeds the
-                    // sums with the flushed products
-                    auto row = [&](auto first_tag, int in) {
-                        constexpr bool FIRST = decltype(first_tag)::value;
-                        const float w8[8] = {sw.x, sw.y, sw.z, sw.w, aw.x, aw.y, aw.z, aw.w};
-                        const u64 DQ[4] = {q01.x, q01.y, q23.x, q23.y}, DG[4] = {g01.x, g01.y, g23.x, g23.y};
-                        sw = *reinterpret_cast<const float4*>(S + in * BT_P);
-                        aw = *reinterpret_cast<const float4*>(A + in * BT_P);
-                        q01 = *reinterpret_cast<const ulonglong2*>(Qr + in * HD);
-                        q23 = *reinterpret_cast<const ulonglong2*>(Qr + in * HD + HD / 2);
-                        g01 = *reinterpret_cast<const ulonglong2*>(Gr + in * HD);
-                        g23 = *reinterpret_cast<const ulonglong2*>(Gr + in * HD + HD / 2);
-                        u64 cur[4];
-                        {
-                            const u64 P = pack2(w8[0], w8[0]);
+                // operands of the next query row, loaded one row ahead
+                float4 sw, aw;
+                ulonglong2 q01, q23, g01, g23;
+                auto load = [&](int i) {
+                    sw = *reinterpret_cast<const float4*>(S + i * BT_P);
+                    aw = *reinterpret_cast<const float4*>(A + i * BT_P);
+                    q01 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD);
+                    q23 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD + HD / 2);
+                    g01 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD);
+                    g23 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD + HD / 2);
+                };
+                // one query row with every key valid: the 8 (key, tensor) rows of
+                // products, those of row x + 1 formed before the adds of row x;
+                // FIRST seeds the sums with the flushed products; then row `in`
+                // is loaded
+                auto row = [&](auto first_tag, int in) {
+                    constexpr bool FIRST = decltype(first_tag)::value;
+                    const float w8[8] = {sw.x, sw.y, sw.z, sw.w, aw.x, aw.y, aw.z, aw.w};
+                    const u64 DQ[4] = {q01.x, q01.y, q23.x, q23.y}, DG[4] = {g01.x, g01.y, g23.x, g23.y};
+                    load(in);
+                    u64 cur[4];
+                    {
+                        const u64 P = pack2(w8[0], w8[0]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            cur[q] = fmul2_rn(P, DQ[q]);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) {
+                        u64 nxt[4];
+                        if (x + 1 < 8) {
+                            const u64 P = pack2(w8[x + 1], w8[x + 1]);
 #pragma unroll
                             for (int q = 0; q < 4; ++q)
-                                cur[q] = fmul2_rn(P, DQ[q]);
+                                nxt[q] = fmul2_rn(P, x + 1 < 4 ? DQ[q] : DG[q]);
                         }
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) {
-                            u64 nxt[4];
-                            if (x + 1 < 8) {
-                                const u64 P = pack2(w8[x + 1], w8[x + 1]);
-#pragma unroll
-                                for (int q = 0; q < 4; ++q)
-                                    nxt[q] = fmul2_rn(P, x + 1 < 4 ? DQ[q] : DG[q]);
-                            }
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                u64& acc = x < 4 ? pk[x][q] : pv[x - 4][q];
-                                acc = FIRST ? fadd2_ftz(cur[q], z) : fadd2_ftz(acc, cur[q]);
-                            }
-                            if (x + 1 < 8) {
-#pragma unroll
-                                for (int q = 0; q < 4; ++q)
-                                    cur[q] = nxt[q];
-                            }
+                        for (int q = 0; q < 4; ++q) {
+                            u64& acc = x < 4 ? pk[x][q] : pv[x - 4][q];
+                            acc = FIRST ? fadd2_ftz(cur[q], z) : fadd2_ftz(acc, cur[q]);
                         }
-                    };
+                        if (x + 1 < 8) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                cur[q] = nxt[q];
+                        }
+                    }
+                };
+                if (whole) {
+                    load(0);
                     row(std::true_type{}, 1);
 #pragma unroll 3
                     for (int i = 1; i < AT; ++i)
                         row(std::false_type{}, i + 1 < AT ? i + 1 : i);
                 } else {
-                    // mask-edge group: each key over its own range of queries
-                    int lo_all = AT, hi_all = -1;
+                    // mask-edge group: each key over its own range of queries.
+                    // Rows where all four keys of every thread of the warp are
+                    // valid and already seeded take the packed rows without
+                    // tests (same operations); the ragged ends keep them
+                    int lo_all = AT, hi_all = -1, mid_lo = 0, mid_hi = AT - 1;
 #pragma unroll
                     for (int r = 0; r < 4; ++r) {
                         lo_all = min(lo_all, ib[r]);
                         hi_all = max(hi_all, ie[r]);
+                        mid_lo = max(mid_lo, ib[r] + 1);
+                        mid_hi = min(mid_hi, ie[r]);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
                             pk[r][q] = pv[r][q] = 0ull;
                     }
-                    for (int i = lo_all; i <= hi_all; ++i) {
-                        const float4 sw = *reinterpret_cast<const float4*>(S + i * BT_P);
-                        const float4 aw = *reinterpret_cast<const float4*>(A + i * BT_P);
-                        const ulonglong2 q01 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD);
-                        const ulonglong2 q23 = *reinterpret_cast<const ulonglong2*>(Qr + i * HD + HD / 2);
-                        const ulonglong2 g01 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD);
-                        const ulonglong2 g23 = *reinterpret_cast<const ulonglong2*>(Gr + i * HD + HD / 2);
-                        const float ws[4] = {sw.x, sw.y, sw.z, sw.w}, wa[4] = {aw.x, aw.y, aw.z, aw.w};
-                        const u64 DQ[4] = {q01.x, q01.y, q23.x, q23.y}, DG[4] = {g01.x, g01.y, g23.x, g23.y};
+                    lo_all = __reduce_min_sync(0xffffffffu, lo_all);
+                    hi_all = __reduce_max_sync(0xffffffffu, hi_all);
+                    mid_lo = __reduce_max_sync(0xffffffffu, mid_lo);
+                    mid_hi = __reduce_min_sync(0xffffffffu, mid_hi);
+                    auto edge = [&](int from, int to) {
+                        for (int i = from; i <= to; ++i) {
+                            load(i);
+                            const float ws[4] = {sw.x, sw.y, sw.z, sw.w}, wa[4] = {aw.x, aw.y, aw.z, aw.w};
+                            const u64 DQ[4] = {q01.x, q01.y, q23.x, q23.y}, DG[4] = {g01.x, g01.y, g23.x, g23.y};
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) {
-                            if (i < ib[r] || i > ie[r])
-                                continue;
-                            const u64 PS = pack2(ws[r], ws[r]), PA = pack2(wa[r], wa[r]);
+                            for (int r = 0; r < 4; ++r) {
+                                if (i < ib[r] || i > ie[r])
+                                    continue;
+                                const u64 PS = pack2(ws[r], ws[r]), PA = pack2(wa[r], wa[r]);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const u64 xk = fmul2_rn(PS, DQ[q]), xv = fmul2_rn(PA, DG[q]);
-                                pk[r][q] = i == ib[r] ? fadd2_ftz(xk, z) : fadd2_ftz(pk[r][q], xk);
-                                pv[r][q] = i == ib[r] ? fadd2_ftz(xv, z) : fadd2_ftz(pv[r][q], xv);
+                                for (int q = 0; q < 4; ++q) {
+                                    const u64 xk = fmul2_rn(PS, DQ[q]), xv = fmul2_rn(PA, DG[q]);
+                                    pk[r][q] = i == ib[r] ? fadd2_ftz(xk, z) : fadd2_ftz(pk[r][q], xk);
+                                    pv[r][q] = i == ib[r] ? fadd2_ftz(xv, z) : fadd2_ftz(pv[r][q], xv);
+                                }
                             }
                         }
+                    };
+                    if (mid_lo <= mid_hi) {
+                        edge(lo_all, mid_lo - 1);
+                        load(mid_lo);
+                        for (int i = mid_lo; i <= mid_hi; ++i)
+                            row(std::false_type{}, i + 1 <= mid_hi ? i + 1 : i);
+                        edge(mid_hi + 1, hi_all);
+                    } else {
+                        edge(lo_all, hi_all);
                     }
                 }
                 __syncwarp();
