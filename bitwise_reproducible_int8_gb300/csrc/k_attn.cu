@@ -2309,100 +2309,107 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
                     jb[r] = AT, je[r] = -1;
                 whole = whole && jb[r] == 0 && je[r] == AT - 1;
             }
+            // one path per warp (the edge path's warp reductions need every lane)
+            whole = __all_sync(0xffffffffu, whole);
             u64 pp[4][4];   // [row][pair of columns]
-            if (whole) {
-                float sv[4];
-                ulonglong2 k01, k23;
+            // operands of the next key, loaded one key ahead
+            float sv[4];
+            ulonglong2 k01, k23;
+            auto load = [&](int j) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r)
-                    sv[r] = S[r * BT_P];
-                k01 = *reinterpret_cast<const ulonglong2*>(Kr);
-                k23 = *reinterpret_cast<const ulonglong2*>(Kr + HD / 2);
+                    sv[r] = S[r * BT_P + j];
+                k01 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD);
+                k23 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD + HD / 2);
+            };
+            // one key with every row valid: the products of row r + 1 formed
+            // before the adds of row r, so no add waits on the multiply just
+            // issued; FIRST seeds the sums with the flushed products; then key
+            // `jn` is loaded
+            auto key = [&](auto first_tag, int jn) {
+                constexpr bool FIRST = decltype(first_tag)::value;
+                const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
+                const float c4[4] = {sv[0], sv[1], sv[2], sv[3]};
+                load(jn);
+                u64 cur[4];
                 {
-                    const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
-                    float c4[4];
+                    const u64 P = pack2(c4[0], c4[0]);
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        c4[r] = sv[r];
-                        sv[r] = S[r * BT_P + 1];
-                    }
-                    k01 = *reinterpret_cast<const ulonglong2*>(Kr + HD);
-                    k23 = *reinterpret_cast<const ulonglong2*>(Kr + HD + HD / 2);
+                    for (int q = 0; q < 4; ++q)
+                        cur[q] = fmul2_rn(P, D[q]);
+                }
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const u64 P = pack2(c4[r], c4[r]);
+                for (int r = 0; r < 4; ++r) {
+                    u64 nxt[4];
+                    if (r + 1 < 4) {
+                        const u64 P = pack2(c4[r + 1], c4[r + 1]);
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
-                            pp[r][q] = fadd2_ftz(fmul2_rn(P, D[q]), z);
+                            nxt[q] = fmul2_rn(P, D[q]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        pp[r][q] = FIRST ? fadd2_ftz(cur[q], z) : fadd2_ftz(pp[r][q], cur[q]);
+                    if (r + 1 < 4) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            cur[q] = nxt[q];
                     }
                 }
+            };
+            if (whole) {
+                load(0);
+                key(std::true_type{}, 1);
 #pragma unroll 7
-                for (int j = 1; j < AT; ++j) {
-                    const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
-                    float c4[4];
-                    const int jn = j + 1 < AT ? j + 1 : j;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        c4[r] = sv[r];
-                        sv[r] = S[r * BT_P + jn];
-                    }
-                    k01 = *reinterpret_cast<const ulonglong2*>(Kr + jn * HD);
-                    k23 = *reinterpret_cast<const ulonglong2*>(Kr + jn * HD + HD / 2);
-                    // the products of row r + 1 are formed before the adds of row
-                    // r, so no add waits on the multiply just issued
-                    u64 cur[4];
-                    {
-                        const u64 P = pack2(c4[0], c4[0]);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            cur[q] = fmul2_rn(P, D[q]);
-                    }
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        u64 nxt[4];
-                        if (r + 1 < 4) {
-                            const u64 P = pack2(c4[r + 1], c4[r + 1]);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                nxt[q] = fmul2_rn(P, D[q]);
-                        }
-#pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            pp[r][q] = fadd2_ftz(pp[r][q], cur[q]);
-                        if (r + 1 < 4) {
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                cur[q] = nxt[q];
-                        }
-                    }
-                }
+                for (int j = 1; j < AT; ++j)
+                    key(std::false_type{}, j + 1 < AT ? j + 1 : j);
             } else {
-                // mask-edge tile: each row over its own range of keys
-                int lo_all = AT, hi_all = -1;
+                // mask-edge tile: each row over its own range of keys.  Keys
+                // where all four rows of every thread of the warp are valid and
+                // already seeded take the packed keys without tests (same
+                // operations); the ragged ends keep them
+                int lo_all = AT, hi_all = -1, mid_lo = 0, mid_hi = AT - 1;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     lo_all = min(lo_all, jb[r]);
                     hi_all = max(hi_all, je[r]);
+                    mid_lo = max(mid_lo, jb[r] + 1);
+                    mid_hi = min(mid_hi, je[r]);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         pp[r][q] = 0ull;
                 }
-                for (int j = lo_all; j <= hi_all; ++j) {
-                    const ulonglong2 k01 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD);
-                    const ulonglong2 k23 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD + HD / 2);
-                    const u64 D[4] = {k01.x, k01.y, k23.x, k23.y};
+                lo_all = __reduce_min_sync(0xffffffffu, lo_all);
+                hi_all = __reduce_max_sync(0xffffffffu, hi_all);
+                mid_lo = __reduce_max_sync(0xffffffffu, mid_lo);
+                mid_hi = __reduce_min_sync(0xffffffffu, mid_hi);
+                auto edge = [&](int from, int to) {
+                    for (int j = from; j <= to; ++j) {
+                        const ulonglong2 e01 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD);
+                        const ulonglong2 e23 = *reinterpret_cast<const ulonglong2*>(Kr + j * HD + HD / 2);
+                        const u64 D[4] = {e01.x, e01.y, e23.x, e23.y};
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        if (j < jb[r] || j > je[r])
-                            continue;
-                        const float sv = S[r * BT_P + j];
-                        const u64 P = pack2(sv, sv);
+                        for (int r = 0; r < 4; ++r) {
+                            if (j < jb[r] || j > je[r])
+                                continue;
+                            const float w = S[r * BT_P + j];
+                            const u64 P = pack2(w, w);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const u64 pr = fmul2_rn(P, D[q]);
-                            pp[r][q] = j == jb[r] ? fadd2_ftz(pr, z) : fadd2_ftz(pp[r][q], pr);
+                            for (int q = 0; q < 4; ++q) {
+                                const u64 pr = fmul2_rn(P, D[q]);
+                                pp[r][q] = j == jb[r] ? fadd2_ftz(pr, z) : fadd2_ftz(pp[r][q], pr);
+                            }
                         }
                     }
+                };
+                if (mid_lo <= mid_hi) {
+                    edge(lo_all, mid_lo - 1);
+                    load(mid_lo);
+                    for (int j = mid_lo; j <= mid_hi; ++j)
+                        key(std::false_type{}, j + 1 <= mid_hi ? j + 1 : j);
+                    edge(mid_hi + 1, hi_all);
+                } else {
+                    edge(lo_all, hi_all);
                 }
             }
             __syncwarp();
