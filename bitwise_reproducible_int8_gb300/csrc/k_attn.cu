@@ -1421,9 +1421,11 @@ __global__ void __launch_bounds__(PV_NTH, 2) k_attn_pv(const AttnPVArgs pa)
 //           a_ij (x) dO_id over the query heads of kv head g (ascending) and
 //           the 64-aligned query tiles (ascending), each tile summed left to
 //           right from its first valid term, the tile partials folded left.
-// k_attn_bwd: one CTA per (64-key tile, kv head, sequence) visits its query
-// tiles in that order, so dK and dV stay in registers; dQ tile partials go
-// to an int64 accumulator with atomicAdd and are converted at the end.
+// k_attn_bwd (the route without the forward's cache): one CTA per (64-key
+// tile, kv head, sequence) recomputes the logits and visits its query tiles
+// in that order, so dK and dV stay in tensor memory; dQ tile partials go to
+// an int64 accumulator with atomicAdd and are converted at the end.  With the
+// cache the three kernels further below take its place.
 // ---------------------------------------------------------------------------
 
 constexpr int PR = 132;   // pitch (floats) of the row-major 64 x 128 tiles
@@ -1440,7 +1442,6 @@ struct AttnBwdArgs {
     unsigned long long* dq_acc;
     float* dk;
     float* dv;
-    const float* lcache;   // optional: the forward's logit cache for these inputs
     int64_t T, Hq, Hkv, W;
     int64_t tiles_bh;
     float c;
@@ -1693,26 +1694,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
             // a and dS for the 64 x 64 pairs (query row ty+16r, key tx+16cc)
             {
                 float sv[4][4], dav[4][4];
-                if (a.lcache) {
-                    // the forward's cache of this (query tile, key tile), which holds
-                    // p_ij = e^(s_ij - m_i) once the forward has run: forward thread
-                    // f = (i/4)*16 + j/4 keeps pair (i, j) at float
-                    // f*16 + 2*(((i%4)/2)*4 + j%4) + i%2
-                    const int64_t qt = i0 / AT;
-                    const int64_t tlo = (W > 0 ? max((int64_t)0, i0 - W + 1) : (int64_t)0) / AT;
-                    const float* tile = a.lcache + ((b * Hq + h) * a.tiles_bh + tile_prefix(qt, W) +
-                                                    (j0 / AT - tlo)) * (AT * AT);
-#pragma unroll
-                    for (int r = 0; r < 4; ++r)
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const int ir = ty + 16 * r, jc = tx + 16 * cc;
-                            const int f = (ir >> 2) * 16 + (jc >> 2);
-                            sv[r][cc] = tile[f * 16 + 2 * (((ir & 3) >> 1) * 4 + (jc & 3)) + (ir & 1)];
-                        }
-                } else {
-                    tile_dot(sv, Qs, Ks, ty, tx);
-                }
+                tile_dot(sv, Qs, Ks, ty, tx);
                 tile_dot(dav, Gs, Vs, ty, tx);
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -1724,9 +1706,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                         const int64_t j = j0 + jc;
                         float av = 0.f, dsv = 0.f;
                         if (i < T && j <= i && (W == 0 || i - j < W)) {
-                            // with the forward's cache, sv already holds p
-                            const float p = a.lcache ? sv[r][cc]
-                                                     : exp_r(fadd_ftz(fmul_flush(sv[r][cc], c), -rm[ir]));
+                            const float p = exp_r(fadd_ftz(fmul_flush(sv[r][cc], c), -rm[ir]));
                             av = flush(__fdiv_rn(p, rl[ir]));
                             dsv = fmul_flush(av, fadd_ftz(dav[r][cc], -rd[ir]));
                         }
@@ -2866,7 +2846,6 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
     a.dq_acc = L.acc;
     a.dk = dk;
     a.dv = dv;
-    a.lcache = static_cast<const float*>(lcache);
     a.T = T;
     a.Hq = Hq;
     a.Hkv = Hkv;
