@@ -26,7 +26,6 @@
 //     sequence) runs both passes; pass 2 reads the cached logits or recomputes
 //     them, and P.V runs on dp4a (exact int32).  Logits: 256 threads own 4 x 4
 //     outputs each, packed f32x2 products over d with the chunk-of-64 order.
-#include <climits>
 #include <type_traits>
 
 #include "bwd_tile.cuh"
@@ -2121,27 +2120,41 @@ __global__ void k_attn_bimg(const AttnBwdImg a)
     }
 }
 
-// fx(v) = the nearest int64 to v (x) 2^48, ties to even, saturating -- what
-// the 64-bit rounding conversion gives, built from the float's bits with
-// 32-bit integer operations (the 64-bit conversion runs on the FP64 pipe).
-// y = RN(v (x) 2^48) is exact for a flushed v unless it overflows.  With
-// biased exponent e: below 150 (|y| < 2^23) the 32-bit rounding conversion is
-// exact; from 150 to 189 y is the integer significand (x) 2^(e - 150) < 2^63;
-// from 190 (|y| >= 2^63, or infinite) it saturates, and NaN gives 0.  Chosen
-// per lane without branches
-__device__ __forceinline__ unsigned long long fx48(float v)
+
+// fx(v) = the nearest int64 to v (x) 2^48, ties to even, saturating, for the
+// two lanes of a pair -- the value of the 64-bit rounding conversion, which
+// runs on the FP64 pipe, built from two 32-bit ones.  For a flushed v,
+// |y| = |v| (x) 2^48 is exact unless it overflows.  |y| = h 2^32 + l with
+// h = trunc(|y| 2^-32) and l = |y| (-) h 2^32, both exact (l is |y| when
+// |y| < 2^32, else a multiple of |y|'s spacing below 2^32), so
+// rn(|y|) = h 2^32 + rn(l) (h 2^32 is even) with h < 2^31 and rn(l) < 2^32;
+// then the sign.  |y| >= 2^63 (or infinite) saturates; NaN converts to 0 in
+// both halves.  No branches
+__device__ __forceinline__ void fx48x2(u64 vv, unsigned long long& r0, unsigned long long& r1)
 {
-    const float y = fmul_rn(v, 0x1p48f);
-    const uint32_t u = __float_as_uint(y);
-    const int e = (int)((u >> 23) & 0xffu);
-    const bool neg = (u >> 31) != 0;
-    const long long small = (long long)__float2int_rn(y);
-    const long long mag = (long long)((u & 0x7fffffu) | 0x800000u) << min(max(e - 150, 0), 39);
-    const long long big = neg ? -mag : mag;
-    long long sat = neg ? LLONG_MIN : LLONG_MAX;
-    if (e == 255 && (u & 0x7fffffu) != 0)
-        sat = 0;
-    return (unsigned long long)(e < 150 ? small : (e < 190 ? big : sat));
+    float v[2];
+    unpack2(vv, v[0], v[1]);
+    float a[2] = {fabsf(v[0]), fabsf(v[1])};
+    unpack2(fmul2_rn(pack2(a[0], a[1]), pack2(0x1p48f, 0x1p48f)), a[0], a[1]);
+    float hs[2];
+    unpack2(fmul2_rn(pack2(a[0], a[1]), pack2(0x1p-32f, 0x1p-32f)), hs[0], hs[1]);
+    const float h0 = truncf(hs[0]), h1 = truncf(hs[1]);
+    float l[2];
+    unpack2(fadd2_ftz(pack2(a[0], a[1]), fmul2_rn(pack2(h0, h1), pack2(-0x1p32f, -0x1p32f))), l[0], l[1]);
+    const float hf[2] = {h0, h1};
+    unsigned long long out[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        const unsigned long long mag =
+            ((unsigned long long)__float2uint_rz(hf[x]) << 32) | (unsigned long long)__float2uint_rn(l[x]);
+        const bool neg = __float_as_uint(v[x]) >> 31;
+        unsigned long long r = neg ? 0ull - mag : mag;
+        if (a[x] >= 0x1p63f)
+            r = neg ? 0x8000000000000000ull : 0x7fffffffffffffffull;
+        out[x] = r;
+    }
+    r0 = out[0];
+    r1 = out[1];
 }
 
 struct AttnDqArgs {
@@ -2182,7 +2195,7 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (lt < 32) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" ::"r"(
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(
                          su32(&tmem_slot))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -2191,10 +2204,13 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
     __syncthreads();
     fence_after();
     // this thread's 32 fixed-point sums live in its own tensor-memory lane:
-    // lane 32 (warp % 4) + lane, columns 64 (warp / 4) .. + 63 (two 32-bit
-    // columns per sum), keeping registers for two CTAs per SM
+    // lane 32 (warp % 4) + lane, columns 128 (warp / 4) .. + 63 (two 32-bit
+    // columns per sum), keeping registers for two CTAs per SM; the next 32
+    // columns park a key tile's 32 partials until the next key tile's loop
+    // converts them (sum v at column 32 (v / 16) + 2 (v % 16), partial v at
+    // 64 + v, v = 8 row + 2 pair + lane)
     const uint32_t tacc =
-        tmem_slot + ((uint32_t)(32 * ((lt >> 5) & 3)) << 16) + (uint32_t)(64 * (lt >> 7));
+        tmem_slot + ((uint32_t)(32 * ((lt >> 5) & 3)) << 16) + (uint32_t)(128 * (lt >> 7));
     const int T = (int)a.T, W = (int)a.W;
     auto tile_of = [&](const QTile& q, int t) {   // the cache tile of (query tile q, key tile t)
         return ((q.b * a.Hq + q.h) * a.tiles_bh + tile_prefix(q.i0 / AT, W)) + (t - q.t_lo);
@@ -2255,6 +2271,26 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
         issue_next();
     }
 
+    // partials v = 4c .. 4c + 3 of the previous key tile, parked in tensor
+    // memory, into the fixed-point sums (the first key tile's start them); a
+    // row without keys there parked +0, which adds nothing
+    auto defer_chunk = [&](int c, bool first) {
+        uint32_t rw[4], sw[8];
+        const uint32_t scol = tacc + 32 * (c >> 2) + 8 * (c & 3);
+        tmem_ld4_ld8(tacc + 64 + 4 * c, rw, scol, sw);
+        u64 fx[4];
+        fx48x2((u64)rw[0] | ((u64)rw[1] << 32), fx[0], fx[1]);
+        fx48x2((u64)rw[2] | ((u64)rw[3] << 32), fx[2], fx[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            u64 f = fx[e];
+            if (!first)
+                f += (u64)sw[2 * e] | ((u64)sw[2 * e + 1] << 32);
+            sw[2 * e] = (uint32_t)f;
+            sw[2 * e + 1] = (uint32_t)(f >> 32);
+        }
+        tmem_st8(scol, sw);
+    };
     uint32_t used = 0;
     bool fail = false, dead = false;
     const u64 z = pack2(-0.0f, -0.0f);
@@ -2337,13 +2373,33 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
                     }
                 }
             };
+            // the previous key tile's partials, converted a chunk at a time
+            // between groups of 8 keys (whole tiles) or before the keys (edge
+            // tiles), so the integer work overlaps the products
+            const bool defer = t > qt.t_lo, pfirst = t - 1 == qt.t_lo;
             if (whole) {
                 load(0);
                 key(std::true_type{}, 1);
-#pragma unroll 7
-                for (int j = 1; j < AT; ++j)
-                    key(std::false_type{}, j + 1 < AT ? j + 1 : j);
+#pragma unroll
+                for (int j = 1; j < 8; ++j)
+                    key(std::false_type{}, j + 1);
+                if (defer)
+                    defer_chunk(0, pfirst);
+#pragma unroll 1
+                for (int g = 1; g < AT / 8; ++g) {
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = 8 * g + jj;
+                        key(std::false_type{}, j + 1 < AT ? j + 1 : j);
+                    }
+                    if (defer)
+                        defer_chunk(g, pfirst);
+                }
             } else {
+                if (defer)
+#pragma unroll 1
+                    for (int c = 0; c < 8; ++c)
+                        defer_chunk(c, pfirst);
                 // mask-edge tile: each row over its own range of keys.  Keys
                 // where all four rows of every thread of the warp are valid and
                 // already seeded take the packed keys without tests (same
@@ -2396,8 +2452,17 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
             if (lane == 0)
                 mbar_arrive(&empty[s]);
             ++used;
-            // the tile partials into the fixed-point sums (wrapping like the
-            // int64 adds they replace); rows without keys here add nothing
+            if (t < qt.t_hi) {
+                // parked for the next key tile's loop
+                const u64 flat[16] = {pp[0][0], pp[0][1], pp[0][2], pp[0][3], pp[1][0], pp[1][1],
+                                      pp[1][2], pp[1][3], pp[2][0], pp[2][1], pp[2][2], pp[2][3],
+                                      pp[3][0], pp[3][1], pp[3][2], pp[3][3]};
+                tmem_st32(tacc + 64, flat);
+                continue;
+            }
+            // the query tile's last key tile: its partials into the fixed-point
+            // sums now (wrapping like the int64 adds they replace); rows
+            // without keys here add nothing
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {   // rows 2hf, 2hf + 1: 16 sums, 32 columns
                 u64 f[16];
@@ -2406,11 +2471,11 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
                     const int r = 2 * hf + rr;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        float v0, v1;
-                        unpack2(pp[r][q], v0, v1);
+                        u64 c0, c1;
+                        fx48x2(pp[r][q], c0, c1);
                         const bool any = jb[r] <= je[r];
-                        f[8 * rr + 2 * q] = any ? fx48(v0) : 0ull;
-                        f[8 * rr + 2 * q + 1] = any ? fx48(v1) : 0ull;
+                        f[8 * rr + 2 * q] = any ? c0 : 0ull;
+                        f[8 * rr + 2 * q + 1] = any ? c1 : 0ull;
                     }
                 }
                 if (t != qt.t_lo) {
@@ -2452,7 +2517,7 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
     __syncthreads();
     if (lt < 32) {
         fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" ::"r"(tmem_slot) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem_slot) : "memory");
     }
     if (fail)
         atomicExch(a.err, 1);
