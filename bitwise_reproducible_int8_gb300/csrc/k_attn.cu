@@ -1834,7 +1834,11 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bwd(const AttnBwdArgs a)
                     unsigned long long* dst = a.dq_acc + ((b * T + i) * Hq + h) * HD + 4 * dg;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const long long fx = __float2ll_rn(fmul_rn(part[r][e], 0x1p48f));
+                        // fx: the 64-bit rounding conversion saturates, and a
+                        // NaN partial adds 0 (that conversion would give the
+                        // minimum)
+                        const float x = part[r][e];
+                        const long long fx = x != x ? 0ll : __float2ll_rn(fmul_rn(x, 0x1p48f));
                         atomicAdd(dst + e, (unsigned long long)fx);
                     }
                 }

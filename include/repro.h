@@ -313,9 +313,10 @@ size_t repro_attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);
  *   dQ_id = fix2f(sum over 64-aligned key tiles t of fx(S_t)) (x) c, where
  *     S_t is the left-to-right sum over the valid keys of tile t of
  *     dS_ij (x) k_jd (seeded with the first term), fx(x) = the nearest int64
- *     to x * 2^48 (ties to even, saturating) and fix2f(A) = i2f(A) * 2^-48,
- *     flushed: the key tiles' partials meet in 64-bit fixed point, exactly
- *     and in any order;
+ *     to x * 2^48 (ties to even, saturating, NaN to 0) and
+ *     fix2f(A) = i2f(A) * 2^-48, flushed: the key tiles' partials meet in
+ *     64-bit fixed point, exactly and in any order (the int64 sum wraps
+ *     modulo 2^64 if saturated partials overflow it);
  *   dK_jd = F_K (x) c and dV_jd = F_V, where the terms dS_ij (x) q_id (F_K)
  *     and a_ij (x) dO_id (F_V) run over the query heads of kv head g in
  *     ascending order and, within a head, over the valid queries i, grouped

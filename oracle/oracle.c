@@ -586,9 +586,10 @@ void oracle_attn_fwd_rows(const float* q, const float* k, const int8_t* vq, floa
 /*   dQ_id = (fix2f(sum over key tiles t of fx(T_t))) (x) c, where T_t is the */
 /*     left-to-right sum over the valid keys j of the 64-aligned key tile t   */
 /*     of dS_ij (x) k_jd (seeded with the first such term), fx(x) = the       */
-/*     nearest int64 to x * 2^48 (ties to even, saturating) and fix2f(A) =    */
-/*     flush(i2f(A) * 2^-48): the tile partials are accumulated in 64-bit     */
-/*     fixed point, exactly and in any order;                                 */
+/*     nearest int64 to x * 2^48 (ties to even, saturating, NaN to 0) and     */
+/*     fix2f(A) = flush(i2f(A) * 2^-48): the tile partials are accumulated in */
+/*     64-bit fixed point, exactly and in any order (the int64 sum wraps      */
+/*     modulo 2^64 where saturated partials overflow it);                     */
 /*   dK_jd = (fold) (x) c and dV_jd = (fold), where the terms dS_ij (x) q_id  */
 /*     (dK) and a_ij (x) dO_id (dV) run over the query heads h of kv head g   */
 /*     in ascending order and, within a head, over the valid queries i;       */
@@ -601,6 +602,8 @@ void oracle_attn_fwd_rows(const float* q, const float* k, const int8_t* vq, floa
 int64_t oracle_attn_fx(float x)
 {
     const double v = nearbyint((double)oracle_flush(x) * 281474976710656.0); /* exact */
+    if (v != v)
+        return 0; /* NaN */
     if (v >= 9223372036854775807.0)
         return INT64_MAX;
     if (v <= -9223372036854775808.0)
@@ -647,7 +650,7 @@ static void attn_dq_row(const float* q, const float* k, const int8_t* vq, float 
     const float c = attn_c(D);
     float* tmp = (float*)malloc((size_t)D * sizeof(float));
     float* part = (float*)malloc((size_t)D * sizeof(float));
-    int64_t* acc = (int64_t*)calloc((size_t)D, sizeof(int64_t));
+    uint64_t* acc = (uint64_t*)calloc((size_t)D, sizeof(uint64_t)); /* wraps modulo 2^64 */
     const float drow = attn_drow(o, dout, r, D, tmp);
     for (int64_t t0 = (lo / ATTN_TILE) * ATTN_TILE; t0 <= i; t0 += ATTN_TILE) {
         const int64_t jb = t0 > lo ? t0 : lo, je = t0 + ATTN_TILE - 1 < i ? t0 + ATTN_TILE - 1 : i;
@@ -662,10 +665,13 @@ static void attn_dq_row(const float* q, const float* k, const int8_t* vq, float 
             }
         }
         for (int64_t d = 0; d < D; ++d)
-            acc[d] += oracle_attn_fx(part[d]);
+            acc[d] += (uint64_t)oracle_attn_fx(part[d]);
     }
-    for (int64_t d = 0; d < D; ++d)
-        dq[d] = oracle_mul(oracle_attn_fix2f(acc[d]), c);
+    for (int64_t d = 0; d < D; ++d) {
+        int64_t a;
+        memcpy(&a, &acc[d], sizeof a); /* the two's-complement value */
+        dq[d] = oracle_mul(oracle_attn_fix2f(a), c);
+    }
     free(tmp);
     free(part);
     free(acc);

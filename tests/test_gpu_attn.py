@@ -194,6 +194,38 @@ def test_attn_bwd_fixed_point_magnitudes(orc, W):
 
 
 @pytest.mark.parametrize("W", [0, 100])
+def test_attn_bwd_fixed_point_saturation_and_nan(orc, W):
+    # dQ partials beyond the fixed point's range: every third key row scaled
+    # by 2^24 (q scaled down so the logits stay moderate), so tile partials
+    # reach |T 2^48| >= 2^63 and saturate, and a row's saturated partials of
+    # one sign wrap its int64 sum; one dO element is infinite, so that row's
+    # dS and dQ partials are NaN and convert to 0.  dQ matches the oracle bit
+    # for bit on both routes; dK and dV, which carry the NaNs, are NaN in the
+    # same places and bit-identical elsewhere
+    B, T, Hq, Hkv = 1, 200, 2, 1
+    q, k, vq, s_v = _case(303 + W, B, T, Hq, Hkv)
+    q *= np.float32(2.0 ** -24)
+    k[:, ::3] *= np.float32(2.0 ** 24)
+    o, m, l, fwd_ws = gpu_attn_fwd(q, k, vq, s_v, W, keep_cache=True)
+    dout = np.random.default_rng(29).standard_normal(o.shape).astype(np.float32)
+    dout[0, 137, 1, 5] = np.inf
+    rq, rk, rv = orc.attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    assert np.all(rq[0, 137, 1] == 0) and np.isfinite(rq).all()
+    with np.errstate(over="ignore", invalid="ignore"):
+        big = np.abs(rq.astype(np.float64)) * 2.0 ** 48 / (1.0 / np.sqrt(128.0))
+    assert (big > 2.0 ** 60).any()            # saturated or wrapped sums are present
+    assert np.isnan(rk).any()
+    for fws in (fwd_ws, None):
+        dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=fws)
+        G.assert_bits_equal(dq, rq, "dq")
+        for got, exp, what in ((dk, rk, "dk"), (dv, rv, "dv")):
+            nan = np.isnan(exp)
+            assert np.array_equal(np.isnan(got), nan), what
+            G.assert_bits_equal(np.where(nan, 0, got).astype(np.float32),
+                                np.where(nan, 0, exp).astype(np.float32), what)
+
+
+@pytest.mark.parametrize("W", [0, 100])
 def test_attn_bwd_underflowing_probabilities(orc, W):
     # logits spread over hundreds: most p underflow to 0, so a and dS are
     # exact zeros and many backward terms are signed zeros, which the canonical

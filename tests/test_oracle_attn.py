@@ -45,6 +45,11 @@ def test_quant_p_and_fixed_point(orc):
     assert orc.attn_fx(3 * 2.0 ** -49) == 2           # 1.5 -> even
     assert orc.attn_fx(5 * 2.0 ** -49) == 2           # 2.5 -> even
     assert orc.attn_fx(2.0 ** 16) == (1 << 63) - 1    # saturates
+    assert orc.attn_fx(2.0 ** 15) == (1 << 63) - 1    # 2^63 itself is out of range
+    assert orc.attn_fx(-(2.0 ** 15)) == -(1 << 63)    # -2^63 is the minimum
+    assert orc.attn_fx(np.float32(2.0 ** 15) * np.float32(1 - 2.0 ** -24)) == (1 << 63) - (1 << 39)
+    assert orc.attn_fx(np.inf) == (1 << 63) - 1 and orc.attn_fx(-np.inf) == -(1 << 63)
+    assert orc.attn_fx(np.nan) == 0                   # a NaN partial adds nothing
     assert orc.attn_fx(1e-30) == 0
     assert orc.attn_fix2f(1 << 48) == 1.0
     assert orc.attn_fix2f(3) == np.float32(3 * 2.0 ** -48)
