@@ -484,6 +484,10 @@ float oracle_exp(float x)
         p = oracle_add(oracle_mul(p, r), c[n]);
     if (kf < -126.0f)
         return 0.0f;
+    if (kf > 254.0f)
+        return INFINITY; /* 2^k alone overflows, whatever p is (so e^+inf = +inf) */
+    if (kf != kf)
+        return kf; /* NaN */
     return oracle_flush(ldexpf(p, (int)kf));
 }
 

@@ -18,6 +18,17 @@ def ulps(a: np.float32, b: float) -> float:
     return abs(a - b) / float(np.spacing(np.float32(abs(b))))
 
 
+def test_exp_special_arguments(orc):
+    # the scaling by 2^k decides these: k < -126 gives 0, k > 254 overflows
+    # whatever the polynomial gave (at +inf the reduction itself is NaN), and a
+    # NaN argument stays NaN
+    assert orc.exp(float("inf")) == np.inf
+    assert orc.exp(1e38) == np.inf and orc.exp(177.0) == np.inf
+    assert orc.exp(float("-inf")) == 0.0 and orc.exp(-1e38) == 0.0
+    assert np.isnan(orc.exp(float("nan")))
+    assert orc.exp(0.0) == 1.0 and orc.exp(-0.0) == 1.0
+
+
 def test_exp_within_two_ulp(orc):
     rng = np.random.default_rng(0)
     xs = np.concatenate([-rng.random(20000) * 87.0, -rng.random(2000) * 1e-3,
