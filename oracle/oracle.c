@@ -515,6 +515,8 @@ static float attn_logit(const float* q, const float* k, int64_t b, int64_t i, in
 int oracle_attn_quant_p(float p)
 {
     float r = nearbyintf(oracle_mul(p, 127.0f));
+    if (r != r)
+        return 0; /* NaN: the clamp's lower bound */
     if (r > 127.0f)
         r = 127.0f;
     if (r < 0.0f)

@@ -50,6 +50,8 @@ def test_quant_p_and_fixed_point(orc):
     assert orc.attn_quant_p(1.0) == 127 and orc.attn_quant_p(0.0) == 0
     assert orc.attn_quant_p(0.5 / 127) == 0          # tie -> even
     assert orc.attn_quant_p(1.5 / 127 + 1e-6) == 2
+    assert orc.attn_quant_p(float("nan")) == 0       # the clamp's lower bound
+    assert orc.attn_quant_p(float("inf")) == 127 and orc.attn_quant_p(-1.0) == 0
     assert orc.attn_fx(1.0) == 1 << 48
     assert orc.attn_fx(-1.0) == -(1 << 48)
     assert orc.attn_fx(2.0 ** -49) == 0               # 0.5 -> even
