@@ -92,6 +92,17 @@ def test_quant_golden(orc):
         assert int(got[0]) == q, (hex(xb), hex(sb), int(got[0]))
 
 
+def test_quant_non_finite(orc):
+    # a NaN quotient gives 0 and infinite ones clamp to +-127, as the oracle
+    # states; the 16-element groups of the kernel and its ragged tail both
+    x = np.array([np.nan, np.inf, -np.inf, 1.0, -np.nan, 3.0e38, -3.0e38, 0.5], np.float32)
+    x = np.concatenate([x, x[::-1], x[:5]])
+    for s in [np.float32(0.0284), np.float32(1.0), np.float32(1e-30)]:
+        exp = orc.quant_i8(x, s)
+        assert list(exp[:3]) == [0, 127, -127]
+        G.assert_bits_equal(G.gpu_quant(x, s), exp, f"non-finite quotients, s {s}")
+
+
 def test_quant_half_integers(orc):
     s = np.float32(0.0371)
     x = ((np.arange(-300, 300, dtype=np.float32) + np.float32(0.5)) * s).astype(np.float32)
