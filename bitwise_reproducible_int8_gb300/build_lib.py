@@ -22,7 +22,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librepro.so")
 
 SOURCES = ["api.cu", "k_scale.cu", "k_quant.cu", "k_fwd.cu", "k_fwd_tc.cu", "k_bwd.cu", "k_bwd_prefetch.cu", "k_bwd_tma.cu",
-           "k_reduce.cu", "k_scale_noalloc.cu", "k_optim.cu", "k_hash.cu", "k_attn.cu", "k_selftest.cu"]
+           "k_reduce.cu", "k_scale_noalloc.cu", "k_optim.cu", "k_hash.cu", "k_attn_fwd.cu", "k_attn_bwd.cu", "k_selftest.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + [

@@ -87,7 +87,7 @@ cudaError_t launch_running_sum(const float* const* parts, int S, int64_t n, floa
 cudaError_t launch_treefold(const float* const* parts, int R, int64_t n, float* out, int grid,
                             cudaStream_t st);
 
-// ---- attention with int8 P.V (k_attn.cu)
+// ---- attention with int8 P.V (k_attn_fwd.cu, k_attn_bwd.cu)
 size_t attn_fwd_ws_bytes(int64_t B, int64_t T, int64_t Hq, int64_t W);
 cudaError_t launch_attn_fwd(const float* q, const float* k, const int8_t* vq, const float* s_v,
                             float* o, float* m, float* l, int64_t B, int64_t T, int64_t Hq,

@@ -1,5 +1,5 @@
 // umma.cuh -- the 5th-generation tensor-core pieces shared by the exact
-// int8 forward (k_fwd_tc.cu) and the attention's P.V (k_attn.cu): shared-
+// int8 forward (k_fwd_tc.cu) and the attention's P.V (k_attn_fwd.cu): shared-
 // memory matrix descriptors for 128-byte-swizzled K-major bf16 tiles, the
 // kind::f16 instruction descriptor with an fp32 accumulator, the MMA issue
 // and commit, and tensor-memory loads.
