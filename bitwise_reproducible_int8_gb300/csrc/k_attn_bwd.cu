@@ -1396,17 +1396,32 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
                 if (lane == 0)
                     mbar_arrive(&empty[s]);
                 ++used;
-                // fold the group partials, left to right over the groups
+                // fold the group partials, left to right over the groups; once
+                // every key of the warp has started and has queries here, plain adds
+                bool plain = true;
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    if (ib[r] > ie[r])
-                        continue;
+                for (int r = 0; r < 4; ++r)
+                    plain = plain && started[r] && ib[r] <= ie[r];
+                if (__all_sync(0xffffffffu, plain)) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        fk[r][q] = started[r] ? fadd2_ftz(fk[r][q], pk[r][q]) : pk[r][q];
-                        fv[r][q] = started[r] ? fadd2_ftz(fv[r][q], pv[r][q]) : pv[r][q];
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            fk[r][q] = fadd2_ftz(fk[r][q], pk[r][q]);
+                            fv[r][q] = fadd2_ftz(fv[r][q], pv[r][q]);
+                        }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        if (ib[r] > ie[r])
+                            continue;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            fk[r][q] = started[r] ? fadd2_ftz(fk[r][q], pk[r][q]) : pk[r][q];
+                            fv[r][q] = started[r] ? fadd2_ftz(fv[r][q], pv[r][q]) : pv[r][q];
+                        }
+                        started[r] = true;
                     }
-                    started[r] = true;
                 }
             }
         const u64 cc = pack2(a.c, a.c);
