@@ -1039,7 +1039,8 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
 #pragma unroll
                             for (int q = 0; q < 4; ++q) {
                                 const u64 pr = fmul2_rn(P, D[q]);
-                                pp[r][q] = j == jb[r] ? fadd2_ftz(pr, z) : fadd2_ftz(pp[r][q], pr);
+                                // the first term is flushed as -0 (+) t, the same as t (+) -0
+                                pp[r][q] = fadd2_ftz(j == jb[r] ? z : pp[r][q], pr);
                             }
                         }
                     }
@@ -1376,8 +1377,9 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
 #pragma unroll
                                 for (int q = 0; q < 4; ++q) {
                                     const u64 xk = fmul2_rn(PS, DQ[q]), xv = fmul2_rn(PA, DG[q]);
-                                    pk[r][q] = i == ib[r] ? fadd2_ftz(xk, z) : fadd2_ftz(pk[r][q], xk);
-                                    pv[r][q] = i == ib[r] ? fadd2_ftz(xv, z) : fadd2_ftz(pv[r][q], xv);
+                                    // the first term is flushed as -0 (+) t, the same as t (+) -0
+                                    pk[r][q] = fadd2_ftz(i == ib[r] ? z : pk[r][q], xk);
+                                    pv[r][q] = fadd2_ftz(i == ib[r] ? z : pv[r][q], xv);
                                 }
                             }
                         }
