@@ -534,10 +534,10 @@ static void attn_fwd_row(const float* q, const float* k, const int8_t* vq, float
     float* s = (float*)malloc((size_t)n * sizeof(float));
     float* tmp = (float*)malloc((size_t)(D > n ? D : n) * sizeof(float));
     int64_t* acc = (int64_t*)calloc((size_t)D, sizeof(int64_t));
-    float m = 0.0f;
+    float m = -INFINITY; /* the maximum of no logit */
     for (int64_t t = 0; t < n; ++t) {
         s[t] = attn_logit(q, k, b, i, lo + t, h, g, T, Hq, Hkv, D, c, tmp);
-        if (t == 0 || s[t] > m)
+        if (s[t] > m) /* a NaN logit never compares greater: it is passed over */
             m = s[t];
     }
     if (m == 0.0f)

@@ -193,6 +193,30 @@ def test_attn_bwd_fixed_point_magnitudes(orc, W):
         G.assert_bits_equal(dv, rv, "dv")
 
 
+@pytest.mark.parametrize("cache", [True, False])
+@pytest.mark.parametrize("W", [0, 100])
+def test_attn_fwd_nan_keys(orc, W, cache):
+    # a NaN in key rows 0 and 140 makes those keys' logits NaN for every query:
+    # the row maximum passes over them (and is -inf for row 0, whose only key
+    # is key 0); l and o are NaN exactly where a row sees one of those keys
+    # and bit-identical to the oracle elsewhere
+    B, T, Hq, Hkv = 1, 150, 2, 1
+    q, k, vq, s_v = _case(404 + W, B, T, Hq, Hkv)
+    k[0, 0, 0, 3] = np.nan
+    k[0, 140, 0, 7] = np.nan
+    o, m, l = gpu_attn_fwd(q, k, vq, s_v, W, cache=cache)
+    ro, rm, rl = orc.attn_fwd(q, k, vq, s_v, W)
+    assert np.isfinite(rm[0, 1:]).all() and np.all(rm[0, 0] == -np.inf)
+    G.assert_bits_equal(m, rm, "m")
+    for got, exp, what in ((l, rl, "l"), (o, ro, "o")):
+        nan = np.isnan(exp)
+        assert np.array_equal(np.isnan(got), nan), what
+        G.assert_bits_equal(np.where(nan, 0, got).astype(np.float32),
+                            np.where(nan, 0, exp).astype(np.float32), what)
+    if W:
+        assert not np.isnan(rl[0, 100:140]).any()   # rows that see neither key stay finite
+
+
 @pytest.mark.parametrize("W", [0, 100])
 def test_attn_bwd_fixed_point_saturation_and_nan(orc, W):
     # dQ partials beyond the fixed point's range: every third key row scaled
