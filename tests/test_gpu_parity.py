@@ -75,6 +75,25 @@ def test_amax_grid_invariance(orc, n, grid):
     G.assert_bits_equal(np.float32(G.gpu_scale(x, 1)), ref, f"amax n {n} grid {grid}")
 
 
+def test_scale_non_finite(orc):
+    # the activation scale's maximum passes over NaN elements and an infinite
+    # one makes it infinite; the weight scale's sum carries a NaN (any NaN
+    # pattern) and an infinity through
+    rng = np.random.default_rng(8)
+    base = rng.standard_normal(70_000).astype(np.float32)
+    for bad in (np.nan, np.inf, -np.inf):
+        x = base.copy()
+        x[[3, 4097, 69_999]] = bad
+        for mode in (0, 1):
+            got, exp = np.float32(G.gpu_scale(x, mode)), np.float32(orc.wscale(x, mode))
+            if np.isnan(exp):
+                assert np.isnan(got), (bad, mode)
+            else:
+                G.assert_bits_equal(got, exp, f"scale mode {mode} with {bad}")
+        if np.isnan(bad):
+            assert np.isfinite(orc.wscale(x, 1))
+
+
 # ----------------------------------------------------------------- quantiser
 
 @pytest.mark.parametrize("n", [1, 15, 16, 17, 1000, 65536 + 9])
