@@ -14,5 +14,6 @@ from .repro import (  # noqa: F401
     repro_quant_i8, repro_quant_i8_multi, repro_wscale_multi, repro_wscale_multi_ws_bytes,
     repro_selftest, repro_set_launch_cfg, repro_state_hash, repro_state_hash_ws_bytes, repro_status_str,
     repro_treefold, repro_version, repro_wait_probe, repro_wscale, repro_wscale_ws_bytes,
-    REPRO_HASH_LEAF_BYTES,
+    REPRO_HASH_LEAF_BYTES, REPRO_DEBUG_CHECK_FINITE, REPRO_ERR_NONFINITE, REPRO_ERR_TIMEOUT,
+    repro_set_debug,
 )

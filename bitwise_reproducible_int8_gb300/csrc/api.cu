@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <initializer_list>
 
 #include "internal.h"
 #include "repro.h"
@@ -29,6 +30,8 @@ std::atomic<int> g_tc_state[kMaxDevices];
 std::atomic<int> g_tc_notice[kMaxDevices];
 
 unsigned long long g_launches;    // kernels enqueued by this library
+
+std::atomic<int> g_debug{0};      // repro_set_debug flags
 
 int current_device()
 {
@@ -57,6 +60,20 @@ int num_sms()
 }
 
 void count_launches(int k) { __atomic_fetch_add(&g_launches, (unsigned long long)k, __ATOMIC_RELAXED); }
+
+int scan_inputs(void* stream, std::initializer_list<FloatSpan> spans)
+{
+    if ((g_debug.load(std::memory_order_relaxed) & REPRO_DEBUG_CHECK_FINITE) == 0)
+        return REPRO_OK;
+    int* err = device_error_word();
+    if (!err)
+        return REPRO_ERR_LAUNCH;
+    for (const FloatSpan& f : spans)
+        if (f.p && f.n > 0 &&
+            launch_check_finite(f.p, f.n, err, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return REPRO_ERR_LAUNCH;
+    return REPRO_OK;
+}
 
 int* device_error_word()
 {
@@ -190,6 +207,7 @@ const char* repro_status_str(int s)
     case REPRO_ERR_WORKSPACE: return "workspace missing or too small";
     case REPRO_ERR_ALIAS: return "buffers that must not overlap do";
     case REPRO_ERR_SELFTEST: return "the tensor-core forward differs from the exact CUDA-core forward";
+    case REPRO_ERR_NONFINITE: return "debug mode: a float input held a NaN or an infinity";
     default: return "unknown status";
     }
 }
@@ -197,6 +215,14 @@ const char* repro_status_str(int s)
 int repro_version(void) { return REPRO_VERSION; }
 
 uint64_t repro_launch_count(void) { return (uint64_t)__atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+int repro_set_debug(int flags)
+{
+    if (flags & ~REPRO_DEBUG_CHECK_FINITE)
+        return REPRO_ERR_ARG;
+    g_debug.store(flags, std::memory_order_relaxed);
+    return REPRO_OK;
+}
 
 int repro_set_launch_cfg(const repro_launch_cfg* cfg)
 {
@@ -270,7 +296,7 @@ int repro_device_check(void* stream)
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess)
             return REPRO_ERR_LAUNCH;
-        return REPRO_ERR_TIMEOUT;
+        return (v & kErrTimeoutBit) || !(v & kErrNonfiniteBit) ? REPRO_ERR_TIMEOUT : REPRO_ERR_NONFINITE;
     }
     const int dev = current_device();
     if (dev >= 0 && dev < kMaxDevices && g_tc_notice[dev].exchange(0) != 0)
@@ -307,6 +333,8 @@ int repro_wscale(const float* x, int64_t n, int mode, int qmax, float* scale_out
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    if ((st = scan_inputs(stream, {{x, n}})) != REPRO_OK)
+        return st;
     if (mode == REPRO_SCALE_WEIGHT_MEANABS)
         return status_of(launch_wscale_meanabs(x, n, qmax, scale_out, ws, g_cfg.reduce_block_log2,
                                                as_stream(stream)));
@@ -337,6 +365,8 @@ int repro_quant_i8(const float* x, int64_t n, const float* scale, int qmax, int8
         return REPRO_ERR_ALIAS;
     int st = check_arch();
     if (st != REPRO_OK)
+        return st;
+    if ((st = scan_inputs(stream, {{x, n}, {scale, 1}})) != REPRO_OK)
         return st;
     // up to 32 CTAs per SM: on GB300 the quantiser streams 92M elements in 78.5 us
     // this way against 90.8 us with the grid capped at one resident wave
@@ -388,6 +418,9 @@ int repro_wscale_multi(const float* const* xs, const int64_t* ns, int count, int
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    for (int t = 0; t < count; ++t)
+        if ((st = scan_inputs(stream, {{xs[t], ns[t]}})) != REPRO_OK)
+            return st;
     return status_of(launch_wscale_multi(xs, ns, count, mode, qmax, scales_out, ws,
                                          g_cfg.reduce_block_log2, as_stream(stream)));
 }
@@ -431,6 +464,11 @@ int repro_quant_i8_multi(const float* const* xs, const int64_t* ns, int count,
         return REPRO_OK;
     int st = check_arch();
     if (st != REPRO_OK)
+        return st;
+    for (int t = 0; t < count; ++t)
+        if ((st = scan_inputs(stream, {{xs[t], ns[t]}})) != REPRO_OK)
+            return st;
+    if ((st = scan_inputs(stream, {{scales, count}})) != REPRO_OK)
         return st;
     return status_of(launch_quant_multi(xs, ns, count, scales, qmax, q_outs,
                                         stream_grid(total / 16, 32), as_stream(stream)));
@@ -481,6 +519,8 @@ int repro_linear_fwd(const int8_t* xq, const int8_t* wq, const float* s_x, const
     }
     int st = check_arch();
     if (st != REPRO_OK)
+        return st;
+    if ((st = scan_inputs(stream, {{s_x, 1}, {s_w, 1}})) != REPRO_OK)
         return st;
     if (tc && g_cfg.fwd_path < 1) {   // the default path is gated; explicit tile paths are not
         const int gate = tc_gate(ws, as_stream(stream));
@@ -543,6 +583,8 @@ int repro_linear_bwd(const float* dy, const int8_t* xq, const int8_t* wq, const 
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    if ((st = scan_inputs(stream, {{dy, M * N}, {want_dw ? s_x : nullptr, 1}, {want_dx ? s_w : nullptr, 1}})) != REPRO_OK)
+        return st;
     cudaStream_t s = as_stream(stream);
     if (want_dx) {
         cudaError_t e = launch_bwd_dx(dy, wq, s_w, dx, M, N, K, sl, static_cast<float*>(ws), s);
@@ -574,6 +616,8 @@ int repro_grad_accum(float* acc, const float* g, int64_t n, void* stream)
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    if ((st = scan_inputs(stream, {{acc, n}, {g, n}})) != REPRO_OK)
+        return st;
     return status_of(launch_grad_accum(acc, g, n, stream_grid(n / 4), as_stream(stream)));
 }
 
@@ -601,6 +645,8 @@ int repro_sumsq(const float* g, int64_t n, float* out, void* ws, size_t ws_bytes
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    if ((st = scan_inputs(stream, {{g, n}})) != REPRO_OK)
+        return st;
     return status_of(launch_sumsq(g, n, out, ws, g_cfg.reduce_block_log2, as_stream(stream)));
 }
 
@@ -624,6 +670,8 @@ int repro_adamw_step(float* p, float* m, float* v, const float* g, int64_t n, co
         return REPRO_ERR_ALIAS;
     int st = check_arch();
     if (st != REPRO_OK)
+        return st;
+    if ((st = scan_inputs(stream, {{p, n}, {m, n}, {v, n}, {g, n}, {sumsq, 1}})) != REPRO_OK)
         return st;
     AdamWArgs h{hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_norm};
     return status_of(launch_adamw(p, m, v, g, n, sumsq, h, t, stream_grid(n / 4), as_stream(stream)));
@@ -664,6 +712,9 @@ int repro_running_sum(const float* const* parts, int S, int64_t n, float* out, v
     st = check_arch();
     if (st != REPRO_OK)
         return st;
+    for (int r = 0; r < S; ++r)
+        if ((st = scan_inputs(stream, {{parts[r], n}})) != REPRO_OK)
+            return st;
     return status_of(launch_running_sum(parts, S, n, out, stream_grid(n / 4), as_stream(stream)));
 }
 
@@ -695,6 +746,9 @@ int repro_treefold(const float* const* parts, int R, int64_t n, float* out, void
     int st = check_arch();
     if (st != REPRO_OK)
         return st;
+    for (int r = 0; r < R; ++r)
+        if ((st = scan_inputs(stream, {{parts[r], n}})) != REPRO_OK)
+            return st;
     return status_of(launch_treefold(parts, R, n, out, stream_grid(n / 4), as_stream(stream)));
 }
 
@@ -742,6 +796,8 @@ int repro_attn_fwd(const float* q, const float* k, const int8_t* vq, const float
     }
     int st = check_arch();
     if (st != REPRO_OK)
+        return st;
+    if ((st = scan_inputs(stream, {{q, B * T * Hq * D}, {k, B * T * Hkv * D}, {s_v, 1}})) != REPRO_OK)
         return st;
     // P.V on the tensor cores needs the logit cache and a device whose exactness
     // check has passed (run here, in the cache's space, if it has not run yet)
@@ -822,6 +878,9 @@ int repro_attn_bwd(const float* q, const float* k, const int8_t* vq, const float
     }
     int st = check_arch();
     if (st != REPRO_OK)
+        return st;
+    if ((st = scan_inputs(stream, {{q, B * T * Hq * D}, {k, B * T * Hkv * D}, {s_v, 1}, {o, B * T * Hq * D},
+                                   {dout, B * T * Hq * D}, {m, B * T * Hq}, {l, B * T * Hq}})) != REPRO_OK)
         return st;
     return status_of(launch_attn_bwd(q, k, vq, s_v, o, dout, m, l, dq, dk, dv, B, T, Hq, Hkv, W,
                                      ws, fwd_ws, as_stream(stream)));

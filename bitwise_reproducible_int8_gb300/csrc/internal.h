@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <initializer_list>
+
 #define REPRO_MAX_PARTS_INTERNAL 64
 #define REPRO_MAX_TENSORS_INTERNAL 64
 
@@ -21,8 +23,17 @@ struct LaunchCfg {
 };
 
 const LaunchCfg& launch_cfg();
+// debug mode (repro_set_debug): the scans of a call's float inputs, enqueued
+// before its kernels; REPRO_OK, or REPRO_ERR_LAUNCH if one could not be enqueued
+struct FloatSpan {
+    const float* p;
+    int64_t n;
+};
+int scan_inputs(void* stream, std::initializer_list<FloatSpan> spans);
 int num_sms();
-int* device_error_word();   // device address of the bounded-wait error flag
+int* device_error_word();   // device address of the error word: bit 0 a bounded wait gave up,
+                            // bit 1 the debug scan found a non-finite input
+constexpr int kErrTimeoutBit = 1, kErrNonfiniteBit = 2;
 int arch_status();          // REPRO_OK when the current device is a GB300
 void count_launches(int k); // adds k to the process-wide launch counter
 // status code of a CUDA runtime result, the same for every entry point
@@ -102,6 +113,9 @@ cudaError_t launch_attn_bwd(const float* q, const float* k, const int8_t* vq, co
 
 // ---- bounded-wait probe (k_bwd_tma.cu)
 cudaError_t launch_wait_probe(int arrive, cudaStream_t st);
+// debug mode: ORs kErrNonfiniteBit into *err if any of the n floats at p is a
+// NaN or an infinity
+cudaError_t launch_check_finite(const float* p, int64_t n, int* err, cudaStream_t st);
 
 // ---- forward exactness self-test (k_selftest.cu)
 size_t selftest_ws_bytes();

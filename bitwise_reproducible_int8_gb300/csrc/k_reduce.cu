@@ -168,6 +168,23 @@ k_running_sum_generic(const Parts parts, int S, int64_t n, float* out)
     }
 }
 
+// debug scan: any NaN or infinity among n floats ORs the non-finite bit into
+// the error word (one atomic per warp that finds one).  p is 16-byte aligned
+__global__ void __launch_bounds__(256) k_check_finite(const float* __restrict__ p, int64_t n, int* err)
+{
+    const int64_t nv = n >> 2;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    bool bad = false;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nv; i += stride) {
+        const float4 v = ld_stream(reinterpret_cast<const float4*>(p) + i);
+        bad = bad || !isfinite(v.x) || !isfinite(v.y) || !isfinite(v.z) || !isfinite(v.w);
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 3))
+        bad = bad || !isfinite(p[(nv << 2) + threadIdx.x]);
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0)
+        atomicOr(err, kErrNonfiniteBit);
+}
+
 } // namespace
 
 cudaError_t launch_running_sum(const float* const* parts, int S, int64_t n, float* out, int grid,
@@ -215,6 +232,17 @@ cudaError_t launch_treefold(const float* const* parts, int R, int64_t n, float* 
     case 8: k_treefold<8><<<grid, 256, 0, st>>>(P, n, out); break;
     default: k_treefold_generic<<<grid, 256, 0, st>>>(P, R, n, out); break;
     }
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_check_finite(const float* p, int64_t n, int* err, cudaStream_t st)
+{
+    if (n <= 0)
+        return cudaSuccess;
+    const int64_t want = ((n >> 2) + 255) / 256;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    k_check_finite<<<(unsigned)(want < 1 ? 1 : (want > cap ? cap : want)), 256, 0, st>>>(p, n, err);
     count_launches(1);
     return cudaGetLastError();
 }

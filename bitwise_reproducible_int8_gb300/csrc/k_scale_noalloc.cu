@@ -71,6 +71,8 @@ extern "C" int repro_wscale_noalloc(const float* x, int64_t n, int mode, int qma
     int st = arch_status();
     if (st != REPRO_OK)
         return st;
+    if ((st = scan_inputs(stream, {{x, n}})) != REPRO_OK)
+        return st;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev)
         return REPRO_ERR_LAUNCH;

@@ -20,7 +20,11 @@ STATUS_NAMES = {
     0: "REPRO_OK", -1: "REPRO_ERR_ARG", -2: "REPRO_ERR_SHAPE", -3: "REPRO_ERR_ALIGN",
     -4: "REPRO_ERR_ARCH", -5: "REPRO_ERR_LAUNCH", -6: "REPRO_ERR_TIMEOUT",
     -7: "REPRO_ERR_WORKSPACE", -8: "REPRO_ERR_ALIAS", -9: "REPRO_ERR_SELFTEST",
+    -10: "REPRO_ERR_NONFINITE",
 }
+REPRO_ERR_TIMEOUT = -6
+REPRO_ERR_NONFINITE = -10
+REPRO_DEBUG_CHECK_FINITE = 1
 REPRO_SCALE_WEIGHT_MEANABS = 0
 REPRO_SCALE_ACT_AMAX = 1
 REPRO_BWD_DW_ACCUMULATE = 1
@@ -90,6 +94,7 @@ _SIGNATURES = {
     "repro_wait_probe": (_int, [_int, _vp]),
     "repro_launch_count": (ctypes.c_uint64, []),
     "repro_set_launch_cfg": (_int, [ctypes.POINTER(LaunchCfg)]),
+    "repro_set_debug": (_int, [_int]),
 }
 
 _lib = None
@@ -434,6 +439,12 @@ def repro_device_check(stream=None) -> int:
 def repro_wait_probe(arrive: int, stream=None) -> int:
     """Enqueue the bounded-wait probe; arrive=0 makes the wait run out."""
     return int(lib().repro_wait_probe(int(arrive), _stream(stream)))
+
+
+def repro_set_debug(flags: int) -> None:
+    """Debug checks (REPRO_DEBUG_CHECK_FINITE: scan every float input; a NaN or
+    an infinity makes the next repro_device_check return REPRO_ERR_NONFINITE)."""
+    _check("repro_set_debug", lib().repro_set_debug(int(flags)))
 
 
 def repro_set_launch_cfg(bwd_segment_log2: int = -1, reduce_block_log2: int = -1,

@@ -76,7 +76,9 @@ typedef enum {
     REPRO_ERR_TIMEOUT = -6,   /* a bounded device-side wait gave up (repro_device_check) */
     REPRO_ERR_WORKSPACE = -7, /* workspace NULL or smaller than *_ws_bytes() */
     REPRO_ERR_ALIAS = -8,     /* two buffers that must not overlap do */
-    REPRO_ERR_SELFTEST = -9   /* repro_selftest found the tensor-core forward inexact */
+    REPRO_ERR_SELFTEST = -9,  /* repro_selftest found the tensor-core forward inexact */
+    REPRO_ERR_NONFINITE = -10 /* debug mode: a float input held a NaN or an infinity
+                                 (repro_device_check; see repro_set_debug) */
 } repro_status;
 
 typedef enum {
@@ -450,7 +452,8 @@ size_t repro_selftest_ws_bytes(void);
  * Failure-detection hook.  Every pipeline wait in the library is bounded: a
  * wait that is not satisfied within about two seconds at the boost clock
  * sets the device error word, lets the kernel return, and is reported by
- * repro_device_check() as REPRO_ERR_TIMEOUT, leaving the CUDA context usable.
+ * repro_device_check() as REPRO_ERR_TIMEOUT, leaving the CUDA context usable
+ * (REPRO_ERR_NONFINITE is the debug mode's report, see repro_set_debug).
  * repro_wait_probe enqueues one thread that performs that same bounded wait
  * on a shared-memory barrier phase which completes only when `arrive` is 1.
  * With arrive = 0 nothing completes it, so the wait runs out (about two
@@ -459,6 +462,23 @@ size_t repro_selftest_ws_bytes(void);
  * Enqueues only.  arrive outside {0, 1} -> REPRO_ERR_ARG.
  * ------------------------------------------------------------------------ */
 int repro_wait_probe(int arrive, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Debug checks, all off by default (flags = 0).  Non-finite inputs are
+ * outside the method's contract (the calls still compute their documented
+ * results for them: a NaN quotient quantises to 0, a NaN logit is passed over
+ * by the row maximum, and so on); this mode finds where they enter.
+ *   REPRO_DEBUG_CHECK_FINITE: every call that reads float tensors or scales
+ *     first enqueues, on its own stream, one scan of each of them (an extra
+ *     read of every such input); a NaN or an infinity sets the device error
+ *     word, and the next repro_device_check() returns REPRO_ERR_NONFINITE (a
+ *     bounded wait that gave up in the same interval reports
+ *     REPRO_ERR_TIMEOUT instead).  The scan does not stop the call.
+ * Process-wide, like the launch configuration.  Unknown flags ->
+ * REPRO_ERR_ARG.
+ * ------------------------------------------------------------------------ */
+#define REPRO_DEBUG_CHECK_FINITE 1
+int repro_set_debug(int flags);
 int repro_version(void);
 int repro_device_check(void* stream);
 uint64_t repro_launch_count(void);

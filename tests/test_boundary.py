@@ -30,9 +30,18 @@ def test_exports_every_declared_symbol(L):
 
 def test_status_strings_and_version(L):
     assert repro.repro_version() == 1
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         assert repro.repro_status_str(code) != "unknown status"
     assert repro.repro_status_str(-99) == "unknown status"
+
+
+def test_debug_flags(L):
+    assert L.repro_set_debug(2) == -1 and L.repro_set_debug(-1) == -1   # unknown flags
+    assert L.repro_set_debug(repro.REPRO_DEBUG_CHECK_FINITE) == 0
+    # invalid arguments are still rejected before anything (a scan included) is enqueued
+    assert L.repro_wscale(None, 10, 0, 127, A, A * 4, 1 << 20, None) == -1
+    assert L.repro_set_debug(0) == 0
+    assert repro.STATUS_NAMES[-10] == "REPRO_ERR_NONFINITE"
 
 
 def test_wscale_argument_checks(L):
