@@ -350,6 +350,7 @@ def run_ours(args, wl):
     host = S.generate_host_inputs(wl_r)
     hp = S.HotPathStep(wl_r, host, fused_accum=not args.unfused_accum,
                        dw_stream=False if args.no_dw_stream else None)
+    inputs_sha256 = hp.input_digest()   # untimed, before any step changes the weights
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         if wl_r.replicas > 1 or wl_r.shards > 1:
@@ -510,7 +511,11 @@ def run_ours(args, wl):
                              (f"inputs fit in L2 ({resident_gb(hp) * 1e3:.1f} MB resident): a "
                               "launch-latency case, L2 not flushed"),
                        "launch": "one CUDA graph replay per step" if graph is not None
-                       else "eager calls"},
+                       else "eager calls",
+                       "inputs_sha256": inputs_sha256,
+                       "inputs_sha256_of": "RFC 6962 Merkle root (SHA-256, 4 KB leaves) of rank 0's "
+                                           "flat weights, then X and dY per linear, micro-batch "
+                                           "by micro-batch"},
             "roofline": roofline, "other_kernels": other,
             "ms_per_step_by_call": {k: v / args.steps for k, v in per_class.items()},
             "overlapping_calls": ["bwd_dw", "fwd", "bwd_dx"] if hp.s_dw is not None else [],
@@ -736,6 +741,10 @@ def run_attn(args, aw):
     ws_f = torch.empty(max(R.repro_attn_fwd_ws_bytes(B, T, Hq, aw.window), 16), dtype=torch.uint8,
                        device=dev)   # the forward's logit cache
     dev_bufs = (tq, tk, tv, tdo, dq, dk, dv)
+    d32 = torch.empty(32, dtype=torch.uint8, device=dev)
+    R.repro_state_hash([tq, tk, tv, tdo], d32)   # untimed record of the inputs
+    torch.cuda.synchronize()
+    inputs_sha256 = bytes(d32.cpu().numpy()).hex()
     torch.cuda.synchronize()   # s_v's fill ran on the default stream
     stream = torch.cuda.Stream()
     timers = {}
@@ -900,7 +909,10 @@ def run_attn(args, aw):
                        "sequences": aw.sequences, "seq_len": aw.seq_len, "heads_q": aw.heads_q,
                        "heads_kv": aw.heads_kv, "head_dim": D, "window": aw.window,
                        "pairs_per_step": pairs, "parallelism": "replicas only",
-                       "l2": "inputs larger than L2: q, k, v, dO and outputs ~0.7 GB"},
+                       "l2": "inputs larger than L2: q, k, v, dO and outputs ~0.7 GB",
+                       "inputs_sha256": inputs_sha256,
+                       "inputs_sha256_of": "RFC 6962 Merkle root (SHA-256, 4 KB leaves) of rank 0's "
+                                           "q, k, v and dO"},
             "roofline": roofline,
             "ms_per_step_by_call": {kk: vv / args.steps for kk, vv in per_class.items()},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),

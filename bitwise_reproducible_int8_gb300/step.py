@@ -320,6 +320,21 @@ class HotPathStep:
             R.repro_grad_accum(p, torch.from_numpy(self.host.noise[r]).to(self.dev), stream=stream)
             self.parts.append(p)
 
+    def input_buffers(self) -> list:
+        """The step's seeded inputs in a fixed order: the flat weights, then X
+        and dY of every linear, micro-batch by micro-batch."""
+        L, J = len(self.wl.linears), self.wl.microbatches
+        return [self.Wflat] + [t for j in range(J) for i in range(L) for t in (self.X[i][j], self.dY[i][j])]
+
+    def input_digest(self) -> str:
+        """RFC 6962 Merkle Tree Hash (SHA-256 over 4 KB leaves) of
+        input_buffers(), taken on the device by repro_state_hash, as hex: the
+        record of which bytes a run computed on.  Synchronises the device."""
+        d = torch.empty(32, dtype=torch.uint8, device=self.dev)
+        R.repro_state_hash(self.input_buffers(), d)
+        torch.cuda.synchronize(self.dev)
+        return bytes(d.cpu().numpy()).hex()
+
     def result(self) -> torch.Tensor:
         """The step's result: the folded gradient (or the level-2 sum, or G)."""
         if self.TF is not None:

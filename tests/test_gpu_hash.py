@@ -71,3 +71,19 @@ def test_repeatable_across_streams():
     a = _bytes(rng, 300 * LEAF + 1)
     s = torch.cuda.Stream()
     assert _gpu_hash([a]) == _gpu_hash([a], stream=s)
+
+
+def test_bench_input_digest_is_the_seeded_inputs():
+    # the digest bench.py records is the Merkle root of exactly the seeded
+    # inputs the step reads, in its stated order, and the same on a rerun
+    from oracle import merkle
+    from bitwise_reproducible_int8_gb300 import inputs, step
+    wl = inputs.WORKLOADS["tiny"]
+    host = step.generate_host_inputs(wl)
+    hp = step.HotPathStep(wl, host)
+    got = hp.input_digest()
+    L, J = len(wl.linears), wl.microbatches
+    bufs = [np.concatenate([w.ravel() for w in host.W]).tobytes()]
+    bufs += [a.tobytes() for j in range(J) for i in range(L) for a in (host.X[i][j], host.dY[i][j])]
+    assert got == merkle.state_hash(bufs).hex()
+    assert step.HotPathStep(wl, step.generate_host_inputs(wl)).input_digest() == got
