@@ -50,7 +50,8 @@ def gpu_attn_fwd(q, k, vq, s_v, W, cache=True, keep_cache=False):
 
 
 SHAPES = [(1, 1, 4, 2), (1, 5, 4, 2), (1, 63, 2, 2), (1, 64, 4, 1), (2, 65, 4, 2),
-          (1, 130, 8, 2), (2, 200, 4, 4), (1, 257, 4, 2), (1, 600, 4, 2)]
+          (1, 130, 8, 2), (2, 200, 4, 4), (1, 257, 4, 2), (1, 600, 4, 2),
+          (1, 130, 16, 2), (1, 70, 16, 1)]   # the last two: 8 and 16 query heads per kv head
 
 # cached: the logit cache on, P.V on the tensor cores (the default); cached_dp4a:
 # the cache on, P.V on CUDA cores (the launch-configuration hook's fwd_path 0);
