@@ -86,4 +86,37 @@ __device__ __forceinline__ void step(u64 (&acc)[16], const ulonglong2& a03, cons
     }
 }
 
+// the same step with the products two row pairs ahead of their adds
+template <bool FIRST>
+__device__ __forceinline__ void step_ahead2(u64 (&acc)[16], const ulonglong2& a03, const ulonglong2& a47,
+                                            const float4& b)
+{
+    const u64 P[4] = {a03.x, a03.y, a47.x, a47.y};
+    const u64 D[4] = {pack2(b.x, b.x), pack2(b.y, b.y), pack2(b.z, b.z), pack2(b.w, b.w)};
+    u64 c0[4], c1[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        c0[j] = fmul2_rn(P[0], D[j]);
+        c1[j] = fmul2_rn(P[1], D[j]);
+    }
+#pragma unroll
+    for (int ip = 0; ip < 4; ++ip) {
+        u64 nx[4];
+        if (ip + 2 < 4) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                nx[j] = fmul2_rn(P[ip + 2], D[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            acc[ip * 4 + j] = FIRST ? c0[j] : fadd2_ftz(acc[ip * 4 + j], c0[j]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            c0[j] = c1[j];
+            if (ip + 2 < 4)
+                c1[j] = nx[j];
+        }
+    }
+}
+
 } // namespace repro

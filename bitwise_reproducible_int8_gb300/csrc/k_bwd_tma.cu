@@ -28,11 +28,11 @@
 //     stages; at the start of chunk c it refills the stage that every warp
 //     released at the end of chunk c - 2 with chunk c + 2, so no warp runs
 //     more than two chunks ahead of warp 0 and every wait ends;
-//   * with 8 warps a thread may hold 255 registers: tree levels 0..RL-1
-//     (RL = 2) stay in registers, beside the products formed one row pair
-//     ahead of their adds, and the rest live in tensor memory (thread: lane
+//   * with 8 warps a thread may hold 255 registers: tree level 0 (RL = 1)
+//     stays in registers, beside the products formed two row pairs ahead of
+//     their adds, and the rest live in tensor memory (thread: lane
 //     32*(warp%4) + lane, columns (warp/4)*256 + 32*(level-RL)), touched once
-//     every 4 chunks.
+//     every 2 chunks.
 // Every wait is bounded: past the limit the CTA records a failure in the
 // device error word, lets its copies land, frees its tensor memory and exits.
 #include <cuda.h>
@@ -48,7 +48,7 @@ namespace repro {
 namespace {
 
 constexpr int NC = 256;                        // threads (8 warps)
-constexpr int RL = 2;                          // tree levels kept in registers
+constexpr int RL = 1;                          // tree levels kept in registers
 constexpr int TI = BWD_TMA_ROWS;               // 128 tile rows (i)
 constexpr int STG = 4;                         // ring stages
 constexpr int A_BYTES = CH * TI * 4;           // 32768: A[r][i]
@@ -72,7 +72,7 @@ __device__ __forceinline__ void chunk_sum(u64 (&acc)[16], const float* __restric
             a47 = *reinterpret_cast<const ulonglong2*>(Ar + TI + 4);
             b = *reinterpret_cast<const float4*>(Br + BT);
         }
-        step<true>(acc, c03, c47, cb);
+        step_ahead2<true>(acc, c03, c47, cb);
     }
     if (valid == CH) {
 #pragma unroll 21
@@ -83,7 +83,7 @@ __device__ __forceinline__ void chunk_sum(u64 (&acc)[16], const float* __restric
             a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * TI);
             a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * TI + 4);
             b = *reinterpret_cast<const float4*>(Br + rn * BT);
-            step<false>(acc, c03, c47, cb);
+            step_ahead2<false>(acc, c03, c47, cb);
         }
     } else {
         for (int r = 1; r < valid; ++r) {
@@ -93,7 +93,7 @@ __device__ __forceinline__ void chunk_sum(u64 (&acc)[16], const float* __restric
             a03 = *reinterpret_cast<const ulonglong2*>(Ar + rn * TI);
             a47 = *reinterpret_cast<const ulonglong2*>(Ar + rn * TI + 4);
             b = *reinterpret_cast<const float4*>(Br + rn * BT);
-            step<false>(acc, c03, c47, cb);
+            step_ahead2<false>(acc, c03, c47, cb);
         }
     }
 }
@@ -110,7 +110,7 @@ __device__ __forceinline__ void chunk_head(u64 (&acc)[16], const float* __restri
         a03 = *reinterpret_cast<const ulonglong2*>(Ar + TI);
         a47 = *reinterpret_cast<const ulonglong2*>(Ar + TI + 4);
         b = *reinterpret_cast<const float4*>(Br + BT);
-        step<true>(acc, c03, c47, cb);
+        step_ahead2<true>(acc, c03, c47, cb);
     }
 #pragma unroll 31
     for (int r = 1; r < CH - 1; ++r) {
@@ -119,7 +119,7 @@ __device__ __forceinline__ void chunk_head(u64 (&acc)[16], const float* __restri
         a03 = *reinterpret_cast<const ulonglong2*>(Ar + (r + 1) * TI);
         a47 = *reinterpret_cast<const ulonglong2*>(Ar + (r + 1) * TI + 4);
         b = *reinterpret_cast<const float4*>(Br + (r + 1) * BT);
-        step<false>(acc, c03, c47, cb);
+        step_ahead2<false>(acc, c03, c47, cb);
     }
 }
 
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(NC, 1)
                 __syncwarp();   // every lane's reads of stage s precede lane 0's release
                 if (lane == 0)
                     mbar_arrive(&empty[s]);
-                step<false>(acc, l03, l47, lb);
+                step_ahead2<false>(acc, l03, l47, lb);
                 if (!next_ok) {
                     ok = false;
                     if (lane == 0)
