@@ -43,7 +43,7 @@ METRIC = "tokens/s bit-exact int8-QAT linear fwd+bwd (1 GB300); % of int8/FP32/H
 # DRAM bytes per backward launch: mean over the block step's eight launch shapes,
 # from one ncu capture (-k regex:k_bwd_tma -c 8, dram__bytes_read.sum +
 # dram__bytes_write.sum) of the one-micro-batch profiling case block_1mb
-BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd_tma"): 1649.5e6, ("block_1mb", "k_bwd_tma"): 1649.5e6}
+BWD_TRAFFIC_PER_LAUNCH = {("block", "k_bwd_tma"): 1678.0e6, ("block_1mb", "k_bwd_tma"): 1678.0e6}
 BWD_TRAFFIC_SOURCE = ("profiles/k_bwd_tma_traffic_block.md: ncu -k regex:k_bwd_tma -c 8 "
                       "--metrics dram__bytes_read.sum,dram__bytes_write.sum on block_1mb "
                       "(the block step's eight backward shapes), mean per launch")
