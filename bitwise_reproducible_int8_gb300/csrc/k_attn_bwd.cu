@@ -1341,7 +1341,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
                 if (whole) {
                     load(0);
                     row(std::true_type{}, 1);
-#pragma unroll 3
+#pragma unroll 7
                     for (int i = 1; i < AT; ++i)
                         row(std::false_type{}, i + 1 < AT ? i + 1 : i);
                 } else {
