@@ -77,6 +77,16 @@ __device__ __forceinline__ unsigned long long fadd2_ftz(unsigned long long a, un
     return r;
 }
 
+// a * b + c with one rounding, gradual underflow.  Not an operation of the
+// method: only for computing a correctly rounded quotient (k_attn.cuh)
+__device__ __forceinline__ unsigned long long ffma2_rn(unsigned long long a, unsigned long long b,
+                                                       unsigned long long c)
+{
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // dequantised operand: float(q) (x) s, flushed (q is an exact small integer)
 __device__ __forceinline__ float dequant(int q, float s)
 {

@@ -239,6 +239,29 @@ __device__ __forceinline__ void logit_chunk84(u64 (&acc)[16], const float* __res
     }
 }
 
+// RN(p / l) for a packed pair of quotients, from nl = -l and y = RN(1 / l).
+// q = p (x) y is within two units in the last place; one correction
+// (r = p - l q, then q + r y, each with a single rounding) leaves it within
+// 1/2 unit plus 2^-46 relative, so it is faithful; a second correction then
+// returns the correctly rounded quotient by Markstein's theorem (P. Markstein,
+// IBM J. Res. Dev. 34(1), 1990; Muller et al., Handbook of Floating-Point
+// Arithmetic, chapter 5, division with a fused multiply-add), and the
+// remainder it uses is exact.  Both need every intermediate normal: the
+// caller takes this only for l in [2^-30, 2^30) and p = +0 or p in
+// [2^-90, 2^90), where q stays in (2^-120, 2^120) and every remainder is zero
+// or above 2^-114, and divides otherwise.
+__device__ __forceinline__ u64 div2_rn(u64 p, u64 nl, u64 y)
+{
+    u64 q = fmul2_rn(p, y);
+    q = ffma2_rn(ffma2_rn(nl, q, p), y, q);
+    return ffma2_rn(ffma2_rn(nl, q, p), y, q);
+}
+
+constexpr uint32_t DIV_L_LO = 0x30800000u;   // 2^-30: bits of the smallest l taken
+constexpr uint32_t DIV_L_SPAN = 0x1E000000u; // up to 2^30 (excluded)
+constexpr uint32_t DIV_P_LO = 0x12800000u;   // 2^-90: the smallest nonzero p taken
+constexpr uint32_t DIV_P_HI = 0x6C800000u;   // 2^90 (excluded)
+
 template <bool BWD>
 __global__ void __launch_bounds__(LG_NT, 1) k_attn_rows(const AttnLogitArgs a)
 {
@@ -358,6 +381,20 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_rows(const AttnLogitArgs a)
             }
         }
         asm volatile("bar.sync %0, %1;" ::"r"(gbar), "n"(LG_G) : "memory");
+        // backward: -l and RN(1 / l) of the thread's row pairs, and whether
+        // all eight l admit the quotient by correction (div2_rn)
+        u64 nl2[4], y2[4];
+        bool l_ok = true;
+        if constexpr (BWD) {
+#pragma unroll
+            for (int ip = 0; ip < 4; ++ip) {
+                const float l0 = lrw[8 * ty + 2 * ip], l1 = lrw[8 * ty + 2 * ip + 1];
+                nl2[ip] = pack2(-l0, -l1);
+                y2[ip] = pack2(__frcp_rn(l0), __frcp_rn(l1));
+                l_ok = l_ok && __float_as_uint(l0) - DIV_L_LO < DIV_L_SPAN &&
+                       __float_as_uint(l1) - DIV_L_LO < DIV_L_SPAN;
+            }
+        }
         const int64_t tile0 = (qt.b * a.Hq + qt.h) * a.tiles_bh + tile_prefix(qt.i0 / AT, W);
         float* cache = a.cache + tile0 * (AT * AT);
         float mx[8];
@@ -456,19 +493,41 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_rows(const AttnLogitArgs a)
                 }
                 const int j0 = t * AT;
                 const bool inner = qt.i0 + AT - 1 < T && j0 + AT - 1 <= qt.i0 && (W == 0 || j0 >= qt.i0 + AT - W);
+                // a = p (/) l_i, flushed, for the thread's 16 pairs: by
+                // correction when every p and l admits it, else divided
+                u64 a2[16];
+                {
+                    uint32_t lo = 0xffffffffu, hi = 0u;   // min of bits - 1 (+0 wraps), max of bits
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint32_t b0 = (uint32_t)pv[e], b1 = (uint32_t)(pv[e] >> 32);
+                        lo = min(lo, min(b0 - 1u, b1 - 1u));
+                        hi = max(hi, max(b0, b1));
+                    }
+                    if (l_ok && lo >= DIV_P_LO - 1u && hi < DIV_P_HI) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            a2[e] = fadd2_ftz(div2_rn(pv[e], nl2[e >> 2], y2[e >> 2]), z);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int r0 = 8 * ty + 2 * (e >> 2);
+                            float p0, p1;
+                            unpack2(pv[e], p0, p1);
+                            a2[e] = pack2(flush(__fdiv_rn(p0, lrw[r0])), flush(__fdiv_rn(p1, lrw[r0 + 1])));
+                        }
+                    }
+                }
                 float av[8][4], dv[8][4];   // rows 8ty + rr, keys 4tx + j
 #pragma unroll
                 for (int ip = 0; ip < 4; ++ip)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int e = ip * 4 + j, r0 = 8 * ty + 2 * ip;
-                        float p[2], aa[2];
-                        unpack2(pv[e], p[0], p[1]);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            aa[h] = flush(__fdiv_rn(p[h], lrw[r0 + h]));
+                        float aa[2];
+                        unpack2(a2[e], aa[0], aa[1]);
                         float d[2];
-                        unpack2(fadd2_ftz(fmul2_rn(pack2(aa[0], aa[1]),
+                        unpack2(fadd2_ftz(fmul2_rn(a2[e],
                                                    fadd2_ftz(fadd2_ftz(t0[e], t1[e]), pack2(-drw[r0], -drw[r0 + 1]))),
                                           z),
                                 d[0], d[1]);

@@ -280,6 +280,49 @@ def test_attn_bwd_underflowing_probabilities(orc, W):
     assert below[..., valid].mean() > 0.3
 
 
+@pytest.mark.parametrize("W", [0, 100])
+def test_attn_bwd_row_sums_around_the_quotient_range(orc, W):
+    # a = p (/) l is formed by correction when l is in [2^-30, 2^30) and by a
+    # division otherwise (csrc/k_attn.cuh); a thread holds eight consecutive
+    # rows, so l is changed per aligned group of eight rows: unchanged, scaled
+    # out of the range both ways, at both ends of it (kept: 2^-30 and the
+    # float below 2^30; divided: 2^30), and a group with a zero, a negative
+    # and a NaN l.  Both backward routes match the oracle
+    B, T, Hq, Hkv = 1, 200, 4, 2
+    q, k, vq, s_v = _case(606 + W, B, T, Hq, Hkv)
+    o, m, l, fwd_ws = gpu_attn_fwd(q, k, vq, s_v, W, keep_cache=True)
+    l = l.copy()
+    below_2_30 = np.nextafter(np.float32(2.0 ** 30), np.float32(0))
+    for t in range(T):
+        g = (t // 8) % 8
+        if g == 1:
+            l[0, t] *= np.float32(2.0 ** 40)
+        elif g == 2:
+            l[0, t] *= np.float32(2.0 ** -40)
+        elif g == 3:
+            l[0, t] = np.float32(2.0 ** -30)
+        elif g == 4:
+            l[0, t] = below_2_30
+        elif g == 5:
+            l[0, t] = np.float32(2.0 ** 30)
+        elif g == 6 and t % 8 == 0:
+            l[0, t] = 0.0
+        elif g == 6 and t % 8 == 1:
+            l[0, t] = -l[0, t]
+        elif g == 6 and t % 8 == 2:
+            l[0, t] = np.nan
+    dout = (np.random.default_rng(61).standard_normal(o.shape) * 1e-3).astype(np.float32)
+    rq, rk, rv = orc.attn_bwd(q, k, vq, s_v, o, dout, m, l, W)
+    for fws in (fwd_ws, None):
+        dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=fws)
+        G.assert_bits_equal(dq, rq, "dq")
+        for got, exp, what in ((dk, rk, "dk"), (dv, rv, "dv")):
+            nan = np.isnan(exp)
+            assert np.array_equal(np.isnan(got), nan), what
+            G.assert_bits_equal(np.where(nan, 0, got).astype(np.float32),
+                                np.where(nan, 0, exp).astype(np.float32), what)
+
+
 @pytest.mark.parametrize("W", [512, 0])
 def test_attn_bwd_full_size_sampled(orc, W):
     B, T, Hq, Hkv = 4, 4096, 16, 4
