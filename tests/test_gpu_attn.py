@@ -344,6 +344,33 @@ def test_attn_bwd_full_size_sampled(orc, W):
     G.assert_bits_equal(dv.reshape(-1, D)[krows], rv, "dv rows")
 
 
+@pytest.mark.parametrize("W", [512, 0])
+def test_attn_full_size_whole_tile_bands(orc, W):
+    # every element of whole 64-row query tiles (o, m, l, dQ) and whole
+    # 64-key tiles (dK, dV) at full size, on the bench's launch configuration
+    # (cached forward, tensor-core P.V, cached backward): the first tile of a
+    # sequence (truncated windows), the tile where the window first fills, and
+    # the last tile, each in another sequence and head
+    B, T, Hq, Hkv = 4, 4096, 16, 4
+    q, k, vq, s_v = _case(300 + W, B, T, Hq, Hkv)
+    o, m, l, fws = gpu_attn_fwd(q, k, vq, s_v, W, keep_cache=True)
+    dout = (np.random.default_rng(W + 3).standard_normal(o.shape) * 1e-3).astype(np.float32)
+    dq, dk, dv = gpu_attn_bwd(q, k, vq, s_v, o, dout, m, l, W, fwd_ws=fws)
+    i = np.arange(64)
+    qrows = np.concatenate([(0 * T + i) * Hq + 0, (1 * T + 448 + i) * Hq + 7,
+                            (3 * T + T - 64 + i) * Hq + 15])
+    krows = np.concatenate([(0 * T + i) * Hkv + 0, (2 * T + 2048 + i) * Hkv + 3,
+                            (3 * T + T - 64 + i) * Hkv + 1])
+    ro, rm, rl = orc.attn_fwd_rows(q, k, vq, s_v, W, qrows)
+    G.assert_bits_equal(o.reshape(-1, D)[qrows], ro, "o bands")
+    G.assert_bits_equal(m.reshape(-1)[qrows], rm, "m bands")
+    G.assert_bits_equal(l.reshape(-1)[qrows], rl, "l bands")
+    rq, rk, rv = orc.attn_bwd_rows(q, k, vq, s_v, o, dout, m, l, W, qrows, krows)
+    G.assert_bits_equal(dq.reshape(-1, D)[qrows], rq, "dq bands")
+    G.assert_bits_equal(dk.reshape(-1, D)[krows], rk, "dk bands")
+    G.assert_bits_equal(dv.reshape(-1, D)[krows], rv, "dv bands")
+
+
 def test_attn_bwd_repeatable():
     q, k, vq, s_v = _case(4, 2, 300, 8, 2)
     o, m, l = gpu_attn_fwd(q, k, vq, s_v, 100)
