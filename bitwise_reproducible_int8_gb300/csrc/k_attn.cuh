@@ -427,14 +427,59 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_rows(const AttnLogitArgs a)
                 }
             }
             const float* Kc = Kr + s * (HD * AT);
+            const int j0 = t * AT;
+            // every (query, key) pair of the tile valid: no per-pair test
+            const bool inner = qt.i0 + AT - 1 < T && j0 + AT - 1 <= qt.i0 && (W == 0 || j0 >= qt.i0 + AT - W);
+            // A mask-edge tile may leave a warp (rows r0w .. r0w + 15) with
+            // valid keys in at most 8 of its 16 four-key column blocks
+            // [ca, cb]: then each such block's two 64-term chunks are summed by
+            // two threads of its half-warp -- d 0..63 by the block's thread,
+            // d 64..127 by one whose own block has no valid key -- and the
+            // second sum is handed over; with no valid key at all the warp
+            // skips the tile.  Each logit is still (chunk 0 (+) chunk 1) (x) c
             u64 t0[16], t1[16];
-            logit_chunk84(t0, Qt + 8 * ty, Kc + 4 * tx);
-            logit_chunk84(t1, Qt + 64 * PT + 8 * ty, Kc + 64 * AT + 4 * tx);
+            bool need = true;   // this thread's own block is formed and used
+            int ca = 0, cb = AT / 4 - 1;
+            bool pair = false, skip = false;
+            if (!inner) {
+                const int r0w = qt.i0 + 16 * (lt >> 5), r1w = min(r0w + 15, T - 1);
+                const int ka = max((W > 0 ? max(0, r0w - W + 1) : 0) - j0, 0);
+                const int kb = min(r1w - j0, AT - 1);
+                skip = r0w >= T || kb < ka;
+                if (!skip) {
+                    ca = ka >> 2;
+                    cb = kb >> 2;
+                    pair = cb - ca + 1 <= 8;
+                }
+            }
+            if (skip) {
+                need = false;
+            } else if (pair) {
+                const int n = cb - ca + 1;
+                const bool prim = tx >= ca && tx <= cb;
+                const int k = tx < ca ? tx : tx - n;       // rank among the blocks outside [ca, cb]
+                const bool help = !prim && k < n;
+                const int own = help ? ca + k : tx;        // the block this thread's chunk belongs to
+                const int dofs = help ? 64 : 0;
+                logit_chunk84(t0, Qt + dofs * PT + 8 * ty, Kc + dofs * AT + 4 * own);
+                const int kp = tx - ca;                    // a block's rank: its helper has the same
+                const int src = (lane & 16) | (prim ? (kp < ca ? kp : kp + n) : tx);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    t1[e] = __shfl_sync(0xffffffffu, t0[e], src);
+                need = prim;
+            } else {
+                logit_chunk84(t0, Qt + 8 * ty, Kc + 4 * tx);
+                logit_chunk84(t1, Qt + 64 * PT + 8 * ty, Kc + 64 * AT + 4 * tx);
+            }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[gp][s]);
             ++used;
-            if constexpr (!BWD) {
+            if (!need) {
+                // nothing of this thread's block is valid: no logits, maxima
+                // or (backward) a and dS to form
+            } else if constexpr (!BWD) {
                 const u64 cc = pack2(a.c, a.c);
                 u64 sv[16];
 #pragma unroll
@@ -452,8 +497,6 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_rows(const AttnLogitArgs a)
                             dst[e] = make_ulonglong2(sv[8 * blk + 2 * e], sv[8 * blk + 2 * e + 1]);
                     }
                 }
-                const int j0 = t * AT;
-                const bool inner = qt.i0 + AT - 1 < T && j0 + AT - 1 <= qt.i0 && (W == 0 || j0 >= qt.i0 + AT - W);
 #pragma unroll
                 for (int ip = 0; ip < 4; ++ip)
 #pragma unroll
@@ -491,8 +534,6 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_rows(const AttnLogitArgs a)
                         pv[8 * blk + 2 * e + 1] = v.y;
                     }
                 }
-                const int j0 = t * AT;
-                const bool inner = qt.i0 + AT - 1 < T && j0 + AT - 1 <= qt.i0 && (W == 0 || j0 >= qt.i0 + AT - W);
                 // a = p (/) l_i, flushed, for the thread's 16 pairs: by
                 // correction when every p and l admits it, else divided
                 u64 a2[16];
