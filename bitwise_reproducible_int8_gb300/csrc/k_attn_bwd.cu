@@ -1048,6 +1048,7 @@ __global__ void __launch_bounds__(NT, 2) k_attn_bdq(const AttnDqArgs a)
                 if (mid_lo <= mid_hi) {
                     edge(lo_all, mid_lo - 1);
                     load(mid_lo);
+#pragma unroll 4
                     for (int j = mid_lo; j <= mid_hi; ++j)
                         key(std::false_type{}, j + 1 <= mid_hi ? j + 1 : j);
                     edge(mid_hi + 1, hi_all);
@@ -1387,6 +1388,7 @@ __global__ void __launch_bounds__(NT, 1) k_attn_bdkv(const AttnDkvArgs a)
                     if (mid_lo <= mid_hi) {
                         edge(lo_all, mid_lo - 1);
                         load(mid_lo);
+#pragma unroll 4
                         for (int i = mid_lo; i <= mid_hi; ++i)
                             row(std::false_type{}, i + 1 <= mid_hi ? i + 1 : i);
                         edge(mid_hi + 1, hi_all);
