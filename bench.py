@@ -841,15 +841,19 @@ def run_attn(args, aw):
         a0.record(stream)
         up.wait_stream(stream)
         last_down = None
+        h2d_ev = []   # each step's uploads, from their start to their end
         for step in range(args.steps):
             cur = sets[step % 2]
             with torch.cuda.stream(up):
                 if in_free[step % 2] is not None:
                     up.wait_event(in_free[step % 2])
+                u0 = torch.cuda.Event(enable_timing=True)
+                u0.record(up)
                 for d, h in zip(cur[:4], (hq, hk, hv, hdo)):
                     d.copy_(h, non_blocking=True)
-                ready = torch.cuda.Event()
+                ready = torch.cuda.Event(enable_timing=True)
                 ready.record(up)
+                h2d_ev.append((u0, ready))
             stream.wait_event(ready)
             if out_free[step % 2] is not None:
                 stream.wait_event(out_free[step % 2])
@@ -878,6 +882,11 @@ def run_attn(args, aw):
                "h2d_bytes_per_step": int(4 * (q.size + k.size + v.size + do.size)),
                "d2h_bytes_per_step": int(4 * (dq.numel() + dk.numel() + dv.numel())),
                "ms_per_step": e_ms / args.steps}
+        # the host link as these steps saw it: the uploads hide behind a step
+        # only while they take less than it
+        up_ms = sum(x.elapsed_time(y) for x, y in h2d_ev) / args.steps
+        e2e["h2d_ms_per_step"] = up_ms
+        e2e["h2d_gbs"] = e2e["h2d_bytes_per_step"] / (up_ms / 1e3) / 1e9 if up_ms > 0 else None
 
     if rank == 0:
         peaks = load_peaks()
