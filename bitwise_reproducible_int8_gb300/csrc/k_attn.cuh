@@ -462,7 +462,8 @@ __global__ void __launch_bounds__(LG_NT, 1) k_attn_rows(const AttnLogitArgs a)
                 const int own = help ? ca + k : tx;        // the block this thread's chunk belongs to
                 const int dofs = help ? 64 : 0;
                 logit_chunk84(t0, Qt + dofs * PT + 8 * ty, Kc + dofs * AT + 4 * own);
-                const int kp = tx - ca;                    // a block's rank: its helper has the same
+                // a valid block's helper: the column outside [ca, cb] of the same rank
+                const int kp = tx - ca;
                 const int src = (lane & 16) | (prim ? (kp < ca ? kp : kp + n) : tx);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
